@@ -1,0 +1,226 @@
+"""Seeded synthetic inputs shared by the CUDA engine's tests/bench and the CPU oracle.
+
+Holds no arithmetic of the decode step: it draws weights (std 0.02 normals
+rounded to the storage dtype, RMSNorm gains 1.0, row-scaled e4m3 experts),
+prompt ids, sampling uniforms and synthetic KV prefixes, and describes the
+workload shapes. Both sides then read the same bytes.
+
+The workloads are the five decoder configurations of the single-request decode
+study in "Real-time LLM inference on standard GPUs: 3,000 tokens/s per request"
+(Kog AI; summarised at hakusoku.com, section "GPU推論の速度制限要因：メモリ帯域幅",
+and aether-echoes.com, section "モデルは 2B・HumanEval 50%": a 2.3B FP16
+decoder, 25 layers, context 4096, batch 1), with trained weights replaced by
+seeded random ones of the same shapes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+from .configs import CONFIGS, get_config, shrink  # noqa: F401
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libsynth.so")
+_lock = threading.Lock()
+_lib = None
+
+# Seeds (fixed per workload): weights = 1000 + index, prompt = 2000 + index,
+# sampling stream = 3000, synthetic KV prefix = 4000 + index.
+SEED_WEIGHTS = 1000
+SEED_PROMPT = 2000
+SEED_SAMPLING = 3000
+SEED_KV = 4000
+
+WEIGHT_STD = 0.02
+
+
+def build_lib(force: bool = False) -> str:
+    """Compile gen.c into libsynth.so beside it (gcc, OpenMP)."""
+    src = os.path.join(_HERE, "gen.c")
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(src):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11",
+                           "-ffp-contract=off", "-o", tmp, src, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build_lib()
+            L = ctypes.CDLL(_LIB_PATH)
+            u64, f32, sz = ctypes.c_uint64, ctypes.c_float, ctypes.c_size_t
+            vp = ctypes.c_void_p
+            L.synth_normal_f32.argtypes = [u64, u64, f32, vp, sz]
+            L.synth_normal_f16.argtypes = [u64, u64, f32, vp, sz]
+            L.synth_normal_bf16.argtypes = [u64, u64, f32, vp, sz]
+            L.synth_normal_e4m3_rows.argtypes = [u64, u64, f32, sz, sz, vp, vp]
+            L.synth_f32_to_f16.argtypes = [vp, vp, sz]
+            L.synth_f32_to_bf16.argtypes = [vp, vp, sz]
+            L.synth_f32_to_e4m3.argtypes = [vp, vp, sz]
+            L.synth_tokens.argtypes = [u64, u64, ctypes.c_uint32, vp, sz]
+            L.synth_uniforms.argtypes = [u64, u64, vp, sz]
+            L.synth_key.argtypes = [u64, u64]
+            L.synth_key.restype = u64
+            _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+# ---------------------------------------------------------------- primitives
+
+def normal_f32(seed: int, tensor_id: int, shape, std: float = 1.0) -> np.ndarray:
+    out = np.empty(shape, dtype=np.float32)
+    lib().synth_normal_f32(seed, tensor_id, std, _ptr(out), out.size)
+    return out
+
+
+def normal_stored(seed: int, tensor_id: int, shape, dtype: str, std: float = WEIGHT_STD) -> np.ndarray:
+    """std-normal draws x std, rounded RNE to 'f16' or 'bf16'. Returned as raw uint16 bits."""
+    out = np.empty(shape, dtype=np.uint16)
+    if dtype == "f16":
+        lib().synth_normal_f16(seed, tensor_id, std, _ptr(out), out.size)
+    elif dtype == "bf16":
+        lib().synth_normal_bf16(seed, tensor_id, std, _ptr(out), out.size)
+    else:
+        raise ValueError(dtype)
+    return out
+
+
+def normal_e4m3_rows(seed: int, tensor_id: int, rows: int, cols: int, std: float = WEIGHT_STD):
+    q = np.empty((rows, cols), dtype=np.uint8)
+    s = np.empty((rows,), dtype=np.float32)
+    lib().synth_normal_e4m3_rows(seed, tensor_id, std, rows, cols, _ptr(q), _ptr(s))
+    return q, s
+
+
+def f32_to_stored(x: np.ndarray, dtype: str) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == "e4m3":
+        out = np.empty(x.shape, dtype=np.uint8)
+        lib().synth_f32_to_e4m3(_ptr(x), _ptr(out), x.size)
+        return out
+    out = np.empty(x.shape, dtype=np.uint16)
+    if dtype == "f16":
+        lib().synth_f32_to_f16(_ptr(x), _ptr(out), x.size)
+    elif dtype == "bf16":
+        lib().synth_f32_to_bf16(_ptr(x), _ptr(out), x.size)
+    else:
+        raise ValueError(dtype)
+    return out
+
+
+def ones_stored(n: int, dtype: str) -> np.ndarray:
+    """RMSNorm gains: exactly 1.0 in the storage dtype."""
+    return np.full((n,), 0x3C00 if dtype == "f16" else 0x3F80, dtype=np.uint16)
+
+
+def tokens(seed: int, stream_id: int, n: int, vocab: int) -> np.ndarray:
+    out = np.empty((n,), dtype=np.int32)
+    lib().synth_tokens(seed, stream_id, vocab, _ptr(out), n)
+    return out
+
+
+def uniforms(seed: int, first: int, n: int) -> np.ndarray:
+    out = np.empty((n,), dtype=np.float32)
+    lib().synth_uniforms(seed, first, _ptr(out), n)
+    return out
+
+
+# ---------------------------------------------------------------- tensor ids
+
+def _tid_layer(layer: int, kind: int) -> int:
+    return 1000 + layer * 64 + kind
+
+
+def _tid_expert(layer: int, expert: int, kind: int) -> int:
+    return 1_000_000 + (layer * 1024 + expert) * 4 + kind
+
+
+TID_EMB, TID_LM = 1, 2
+K_WQ, K_WK, K_WV, K_WO, K_WG, K_WU, K_WD, K_ROUTER = range(8)
+E_GATE, E_UP, E_DOWN = range(3)
+
+
+# ---------------------------------------------------------------- model weights
+
+def model_weights(cfg: dict, seed: int | None = None) -> dict:
+    """Host copies of every stored tensor of a model, as numpy arrays of raw bits.
+
+    Layout (row-major [out, in]):
+      tok_emb [V, d]; lm_head [V, d] (None when tied); final_norm [d]
+      layers[l]: attn_norm [d], wq [hq*hd, d], wk/wv [hkv*hd, d], wo [d, hq*hd], ffn_norm [d],
+        dense: w_gate/w_up [ff, d], w_down [d, ff]
+        MoE:   router [E, d]; e_gate/e_up [E, f, d] e4m3; e_down [E, d, f] e4m3;
+               e_gate_scale/e_up_scale [E, f] f32; e_down_scale [E, d] f32
+    """
+    c = cfg
+    if seed is None:
+        seed = SEED_WEIGHTS + c["index"]
+    wdt = c["weight_dtype"]
+    d, hq, hkv, hd = c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"]
+    V = c["vocab"]
+    W = {"tok_emb": normal_stored(seed, TID_EMB, (V, d), wdt)}
+    W["lm_head"] = None if c["tied_embeddings"] else normal_stored(seed, TID_LM, (V, d), wdt)
+    W["final_norm"] = ones_stored(d, wdt)
+    layers = []
+    for l in range(c["n_layers"]):
+        L = {
+            "attn_norm": ones_stored(d, wdt),
+            "wq": normal_stored(seed, _tid_layer(l, K_WQ), (hq * hd, d), wdt),
+            "wk": normal_stored(seed, _tid_layer(l, K_WK), (hkv * hd, d), wdt),
+            "wv": normal_stored(seed, _tid_layer(l, K_WV), (hkv * hd, d), wdt),
+            "wo": normal_stored(seed, _tid_layer(l, K_WO), (d, hq * hd), wdt),
+            "ffn_norm": ones_stored(d, wdt),
+        }
+        if c["n_experts"] == 0:
+            ff = c["d_ff"]
+            L["w_gate"] = normal_stored(seed, _tid_layer(l, K_WG), (ff, d), wdt)
+            L["w_up"] = normal_stored(seed, _tid_layer(l, K_WU), (ff, d), wdt)
+            L["w_down"] = normal_stored(seed, _tid_layer(l, K_WD), (d, ff), wdt)
+        else:
+            E, f = c["n_experts"], c["d_expert"]
+            L["router"] = normal_stored(seed, _tid_layer(l, K_ROUTER), (E, d), c["router_dtype"])
+            eg = np.empty((E, f, d), np.uint8); eu = np.empty((E, f, d), np.uint8); ed = np.empty((E, d, f), np.uint8)
+            sg = np.empty((E, f), np.float32); su = np.empty((E, f), np.float32); sd = np.empty((E, d), np.float32)
+            for e in range(E):
+                eg[e], sg[e] = normal_e4m3_rows(seed, _tid_expert(l, e, E_GATE), f, d)
+                eu[e], su[e] = normal_e4m3_rows(seed, _tid_expert(l, e, E_UP), f, d)
+                ed[e], sd[e] = normal_e4m3_rows(seed, _tid_expert(l, e, E_DOWN), d, f)
+            L.update(e_gate=eg, e_up=eu, e_down=ed, e_gate_scale=sg, e_up_scale=su, e_down_scale=sd)
+        layers.append(L)
+    W["layers"] = layers
+    return W
+
+
+def prompt(cfg: dict, n: int | None = None, seed: int | None = None) -> np.ndarray:
+    if seed is None:
+        seed = SEED_PROMPT + cfg["index"]
+    return tokens(seed, 7, cfg["prompt_len"] if n is None else n, cfg["vocab"])
+
+
+def sampling_uniforms(n: int, first: int = 0, seed: int = SEED_SAMPLING) -> np.ndarray:
+    return uniforms(seed, first, n)
+
+
+def kv_prefix(cfg: dict, length: int, seed: int | None = None):
+    """Synthetic KV-cache contents for positions [0, length): N(0, 1) in the KV storage dtype,
+    shaped [L, hkv, length, hd] (raw bits). N(0,1) matches the scale of K/V rows that a
+    std-0.02 projection produces from a unit-RMS input when d_model ~ 2500."""
+    if seed is None:
+        seed = SEED_KV + cfg["index"]
+    shp = (cfg["n_layers"], cfg["n_kv_heads"], length, cfg["head_dim"])
+    k = normal_stored(seed, 11, shp, cfg["kv_dtype"], std=1.0)
+    v = normal_stored(seed, 12, shp, cfg["kv_dtype"], std=1.0)
+    return k, v
