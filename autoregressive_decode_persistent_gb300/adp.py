@@ -1,0 +1,257 @@
+"""ctypes binding of the engine's C ABI (include/adp.h), with the same names.
+
+Argument marshalling only: every step of the decode path runs in the CUDA kernels of
+libadp.so. There is no fallback: if the library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libadp.so")
+
+ADP_F16, ADP_BF16, ADP_E4M3, ADP_F32 = 0, 1, 2, 3
+DTYPES = {"f16": ADP_F16, "bf16": ADP_BF16, "e4m3": ADP_E4M3, "f32": ADP_F32}
+
+ADP_OK = 0
+ADP_ERR_INVALID_ARG = -1
+ADP_ERR_UNSUPPORTED_CONFIG = -2
+ADP_ERR_CONTEXT_OVERFLOW = -3
+ADP_ERR_CUDA = -4
+ADP_ERR_NOT_CORESIDENT = -5
+ADP_ERR_BARRIER_TIMEOUT = -6
+ADP_ERR_PIPELINE_TIMEOUT = -7
+ADP_ERR_UNIMPLEMENTED = -8
+
+
+class AdpError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = status_string(code)
+        if code == ADP_ERR_CUDA:
+            msg += ": " + last_error()
+        super().__init__(f"{where}: {msg} ({code})")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("n_layers", "d_model", "n_heads", "n_kv_heads", "head_dim",
+                                               "d_ff", "vocab", "max_ctx")] + \
+               [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)] + \
+               [(n, ctypes.c_int32) for n in ("tied_embeddings", "weight_dtype", "kv_dtype", "n_experts",
+                                               "top_k", "d_expert", "router_dtype", "expert_dtype")]
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up",
+                                                "w_down", "router", "e_gate", "e_up", "e_down", "e_gate_scale",
+                                                "e_up_scale", "e_down_scale")]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("tok_emb", ctypes.c_void_p), ("lm_head", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
+                ("layers", ctypes.POINTER(LayerWeights))]
+
+
+class Sampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("u", ctypes.c_float)]
+
+
+_lib = None
+
+# (name, restype, argtypes)
+_SIGS = [
+    ("adp_create_model", ctypes.c_int, [ctypes.POINTER(Config), ctypes.POINTER(Weights), ctypes.c_void_p,
+                                        ctypes.POINTER(ctypes.c_void_p)]),
+    ("adp_destroy_model", None, [ctypes.c_void_p]),
+    ("adp_kv_create", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]),
+    ("adp_kv_destroy", None, [ctypes.c_void_p]),
+    ("adp_kv_reset", ctypes.c_int, [ctypes.c_void_p]),
+    ("adp_kv_len", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
+    ("adp_kv_load", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]),
+    ("adp_kv_read", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]),
+    ("adp_decode_step", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(Sampling),
+                                       ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
+    ("adp_prefill", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                   ctypes.POINTER(Sampling), ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
+    ("adp_generate_async", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]),
+    ("adp_sync", ctypes.c_int, [ctypes.c_void_p]),
+    ("adp_reset", ctypes.c_int, [ctypes.c_void_p]),
+    ("adp_status_string", ctypes.c_char_p, [ctypes.c_int]),
+    ("adp_last_error", ctypes.c_char_p, []),
+    ("adp_num_ctas", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
+    ("adp_image_bytes", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint64)]),
+    ("adp_launches_per_step", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
+    ("adp_debug_kernel_mode", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    ("adp_debug_force_experts", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    ("adp_debug_read_experts", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    ("adp_debug_trace_residual", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    ("adp_debug_set_wait_limit", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64]),
+    ("adp_debug_skip_barrier_arrival", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]),
+]
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libadp.so (build it first with autoregressive_decode_persistent_gb300.build.build())."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: the CUDA engine must be built (no CPU fallback exists)")
+    L = ctypes.CDLL(p)
+    for name, res, args in _SIGS:
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    if path is None:
+        _lib = L
+    return L
+
+
+def _check(rc: int, where: str):
+    if rc != ADP_OK:
+        raise AdpError(rc, where)
+
+
+def status_string(code: int) -> str:
+    return load_library().adp_status_string(code).decode()
+
+
+def last_error() -> str:
+    return load_library().adp_last_error().decode()
+
+
+def _ptr(x) -> int | None:
+    """Device or host address of a torch tensor / numpy array / int, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    return x.data_ptr()
+
+
+# ---------------------------------------------------------------- the C ABI, one to one
+
+def adp_create_model(cfg: Config, weights: Weights, stream: int = 0):
+    h = ctypes.c_void_p()
+    _check(load_library().adp_create_model(ctypes.byref(cfg), ctypes.byref(weights), stream or None,
+                                           ctypes.byref(h)), "adp_create_model")
+    return h
+
+
+def adp_destroy_model(model):
+    load_library().adp_destroy_model(model)
+
+
+def adp_kv_create(model):
+    h = ctypes.c_void_p()
+    _check(load_library().adp_kv_create(model, ctypes.byref(h)), "adp_kv_create")
+    return h
+
+
+def adp_kv_destroy(kv):
+    load_library().adp_kv_destroy(kv)
+
+
+def adp_kv_reset(kv):
+    _check(load_library().adp_kv_reset(kv), "adp_kv_reset")
+
+
+def adp_kv_len(kv) -> int:
+    n = ctypes.c_int32()
+    _check(load_library().adp_kv_len(kv, ctypes.byref(n)), "adp_kv_len")
+    return n.value
+
+
+def adp_kv_load(kv, host_k: np.ndarray, host_v: np.ndarray, length: int):
+    _check(load_library().adp_kv_load(kv, _ptr(np.ascontiguousarray(host_k)), _ptr(np.ascontiguousarray(host_v)),
+                                      length), "adp_kv_load")
+
+
+def adp_kv_read(kv, host_k: np.ndarray, host_v: np.ndarray, length: int):
+    assert host_k.flags["C_CONTIGUOUS"] and host_v.flags["C_CONTIGUOUS"]
+    _check(load_library().adp_kv_read(kv, _ptr(host_k), _ptr(host_v), length), "adp_kv_read")
+
+
+def _sampling(temperature: float, u: float):
+    return ctypes.byref(Sampling(float(temperature), float(u))) if temperature > 0 else None
+
+
+def adp_decode_step(model, kv, token: int, temperature: float = 0.0, u: float = 0.0, dev_logits=None) -> int:
+    nxt = ctypes.c_int32()
+    _check(load_library().adp_decode_step(model, kv, int(token), _sampling(temperature, u), ctypes.byref(nxt),
+                                          _ptr(dev_logits)), "adp_decode_step")
+    return nxt.value
+
+
+def adp_prefill(model, kv, tokens, temperature: float = 0.0, u: float = 0.0, dev_logits=None) -> int:
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    nxt = ctypes.c_int32()
+    _check(load_library().adp_prefill(model, kv, _ptr(t), len(t), _sampling(temperature, u), ctypes.byref(nxt),
+                                      _ptr(dev_logits)), "adp_prefill")
+    return nxt.value
+
+
+def adp_generate_async(model, kv, token: int, n: int, temperature: float, dev_u, dev_tokens_out):
+    _check(load_library().adp_generate_async(model, kv, int(token), int(n), float(temperature), _ptr(dev_u),
+                                             _ptr(dev_tokens_out)), "adp_generate_async")
+
+
+def adp_sync(model):
+    _check(load_library().adp_sync(model), "adp_sync")
+
+
+def adp_reset(model):
+    _check(load_library().adp_reset(model), "adp_reset")
+
+
+def adp_num_ctas(model) -> int:
+    n = ctypes.c_int32()
+    _check(load_library().adp_num_ctas(model, ctypes.byref(n)), "adp_num_ctas")
+    return n.value
+
+
+def adp_image_bytes(model) -> int:
+    n = ctypes.c_uint64()
+    _check(load_library().adp_image_bytes(model, ctypes.byref(n)), "adp_image_bytes")
+    return n.value
+
+
+def adp_launches_per_step(model) -> int:
+    n = ctypes.c_int32()
+    _check(load_library().adp_launches_per_step(model, ctypes.byref(n)), "adp_launches_per_step")
+    return n.value
+
+
+def adp_debug_kernel_mode(model, mode: int):
+    _check(load_library().adp_debug_kernel_mode(model, mode), "adp_debug_kernel_mode")
+
+
+def adp_debug_force_experts(model, host_idx):
+    arr = None if host_idx is None else np.ascontiguousarray(host_idx, dtype=np.int32)
+    _check(load_library().adp_debug_force_experts(model, _ptr(arr)), "adp_debug_force_experts")
+
+
+def adp_debug_read_experts(model, n_layers: int, top_k: int) -> np.ndarray:
+    out = np.zeros((n_layers, top_k), dtype=np.int32)
+    _check(load_library().adp_debug_read_experts(model, _ptr(out)), "adp_debug_read_experts")
+    return out
+
+
+def adp_debug_trace_residual(model, dev_buf):
+    _check(load_library().adp_debug_trace_residual(model, _ptr(dev_buf)), "adp_debug_trace_residual")
+
+
+def adp_debug_set_wait_limit(model, ns: int):
+    _check(load_library().adp_debug_set_wait_limit(model, int(ns)), "adp_debug_set_wait_limit")
+
+
+def adp_debug_skip_barrier_arrival(model, cta: int, barrier: int):
+    _check(load_library().adp_debug_skip_barrier_arrival(model, int(cta), int(barrier)),
+           "adp_debug_skip_barrier_arrival")

@@ -1,0 +1,695 @@
+// Host engine behind the C ABI of include/adp.h: configuration checks, the per-SM weight
+// stream plan, the tile-ordered weight image, scratch, KV caches and the decode-step launches.
+//
+// Pages followed: "標準GPUによるリアルタイムLLM推論：リクエストあたり3,000トークン/秒" (hakusoku.com),
+// sections "単一リクエストLLMデコード速度の重要性" (batch-1, one request), "標準推論スタックのボトルネック
+// とKogの工夫" (one GPU-resident launch per step instead of ~10 kernels per layer) and
+// "Kog Inference Engineの特徴とイノベーション" (the engine orders sync and prefetch itself).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/adp.h"
+#include "launch.h"
+#include "plan.h"
+
+using namespace adp;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int cuda_fail(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return ADP_ERR_CUDA;
+}
+
+#define CK(call)                                   \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+int elem_bytes(int dt) { return dt == ADP_E4M3 ? 1 : (dt == ADP_F32 ? 4 : 2); }
+
+}  // namespace
+
+struct adp_kv {
+  adp_model* m = nullptr;
+  uint16_t* k = nullptr;
+  uint16_t* v = nullptr;
+  int32_t len = 0;
+  size_t bytes = 0;  // of each of k and v
+};
+
+struct adp_model {
+  adp_config cfg{};
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  int G = 0;
+  int xbuf_floats = 0;
+  size_t smem = 0;
+  std::vector<PhaseDesc> phases;
+  PhaseDesc* d_phases = nullptr;
+  uint8_t* image = nullptr;
+  uint64_t image_bytes = 0;
+  Params p{};            // fields that do not change between steps
+  std::vector<void*> allocs;
+  StepState* h_state = nullptr;  // pinned
+  cudaEvent_t state_copied = nullptr;  // the last host->device copy of h_state has executed
+  int32_t* h_out = nullptr;      // pinned: out_token, err
+  int32_t* d_tokseq = nullptr;
+  int32_t tokseq_cap = 0;
+  int32_t* d_force = nullptr;
+  bool force_on = false;
+  float* d_logits_scratch = nullptr;
+  int mode = 0;
+  // multi-kernel graph cache
+  cudaGraphExec_t graph = nullptr;
+  const void* graph_key_kv = nullptr;
+  const void* graph_key_logits = nullptr;
+  bool graph_key_sample = false;
+  int sticky = ADP_OK;
+
+  template <class T>
+  int alloc(T** ptr, size_t count) {
+    void* q = nullptr;
+    cudaError_t e = cudaMalloc(&q, std::max<size_t>(count * sizeof(T), 16));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    allocs.push_back(q);
+    *ptr = static_cast<T*>(q);
+    return ADP_OK;
+  }
+};
+
+// ---------------------------------------------------------------- validation and planning
+
+static int validate(const adp_config* c, const adp_weights* w) {
+  if (!c || !w || !w->layers || !w->tok_emb || !w->final_norm) return ADP_ERR_INVALID_ARG;
+  if (c->n_layers < 1 || c->d_model < 8 || c->n_heads < 1 || c->n_kv_heads < 1 || c->vocab < 8 || c->max_ctx < 1)
+    return ADP_ERR_INVALID_ARG;
+  if (c->n_kv_heads > c->n_heads) return ADP_ERR_UNSUPPORTED_CONFIG;
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return ADP_ERR_UNSUPPORTED_CONFIG;
+  if (c->d_model % 8 || c->vocab % 8 || (c->n_heads * c->head_dim) % 8) return ADP_ERR_UNSUPPORTED_CONFIG;
+  if (c->weight_dtype != ADP_F16 && c->weight_dtype != ADP_BF16) return ADP_ERR_UNSUPPORTED_CONFIG;
+  if (c->kv_dtype != ADP_F16 && c->kv_dtype != ADP_BF16) return ADP_ERR_UNSUPPORTED_CONFIG;
+  if (!c->tied_embeddings && !w->lm_head) return ADP_ERR_INVALID_ARG;
+  if (c->n_experts == 0) {
+    if (c->d_ff < 8 || c->d_ff % 8) return ADP_ERR_UNSUPPORTED_CONFIG;
+  } else {
+    if (c->expert_dtype != ADP_E4M3) return ADP_ERR_UNSUPPORTED_CONFIG;
+    if (c->router_dtype != ADP_F16 && c->router_dtype != ADP_BF16) return ADP_ERR_UNSUPPORTED_CONFIG;
+    if (c->n_experts > 1024 || c->top_k < 1 || c->top_k > c->n_experts) return ADP_ERR_UNSUPPORTED_CONFIG;
+    if (c->top_k != 1 && c->top_k != 2 && c->top_k != 4 && c->top_k != 8) return ADP_ERR_UNSUPPORTED_CONFIG;
+    if (c->d_expert < 16 || c->d_expert % 16 || c->d_model % 16) return ADP_ERR_UNSUPPORTED_CONFIG;
+  }
+  for (int l = 0; l < c->n_layers; ++l) {
+    const adp_layer_weights& L = w->layers[l];
+    if (!L.attn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.ffn_norm) return ADP_ERR_INVALID_ARG;
+    if (c->n_experts == 0 && (!L.w_gate || !L.w_up || !L.w_down)) return ADP_ERR_INVALID_ARG;
+    if (c->n_experts && (!L.router || !L.e_gate || !L.e_up || !L.e_down || !L.e_gate_scale || !L.e_up_scale ||
+                         !L.e_down_scale))
+      return ADP_ERR_INVALID_ARG;
+  }
+  return ADP_OK;
+}
+
+// Append a phase; weighted phases get a region of the image and a K-chunk width such that one
+// round of units fits one ring slot.
+static void add_phase(adp_model* m, int kind, int layer, int n_units, int unit_rows, int slots, int K, int eb,
+                      int wdt, bool weights, int experts) {
+  PhaseDesc P{};
+  P.kind = kind;
+  P.layer = layer;
+  P.has_weights = weights ? 1 : 0;
+  if (weights) {
+    P.n_units = n_units;
+    P.unit_rows = unit_rows;
+    P.slots = slots;
+    P.K = K;
+    P.eb = eb;
+    P.wdt = wdt;
+    int upr = kConsumerWarps;
+    while (upr > 1 && (long long)upr * unit_rows * slots * eb * kChunkAlign > kSlotBytes) --upr;
+    P.upr = upr;
+    int KC = (kSlotBytes / (upr * unit_rows * slots * eb)) / kChunkAlign * kChunkAlign;
+    const int Kr = (K + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
+    KC = std::min(KC, Kr);
+    P.KC = KC;
+    P.n_chunks = (K + KC - 1) / KC;
+    const uint64_t region = (uint64_t)n_units * unit_rows * K * eb;
+    P.region = m->image_bytes;
+    P.expert_stride = (region + 255) / 256 * 256;
+    m->image_bytes += P.expert_stride * (uint64_t)experts;
+  }
+  m->phases.push_back(P);
+}
+
+static void plan(adp_model* m) {
+  const adp_config& c = m->cfg;
+  const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim;
+  const int eb = elem_bytes(c.weight_dtype);
+  for (int l = 0; l < c.n_layers; ++l) {
+    add_phase(m, PK_QKV, l, (hq + 2 * hkv) * hd / 2, 2, 1, d, eb, c.weight_dtype, true, 1);
+    add_phase(m, PK_ATTN, l, 0, 0, 0, 0, 0, 0, false, 0);
+    add_phase(m, PK_WO, l, d / 2, 2, 1, hq * hd, eb, c.weight_dtype, true, 1);
+    if (c.n_experts == 0) {
+      add_phase(m, PK_GU, l, c.d_ff, 2, 1, d, eb, c.weight_dtype, true, 1);
+      add_phase(m, PK_DOWN, l, d / 2, 2, 1, c.d_ff, eb, c.weight_dtype, true, 1);
+    } else {
+      add_phase(m, PK_ROUTER, l, c.n_experts, 1, 1, d, elem_bytes(c.router_dtype), c.router_dtype, true, 1);
+      add_phase(m, PK_EGU, l, c.d_expert, 2, c.top_k, d, 1, ADP_E4M3, true, c.n_experts);
+      add_phase(m, PK_EDOWN, l, d, 1, c.top_k, c.d_expert, 1, ADP_E4M3, true, c.n_experts);
+    }
+  }
+  add_phase(m, PK_LM, c.n_layers, c.vocab / 4, 4, 1, d, eb, c.weight_dtype, true, 1);
+  add_phase(m, PK_SAMPLE, c.n_layers, 0, 0, 0, 0, 0, 0, false, 0);
+}
+
+// ---------------------------------------------------------------- model creation
+
+static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
+  const adp_config& c = *cfg;
+  CK(cudaGetDevice(&m->device));
+  cudaDeviceProp prop;
+  CK(cudaGetDeviceProperties(&prop, m->device));
+  if (!prop.cooperativeLaunch) return ADP_ERR_NOT_CORESIDENT;
+  plan(m);
+  const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim, L = c.n_layers;
+  const int ffw = c.n_experts ? c.top_k * c.d_expert : c.d_ff;
+  m->xbuf_floats = std::max(std::max(d, hq * hd), ffw);
+  m->smem = (size_t)kSlots * kSlotBytes + (((size_t)m->xbuf_floats * 4 + 127) & ~(size_t)127) + ctl_bytes();
+  if (m->smem > (size_t)prop.sharedMemPerBlockOptin) return ADP_ERR_UNSUPPORTED_CONFIG;
+  int bps = 0;
+  CK(decode_prepare(m->smem, &bps));
+  if (bps < 1) return ADP_ERR_NOT_CORESIDENT;
+  m->G = prop.multiProcessorCount;  // one persistent CTA per SM
+
+  // weight image
+  int rc;
+  if ((rc = m->alloc(&m->image, m->image_bytes))) return rc;
+  if ((rc = m->alloc(&m->d_phases, m->phases.size()))) return rc;
+  CK(cudaMemcpyAsync(m->d_phases, m->phases.data(), m->phases.size() * sizeof(PhaseDesc), cudaMemcpyHostToDevice,
+                     m->stream));
+  const int eb = elem_bytes(c.weight_dtype);
+  for (const PhaseDesc& P : m->phases) {
+    if (!P.has_weights) continue;
+    RepackSrc S{};
+    S.hd = hd;
+    S.hq = hq;
+    S.hkv = hkv;
+    int experts = 1;
+    if (P.kind == PK_LM) {
+      S.a = (const uint8_t*)(c.tied_embeddings ? w->tok_emb : w->lm_head);
+    } else {
+      const adp_layer_weights& Lw = w->layers[P.layer];
+      switch (P.kind) {
+        case PK_QKV: S.a = (const uint8_t*)Lw.wq; S.b = (const uint8_t*)Lw.wk; S.c = (const uint8_t*)Lw.wv; break;
+        case PK_WO: S.a = (const uint8_t*)Lw.wo; break;
+        case PK_GU: S.a = (const uint8_t*)Lw.w_gate; S.b = (const uint8_t*)Lw.w_up; break;
+        case PK_DOWN: S.a = (const uint8_t*)Lw.w_down; break;
+        case PK_ROUTER: S.a = (const uint8_t*)Lw.router; break;
+        case PK_EGU:
+          S.a = (const uint8_t*)Lw.e_gate; S.b = (const uint8_t*)Lw.e_up;
+          S.expert_src_stride = (uint64_t)c.d_expert * d;
+          experts = c.n_experts;
+          break;
+        case PK_EDOWN:
+          S.a = (const uint8_t*)Lw.e_down;
+          S.expert_src_stride = (uint64_t)d * c.d_expert;
+          experts = c.n_experts;
+          break;
+        default: break;
+      }
+    }
+    CK(repack_launch(m->image, P, S, m->G, experts, m->stream));
+  }
+  (void)eb;
+
+  // per-layer pointer tables
+  std::vector<const void*> an(L), fn(L);
+  std::vector<const float*> sg(L), su(L), sd(L);
+  for (int l = 0; l < L; ++l) {
+    an[l] = w->layers[l].attn_norm;
+    fn[l] = w->layers[l].ffn_norm;
+    sg[l] = w->layers[l].e_gate_scale;
+    su[l] = w->layers[l].e_up_scale;
+    sd[l] = w->layers[l].e_down_scale;
+  }
+  const void** d_an; const void** d_fn; const float** d_sg; const float** d_su; const float** d_sd;
+  if ((rc = m->alloc(&d_an, L)) || (rc = m->alloc(&d_fn, L)) || (rc = m->alloc(&d_sg, L)) ||
+      (rc = m->alloc(&d_su, L)) || (rc = m->alloc(&d_sd, L)))
+    return rc;
+  CK(cudaMemcpyAsync(d_an, an.data(), L * sizeof(void*), cudaMemcpyHostToDevice, m->stream));
+  CK(cudaMemcpyAsync(d_fn, fn.data(), L * sizeof(void*), cudaMemcpyHostToDevice, m->stream));
+  CK(cudaMemcpyAsync(d_sg, sg.data(), L * sizeof(void*), cudaMemcpyHostToDevice, m->stream));
+  CK(cudaMemcpyAsync(d_su, su.data(), L * sizeof(void*), cudaMemcpyHostToDevice, m->stream));
+  CK(cudaMemcpyAsync(d_sd, sd.data(), L * sizeof(void*), cudaMemcpyHostToDevice, m->stream));
+
+  // RoPE tables [max_ctx][hd/2]: inv_freq_i = theta^(-2i/hd), angle = p * inv_freq_i (double),
+  // cos and sin rounded to fp32 (the reading the step's arithmetic contract fixes).
+  const int half = hd / 2;
+  std::vector<float> cs((size_t)c.max_ctx * half), sn((size_t)c.max_ctx * half);
+  for (int i = 0; i < half; ++i) {
+    const double ex = (double)(2 * i) / (double)hd;
+    const double inv = std::pow((double)c.rope_theta, -ex);
+    for (int p = 0; p < c.max_ctx; ++p) {
+      const double ang = (double)p * inv;
+      cs[(size_t)p * half + i] = (float)std::cos(ang);
+      sn[(size_t)p * half + i] = (float)std::sin(ang);
+    }
+  }
+  float *d_cos, *d_sin;
+  if ((rc = m->alloc(&d_cos, cs.size())) || (rc = m->alloc(&d_sin, sn.size()))) return rc;
+  CK(cudaMemcpyAsync(d_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice, m->stream));
+  CK(cudaMemcpyAsync(d_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice, m->stream));
+
+  // scratch
+  Params& p = m->p;
+  const int nbmax = (c.max_ctx + kAttnBlock - 1) / kAttnBlock;
+  const int nblk = (c.vocab + kVocabBlock - 1) / kVocabBlock;
+  const int topk = std::max(c.top_k, 1);
+  if ((rc = m->alloc(&p.x, d)) || (rc = m->alloc(&p.q, hq * hd)) || (rc = m->alloc(&p.attn, hq * hd)) ||
+      (rc = m->alloc(&p.h, ffw)) || (rc = m->alloc(&p.rlog, std::max(c.n_experts, 1))) ||
+      (rc = m->alloc(&p.part_m, (size_t)hq * nbmax)) || (rc = m->alloc(&p.part_l, (size_t)hq * nbmax)) ||
+      (rc = m->alloc(&p.part_o, (size_t)hq * nbmax * hd)) || (rc = m->alloc(&p.head_ctr, hq)) ||
+      (rc = m->alloc(&p.sblock, nblk)) || (rc = m->alloc(&p.sample_ctr, 1)) || (rc = m->alloc(&p.argkey, 1)) ||
+      (rc = m->alloc(&p.lm_ctr, 1)) || (rc = m->alloc(&p.bar_ctr, 1)) || (rc = m->alloc(&p.err, 1)) ||
+      (rc = m->alloc(&p.sel_out, (size_t)L * topk)) || (rc = m->alloc(&p.state, 1)) ||
+      (rc = m->alloc(&m->d_force, (size_t)L * topk)) || (rc = m->alloc(&m->d_logits_scratch, c.vocab)))
+    return rc;
+  CK(cudaMemsetAsync(p.head_ctr, 0, hq * 4, m->stream));
+  CK(cudaMemsetAsync(p.sample_ctr, 0, 4, m->stream));
+  CK(cudaMemsetAsync(p.argkey, 0, 8, m->stream));
+  CK(cudaMemsetAsync(p.lm_ctr, 0, 4, m->stream));
+  CK(cudaMemsetAsync(p.bar_ctr, 0, 8, m->stream));
+  CK(cudaMemsetAsync(p.err, 0, 4, m->stream));
+  CK(cudaMemsetAsync(p.sel_out, 0, (size_t)L * topk * 4, m->stream));
+  CK(cudaMemsetAsync(p.state, 0, sizeof(StepState), m->stream));
+  CK(cudaMallocHost(&m->h_state, sizeof(StepState)));
+  CK(cudaEventCreateWithFlags(&m->state_copied, cudaEventDisableTiming));
+  CK(cudaEventRecord(m->state_copied, m->stream));
+  CK(cudaMallocHost(&m->h_out, 2 * sizeof(int32_t)));
+
+  p.image = m->image;
+  p.tok_emb = w->tok_emb;
+  p.attn_norm = d_an;
+  p.ffn_norm = d_fn;
+  p.final_norm = w->final_norm;
+  p.e_gate_scale = d_sg;
+  p.e_up_scale = d_su;
+  p.e_down_scale = d_sd;
+  p.phases = m->d_phases;
+  p.n_phases = (int)m->phases.size();
+  p.L = L; p.d = d; p.hq = hq; p.hkv = hkv; p.hd = hd; p.ff = c.d_ff; p.V = c.vocab; p.max_ctx = c.max_ctx;
+  p.E = c.n_experts; p.topk = c.n_experts ? c.top_k : 0; p.fexp = c.d_expert;
+  p.wdt = c.weight_dtype; p.kvdt = c.kv_dtype; p.rdt = c.router_dtype;
+  p.eps = c.rms_eps;
+  p.attn_scale = (float)(1.0 / std::sqrt((double)hd));
+  p.nbmax = nbmax;
+  p.rope_cos = d_cos;
+  p.rope_sin = d_sin;
+  p.wait_ns = 200000000ull;
+  p.skip_cta = -1;
+  p.skip_barrier = -1;
+  CK(cudaStreamSynchronize(m->stream));
+  CK(cudaGetLastError());
+  return ADP_OK;
+}
+
+extern "C" int adp_create_model(const adp_config* cfg, const adp_weights* w, void* stream, adp_model** out) {
+  if (!out) return ADP_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = validate(cfg, w);
+  if (rc) return rc;
+  adp_model* m = new adp_model();
+  m->cfg = *cfg;
+  m->stream = (cudaStream_t)stream;
+  rc = create(m, cfg, w);
+  if (rc) {
+    adp_destroy_model(m);
+    return rc;
+  }
+  *out = m;
+  return ADP_OK;
+}
+
+extern "C" void adp_destroy_model(adp_model* m) {
+  if (!m) return;
+  if (m->stream) cudaStreamSynchronize(m->stream);
+  else cudaDeviceSynchronize();
+  if (m->graph) cudaGraphExecDestroy(m->graph);
+  if (m->state_copied) cudaEventDestroy(m->state_copied);
+  for (void* q : m->allocs) cudaFree(q);
+  if (m->h_state) cudaFreeHost(m->h_state);
+  if (m->h_out) cudaFreeHost(m->h_out);
+  delete m;
+}
+
+// ---------------------------------------------------------------- KV caches
+
+extern "C" int adp_kv_create(adp_model* m, adp_kv** out) {
+  if (!m || !out) return ADP_ERR_INVALID_ARG;
+  *out = nullptr;
+  const adp_config& c = m->cfg;
+  adp_kv* kv = new adp_kv();
+  kv->m = m;
+  kv->bytes = (size_t)c.n_layers * c.n_kv_heads * c.max_ctx * c.head_dim * 2;
+  cudaError_t e = cudaMalloc(&kv->k, kv->bytes);
+  if (e == cudaSuccess) e = cudaMalloc(&kv->v, kv->bytes);
+  if (e == cudaSuccess) e = cudaMemsetAsync(kv->k, 0, kv->bytes, m->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(kv->v, 0, kv->bytes, m->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+  if (e != cudaSuccess) {
+    adp_kv_destroy(kv);
+    return cuda_fail(e, "adp_kv_create");
+  }
+  *out = kv;
+  return ADP_OK;
+}
+
+extern "C" void adp_kv_destroy(adp_kv* kv) {
+  if (!kv) return;
+  if (kv->m && kv->m->stream) cudaStreamSynchronize(kv->m->stream);
+  if (kv->k) cudaFree(kv->k);
+  if (kv->v) cudaFree(kv->v);
+  delete kv;
+}
+
+extern "C" int adp_kv_reset(adp_kv* kv) {
+  if (!kv) return ADP_ERR_INVALID_ARG;
+  kv->len = 0;
+  return ADP_OK;
+}
+
+extern "C" int adp_kv_len(const adp_kv* kv, int32_t* len) {
+  if (!kv || !len) return ADP_ERR_INVALID_ARG;
+  *len = kv->len;
+  return ADP_OK;
+}
+
+static int kv_copy(const adp_kv* kv, void* host_k, void* host_v, int32_t len, bool load) {
+  const adp_config& c = kv->m->cfg;
+  const size_t row = (size_t)c.head_dim * 2;
+  for (int l = 0; l < c.n_layers; ++l)
+    for (int g = 0; g < c.n_kv_heads; ++g) {
+      const size_t dev_off = (((size_t)l * c.n_kv_heads + g) * c.max_ctx) * row;
+      const size_t host_off = (((size_t)l * c.n_kv_heads + g) * (size_t)len) * row;
+      if (load) {
+        CK(cudaMemcpyAsync((uint8_t*)kv->k + dev_off, (const uint8_t*)host_k + host_off, len * row,
+                           cudaMemcpyHostToDevice, kv->m->stream));
+        CK(cudaMemcpyAsync((uint8_t*)kv->v + dev_off, (const uint8_t*)host_v + host_off, len * row,
+                           cudaMemcpyHostToDevice, kv->m->stream));
+      } else {
+        CK(cudaMemcpyAsync((uint8_t*)host_k + host_off, (const uint8_t*)kv->k + dev_off, len * row,
+                           cudaMemcpyDeviceToHost, kv->m->stream));
+        CK(cudaMemcpyAsync((uint8_t*)host_v + host_off, (const uint8_t*)kv->v + dev_off, len * row,
+                           cudaMemcpyDeviceToHost, kv->m->stream));
+      }
+    }
+  CK(cudaStreamSynchronize(kv->m->stream));
+  return ADP_OK;
+}
+
+extern "C" int adp_kv_load(adp_kv* kv, const void* host_k, const void* host_v, int32_t len) {
+  if (!kv || len < 0 || (len > 0 && (!host_k || !host_v))) return ADP_ERR_INVALID_ARG;
+  if (len > kv->m->cfg.max_ctx) return ADP_ERR_CONTEXT_OVERFLOW;
+  int rc = kv_copy(kv, const_cast<void*>(host_k), const_cast<void*>(host_v), len, true);
+  if (rc == ADP_OK) kv->len = len;
+  return rc;
+}
+
+extern "C" int adp_kv_read(const adp_kv* kv, void* host_k, void* host_v, int32_t len) {
+  if (!kv || len < 0 || (len > 0 && (!host_k || !host_v))) return ADP_ERR_INVALID_ARG;
+  if (len > kv->m->cfg.max_ctx) return ADP_ERR_CONTEXT_OVERFLOW;
+  return kv_copy(kv, host_k, host_v, len, false);
+}
+
+// ---------------------------------------------------------------- decode
+
+// Copy the step state to the device; the pinned staging buffer is reused only after the
+// previous copy out of it has executed.
+static int put_state(adp_model* m, int32_t pos, int32_t token, float T, float u) {
+  CK(cudaEventSynchronize(m->state_copied));
+  m->h_state->pos = pos;
+  m->h_state->token = token;
+  m->h_state->temperature = T;
+  m->h_state->u = u;
+  m->h_state->seq_index = 0;
+  m->h_state->out_token = -1;
+  CK(cudaMemcpyAsync(m->p.state, m->h_state, sizeof(StepState), cudaMemcpyHostToDevice, m->stream));
+  CK(cudaEventRecord(m->state_copied, m->stream));
+  return ADP_OK;
+}
+
+static int map_device_error(int32_t e) {
+  if (e == DE_BARRIER_TIMEOUT) return ADP_ERR_BARRIER_TIMEOUT;
+  if (e == DE_PIPELINE_TIMEOUT) return ADP_ERR_PIPELINE_TIMEOUT;
+  return e ? ADP_ERR_CUDA : ADP_OK;
+}
+
+static Params step_params(adp_model* m, adp_kv* kv, float* logits, const int32_t* tok_seq, const float* u_seq,
+                          int32_t* out_seq) {
+  Params p = m->p;
+  p.kc = kv->k;
+  p.vc = kv->v;
+  p.logits = logits ? logits : m->d_logits_scratch;
+  p.tok_seq = tok_seq;
+  p.u_seq = u_seq;
+  p.out_seq = out_seq;
+  p.force_sel = m->force_on ? m->d_force : nullptr;
+  return p;
+}
+
+// Enqueue the launches of one decode step in the model's kernel mode.
+static int enqueue_step(adp_model* m, const Params& p, bool sampling) {
+  const int nph = (int)m->phases.size();
+  const int last = sampling ? nph : nph - 1;  // the sampling phase runs only at temperature > 0
+  if (m->mode == 0) {
+    CK(decode_launch(p, 0, last, true, m->G, m->smem, m->xbuf_floats, m->stream));
+    return ADP_OK;
+  }
+  if (m->mode == 2) {
+    const bool hit = m->graph && m->graph_key_kv == (const void*)p.kc && m->graph_key_logits == (const void*)p.logits &&
+                     m->graph_key_sample == sampling && !p.tok_seq && !p.u_seq && !p.out_seq;
+    if (!hit && !p.tok_seq && !p.u_seq && !p.out_seq) {
+      if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
+      cudaStream_t cap;
+      CK(cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking));
+      cudaGraph_t g;
+      CK(cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal));
+      for (int ph = 0; ph < last; ++ph) {
+        cudaError_t e = decode_launch(p, ph, ph + 1, false, m->G, m->smem, m->xbuf_floats, cap);
+        if (e != cudaSuccess) { cudaStreamEndCapture(cap, &g); cudaStreamDestroy(cap); return cuda_fail(e, "capture"); }
+      }
+      CK(cudaStreamEndCapture(cap, &g));
+      CK(cudaGraphInstantiate(&m->graph, g, 0));
+      cudaGraphDestroy(g);
+      cudaStreamDestroy(cap);
+      m->graph_key_kv = p.kc;
+      m->graph_key_logits = p.logits;
+      m->graph_key_sample = sampling;
+    }
+    if (m->graph && !p.tok_seq && !p.u_seq && !p.out_seq) {
+      CK(cudaGraphLaunch(m->graph, m->stream));
+      return ADP_OK;
+    }
+  }
+  for (int ph = 0; ph < last; ++ph) CK(decode_launch(p, ph, ph + 1, false, m->G, m->smem, m->xbuf_floats, m->stream));
+  return ADP_OK;
+}
+
+static int finish(adp_model* m) {
+  CK(cudaMemcpyAsync(&m->h_out[0], &m->p.state->out_token, 4, cudaMemcpyDeviceToHost, m->stream));
+  CK(cudaMemcpyAsync(&m->h_out[1], m->p.err, 4, cudaMemcpyDeviceToHost, m->stream));
+  CK(cudaStreamSynchronize(m->stream));
+  const int rc = map_device_error(m->h_out[1]);
+  if (rc) m->sticky = rc;
+  return rc;
+}
+
+extern "C" int adp_decode_step(adp_model* m, adp_kv* kv, int32_t token, const adp_sampling* sampling,
+                               int32_t* next_token, float* dev_logits) {
+  if (!m || !kv || !next_token || kv->m != m) return ADP_ERR_INVALID_ARG;
+  if (m->sticky) return m->sticky;
+  if (token < 0 || token >= m->cfg.vocab) return ADP_ERR_INVALID_ARG;
+  if (kv->len >= m->cfg.max_ctx) return ADP_ERR_CONTEXT_OVERFLOW;
+  const float T = sampling ? sampling->temperature : 0.0f;
+  int rs = put_state(m, kv->len, token, T, sampling ? sampling->u : 0.0f);
+  if (rs) return rs;
+  Params p = step_params(m, kv, dev_logits, nullptr, nullptr, nullptr);
+  int rc = enqueue_step(m, p, T > 0.0f);
+  m->p.skip_cta = m->p.skip_barrier = -1;
+  if (rc) return rc;
+  rc = finish(m);
+  if (rc) return rc;
+  *next_token = m->h_out[0];
+  kv->len += 1;
+  return ADP_OK;
+}
+
+extern "C" int adp_prefill(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t n,
+                           const adp_sampling* sampling, int32_t* next_token, float* dev_logits) {
+  if (!m || !kv || !next_token || kv->m != m || n < 1 || !host_tokens) return ADP_ERR_INVALID_ARG;
+  if (m->sticky) return m->sticky;
+  if (kv->len + n > m->cfg.max_ctx) return ADP_ERR_CONTEXT_OVERFLOW;
+  for (int i = 0; i < n; ++i)
+    if (host_tokens[i] < 0 || host_tokens[i] >= m->cfg.vocab) return ADP_ERR_INVALID_ARG;
+  if (n > m->tokseq_cap) {
+    int32_t* q = nullptr;
+    int rc = m->alloc(&q, (size_t)n);
+    if (rc) return rc;
+    m->d_tokseq = q;
+    m->tokseq_cap = n;
+  }
+  CK(cudaMemcpyAsync(m->d_tokseq, host_tokens, (size_t)n * 4, cudaMemcpyHostToDevice, m->stream));
+  const float T = sampling ? sampling->temperature : 0.0f;
+  int rs = put_state(m, kv->len, 0, T, sampling ? sampling->u : 0.0f);
+  if (rs) return rs;
+  for (int i = 0; i < n; ++i) {
+    Params p = step_params(m, kv, i == n - 1 ? dev_logits : nullptr, m->d_tokseq, nullptr, nullptr);
+    int rc = enqueue_step(m, p, T > 0.0f);
+    if (rc) return rc;
+  }
+  m->p.skip_cta = m->p.skip_barrier = -1;
+  int rc = finish(m);
+  if (rc) return rc;
+  *next_token = m->h_out[0];
+  kv->len += n;
+  return ADP_OK;
+}
+
+extern "C" int adp_generate_async(adp_model* m, adp_kv* kv, int32_t token, int32_t n, float temperature,
+                                  const float* dev_u, int32_t* dev_tokens_out) {
+  if (!m || !kv || kv->m != m || n < 0 || !dev_tokens_out) return ADP_ERR_INVALID_ARG;
+  if (m->sticky) return m->sticky;
+  if (token < 0 || token >= m->cfg.vocab) return ADP_ERR_INVALID_ARG;
+  if (temperature > 0.0f && !dev_u) return ADP_ERR_INVALID_ARG;
+  if (kv->len + n > m->cfg.max_ctx) return ADP_ERR_CONTEXT_OVERFLOW;
+  if (n == 0) return ADP_OK;
+  int rs = put_state(m, kv->len, token, temperature, 0.0f);
+  if (rs) return rs;
+  Params p = step_params(m, kv, nullptr, nullptr, temperature > 0.0f ? dev_u : nullptr, dev_tokens_out);
+  for (int i = 0; i < n; ++i) {
+    int rc = enqueue_step(m, p, temperature > 0.0f);
+    if (rc) return rc;
+  }
+  kv->len += n;
+  return ADP_OK;
+}
+
+extern "C" int adp_sync(adp_model* m) {
+  if (!m) return ADP_ERR_INVALID_ARG;
+  if (m->sticky) return m->sticky;
+  return finish(m);
+}
+
+extern "C" int adp_reset(adp_model* m) {
+  if (!m) return ADP_ERR_INVALID_ARG;
+  cudaStreamSynchronize(m->stream);
+  const Params& p = m->p;
+  CK(cudaMemsetAsync(p.head_ctr, 0, (size_t)m->cfg.n_heads * 4, m->stream));
+  CK(cudaMemsetAsync(p.sample_ctr, 0, 4, m->stream));
+  CK(cudaMemsetAsync(p.argkey, 0, 8, m->stream));
+  CK(cudaMemsetAsync(p.lm_ctr, 0, 4, m->stream));
+  CK(cudaMemsetAsync(p.bar_ctr, 0, 8, m->stream));
+  CK(cudaMemsetAsync(p.err, 0, 4, m->stream));
+  CK(cudaStreamSynchronize(m->stream));
+  m->sticky = ADP_OK;
+  m->p.skip_cta = m->p.skip_barrier = -1;
+  return ADP_OK;
+}
+
+extern "C" const char* adp_status_string(int status) {
+  switch (status) {
+    case ADP_OK: return "ok";
+    case ADP_ERR_INVALID_ARG: return "invalid argument";
+    case ADP_ERR_UNSUPPORTED_CONFIG: return "unsupported configuration";
+    case ADP_ERR_CONTEXT_OVERFLOW: return "position beyond max_ctx";
+    case ADP_ERR_CUDA: return "CUDA runtime error";
+    case ADP_ERR_NOT_CORESIDENT: return "persistent grid cannot be co-resident";
+    case ADP_ERR_BARRIER_TIMEOUT: return "grid barrier wait ran out (sticky until adp_reset)";
+    case ADP_ERR_PIPELINE_TIMEOUT: return "weight pipeline wait ran out (sticky until adp_reset)";
+    case ADP_ERR_UNIMPLEMENTED: return "unimplemented";
+    default: return "unknown status";
+  }
+}
+
+extern "C" const char* adp_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" int adp_num_ctas(const adp_model* m, int32_t* ctas) {
+  if (!m || !ctas) return ADP_ERR_INVALID_ARG;
+  *ctas = m->G;
+  return ADP_OK;
+}
+
+extern "C" int adp_image_bytes(const adp_model* m, uint64_t* bytes) {
+  if (!m || !bytes) return ADP_ERR_INVALID_ARG;
+  *bytes = m->image_bytes;
+  return ADP_OK;
+}
+
+extern "C" int adp_launches_per_step(const adp_model* m, int32_t* n) {
+  if (!m || !n) return ADP_ERR_INVALID_ARG;
+  *n = m->mode == 0 ? 1 : (int32_t)m->phases.size() - 1;
+  return ADP_OK;
+}
+
+// ---------------------------------------------------------------- debug and ablation hooks
+
+extern "C" int adp_debug_kernel_mode(adp_model* m, int mode) {
+  if (!m || mode < 0 || mode > 2) return ADP_ERR_INVALID_ARG;
+  m->mode = mode;
+  return ADP_OK;
+}
+
+extern "C" int adp_debug_force_experts(adp_model* m, const int32_t* host_idx) {
+  if (!m) return ADP_ERR_INVALID_ARG;
+  if (!m->cfg.n_experts) return host_idx ? ADP_ERR_UNSUPPORTED_CONFIG : ADP_OK;
+  if (!host_idx) {
+    m->force_on = false;
+    return ADP_OK;
+  }
+  const size_t n = (size_t)m->cfg.n_layers * m->cfg.top_k;
+  for (size_t i = 0; i < n; ++i)
+    if (host_idx[i] < 0 || host_idx[i] >= m->cfg.n_experts) return ADP_ERR_INVALID_ARG;
+  CK(cudaMemcpyAsync(m->d_force, host_idx, n * 4, cudaMemcpyHostToDevice, m->stream));
+  CK(cudaStreamSynchronize(m->stream));
+  m->force_on = true;
+  return ADP_OK;
+}
+
+extern "C" int adp_debug_read_experts(const adp_model* m, int32_t* host_idx) {
+  if (!m || !host_idx) return ADP_ERR_INVALID_ARG;
+  if (!m->cfg.n_experts) return ADP_ERR_UNSUPPORTED_CONFIG;
+  CK(cudaMemcpyAsync(host_idx, m->p.sel_out, (size_t)m->cfg.n_layers * m->cfg.top_k * 4, cudaMemcpyDeviceToHost,
+                     m->stream));
+  CK(cudaStreamSynchronize(m->stream));
+  return ADP_OK;
+}
+
+extern "C" int adp_debug_trace_residual(adp_model* m, float* dev_buf) {
+  if (!m) return ADP_ERR_INVALID_ARG;
+  m->p.trace = dev_buf;
+  if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
+  return ADP_OK;
+}
+
+extern "C" int adp_debug_set_wait_limit(adp_model* m, uint64_t ns) {
+  if (!m || ns == 0) return ADP_ERR_INVALID_ARG;
+  m->p.wait_ns = ns;
+  if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
+  return ADP_OK;
+}
+
+extern "C" int adp_debug_skip_barrier_arrival(adp_model* m, int32_t cta, int32_t barrier) {
+  if (!m) return ADP_ERR_INVALID_ARG;
+  m->p.skip_cta = cta;
+  m->p.skip_barrier = barrier;
+  return ADP_OK;
+}

@@ -1,0 +1,26 @@
+// Host-side entry points of the CUDA translation units (engine <-> kernels).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "plan.h"
+
+namespace adp {
+
+// Source matrices of one phase for the repack into the tile-ordered image.
+struct RepackSrc {
+  const uint8_t* a;            // wq / wo / w_gate / w_down / head / router / e_gate / e_down
+  const uint8_t* b;            // wk / w_up / e_up
+  const uint8_t* c;            // wv
+  uint64_t expert_src_stride;  // bytes of one expert's matrix in the caller's [E, rows, K] tensor
+  int32_t hd, hq, hkv;
+};
+
+cudaError_t decode_prepare(size_t smem_bytes, int* blocks_per_sm);
+cudaError_t decode_launch(const Params& p, int ph0, int ph1, bool persistent, int grid, size_t smem_bytes,
+                          int xbuf_floats, cudaStream_t stream);
+cudaError_t repack_launch(uint8_t* image, const PhaseDesc& P, const RepackSrc& S, int grid, int experts,
+                          cudaStream_t stream);
+size_t ctl_bytes();
+
+}  // namespace adp

@@ -1,0 +1,120 @@
+// Plan and parameter structures shared by the host engine and the decode kernel.
+//
+// The decode step is a fixed sequence of phases per layer (QKV, attention, Wo, FFN
+// gate|up, FFN down; for MoE: router, expert gate|up, expert down), then the LM head
+// and, when sampling, a sampling phase.  Weighted phases split their "units" (one row,
+// a RoPE pair, a gate/up pair, a row group) evenly over the persistent CTAs (one per
+// SM); each CTA streams its share as tiles of whole units x one K-chunk, laid out
+// contiguously in a model-owned weight image in exactly the order the CTA consumes
+// them, so one TMA bulk copy moves a tile.
+#pragma once
+#include <stdint.h>
+
+namespace adp {
+
+constexpr int kConsumerWarps = 16;                  // compute warps per CTA
+constexpr int kThreads = (kConsumerWarps + 1) * 32; // + one producer (TMA) warp
+constexpr int kSlotBytes = 32768;                   // one ring slot
+constexpr int kSlots = 4;                           // ring depth (128 KB in flight per SM)
+constexpr int kAttnBlock = 32;                      // positions per attention block (contract)
+constexpr int kVocabBlock = 256;                    // vocabulary entries per sampling block (contract)
+constexpr int kMaxTopK = 8;
+constexpr int kChunkAlign = 256;                    // K-chunks start at multiples of 32 lanes x 8 elements
+
+enum PhaseKind : int32_t {
+  PK_QKV = 0,    // rmsnorm prologue; RoPE pairs of q/k, v; epilogue writes q and the KV rows
+  PK_ATTN = 1,   // split-sequence attention + per-head merge (no weights)
+  PK_WO = 2,     // x += Wo attn
+  PK_GU = 3,     // h = silu(Wg xn) * (Wu xn)
+  PK_DOWN = 4,   // x += Wd h
+  PK_ROUTER = 5, // r = Wr xn
+  PK_EGU = 6,    // per chosen expert: h_s = silu(sg*(Qg xn)) * (su*(Qu xn))
+  PK_EDOWN = 7,  // x += sum_s gate_s * sd*(Qd_s h_s)
+  PK_LM = 8,     // logits = W_lm rmsnorm(x), running argmax
+  PK_SAMPLE = 9  // inverse-CDF sampling over the logits (temperature > 0 only)
+};
+
+enum DType : int32_t { DT_F16 = 0, DT_BF16 = 1, DT_E4M3 = 2, DT_F32 = 3 };
+
+struct PhaseDesc {
+  int32_t kind, layer;
+  int32_t n_units;        // units of the whole phase
+  int32_t unit_rows;      // weight rows per unit (per expert slot)
+  int32_t slots;          // expert slots per tile: 1, or top_k for expert phases
+  int32_t K;              // reduction length
+  int32_t KC;             // K-chunk width, multiple of kChunkAlign
+  int32_t n_chunks;       // ceil(K / KC)
+  int32_t upr;            // units per round (<= kConsumerWarps)
+  int32_t eb;             // weight element bytes
+  int32_t wdt;            // weight DType
+  int32_t has_weights;
+  uint64_t region;        // byte offset of the phase's region in the image (expert 0 for expert phases)
+  uint64_t expert_stride; // bytes of one expert's region
+};
+
+struct StepState {
+  int32_t pos;        // position of the token being decoded
+  int32_t token;      // input token (ignored when a token sequence is given)
+  float temperature;  // 0: greedy
+  float u;            // uniform for sampling (ignored when a uniform sequence is given)
+  int32_t seq_index;  // index into token / uniform / output sequences
+  int32_t out_token;  // chosen token of the last completed step
+  int32_t pad0, pad1;
+};
+
+struct Params {
+  // weights
+  const uint8_t* image;
+  const void* tok_emb;
+  const void* const* attn_norm;       // [L] device pointers
+  const void* const* ffn_norm;        // [L]
+  const void* final_norm;
+  const float* const* e_gate_scale;   // [L] -> [E][f]
+  const float* const* e_up_scale;     // [L] -> [E][f]
+  const float* const* e_down_scale;   // [L] -> [E][d]
+  const PhaseDesc* phases;
+  int32_t n_phases;
+  // shapes
+  int32_t L, d, hq, hkv, hd, ff, V, max_ctx, E, topk, fexp;
+  int32_t wdt, kvdt, rdt;
+  float eps;
+  float attn_scale;
+  int32_t nbmax;                      // max attention blocks = ceil(max_ctx / 32)
+  // KV cache [L][hkv][max_ctx][hd]
+  uint16_t* kc;
+  uint16_t* vc;
+  // RoPE tables [max_ctx][hd/2]
+  const float* rope_cos;
+  const float* rope_sin;
+  // scratch
+  float* x;        // [d] residual
+  float* q;        // [hq*hd] post-RoPE queries
+  float* attn;     // [hq*hd] attention output
+  float* h;        // [max(ff, topk*f)] FFN activations
+  float* rlog;     // [E] router logits
+  float* part_m;   // [hq][nbmax]
+  float* part_l;   // [hq][nbmax]
+  float* part_o;   // [hq][nbmax][hd]
+  uint32_t* head_ctr;          // [hq]
+  float* sblock;               // [ceil(V/256)] sampling block sums
+  uint32_t* sample_ctr;
+  unsigned long long* argkey;  // packed (ordered logit, ~index) maximum
+  uint32_t* lm_ctr;
+  unsigned long long* bar_ctr; // monotonic grid-barrier counter
+  int32_t* err;                // sticky device error word
+  int32_t* sel_out;            // [L][topk] router choices
+  const int32_t* force_sel;    // [L][topk] forced experts or null
+  float* trace;                // [L+1][d] residual trace or null
+  StepState* state;
+  const int32_t* tok_seq;      // token per step (prefill) or null
+  const float* u_seq;          // uniform per step or null
+  int32_t* out_seq;            // chosen token per step or null
+  float* logits;               // [V] logits output
+  uint64_t wait_ns;            // limit of every in-kernel wait
+  int32_t skip_cta, skip_barrier;
+};
+
+// Device error codes (the host maps them to ADP_ERR_*).
+enum DevErr : int32_t { DE_NONE = 0, DE_BARRIER_TIMEOUT = 1, DE_PIPELINE_TIMEOUT = 2 };
+
+}  // namespace adp

@@ -1,0 +1,69 @@
+// Copy the caller's row-major weight matrices into the model-owned image, in the order each
+// persistent CTA consumes them: for CTA c, its units [u0, u0 + n) in rounds of `upr` units,
+// each round as K-chunks, each chunk as [unit][row][KC elements].  One TMA bulk copy then
+// moves one tile.  Runs once, at model creation.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "launch.h"
+
+namespace adp {
+
+// Source row (as a byte pointer) of row j of unit u of phase P, expert e.
+__device__ __forceinline__ const uint8_t* source_row(const PhaseDesc& P, const RepackSrc& S, int u, int j, int e) {
+  const uint64_t row_bytes = (uint64_t)P.K * P.eb;
+  switch (P.kind) {
+    case PK_QKV: {
+      const int half = S.hd / 2, nq = S.hq * half, nk = S.hkv * half;
+      const uint8_t* m = S.a;
+      int uu = u;
+      if (u >= nq + nk) { m = S.c; uu = u - nq - nk; }
+      else if (u >= nq) { m = S.b; uu = u - nq; }
+      const int head = uu / half, i = uu % half;
+      return m + (uint64_t)(head * S.hd + i + j * half) * row_bytes;
+    }
+    case PK_GU:
+      return (j == 0 ? S.a : S.b) + (uint64_t)u * row_bytes;
+    case PK_EGU:
+      return (j == 0 ? S.a : S.b) + (uint64_t)e * S.expert_src_stride + (uint64_t)u * row_bytes;
+    case PK_EDOWN:
+      return S.a + (uint64_t)e * S.expert_src_stride + (uint64_t)(u * P.unit_rows + j) * row_bytes;
+    default:  // PK_WO, PK_DOWN, PK_LM, PK_ROUTER: row groups
+      return S.a + (uint64_t)(u * P.unit_rows + j) * row_bytes;
+  }
+}
+
+__global__ void repack_kernel(uint8_t* image, PhaseDesc P, RepackSrc S) {
+  const uint32_t c = blockIdx.x, G = gridDim.x;
+  const int e = blockIdx.y;
+  const long long a0 = (long long)c * P.n_units / G, a1 = (long long)(c + 1) * P.n_units / G;
+  const int u0 = (int)a0, n = (int)(a1 - a0);
+  if (n <= 0) return;
+  const uint64_t unit_bytes = (uint64_t)P.unit_rows * P.K * P.eb;
+  uint8_t* dst_cta = image + P.region + (uint64_t)e * P.expert_stride + (uint64_t)u0 * unit_bytes;
+  const int per16 = 16 / P.eb;               // elements per 16-byte vector
+  const int nv16 = P.K / per16;               // vectors per row
+  const long long total = (long long)n * P.unit_rows * nv16;
+  for (long long idx = threadIdx.x; idx < total; idx += blockDim.x) {
+    const int lu = (int)(idx / ((long long)P.unit_rows * nv16));
+    const int rem = (int)(idx % ((long long)P.unit_rows * nv16));
+    const int j = rem / nv16, cv = rem % nv16;
+    const int col = cv * per16;
+    const int ck = col / P.KC;
+    const int kck = min(P.KC, P.K - ck * P.KC);
+    const int r = lu / P.upr, i = lu % P.upr;
+    const int m = min(P.upr, n - r * P.upr);
+    const uint64_t off = (uint64_t)r * P.upr * unit_bytes + (uint64_t)m * P.unit_rows * ck * P.KC * P.eb +
+                         ((uint64_t)(i * P.unit_rows + j) * kck + (col - ck * P.KC)) * P.eb;
+    const uint8_t* src = source_row(P, S, u0 + lu, j, e) + (uint64_t)col * P.eb;
+    *reinterpret_cast<uint4*>(dst_cta + off) = *reinterpret_cast<const uint4*>(src);
+  }
+}
+
+cudaError_t repack_launch(uint8_t* image, const PhaseDesc& P, const RepackSrc& S, int grid, int experts,
+                          cudaStream_t stream) {
+  repack_kernel<<<dim3(grid, experts), 256, 0, stream>>>(image, P, S);
+  return cudaGetLastError();
+}
+
+}  // namespace adp

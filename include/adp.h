@@ -1,0 +1,195 @@
+/*
+ * adp.h — C ABI of a batch-1 persistent decode engine for one GB300 (sm_103a).
+ *
+ * The engine runs one autoregressive decode step of a decoder-only transformer
+ * (dense SwiGLU or top-k MoE with e4m3 experts) as ONE persistent CUDA kernel per
+ * step with grid-wide barriers, instead of a kernel per operation.
+ *
+ * Pages this interface follows (cited by title and section):
+ *  [H] "標準GPUによるリアルタイムLLM推論：リクエストあたり3,000トークン/秒" (hakusoku.com
+ *      summary of Kog AI, "Real-time LLM inference on standard GPUs: 3,000 tokens/s per request"):
+ *      §"単一リクエストLLMデコード速度の重要性" (single-request decode speed is the metric),
+ *      §"GPU推論の速度制限要因：メモリ帯域幅" (batch-1 decode is matrix-vector work that streams
+ *        every active weight and the KV cache: tokens/s <= bandwidth / (beta*weights + KV)),
+ *      §"標準推論スタックのボトルネックとKogの工夫" (per-kernel launch/cleanup overhead; one
+ *        GPU-resident program runs the whole decode path),
+ *      §"Kog Inference Engineの特徴とイノベーション" (the program covers MatMul, attention,
+ *        normalization, routing and sampling, and controls sync, prefetch and order).
+ *  [A] "標準 GPU で LLM 推論 3000 tokens/s/req — 数字の前提を運用者目線で読む" (aether-echoes.com),
+ *      §"どう出したか": no quantization, speculative decoding, pruning or KV compression.
+ *  [S] "「ソフトウェア・ファースト」戦略でGPUの限界を突破" (studioglobal.ai),
+ *      §"独自の3層共同設計アプローチ" item 1 (monokernel: the whole decode as one persistent kernel).
+ *
+ * Conventions for every call:
+ *  - Return value: ADP_OK (0) or a negative ADP_ERR_* code; no call aborts or throws.
+ *  - Device errors (a barrier or pipeline wait that ran out) are sticky: every later
+ *    decode call on the model returns the same code until adp_reset.
+ *  - Calls on one model are not thread-safe; all GPU work goes on the model's stream.
+ *  - "device pointer" = cudaMalloc'd (or equivalent) memory of the current device;
+ *    "host pointer" = ordinary (pageable or pinned) host memory.
+ */
+#ifndef ADP_H_
+#define ADP_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
+/* Storage types of weights and of the KV cache. */
+typedef enum { ADP_F16 = 0, ADP_BF16 = 1, ADP_E4M3 = 2, ADP_F32 = 3 } adp_dtype;
+
+enum {
+  ADP_OK = 0,
+  ADP_ERR_INVALID_ARG = -1,        /* null pointer, bad token id, n < 0 ... */
+  ADP_ERR_UNSUPPORTED_CONFIG = -2, /* shape or dtype combination the kernel does not implement */
+  ADP_ERR_CONTEXT_OVERFLOW = -3,   /* position >= max_ctx */
+  ADP_ERR_CUDA = -4,               /* a CUDA runtime call failed (message: adp_last_error) */
+  ADP_ERR_NOT_CORESIDENT = -5,     /* the persistent grid cannot be co-resident on this GPU */
+  ADP_ERR_BARRIER_TIMEOUT = -6,    /* a grid barrier wait ran out (sticky until adp_reset) */
+  ADP_ERR_PIPELINE_TIMEOUT = -7,   /* a weight-pipeline wait ran out (sticky until adp_reset) */
+  ADP_ERR_UNIMPLEMENTED = -8
+};
+
+/* Model shape and types.  Row-major [out, in] weights, no biases, pre-norm decoder:
+ * x += Wo . attn(rope(Wq xn), rope(Wk xn), Wv xn);  x += FFN(rmsnorm(x));  logits = W_lm rmsnorm(x).
+ * RMSNorm with eps inside the root, rotate-half RoPE (pairs i, i + head_dim/2) with
+ * inv_freq_i = rope_theta^(-2i/head_dim), grouped-query attention where query head h reads
+ * KV head floor(h * n_kv_heads / n_heads).  n_experts == 0 selects the dense SwiGLU FFN
+ * (d_ff wide); otherwise a softmax top_k router over n_experts SwiGLU experts of width d_expert,
+ * gates renormalised over the chosen experts ([H] §"Kog Inference Engineの特徴とイノベーション":
+ * routing is one of the stages; Hacker News author reply: FP8 MoE models at batch 1). */
+typedef struct {
+  int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, d_ff, vocab, max_ctx;
+  float rms_eps, rope_theta;
+  int32_t tied_embeddings;          /* 1: logits use tok_emb as the LM head */
+  int32_t weight_dtype, kv_dtype;   /* adp_dtype: ADP_F16 or ADP_BF16 for both */
+  int32_t n_experts, top_k, d_expert;
+  int32_t router_dtype, expert_dtype; /* router: ADP_F16/ADP_BF16; experts: ADP_E4M3 */
+} adp_config;
+
+/* Per-layer weights: DEVICE pointers, contiguous row-major, borrowed (never written; the
+ * engine copies the matrices into its own streaming layout at creation, but tok_emb, the
+ * norm gains and the expert scales are read in place, so all must outlive the model). */
+typedef struct {
+  const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm;   /* [d], [hq*hd, d], [hkv*hd, d] x2, [d, hq*hd], [d] */
+  const void *w_gate, *w_up, *w_down;                     /* dense: [ff, d], [ff, d], [d, ff]; else NULL */
+  const void *router;                                     /* MoE: [E, d]; else NULL */
+  const void *e_gate, *e_up, *e_down;                     /* MoE: [E, f, d], [E, f, d], [E, d, f] e4m3 */
+  const float *e_gate_scale, *e_up_scale, *e_down_scale;  /* MoE: [E, f], [E, f], [E, d] fp32, applied
+                                                             to each output channel after its dot product */
+} adp_layer_weights;
+
+typedef struct {
+  const void *tok_emb;     /* [vocab, d] device */
+  const void *lm_head;     /* [vocab, d] device, or NULL when tied */
+  const void *final_norm;  /* [d] device */
+  const adp_layer_weights *layers; /* HOST array of n_layers entries */
+} adp_weights;
+
+/* Sampling of the next token ([H] §"Kog Inference Engineの特徴とイノベーション": sampling is
+ * a stage of the GPU program).  temperature == 0: greedy argmax, lowest index on ties.
+ * temperature > 0: inverse-CDF draw from softmax(logits / temperature) with the caller's
+ * uniform u in [0, 1) (the engine draws no random numbers itself). */
+typedef struct {
+  float temperature;
+  float u;
+} adp_sampling;
+
+typedef struct adp_model adp_model;
+typedef struct adp_kv adp_kv;
+
+/* Create a model on the current CUDA device.
+ *  cfg, w     host structs as above (w->layers host array; tensors device pointers)
+ *  stream     cudaStream_t (as void*) the model launches on; NULL = the legacy default stream
+ *  out        receives the model handle
+ * Validates the shapes (head_dim even and <= 256; d_model, widths and vocab multiples of 8;
+ * the persistent grid co-resident: one CTA per SM), plans the per-SM weight streams, copies
+ * the matrices into the engine's own tile-ordered image (device memory owned by the model),
+ * and allocates scratch.  Synchronises the stream before returning.
+ * Errors: ADP_ERR_INVALID_ARG, ADP_ERR_UNSUPPORTED_CONFIG, ADP_ERR_NOT_CORESIDENT, ADP_ERR_CUDA. */
+int adp_create_model(const adp_config* cfg, const adp_weights* w, void* stream, adp_model** out);
+void adp_destroy_model(adp_model* m);
+
+/* KV cache of one sequence ([H] §"GPU推論の速度制限要因：メモリ帯域幅": the KV cache is the
+ * other stream each token reads; [A] §"どう出したか": kept uncompressed).  Engine-owned device
+ * memory, layout [n_layers][n_kv_heads][max_ctx][head_dim] of cfg.kv_dtype for K and for V;
+ * K rows hold post-RoPE keys.  A cache belongs to the model it was created from. */
+int adp_kv_create(adp_model* m, adp_kv** out);
+void adp_kv_destroy(adp_kv* kv);
+int adp_kv_reset(adp_kv* kv);                        /* length := 0 */
+int adp_kv_len(const adp_kv* kv, int32_t* len);      /* number of cached positions */
+/* Copy positions [0, len) in from / out to HOST arrays k, v of shape [n_layers][n_kv_heads][len][head_dim]
+ * (storage bits of kv_dtype).  Load sets the length to len.  This is the whole decode state, so
+ * it also serves as checkpoint save/restore.  Synchronous.  ADP_ERR_CONTEXT_OVERFLOW if len > max_ctx. */
+int adp_kv_load(adp_kv* kv, const void* host_k, const void* host_v, int32_t len);
+int adp_kv_read(const adp_kv* kv, void* host_k, void* host_v, int32_t len);
+
+/* One decode step ([H] §"単一リクエストLLMデコード速度の重要性"): token `token` at position
+ * p = current length; writes its K/V rows to the cache, returns the next token.
+ *  sampling     host struct, NULL = greedy
+ *  next_token   host pointer, receives the sampled/greedy next token
+ *  dev_logits   optional DEVICE pointer [vocab] fp32 that receives the step's logits
+ * One cooperative kernel launch (one grid barrier between dependent phases), a 4-byte token
+ * and the 16-byte step state in, the token and status word out; synchronises the stream.
+ * Errors: ADP_ERR_CONTEXT_OVERFLOW (p >= max_ctx; nothing launched), ADP_ERR_INVALID_ARG,
+ * ADP_ERR_BARRIER_TIMEOUT / ADP_ERR_PIPELINE_TIMEOUT (sticky), ADP_ERR_CUDA. */
+int adp_decode_step(adp_model* m, adp_kv* kv, int32_t token, const adp_sampling* sampling,
+                    int32_t* next_token, float* dev_logits);
+
+/* Prefill: n successive decode steps over HOST tokens[0..n) (positions len..len+n-1) through the
+ * same kernel, so prompt-written and decode-written KV rows follow one arithmetic; returns the
+ * next token after the last one (and its logits if dev_logits).  One host->device copy of the
+ * tokens, n launches, one synchronisation. */
+int adp_prefill(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t n, const adp_sampling* sampling,
+                int32_t* next_token, float* dev_logits);
+
+/* Generation without host round trips: n decode steps starting from `token`, each step feeding
+ * the token the previous one chose.  dev_u: optional DEVICE array of n uniforms (used when
+ * temperature > 0).  dev_tokens_out: DEVICE array [n] that receives the chosen tokens.  Returns
+ * after enqueueing (does not synchronise); adp_sync reports device errors. */
+int adp_generate_async(adp_model* m, adp_kv* kv, int32_t token, int32_t n, float temperature, const float* dev_u,
+                       int32_t* dev_tokens_out);
+int adp_sync(adp_model* m);                          /* synchronise the stream; report sticky errors */
+
+int adp_reset(adp_model* m);                         /* clear a sticky device error and sync counters */
+const char* adp_status_string(int status);
+const char* adp_last_error(void);                    /* text of the last ADP_ERR_CUDA in this thread */
+
+/* Introspection used by tests and the benchmark. */
+int adp_num_ctas(const adp_model* m, int32_t* ctas);            /* persistent grid size (SMs) */
+int adp_image_bytes(const adp_model* m, uint64_t* bytes);       /* bytes of the tile-ordered weight image */
+int adp_launches_per_step(const adp_model* m, int32_t* n);      /* kernel launches of one decode step */
+
+/* Debug and ablation hooks ([H] §"標準推論スタックのボトルネックとKogの工夫": the launch
+ * overhead the persistent kernel removes is measured by running the same device code as one
+ * launch per phase).
+ *  mode 0: persistent (one cooperative launch per step, grid barriers)
+ *  mode 1: multi-kernel (one launch per phase, same device functions, same arithmetic)
+ *  mode 2: multi-kernel, captured once into a CUDA graph and replayed per step */
+int adp_debug_kernel_mode(adp_model* m, int mode);
+/* Force MoE expert choices: HOST array [n_layers][top_k] of expert ids (NULL = router decides).
+ * Gates are the router's probabilities of the forced experts, renormalised over them. */
+int adp_debug_force_experts(adp_model* m, const int32_t* host_idx);
+/* The router's own choices of the last step: HOST array [n_layers][top_k]. */
+int adp_debug_read_experts(const adp_model* m, int32_t* host_idx);
+/* Record the residual entering each layer (and the final one) of every step into a DEVICE
+ * buffer [n_layers + 1][d_model] fp32 (NULL = off). */
+int adp_debug_trace_residual(adp_model* m, float* dev_buf);
+/* Wait limit of every in-kernel spin (grid barrier, weight pipeline), nanoseconds (default 2e8). */
+int adp_debug_set_wait_limit(adp_model* m, uint64_t ns);
+/* Test hook: CTA `cta` skips its arrival at grid barrier number `barrier` of the next step
+ * (-1 = off), so that the others' wait runs out and the step returns ADP_ERR_BARRIER_TIMEOUT. */
+int adp_debug_skip_barrier_arrival(adp_model* m, int32_t cta, int32_t barrier);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
+#ifdef __cplusplus
+}
+#endif
+#endif /* ADP_H_ */

@@ -30,7 +30,7 @@
  *    dot(w,x,K,VW): 32 partial sums; vector v (VW consecutive elements) goes to
  *        partial v mod 32 in ascending v, its elements fused-multiply-added in
  *        ascending order; the partials are then folded pairwise (i, i+16), (i, i+8),
- *        (i, i+4), (i, i+2), (i, i+1).  VW = 16 for 8-bit weights, else 8.
+ *        (i, i+4), (i, i+2), (i, i+1).  The step uses VW = 8 for every operand type.
  *    rmsnorm: ss = dot(x,x,d,8); r = 1/sqrtf(ss/d + eps); xn_i = (x_i*r)*g_i.
  *    rope:    a' = fma(a, c, -(b*s)); b' = fma(b, c, a*s); cos/sin tables from
  *             double pow/cos/sin rounded to fp32.
@@ -252,7 +252,7 @@ static inline float expm(float x, int mode) { return mode == ORC_EXACT ? orc_exp
 
 /* y[r] = scale[r] * (W[r,:] . x) for r < rows (scale NULL -> 1, applied after the dot). */
 static int gemv(const void* Wt, int dt, int rows, int K, const float* x, const float* scale, float* y, int mode) {
-  const int VW = dt == ORC_E4M3 ? 16 : 8;
+  const int VW = 8;
   int fail = 0;
 #pragma omp parallel reduction(| : fail)
   {
