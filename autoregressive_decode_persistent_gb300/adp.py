@@ -69,6 +69,7 @@ _SIGS = [
     ("adp_kv_create", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]),
     ("adp_kv_destroy", None, [ctypes.c_void_p]),
     ("adp_kv_reset", ctypes.c_int, [ctypes.c_void_p]),
+    ("adp_kv_truncate", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     ("adp_kv_len", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     ("adp_kv_load", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]),
     ("adp_kv_read", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]),
@@ -161,6 +162,10 @@ def adp_kv_destroy(kv):
 
 def adp_kv_reset(kv):
     _check(load_library().adp_kv_reset(kv), "adp_kv_reset")
+
+
+def adp_kv_truncate(kv, length: int):
+    _check(load_library().adp_kv_truncate(kv, int(length)), "adp_kv_truncate")
 
 
 def adp_kv_len(kv) -> int:

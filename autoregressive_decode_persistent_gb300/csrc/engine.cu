@@ -387,6 +387,12 @@ extern "C" int adp_kv_reset(adp_kv* kv) {
   return ADP_OK;
 }
 
+extern "C" int adp_kv_truncate(adp_kv* kv, int32_t len) {
+  if (!kv || len < 0 || len > kv->len) return ADP_ERR_INVALID_ARG;
+  kv->len = len;
+  return ADP_OK;
+}
+
 extern "C" int adp_kv_len(const adp_kv* kv, int32_t* len) {
   if (!kv || !len) return ADP_ERR_INVALID_ARG;
   *len = kv->len;

@@ -34,7 +34,10 @@ def make_config(cfg: dict) -> adp.Config:
 class DecodeModel:
     """A model on one GPU plus its KV caches (see include/adp.h for the semantics)."""
 
-    def __init__(self, cfg: dict, host_weights: dict, device: str = "cuda:0", stream: torch.cuda.Stream | None = None):
+    _MATRICES = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "router", "e_gate", "e_up", "e_down")
+
+    def __init__(self, cfg: dict, host_weights: dict, device: str = "cuda:0", stream: torch.cuda.Stream | None = None,
+                 keep_matrices: bool = False):
         self.cfg = cfg
         self.device = torch.device(device)
         torch.cuda.set_device(self.device)
@@ -42,26 +45,34 @@ class DecodeModel:
         W = host_weights
         self._dev = {}
         keep = []
+        matrices = []
 
-        def up(a):
+        def up(a, matrix=False):
             t = to_device(a, self.device)
             if t is not None:
-                keep.append(t)
+                (matrices if matrix else keep).append(t)
             return None if t is None else t.data_ptr()
 
         layers = (adp.LayerWeights * cfg["n_layers"])()
         for i, Lw in enumerate(W["layers"]):
-            f = {k: up(Lw.get(k)) for k in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up",
+            f = {k: up(Lw.get(k), k in self._MATRICES) for k in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up",
                                              "w_down", "router", "e_gate", "e_up", "e_down", "e_gate_scale",
                                              "e_up_scale", "e_down_scale")}
             layers[i] = adp.LayerWeights(**f)
         self._layers = layers
-        self.weights = adp.Weights(up(W["tok_emb"]), up(W.get("lm_head")), up(W["final_norm"]), layers)
+        self.weights = adp.Weights(up(W["tok_emb"]), up(W.get("lm_head"), True), up(W["final_norm"]), layers)
         self._keep = keep
         self.config = make_config(cfg)
         torch.cuda.synchronize(self.device)
         sh = stream.cuda_stream if stream is not None else 0
         self.handle = adp.adp_create_model(self.config, self.weights, sh)
+        # The engine copied every matrix into its own tile-ordered image at creation and reads
+        # only the embedding, norm gains and expert scales in place afterwards.
+        if keep_matrices:
+            self._keep += matrices
+        del matrices
+        torch.cuda.synchronize(self.device)
+        torch.cuda.empty_cache()
 
     def close(self):
         if getattr(self, "handle", None):
@@ -117,6 +128,9 @@ class KVCache:
 
     def reset(self):
         adp.adp_kv_reset(self.handle)
+
+    def truncate(self, length: int):
+        adp.adp_kv_truncate(self.handle, length)
 
     def load(self, k: np.ndarray, v: np.ndarray):
         adp.adp_kv_load(self.handle, k, v, k.shape[2])

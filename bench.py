@@ -1,0 +1,355 @@
+"""Batch-1 decode throughput of the 2.3B-class fp16 decoder on one GB300.
+
+Workload: 25 layers, d_model 2560, 20 query heads x 128, 4 KV heads, SwiGLU 9728, tied
+vocabulary 32000, fp16 weights ~N(0, 0.02) from a seed; a 512-token uniform-random prompt is
+prefilled, then greedy decode steps run at contexts 513..1024 (a run longer than 512 steps
+rewinds the cache to 512 and decodes the window again). One step = one decode step of the
+whole model = one persistent kernel launch.
+
+Printed (one JSON line, rank 0):
+  value      tokens/s, device-timed: the steps chained on the GPU (adp_generate_async), weights
+             and KV resident in HBM, CUDA events around the timed region on the model's stream;
+  e2e        tokens/s through adp_decode_step with the token in and out of host memory every
+             step (a 32-byte step state host->device, 8 bytes device->host, one sync per step);
+  roofline   algorithmic bytes per launch (every weight once + KV of the context + the new KV
+             row) / average launch duration, against the measured HBM copy bandwidth;
+  cpu_baseline  the CPU oracle (plain fp32, all host cores) timed on a bounded sample.
+
+--impl reference times the CPU oracle as the reference arm on the same workload.
+Several GPUs (torchrun): independent replicas, one per GPU, no collective; value = all
+tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 decode tokens/s/request (2.3B fp16); achieved HBM GB/s vs GB300 peak"
+WORKLOAD = "dense-2.3b-fp16"
+WINDOW = 512  # decode steps per pass over contexts 513..1024
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "autoregressive_decode_persistent_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_kernel_dense-2.3b-fp16.md")
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel source sha256\[:16\]:\s*`?([0-9a-f]{16})", text)
+    m_tr = re.search(r"traffic bytes per launch:\s*`?([0-9.e+]+)", text)
+    if not m_hash or not m_tr or m_hash.group(1) != src_hash:
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons sampled while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(cfg, W, seconds: float = 15.0, max_steps: int | None = None):
+    """The CPU oracle as it stands (plain mode) on a bounded sample of the workload."""
+    import synth
+    from oracle import PLAIN, OracleModel
+    om = OracleModel(cfg, W)
+    om.load_kv_prefix(*synth.kv_prefix(cfg, cfg["prompt_len"]))
+    toks = synth.prompt(cfg, 64, seed=99)
+    om.step(int(toks[0]), PLAIN)  # first call: tables, page-in
+    n, t0 = 0, time.perf_counter()
+    while True:
+        om.step(int(toks[(n + 1) % len(toks)]), PLAIN)
+        n += 1
+        el = time.perf_counter() - t0
+        if (el >= seconds and n >= 2) or (max_steps and n >= max_steps):
+            break
+    cores = len(os.sched_getaffinity(0))
+    return {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} plain-fp32 decode steps of the full 2.3B model at contexts "
+                      f"{cfg['prompt_len'] + 1}..{cfg['prompt_len'] + n + 1} (synthetic 512-position KV prefix), "
+                      f"OpenMP over {cores} host threads, {el:.1f} s"}, n, el
+
+
+def run_engine(args, rank: int, world: int):
+    import torch
+
+    import synth
+    from autoregressive_decode_persistent_gb300 import bound, build
+    from autoregressive_decode_persistent_gb300.model import DecodeModel
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(dev)
+    build.build()
+    cfg = synth.get_config(WORKLOAD)
+    W = synth.model_weights(cfg)
+    prompt = synth.prompt(cfg)
+    model = DecodeModel(cfg, W, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kv = model.new_kv()
+    P = cfg["prompt_len"]
+    tok0 = kv.prefill(prompt)
+    out = torch.empty(WINDOW, dtype=torch.int32, device=dev)
+
+    def passes(n_steps):
+        """Decode n_steps chained steps in windows of contexts P+1..P+WINDOW."""
+        t = tok0
+        left = n_steps
+        while left > 0:
+            k = min(left, WINDOW)
+            kv.truncate(P)
+            kv.generate_async(t, k, out)
+            left -= k
+
+    # warm-up (untimed)
+    passes(args.warmup)
+    from autoregressive_decode_persistent_gb300 import adp
+    adp.adp_sync(model.handle)
+    torch.cuda.synchronize(dev)
+
+    # timed region: device events on the model's stream
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record(stream)
+        passes(args.steps)
+        e1.record(stream)
+        e1.synchronize()
+    adp.adp_sync(model.handle)
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # algorithmic bytes: contexts P+1 .. P+k in each window
+    total_bytes = 0
+    left = args.steps
+    while left > 0:
+        k = min(left, WINDOW)
+        total_bytes += bound.mean_bytes_per_token(cfg, P + 1, k) * k
+        left -= k
+    per_launch = total_bytes / args.steps
+    launch_ms = ms / args.steps
+    peak, peak_kind = _peaks()
+    achieved = per_launch / (launch_ms * 1e-3) / 1e9
+
+    # e2e through the public per-step call, host token in and out every step
+    n_e2e = min(args.steps, 2 * WINDOW)
+    kv.truncate(P)
+    t = tok0
+    torch.cuda.synchronize(dev)
+    h0 = time.perf_counter()
+    for i in range(n_e2e):
+        if i and i % WINDOW == 0:
+            kv.truncate(P)
+        t = kv.step(t)
+    h1 = time.perf_counter()
+    e2e = n_e2e / (h1 - h0)
+
+    res = {
+        "ms": ms, "steps": args.steps, "achieved_gbs": achieved, "per_launch_bytes": per_launch,
+        "launch_ms": launch_ms, "peak": peak, "peak_kind": peak_kind, "e2e": e2e, "n_e2e": n_e2e,
+        "clocks": clocks.summary(), "ctas": model.num_ctas, "image_bytes": model.image_bytes,
+        "launches": model.launches_per_step * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu"] = cpu_baseline(cfg, W, seconds=args.cpu_seconds)[0]
+    kv.close()
+    model.close()
+    return cfg, res
+
+
+def emit_engine(args, cfg, res, world):
+    value = world * res["steps"] / (res["ms"] * 1e-3)
+    src = kernel_source_hash()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": res["steps"],
+        "warmup": args.warmup,
+        "ms_per_step": round(res["ms"] / res["steps"], 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic: seeded N(0,0.02) fp16 weights, 512 uniform-random prompt ids",
+        "config": {
+            "workload": f"{WORKLOAD}: 25 layers, d 2560, 20x128 q heads, 4 kv heads, ffn 9728, tied vocab 32000; "
+                        "batch 1, prompt 512, greedy decode at contexts 513..1024",
+            "weights": "f16", "kv_cache": "f16", "batch": 1, "prompt": cfg["prompt_len"],
+            "contexts": f"{cfg['prompt_len'] + 1}..{cfg['prompt_len'] + min(res['steps'], WINDOW)}",
+            "kernel": "persistent (one cooperative launch per decode step)",
+            "ctas": res["ctas"],
+            "l2": "inputs larger than L2: every step streams 4.69 GB of weights (L2 129 MB)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "e2e": {"value": round(res["e2e"] * world, 2), "unit": "tokens/s", "h2d_bytes_per_step": 32,
+                "d2h_bytes_per_step": 8, "steps": res["n_e2e"],
+                "path": "adp_decode_step per token (host token in, host token out, stream sync)"},
+        "roofline": {"bound": "hbm", "achieved": round(res["achieved_gbs"], 1), "peak": res["peak"],
+                     "unit": "GB/s", "frac": round(res["achieved_gbs"] / res["peak"], 4),
+                     "traffic": profiled_traffic(src), "kernel": "adp::decode_kernel",
+                     "bytes_per_launch": int(res["per_launch_bytes"]),
+                     "launch_ms": round(res["launch_ms"], 5),
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({res['peak_kind']}; read+write copy)",
+                     "frac_of_8000": round(res["achieved_gbs"] / 8000.0, 4)},
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "kernel_source": src,
+    }
+    if "cpu" in res:
+        line["cpu_baseline"] = res["cpu"]
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank: int, world: int):
+    """Reference arm: the CPU oracle (plain fp32) on the same workload, bounded."""
+    if rank != 0:
+        return
+    import synth
+    cfg = synth.get_config(WORKLOAD)
+    W = synth.model_weights(cfg)
+    budget = max(10.0, min(120.0, args.cpu_seconds * 4))
+    cpu, n, el = cpu_baseline(cfg, W, seconds=budget, max_steps=max(2, args.steps))
+    value = cpu["value"]
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": n,
+        "warmup": 1,
+        "ms_per_step": round(el * 1e3 / n, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic: seeded N(0,0.02) fp16 weights",
+        "config": {"workload": f"{WORKLOAD}: 25 layers, d 2560, tied vocab 32000; batch 1, greedy decode at "
+                               "contexts from 513", "weights": "f16", "batch": 1, "prompt": cfg["prompt_len"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "reference": "CPU oracle (oracle/oracle.c, plain mode): the pages publish no code to install",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["engine", "reference"], default="engine")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        cfg, res = run_engine(args, rank, world)
+        if rank == 0:
+            emit_engine(args, cfg, res, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

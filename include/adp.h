@@ -122,6 +122,9 @@ void adp_destroy_model(adp_model* m);
 int adp_kv_create(adp_model* m, adp_kv** out);
 void adp_kv_destroy(adp_kv* kv);
 int adp_kv_reset(adp_kv* kv);                        /* length := 0 */
+/* Rewind to the first len positions (0 <= len <= current length); later rows are overwritten
+ * by the next steps.  Host-side only.  ADP_ERR_INVALID_ARG if len is out of range. */
+int adp_kv_truncate(adp_kv* kv, int32_t len);
 int adp_kv_len(const adp_kv* kv, int32_t* len);      /* number of cached positions */
 /* Copy positions [0, len) in from / out to HOST arrays k, v of shape [n_layers][n_kv_heads][len][head_dim]
  * (storage bits of kv_dtype).  Load sets the length to len.  This is the whole decode state, so

@@ -1,0 +1,84 @@
+"""Full-size workloads on the GPU, in the launch configuration the benchmark times (persistent
+kernel, one CTA per SM), against the CPU oracle on sampled steps.
+
+Each case loads a synthetic KV prefix of the workload's prompt length into both the engine and
+the oracle (the cache is the whole decode state; its contents are seeded N(0,1) values in the KV
+dtype), then decodes a few steps teacher-forced on the oracle's tokens: bit-exact against the
+oracle's contract mode (logits, tokens, every new KV row, MoE routing) and within the stated
+tolerances against its plain fp32 mode."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import EXACT, PLAIN
+
+from gpu_common import assert_logits_within_tolerance, engine_forced, oracle_forced, oracle_free_run
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def built():
+    import torch
+    assert torch.cuda.is_available()
+    from autoregressive_decode_persistent_gb300 import build
+    build.build()
+
+
+@pytest.mark.parametrize("name,prefix,steps,temperature", [
+    ("dense-2.3b-fp16", 512, 6, 0.0),
+    ("dense-2.3b-fp16-long-t0.7", 3584, 4, 0.7),
+    ("dense-8b-bf16", 1024, 3, 0.0),
+    ("moe-32x1408-top4-e4m3", 256, 5, 0.0),
+])
+def test_full_size_workload(built, name, prefix, steps, temperature):
+    from autoregressive_decode_persistent_gb300.model import DecodeModel
+    cfg = synth.get_config(name)
+    W = synth.model_weights(cfg)
+    kvp = synth.kv_prefix(cfg, prefix)
+    first = synth.prompt(cfg, 1)
+    us = synth.sampling_uniforms(steps, first=prefix) if temperature > 0 else None
+    toks, ref_e, next_e, experts_e, om = oracle_free_run(cfg, W, first, steps - 1, EXACT, temperature, us, kvp)
+    model = DecodeModel(cfg, W)
+    got, next_g, k, v, experts_g = engine_forced(model, toks, temperature, us, kvp,
+                                                 read_experts=bool(cfg["n_experts"]))
+    model.close()
+    n = prefix + len(toks)
+    assert next_g == next_e
+    assert np.array_equal(got.view(np.uint32), ref_e.view(np.uint32))
+    assert np.array_equal(k[:, :, prefix:n], om.kc[:, :, prefix:n])
+    assert np.array_equal(v[:, :, prefix:n], om.vc[:, :, prefix:n])
+    assert np.array_equal(k[:, :, :prefix], kvp[0]) and np.array_equal(v[:, :, :prefix], kvp[1])
+    if cfg["n_experts"]:
+        for i in range(len(toks)):
+            assert np.array_equal(experts_g[i], experts_e[i])
+    ref_p, _, _ = oracle_forced(cfg, W, toks, PLAIN, temperature, us, kvp)
+    assert_logits_within_tolerance(got, ref_p)
+
+
+def test_full_size_prefill_path(built):
+    """The prompt path at full size: adp_prefill of 16 tokens then 2 decode steps, against the
+    oracle run step by step from an empty cache."""
+    import torch
+    from autoregressive_decode_persistent_gb300.model import DecodeModel
+    from oracle import OracleModel
+    cfg = synth.get_config("dense-2.3b-fp16")
+    W = synth.model_weights(cfg)
+    prompt = synth.prompt(cfg, 16)
+    om = OracleModel(cfg, W)
+    out = None
+    for t in prompt:
+        out = om.step(int(t), EXACT)
+    model = DecodeModel(cfg, W)
+    kv = model.new_kv()
+    lg = torch.empty(cfg["vocab"], device=model.device)
+    nxt = kv.prefill(prompt, logits=lg)
+    assert nxt == out["next"]
+    assert np.array_equal(lg.cpu().numpy().view(np.uint32), out["logits"].view(np.uint32))
+    for _ in range(2):
+        ref = om.step(nxt, EXACT)
+        nxt = kv.step(nxt, logits=lg)
+        assert nxt == ref["next"]
+        assert np.array_equal(lg.cpu().numpy().view(np.uint32), ref["logits"].view(np.uint32))
+    k, v = kv.read()
+    assert np.array_equal(k, om.kc[:, :, :18]) and np.array_equal(v, om.vc[:, :, :18])
