@@ -90,6 +90,10 @@ _SIGS = [
     ("adp_debug_force_experts", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     ("adp_debug_read_experts", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     ("adp_debug_trace_residual", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    ("adp_debug_timeline", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    ("adp_debug_timeline_shape", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32),
+                                                ctypes.POINTER(ctypes.c_int32)]),
+    ("adp_debug_set_l2_lookahead", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
     ("adp_debug_set_wait_limit", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64]),
     ("adp_debug_skip_barrier_arrival", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]),
 ]
@@ -251,6 +255,21 @@ def adp_debug_read_experts(model, n_layers: int, top_k: int) -> np.ndarray:
 
 def adp_debug_trace_residual(model, dev_buf):
     _check(load_library().adp_debug_trace_residual(model, _ptr(dev_buf)), "adp_debug_trace_residual")
+
+
+def adp_debug_timeline(model, dev_buf):
+    _check(load_library().adp_debug_timeline(model, _ptr(dev_buf)), "adp_debug_timeline")
+
+
+def adp_debug_timeline_shape(model):
+    c, p = ctypes.c_int32(), ctypes.c_int32()
+    _check(load_library().adp_debug_timeline_shape(model, ctypes.byref(c), ctypes.byref(p)),
+           "adp_debug_timeline_shape")
+    return c.value, p.value
+
+
+def adp_debug_set_l2_lookahead(model, nbytes: int):
+    _check(load_library().adp_debug_set_l2_lookahead(model, int(nbytes)), "adp_debug_set_l2_lookahead")
 
 
 def adp_debug_set_wait_limit(model, ns: int):

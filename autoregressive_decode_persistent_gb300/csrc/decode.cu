@@ -42,6 +42,13 @@ struct Ctl {
   int32_t flag;
   int32_t sel[kMaxTopK];
   float gate[kMaxTopK];
+  float stage[1024];  // router logits or sampling block sums, loaded in one batch
+  uint64_t att_bar[kAttnSlots];  // TMA completion of each attention slot's K/V block
+  uint64_t vec_bar;              // TMA completion of a prologue's activation vector
+  int32_t n_done;                // KV groups whose last attention block finished in this CTA
+  int32_t done[64];
+  float rope_cs[128], rope_sn[128];  // RoPE row of this step's position (QKV epilogue)
+  float xres[64];                    // residual rows this CTA updates (Wo / down epilogues)
 };
 
 struct Step {
@@ -56,6 +63,11 @@ __device__ __forceinline__ void set_error(const Params& p, Ctl* ctl, int32_t cod
 
 __device__ __forceinline__ bool aborted(Ctl* ctl) { return *(volatile int32_t*)&ctl->abort != 0; }
 
+// Timeline stamp k of phase ph for this CTA (debug hook; one thread writes each slot).
+__device__ __forceinline__ void stamp(const Params& p, uint32_t c, int ph, int k) {
+  if (p.timeline) p.timeline[((size_t)c * p.n_phases + ph) * 8 + k] = globaltimer();
+}
+
 // Per-CTA share of a phase: units [u0, u0 + n).
 __device__ __forceinline__ void cta_units(const PhaseDesc& P, uint32_t c, uint32_t G, int32_t& u0, int32_t& n) {
   const long long a = (long long)c * P.n_units / G, b = (long long)(c + 1) * P.n_units / G;
@@ -65,18 +77,52 @@ __device__ __forceinline__ void cta_units(const PhaseDesc& P, uint32_t c, uint32
 
 // ---------------------------------------------------------------- producer (TMA) warp
 
+constexpr uint32_t kL2Chunk = 32 * 1024;
+
+// Cursor over this CTA's weight stream for L2 prefetch.  Positions count bytes of the dense
+// phases' shares (each contiguous in the image) in consumption order.  The cursor runs up to
+// p.l2_lookahead bytes beyond the TMA issue position and stops at an expert phase until routing
+// has chosen the experts.
+struct L2Cursor {
+  int ph;
+  uint64_t off;  // within the current phase's share
+  uint64_t pos;  // stream position of the cursor
+};
+
+__device__ __forceinline__ void l2_advance(const Params& p, L2Cursor& cur, uint64_t issue_pos, int ph1, uint32_t c,
+                                           uint32_t G) {
+  while (cur.pos < issue_pos + p.l2_lookahead && cur.ph < ph1) {
+    const PhaseDesc& Q = p.phases[cur.ph];
+    if (!Q.has_weights) { ++cur.ph; cur.off = 0; continue; }
+    if (Q.kind == PK_EGU || Q.kind == PK_EDOWN) return;  // experts not chosen yet
+    int32_t u0, n;
+    cta_units(Q, c, G, u0, n);
+    const uint64_t unit_bytes = (uint64_t)Q.unit_rows * Q.K * Q.eb;
+    const uint64_t len = (uint64_t)n * unit_bytes;
+    if (cur.off >= len) { ++cur.ph; cur.off = 0; continue; }
+    const uint64_t left = len - cur.off;
+    const uint32_t chunk = left < kL2Chunk ? (uint32_t)left : kL2Chunk;
+    if (cur.pos >= issue_pos) prefetch_l2(p.image + Q.region + (uint64_t)u0 * unit_bytes + cur.off, chunk);
+    cur.off += chunk;
+    cur.pos += chunk;
+  }
+}
+
 __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, uint32_t G, int ph0, int ph1) {
   const uint64_t pol = policy_evict_first();
   uint32_t t = 0;
   uint32_t sel_uses = 0;
   int sel_layer = -1;
   bool stop = false;
+  L2Cursor cur{ph0, 0, 0};
+  uint64_t issue_pos = 0;  // stream position of the next dense tile
   for (int ph = ph0; ph < ph1 && !stop; ++ph) {
     const PhaseDesc P = p.phases[ph];
     if (!P.has_weights) continue;
     int32_t u0, n;
     cta_units(P, c, G, u0, n);
     const bool expert = P.kind == PK_EGU || P.kind == PK_EDOWN;
+    if (!expert && cur.ph < ph) cur = L2Cursor{ph, 0, issue_pos};  // behind, or waited at the experts
     if (expert && sel_layer != P.layer) {
       // expert weights are known only after routing: wait for this layer's selection
       if (!mbar_wait(&ctl->sel_bar, sel_uses & 1, &ctl->abort, p.wait_ns)) {
@@ -90,6 +136,7 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
     const uint64_t unit_bytes = (uint64_t)P.unit_rows * P.K * P.eb;
     const uint8_t* base = p.image + P.region + (uint64_t)u0 * unit_bytes;
     const int rounds = (n + P.upr - 1) / P.upr;
+    bool first = true;
     for (int r = 0; r < rounds && !stop; ++r) {
       const int m = min(P.upr, n - r * P.upr);
       const uint64_t round_off = (uint64_t)r * P.upr * unit_bytes;
@@ -99,11 +146,17 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
         const uint32_t bytes = (uint32_t)m * P.unit_rows * kck * P.eb;
         const uint64_t off = round_off + (uint64_t)m * P.unit_rows * ck * P.KC * P.eb;
         const uint32_t slot = t % kSlots, use = t / kSlots;
-        if (t >= kSlots && !mbar_wait(&ctl->empty[slot], (use - 1) & 1, &ctl->abort, p.wait_ns)) {
-          if (!aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
-          stop = true;
-          break;
+        if (t >= kSlots) {
+          if (!mbar_try_wait(&ctl->empty[slot], (use - 1) & 1)) {
+            l2_advance(p, cur, issue_pos, ph1, c, G);  // keep HBM busy while the consumers catch up
+            if (!mbar_wait(&ctl->empty[slot], (use - 1) & 1, &ctl->abort, p.wait_ns)) {
+              if (!aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
+              stop = true;
+              break;
+            }
+          }
         }
+        if (first) { stamp(p, c, ph, 4); first = false; }
         mbar_arrive_expect_tx(&ctl->full[slot], bytes * P.slots);
         uint8_t* dst = ring + (size_t)slot * kSlotBytes;
         for (int s = 0; s < P.slots; ++s) {
@@ -111,9 +164,11 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
           if (expert) src += (uint64_t)(*(volatile int32_t*)&ctl->sel[s]) * P.expert_stride;
           tma_load_1d(dst + (size_t)s * bytes, src, bytes, &ctl->full[slot], pol);
         }
+        if (!expert) issue_pos += bytes;
         ++t;
       }
     }
+    stamp(p, c, ph, 5);
   }
   // No bulk copy may still be writing this CTA's shared memory when it exits.
   int32_t never = 0;
@@ -137,21 +192,63 @@ __device__ __forceinline__ void ldcg_x8(const float* g, float (&x)[8]) {
   x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
-// xn = rmsnorm(src) * gain into xbuf (all consumer warps; ends with consumer_sync).
-// src is the fp32 residual in global memory, or (layer 0) the token's embedding row.
+constexpr int kPrologueRegs = 16;  // d_model <= 16 * 15 * 32 = 7680 (checked at model creation)
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// One TMA bulk copy of an activation vector (written by other CTAs before the last grid
+// barrier) into xbuf; issued by one consumer thread, completed on ctl->vec_bar.
+__device__ __forceinline__ void fetch_vector(Ctl* ctl, float* xbuf, const float* src, int n) {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  mbar_arrive_expect_tx(&ctl->vec_bar, (uint32_t)n * 4u);
+  tma_load_1d(xbuf, src, (uint32_t)n * 4u, &ctl->vec_bar, policy_evict_last());
+}
+
+__device__ __forceinline__ void wait_vector(const Params& p, Ctl* ctl, uint32_t& vec_uses, int lane) {
+  const bool ok = aborted(ctl) || mbar_wait(&ctl->vec_bar, vec_uses & 1, &ctl->abort, p.wait_ns);
+  ++vec_uses;
+  if (!ok && lane == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
+}
+
+// xn = rmsnorm(src) * gain into xbuf (all consumer warps; ends with consumer_sync).  src is the
+// fp32 residual (fetched by TMA) or, for layer 0, the token's embedding row (widened here).
 __device__ void rmsnorm_prologue(const Params& p, Ctl* ctl, float* xbuf, const void* gain, const void* emb_row,
-                                 int cw, int lane) {
+                                 int cw, int lane, uint32_t& vec_uses) {
   const int d = p.d;
+  const int tid = cw * 32 + lane;
+  constexpr int T = kConsumerWarps * 32;
+  if (!emb_row && tid == 0) fetch_vector(ctl, xbuf, p.x, d);
+  uint16_t gr[kPrologueRegs];  // gains kept in their 16-bit storage form
+  float xr[kPrologueRegs];
+#pragma unroll
+  for (int k = 0; k < kPrologueRegs; ++k) {
+    const int i = tid + k * T;
+    gr[k] = 0;
+    xr[k] = 0.0f;
+    if (i < d) {
+      gr[k] = __ldg(reinterpret_cast<const unsigned short*>(gain) + i);
+      if (emb_row) xr[k] = load_elem(emb_row, (size_t)i, p.wdt);
+    }
+  }
+  if (emb_row) {
+#pragma unroll
+    for (int k = 0; k < kPrologueRegs; ++k) {
+      const int i = tid + k * T;
+      if (i < d) xbuf[i] = xr[k];
+    }
+    consumer_sync();
+  } else {
+    wait_vector(p, ctl, vec_uses, lane);
+  }
   if (cw == 0) {
     float acc = 0.0f;
     for (int v = lane; v < d / 8; v += 32) {
       float x8[8];
-      if (emb_row) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x8[e] = load_elem(emb_row, (size_t)v * 8 + e, p.wdt);
-      } else {
-        ldcg_x8(p.x + v * 8, x8);
-      }
+      load_x8(xbuf + v * 8, x8);
       acc = fma8(x8, x8, acc);
     }
     const float ss = warp_fold(acc);
@@ -161,92 +258,119 @@ __device__ void rmsnorm_prologue(const Params& p, Ctl* ctl, float* xbuf, const v
   }
   consumer_sync();
   const float r = ctl->bcast;
-  for (int i = cw * 32 + lane; i < d; i += kConsumerWarps * 32) {
-    const float xi = emb_row ? load_elem(emb_row, (size_t)i, p.wdt) : __ldcg(p.x + i);
-    xbuf[i] = __fmul_rn(__fmul_rn(xi, r), load_elem(gain, (size_t)i, p.wdt));
-  }
-  consumer_sync();
-}
-
-__device__ void copy_prologue(float* xbuf, const float* src, int n, int cw, int lane) {
-  for (int i = cw * 32 + lane; i < n; i += kConsumerWarps * 32) xbuf[i] = __ldcg(src + i);
-  consumer_sync();
-}
-
-// Router softmax + top-k in one lane (ties to the lower index), gates renormalised over the
-// choice; forced experts (test hook) keep the router's probabilities of those experts.
-__device__ void select_experts(const Params& p, Ctl* ctl, int layer) {
-  const int E = p.E, K = p.topk;
-  float M = __ldcg(p.rlog);
-  for (int e = 1; e < E; ++e) {
-    const float r = __ldcg(p.rlog + e);
-    M = r > M ? r : M;
-  }
-  float Z = 0.0f;
-  for (int e = 0; e < E; ++e) Z = __fadd_rn(Z, exp_c(__fsub_rn(__ldcg(p.rlog + e), M)));
-  uint32_t used[32] = {0};  // bit set over up to 1024 experts
-  float Zs = 0.0f;
-  for (int i = 0; i < K; ++i) {
-    int best = -1;
-    float bp = 0.0f;
-    if (p.force_sel) {
-      best = p.force_sel[layer * K + i];
-      bp = __fdiv_rn(exp_c(__fsub_rn(__ldcg(p.rlog + best), M)), Z);
-    } else {
-      for (int e = 0; e < E; ++e) {
-        if (used[e >> 5] & (1u << (e & 31))) continue;
-        const float pe = __fdiv_rn(exp_c(__fsub_rn(__ldcg(p.rlog + e), M)), Z);
-        if (best < 0 || pe > bp) { best = e; bp = pe; }
-      }
-      used[best >> 5] |= 1u << (best & 31);
+#pragma unroll
+  for (int k = 0; k < kPrologueRegs; ++k) {
+    const int i = tid + k * T;
+    if (i < d) {
+      const float g = p.wdt == DT_BF16 ? bf16_bits_to_f32(gr[k]) : __half2float(__ushort_as_half(gr[k]));
+      xbuf[i] = __fmul_rn(__fmul_rn(xbuf[i], r), g);
     }
-    ctl->sel[i] = best;
-    ctl->gate[i] = bp;  // probability for now
-    Zs = __fadd_rn(Zs, bp);
   }
-  for (int i = 0; i < K; ++i) ctl->gate[i] = __fdiv_rn(ctl->gate[i], Zs);
+  consumer_sync();
+}
+
+// xbuf[0..n) = src[0..n) by one TMA bulk copy.
+__device__ void copy_prologue(const Params& p, Ctl* ctl, float* xbuf, const float* src, int n, int cw, int lane,
+                              uint32_t& vec_uses) {
+  if (cw == 0 && lane == 0) fetch_vector(ctl, xbuf, src, n);
+  wait_vector(p, ctl, vec_uses, lane);
+  consumer_sync();
+}
+
+// The residual rows this CTA's units update (rows_per_unit rows each), staged in shared memory
+// so that the epilogue does not wait for a load.
+__device__ void stage_residual(const Params& p, Ctl* ctl, const PhaseDesc& P, uint32_t c, uint32_t G,
+                               int rows_per_unit, int cw, int lane) {
+  int32_t u0, n;
+  cta_units(P, c, G, u0, n);
+  const int tid = cw * 32 + lane;
+  if (tid < n * rows_per_unit) ctl->xres[tid] = __ldcg(p.x + (size_t)u0 * rows_per_unit + tid);
+}
+
+// Router softmax + top-k (ties to the lower index), gates renormalised over the choice; forced
+// experts (test hook) keep the router's probabilities of those experts.  Called by a whole warp:
+// the logits are staged in shared memory in one batch, lane 0 does the sequential part.
+__device__ void select_experts(const Params& p, Ctl* ctl, int layer, int lane) {
+  const int E = p.E, K = p.topk;
+  for (int e = lane; e < E; e += 32) ctl->stage[e] = __ldcg(p.rlog + e);
+  __syncwarp();
+  if (lane == 0) {
+    const float* r = ctl->stage;
+    float M = r[0];
+    for (int e = 1; e < E; ++e) M = r[e] > M ? r[e] : M;
+    float Z = 0.0f;
+    for (int e = 0; e < E; ++e) Z = __fadd_rn(Z, exp_c(__fsub_rn(r[e], M)));
+    uint32_t used[32] = {0};  // bit set over up to 1024 experts
+    float Zs = 0.0f;
+    for (int i = 0; i < K; ++i) {
+      int best = -1;
+      float bp = 0.0f;
+      if (p.force_sel) {
+        best = p.force_sel[layer * K + i];
+        bp = __fdiv_rn(exp_c(__fsub_rn(r[best], M)), Z);
+      } else {
+        for (int e = 0; e < E; ++e) {
+          if (used[e >> 5] & (1u << (e & 31))) continue;
+          const float pe = __fdiv_rn(exp_c(__fsub_rn(r[e], M)), Z);
+          if (best < 0 || pe > bp) { best = e; bp = pe; }
+        }
+        used[best >> 5] |= 1u << (best & 31);
+      }
+      ctl->sel[i] = best;
+      ctl->gate[i] = bp;  // probability for now
+      Zs = __fadd_rn(Zs, bp);
+    }
+    for (int i = 0; i < K; ++i) ctl->gate[i] = __fdiv_rn(ctl->gate[i], Zs);
+  }
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------- GEMV phases
 
 template <int ROWS, int SLOTS, int WDT, bool XPERSLOT>
-__device__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, const PhaseDesc& P,
-                           const Step& st, uint32_t c, uint32_t G, int cw, int lane, uint32_t& t) {
+__device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, const PhaseDesc& Pd,
+                                        const Step& st, uint32_t c, uint32_t G, int cw, int lane, uint32_t& t_io) {
+  // every field the loops use lives in registers (the descriptors are in local memory, and each
+  // mbarrier asm statement would otherwise force them to be reloaded)
+  constexpr int EB = WDT == DT_E4M3 ? 1 : 2;
+  const int kind = Pd.kind, L = Pd.layer, K = Pd.K, KC = Pd.KC, n_chunks = Pd.n_chunks, upr = Pd.upr;
+  const int pos = st.pos;
+  const uint64_t wait_ns = p.wait_ns;
+  uint32_t t = t_io;
   int32_t u0, n;
-  cta_units(P, c, G, u0, n);
-  const int L = P.layer;
+  cta_units(Pd, c, G, u0, n);
   unsigned long long best = 0ull;  // LM: packed running maximum of this warp
-  const int rounds = n > 0 ? (n + P.upr - 1) / P.upr : 0;
+  const int rounds = n > 0 ? (n + upr - 1) / upr : 0;
   for (int r = 0; r < rounds; ++r) {
-    const int m = min(P.upr, n - r * P.upr);
+    const int m = min(upr, n - r * upr);
     const bool active = cw < m;
-    const int unit = u0 + r * P.upr + cw;
+    const int unit = u0 + r * upr + cw;
     float acc[SLOTS * ROWS];
 #pragma unroll
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = 0.0f;
-    for (int ck = 0; ck < P.n_chunks; ++ck) {
+    for (int ck = 0; ck < n_chunks; ++ck) {
       const uint32_t slot = t % kSlots, use = t / kSlots;
-      bool ok = aborted(ctl) || mbar_wait(&ctl->full[slot], use & 1, &ctl->abort, p.wait_ns);
+      bool ok = aborted(ctl) || mbar_wait(&ctl->full[slot], use & 1, &ctl->abort, wait_ns);
       if (!ok) {
         if (lane == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
         __syncwarp();
       }
       if (active && !aborted(ctl)) {
-        const int kck = min(P.KC, P.K - ck * P.KC);
+        const int kck = min(KC, K - ck * KC);
         const int nvec = kck >> 3;
-        const uint32_t slot_bytes = (uint32_t)m * ROWS * kck * P.eb;
+        const uint32_t slot_bytes = (uint32_t)m * ROWS * kck * EB;
         const uint8_t* tile = ring + (size_t)slot * kSlotBytes;
-        const int xoff = ck * P.KC;
+        const int xoff = ck * KC;
         for (int v = lane; v < nvec; v += 32) {
           float x8[8];
           if (!XPERSLOT) load_x8(xbuf + xoff + v * 8, x8);
 #pragma unroll
           for (int s = 0; s < SLOTS; ++s) {
-            if (XPERSLOT) load_x8(xbuf + s * P.K + xoff + v * 8, x8);
+            if (XPERSLOT) load_x8(xbuf + s * K + xoff + v * 8, x8);
 #pragma unroll
             for (int j = 0; j < ROWS; ++j) {
               float w8[8];
-              load8<WDT>(tile + (size_t)s * slot_bytes + ((size_t)(cw * ROWS + j) * kck + (size_t)v * 8) * P.eb, w8);
+              load8<WDT>(tile + (size_t)s * slot_bytes + ((size_t)(cw * ROWS + j) * kck + (size_t)v * 8) * EB, w8);
               acc[s * ROWS + j] = fma8(w8, x8, acc[s * ROWS + j]);
             }
           }
@@ -260,7 +384,7 @@ __device__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf
 #pragma unroll
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = warp_fold(acc[i]);
     // ---- epilogues
-    if (P.kind == PK_QKV) {
+    if (kind == PK_QKV) {
       if (lane == 0) {
         const int half = p.hd / 2;
         const int nq = p.hq * half, nk = p.hkv * half;
@@ -269,44 +393,44 @@ __device__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf
           const bool isq = unit < nq;
           const int uu = isq ? unit : unit - nq;
           const int head = uu / half, i = uu % half;
-          const float cs = __ldg(p.rope_cos + (size_t)st.pos * half + i);
-          const float sn = __ldg(p.rope_sin + (size_t)st.pos * half + i);
+          const float cs = ctl->rope_cs[i];
+          const float sn = ctl->rope_sn[i];
           const float a2 = fmaf(a, cs, -__fmul_rn(b, sn));
           const float b2 = fmaf(b, cs, __fmul_rn(a, sn));
           if (isq) {
             __stcg(p.q + head * p.hd + i, a2);
             __stcg(p.q + head * p.hd + i + half, b2);
           } else {
-            const size_t row = (((size_t)L * p.hkv + head) * p.max_ctx + st.pos) * p.hd;
+            const size_t row = (((size_t)L * p.hkv + head) * p.max_ctx + pos) * p.hd;
             p.kc[row + i] = round_kv(a2, p.kvdt);
             p.kc[row + i + half] = round_kv(b2, p.kvdt);
           }
         } else {
           const int uu = unit - nq - nk;
           const int head = uu / half, i = uu % half;
-          const size_t row = (((size_t)L * p.hkv + head) * p.max_ctx + st.pos) * p.hd;
+          const size_t row = (((size_t)L * p.hkv + head) * p.max_ctx + pos) * p.hd;
           p.vc[row + i] = round_kv(a, p.kvdt);
           p.vc[row + i + half] = round_kv(b, p.kvdt);
         }
       }
-    } else if (P.kind == PK_WO || P.kind == PK_DOWN) {
+    } else if (kind == PK_WO || kind == PK_DOWN) {
       if (lane < ROWS) {
         const int row = unit * ROWS + lane;
         float y = acc[0];
 #pragma unroll
         for (int j = 1; j < ROWS; ++j) if (lane == j) y = acc[j];
-        __stcg(p.x + row, __fadd_rn(__ldcg(p.x + row), y));
+        __stcg(p.x + row, __fadd_rn(ctl->xres[row - u0 * ROWS], y));
       }
-    } else if (P.kind == PK_GU) {
+    } else if (kind == PK_GU) {
       if (lane == 0) __stcg(p.h + unit, silu_mul(acc[0], acc[1]));
-    } else if (P.kind == PK_ROUTER) {
+    } else if (kind == PK_ROUTER) {
       if (lane < ROWS) {
         float y = acc[0];
 #pragma unroll
         for (int j = 1; j < ROWS; ++j) if (lane == j) y = acc[j];
         __stcg(p.rlog + unit * ROWS + lane, y);
       }
-    } else if (P.kind == PK_EGU) {
+    } else if (kind == PK_EGU) {
       if (lane < p.topk) {
         float g = acc[0], uval = acc[1];
 #pragma unroll
@@ -317,7 +441,7 @@ __device__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf
         const float su = __ldg(p.e_up_scale[L] + (size_t)e * p.fexp + unit);
         __stcg(p.h + lane * p.fexp + unit, silu_mul(__fmul_rn(sg, g), __fmul_rn(su, uval)));
       }
-    } else if (P.kind == PK_EDOWN) {
+    } else if (kind == PK_EDOWN) {
       if (lane == 0) {
         float ax = 0.0f;
 #pragma unroll
@@ -328,9 +452,9 @@ __device__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf
             ax = fmaf(ctl->gate[s], y, ax);
           }
         }
-        __stcg(p.x + unit, __fadd_rn(__ldcg(p.x + unit), ax));
+        __stcg(p.x + unit, __fadd_rn(ctl->xres[unit - u0], ax));
       }
-    } else if (P.kind == PK_LM) {
+    } else if (kind == PK_LM) {
       if (lane == 0) {
 #pragma unroll
         for (int j = 0; j < ROWS; ++j) {
@@ -342,7 +466,7 @@ __device__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf
       }
     }
   }
-  if (P.kind == PK_LM) {
+  if (kind == PK_LM) {
     if (lane == 0) ctl->red_k[cw] = best;
     consumer_sync();
     if (cw == 0 && lane == 0) {
@@ -359,6 +483,7 @@ __device__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf
     }
     consumer_sync();
   }
+  t_io = t;
 }
 
 // ---------------------------------------------------------------- finalisation
@@ -375,116 +500,255 @@ __device__ void finalize_token(const Params& p, const Step& st, int32_t token) {
 
 // ---------------------------------------------------------------- attention phase
 
-template <int NV>  // 8-element vectors per head (head_dim / 8)
-__device__ void attention_phase(const Params& p, Ctl* ctl, const PhaseDesc& P, const Step& st, uint32_t c,
-                                uint32_t G, int cw, int lane) {
-  constexpr int HD = NV * 8;
-  constexpr int DPL = HD / 32;  // output dims per lane
+// DPL consecutive KV values (one lane's share of a head_dim row) -> fp32.
+template <int DPL>
+__device__ __forceinline__ void load_kv_dims(const uint16_t* src, int kvdt, float (&out)[DPL]) {
+  if constexpr (DPL == 2) {
+    const uint32_t w = __ldcg(reinterpret_cast<const unsigned int*>(src));
+    out[0] = kv_to_f32((uint16_t)(w & 0xFFFFu), kvdt);
+    out[1] = kv_to_f32((uint16_t)(w >> 16), kvdt);
+  } else if constexpr (DPL == 4) {
+    const uint2 w = __ldcg(reinterpret_cast<const uint2*>(src));
+    out[0] = kv_to_f32((uint16_t)(w.x & 0xFFFFu), kvdt);
+    out[1] = kv_to_f32((uint16_t)(w.x >> 16), kvdt);
+    out[2] = kv_to_f32((uint16_t)(w.y & 0xFFFFu), kvdt);
+    out[3] = kv_to_f32((uint16_t)(w.y >> 16), kvdt);
+  } else {
+    const uint4 w = __ldcg(reinterpret_cast<const uint4*>(src));
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      out[2 * i] = kv_to_f32((uint16_t)(u[i] & 0xFFFFu), kvdt);
+      out[2 * i + 1] = kv_to_f32((uint16_t)(u[i] >> 16), kvdt);
+    }
+  }
+}
+
+// Heads [h0, h1) read KV head g: floor(h * hkv / hq) == g.
+__device__ __forceinline__ void group_heads(int g, int hq, int hkv, int& h0, int& h1) {
+  h0 = (g * hq + hkv - 1) / hkv;
+  h1 = ((g + 1) * hq + hkv - 1) / hkv;
+}
+
+// Attention over the KV cache, split along the sequence.  Item = (KV group g, block b of 32
+// positions).  A CTA runs p.att_slots items at a time; slot s uses warps [s*gmax, (s+1)*gmax)
+// (gmax = largest group), one warp per query head of the group, sharing the block's K and V
+// rows that the slot's first warp fetches into the slot's staging area with two TMA bulk
+// copies.  Each warp produces its head's block partial (m_b, l_b, o_b) of the contract.  The
+// CTA that finishes a group's last block merges the group's blocks with all consumer warps.
+template <int HD>
+__device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* xbuf, const PhaseDesc& P,
+                                             const Step& st, uint32_t c, uint32_t G, int cw, int lane,
+                                             uint32_t& att_uses_io) {
+  constexpr int NV = HD / 8;         // 8-element vectors per K row (partial sums of the contract dot)
+  constexpr int PPI = 32 / NV;       // positions per score pass (NV lanes per position)
+  constexpr int NPASS = kAttnBlock / PPI;
+  constexpr int DPL = HD / 32;       // output dims per lane in the PV pass
+  // parameters in registers (see gemv_phase)
   const int L = P.layer;
   const int ctx = st.pos + 1;
+  const int kvdt = p.kvdt, nbmax = p.nbmax, max_ctx = p.max_ctx;
+  const int slots = p.att_slots, gmax = p.att_gmax, slot_bytes = p.att_slot_bytes;
+  const float scale = p.attn_scale;
+  const uint64_t wait_ns = p.wait_ns;
+  const uint16_t* __restrict__ kc = p.kc;
+  const uint16_t* __restrict__ vc = p.vc;
+  const float* __restrict__ qg = p.q;
+  float* part_m = p.part_m;
+  float* part_l = p.part_l;
+  float* part_o = p.part_o;
+  uint32_t* head_ctr = p.head_ctr;
+  float* attn = p.attn;
+  uint32_t att_uses = att_uses_io;
   const int nb = (ctx + kAttnBlock - 1) / kAttnBlock;
-  const int items = p.hq * nb;
-  const int stride = (int)G * kConsumerWarps;
-  for (int it = cw * (int)G + (int)c; it < items; it += stride) {
-    if (aborted(ctl)) break;
-    const int h = it % p.hq, b = it / p.hq;
-    const int g = (int)(((long long)h * p.hkv) / p.hq);
-    const size_t cache0 = ((size_t)L * p.hkv + g) * p.max_ctx * HD;
-    const int j0 = b * kAttnBlock;
-    const int nvalid = min(kAttnBlock, ctx - j0);
-    const float* qh = p.q + h * HD;
-    // scores: lane <-> position j0 + lane; contract dot over head_dim
-    float s = __int_as_float(0xFF800000);  // -inf
-    if (lane < nvalid) {
-      float pv[32];
-      const uint16_t* krow = p.kc + cache0 + (size_t)(j0 + lane) * HD;
+  const int hq = p.hq, hkv = p.hkv;
+  const int items = hkv * nb;
+  const int tid = cw * 32 + lane;
+  const int slot = cw / gmax, hh = cw % gmax;
+  if (slot < slots && !aborted(ctl)) {
+    uint8_t* stg = reinterpret_cast<uint8_t*>(xbuf) + (size_t)slot * slot_bytes;
+    uint16_t* SK = reinterpret_cast<uint16_t*>(stg);
+    uint16_t* SV = SK + kAttnBlock * HD;
+    float* SS = reinterpret_cast<float*>(SV + kAttnBlock * HD);  // [gmax][32] scores
+    for (int it = (int)c + (int)G * slot; it < items; it += (int)G * slots) {
+      const int g = it % hkv, b = it / hkv;
+      int h0, h1;
+      group_heads(g, hq, hkv, h0, h1);
+      const bool active = hh < h1 - h0;
+      const int h = h0 + hh;
+      const int j0 = b * kAttnBlock;
+      const int nvalid = min(kAttnBlock, ctx - j0);
+      const size_t cache0 = (((size_t)L * hkv + g) * max_ctx + j0) * HD;
+      const uint32_t bytes = (uint32_t)nvalid * HD * 2;
+      if (hh == 0 && lane == 0) {
+        // the newest row was written this step by generic stores of other CTAs
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        mbar_arrive_expect_tx(&ctl->att_bar[slot], 2 * bytes);
+        tma_load_1d(SK, kc + cache0, bytes, &ctl->att_bar[slot], policy_evict_first());
+        tma_load_1d(SV, vc + cache0, bytes, &ctl->att_bar[slot], policy_evict_first());
+      }
+      // this lane's 8 query elements (the same vector index v in every score pass)
+      const int v = lane % NV;
+      float q8[8];
+      if (active) ldcg_x8(qg + (size_t)h * HD + v * 8, q8);
+      const bool ok = mbar_wait(&ctl->att_bar[slot], att_uses & 1, &ctl->abort, wait_ns);
+      ++att_uses;
+      if (!ok && lane == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
+      if (cw == 0 && lane == 0 && it == (int)c) stamp(p, c, P.index, 4);
+      if (active && ok) {
+        // scores: NV lanes per position, lane = contract partial index v, folded like the contract
+        float sc[NPASS];
 #pragma unroll
-      for (int v = 0; v < NV; ++v) {
-        const uint4 kw = __ldcg(reinterpret_cast<const uint4*>(krow) + v);
-        const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w};
-        float k8[8], q8[8];
+        for (int pass = 0; pass < NPASS; ++pass) {
+          const int jj = pass * PPI + lane / NV;
+          const uint4 kw = *reinterpret_cast<const uint4*>(SK + (size_t)jj * HD + v * 8);
+          const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w};
+          float k8[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          k8[2 * i] = kv_to_f32((uint16_t)(kk[i] & 0xFFFFu), p.kvdt);
-          k8[2 * i + 1] = kv_to_f32((uint16_t)(kk[i] >> 16), p.kvdt);
+          for (int t2 = 0; t2 < 4; ++t2) {
+            k8[2 * t2] = kv_to_f32((uint16_t)(kk[t2] & 0xFFFFu), kvdt);
+            k8[2 * t2 + 1] = kv_to_f32((uint16_t)(kk[t2] >> 16), kvdt);
+          }
+          sc[pass] = fma8(k8, q8, 0.0f);
         }
-        ldcg_x8(qh + v * 8, q8);
-        pv[v] = fma8(k8, q8, 0.0f);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+#pragma unroll
+          for (int pass = 0; pass < NPASS; ++pass) {
+            if (off >= NV) sc[pass] = __fadd_rn(sc[pass], 0.0f);  // empty partial slots of the 32-slot tree
+            else sc[pass] = __fadd_rn(sc[pass], __shfl_xor_sync(0xFFFFFFFFu, sc[pass], off));
+          }
+        }
+        float* ss = SS + hh * kAttnBlock;
+#pragma unroll
+        for (int pass = 0; pass < NPASS; ++pass) {
+          const int jj = pass * PPI + lane / NV;
+          if (v == 0) ss[jj] = __fmul_rn(sc[pass], scale);
+        }
+        __syncwarp();
+        // block maximum and weights e_j = exp(s_j - m_b): lane j holds e_j
+        const float sj = lane < nvalid ? ss[lane] : __int_as_float(0xFF800000);
+        float m = sj;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+        const float e = lane < nvalid ? exp_c(__fsub_rn(sj, m)) : 0.0f;
+        // l = sequential sum of e_j; o = sequential fma chain over j
+        float l = 0.0f, o[DPL];
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) o[i] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kAttnBlock; ++j) {
+          const float ej = __shfl_sync(0xFFFFFFFFu, e, j);
+          if (j < nvalid) {
+            const uint16_t* vr = SV + (size_t)j * HD + lane * DPL;
+            l = __fadd_rn(l, ej);
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) o[i] = fmaf(ej, kv_to_f32(vr[i], kvdt), o[i]);
+          }
+        }
+        if (cw == 0 && lane == 0 && it == (int)c) stamp(p, c, P.index, 6);
+        // block partial; o is stored [head][block][dim]: coalesced stores here and loads in the merge
+        if (lane == 0) {
+          __stcg(part_m + (size_t)h * nbmax + b, m);
+          __stcg(part_l + (size_t)h * nbmax + b, l);
+        }
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) __stcg(part_o + ((size_t)h * nbmax + b) * HD + lane * DPL + i, o[i]);
+        __syncwarp();
+        if (lane == 0) {
+          // release: this warp's partials before the count; acquire: the merger sees every partial
+          uint32_t old;
+          asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(head_ctr + g) : "memory");
+          if (old == (uint32_t)((h1 - h0) * nb - 1)) {
+            const int k = atomicAdd(&ctl->n_done, 1);
+            ctl->done[k] = g;
+          }
+        }
+        if (cw == 0 && lane == 0 && it == (int)c) stamp(p, c, P.index, 5);
       }
-#pragma unroll
-      for (int v = NV; v < 32; ++v) pv[v] = 0.0f;
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1)
-#pragma unroll
-        for (int i = 0; i < off; ++i) pv[i] = __fadd_rn(pv[i], pv[i + off]);
-      s = __fmul_rn(pv[0], p.attn_scale);
+      // the slot's staging area is reused by its next item only after every warp of the slot is done
+      asm volatile("bar.sync %0, %1;" ::"r"(2 + slot), "r"(gmax * 32) : "memory");
     }
-    float mb = s;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, off));
-    const float e = lane < nvalid ? exp_c(__fsub_rn(s, mb)) : 0.0f;
-    float l = 0.0f;
-    float o[DPL];
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) o[i] = 0.0f;
-    const uint16_t* vblk = p.vc + cache0 + (size_t)j0 * HD + lane * DPL;
-    for (int j = 0; j < nvalid; ++j) {
-      const float ej = __shfl_sync(0xFFFFFFFFu, e, j);
-      l = __fadd_rn(l, ej);
-      const uint16_t* vr = vblk + (size_t)j * HD;
-      float vv[DPL];
-      if constexpr (DPL == 4) {
-        const uint2 w = __ldcg(reinterpret_cast<const uint2*>(vr));
-        vv[0] = kv_to_f32((uint16_t)(w.x & 0xFFFFu), p.kvdt);
-        vv[1] = kv_to_f32((uint16_t)(w.x >> 16), p.kvdt);
-        vv[2] = kv_to_f32((uint16_t)(w.y & 0xFFFFu), p.kvdt);
-        vv[3] = kv_to_f32((uint16_t)(w.y >> 16), p.kvdt);
-      } else {
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) vv[i] = kv_to_f32(__ldcg(vr + i), p.kvdt);
-      }
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) o[i] = fmaf(ej, vv[i], o[i]);
-    }
-    const size_t pi = (size_t)h * p.nbmax + b;
-    if (lane == 0) {
-      __stcg(p.part_m + pi, mb);
-      __stcg(p.part_l + pi, l);
-    }
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) __stcg(p.part_o + pi * HD + lane * DPL + i, o[i]);
-    __threadfence();
-    __syncwarp();
-    uint32_t last = 0;
-    if (lane == 0) last = atomicAdd(p.head_ctr + h, 1u) == (uint32_t)(nb - 1) ? 1u : 0u;
-    last = __shfl_sync(0xFFFFFFFFu, last, 0);
-    if (!last) continue;
-    // this warp completed head h: merge its nb blocks in ascending order
-    __threadfence();
-    float M = __int_as_float(0xFF800000);
-    for (int bb = lane; bb < nb; bb += 32) M = fmaxf(M, __ldcg(p.part_m + (size_t)h * p.nbmax + bb));
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
-    float Lsum = 0.0f;
-    float O[DPL];
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) O[i] = 0.0f;
-    for (int bb = 0; bb < nb; ++bb) {
-      const size_t q = (size_t)h * p.nbmax + bb;
-      const float w = exp_c(__fsub_rn(__ldcg(p.part_m + q), M));
-      Lsum = fmaf(w, __ldcg(p.part_l + q), Lsum);
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) O[i] = fmaf(w, __ldcg(p.part_o + q * HD + lane * DPL + i), O[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) __stcg(p.attn + h * HD + lane * DPL + i, __fdiv_rn(O[i], Lsum));
-    if (lane == 0) p.head_ctr[h] = 0u;
   }
+  consumer_sync();
+  if (tid == 0) stamp(p, c, P.index, 7);
+  // merge the groups completed here: all consumer warps, in ascending block order
+  const int nd = *(volatile int32_t*)&ctl->n_done;
+  for (int k = 0; k < nd; ++k) {
+    const int g = ctl->done[k];
+    int h0, h1;
+    group_heads(g, hq, hkv, h0, h1);
+    const int gh = h1 - h0;
+    float* Wm = xbuf;                         // [gh][nbmax] block maxima, then weights w_b
+    float* Wl = xbuf + kMaxGroup * nbmax;     // [gh][nbmax] block sums
+    constexpr int T = kConsumerWarps * 32;
+    constexpr int kPre = 32;                  // blocks of each output prefetched before the syncs
+    const int n_out = gh * HD;
+    float pre[2][kPre];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int oi = tid + r * T;
+      if (oi < n_out) {
+        const float* src = part_o + (size_t)(h0 + oi / HD) * nbmax * HD + oi % HD;
+#pragma unroll
+        for (int t2 = 0; t2 < kPre; ++t2) pre[r][t2] = t2 < nb ? __ldcg(src + (size_t)t2 * HD) : 0.0f;
+      }
+    }
+    for (int i = tid; i < gh * nb; i += T) {
+      const int hx = i / nb, bb = i % nb;
+      Wm[hx * nbmax + bb] = __ldcg(part_m + (size_t)(h0 + hx) * nbmax + bb);
+      Wl[hx * nbmax + bb] = __ldcg(part_l + (size_t)(h0 + hx) * nbmax + bb);
+    }
+    consumer_sync();
+    if (cw < gh) {  // one warp per head: M = max_b m_b, then w_b = exp(m_b - M)
+      float M = __int_as_float(0xFF800000);
+      for (int bb = lane; bb < nb; bb += 32) M = fmaxf(M, Wm[cw * nbmax + bb]);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+      for (int bb = lane; bb < nb; bb += 32) Wm[cw * nbmax + bb] = exp_c(__fsub_rn(Wm[cw * nbmax + bb], M));
+    }
+    consumer_sync();
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int oi = tid + r * T;
+      if (oi < n_out) {
+        const int hx = oi / HD, dd = oi % HD;
+        const float* w = Wm + hx * nbmax;
+        const float* lsum = Wl + hx * nbmax;
+        const float* src = part_o + (size_t)(h0 + hx) * nbmax * HD + dd;
+        float Ls = 0.0f, O = 0.0f;
+#pragma unroll
+        for (int t2 = 0; t2 < kPre; ++t2) {
+          if (t2 < nb) {
+            Ls = fmaf(w[t2], lsum[t2], Ls);
+            O = fmaf(w[t2], pre[r][t2], O);
+          }
+        }
+        for (int b0 = kPre; b0 < nb; b0 += kPre) {
+          float ob[kPre];
+#pragma unroll
+          for (int t2 = 0; t2 < kPre; ++t2) ob[t2] = b0 + t2 < nb ? __ldcg(src + (size_t)(b0 + t2) * HD) : 0.0f;
+#pragma unroll
+          for (int t2 = 0; t2 < kPre; ++t2) {
+            if (b0 + t2 < nb) {
+              Ls = fmaf(w[b0 + t2], lsum[b0 + t2], Ls);
+              O = fmaf(w[b0 + t2], ob[t2], O);
+            }
+          }
+        }
+        __stcg(attn + (size_t)(h0 + hx) * HD + dd, __fdiv_rn(O, Ls));
+      }
+    }
+    consumer_sync();
+    if (tid == 0) head_ctr[g] = 0u;
+  }
+  if (tid == 0) ctl->n_done = 0;
+  att_uses_io = att_uses;
 }
 
 // ---------------------------------------------------------------- sampling phase
 
-__device__ void sample_phase(const Params& p, Ctl* ctl, const Step& st, uint32_t c, uint32_t G, int cw, int lane) {
+__device__ __noinline__ void sample_phase(const Params& p, Ctl* ctl, const Step& st, uint32_t c, uint32_t G, int cw, int lane) {
   const unsigned long long key = __ldcg(p.argkey);
   const float M = order_float((uint32_t)(key >> 32));
   const float T = st.temperature;
@@ -504,8 +768,8 @@ __device__ void sample_phase(const Params& p, Ctl* ctl, const Step& st, uint32_t
         acc = fmaf(ev, 1.0f, acc);
       }
     }
-    const float S = warp_fold(acc);
-    if (lane == 0) __stcg(p.sblock + it, S);
+    const float Sb = warp_fold(acc);
+    if (lane == 0) __stcg(p.sblock + it, Sb);
     __threadfence();
     __syncwarp();
     uint32_t last = 0;
@@ -513,14 +777,17 @@ __device__ void sample_phase(const Params& p, Ctl* ctl, const Step& st, uint32_t
     last = __shfl_sync(0xFFFFFFFFu, last, 0);
     if (!last) continue;
     __threadfence();
-    // inverse CDF over the block sums, then within the chosen block
+    // inverse CDF over the block sums (staged in shared memory), then within the chosen block
+    float* S = ctl->stage;
+    for (int b = lane; b < nblk; b += 32) S[b] = __ldcg(p.sblock + b);
+    __syncwarp();
     float Z = 0.0f;
-    for (int b = 0; b < nblk; ++b) Z = __fadd_rn(Z, __ldcg(p.sblock + b));
+    for (int b = 0; b < nblk; ++b) Z = __fadd_rn(Z, S[b]);
     const float tau = __fmul_rn(st.u, Z);
     float P = 0.0f;
     int bstar = -1;
     for (int b = 0; b < nblk; ++b) {
-      const float Pn = __fadd_rn(P, __ldcg(p.sblock + b));
+      const float Pn = __fadd_rn(P, S[b]);
       if (Pn > tau) { bstar = b; break; }
       P = Pn;
     }
@@ -529,7 +796,7 @@ __device__ void sample_phase(const Params& p, Ctl* ctl, const Step& st, uint32_t
       from_end = true;
       bstar = 0;
       for (int b = nblk - 1; b >= 0; --b)
-        if (__ldcg(p.sblock + b) > 0.0f) { bstar = b; break; }
+        if (S[b] > 0.0f) { bstar = b; break; }
     }
     const int b0 = bstar * kVocabBlock;
     const int nb2 = min(kVocabBlock, V - b0);
@@ -612,10 +879,12 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
   uint32_t t = 0;
   int bidx = 0;
   int sel_layer = -1;
+  uint32_t att_uses = 0, vec_uses = 0;
   for (int ph = ph0; ph < ph1; ++ph) {
     const PhaseDesc P = p.phases[ph];
     const int L = P.layer;
     const bool ab = aborted(ctl);
+    if (cw == 0 && lane == 0) stamp(p, c, ph, 0);
     // ---- prologue: the GEMV input vector into shared memory
     switch (P.kind) {
       case PK_QKV: {
@@ -630,47 +899,64 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
           for (int i = cw * 32 + lane; i < p.d; i += kConsumerWarps * 32)
             p.trace[(size_t)L * p.d + i] = emb ? load_elem(emb, (size_t)i, p.wdt) : __ldcg(p.x + i);
         }
-        rmsnorm_prologue(p, ctl, xbuf, p.attn_norm[L], emb, cw, lane);
+        {  // the RoPE row of this position, for the epilogue (overlaps the prologue's round trip)
+          const int half = p.hd / 2, tid = cw * 32 + lane;
+          if (tid < half) {
+            ctl->rope_cs[tid] = __ldg(p.rope_cos + (size_t)st.pos * half + tid);
+            ctl->rope_sn[tid] = __ldg(p.rope_sin + (size_t)st.pos * half + tid);
+          }
+        }
+        rmsnorm_prologue(p, ctl, xbuf, p.attn_norm[L], emb, cw, lane, vec_uses);
         break;
       }
-      case PK_WO: copy_prologue(xbuf, p.attn, p.hq * p.hd, cw, lane); break;
-      case PK_DOWN: copy_prologue(xbuf, p.h, p.ff, cw, lane); break;
+      case PK_WO:
+        stage_residual(p, ctl, P, c, G, 2, cw, lane);
+        copy_prologue(p, ctl, xbuf, p.attn, p.hq * p.hd, cw, lane, vec_uses);
+        break;
+      case PK_DOWN:
+        stage_residual(p, ctl, P, c, G, 2, cw, lane);
+        copy_prologue(p, ctl, xbuf, p.h, p.ff, cw, lane, vec_uses);
+        break;
       case PK_EDOWN:
         if (sel_layer != L) {
-          if (cw == 0 && lane == 0) {
-            select_experts(p, ctl, L);
-            mbar_arrive(&ctl->sel_bar);
+          if (cw == 0) {
+            select_experts(p, ctl, L, lane);
+            if (lane == 0) mbar_arrive(&ctl->sel_bar);
           }
           sel_layer = L;
         }
-        copy_prologue(xbuf, p.h, p.topk * p.fexp, cw, lane);
+        stage_residual(p, ctl, P, c, G, 1, cw, lane);
+        copy_prologue(p, ctl, xbuf, p.h, p.topk * p.fexp, cw, lane, vec_uses);
         break;
       case PK_GU:
-      case PK_ROUTER: rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, cw, lane); break;
+      case PK_ROUTER: rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, cw, lane, vec_uses); break;
       case PK_EGU: {
-        if (cw == 0 && lane == 0) {
-          select_experts(p, ctl, L);
-          if (c == 0 && !ab) for (int i = 0; i < p.topk; ++i) p.sel_out[L * p.topk + i] = ctl->sel[i];
-          mbar_arrive(&ctl->sel_bar);  // release the choice to the producer
+        if (cw == 0) {
+          select_experts(p, ctl, L, lane);
+          if (lane == 0) {
+            if (c == 0 && !ab) for (int i = 0; i < p.topk; ++i) p.sel_out[L * p.topk + i] = ctl->sel[i];
+            mbar_arrive(&ctl->sel_bar);  // release the choice to the producer
+          }
         }
         sel_layer = L;
-        rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, cw, lane);
+        rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, cw, lane, vec_uses);
         break;
       }
       case PK_LM: {
         if (p.trace && c == 0 && !ab)
           for (int i = cw * 32 + lane; i < p.d; i += kConsumerWarps * 32)
             p.trace[(size_t)p.L * p.d + i] = __ldcg(p.x + i);
-        rmsnorm_prologue(p, ctl, xbuf, p.final_norm, nullptr, cw, lane);
+        rmsnorm_prologue(p, ctl, xbuf, p.final_norm, nullptr, cw, lane, vec_uses);
         break;
       }
       default: break;
     }
     // ---- body
+    if (cw == 0 && lane == 0) stamp(p, c, ph, 1);
     if (P.kind == PK_ATTN) {
-      if (p.hd == 128) attention_phase<16>(p, ctl, P, st, c, G, cw, lane);
-      else if (p.hd == 64) attention_phase<8>(p, ctl, P, st, c, G, cw, lane);
-      else attention_phase<32>(p, ctl, P, st, c, G, cw, lane);
+      if (p.hd == 128) attention_phase<128>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses);
+      else if (p.hd == 64) attention_phase<64>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses);
+      else attention_phase<256>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses);
     } else if (P.kind == PK_SAMPLE) {
       if (st.temperature > 0.0f) sample_phase(p, ctl, st, c, G, cw, lane);
     } else if (P.kind == PK_EGU || P.kind == PK_EDOWN) {
@@ -698,15 +984,18 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
       *p.lm_ctr = 0u;  // sampling: the maximum stays in argkey for the sampling phase
     }
     // ---- grid barrier between dependent phases
+    if (cw == 0 && lane == 0) stamp(p, c, ph, 2);
     if (use_barrier && ph + 1 < ph1) {
       const bool need = !(P.kind == PK_LM && st.temperature <= 0.0f);
       if (need) grid_barrier(p, ctl, c, G, bidx);
     }
+    if (cw == 0 && lane == 0) stamp(p, c, ph, 3);
   }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_kernel(const Params p, int32_t ph0, int32_t ph1, int32_t use_barrier, int32_t xbuf_floats) {
+    decode_kernel(const __grid_constant__ Params p, int32_t ph0, int32_t ph1, int32_t use_barrier,
+                  int32_t xbuf_floats) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   float* xbuf = reinterpret_cast<float*>(smem + (size_t)kSlots * kSlotBytes);
@@ -719,6 +1008,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->empty[s], kConsumerWarps);
     }
     mbar_init(&ctl->sel_bar, 1);
+    for (int w = 0; w < kAttnSlots; ++w) mbar_init(&ctl->att_bar[w], 1);
+    mbar_init(&ctl->vec_bar, 1);
+    ctl->n_done = 0;
     ctl->abort = *(volatile int32_t*)p.err != 0 ? 1 : 0;
     ctl->flag = 0;
     mbar_fence_init();

@@ -68,6 +68,11 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
       : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (no completion; bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -82,13 +87,13 @@ __device__ __forceinline__ void consumer_sync() {
 // ---------------------------------------------------------------- grid barrier
 
 // Monotonic 64-bit arrival counter shared by all launches of a model: barrier instance k of
-// a step completes when the counter reaches the next multiple of the grid size.  Arrival uses
-// release semantics, the wait acquire; the wait is bounded by limit_ns.  Returns false on
-// timeout.  Called by one thread per CTA, between two consumer_sync()s.
+// a step completes when the counter reaches the next multiple of the grid size.  Arrival is a
+// release RMW (cumulative over the CTA's writes ordered before it by the preceding CTA barrier),
+// the wait an acquire load; the wait is bounded by limit_ns.  Returns false on timeout.  Called
+// by one thread per CTA, between two consumer_sync()s.
 __device__ __forceinline__ bool grid_arrive_wait(unsigned long long* ctr, uint32_t G, bool arrive, bool wait,
                                                  uint64_t limit_ns) {
   unsigned long long old = 0;
-  __threadfence();
   if (arrive) {
     asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
   } else {
@@ -103,7 +108,6 @@ __device__ __forceinline__ bool grid_arrive_wait(unsigned long long* ctr, uint32
     if (v >= target) break;
     if ((it & 31) == 31 && globaltimer() - t0 > limit_ns) return false;
   }
-  __threadfence();
   return true;
 }
 

@@ -96,6 +96,7 @@ static int validate(const adp_config* c, const adp_weights* w) {
   if (c->n_kv_heads > c->n_heads) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (c->d_model % 8 || c->vocab % 8 || (c->n_heads * c->head_dim) % 8) return ADP_ERR_UNSUPPORTED_CONFIG;
+  if (c->d_model > 7680 || c->vocab > 1024 * 256) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (c->weight_dtype != ADP_F16 && c->weight_dtype != ADP_BF16) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (c->kv_dtype != ADP_F16 && c->kv_dtype != ADP_BF16) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (!c->tied_embeddings && !w->lm_head) return ADP_ERR_INVALID_ARG;
@@ -126,6 +127,7 @@ static void add_phase(adp_model* m, int kind, int layer, int n_units, int unit_r
   PhaseDesc P{};
   P.kind = kind;
   P.layer = layer;
+  P.index = (int32_t)m->phases.size();
   P.has_weights = weights ? 1 : 0;
   if (weights) {
     P.n_units = n_units;
@@ -134,7 +136,10 @@ static void add_phase(adp_model* m, int kind, int layer, int n_units, int unit_r
     P.K = K;
     P.eb = eb;
     P.wdt = wdt;
-    int upr = kConsumerWarps;
+    // balanced rounds of at most kConsumerWarps units over the largest per-CTA share
+    const int maxu = std::max(1, (n_units + m->G - 1) / m->G);
+    const int nrounds = (maxu + kConsumerWarps - 1) / kConsumerWarps;
+    int upr = (maxu + nrounds - 1) / nrounds;
     while (upr > 1 && (long long)upr * unit_rows * slots * eb * kChunkAlign > kSlotBytes) --upr;
     P.upr = upr;
     int KC = (kSlotBytes / (upr * unit_rows * slots * eb)) / kChunkAlign * kChunkAlign;
@@ -179,16 +184,37 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   cudaDeviceProp prop;
   CK(cudaGetDeviceProperties(&prop, m->device));
   if (!prop.cooperativeLaunch) return ADP_ERR_NOT_CORESIDENT;
+  m->G = prop.multiProcessorCount;  // one persistent CTA per SM
   plan(m);
   const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim, L = c.n_layers;
   const int ffw = c.n_experts ? c.top_k * c.d_expert : c.d_ff;
-  m->xbuf_floats = std::max(std::max(d, hq * hd), ffw);
-  m->smem = (size_t)kSlots * kSlotBytes + (((size_t)m->xbuf_floats * 4 + 127) & ~(size_t)127) + ctl_bytes();
+  // xbuf holds a phase's input vector, the attention warps' K/V staging areas, or the merge's
+  // per-block weights: sized for the largest use that fits beside the ring.
+  const int nbmax_ = (c.max_ctx + kAttnBlock - 1) / kAttnBlock;
+  const size_t ctl_sz = (ctl_bytes() + 127) & ~(size_t)127;
+  const size_t budget = (size_t)prop.sharedMemPerBlockOptin - (size_t)kSlots * kSlotBytes - ctl_sz;
+  int gmax = 0;  // most query heads sharing one KV head (floor(h * hkv / hq) grouping)
+  for (int g = 0; g < c.n_kv_heads; ++g) {
+    const int h0 = (g * hq + c.n_kv_heads - 1) / c.n_kv_heads, h1 = ((g + 1) * hq + c.n_kv_heads - 1) / c.n_kv_heads;
+    gmax = std::max(gmax, h1 - h0);
+  }
+  if (gmax < 1 || gmax > kMaxGroup) return ADP_ERR_UNSUPPORTED_CONFIG;
+  const size_t item = (size_t)2 * kAttnBlock * hd * 2 + (size_t)kMaxGroup * kAttnBlock * 4;  // K, V, scores
+  const int att_slots = (int)std::min<size_t>(std::min(kAttnSlots, kConsumerWarps / gmax), budget / item);
+  if (att_slots < 1) return ADP_ERR_UNSUPPORTED_CONFIG;
+  size_t xbytes = (size_t)std::max(std::max(d, hq * hd), ffw) * 4;
+  xbytes = std::max(xbytes, (size_t)att_slots * item);
+  xbytes = std::max(xbytes, ((size_t)2 * 8 * nbmax_ + 8) * 4);
+  xbytes = (xbytes + 127) & ~(size_t)127;
+  m->xbuf_floats = (int)(xbytes / 4);
+  m->smem = (size_t)kSlots * kSlotBytes + xbytes + ctl_bytes();
   if (m->smem > (size_t)prop.sharedMemPerBlockOptin) return ADP_ERR_UNSUPPORTED_CONFIG;
+  m->p.att_slots = att_slots;
+  m->p.att_gmax = gmax;
+  m->p.att_slot_bytes = (int)item;
   int bps = 0;
   CK(decode_prepare(m->smem, &bps));
   if (bps < 1) return ADP_ERR_NOT_CORESIDENT;
-  m->G = prop.multiProcessorCount;  // one persistent CTA per SM
 
   // weight image
   int rc;
@@ -315,6 +341,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   p.rope_cos = d_cos;
   p.rope_sin = d_sin;
   p.wait_ns = 200000000ull;
+  p.l2_lookahead = 0;
   p.skip_cta = -1;
   p.skip_barrier = -1;
   CK(cudaStreamSynchronize(m->stream));
@@ -682,6 +709,27 @@ extern "C" int adp_debug_read_experts(const adp_model* m, int32_t* host_idx) {
 extern "C" int adp_debug_trace_residual(adp_model* m, float* dev_buf) {
   if (!m) return ADP_ERR_INVALID_ARG;
   m->p.trace = dev_buf;
+  if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
+  return ADP_OK;
+}
+
+extern "C" int adp_debug_timeline(adp_model* m, uint64_t* dev_buf) {
+  if (!m) return ADP_ERR_INVALID_ARG;
+  m->p.timeline = reinterpret_cast<unsigned long long*>(dev_buf);
+  if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
+  return ADP_OK;
+}
+
+extern "C" int adp_debug_timeline_shape(const adp_model* m, int32_t* ctas, int32_t* phases) {
+  if (!m || !ctas || !phases) return ADP_ERR_INVALID_ARG;
+  *ctas = m->G;
+  *phases = (int32_t)m->phases.size();
+  return ADP_OK;
+}
+
+extern "C" int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes) {
+  if (!m) return ADP_ERR_INVALID_ARG;
+  m->p.l2_lookahead = bytes;
   if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
   return ADP_OK;
 }

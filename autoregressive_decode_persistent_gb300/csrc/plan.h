@@ -12,13 +12,15 @@
 
 namespace adp {
 
-constexpr int kConsumerWarps = 16;                  // compute warps per CTA
+constexpr int kConsumerWarps = 15;                  // compute warps per CTA (16 warps in all: <= 128 registers)
 constexpr int kThreads = (kConsumerWarps + 1) * 32; // + one producer (TMA) warp
 constexpr int kSlotBytes = 32768;                   // one ring slot
 constexpr int kSlots = 4;                           // ring depth (128 KB in flight per SM)
 constexpr int kAttnBlock = 32;                      // positions per attention block (contract)
 constexpr int kVocabBlock = 256;                    // vocabulary entries per sampling block (contract)
 constexpr int kMaxTopK = 8;
+constexpr int kAttnSlots = 8;                       // attention items in flight per CTA (max)
+constexpr int kMaxGroup = 8;                        // query heads per KV head (max)
 constexpr int kChunkAlign = 256;                    // K-chunks start at multiples of 32 lanes x 8 elements
 
 enum PhaseKind : int32_t {
@@ -48,6 +50,8 @@ struct PhaseDesc {
   int32_t eb;             // weight element bytes
   int32_t wdt;            // weight DType
   int32_t has_weights;
+  int32_t index;          // position of this phase in the step's phase list
+  int32_t pad_;
   uint64_t region;        // byte offset of the phase's region in the image (expert 0 for expert phases)
   uint64_t expert_stride; // bytes of one expert's region
 };
@@ -80,6 +84,9 @@ struct Params {
   float eps;
   float attn_scale;
   int32_t nbmax;                      // max attention blocks = ceil(max_ctx / 32)
+  int32_t att_slots;                  // attention items a CTA works on at once
+  int32_t att_gmax;                   // warps per slot (largest number of query heads per KV head)
+  int32_t att_slot_bytes;             // shared-memory staging bytes of one slot
   // KV cache [L][hkv][max_ctx][hd]
   uint16_t* kc;
   uint16_t* vc;
@@ -95,7 +102,7 @@ struct Params {
   float* part_m;   // [hq][nbmax]
   float* part_l;   // [hq][nbmax]
   float* part_o;   // [hq][nbmax][hd]
-  uint32_t* head_ctr;          // [hq]
+  uint32_t* head_ctr;          // [hkv] attention blocks finished per KV group
   float* sblock;               // [ceil(V/256)] sampling block sums
   uint32_t* sample_ctr;
   unsigned long long* argkey;  // packed (ordered logit, ~index) maximum
@@ -110,7 +117,9 @@ struct Params {
   const float* u_seq;          // uniform per step or null
   int32_t* out_seq;            // chosen token per step or null
   float* logits;               // [V] logits output
+  unsigned long long* timeline; // [G][n_phases][8] %globaltimer stamps or null
   uint64_t wait_ns;            // limit of every in-kernel wait
+  uint32_t l2_lookahead;       // bytes of weight stream prefetched into L2 beyond the TMA loads
   int32_t skip_cta, skip_barrier;
 };
 

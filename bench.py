@@ -162,6 +162,8 @@ def run_engine(args, rank: int, world: int):
     torch.cuda.set_device(dev)
     build.build()
     cfg = synth.get_config(WORKLOAD)
+    if args.layers:
+        cfg["n_layers"] = args.layers  # profiling only: a shorter model with the same layer shapes
     W = synth.model_weights(cfg)
     prompt = synth.prompt(cfg)
     model = DecodeModel(cfg, W, device=dev)
@@ -232,6 +234,9 @@ def run_engine(args, rank: int, world: int):
     h1 = time.perf_counter()
     e2e = n_e2e / (h1 - h0)
 
+    if args.timeline:
+        write_timeline(args.timeline, model, kv, tok0, P, cfg)
+
     res = {
         "ms": ms, "steps": args.steps, "achieved_gbs": achieved, "per_launch_bytes": per_launch,
         "launch_ms": launch_ms, "peak": peak, "peak_kind": peak_kind, "e2e": e2e, "n_e2e": n_e2e,
@@ -243,6 +248,73 @@ def run_engine(args, rank: int, world: int):
     kv.close()
     model.close()
     return cfg, res
+
+
+def write_timeline(path, model, kv, tok0, P, cfg):
+    """Per-phase breakdown of one decode step from the kernel's %globaltimer stamps."""
+    import numpy as np
+    import torch
+    from autoregressive_decode_persistent_gb300 import adp
+    G, nph = adp.adp_debug_timeline_shape(model.handle)
+    buf = torch.zeros(G * nph * 8, dtype=torch.int64, device=model.device)  # zero = no stamp
+    adp.adp_debug_timeline(model.handle, buf)
+    kv.truncate(P)
+    t = tok0
+    for _ in range(4):
+        t = kv.step(t)
+    adp.adp_debug_timeline(model.handle, None)
+    tl = buf.view(G, nph, 8).cpu().numpy().astype(np.float64)
+    names = {0: "qkv", 1: "attn", 2: "wo", 3: "gate_up", 4: "down", 5: "router", 6: "expert_gate_up",
+             7: "expert_down", 8: "lm_head", 9: "sample"}
+    kinds = [names[k] for k in _phase_kinds(cfg)]
+    origin = tl[:, 0, 0].min()
+    per_kind = {}
+    rows = []
+    for ph in range(nph - 1):  # the sampling phase does not run at temperature 0
+        s = tl[:, ph, :]
+        pro = np.mean(s[:, 1] - s[:, 0]) / 1e3
+        body = np.mean(s[:, 2] - s[:, 1]) / 1e3
+        bar = np.mean(s[:, 3] - s[:, 2]) / 1e3
+        span = (s[:, 3].max() - s[:, 0].min()) / 1e3
+        k = kinds[ph]
+        d = per_kind.setdefault(k, {"prologue_us": 0.0, "body_us": 0.0, "barrier_us": 0.0, "count": 0})
+        d["prologue_us"] += pro
+        d["body_us"] += body
+        d["barrier_us"] += bar
+        d["count"] += 1
+        if k == "attn":
+            w = s[:, 4] > 0
+            if w.any():
+                d.setdefault("tma_us", 0.0)
+                d["tma_us"] += float(np.mean(s[w, 4] - s[w, 1]) / 1e3)
+                d.setdefault("compute_us", 0.0)
+                d["compute_us"] += float(np.mean(s[w, 6] - s[w, 4]) / 1e3)
+                d.setdefault("publish_us", 0.0)
+                d["publish_us"] += float(np.mean(s[w, 5] - s[w, 6]) / 1e3)
+            d.setdefault("merge_us_max", 0.0)
+            d["merge_us_max"] += float(np.max(s[:, 2] - s[:, 7]) / 1e3)
+            d.setdefault("items_end_us_max", 0.0)
+            d["items_end_us_max"] += float(np.max(s[:, 7] - s[:, 1]) / 1e3)
+        rows.append({"phase": ph, "kind": k, "start_us": (s[:, 0].min() - origin) / 1e3, "prologue_us": pro,
+                     "body_us": body, "barrier_us": bar, "span_us": span,
+                     "body_max_us": float(np.max(s[:, 2] - s[:, 1]) / 1e3)})
+    step_us = (tl[:, nph - 2, 3].max() - origin) / 1e3
+    out = {"step_us": step_us, "ctas": G, "phases": nph, "per_kind": per_kind, "per_phase": rows}
+    with open(path, "w") as f:
+        json.dump(out, f, indent=1)
+    print(f"timeline: step {step_us:.1f} us", file=sys.stderr)
+    for k, d in per_kind.items():
+        extra = "  ".join(f"{n} {v:.1f}" for n, v in d.items() if n not in ("prologue_us", "body_us", "barrier_us",
+                                                                                 "count"))
+        print(f"  {k:16s} x{d['count']:3d}  prologue {d['prologue_us']:8.1f}  body {d['body_us']:8.1f}  "
+              f"barrier {d['barrier_us']:8.1f} us  {extra}", file=sys.stderr)
+
+
+def _phase_kinds(cfg):
+    ks = []
+    for _ in range(cfg["n_layers"]):
+        ks += [0, 1, 2] + ([3, 4] if not cfg["n_experts"] else [5, 6, 7])
+    return ks + [8, 9]
 
 
 def emit_engine(args, cfg, res, world):
@@ -282,6 +354,7 @@ def emit_engine(args, cfg, res, world):
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({res['peak_kind']}; read+write copy)",
                      "frac_of_8000": round(res["achieved_gbs"] / 8000.0, 4)},
         "gpu_launches": res["launches"],
+        **({"profiling_variant": f"{cfg['n_layers']} layers (not the workload)"} if args.layers else {}),
         "clocks": res["clocks"],
         "kernel_source": src,
     }
@@ -331,6 +404,9 @@ def main():
     ap.add_argument("--impl", choices=["engine", "reference"], default="engine")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--timeline", default=None, help="write a per-phase breakdown of one step (JSON) here")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: use this many layers of the workload's shape (the line says so)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

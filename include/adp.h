@@ -183,6 +183,16 @@ int adp_debug_read_experts(const adp_model* m, int32_t* host_idx);
 /* Record the residual entering each layer (and the final one) of every step into a DEVICE
  * buffer [n_layers + 1][d_model] fp32 (NULL = off). */
 int adp_debug_trace_residual(adp_model* m, float* dev_buf);
+/* Per-phase timeline of every CTA: DEVICE buffer [ctas][phases][8] of %globaltimer stamps (ns):
+ * 0 phase entry, 1 after the prologue, 2 after the phase body, 3 after the grid barrier (consumer
+ * warp 0), 4 first and 5 last weight tile issued (producer warp).  NULL = off.  Sizes from
+ * adp_debug_timeline_shape. */
+int adp_debug_timeline(adp_model* m, uint64_t* dev_buf);
+int adp_debug_timeline_shape(const adp_model* m, int32_t* ctas, int32_t* phases);
+/* Bytes of each SM's weight stream the producer warp keeps prefetched into L2 beyond its TMA
+ * loads (default 0 = off).  A tuning knob: it lets HBM keep streaming while the compute
+ * warps wait at barriers. */
+int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes);
 /* Wait limit of every in-kernel spin (grid barrier, weight pipeline), nanoseconds (default 2e8). */
 int adp_debug_set_wait_limit(adp_model* m, uint64_t ns);
 /* Test hook: CTA `cta` skips its arrival at grid barrier number `barrier` of the next step
