@@ -93,9 +93,10 @@ _SIGS = [
     ("adp_debug_timeline", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     ("adp_debug_timeline_shape", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32),
                                                 ctypes.POINTER(ctypes.c_int32)]),
+    ("adp_debug_barriers", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     ("adp_debug_set_l2_lookahead", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
     ("adp_debug_set_wait_limit", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64]),
-    ("adp_debug_skip_barrier_arrival", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]),
+    ("adp_debug_skip_publication", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]),
 ]
 
 
@@ -268,6 +269,10 @@ def adp_debug_timeline_shape(model):
     return c.value, p.value
 
 
+def adp_debug_barriers(model, on: bool):
+    _check(load_library().adp_debug_barriers(model, 1 if on else 0), "adp_debug_barriers")
+
+
 def adp_debug_set_l2_lookahead(model, nbytes: int):
     _check(load_library().adp_debug_set_l2_lookahead(model, int(nbytes)), "adp_debug_set_l2_lookahead")
 
@@ -276,6 +281,5 @@ def adp_debug_set_wait_limit(model, ns: int):
     _check(load_library().adp_debug_set_wait_limit(model, int(ns)), "adp_debug_set_wait_limit")
 
 
-def adp_debug_skip_barrier_arrival(model, cta: int, barrier: int):
-    _check(load_library().adp_debug_skip_barrier_arrival(model, int(cta), int(barrier)),
-           "adp_debug_skip_barrier_arrival")
+def adp_debug_skip_publication(model, cta: int, phase: int):
+    _check(load_library().adp_debug_skip_publication(model, int(cta), int(phase)), "adp_debug_skip_publication")

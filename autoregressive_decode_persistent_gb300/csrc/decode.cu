@@ -44,7 +44,6 @@ struct Ctl {
   float gate[kMaxTopK];
   float stage[1024];  // router logits or sampling block sums, loaded in one batch
   uint64_t att_bar[kAttnSlots];  // TMA completion of each attention slot's K/V block
-  uint64_t vec_bar;              // TMA completion of a prologue's activation vector
   int32_t n_done;                // KV groups whose last attention block finished in this CTA
   int32_t done[64];
   float rope_cs[128], rope_sn[128];  // RoPE row of this step's position (QKV epilogue)
@@ -54,6 +53,7 @@ struct Ctl {
 struct Step {
   int32_t pos, token, seq_index;
   float temperature, u;
+  uint32_t ebase;  // epoch of phase ph in this step = ebase + 1 + ph
 };
 
 __device__ __forceinline__ void set_error(const Params& p, Ctl* ctl, int32_t code) {
@@ -137,6 +137,7 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
     const uint8_t* base = p.image + P.region + (uint64_t)u0 * unit_bytes;
     const int rounds = (n + P.upr - 1) / P.upr;
     bool first = true;
+    uint64_t blocked = 0;  // ns spent with the ring full (timeline only)
     for (int r = 0; r < rounds && !stop; ++r) {
       const int m = min(P.upr, n - r * P.upr);
       const uint64_t round_off = (uint64_t)r * P.upr * unit_bytes;
@@ -148,12 +149,14 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
         const uint32_t slot = t % kSlots, use = t / kSlots;
         if (t >= kSlots) {
           if (!mbar_try_wait(&ctl->empty[slot], (use - 1) & 1)) {
+            const uint64_t tb = p.timeline ? globaltimer() : 0;
             l2_advance(p, cur, issue_pos, ph1, c, G);  // keep HBM busy while the consumers catch up
             if (!mbar_wait(&ctl->empty[slot], (use - 1) & 1, &ctl->abort, p.wait_ns)) {
               if (!aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
               stop = true;
               break;
             }
+            if (p.timeline) blocked += globaltimer() - tb;
           }
         }
         if (first) { stamp(p, c, ph, 4); first = false; }
@@ -169,6 +172,7 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
       }
     }
     stamp(p, c, ph, 5);
+    if (p.timeline) p.timeline[((size_t)c * p.n_phases + ph) * 8 + 7] = blocked;
   }
   // No bulk copy may still be writing this CTA's shared memory when it exits.
   int32_t never = 0;
@@ -194,56 +198,65 @@ __device__ __forceinline__ void ldcg_x8(const float* g, float (&x)[8]) {
 
 constexpr int kPrologueRegs = 16;  // d_model <= 16 * 15 * 32 = 7680 (checked at model creation)
 
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
+// Wait until *src carries `epoch` (w holds the word already loaded).  Bounded; on timeout the
+// CTA records a dependency-wait error and stops waiting.
+__device__ __forceinline__ bool ll_wait(const ll_t* src, uint32_t epoch, ll_t& w, const Params& p, Ctl* ctl) {
+  if (ll_epoch(w) == epoch) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 0;; ++it) {
+    w = ll_load(src);
+    if (ll_epoch(w) == epoch) return true;
+    if ((it & 15) == 15) {
+      if (aborted(ctl)) return false;
+      if (globaltimer() - t0 > p.wait_ns) {
+        set_error(p, ctl, DE_BARRIER_TIMEOUT);
+        return false;
+      }
+    }
+  }
 }
 
-// One TMA bulk copy of an activation vector (written by other CTAs before the last grid
-// barrier) into xbuf; issued by one consumer thread, completed on ctl->vec_bar.
-__device__ __forceinline__ void fetch_vector(Ctl* ctl, float* xbuf, const float* src, int n) {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-  mbar_arrive_expect_tx(&ctl->vec_bar, (uint32_t)n * 4u);
-  tma_load_1d(xbuf, src, (uint32_t)n * 4u, &ctl->vec_bar, policy_evict_last());
+// dst[0..n) = the values of src[0..n) once each carries `epoch` (all consumer threads, eight
+// loads in flight per thread; ends with consumer_sync).
+__device__ void ll_fetch(const Params& p, Ctl* ctl, float* dst, const ll_t* src, int n, uint32_t epoch, int tid) {
+  constexpr int B = 8, T = kConsumerWarps * 32;
+  for (int base = tid; base < n; base += B * T) {
+    ll_t w[B];
+#pragma unroll
+    for (int k = 0; k < B; ++k) {
+      const int i = base + k * T;
+      w[k] = i < n ? ll_load(src + i) : 0ull;
+    }
+#pragma unroll
+    for (int k = 0; k < B; ++k) {
+      const int i = base + k * T;
+      if (i < n && ll_wait(src + i, epoch, w[k], p, ctl)) dst[i] = ll_value(w[k]);
+    }
+  }
+  consumer_sync();
 }
 
-__device__ __forceinline__ void wait_vector(const Params& p, Ctl* ctl, uint32_t& vec_uses, int lane) {
-  const bool ok = aborted(ctl) || mbar_wait(&ctl->vec_bar, vec_uses & 1, &ctl->abort, p.wait_ns);
-  ++vec_uses;
-  if (!ok && lane == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
-}
-
-// xn = rmsnorm(src) * gain into xbuf (all consumer warps; ends with consumer_sync).  src is the
-// fp32 residual (fetched by TMA) or, for layer 0, the token's embedding row (widened here).
+// xn = rmsnorm(x) * gain into xbuf (all consumer warps; ends with consumer_sync).  x is the
+// residual as published by phase `x_epoch`, or, for layer 0, the token's embedding row.
 __device__ void rmsnorm_prologue(const Params& p, Ctl* ctl, float* xbuf, const void* gain, const void* emb_row,
-                                 int cw, int lane, uint32_t& vec_uses) {
+                                 uint32_t x_epoch, int trace_layer, uint32_t c, int cw, int lane) {
   const int d = p.d;
   const int tid = cw * 32 + lane;
   constexpr int T = kConsumerWarps * 32;
-  if (!emb_row && tid == 0) fetch_vector(ctl, xbuf, p.x, d);
   uint16_t gr[kPrologueRegs];  // gains kept in their 16-bit storage form
-  float xr[kPrologueRegs];
 #pragma unroll
   for (int k = 0; k < kPrologueRegs; ++k) {
     const int i = tid + k * T;
-    gr[k] = 0;
-    xr[k] = 0.0f;
-    if (i < d) {
-      gr[k] = __ldg(reinterpret_cast<const unsigned short*>(gain) + i);
-      if (emb_row) xr[k] = load_elem(emb_row, (size_t)i, p.wdt);
-    }
+    gr[k] = i < d ? __ldg(reinterpret_cast<const unsigned short*>(gain) + i) : (uint16_t)0;
   }
   if (emb_row) {
-#pragma unroll
-    for (int k = 0; k < kPrologueRegs; ++k) {
-      const int i = tid + k * T;
-      if (i < d) xbuf[i] = xr[k];
-    }
+    for (int i = tid; i < d; i += T) xbuf[i] = load_elem(emb_row, (size_t)i, p.wdt);
     consumer_sync();
   } else {
-    wait_vector(p, ctl, vec_uses, lane);
+    ll_fetch(p, ctl, xbuf, p.x, d, x_epoch, tid);
   }
+  if (p.trace && c == 0 && trace_layer >= 0)
+    for (int i = tid; i < d; i += T) p.trace[(size_t)trace_layer * d + i] = xbuf[i];
   if (cw == 0) {
     float acc = 0.0f;
     for (int v = lane; v < d / 8; v += 32) {
@@ -269,30 +282,29 @@ __device__ void rmsnorm_prologue(const Params& p, Ctl* ctl, float* xbuf, const v
   consumer_sync();
 }
 
-// xbuf[0..n) = src[0..n) by one TMA bulk copy.
-__device__ void copy_prologue(const Params& p, Ctl* ctl, float* xbuf, const float* src, int n, int cw, int lane,
-                              uint32_t& vec_uses) {
-  if (cw == 0 && lane == 0) fetch_vector(ctl, xbuf, src, n);
-  wait_vector(p, ctl, vec_uses, lane);
-  consumer_sync();
-}
-
 // The residual rows this CTA's units update (rows_per_unit rows each), staged in shared memory
-// so that the epilogue does not wait for a load.
+// so that the epilogue does not wait for a load (visible after the next consumer_sync).
 __device__ void stage_residual(const Params& p, Ctl* ctl, const PhaseDesc& P, uint32_t c, uint32_t G,
-                               int rows_per_unit, int cw, int lane) {
+                               int rows_per_unit, uint32_t x_epoch, int cw, int lane) {
   int32_t u0, n;
   cta_units(P, c, G, u0, n);
   const int tid = cw * 32 + lane;
-  if (tid < n * rows_per_unit) ctl->xres[tid] = __ldcg(p.x + (size_t)u0 * rows_per_unit + tid);
+  if (tid < n * rows_per_unit) {
+    const ll_t* src = p.x + (size_t)u0 * rows_per_unit + tid;
+    ll_t w = ll_load(src);
+    if (ll_wait(src, x_epoch, w, p, ctl)) ctl->xres[tid] = ll_value(w);
+  }
 }
 
 // Router softmax + top-k (ties to the lower index), gates renormalised over the choice; forced
 // experts (test hook) keep the router's probabilities of those experts.  Called by a whole warp:
 // the logits are staged in shared memory in one batch, lane 0 does the sequential part.
-__device__ void select_experts(const Params& p, Ctl* ctl, int layer, int lane) {
+__device__ void select_experts(const Params& p, Ctl* ctl, int layer, uint32_t r_epoch, int lane) {
   const int E = p.E, K = p.topk;
-  for (int e = lane; e < E; e += 32) ctl->stage[e] = __ldcg(p.rlog + e);
+  for (int e = lane; e < E; e += 32) {
+    ll_t w = ll_load(p.rlog + e);
+    ctl->stage[e] = ll_wait(p.rlog + e, r_epoch, w, p, ctl) ? ll_value(w) : 0.0f;
+  }
   __syncwarp();
   if (lane == 0) {
     const float* r = ctl->stage;
@@ -329,7 +341,8 @@ __device__ void select_experts(const Params& p, Ctl* ctl, int layer, int lane) {
 
 template <int ROWS, int SLOTS, int WDT, bool XPERSLOT>
 __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, const PhaseDesc& Pd,
-                                        const Step& st, uint32_t c, uint32_t G, int cw, int lane, uint32_t& t_io) {
+                                        const Step& st, uint32_t c, uint32_t G, int cw, int lane, uint32_t& t_io,
+                                        uint32_t ew) {
   // every field the loops use lives in registers (the descriptors are in local memory, and each
   // mbarrier asm statement would otherwise force them to be reloaded)
   constexpr int EB = WDT == DT_E4M3 ? 1 : 2;
@@ -398,19 +411,25 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
           const float a2 = fmaf(a, cs, -__fmul_rn(b, sn));
           const float b2 = fmaf(b, cs, __fmul_rn(a, sn));
           if (isq) {
-            __stcg(p.q + head * p.hd + i, a2);
-            __stcg(p.q + head * p.hd + i + half, b2);
+            ll_store(p.q + head * p.hd + i, ll_pack(a2, ew));
+            ll_store(p.q + head * p.hd + i + half, ll_pack(b2, ew));
           } else {
             const size_t row = (((size_t)L * p.hkv + head) * p.max_ctx + pos) * p.hd;
-            p.kc[row + i] = round_kv(a2, p.kvdt);
-            p.kc[row + i + half] = round_kv(b2, p.kvdt);
+            const uint16_t ka = round_kv(a2, p.kvdt), kb = round_kv(b2, p.kvdt);
+            p.kc[row + i] = ka;
+            p.kc[row + i + half] = kb;
+            ll_store(p.knew + head * p.hd + i, ll_pack_bits(ka, ew));
+            ll_store(p.knew + head * p.hd + i + half, ll_pack_bits(kb, ew));
           }
         } else {
           const int uu = unit - nq - nk;
           const int head = uu / half, i = uu % half;
           const size_t row = (((size_t)L * p.hkv + head) * p.max_ctx + pos) * p.hd;
-          p.vc[row + i] = round_kv(a, p.kvdt);
-          p.vc[row + i + half] = round_kv(b, p.kvdt);
+          const uint16_t va = round_kv(a, p.kvdt), vb = round_kv(b, p.kvdt);
+          p.vc[row + i] = va;
+          p.vc[row + i + half] = vb;
+          ll_store(p.vnew + head * p.hd + i, ll_pack_bits(va, ew));
+          ll_store(p.vnew + head * p.hd + i + half, ll_pack_bits(vb, ew));
         }
       }
     } else if (kind == PK_WO || kind == PK_DOWN) {
@@ -419,16 +438,16 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
         float y = acc[0];
 #pragma unroll
         for (int j = 1; j < ROWS; ++j) if (lane == j) y = acc[j];
-        __stcg(p.x + row, __fadd_rn(ctl->xres[row - u0 * ROWS], y));
+        ll_store(p.x + row, ll_pack(__fadd_rn(ctl->xres[row - u0 * ROWS], y), ew));
       }
     } else if (kind == PK_GU) {
-      if (lane == 0) __stcg(p.h + unit, silu_mul(acc[0], acc[1]));
+      if (lane == 0) ll_store(p.h + unit, ll_pack(silu_mul(acc[0], acc[1]), ew));
     } else if (kind == PK_ROUTER) {
       if (lane < ROWS) {
         float y = acc[0];
 #pragma unroll
         for (int j = 1; j < ROWS; ++j) if (lane == j) y = acc[j];
-        __stcg(p.rlog + unit * ROWS + lane, y);
+        ll_store(p.rlog + unit * ROWS + lane, ll_pack(y, ew));
       }
     } else if (kind == PK_EGU) {
       if (lane < p.topk) {
@@ -439,7 +458,7 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
         const int e = ctl->sel[lane];
         const float sg = __ldg(p.e_gate_scale[L] + (size_t)e * p.fexp + unit);
         const float su = __ldg(p.e_up_scale[L] + (size_t)e * p.fexp + unit);
-        __stcg(p.h + lane * p.fexp + unit, silu_mul(__fmul_rn(sg, g), __fmul_rn(su, uval)));
+        ll_store(p.h + lane * p.fexp + unit, ll_pack(silu_mul(__fmul_rn(sg, g), __fmul_rn(su, uval)), ew));
       }
     } else if (kind == PK_EDOWN) {
       if (lane == 0) {
@@ -452,7 +471,7 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
             ax = fmaf(ctl->gate[s], y, ax);
           }
         }
-        __stcg(p.x + unit, __fadd_rn(ctl->xres[unit - u0], ax));
+        ll_store(p.x + unit, ll_pack(__fadd_rn(ctl->xres[unit - u0], ax), ew));
       }
     } else if (kind == PK_LM) {
       if (lane == 0) {
@@ -489,6 +508,7 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
 // ---------------------------------------------------------------- finalisation
 
 __device__ void finalize_token(const Params& p, const Step& st, int32_t token) {
+  *p.epoch = st.ebase + (uint32_t)p.n_phases;  // the next step's phases publish new epochs
   StepState* s = p.state;
   s->out_token = token;
   if (p.out_seq) p.out_seq[st.seq_index] = token;
@@ -539,7 +559,7 @@ __device__ __forceinline__ void group_heads(int g, int hq, int hkv, int& h0, int
 template <int HD>
 __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* xbuf, const PhaseDesc& P,
                                              const Step& st, uint32_t c, uint32_t G, int cw, int lane,
-                                             uint32_t& att_uses_io) {
+                                             uint32_t& att_uses_io, uint32_t ew) {
   constexpr int NV = HD / 8;         // 8-element vectors per K row (partial sums of the contract dot)
   constexpr int PPI = 32 / NV;       // positions per score pass (NV lanes per position)
   constexpr int NPASS = kAttnBlock / PPI;
@@ -553,12 +573,15 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
   const uint64_t wait_ns = p.wait_ns;
   const uint16_t* __restrict__ kc = p.kc;
   const uint16_t* __restrict__ vc = p.vc;
-  const float* __restrict__ qg = p.q;
+  const ll_t* qg = p.q;
+  const ll_t* knew = p.knew;
+  const ll_t* vnew = p.vnew;
+  const uint32_t qe = st.ebase + 1 + (uint32_t)P.src_ph;  // epoch of this layer's QKV outputs
   float* part_m = p.part_m;
   float* part_l = p.part_l;
   float* part_o = p.part_o;
   uint32_t* head_ctr = p.head_ctr;
-  float* attn = p.attn;
+  ll_t* attn = p.attn;
   uint32_t att_uses = att_uses_io;
   const int nb = (ctx + kAttnBlock - 1) / kAttnBlock;
   const int hq = p.hq, hkv = p.hkv;
@@ -590,10 +613,29 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
       // this lane's 8 query elements (the same vector index v in every score pass)
       const int v = lane % NV;
       float q8[8];
-      if (active) ldcg_x8(qg + (size_t)h * HD + v * 8, q8);
-      const bool ok = mbar_wait(&ctl->att_bar[slot], att_uses & 1, &ctl->abort, wait_ns);
+      if (active) {
+        const ll_t* qs = qg + (size_t)h * HD + v * 8;
+        ll_t w8[8];
+#pragma unroll
+        for (int e2 = 0; e2 < 8; ++e2) w8[e2] = ll_load(qs + e2);
+#pragma unroll
+        for (int e2 = 0; e2 < 8; ++e2) q8[e2] = ll_wait(qs + e2, qe, w8[e2], p, ctl) ? ll_value(w8[e2]) : 0.0f;
+      }
+      bool ok = mbar_wait(&ctl->att_bar[slot], att_uses & 1, &ctl->abort, wait_ns);
       ++att_uses;
       if (!ok && lane == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
+      if (hh == 0 && j0 + nvalid == ctx) {
+        // the block holding this step's position: its K/V row comes from the tagged copies
+        // (the cache row may not have landed when the bulk copy read it)
+        const int jr = ctx - 1 - j0;
+        for (int i = lane; i < HD; i += 32) {
+          ll_t wk = ll_load(knew + (size_t)g * HD + i), wv = ll_load(vnew + (size_t)g * HD + i);
+          if (ll_wait(knew + (size_t)g * HD + i, qe, wk, p, ctl)) SK[(size_t)jr * HD + i] = (uint16_t)wk;
+          if (ll_wait(vnew + (size_t)g * HD + i, qe, wv, p, ctl)) SV[(size_t)jr * HD + i] = (uint16_t)wv;
+        }
+      }
+      asm volatile("bar.sync %0, %1;" ::"r"(2 + slot), "r"(gmax * 32) : "memory");
+      ok = ok && !aborted(ctl);
       if (cw == 0 && lane == 0 && it == (int)c) stamp(p, c, P.index, 4);
       if (active && ok) {
         // scores: NV lanes per position, lane = contract partial index v, folded like the contract
@@ -699,6 +741,12 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
       Wm[hx * nbmax + bb] = __ldcg(part_m + (size_t)(h0 + hx) * nbmax + bb);
       Wl[hx * nbmax + bb] = __ldcg(part_l + (size_t)(h0 + hx) * nbmax + bb);
     }
+    if (tid == 0) {
+      // rearm the group's counter before any merged output can be seen (the next layer's
+      // blocks depend on this output)
+      atomicExch(head_ctr + g, 0u);
+      __threadfence();
+    }
     consumer_sync();
     if (cw < gh) {  // one warp per head: M = max_b m_b, then w_b = exp(m_b - M)
       float M = __int_as_float(0xFF800000);
@@ -736,11 +784,10 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
             }
           }
         }
-        __stcg(attn + (size_t)(h0 + hx) * HD + dd, __fdiv_rn(O, Ls));
+        ll_store(attn + (size_t)(h0 + hx) * HD + dd, ll_pack(__fdiv_rn(O, Ls), ew));
       }
     }
     consumer_sync();
-    if (tid == 0) head_ctr[g] = 0u;
   }
   if (tid == 0) ctl->n_done = 0;
   att_uses_io = att_uses;
@@ -835,9 +882,8 @@ __device__ __noinline__ void sample_phase(const Params& p, Ctl* ctl, const Step&
 __device__ bool grid_barrier(const Params& p, Ctl* ctl, uint32_t c, uint32_t G, int& bidx) {
   consumer_sync();
   if (threadIdx.x == 0) {
-    const bool skip = (int)c == p.skip_cta && bidx == p.skip_barrier;
     const bool was_aborted = aborted(ctl);
-    if (!grid_arrive_wait(p.bar_ctr, G, !skip, !was_aborted, p.wait_ns)) set_error(p, ctl, DE_BARRIER_TIMEOUT);
+    if (!grid_arrive_wait(p.bar_ctr, G, true, !was_aborted, p.wait_ns)) set_error(p, ctl, DE_BARRIER_TIMEOUT);
     if (!aborted(ctl) && *(volatile int32_t*)p.err != 0) *(volatile int32_t*)&ctl->abort = 1;
   }
   ++bidx;
@@ -847,18 +893,18 @@ __device__ bool grid_barrier(const Params& p, Ctl* ctl, uint32_t c, uint32_t G, 
 
 template <int WDT>
 __device__ void run_gemv(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, const PhaseDesc& P, const Step& st,
-                         uint32_t c, uint32_t G, int cw, int lane, uint32_t& t) {
+                         uint32_t c, uint32_t G, int cw, int lane, uint32_t& t, uint32_t ew) {
   switch (P.kind) {
     case PK_QKV:
     case PK_GU:
-      gemv_phase<2, 1, WDT, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t);
+      gemv_phase<2, 1, WDT, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
       break;
     case PK_WO:
     case PK_DOWN:
-      gemv_phase<2, 1, WDT, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t);
+      gemv_phase<2, 1, WDT, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
       break;
     case PK_LM:
-      gemv_phase<4, 1, WDT, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t);
+      gemv_phase<4, 1, WDT, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
       break;
     default:
       break;
@@ -867,11 +913,11 @@ __device__ void run_gemv(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
 
 template <int SLOTS>
 __device__ void run_expert(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, const PhaseDesc& P, const Step& st,
-                           uint32_t c, uint32_t G, int cw, int lane, uint32_t& t) {
+                           uint32_t c, uint32_t G, int cw, int lane, uint32_t& t, uint32_t ew) {
   if (P.kind == PK_EGU)
-    gemv_phase<2, SLOTS, DT_E4M3, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t);
+    gemv_phase<2, SLOTS, DT_E4M3, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
   else
-    gemv_phase<1, SLOTS, DT_E4M3, true>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t);
+    gemv_phase<1, SLOTS, DT_E4M3, true>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
 }
 
 __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, const Step& st, uint32_t c,
@@ -879,99 +925,112 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
   uint32_t t = 0;
   int bidx = 0;
   int sel_layer = -1;
-  uint32_t att_uses = 0, vec_uses = 0;
+  uint32_t att_uses = 0;
+  const int tid = cw * 32 + lane;
   for (int ph = ph0; ph < ph1; ++ph) {
+    // every warp of this CTA has left the previous phase before this one reuses the shared input
+    // vector, the staging areas and the staged residual rows
+    if (ph > ph0) consumer_sync();
     const PhaseDesc P = p.phases[ph];
     const int L = P.layer;
     const bool ab = aborted(ctl);
+    // epochs: what this phase publishes (0 = withheld by the test hook) and what it reads
+    const uint32_t ew = ((int)c == p.skip_cta && ph == p.skip_phase) ? 0u : st.ebase + 1 + (uint32_t)ph;
+    const uint32_t e_src = st.ebase + 1 + (uint32_t)P.src_ph;
+    const uint32_t e_res = st.ebase + 1 + (uint32_t)P.res_ph;
+    const uint32_t e_sel = st.ebase + 1 + (uint32_t)P.sel_ph;
+    int32_t u0, n;
+    cta_units(P, c, G, u0, n);
     if (cw == 0 && lane == 0) stamp(p, c, ph, 0);
-    // ---- prologue: the GEMV input vector into shared memory
+    // ---- prologue: the GEMV input vector into shared memory (skipped by CTAs without units)
     switch (P.kind) {
       case PK_QKV: {
-        const void* emb = L == 0 ? (const uint8_t*)p.tok_emb + (size_t)st.token * p.d * (p.wdt == DT_E4M3 ? 1 : 2)
-                                 : nullptr;
-        if (L == 0 && !ab) {
+        const void* emb = L == 0 ? (const uint8_t*)p.tok_emb + (size_t)st.token * p.d * 2 : nullptr;
+        if (L == 0 && !ab) {  // the residual starts as the embedding row: publish this CTA's slice
           const int a = (int)((long long)c * p.d / G), b = (int)((long long)(c + 1) * p.d / G);
-          for (int i = a + cw * 32 + lane; i < b; i += kConsumerWarps * 32)
-            __stcg(p.x + i, load_elem(emb, (size_t)i, p.wdt));
+          for (int i = a + tid; i < b; i += kConsumerWarps * 32)
+            ll_store(p.x + i, ll_pack(load_elem(emb, (size_t)i, p.wdt), ew));
         }
-        if (p.trace && c == 0 && !ab) {
-          for (int i = cw * 32 + lane; i < p.d; i += kConsumerWarps * 32)
-            p.trace[(size_t)L * p.d + i] = emb ? load_elem(emb, (size_t)i, p.wdt) : __ldcg(p.x + i);
-        }
-        {  // the RoPE row of this position, for the epilogue (overlaps the prologue's round trip)
-          const int half = p.hd / 2, tid = cw * 32 + lane;
+        if (n > 0) {
+          const int half = p.hd / 2;  // the RoPE row of this position, for the epilogue
           if (tid < half) {
             ctl->rope_cs[tid] = __ldg(p.rope_cos + (size_t)st.pos * half + tid);
             ctl->rope_sn[tid] = __ldg(p.rope_sin + (size_t)st.pos * half + tid);
           }
+          rmsnorm_prologue(p, ctl, xbuf, p.attn_norm[L], emb, e_src, L, c, cw, lane);
         }
-        rmsnorm_prologue(p, ctl, xbuf, p.attn_norm[L], emb, cw, lane, vec_uses);
         break;
       }
       case PK_WO:
-        stage_residual(p, ctl, P, c, G, 2, cw, lane);
-        copy_prologue(p, ctl, xbuf, p.attn, p.hq * p.hd, cw, lane, vec_uses);
+        if (n > 0) {
+          stage_residual(p, ctl, P, c, G, 2, e_res, cw, lane);
+          ll_fetch(p, ctl, xbuf, p.attn, p.hq * p.hd, e_src, tid);
+        }
         break;
       case PK_DOWN:
-        stage_residual(p, ctl, P, c, G, 2, cw, lane);
-        copy_prologue(p, ctl, xbuf, p.h, p.ff, cw, lane, vec_uses);
+        if (n > 0) {
+          stage_residual(p, ctl, P, c, G, 2, e_res, cw, lane);
+          ll_fetch(p, ctl, xbuf, p.h, p.ff, e_src, tid);
+        }
         break;
       case PK_EDOWN:
         if (sel_layer != L) {
           if (cw == 0) {
-            select_experts(p, ctl, L, lane);
+            select_experts(p, ctl, L, e_sel, lane);
             if (lane == 0) mbar_arrive(&ctl->sel_bar);
           }
           sel_layer = L;
         }
-        stage_residual(p, ctl, P, c, G, 1, cw, lane);
-        copy_prologue(p, ctl, xbuf, p.h, p.topk * p.fexp, cw, lane, vec_uses);
+        if (n > 0) {
+          stage_residual(p, ctl, P, c, G, 1, e_res, cw, lane);
+          ll_fetch(p, ctl, xbuf, p.h, p.topk * p.fexp, e_src, tid);
+        } else {
+          consumer_sync();  // the choice (shared memory) is read by every warp's epilogue
+        }
         break;
       case PK_GU:
-      case PK_ROUTER: rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, cw, lane, vec_uses); break;
+      case PK_ROUTER:
+        if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, e_src, -1, c, cw, lane);
+        break;
       case PK_EGU: {
         if (cw == 0) {
-          select_experts(p, ctl, L, lane);
+          select_experts(p, ctl, L, e_sel, lane);
           if (lane == 0) {
             if (c == 0 && !ab) for (int i = 0; i < p.topk; ++i) p.sel_out[L * p.topk + i] = ctl->sel[i];
             mbar_arrive(&ctl->sel_bar);  // release the choice to the producer
           }
         }
         sel_layer = L;
-        rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, cw, lane, vec_uses);
+        if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, e_src, -1, c, cw, lane);
+        else consumer_sync();
         break;
       }
-      case PK_LM: {
-        if (p.trace && c == 0 && !ab)
-          for (int i = cw * 32 + lane; i < p.d; i += kConsumerWarps * 32)
-            p.trace[(size_t)p.L * p.d + i] = __ldcg(p.x + i);
-        rmsnorm_prologue(p, ctl, xbuf, p.final_norm, nullptr, cw, lane, vec_uses);
+      case PK_LM:
+        if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.final_norm, nullptr, e_src, p.L, c, cw, lane);
         break;
-      }
       default: break;
     }
     // ---- body
     if (cw == 0 && lane == 0) stamp(p, c, ph, 1);
     if (P.kind == PK_ATTN) {
-      if (p.hd == 128) attention_phase<128>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses);
-      else if (p.hd == 64) attention_phase<64>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses);
-      else attention_phase<256>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses);
+      if (p.hd == 128) attention_phase<128>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+      else if (p.hd == 64) attention_phase<64>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+      else attention_phase<256>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
     } else if (P.kind == PK_SAMPLE) {
       if (st.temperature > 0.0f) sample_phase(p, ctl, st, c, G, cw, lane);
     } else if (P.kind == PK_EGU || P.kind == PK_EDOWN) {
       switch (p.topk) {
-        case 1: run_expert<1>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t); break;
-        case 2: run_expert<2>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t); break;
-        case 4: run_expert<4>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t); break;
-        default: run_expert<8>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t); break;
+        case 1: run_expert<1>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
+        case 2: run_expert<2>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
+        case 4: run_expert<4>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
+        default: run_expert<8>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
       }
     } else if (P.kind == PK_ROUTER) {
-      if (p.rdt == DT_BF16) gemv_phase<1, 1, DT_BF16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t);
-      else gemv_phase<1, 1, DT_F16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t);
+      if (p.rdt == DT_BF16) gemv_phase<1, 1, DT_BF16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+      else gemv_phase<1, 1, DT_F16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
     } else {
-      if (p.wdt == DT_BF16) run_gemv<DT_BF16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t);
-      else run_gemv<DT_F16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t);
+      if (p.wdt == DT_BF16) run_gemv<DT_BF16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+      else run_gemv<DT_F16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
     }
     // ---- the LM head's last CTA picks the greedy token
     if (P.kind == PK_LM && ctl->flag && st.temperature <= 0.0f && cw == 0 && lane == 0) {
@@ -983,12 +1042,11 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
     } else if (P.kind == PK_LM && ctl->flag && cw == 0 && lane == 0) {
       *p.lm_ctr = 0u;  // sampling: the maximum stays in argkey for the sampling phase
     }
-    // ---- grid barrier between dependent phases
     if (cw == 0 && lane == 0) stamp(p, c, ph, 2);
-    if (use_barrier && ph + 1 < ph1) {
-      const bool need = !(P.kind == PK_LM && st.temperature <= 0.0f);
-      if (need) grid_barrier(p, ctl, c, G, bidx);
-    }
+    // ---- dependent phases wait on the epochs of their inputs; only sampling, which needs the
+    // maximum over every CTA's logits, takes a grid barrier
+    if (use_barrier && ph + 1 < ph1 && ((P.kind == PK_LM && st.temperature > 0.0f) || p.debug_barriers))
+      grid_barrier(p, ctl, c, G, bidx);
     if (cw == 0 && lane == 0) stamp(p, c, ph, 3);
   }
 }
@@ -1009,7 +1067,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&ctl->sel_bar, 1);
     for (int w = 0; w < kAttnSlots; ++w) mbar_init(&ctl->att_bar[w], 1);
-    mbar_init(&ctl->vec_bar, 1);
     ctl->n_done = 0;
     ctl->abort = *(volatile int32_t*)p.err != 0 ? 1 : 0;
     ctl->flag = 0;
@@ -1025,6 +1082,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     st.temperature = __ldcg(&s->temperature);
     st.token = p.tok_seq ? __ldcg(p.tok_seq + st.seq_index) : __ldcg(&s->token);
     st.u = p.u_seq ? __ldcg(p.u_seq + st.seq_index) : __ldcg(&s->u);
+    st.ebase = __ldcg(p.epoch);
   }
   if (warp == kConsumerWarps) {
     if (lane == 0) producer(p, ctl, ring, c, G, ph0, ph1);

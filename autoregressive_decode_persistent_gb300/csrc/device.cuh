@@ -111,6 +111,27 @@ __device__ __forceinline__ bool grid_arrive_wait(unsigned long long* ctr, uint32
   return true;
 }
 
+// ---------------------------------------------------------------- epoch-tagged words
+
+using ll_t = unsigned long long;
+
+__device__ __forceinline__ ll_t ll_pack(float v, uint32_t epoch) {
+  return ((ll_t)epoch << 32) | (ll_t)__float_as_uint(v);
+}
+__device__ __forceinline__ ll_t ll_pack_bits(uint32_t bits, uint32_t epoch) { return ((ll_t)epoch << 32) | bits; }
+__device__ __forceinline__ uint32_t ll_epoch(ll_t w) { return (uint32_t)(w >> 32); }
+__device__ __forceinline__ float ll_value(ll_t w) { return __uint_as_float((uint32_t)w); }
+
+// One 64-bit store / load: value and epoch become visible together.
+__device__ __forceinline__ void ll_store(ll_t* p, ll_t w) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ ll_t ll_load(const ll_t* p) {
+  ll_t w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+
 // ---------------------------------------------------------------- storage types
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }

@@ -75,6 +75,7 @@ struct adp_model {
   const void* graph_key_logits = nullptr;
   bool graph_key_sample = false;
   int sticky = ADP_OK;
+  size_t ll_bytes[7] = {0};  // sizes of the epoch-tagged exchange buffers
 
   template <class T>
   int alloc(T** ptr, size_t count) {
@@ -159,21 +160,59 @@ static void plan(adp_model* m) {
   const adp_config& c = m->cfg;
   const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim;
   const int eb = elem_bytes(c.weight_dtype);
+  // Which phase produced each input: the residual x, the attention output, the FFN activations
+  // and the router logits are read by epoch, so every phase names its producers.
+  int x_ph = -1;  // latest writer of the residual (-1 before layer 0: the embedding row)
+  auto last = [&]() { return (int)m->phases.size() - 1; };
+  auto link = [&](int src, int res, int sel) {
+    PhaseDesc& P = m->phases.back();
+    P.src_ph = src;
+    P.res_ph = res;
+    P.sel_ph = sel;
+  };
   for (int l = 0; l < c.n_layers; ++l) {
     add_phase(m, PK_QKV, l, (hq + 2 * hkv) * hd / 2, 2, 1, d, eb, c.weight_dtype, true, 1);
+    link(x_ph, -1, -1);
+    const int qkv = last();
+    if (l == 0) x_ph = qkv;  // the QKV phase of layer 0 publishes x = embedding row
     add_phase(m, PK_ATTN, l, 0, 0, 0, 0, 0, 0, false, 0);
+    link(qkv, -1, -1);
+    const int att = last();
     add_phase(m, PK_WO, l, d / 2, 2, 1, hq * hd, eb, c.weight_dtype, true, 1);
+    link(att, x_ph, -1);
+    x_ph = last();
     if (c.n_experts == 0) {
       add_phase(m, PK_GU, l, c.d_ff, 2, 1, d, eb, c.weight_dtype, true, 1);
+      link(x_ph, -1, -1);
+      const int gu = last();
       add_phase(m, PK_DOWN, l, d / 2, 2, 1, c.d_ff, eb, c.weight_dtype, true, 1);
+      link(gu, x_ph, -1);
+      x_ph = last();
     } else {
       add_phase(m, PK_ROUTER, l, c.n_experts, 1, 1, d, elem_bytes(c.router_dtype), c.router_dtype, true, 1);
+      link(x_ph, -1, -1);
+      const int router = last();
       add_phase(m, PK_EGU, l, c.d_expert, 2, c.top_k, d, 1, ADP_E4M3, true, c.n_experts);
+      link(x_ph, -1, router);
+      const int egu = last();
       add_phase(m, PK_EDOWN, l, d, 1, c.top_k, c.d_expert, 1, ADP_E4M3, true, c.n_experts);
+      link(egu, x_ph, router);
+      x_ph = last();
     }
   }
   add_phase(m, PK_LM, c.n_layers, c.vocab / 4, 4, 1, d, eb, c.weight_dtype, true, 1);
+  link(x_ph, -1, -1);
   add_phase(m, PK_SAMPLE, c.n_layers, 0, 0, 0, 0, 0, 0, false, 0);
+  link(-1, -1, -1);
+}
+
+// Zero the epoch base and every epoch-tagged exchange buffer (epoch 0 is never awaited).
+static int clear_exchange(adp_model* m) {
+  const Params& p = m->p;
+  void* bufs[7] = {p.x, p.q, p.attn, p.h, p.rlog, p.knew, p.vnew};
+  for (int i = 0; i < 7; ++i) CK(cudaMemsetAsync(bufs[i], 0, m->ll_bytes[i], m->stream));
+  CK(cudaMemsetAsync(p.epoch, 0, 4, m->stream));
+  return ADP_OK;
 }
 
 // ---------------------------------------------------------------- model creation
@@ -302,6 +341,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   const int topk = std::max(c.top_k, 1);
   if ((rc = m->alloc(&p.x, d)) || (rc = m->alloc(&p.q, hq * hd)) || (rc = m->alloc(&p.attn, hq * hd)) ||
       (rc = m->alloc(&p.h, ffw)) || (rc = m->alloc(&p.rlog, std::max(c.n_experts, 1))) ||
+      (rc = m->alloc(&p.knew, hkv * hd)) || (rc = m->alloc(&p.vnew, hkv * hd)) || (rc = m->alloc(&p.epoch, 1)) ||
       (rc = m->alloc(&p.part_m, (size_t)hq * nbmax)) || (rc = m->alloc(&p.part_l, (size_t)hq * nbmax)) ||
       (rc = m->alloc(&p.part_o, (size_t)hq * nbmax * hd)) || (rc = m->alloc(&p.head_ctr, hq)) ||
       (rc = m->alloc(&p.sblock, nblk)) || (rc = m->alloc(&p.sample_ctr, 1)) || (rc = m->alloc(&p.argkey, 1)) ||
@@ -309,6 +349,14 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
       (rc = m->alloc(&p.sel_out, (size_t)L * topk)) || (rc = m->alloc(&p.state, 1)) ||
       (rc = m->alloc(&m->d_force, (size_t)L * topk)) || (rc = m->alloc(&m->d_logits_scratch, c.vocab)))
     return rc;
+  m->ll_bytes[0] = (size_t)d * 8;
+  m->ll_bytes[1] = (size_t)hq * hd * 8;
+  m->ll_bytes[2] = (size_t)hq * hd * 8;
+  m->ll_bytes[3] = (size_t)ffw * 8;
+  m->ll_bytes[4] = (size_t)std::max(c.n_experts, 1) * 8;
+  m->ll_bytes[5] = (size_t)hkv * hd * 8;
+  m->ll_bytes[6] = (size_t)hkv * hd * 8;
+  if ((rc = clear_exchange(m))) return rc;
   CK(cudaMemsetAsync(p.head_ctr, 0, hq * 4, m->stream));
   CK(cudaMemsetAsync(p.sample_ctr, 0, 4, m->stream));
   CK(cudaMemsetAsync(p.argkey, 0, 8, m->stream));
@@ -343,7 +391,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   p.wait_ns = 200000000ull;
   p.l2_lookahead = 0;
   p.skip_cta = -1;
-  p.skip_barrier = -1;
+  p.skip_phase = -1;
   CK(cudaStreamSynchronize(m->stream));
   CK(cudaGetLastError());
   return ADP_OK;
@@ -557,7 +605,7 @@ extern "C" int adp_decode_step(adp_model* m, adp_kv* kv, int32_t token, const ad
   if (rs) return rs;
   Params p = step_params(m, kv, dev_logits, nullptr, nullptr, nullptr);
   int rc = enqueue_step(m, p, T > 0.0f);
-  m->p.skip_cta = m->p.skip_barrier = -1;
+  m->p.skip_cta = m->p.skip_phase = -1;
   if (rc) return rc;
   rc = finish(m);
   if (rc) return rc;
@@ -589,7 +637,7 @@ extern "C" int adp_prefill(adp_model* m, adp_kv* kv, const int32_t* host_tokens,
     int rc = enqueue_step(m, p, T > 0.0f);
     if (rc) return rc;
   }
-  m->p.skip_cta = m->p.skip_barrier = -1;
+  m->p.skip_cta = m->p.skip_phase = -1;
   int rc = finish(m);
   if (rc) return rc;
   *next_token = m->h_out[0];
@@ -632,9 +680,11 @@ extern "C" int adp_reset(adp_model* m) {
   CK(cudaMemsetAsync(p.lm_ctr, 0, 4, m->stream));
   CK(cudaMemsetAsync(p.bar_ctr, 0, 8, m->stream));
   CK(cudaMemsetAsync(p.err, 0, 4, m->stream));
+  int rc = clear_exchange(m);
+  if (rc) return rc;
   CK(cudaStreamSynchronize(m->stream));
   m->sticky = ADP_OK;
-  m->p.skip_cta = m->p.skip_barrier = -1;
+  m->p.skip_cta = m->p.skip_phase = -1;
   return ADP_OK;
 }
 
@@ -727,6 +777,13 @@ extern "C" int adp_debug_timeline_shape(const adp_model* m, int32_t* ctas, int32
   return ADP_OK;
 }
 
+extern "C" int adp_debug_barriers(adp_model* m, int on) {
+  if (!m) return ADP_ERR_INVALID_ARG;
+  m->p.debug_barriers = on ? 1 : 0;
+  if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
+  return ADP_OK;
+}
+
 extern "C" int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes) {
   if (!m) return ADP_ERR_INVALID_ARG;
   m->p.l2_lookahead = bytes;
@@ -741,9 +798,9 @@ extern "C" int adp_debug_set_wait_limit(adp_model* m, uint64_t ns) {
   return ADP_OK;
 }
 
-extern "C" int adp_debug_skip_barrier_arrival(adp_model* m, int32_t cta, int32_t barrier) {
+extern "C" int adp_debug_skip_publication(adp_model* m, int32_t cta, int32_t phase) {
   if (!m) return ADP_ERR_INVALID_ARG;
   m->p.skip_cta = cta;
-  m->p.skip_barrier = barrier;
+  m->p.skip_phase = phase;
   return ADP_OK;
 }

@@ -51,6 +51,9 @@ struct PhaseDesc {
   int32_t wdt;            // weight DType
   int32_t has_weights;
   int32_t index;          // position of this phase in the step's phase list
+  int32_t src_ph;         // phase whose output vector is this phase's input (-1: the embedding row)
+  int32_t res_ph;         // phase that wrote the residual rows this phase updates (-1: none)
+  int32_t sel_ph;         // router phase whose logits choose this phase's experts (-1: none)
   int32_t pad_;
   uint64_t region;        // byte offset of the phase's region in the image (expert 0 for expert phases)
   uint64_t expert_stride; // bytes of one expert's region
@@ -93,12 +96,17 @@ struct Params {
   // RoPE tables [max_ctx][hd/2]
   const float* rope_cos;
   const float* rope_sin;
-  // scratch
-  float* x;        // [d] residual
-  float* q;        // [hq*hd] post-RoPE queries
-  float* attn;     // [hq*hd] attention output
-  float* h;        // [max(ff, topk*f)] FFN activations
-  float* rlog;     // [E] router logits
+  // Activations exchanged between CTAs, as 64-bit words {fp32 bits (low), epoch (high)} written
+  // with one store each: a reader polls a word until it carries the epoch of the phase that
+  // produces it, so no grid barrier separates dependent phases.
+  unsigned long long* x;     // [d] residual
+  unsigned long long* q;     // [hq*hd] post-RoPE queries
+  unsigned long long* knew;  // [hkv*hd] this step's K rows (storage bits)
+  unsigned long long* vnew;  // [hkv*hd] this step's V rows (storage bits)
+  unsigned long long* attn;  // [hq*hd] attention output
+  unsigned long long* h;     // [max(ff, topk*f)] FFN activations
+  unsigned long long* rlog;  // [E] router logits
+  uint32_t* epoch;           // epoch base of the next step (advanced by the step's last CTA)
   float* part_m;   // [hq][nbmax]
   float* part_l;   // [hq][nbmax]
   float* part_o;   // [hq][nbmax][hd]
@@ -120,10 +128,11 @@ struct Params {
   unsigned long long* timeline; // [G][n_phases][8] %globaltimer stamps or null
   uint64_t wait_ns;            // limit of every in-kernel wait
   uint32_t l2_lookahead;       // bytes of weight stream prefetched into L2 beyond the TMA loads
-  int32_t skip_cta, skip_barrier;
+  int32_t debug_barriers;      // 1: also take a grid barrier after every phase (debugging)
+  int32_t skip_cta, skip_phase;  // test hook: that CTA does not publish that phase's outputs
 };
 
 // Device error codes (the host maps them to ADP_ERR_*).
-enum DevErr : int32_t { DE_NONE = 0, DE_BARRIER_TIMEOUT = 1, DE_PIPELINE_TIMEOUT = 2 };
+enum DevErr : int32_t { DE_NONE = 0, DE_BARRIER_TIMEOUT = 1, DE_PIPELINE_TIMEOUT = 2 };  // 1: a dependency wait
 
 }  // namespace adp

@@ -282,6 +282,11 @@ def write_timeline(path, model, kv, tok0, P, cfg):
         d["body_us"] += body
         d["barrier_us"] += bar
         d["count"] += 1
+        if k not in ("attn", "sample") and np.any(s[:, 4] > 0):
+            d.setdefault("ring_full_us", 0.0)
+            d["ring_full_us"] += float(np.mean(s[:, 7]) / 1e3)
+            d.setdefault("issue_span_us", 0.0)
+            d["issue_span_us"] += float(np.mean(s[:, 5] - s[:, 4]) / 1e3)
         if k == "attn":
             w = s[:, 4] > 0
             if w.any():

@@ -50,7 +50,7 @@ enum {
   ADP_ERR_CONTEXT_OVERFLOW = -3,   /* position >= max_ctx */
   ADP_ERR_CUDA = -4,               /* a CUDA runtime call failed (message: adp_last_error) */
   ADP_ERR_NOT_CORESIDENT = -5,     /* the persistent grid cannot be co-resident on this GPU */
-  ADP_ERR_BARRIER_TIMEOUT = -6,    /* a grid barrier wait ran out (sticky until adp_reset) */
+  ADP_ERR_BARRIER_TIMEOUT = -6,    /* a wait for another CTA's output ran out (sticky until adp_reset) */
   ADP_ERR_PIPELINE_TIMEOUT = -7,   /* a weight-pipeline wait ran out (sticky until adp_reset) */
   ADP_ERR_UNIMPLEMENTED = -8
 };
@@ -137,7 +137,7 @@ int adp_kv_read(const adp_kv* kv, void* host_k, void* host_v, int32_t len);
  *  sampling     host struct, NULL = greedy
  *  next_token   host pointer, receives the sampled/greedy next token
  *  dev_logits   optional DEVICE pointer [vocab] fp32 that receives the step's logits
- * One cooperative kernel launch (one grid barrier between dependent phases), a 4-byte token
+ * One cooperative kernel launch (dependent phases wait on epoch-tagged outputs), a 4-byte token
  * and the 16-byte step state in, the token and status word out; synchronises the stream.
  * Errors: ADP_ERR_CONTEXT_OVERFLOW (p >= max_ctx; nothing launched), ADP_ERR_INVALID_ARG,
  * ADP_ERR_BARRIER_TIMEOUT / ADP_ERR_PIPELINE_TIMEOUT (sticky), ADP_ERR_CUDA. */
@@ -189,15 +189,18 @@ int adp_debug_trace_residual(adp_model* m, float* dev_buf);
  * adp_debug_timeline_shape. */
 int adp_debug_timeline(adp_model* m, uint64_t* dev_buf);
 int adp_debug_timeline_shape(const adp_model* m, int32_t* ctas, int32_t* phases);
+/* 1: also take a grid barrier after every phase (debugging the epoch-tagged exchange). */
+int adp_debug_barriers(adp_model* m, int on);
 /* Bytes of each SM's weight stream the producer warp keeps prefetched into L2 beyond its TMA
  * loads (default 0 = off).  A tuning knob: it lets HBM keep streaming while the compute
  * warps wait at barriers. */
 int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes);
 /* Wait limit of every in-kernel spin (grid barrier, weight pipeline), nanoseconds (default 2e8). */
 int adp_debug_set_wait_limit(adp_model* m, uint64_t ns);
-/* Test hook: CTA `cta` skips its arrival at grid barrier number `barrier` of the next step
- * (-1 = off), so that the others' wait runs out and the step returns ADP_ERR_BARRIER_TIMEOUT. */
-int adp_debug_skip_barrier_arrival(adp_model* m, int32_t cta, int32_t barrier);
+/* Test hook: in the next step, CTA `cta` withholds the outputs of phase number `phase` (-1 = off),
+ * so that every phase waiting for them runs out of time and the step returns
+ * ADP_ERR_BARRIER_TIMEOUT (a dependency wait ran out) instead of hanging. */
+int adp_debug_skip_publication(adp_model* m, int32_t cta, int32_t phase);
 
 #if defined(__GNUC__)
 #pragma GCC visibility pop

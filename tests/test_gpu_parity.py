@@ -157,10 +157,10 @@ def test_context_overflow_is_an_error(torch_cuda):
     assert e.value.code == adp.ADP_ERR_CONTEXT_OVERFLOW
 
 
-def test_barrier_timeout_is_reported_and_recoverable(torch_cuda):
-    """One CTA skips one grid-barrier arrival: every other CTA's wait runs out after 1 ms and the
-    step returns ADP_ERR_BARRIER_TIMEOUT (no hang, no fault); the error is sticky until adp_reset,
-    after which the model computes correctly again."""
+def test_dependency_timeout_is_reported_and_recoverable(torch_cuda):
+    """One CTA withholds its outputs of one phase: every CTA waiting for them gives up after 1 ms
+    and the step returns ADP_ERR_BARRIER_TIMEOUT (no hang, no fault); the error is sticky until
+    adp_reset, after which the model computes correctly again."""
     import torch
     from autoregressive_decode_persistent_gb300 import adp
     cfg = synth.get_config("tiny")
@@ -168,7 +168,7 @@ def test_barrier_timeout_is_reported_and_recoverable(torch_cuda):
     model = _model(cfg, W)
     kv = model.new_kv()
     adp.adp_debug_set_wait_limit(model.handle, 1_000_000)
-    adp.adp_debug_skip_barrier_arrival(model.handle, 3, 2)
+    adp.adp_debug_skip_publication(model.handle, 3, 2)  # CTA 3, the Wo phase of layer 0
     with pytest.raises(adp.AdpError) as e:
         kv.step(5)
     assert e.value.code == adp.ADP_ERR_BARRIER_TIMEOUT
