@@ -32,8 +32,8 @@
 namespace adp {
 
 struct Ctl {
-  uint64_t full[kSlots];
-  uint64_t empty[kSlots];
+  uint64_t full[kMaxSlots];
+  uint64_t empty[kMaxSlots];
   uint64_t sel_bar;
   int32_t abort;
   int32_t pad;
@@ -110,6 +110,7 @@ __device__ __forceinline__ void l2_advance(const Params& p, L2Cursor& cur, uint6
 
 __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, uint32_t G, int ph0, int ph1) {
   const uint64_t pol = policy_evict_first();
+  const uint32_t ns = (uint32_t)p.nslots;
   uint32_t t = 0;
   uint32_t sel_uses = 0;
   int sel_layer = -1;
@@ -146,8 +147,8 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
         const int kck = min(P.KC, P.K - ck * P.KC);
         const uint32_t bytes = (uint32_t)m * P.unit_rows * kck * P.eb;
         const uint64_t off = round_off + (uint64_t)m * P.unit_rows * ck * P.KC * P.eb;
-        const uint32_t slot = t % kSlots, use = t / kSlots;
-        if (t >= kSlots) {
+        const uint32_t slot = t % ns, use = t / ns;
+        if (t >= ns) {
           if (!mbar_try_wait(&ctl->empty[slot], (use - 1) & 1)) {
             const uint64_t tb = p.timeline ? globaltimer() : 0;
             l2_advance(p, cur, issue_pos, ph1, c, G);  // keep HBM busy while the consumers catch up
@@ -176,8 +177,7 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
   }
   // No bulk copy may still be writing this CTA's shared memory when it exits.
   int32_t never = 0;
-  for (uint32_t i = (t > (uint32_t)kSlots ? t - kSlots : 0); i < t; ++i)
-    mbar_wait(&ctl->full[i % kSlots], (i / kSlots) & 1, &never, p.wait_ns);
+  for (uint32_t i = (t > ns ? t - ns : 0); i < t; ++i) mbar_wait(&ctl->full[i % ns], (i / ns) & 1, &never, p.wait_ns);
 }
 
 // ---------------------------------------------------------------- consumer helpers
@@ -349,6 +349,7 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
   const int kind = Pd.kind, L = Pd.layer, K = Pd.K, KC = Pd.KC, n_chunks = Pd.n_chunks, upr = Pd.upr;
   const int pos = st.pos;
   const uint64_t wait_ns = p.wait_ns;
+  const uint32_t ns = (uint32_t)p.nslots;
   uint32_t t = t_io;
   int32_t u0, n;
   cta_units(Pd, c, G, u0, n);
@@ -362,7 +363,7 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
 #pragma unroll
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = 0.0f;
     for (int ck = 0; ck < n_chunks; ++ck) {
-      const uint32_t slot = t % kSlots, use = t / kSlots;
+      const uint32_t slot = t % ns, use = t / ns;
       bool ok = aborted(ctl) || mbar_wait(&ctl->full[slot], use & 1, &ctl->abort, wait_ns);
       if (!ok) {
         if (lane == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
@@ -508,6 +509,8 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
 // ---------------------------------------------------------------- finalisation
 
 __device__ void finalize_token(const Params& p, const Step& st, int32_t token) {
+  // every CTA has finished this step's attention: clear its per-layer block counters
+  for (int i = 0; i < p.L * p.hkv; ++i) p.head_ctr[i] = 0u;
   *p.epoch = st.ebase + (uint32_t)p.n_phases;  // the next step's phases publish new epochs
   StepState* s = p.state;
   s->out_token = token;
@@ -519,30 +522,6 @@ __device__ void finalize_token(const Params& p, const Step& st, int32_t token) {
 }
 
 // ---------------------------------------------------------------- attention phase
-
-// DPL consecutive KV values (one lane's share of a head_dim row) -> fp32.
-template <int DPL>
-__device__ __forceinline__ void load_kv_dims(const uint16_t* src, int kvdt, float (&out)[DPL]) {
-  if constexpr (DPL == 2) {
-    const uint32_t w = __ldcg(reinterpret_cast<const unsigned int*>(src));
-    out[0] = kv_to_f32((uint16_t)(w & 0xFFFFu), kvdt);
-    out[1] = kv_to_f32((uint16_t)(w >> 16), kvdt);
-  } else if constexpr (DPL == 4) {
-    const uint2 w = __ldcg(reinterpret_cast<const uint2*>(src));
-    out[0] = kv_to_f32((uint16_t)(w.x & 0xFFFFu), kvdt);
-    out[1] = kv_to_f32((uint16_t)(w.x >> 16), kvdt);
-    out[2] = kv_to_f32((uint16_t)(w.y & 0xFFFFu), kvdt);
-    out[3] = kv_to_f32((uint16_t)(w.y >> 16), kvdt);
-  } else {
-    const uint4 w = __ldcg(reinterpret_cast<const uint4*>(src));
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      out[2 * i] = kv_to_f32((uint16_t)(u[i] & 0xFFFFu), kvdt);
-      out[2 * i + 1] = kv_to_f32((uint16_t)(u[i] >> 16), kvdt);
-    }
-  }
-}
 
 // Heads [h0, h1) read KV head g: floor(h * hkv / hq) == g.
 __device__ __forceinline__ void group_heads(int g, int hq, int hkv, int& h0, int& h1) {
@@ -556,18 +535,62 @@ __device__ __forceinline__ void group_heads(int g, int hq, int hkv, int& h0, int
 // rows that the slot's first warp fetches into the slot's staging area with two TMA bulk
 // copies.  Each warp produces its head's block partial (m_b, l_b, o_b) of the contract.  The
 // CTA that finishes a group's last block merges the group's blocks with all consumer warps.
-template <int HD>
+// 8 KV-cache values (16 bytes) -> fp32 (exact).
+template <int KVDT>
+__device__ __forceinline__ void kv8(const uint4 w, float (&f)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (KVDT == DT_BF16) {
+      f[2 * i] = __uint_as_float(u[i] << 16);
+      f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+    } else {
+      const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+}
+
+// DPL consecutive KV values of one row (one lane's share of the PV pass) from shared memory.
+template <int KVDT, int DPL>
+__device__ __forceinline__ void kv_dims_smem(const uint16_t* src, float (&f)[DPL]) {
+  if constexpr (DPL == 8) {
+    kv8<KVDT>(*reinterpret_cast<const uint4*>(src), f);
+  } else {
+    uint32_t u[DPL / 2];
+    if constexpr (DPL == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(src);
+      u[0] = w.x;
+      u[1] = w.y;
+    } else {
+      u[0] = *reinterpret_cast<const uint32_t*>(src);
+    }
+#pragma unroll
+    for (int i = 0; i < DPL / 2; ++i) {
+      if constexpr (KVDT == DT_BF16) {
+        f[2 * i] = __uint_as_float(u[i] << 16);
+        f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+      } else {
+        const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+      }
+    }
+  }
+}
+
+template <int HD, int KVDT>
 __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* xbuf, const PhaseDesc& P,
                                              const Step& st, uint32_t c, uint32_t G, int cw, int lane,
                                              uint32_t& att_uses_io, uint32_t ew) {
   constexpr int NV = HD / 8;         // 8-element vectors per K row (partial sums of the contract dot)
-  constexpr int PPI = 32 / NV;       // positions per score pass (NV lanes per position)
-  constexpr int NPASS = kAttnBlock / PPI;
+  constexpr int KSTR = HD + 8;       // padded K row stride in shared memory (conflict-free row reads)
   constexpr int DPL = HD / 32;       // output dims per lane in the PV pass
   // parameters in registers (see gemv_phase)
   const int L = P.layer;
   const int ctx = st.pos + 1;
-  const int kvdt = p.kvdt, nbmax = p.nbmax, max_ctx = p.max_ctx;
+  const int nbmax = p.nbmax, max_ctx = p.max_ctx;
   const int slots = p.att_slots, gmax = p.att_gmax, slot_bytes = p.att_slot_bytes;
   const float scale = p.attn_scale;
   const uint64_t wait_ns = p.wait_ns;
@@ -590,9 +613,10 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
   const int slot = cw / gmax, hh = cw % gmax;
   if (slot < slots && !aborted(ctl)) {
     uint8_t* stg = reinterpret_cast<uint8_t*>(xbuf) + (size_t)slot * slot_bytes;
-    uint16_t* SK = reinterpret_cast<uint16_t*>(stg);
-    uint16_t* SV = SK + kAttnBlock * HD;
-    float* SS = reinterpret_cast<float*>(SV + kAttnBlock * HD);  // [gmax][32] scores
+    uint16_t* SK = reinterpret_cast<uint16_t*>(stg);             // [32][KSTR] K rows, padded
+    uint16_t* SV = SK + kAttnBlock * KSTR;                       // [32][HD] V rows
+    float* SQ = reinterpret_cast<float*>(SV + kAttnBlock * HD);  // [gmax][HD] queries
+    float* SS = SQ + kMaxGroup * HD;                             // [gmax][32] weights e_j
     for (int it = (int)c + (int)G * slot; it < items; it += (int)G * slots) {
       const int g = it % hkv, b = it / hkv;
       int h0, h1;
@@ -603,23 +627,28 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
       const int nvalid = min(kAttnBlock, ctx - j0);
       const size_t cache0 = (((size_t)L * hkv + g) * max_ctx + j0) * HD;
       const uint32_t bytes = (uint32_t)nvalid * HD * 2;
-      if (hh == 0 && lane == 0) {
+      if (hh == 0) {
         // the newest row was written this step by generic stores of other CTAs
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        mbar_arrive_expect_tx(&ctl->att_bar[slot], 2 * bytes);
-        tma_load_1d(SK, kc + cache0, bytes, &ctl->att_bar[slot], policy_evict_first());
-        tma_load_1d(SV, vc + cache0, bytes, &ctl->att_bar[slot], policy_evict_first());
+        if (lane == 0) {
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          mbar_arrive_expect_tx(&ctl->att_bar[slot], 2 * bytes);
+          tma_load_1d(SV, vc + cache0, bytes, &ctl->att_bar[slot], policy_evict_first());
+        }
+        __syncwarp();
+        if (lane < nvalid)  // one K row per lane, into the padded layout
+          tma_load_1d(SK + (size_t)lane * KSTR, kc + cache0 + (size_t)lane * HD, HD * 2, &ctl->att_bar[slot],
+                      policy_evict_first());
       }
-      // this lane's 8 query elements (the same vector index v in every score pass)
-      const int v = lane % NV;
-      float q8[8];
+      // this head's query, staged in shared memory (read by every lane in the score pass)
+      float* sq = SQ + hh * HD;
       if (active) {
-        const ll_t* qs = qg + (size_t)h * HD + v * 8;
-        ll_t w8[8];
+        const ll_t* qs = qg + (size_t)h * HD;
+        ll_t w[DPL];
 #pragma unroll
-        for (int e2 = 0; e2 < 8; ++e2) w8[e2] = ll_load(qs + e2);
+        for (int i = 0; i < DPL; ++i) w[i] = ll_load(qs + lane + 32 * i);
 #pragma unroll
-        for (int e2 = 0; e2 < 8; ++e2) q8[e2] = ll_wait(qs + e2, qe, w8[e2], p, ctl) ? ll_value(w8[e2]) : 0.0f;
+        for (int i = 0; i < DPL; ++i)
+          sq[lane + 32 * i] = ll_wait(qs + lane + 32 * i, qe, w[i], p, ctl) ? ll_value(w[i]) : 0.0f;
       }
       bool ok = mbar_wait(&ctl->att_bar[slot], att_uses & 1, &ctl->abort, wait_ns);
       ++att_uses;
@@ -630,7 +659,7 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
         const int jr = ctx - 1 - j0;
         for (int i = lane; i < HD; i += 32) {
           ll_t wk = ll_load(knew + (size_t)g * HD + i), wv = ll_load(vnew + (size_t)g * HD + i);
-          if (ll_wait(knew + (size_t)g * HD + i, qe, wk, p, ctl)) SK[(size_t)jr * HD + i] = (uint16_t)wk;
+          if (ll_wait(knew + (size_t)g * HD + i, qe, wk, p, ctl)) SK[(size_t)jr * KSTR + i] = (uint16_t)wk;
           if (ll_wait(vnew + (size_t)g * HD + i, qe, wv, p, ctl)) SV[(size_t)jr * HD + i] = (uint16_t)wv;
         }
       }
@@ -638,54 +667,52 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
       ok = ok && !aborted(ctl);
       if (cw == 0 && lane == 0 && it == (int)c) stamp(p, c, P.index, 4);
       if (active && ok) {
-        // scores: NV lanes per position, lane = contract partial index v, folded like the contract
-        float sc[NPASS];
+        // score of position j0 + lane: the contract dot over the K row, its 32-slot tree in registers
+        float sj = __int_as_float(0xFF800000);  // -inf
+        if (lane < nvalid) {
+          float a[32];
 #pragma unroll
-        for (int pass = 0; pass < NPASS; ++pass) {
-          const int jj = pass * PPI + lane / NV;
-          const uint4 kw = *reinterpret_cast<const uint4*>(SK + (size_t)jj * HD + v * 8);
-          const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w};
-          float k8[8];
-#pragma unroll
-          for (int t2 = 0; t2 < 4; ++t2) {
-            k8[2 * t2] = kv_to_f32((uint16_t)(kk[t2] & 0xFFFFu), kvdt);
-            k8[2 * t2 + 1] = kv_to_f32((uint16_t)(kk[t2] >> 16), kvdt);
+          for (int v = 0; v < NV; ++v) {
+            float k8[8], q8[8];
+            kv8<KVDT>(*reinterpret_cast<const uint4*>(SK + (size_t)lane * KSTR + v * 8), k8);
+            load_x8(sq + v * 8, q8);
+            a[v] = fma8(k8, q8, 0.0f);
           }
-          sc[pass] = fma8(k8, q8, 0.0f);
-        }
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
+          for (int v = NV; v < 32; ++v) a[v] = 0.0f;
 #pragma unroll
-          for (int pass = 0; pass < NPASS; ++pass) {
-            if (off >= NV) sc[pass] = __fadd_rn(sc[pass], 0.0f);  // empty partial slots of the 32-slot tree
-            else sc[pass] = __fadd_rn(sc[pass], __shfl_xor_sync(0xFFFFFFFFu, sc[pass], off));
-          }
-        }
-        float* ss = SS + hh * kAttnBlock;
+          for (int off = 16; off >= 1; off >>= 1)
 #pragma unroll
-        for (int pass = 0; pass < NPASS; ++pass) {
-          const int jj = pass * PPI + lane / NV;
-          if (v == 0) ss[jj] = __fmul_rn(sc[pass], scale);
+            for (int i = 0; i < off; ++i) a[i] = __fadd_rn(a[i], a[i + off]);
+          sj = __fmul_rn(a[0], scale);
         }
-        __syncwarp();
-        // block maximum and weights e_j = exp(s_j - m_b): lane j holds e_j
-        const float sj = lane < nvalid ? ss[lane] : __int_as_float(0xFF800000);
+        // block maximum and weights e_j = exp(s_j - m_b), shared with the warp through SS
         float m = sj;
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-        const float e = lane < nvalid ? exp_c(__fsub_rn(sj, m)) : 0.0f;
+        float* se = SS + hh * kAttnBlock;
+        se[lane] = lane < nvalid ? exp_c(__fsub_rn(sj, m)) : 0.0f;
+        __syncwarp();
         // l = sequential sum of e_j; o = sequential fma chain over j
         float l = 0.0f, o[DPL];
 #pragma unroll
         for (int i = 0; i < DPL; ++i) o[i] = 0.0f;
+        const uint16_t* vcol = SV + lane * DPL;
+        for (int jb = 0; jb < nvalid; jb += 8) {
+          float vv[8][DPL], ee[8];
 #pragma unroll
-        for (int j = 0; j < kAttnBlock; ++j) {
-          const float ej = __shfl_sync(0xFFFFFFFFu, e, j);
-          if (j < nvalid) {
-            const uint16_t* vr = SV + (size_t)j * HD + lane * DPL;
-            l = __fadd_rn(l, ej);
+          for (int k = 0; k < 8; ++k) {
+            const int j = min(jb + k, nvalid - 1);
+            kv_dims_smem<KVDT, DPL>(vcol + (size_t)j * HD, vv[k]);
+            ee[k] = se[j];
+          }
 #pragma unroll
-            for (int i = 0; i < DPL; ++i) o[i] = fmaf(ej, kv_to_f32(vr[i], kvdt), o[i]);
+          for (int k = 0; k < 8; ++k) {
+            if (jb + k < nvalid) {
+              l = __fadd_rn(l, ee[k]);
+#pragma unroll
+              for (int i = 0; i < DPL; ++i) o[i] = fmaf(ee[k], vv[k][i], o[i]);
+            }
           }
         }
         if (cw == 0 && lane == 0 && it == (int)c) stamp(p, c, P.index, 6);
@@ -700,7 +727,7 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
         if (lane == 0) {
           // release: this warp's partials before the count; acquire: the merger sees every partial
           uint32_t old;
-          asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(head_ctr + g) : "memory");
+          asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(head_ctr + L * hkv + g) : "memory");
           if (old == (uint32_t)((h1 - h0) * nb - 1)) {
             const int k = atomicAdd(&ctl->n_done, 1);
             ctl->done[k] = g;
@@ -724,7 +751,7 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
     float* Wm = xbuf;                         // [gh][nbmax] block maxima, then weights w_b
     float* Wl = xbuf + kMaxGroup * nbmax;     // [gh][nbmax] block sums
     constexpr int T = kConsumerWarps * 32;
-    constexpr int kPre = 32;                  // blocks of each output prefetched before the syncs
+    constexpr int kPre = 16;                  // blocks of each output prefetched before the syncs
     const int n_out = gh * HD;
     float pre[2][kPre];
 #pragma unroll
@@ -740,12 +767,6 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
       const int hx = i / nb, bb = i % nb;
       Wm[hx * nbmax + bb] = __ldcg(part_m + (size_t)(h0 + hx) * nbmax + bb);
       Wl[hx * nbmax + bb] = __ldcg(part_l + (size_t)(h0 + hx) * nbmax + bb);
-    }
-    if (tid == 0) {
-      // rearm the group's counter before any merged output can be seen (the next layer's
-      // blocks depend on this output)
-      atomicExch(head_ctr + g, 0u);
-      __threadfence();
     }
     consumer_sync();
     if (cw < gh) {  // one warp per head: M = max_b m_b, then w_b = exp(m_b - M)
@@ -1013,9 +1034,15 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
     // ---- body
     if (cw == 0 && lane == 0) stamp(p, c, ph, 1);
     if (P.kind == PK_ATTN) {
-      if (p.hd == 128) attention_phase<128>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
-      else if (p.hd == 64) attention_phase<64>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
-      else attention_phase<256>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+      if (p.kvdt == DT_BF16) {
+        if (p.hd == 128) attention_phase<128, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+        else if (p.hd == 64) attention_phase<64, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+        else attention_phase<256, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+      } else {
+        if (p.hd == 128) attention_phase<128, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+        else if (p.hd == 64) attention_phase<64, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+        else attention_phase<256, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+      }
     } else if (P.kind == PK_SAMPLE) {
       if (st.temperature > 0.0f) sample_phase(p, ctl, st, c, G, cw, lane);
     } else if (P.kind == PK_EGU || P.kind == PK_EDOWN) {
@@ -1056,12 +1083,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                   int32_t xbuf_floats) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
-  float* xbuf = reinterpret_cast<float*>(smem + (size_t)kSlots * kSlotBytes);
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)kSlots * kSlotBytes + (((size_t)xbuf_floats * 4 + 127) & ~(size_t)127));
+  float* xbuf = reinterpret_cast<float*>(smem + (size_t)p.nslots * kSlotBytes);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + (size_t)p.nslots * kSlotBytes + (((size_t)xbuf_floats * 4 + 127) & ~(size_t)127));
   const uint32_t c = blockIdx.x, G = gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < p.nslots; ++s) {
       mbar_init(&ctl->full[s], 1);
       mbar_init(&ctl->empty[s], kConsumerWarps);
     }

@@ -54,6 +54,7 @@ struct adp_model {
   int G = 0;
   int xbuf_floats = 0;
   size_t smem = 0;
+  int max_nslots = 0;
   std::vector<PhaseDesc> phases;
   PhaseDesc* d_phases = nullptr;
   uint8_t* image = nullptr;
@@ -231,23 +232,37 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   // per-block weights: sized for the largest use that fits beside the ring.
   const int nbmax_ = (c.max_ctx + kAttnBlock - 1) / kAttnBlock;
   const size_t ctl_sz = (ctl_bytes() + 127) & ~(size_t)127;
-  const size_t budget = (size_t)prop.sharedMemPerBlockOptin - (size_t)kSlots * kSlotBytes - ctl_sz;
+  const size_t optin = (size_t)prop.sharedMemPerBlockOptin;
   int gmax = 0;  // most query heads sharing one KV head (floor(h * hkv / hq) grouping)
   for (int g = 0; g < c.n_kv_heads; ++g) {
     const int h0 = (g * hq + c.n_kv_heads - 1) / c.n_kv_heads, h1 = ((g + 1) * hq + c.n_kv_heads - 1) / c.n_kv_heads;
     gmax = std::max(gmax, h1 - h0);
   }
   if (gmax < 1 || gmax > kMaxGroup) return ADP_ERR_UNSUPPORTED_CONFIG;
-  const size_t item = (size_t)2 * kAttnBlock * hd * 2 + (size_t)kMaxGroup * kAttnBlock * 4;  // K, V, scores
-  const int att_slots = (int)std::min<size_t>(std::min(kAttnSlots, kConsumerWarps / gmax), budget / item);
-  if (att_slots < 1) return ADP_ERR_UNSUPPORTED_CONFIG;
-  size_t xbytes = (size_t)std::max(std::max(d, hq * hd), ffw) * 4;
-  xbytes = std::max(xbytes, (size_t)att_slots * item);
-  xbytes = std::max(xbytes, ((size_t)2 * 8 * nbmax_ + 8) * 4);
+  // K (rows padded by 16 bytes), V, the group's queries, the weights e_j
+  const size_t item = (size_t)kAttnBlock * (hd + 8) * 2 + (size_t)kAttnBlock * hd * 2 + (size_t)kMaxGroup * hd * 4 +
+                      (size_t)kMaxGroup * kAttnBlock * 4;
+  const size_t vec_bytes = std::max((size_t)std::max(std::max(d, hq * hd), ffw) * 4, ((size_t)2 * 8 * nbmax_ + 8) * 4);
+  // The deepest weight ring (kMaxSlots down to 3 slots) that leaves room for the input vector and
+  // one attention item; the attention slots then take the room that is left (at most one query
+  // head per consumer warp).
+  int nslots = 0, att_slots = 0;
+  size_t xbytes = 0;
+  for (int ns = kMaxSlots; ns >= 3 && !nslots; --ns) {
+    if ((size_t)ns * kSlotBytes + ctl_sz > optin) continue;
+    const size_t room = optin - (size_t)ns * kSlotBytes - ctl_sz;
+    if (room < vec_bytes || room < item) continue;
+    nslots = ns;
+    att_slots = (int)std::min<size_t>(std::min(kAttnSlots, kConsumerWarps / gmax), room / item);
+    xbytes = std::max(vec_bytes, (size_t)att_slots * item);
+  }
+  if (!nslots) return ADP_ERR_UNSUPPORTED_CONFIG;
   xbytes = (xbytes + 127) & ~(size_t)127;
   m->xbuf_floats = (int)(xbytes / 4);
-  m->smem = (size_t)kSlots * kSlotBytes + xbytes + ctl_bytes();
-  if (m->smem > (size_t)prop.sharedMemPerBlockOptin) return ADP_ERR_UNSUPPORTED_CONFIG;
+  m->smem = (size_t)nslots * kSlotBytes + xbytes + ctl_bytes();
+  if (m->smem > optin) return ADP_ERR_UNSUPPORTED_CONFIG;
+  m->p.nslots = nslots;
+  m->max_nslots = nslots;
   m->p.att_slots = att_slots;
   m->p.att_gmax = gmax;
   m->p.att_slot_bytes = (int)item;
@@ -343,7 +358,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
       (rc = m->alloc(&p.h, ffw)) || (rc = m->alloc(&p.rlog, std::max(c.n_experts, 1))) ||
       (rc = m->alloc(&p.knew, hkv * hd)) || (rc = m->alloc(&p.vnew, hkv * hd)) || (rc = m->alloc(&p.epoch, 1)) ||
       (rc = m->alloc(&p.part_m, (size_t)hq * nbmax)) || (rc = m->alloc(&p.part_l, (size_t)hq * nbmax)) ||
-      (rc = m->alloc(&p.part_o, (size_t)hq * nbmax * hd)) || (rc = m->alloc(&p.head_ctr, hq)) ||
+      (rc = m->alloc(&p.part_o, (size_t)hq * nbmax * hd)) || (rc = m->alloc(&p.head_ctr, (size_t)L * hkv)) ||
       (rc = m->alloc(&p.sblock, nblk)) || (rc = m->alloc(&p.sample_ctr, 1)) || (rc = m->alloc(&p.argkey, 1)) ||
       (rc = m->alloc(&p.lm_ctr, 1)) || (rc = m->alloc(&p.bar_ctr, 1)) || (rc = m->alloc(&p.err, 1)) ||
       (rc = m->alloc(&p.sel_out, (size_t)L * topk)) || (rc = m->alloc(&p.state, 1)) ||
@@ -357,7 +372,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   m->ll_bytes[5] = (size_t)hkv * hd * 8;
   m->ll_bytes[6] = (size_t)hkv * hd * 8;
   if ((rc = clear_exchange(m))) return rc;
-  CK(cudaMemsetAsync(p.head_ctr, 0, hq * 4, m->stream));
+  CK(cudaMemsetAsync(p.head_ctr, 0, (size_t)L * hkv * 4, m->stream));
   CK(cudaMemsetAsync(p.sample_ctr, 0, 4, m->stream));
   CK(cudaMemsetAsync(p.argkey, 0, 8, m->stream));
   CK(cudaMemsetAsync(p.lm_ctr, 0, 4, m->stream));
@@ -674,7 +689,7 @@ extern "C" int adp_reset(adp_model* m) {
   if (!m) return ADP_ERR_INVALID_ARG;
   cudaStreamSynchronize(m->stream);
   const Params& p = m->p;
-  CK(cudaMemsetAsync(p.head_ctr, 0, (size_t)m->cfg.n_heads * 4, m->stream));
+  CK(cudaMemsetAsync(p.head_ctr, 0, (size_t)m->cfg.n_layers * m->cfg.n_kv_heads * 4, m->stream));
   CK(cudaMemsetAsync(p.sample_ctr, 0, 4, m->stream));
   CK(cudaMemsetAsync(p.argkey, 0, 8, m->stream));
   CK(cudaMemsetAsync(p.lm_ctr, 0, 4, m->stream));
@@ -790,6 +805,15 @@ extern "C" int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes) {
   if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
   return ADP_OK;
 }
+
+extern "C" int adp_debug_set_ring_slots(adp_model* m, int32_t slots) {
+  if (!m || slots < 3 || slots > m->max_nslots) return ADP_ERR_INVALID_ARG;
+  m->p.nslots = slots;  // the shared-memory size stays the one chosen at creation
+  if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
+  return ADP_OK;
+}
+
+extern "C" int adp_debug_ring_slots(const adp_model* m) { return m ? m->p.nslots : 0; }
 
 extern "C" int adp_debug_set_wait_limit(adp_model* m, uint64_t ns) {
   if (!m || ns == 0) return ADP_ERR_INVALID_ARG;

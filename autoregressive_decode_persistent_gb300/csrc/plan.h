@@ -15,7 +15,7 @@ namespace adp {
 constexpr int kConsumerWarps = 15;                  // compute warps per CTA (16 warps in all: <= 128 registers)
 constexpr int kThreads = (kConsumerWarps + 1) * 32; // + one producer (TMA) warp
 constexpr int kSlotBytes = 32768;                   // one ring slot
-constexpr int kSlots = 4;                           // ring depth (128 KB in flight per SM)
+constexpr int kMaxSlots = 6;                        // ring depth limit (the model picks what fits)
 constexpr int kAttnBlock = 32;                      // positions per attention block (contract)
 constexpr int kVocabBlock = 256;                    // vocabulary entries per sampling block (contract)
 constexpr int kMaxTopK = 8;
@@ -110,7 +110,7 @@ struct Params {
   float* part_m;   // [hq][nbmax]
   float* part_l;   // [hq][nbmax]
   float* part_o;   // [hq][nbmax][hd]
-  uint32_t* head_ctr;          // [hkv] attention blocks finished per KV group
+  uint32_t* head_ctr;          // [L][hkv] attention blocks finished per KV group (cleared per step)
   float* sblock;               // [ceil(V/256)] sampling block sums
   uint32_t* sample_ctr;
   unsigned long long* argkey;  // packed (ordered logit, ~index) maximum
@@ -129,6 +129,7 @@ struct Params {
   uint64_t wait_ns;            // limit of every in-kernel wait
   uint32_t l2_lookahead;       // bytes of weight stream prefetched into L2 beyond the TMA loads
   int32_t debug_barriers;      // 1: also take a grid barrier after every phase (debugging)
+  int32_t nslots;              // weight ring depth (slots of kSlotBytes)
   int32_t skip_cta, skip_phase;  // test hook: that CTA does not publish that phase's outputs
 };
 

@@ -264,6 +264,7 @@ def write_timeline(path, model, kv, tok0, P, cfg):
         t = kv.step(t)
     adp.adp_debug_timeline(model.handle, None)
     tl = buf.view(G, nph, 8).cpu().numpy().astype(np.float64)
+    np.save(os.path.splitext(path)[0] + "_raw.npy", tl)
     names = {0: "qkv", 1: "attn", 2: "wo", 3: "gate_up", 4: "down", 5: "router", 6: "expert_gate_up",
              7: "expert_down", 8: "lm_head", 9: "sample"}
     kinds = [names[k] for k in _phase_kinds(cfg)]

@@ -195,6 +195,11 @@ int adp_debug_barriers(adp_model* m, int on);
  * loads (default 0 = off).  A tuning knob: it lets HBM keep streaming while the compute
  * warps wait at barriers. */
 int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes);
+/* Depth of the per-CTA weight ring in 32 KB slots: the model takes the deepest ring (at most 6)
+ * that fits beside its other shared-memory buffers; this lowers it (3 <= slots <= that depth,
+ * else ADP_ERR_INVALID_ARG), for measurements.  adp_debug_ring_slots reads the current depth. */
+int adp_debug_set_ring_slots(adp_model* m, int32_t slots);
+int adp_debug_ring_slots(const adp_model* m);
 /* Wait limit of every in-kernel spin (grid barrier, weight pipeline), nanoseconds (default 2e8). */
 int adp_debug_set_wait_limit(adp_model* m, uint64_t ns);
 /* Test hook: in the next step, CTA `cta` withholds the outputs of phase number `phase` (-1 = off),
