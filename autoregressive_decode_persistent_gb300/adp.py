@@ -75,6 +75,9 @@ _SIGS = [
     ("adp_kv_read", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]),
     ("adp_decode_step", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(Sampling),
                                        ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
+    ("adp_decode_step_noalloc", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                               ctypes.POINTER(Sampling), ctypes.POINTER(ctypes.c_int32),
+                                               ctypes.c_void_p]),
     ("adp_prefill", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                    ctypes.POINTER(Sampling), ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
     ("adp_generate_async", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
@@ -199,6 +202,14 @@ def adp_decode_step(model, kv, token: int, temperature: float = 0.0, u: float = 
     nxt = ctypes.c_int32()
     _check(load_library().adp_decode_step(model, kv, int(token), _sampling(temperature, u), ctypes.byref(nxt),
                                           _ptr(dev_logits)), "adp_decode_step")
+    return nxt.value
+
+
+def adp_decode_step_noalloc(model, kv, token: int, temperature: float = 0.0, u: float = 0.0,
+                            dev_logits=None) -> int:
+    nxt = ctypes.c_int32()
+    _check(load_library().adp_decode_step_noalloc(model, kv, int(token), _sampling(temperature, u),
+                                                  ctypes.byref(nxt), _ptr(dev_logits)), "adp_decode_step_noalloc")
     return nxt.value
 
 

@@ -17,6 +17,7 @@
 #include "../../include/adp.h"
 #include "launch.h"
 #include "plan.h"
+#include "scratch.h"
 
 using namespace adp;
 
@@ -719,6 +720,109 @@ extern "C" const char* adp_status_string(int status) {
 }
 
 extern "C" const char* adp_last_error(void) { return g_last_error.c_str(); }
+
+// ---------------------------------------------------------------- step in caller-given scratch
+
+void adp::set_last_error(const char* msg) { g_last_error = msg; }
+
+int adp::scratch_layout(const adp_model* m, ScratchLayout* out) {
+  if (!m || !out) return ADP_ERR_INVALID_ARG;
+  const adp_config& c = m->cfg;
+  const size_t d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim, L = c.n_layers;
+  const size_t ffw = c.n_experts ? (size_t)c.top_k * c.d_expert : (size_t)c.d_ff;
+  const size_t nbmax = ((size_t)c.max_ctx + kAttnBlock - 1) / kAttnBlock;
+  const size_t nblk = ((size_t)c.vocab + kVocabBlock - 1) / kVocabBlock;
+  const size_t topk = c.n_experts ? (size_t)c.top_k : 1;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = (off + std::max<size_t>(bytes, 16) + 255) & ~(size_t)255;
+    return at;
+  };
+  ScratchLayout& l = *out;
+  l.x = take(d * 8);
+  l.q = take(hq * hd * 8);
+  l.attn = take(hq * hd * 8);
+  l.h = take(ffw * 8);
+  l.rlog = take((size_t)std::max(c.n_experts, 1) * 8);
+  l.knew = take(hkv * hd * 8);
+  l.vnew = take(hkv * hd * 8);
+  l.epoch = take(4);
+  l.part_m = take(hq * nbmax * 4);
+  l.part_l = take(hq * nbmax * 4);
+  l.part_o = take(hq * nbmax * hd * 4);
+  l.head_ctr = take(L * hkv * 4);
+  l.sblock = take(nblk * 4);
+  l.sample_ctr = take(4);
+  l.argkey = take(8);
+  l.lm_ctr = take(4);
+  l.bar_ctr = take(8);
+  l.err = take(4);
+  l.sel_out = take(L * topk * 4);
+  l.state = take(sizeof(StepState));
+  l.logits = take((size_t)c.vocab * 4);
+  l.total = off;
+  return ADP_OK;
+}
+
+int adp::decode_step_in_scratch(adp_model* m, adp_kv* kv, int32_t token, const adp_sampling* sampling,
+                                int32_t* next_token, float* dev_logits, uint8_t* base, const ScratchLayout& lay,
+                                size_t zero_bytes, size_t clear_bytes) {
+  if (!m || !kv || !next_token || kv->m != m || !base) return ADP_ERR_INVALID_ARG;
+  if (m->sticky) return m->sticky;
+  if (token < 0 || token >= m->cfg.vocab) return ADP_ERR_INVALID_ARG;
+  if (kv->len >= m->cfg.max_ctx) return ADP_ERR_CONTEXT_OVERFLOW;
+  if (zero_bytes) CK(cudaMemsetAsync(base, 0, zero_bytes, m->stream));
+  const float T = sampling ? sampling->temperature : 0.0f;
+  StepState* d_state = reinterpret_cast<StepState*>(base + lay.state);
+  CK(cudaEventSynchronize(m->state_copied));
+  m->h_state->pos = kv->len;
+  m->h_state->token = token;
+  m->h_state->temperature = T;
+  m->h_state->u = sampling ? sampling->u : 0.0f;
+  m->h_state->seq_index = 0;
+  m->h_state->out_token = -1;
+  CK(cudaMemcpyAsync(d_state, m->h_state, sizeof(StepState), cudaMemcpyHostToDevice, m->stream));
+  CK(cudaEventRecord(m->state_copied, m->stream));
+  Params p = step_params(m, kv, dev_logits, nullptr, nullptr, nullptr);
+  auto at = [&](size_t o) { return base + o; };
+  p.x = reinterpret_cast<unsigned long long*>(at(lay.x));
+  p.q = reinterpret_cast<unsigned long long*>(at(lay.q));
+  p.attn = reinterpret_cast<unsigned long long*>(at(lay.attn));
+  p.h = reinterpret_cast<unsigned long long*>(at(lay.h));
+  p.rlog = reinterpret_cast<unsigned long long*>(at(lay.rlog));
+  p.knew = reinterpret_cast<unsigned long long*>(at(lay.knew));
+  p.vnew = reinterpret_cast<unsigned long long*>(at(lay.vnew));
+  p.epoch = reinterpret_cast<uint32_t*>(at(lay.epoch));
+  p.part_m = reinterpret_cast<float*>(at(lay.part_m));
+  p.part_l = reinterpret_cast<float*>(at(lay.part_l));
+  p.part_o = reinterpret_cast<float*>(at(lay.part_o));
+  p.head_ctr = reinterpret_cast<uint32_t*>(at(lay.head_ctr));
+  p.sblock = reinterpret_cast<float*>(at(lay.sblock));
+  p.sample_ctr = reinterpret_cast<uint32_t*>(at(lay.sample_ctr));
+  p.argkey = reinterpret_cast<unsigned long long*>(at(lay.argkey));
+  p.lm_ctr = reinterpret_cast<uint32_t*>(at(lay.lm_ctr));
+  p.bar_ctr = reinterpret_cast<unsigned long long*>(at(lay.bar_ctr));
+  p.err = reinterpret_cast<int32_t*>(at(lay.err));
+  p.sel_out = reinterpret_cast<int32_t*>(at(lay.sel_out));
+  p.state = d_state;
+  if (!dev_logits) p.logits = reinterpret_cast<float*>(at(lay.logits));
+  const int nph = (int)m->phases.size();
+  CK(decode_launch(p, 0, T > 0.0f ? nph : nph - 1, true, m->G, m->smem, m->xbuf_floats, m->stream));
+  CK(cudaMemcpyAsync(&m->h_out[0], &d_state->out_token, 4, cudaMemcpyDeviceToHost, m->stream));
+  CK(cudaMemcpyAsync(&m->h_out[1], p.err, 4, cudaMemcpyDeviceToHost, m->stream));
+  CK(cudaStreamSynchronize(m->stream));
+  const int rc = map_device_error(m->h_out[1]);
+  if (rc) {
+    // counters and exchange words may be left mid-step: start the area over from zero
+    CK(cudaMemsetAsync(base, 0, clear_bytes, m->stream));
+    CK(cudaStreamSynchronize(m->stream));
+    return rc;
+  }
+  *next_token = m->h_out[0];
+  kv->len += 1;
+  return ADP_OK;
+}
 
 extern "C" int adp_num_ctas(const adp_model* m, int32_t* ctas) {
   if (!m || !ctas) return ADP_ERR_INVALID_ARG;

@@ -1,0 +1,34 @@
+// Decode step with its scratch in caller-given device memory (engine.cu <-> noalloc.cu).
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/adp.h"
+
+namespace adp {
+
+// Byte offsets, in one scratch area, of everything a decode step writes besides the KV cache:
+// the epoch-tagged exchange vectors, the epoch base, the attention partials and counters, the
+// sampling and argmax words, the grid-barrier counter, the error word, the router choices, the
+// step state and the logits.  Each region starts at a multiple of 256 bytes.
+struct ScratchLayout {
+  size_t x, q, attn, h, rlog, knew, vnew, epoch, part_m, part_l, part_o, head_ctr, sblock, sample_ctr, argkey,
+      lm_ctr, bar_ctr, err, sel_out, state, logits;
+  size_t total;
+};
+
+// Layout for model m (host only, no CUDA call).  Returns ADP_ERR_INVALID_ARG for a null model.
+int scratch_layout(const adp_model* m, ScratchLayout* out);
+
+// adp_decode_step's work with the step's scratch at `base` (laid out as `lay`, all of it zero
+// before the model's first step there): one persistent launch on the model's stream, then a wait
+// for the result.  If zero_bytes > 0 the first `zero_bytes` bytes at base are cleared first.  On
+// a device-side error the first `clear_bytes` bytes are cleared before the error is returned.
+int decode_step_in_scratch(adp_model* m, adp_kv* kv, int32_t token, const adp_sampling* sampling,
+                           int32_t* next_token, float* dev_logits, uint8_t* base, const ScratchLayout& lay,
+                           size_t zero_bytes, size_t clear_bytes);
+
+// Record a message for adp_last_error().
+void set_last_error(const char* msg);
+
+}  // namespace adp

@@ -144,6 +144,33 @@ int adp_kv_read(const adp_kv* kv, void* host_k, void* host_v, int32_t len);
 int adp_decode_step(adp_model* m, adp_kv* kv, int32_t token, const adp_sampling* sampling,
                     int32_t* next_token, float* dev_logits);
 
+/* adp_decode_step without device allocation.  The persistent-decode method itself has no
+ * counterpart to this call: it changes only where the step keeps its scratch (the activation
+ * exchange words and their epoch base, the attention partials and counters, the sampling and
+ * argmax words, the grid-barrier counter, the error word, the step state and, when dev_logits is
+ * NULL, the logits).  These live in one static 8 MiB (8,388,608-byte) device array compiled into
+ * the library instead of in the model's own buffers, and the call makes no cudaMalloc/cudaFree or
+ * other allocating call.  It is meant for callers that may not allocate device memory while they
+ * decode: a process whose memory manager has already reserved the device's free memory for its
+ * own pool (a further allocation would fail or make the pool give memory back), or a serving loop
+ * that cannot take the device-wide synchronisation that cudaMalloc and cudaFree may cause.
+ * Arguments, results and the kernel are those of adp_decode_step (always the single persistent
+ * launch), with the same output; the model's own scratch is left untouched.
+ *  - The first call on a device sets up: with that device current it looks up the array's device
+ *    address (cudaGetSymbolAddress, which may make the CUDA runtime load the array's module).
+ *    Make that first call before any stream capture begins.  The model's device must be current.
+ *  - A model whose step needs more than 8 MiB of scratch (dominated by 4 * n_heads *
+ *    ceil(max_ctx / 32) * head_dim bytes of attention partials plus 4 * vocab bytes of logits) is
+ *    rejected with ADP_ERR_UNSUPPORTED_CONFIG before anything runs; adp_last_error() gives both sizes.
+ *  - Every call shares the array.  All of it must be zero before a model's first step in it: it
+ *    is at load, a completed step leaves it ready for the next one, and the call zeroes it first
+ *    when the previous call was for a model with another scratch layout or failed.  Calls that
+ *    overlap in time (from two threads, or on two streams) race on the array: serialise them.
+ *  - A device-side error (ADP_ERR_BARRIER_TIMEOUT / ADP_ERR_PIPELINE_TIMEOUT) is returned and the
+ *    array is zeroed; unlike adp_decode_step it does not leave the model in an error state. */
+int adp_decode_step_noalloc(adp_model* m, adp_kv* kv, int32_t token, const adp_sampling* sampling,
+                            int32_t* next_token, float* dev_logits);
+
 /* Prefill: n successive decode steps over HOST tokens[0..n) (positions len..len+n-1) through the
  * same kernel, so prompt-written and decode-written KV rows follow one arithmetic; returns the
  * next token after the last one (and its logits if dev_logits).  One host->device copy of the

@@ -1,0 +1,97 @@
+"""adp_decode_step_noalloc (the decode step with its scratch in the library's static array) against
+adp_decode_step (the model's own scratch), both called through the C ABI on identical KV caches.
+
+Same tolerances as the rest of the GPU tests: logits max-abs <= 2e-2, relative L2 <= 5e-3, and the
+same next token.  The file sorts last so that it also runs after every other GPU test; it passes
+alone in a fresh process too (the first call then does the per-device set-up)."""
+import numpy as np
+import pytest
+
+import synth
+
+from gpu_common import assert_logits_within_tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import torch
+    assert torch.cuda.is_available(), "a CUDA GPU is required"
+    from autoregressive_decode_persistent_gb300 import adp, build
+    build.build()
+    return adp
+
+
+def _pair(cfg, prompt_len):
+    """A model and two KV caches holding the same prompt (written by the model's own path)."""
+    from autoregressive_decode_persistent_gb300.model import DecodeModel
+    model = DecodeModel(cfg, synth.model_weights(cfg))
+    prompt = synth.prompt(cfg, prompt_len)
+    kv_ref, kv_na = model.new_kv(), model.new_kv()
+    t = kv_ref.prefill(prompt)
+    assert kv_na.prefill(prompt) == t
+    return model, kv_ref, kv_na, t
+
+
+def _both(adp, model, kv_ref, kv_na, token, temperature=0.0, u=0.0):
+    import torch
+    lg_ref = torch.empty(model.cfg["vocab"], device=model.device)
+    lg_na = torch.empty(model.cfg["vocab"], device=model.device)
+    t_ref = adp.adp_decode_step(model.handle, kv_ref.handle, token, temperature, u, lg_ref)
+    t_na = adp.adp_decode_step_noalloc(model.handle, kv_na.handle, token, temperature, u, lg_na)
+    assert t_na == t_ref
+    assert_logits_within_tolerance(lg_na.cpu().numpy()[None], lg_ref.cpu().numpy()[None].astype(np.float64))
+    return t_ref
+
+
+def test_two_calls_in_a_row_match_decode_step(lib):
+    import torch
+    cfg = synth.get_config("tiny")
+    model, kv_ref, kv_na, t = _pair(cfg, 12)
+    t = _both(lib, model, kv_ref, kv_na, t)  # first call (on a fresh process: also the set-up)
+    lg_ref = torch.empty(cfg["vocab"], device=model.device)
+    lg_na = torch.empty(cfg["vocab"], device=model.device)
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    t_na = lib.adp_decode_step_noalloc(model.handle, kv_na.handle, t, 0.0, 0.0, lg_na)
+    free_after = torch.cuda.mem_get_info()[0]
+    assert free_after == free_before, (free_before, free_after)  # the call allocated no device memory
+    t_ref = lib.adp_decode_step(model.handle, kv_ref.handle, t, 0.0, 0.0, lg_ref)
+    assert t_na == t_ref
+    assert_logits_within_tolerance(lg_na.cpu().numpy()[None], lg_ref.cpu().numpy()[None].astype(np.float64))
+    assert len(kv_na) == len(kv_ref) == 14
+    k1, v1 = kv_ref.read()
+    k2, v2 = kv_na.read()
+    assert np.array_equal(k1, k2) and np.array_equal(v1, v2)
+    # without a logits pointer the logits go to the static array; the token still matches
+    assert lib.adp_decode_step_noalloc(model.handle, kv_na.handle, t_na, 0.0, 0.0, None) == \
+        lib.adp_decode_step(model.handle, kv_ref.handle, t_ref, 0.0, 0.0, None)
+    model.close()
+
+
+def test_sampling_and_alternating_models(lib):
+    """Temperature sampling, and two models with different scratch layouts taking turns."""
+    a = _pair(synth.get_config("tiny"), 8)
+    b = _pair(synth.shrink(synth.get_config("dense-2.3b-fp16")), 8)
+    ta, tb = a[3], b[3]
+    for i in range(3):
+        ta = _both(lib, *a[:3], ta, 0.7, 0.25 + 0.2 * i)
+        tb = _both(lib, *b[:3], tb)
+    a[0].close()
+    b[0].close()
+
+
+def test_scratch_beyond_the_static_array_is_rejected(lib):
+    import torch
+    from autoregressive_decode_persistent_gb300.model import DecodeModel
+    cfg = synth.shrink(synth.get_config("tiny"), n_heads=32, n_kv_heads=4, max_ctx=40960)
+    model = DecodeModel(cfg, synth.model_weights(cfg))
+    kv = model.new_kv()
+    with pytest.raises(lib.AdpError) as e:
+        lib.adp_decode_step_noalloc(model.handle, kv.handle, 1, 0.0, 0.0, None)
+    assert e.value.code == lib.ADP_ERR_UNSUPPORTED_CONFIG
+    assert "static array" in lib.load_library().adp_last_error().decode()
+    assert len(kv) == 0
+    torch.cuda.synchronize()
+    model.close()
