@@ -65,7 +65,7 @@ __device__ __forceinline__ bool aborted(Ctl* ctl) { return *(volatile int32_t*)&
 
 // Timeline stamp k of phase ph for this CTA (debug hook; one thread writes each slot).
 __device__ __forceinline__ void stamp(const Params& p, uint32_t c, int ph, int k) {
-  if (p.timeline) p.timeline[((size_t)c * p.n_phases + ph) * 8 + k] = globaltimer();
+  if (p.timeline) p.timeline[((size_t)c * p.n_phases + ph) * kStamps + k] = globaltimer();
 }
 
 // Per-CTA share of a phase: units [u0, u0 + n).
@@ -160,7 +160,19 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
             if (p.timeline) blocked += globaltimer() - tb;
           }
         }
-        if (first) { stamp(p, c, ph, 4); first = false; }
+        if (first) {
+          stamp(p, c, ph, 4);
+          first = false;
+          if (P.kind == PK_GU && p.l2_burst) {
+            // the phase before the FFN waits on attention: let HBM fetch more of the FFN weights
+            // into L2 meanwhile than the ring holds
+            const uint64_t len = (uint64_t)n * unit_bytes;
+            const uint64_t lim = (uint64_t)ns * kSlotBytes + p.l2_burst;
+            const uint64_t end = len < lim ? len : lim;
+            for (uint64_t o = (uint64_t)ns * kSlotBytes; o < end; o += kL2Chunk)
+              prefetch_l2(base + o, end - o < kL2Chunk ? (uint32_t)(end - o) : kL2Chunk);
+          }
+        }
         mbar_arrive_expect_tx(&ctl->full[slot], bytes * P.slots);
         uint8_t* dst = ring + (size_t)slot * kSlotBytes;
         for (int s = 0; s < P.slots; ++s) {
@@ -173,7 +185,7 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
       }
     }
     stamp(p, c, ph, 5);
-    if (p.timeline) p.timeline[((size_t)c * p.n_phases + ph) * 8 + 7] = blocked;
+    if (p.timeline) p.timeline[((size_t)c * p.n_phases + ph) * kStamps + 7] = blocked;
   }
   // No bulk copy may still be writing this CTA's shared memory when it exits.
   int32_t never = 0;
@@ -369,6 +381,7 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
         if (lane == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
         __syncwarp();
       }
+      if (r == 0 && ck == 0 && cw == 0 && lane == 0) stamp(p, c, Pd.index, 8);
       if (active && !aborted(ctl)) {
         const int kck = min(KC, K - ck * KC);
         const int nvec = kck >> 3;
@@ -394,6 +407,7 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
       if (lane == 0) mbar_arrive(&ctl->empty[slot]);
       ++t;
     }
+    if (r == rounds - 1 && cw == 0 && lane == 0) stamp(p, c, Pd.index, 9);
     if (!active || aborted(ctl)) continue;
 #pragma unroll
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = warp_fold(acc[i]);
@@ -580,6 +594,41 @@ __device__ __forceinline__ void kv_dims_smem(const uint16_t* src, float (&f)[DPL
   }
 }
 
+// The K/V blocks of this CTA's attention items of layer L (the items the attention phase gives
+// it), prefetched into L2 while the layer's QKV phase runs: they do not depend on this step
+// except for the newest row, which the attention phase takes from the exchange words anyway.
+__device__ __forceinline__ void prefetch_attention_kv(const Params& p, int L, int ctx, uint32_t c, uint32_t G) {
+  const int nb = (ctx + kAttnBlock - 1) / kAttnBlock;
+  const int items = p.hkv * nb;
+  for (int it = (int)c; it < items; it += (int)G) {
+    const int g = it % p.hkv, b = it / p.hkv;
+    const int j0 = b * kAttnBlock;
+    const uint32_t bytes = (uint32_t)min(kAttnBlock, ctx - j0) * p.hd * 2;  // a multiple of 128
+    const size_t cache0 = (((size_t)L * p.hkv + g) * p.max_ctx + j0) * p.hd;
+    prefetch_l2(p.kc + cache0, bytes);
+    prefetch_l2(p.vc + cache0, bytes);
+  }
+}
+
+// Blocks [b0, nb) of one merged output: Ls += w_b l_b, O += w_b o_b in block order, the
+// partials loaded 16 blocks at a time.
+template <int HD>
+__device__ __forceinline__ void merge_tail(const float* w, const float* lsum, const float* src, int b0, int nb,
+                                           float& Ls, float& O) {
+  for (; b0 < nb; b0 += 16) {
+    float ob[16];
+#pragma unroll
+    for (int t2 = 0; t2 < 16; ++t2) ob[t2] = b0 + t2 < nb ? __ldcg(src + (size_t)(b0 + t2) * HD) : 0.0f;
+#pragma unroll
+    for (int t2 = 0; t2 < 16; ++t2) {
+      if (b0 + t2 < nb) {
+        Ls = fmaf(w[b0 + t2], lsum[b0 + t2], Ls);
+        O = fmaf(w[b0 + t2], ob[t2], O);
+      }
+    }
+  }
+}
+
 template <int HD, int KVDT>
 __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* xbuf, const PhaseDesc& P,
                                              const Step& st, uint32_t c, uint32_t G, int cw, int lane,
@@ -751,17 +800,17 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
     float* Wm = xbuf;                         // [gh][nbmax] block maxima, then weights w_b
     float* Wl = xbuf + kMaxGroup * nbmax;     // [gh][nbmax] block sums
     constexpr int T = kConsumerWarps * 32;
-    constexpr int kPre = 16;                  // blocks of each output prefetched before the syncs
+    constexpr int kPre = 32;                  // blocks of a thread's first two outputs loaded up front
     const int n_out = gh * HD;
+    // Every load of a context up to 32 blocks is issued here at once (one round trip to L2):
+    // the block partials of this thread's first two outputs, and the block maxima and sums.
     float pre[2][kPre];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int oi = tid + r * T;
-      if (oi < n_out) {
-        const float* src = part_o + (size_t)(h0 + oi / HD) * nbmax * HD + oi % HD;
+      const float* src = part_o + (size_t)(h0 + oi / HD) * nbmax * HD + oi % HD;
 #pragma unroll
-        for (int t2 = 0; t2 < kPre; ++t2) pre[r][t2] = t2 < nb ? __ldcg(src + (size_t)t2 * HD) : 0.0f;
-      }
+      for (int t2 = 0; t2 < kPre; ++t2) pre[r][t2] = (oi < n_out && t2 < nb) ? __ldcg(src + (size_t)t2 * HD) : 0.0f;
     }
     for (int i = tid; i < gh * nb; i += T) {
       const int hx = i / nb, bb = i % nb;
@@ -769,6 +818,7 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
       Wl[hx * nbmax + bb] = __ldcg(part_l + (size_t)(h0 + hx) * nbmax + bb);
     }
     consumer_sync();
+    if (tid == 0 && k == 0) stamp(p, c, P.index, 10);
     if (cw < gh) {  // one warp per head: M = max_b m_b, then w_b = exp(m_b - M)
       float M = __int_as_float(0xFF800000);
       for (int bb = lane; bb < nb; bb += 32) M = fmaxf(M, Wm[cw * nbmax + bb]);
@@ -777,6 +827,7 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
       for (int bb = lane; bb < nb; bb += 32) Wm[cw * nbmax + bb] = exp_c(__fsub_rn(Wm[cw * nbmax + bb], M));
     }
     consumer_sync();
+    // o_h = (sum_b w_b o_b) / (sum_b w_b l_b), both sums fused-multiply-added in block order
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int oi = tid + r * T;
@@ -784,7 +835,6 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
         const int hx = oi / HD, dd = oi % HD;
         const float* w = Wm + hx * nbmax;
         const float* lsum = Wl + hx * nbmax;
-        const float* src = part_o + (size_t)(h0 + hx) * nbmax * HD + dd;
         float Ls = 0.0f, O = 0.0f;
 #pragma unroll
         for (int t2 = 0; t2 < kPre; ++t2) {
@@ -793,22 +843,18 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
             O = fmaf(w[t2], pre[r][t2], O);
           }
         }
-        for (int b0 = kPre; b0 < nb; b0 += kPre) {
-          float ob[kPre];
-#pragma unroll
-          for (int t2 = 0; t2 < kPre; ++t2) ob[t2] = b0 + t2 < nb ? __ldcg(src + (size_t)(b0 + t2) * HD) : 0.0f;
-#pragma unroll
-          for (int t2 = 0; t2 < kPre; ++t2) {
-            if (b0 + t2 < nb) {
-              Ls = fmaf(w[b0 + t2], lsum[b0 + t2], Ls);
-              O = fmaf(w[b0 + t2], ob[t2], O);
-            }
-          }
-        }
+        merge_tail<HD>(w, lsum, part_o + (size_t)(h0 + hx) * nbmax * HD + dd, kPre, nb, Ls, O);
         ll_store(attn + (size_t)(h0 + hx) * HD + dd, ll_pack(__fdiv_rn(O, Ls), ew));
       }
     }
+    for (int oi = tid + 2 * T; oi < n_out; oi += T) {  // groups of more than 2 x 480 outputs
+      const int hx = oi / HD, dd = oi % HD;
+      float Ls = 0.0f, O = 0.0f;
+      merge_tail<HD>(Wm + hx * nbmax, Wl + hx * nbmax, part_o + (size_t)(h0 + hx) * nbmax * HD + dd, 0, nb, Ls, O);
+      ll_store(attn + (size_t)(h0 + hx) * HD + dd, ll_pack(__fdiv_rn(O, Ls), ew));
+    }
     consumer_sync();
+    if (tid == 0 && k == 0) stamp(p, c, P.index, 11);
   }
   if (tid == 0) ctl->n_done = 0;
   att_uses_io = att_uses;
@@ -972,6 +1018,7 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
           for (int i = a + tid; i < b; i += kConsumerWarps * 32)
             ll_store(p.x + i, ll_pack(load_elem(emb, (size_t)i, p.wdt), ew));
         }
+        if (cw == kConsumerWarps - 1 && lane == 0 && !ab) prefetch_attention_kv(p, L, st.pos + 1, c, G);
         if (n > 0) {
           const int half = p.hd / 2;  // the RoPE row of this position, for the epilogue
           if (tid < half) {

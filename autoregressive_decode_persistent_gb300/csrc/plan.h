@@ -21,7 +21,8 @@ constexpr int kVocabBlock = 256;                    // vocabulary entries per sa
 constexpr int kMaxTopK = 8;
 constexpr int kAttnSlots = 8;                       // attention items in flight per CTA (max)
 constexpr int kMaxGroup = 8;                        // query heads per KV head (max)
-constexpr int kChunkAlign = 256;                    // K-chunks start at multiples of 32 lanes x 8 elements
+constexpr int kChunkAlign = 256;
+constexpr int kStamps = 16;                         // timeline stamps per (CTA, phase)                    // K-chunks start at multiples of 32 lanes x 8 elements
 
 enum PhaseKind : int32_t {
   PK_QKV = 0,    // rmsnorm prologue; RoPE pairs of q/k, v; epilogue writes q and the KV rows
@@ -125,9 +126,10 @@ struct Params {
   const float* u_seq;          // uniform per step or null
   int32_t* out_seq;            // chosen token per step or null
   float* logits;               // [V] logits output
-  unsigned long long* timeline; // [G][n_phases][8] %globaltimer stamps or null
+  unsigned long long* timeline; // [G][n_phases][kStamps] %globaltimer stamps or null
   uint64_t wait_ns;            // limit of every in-kernel wait
   uint32_t l2_lookahead;       // bytes of weight stream prefetched into L2 beyond the TMA loads
+  uint32_t l2_burst;           // bytes of each FFN gate|up share prefetched into L2 when its first tile issues
   int32_t debug_barriers;      // 1: also take a grid barrier after every phase (debugging)
   int32_t nslots;              // weight ring depth (slots of kSlotBytes)
   int32_t skip_cta, skip_phase;  // test hook: that CTA does not publish that phase's outputs

@@ -167,6 +167,36 @@ def whole_job_rate(units_per_rank: int, seconds_max: float, world: int) -> float
     return world * units_per_rank / seconds_max
 
 
+def launch_ablation(model, kv, tok0, P, dev, n):
+    """The same device code as one launch per phase (plain stream, then a CUDA graph of those
+    launches) against the persistent launch, each through adp_decode_step for n steps (host
+    token in and out every step, as in e2e).  Gap per launch = extra time per step / extra launches."""
+    import torch
+    res = {}
+    for mode, name in ((0, "persistent"), (1, "multikernel"), (2, "graph")):
+        model.set_kernel_mode(mode)
+        kv.truncate(P)
+        t = tok0
+        for _ in range(3):  # warm-up (and, in mode 2, the graph capture)
+            t = kv.step(t)
+        kv.truncate(P)
+        t = tok0
+        torch.cuda.synchronize(dev)
+        h0 = time.perf_counter()
+        for _ in range(n):
+            t = kv.step(t)
+        el = time.perf_counter() - h0
+        res[name] = {"tokens_per_s": round(n / el, 2), "us_per_step": round(el / n * 1e6, 1),
+                     "launches_per_step": model.launches_per_step}
+    model.set_kernel_mode(0)
+    extra = res["multikernel"]["launches_per_step"] - 1
+    for name in ("multikernel", "graph"):
+        gap = (res[name]["us_per_step"] - res["persistent"]["us_per_step"]) / max(extra, 1)
+        res[name]["gap_us_per_extra_launch"] = round(gap, 3)
+    res["steps"] = n
+    return res
+
+
 def run_engine(args, rank: int, world: int):
     import torch
 
@@ -247,6 +277,8 @@ def run_engine(args, rank: int, world: int):
     ms, e2e_s = max_over_ranks([ms, h1 - h0], world)
     e2e = whole_job_rate(n_e2e, e2e_s, world)
 
+    ablation = launch_ablation(model, kv, tok0, P, dev, args.ablation_steps) if args.ablation_steps else None
+
     if args.timeline:
         write_timeline(args.timeline, model, kv, tok0, P, cfg)
 
@@ -254,7 +286,7 @@ def run_engine(args, rank: int, world: int):
         "ms": ms, "steps": args.steps, "achieved_gbs": achieved, "per_launch_bytes": per_launch,
         "launch_ms": launch_ms, "peak": peak, "peak_kind": peak_kind, "e2e": e2e, "n_e2e": n_e2e,
         "clocks": clocks.summary(), "ctas": model.num_ctas, "image_bytes": model.image_bytes,
-        "launches": model.launches_per_step * args.steps,
+        "launches": model.launches_per_step * args.steps, "ablation": ablation,
     }
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu"] = cpu_baseline(cfg, W, seconds=args.cpu_seconds)[0]
@@ -269,14 +301,14 @@ def write_timeline(path, model, kv, tok0, P, cfg):
     import torch
     from autoregressive_decode_persistent_gb300 import adp
     G, nph = adp.adp_debug_timeline_shape(model.handle)
-    buf = torch.zeros(G * nph * 8, dtype=torch.int64, device=model.device)  # zero = no stamp
+    buf = torch.zeros(G * nph * 16, dtype=torch.int64, device=model.device)  # zero = no stamp
     adp.adp_debug_timeline(model.handle, buf)
     kv.truncate(P)
     t = tok0
     for _ in range(4):
         t = kv.step(t)
     adp.adp_debug_timeline(model.handle, None)
-    tl = buf.view(G, nph, 8).cpu().numpy().astype(np.float64)
+    tl = buf.view(G, nph, 16).cpu().numpy().astype(np.float64)
     np.save(os.path.splitext(path)[0] + "_raw.npy", tl)
     names = {0: "qkv", 1: "attn", 2: "wo", 3: "gate_up", 4: "down", 5: "router", 6: "expert_gate_up",
              7: "expert_down", 8: "lm_head", 9: "sample"}
@@ -377,6 +409,8 @@ def emit_engine(args, cfg, res, world):
         "clocks": res["clocks"],
         "kernel_source": src,
     }
+    if res.get("ablation"):
+        line["launch_ablation"] = res["ablation"]
     if "cpu" in res:
         line["cpu_baseline"] = res["cpu"]
     print(json.dumps(line), flush=True)
@@ -423,6 +457,8 @@ def main():
     ap.add_argument("--impl", choices=["engine", "reference"], default="engine")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ablation-steps", type=int, default=64,
+                    help="steps of the one-launch-per-phase ablation (0 = skip)")
     ap.add_argument("--timeline", default=None, help="write a per-phase breakdown of one step (JSON) here")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: use this many layers of the workload's shape (the line says so)")

@@ -210,9 +210,12 @@ int adp_debug_read_experts(const adp_model* m, int32_t* host_idx);
 /* Record the residual entering each layer (and the final one) of every step into a DEVICE
  * buffer [n_layers + 1][d_model] fp32 (NULL = off). */
 int adp_debug_trace_residual(adp_model* m, float* dev_buf);
-/* Per-phase timeline of every CTA: DEVICE buffer [ctas][phases][8] of %globaltimer stamps (ns):
+/* Per-phase timeline of every CTA: DEVICE buffer [ctas][phases][16] of %globaltimer stamps (ns):
  * 0 phase entry, 1 after the prologue, 2 after the phase body, 3 after the grid barrier (consumer
- * warp 0), 4 first and 5 last weight tile issued (producer warp).  NULL = off.  Sizes from
+ * warp 0), 4 first and 5 last weight tile issued (producer warp), 7 ns the producer spent with
+ * the ring full; weighted phases: 8 first tile ready and 9 last K-chunk done (consumer warp 0);
+ * attention: 4 first item's data staged, 6 its block computed, 5 its partial published, 7 all
+ * items done, 10 first merge's partials loaded, 11 its outputs published.  Unused entries keep what the buffer held.  NULL = off.  Sizes from
  * adp_debug_timeline_shape. */
 int adp_debug_timeline(adp_model* m, uint64_t* dev_buf);
 int adp_debug_timeline_shape(const adp_model* m, int32_t* ctas, int32_t* phases);
@@ -222,6 +225,10 @@ int adp_debug_barriers(adp_model* m, int on);
  * loads (default 0 = off).  A tuning knob: it lets HBM keep streaming while the compute
  * warps wait at barriers. */
 int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes);
+/* Bytes of each CTA's FFN gate|up share (beyond what the weight ring holds) that the producer
+ * warp prefetches into L2 when it issues the phase's first tile, so that HBM keeps streaming
+ * while the attention and Wo phases wait on their inputs (default 0 = off). */
+int adp_debug_set_l2_burst(adp_model* m, uint32_t bytes);
 /* Depth of the per-CTA weight ring in 32 KB slots: the model takes the deepest ring (at most 6)
  * that fits beside its other shared-memory buffers; this lowers it (3 <= slots <= that depth,
  * else ADP_ERR_INVALID_ARG), for measurements.  adp_debug_ring_slots reads the current depth. */
