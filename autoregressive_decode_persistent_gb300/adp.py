@@ -98,7 +98,6 @@ _SIGS = [
                                                 ctypes.POINTER(ctypes.c_int32)]),
     ("adp_debug_barriers", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     ("adp_debug_set_l2_lookahead", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
-    ("adp_debug_set_l2_burst", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
     ("adp_debug_set_ring_slots", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     ("adp_debug_ring_slots", ctypes.c_int, [ctypes.c_void_p]),
     ("adp_debug_set_wait_limit", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64]),
@@ -289,10 +288,6 @@ def adp_debug_barriers(model, on: bool):
 
 def adp_debug_set_l2_lookahead(model, nbytes: int):
     _check(load_library().adp_debug_set_l2_lookahead(model, int(nbytes)), "adp_debug_set_l2_lookahead")
-
-
-def adp_debug_set_l2_burst(model, nbytes: int):
-    _check(load_library().adp_debug_set_l2_burst(model, int(nbytes)), "adp_debug_set_l2_burst")
 
 
 def adp_debug_set_ring_slots(model, slots: int):

@@ -163,15 +163,6 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
         if (first) {
           stamp(p, c, ph, 4);
           first = false;
-          if (P.kind == PK_GU && p.l2_burst) {
-            // the phase before the FFN waits on attention: let HBM fetch more of the FFN weights
-            // into L2 meanwhile than the ring holds
-            const uint64_t len = (uint64_t)n * unit_bytes;
-            const uint64_t lim = (uint64_t)ns * kSlotBytes + p.l2_burst;
-            const uint64_t end = len < lim ? len : lim;
-            for (uint64_t o = (uint64_t)ns * kSlotBytes; o < end; o += kL2Chunk)
-              prefetch_l2(base + o, end - o < kL2Chunk ? (uint32_t)(end - o) : kL2Chunk);
-          }
         }
         mbar_arrive_expect_tx(&ctl->full[slot], bytes * P.slots);
         uint8_t* dst = ring + (size_t)slot * kSlotBytes;
@@ -352,7 +343,7 @@ __device__ void select_experts(const Params& p, Ctl* ctl, int layer, uint32_t r_
 // ---------------------------------------------------------------- GEMV phases
 
 template <int ROWS, int SLOTS, int WDT, bool XPERSLOT>
-__device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, const PhaseDesc& Pd,
+__device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, const PhaseDesc& Pd,
                                         const Step& st, uint32_t c, uint32_t G, int cw, int lane, uint32_t& t_io,
                                         uint32_t ew) {
   // every field the loops use lives in registers (the descriptors are in local memory, and each
@@ -366,6 +357,7 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
   int32_t u0, n;
   cta_units(Pd, c, G, u0, n);
   unsigned long long best = 0ull;  // LM: packed running maximum of this warp
+  long long cyc_wait = 0, cyc_comp = 0;  // timeline: SM cycles waiting for tiles / computing
   const int rounds = n > 0 ? (n + upr - 1) / upr : 0;
   for (int r = 0; r < rounds; ++r) {
     const int m = min(upr, n - r * upr);
@@ -376,7 +368,10 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = 0.0f;
     for (int ck = 0; ck < n_chunks; ++ck) {
       const uint32_t slot = t % ns, use = t / ns;
+      const long long cy0 = clock64();
       bool ok = aborted(ctl) || mbar_wait(&ctl->full[slot], use & 1, &ctl->abort, wait_ns);
+      const long long cy1 = clock64();
+      cyc_wait += cy1 - cy0;
       if (!ok) {
         if (lane == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
         __syncwarp();
@@ -403,11 +398,18 @@ __device__ __noinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* ring
           }
         }
       }
+      cyc_comp += clock64() - cy1;
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->empty[slot]);
       ++t;
     }
-    if (r == rounds - 1 && cw == 0 && lane == 0) stamp(p, c, Pd.index, 9);
+    if (r == rounds - 1 && cw == 0 && lane == 0) {
+      stamp(p, c, Pd.index, 9);
+      if (p.timeline) {
+        p.timeline[((size_t)c * p.n_phases + Pd.index) * kStamps + 12] = (unsigned long long)cyc_wait;
+        p.timeline[((size_t)c * p.n_phases + Pd.index) * kStamps + 13] = (unsigned long long)cyc_comp;
+      }
+    }
     if (!active || aborted(ctl)) continue;
 #pragma unroll
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = warp_fold(acc[i]);
@@ -630,7 +632,7 @@ __device__ __forceinline__ void merge_tail(const float* w, const float* lsum, co
 }
 
 template <int HD, int KVDT>
-__device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* xbuf, const PhaseDesc& P,
+__device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float* xbuf, const PhaseDesc& P,
                                              const Step& st, uint32_t c, uint32_t G, int cw, int lane,
                                              uint32_t& att_uses_io, uint32_t ew) {
   constexpr int NV = HD / 8;         // 8-element vectors per K row (partial sums of the contract dot)
@@ -862,7 +864,7 @@ __device__ __noinline__ void attention_phase(const Params& p, Ctl* ctl, float* x
 
 // ---------------------------------------------------------------- sampling phase
 
-__device__ __noinline__ void sample_phase(const Params& p, Ctl* ctl, const Step& st, uint32_t c, uint32_t G, int cw, int lane) {
+__device__ __forceinline__ void sample_phase(const Params& p, Ctl* ctl, const Step& st, uint32_t c, uint32_t G, int cw, int lane) {
   const unsigned long long key = __ldcg(p.argkey);
   const float M = order_float((uint32_t)(key >> 32));
   const float T = st.temperature;

@@ -406,7 +406,6 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   p.rope_sin = d_sin;
   p.wait_ns = 200000000ull;
   p.l2_lookahead = 0;
-  p.l2_burst = 0;
   p.skip_cta = -1;
   p.skip_phase = -1;
   CK(cudaStreamSynchronize(m->stream));
@@ -907,13 +906,6 @@ extern "C" int adp_debug_barriers(adp_model* m, int on) {
 extern "C" int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes) {
   if (!m) return ADP_ERR_INVALID_ARG;
   m->p.l2_lookahead = bytes;
-  if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
-  return ADP_OK;
-}
-
-extern "C" int adp_debug_set_l2_burst(adp_model* m, uint32_t bytes) {
-  if (!m) return ADP_ERR_INVALID_ARG;
-  m->p.l2_burst = bytes & ~15u;
   if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
   return ADP_OK;
 }

@@ -129,7 +129,6 @@ struct Params {
   unsigned long long* timeline; // [G][n_phases][kStamps] %globaltimer stamps or null
   uint64_t wait_ns;            // limit of every in-kernel wait
   uint32_t l2_lookahead;       // bytes of weight stream prefetched into L2 beyond the TMA loads
-  uint32_t l2_burst;           // bytes of each FFN gate|up share prefetched into L2 when its first tile issues
   int32_t debug_barriers;      // 1: also take a grid barrier after every phase (debugging)
   int32_t nslots;              // weight ring depth (slots of kSlotBytes)
   int32_t skip_cta, skip_phase;  // test hook: that CTA does not publish that phase's outputs

@@ -225,10 +225,6 @@ int adp_debug_barriers(adp_model* m, int on);
  * loads (default 0 = off).  A tuning knob: it lets HBM keep streaming while the compute
  * warps wait at barriers. */
 int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes);
-/* Bytes of each CTA's FFN gate|up share (beyond what the weight ring holds) that the producer
- * warp prefetches into L2 when it issues the phase's first tile, so that HBM keeps streaming
- * while the attention and Wo phases wait on their inputs (default 0 = off). */
-int adp_debug_set_l2_burst(adp_model* m, uint32_t bytes);
 /* Depth of the per-CTA weight ring in 32 KB slots: the model takes the deepest ring (at most 6)
  * that fits beside its other shared-memory buffers; this lowers it (3 <= slots <= that depth,
  * else ADP_ERR_INVALID_ARG), for measurements.  adp_debug_ring_slots reads the current depth. */
