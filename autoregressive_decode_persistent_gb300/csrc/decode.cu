@@ -192,6 +192,23 @@ __device__ __forceinline__ void load_x8(const float* xs, float (&x)[8]) {
   x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
+// A GEMV input vector sits in shared memory in a split layout, so that 32 lanes reading 32
+// consecutive 8-element vectors hit every bank once per 16-byte load: element e (0..7) of vector
+// v is stored at (v / 32) * 256 + (e / 4) * 128 + (v % 32) * 4 + e % 4.  Vectors of n elements
+// take n rounded up to a multiple of 256 floats.
+__device__ __forceinline__ int xpos(int i) {
+  const int v = i >> 3, e = i & 7;
+  return ((v >> 5) << 8) + ((e >> 2) << 7) + ((v & 31) << 2) + (e & 3);
+}
+
+__device__ __forceinline__ void load_xs8(const float* xb, int v, float (&x)[8]) {
+  const float* a = xb + ((v >> 5) << 8) + ((v & 31) << 2);
+  const float4 lo = *reinterpret_cast<const float4*>(a);
+  const float4 hi = *reinterpret_cast<const float4*>(a + 128);
+  x[0] = lo.x; x[1] = lo.y; x[2] = lo.z; x[3] = lo.w;
+  x[4] = hi.x; x[5] = hi.y; x[6] = hi.z; x[7] = hi.w;
+}
+
 __device__ __forceinline__ void ldcg_x8(const float* g, float (&x)[8]) {
   const float4 a = __ldcg(reinterpret_cast<const float4*>(g));
   const float4 b = __ldcg(reinterpret_cast<const float4*>(g) + 1);
@@ -219,9 +236,11 @@ __device__ __forceinline__ bool ll_wait(const ll_t* src, uint32_t epoch, ll_t& w
   }
 }
 
-// dst[0..n) = the values of src[0..n) once each carries `epoch` (all consumer threads, eight
-// loads in flight per thread; ends with consumer_sync).
-__device__ void ll_fetch(const Params& p, Ctl* ctl, float* dst, const ll_t* src, int n, uint32_t epoch, int tid) {
+// The values of src[0..n) once each carries `epoch`, into dst in the split layout: n/seg vectors
+// of seg elements, each taking segp floats (all consumer threads, eight loads in flight per
+// thread; ends with consumer_sync).
+__device__ void ll_fetch(const Params& p, Ctl* ctl, float* dst, const ll_t* src, int n, int seg, int segp,
+                         uint32_t epoch, int tid) {
   constexpr int B = 8, T = kConsumerWarps * 32;
   for (int base = tid; base < n; base += B * T) {
     ll_t w[B];
@@ -233,7 +252,19 @@ __device__ void ll_fetch(const Params& p, Ctl* ctl, float* dst, const ll_t* src,
 #pragma unroll
     for (int k = 0; k < B; ++k) {
       const int i = base + k * T;
-      if (i < n && ll_wait(src + i, epoch, w[k], p, ctl)) dst[i] = ll_value(w[k]);
+      if (i < n) {
+        if (ll_epoch(w[k]) != epoch) {
+          if (!ll_wait(src + i, epoch, w[k], p, ctl)) break;
+          // the later words of the batch were loaded before this one arrived: reload those
+          // still behind together, so the batch costs one more round trip, not one per word
+#pragma unroll
+          for (int j = k + 1; j < B; ++j) {
+            const int ij = base + j * T;
+            if (ij < n && ll_epoch(w[j]) != epoch) w[j] = ll_load(src + ij);
+          }
+        }
+        dst[seg == n ? xpos(i) : (i / seg) * segp + xpos(i % seg)] = ll_value(w[k]);
+      }
     }
   }
   consumer_sync();
@@ -253,18 +284,18 @@ __device__ void rmsnorm_prologue(const Params& p, Ctl* ctl, float* xbuf, const v
     gr[k] = i < d ? __ldg(reinterpret_cast<const unsigned short*>(gain) + i) : (uint16_t)0;
   }
   if (emb_row) {
-    for (int i = tid; i < d; i += T) xbuf[i] = load_elem(emb_row, (size_t)i, p.wdt);
+    for (int i = tid; i < d; i += T) xbuf[xpos(i)] = load_elem(emb_row, (size_t)i, p.wdt);
     consumer_sync();
   } else {
-    ll_fetch(p, ctl, xbuf, p.x, d, x_epoch, tid);
+    ll_fetch(p, ctl, xbuf, p.x, d, d, 0, x_epoch, tid);
   }
   if (p.trace && c == 0 && trace_layer >= 0)
-    for (int i = tid; i < d; i += T) p.trace[(size_t)trace_layer * d + i] = xbuf[i];
+    for (int i = tid; i < d; i += T) p.trace[(size_t)trace_layer * d + i] = xbuf[xpos(i)];
   if (cw == 0) {
     float acc = 0.0f;
     for (int v = lane; v < d / 8; v += 32) {
       float x8[8];
-      load_x8(xbuf + v * 8, x8);
+      load_xs8(xbuf, v, x8);
       acc = fma8(x8, x8, acc);
     }
     const float ss = warp_fold(acc);
@@ -279,7 +310,7 @@ __device__ void rmsnorm_prologue(const Params& p, Ctl* ctl, float* xbuf, const v
     const int i = tid + k * T;
     if (i < d) {
       const float g = p.wdt == DT_BF16 ? bf16_bits_to_f32(gr[k]) : __half2float(__ushort_as_half(gr[k]));
-      xbuf[i] = __fmul_rn(__fmul_rn(xbuf[i], r), g);
+      xbuf[xpos(i)] = __fmul_rn(__fmul_rn(xbuf[xpos(i)], r), g);
     }
   }
   consumer_sync();
@@ -350,15 +381,18 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
   // mbarrier asm statement would otherwise force them to be reloaded)
   constexpr int EB = WDT == DT_E4M3 ? 1 : 2;
   const int kind = Pd.kind, L = Pd.layer, K = Pd.K, KC = Pd.KC, n_chunks = Pd.n_chunks, upr = Pd.upr;
+  const int Kp = (K + 255) & ~255;  // floats per input vector in the split layout
   const int pos = st.pos;
   const uint64_t wait_ns = p.wait_ns;
   const uint32_t ns = (uint32_t)p.nslots;
   uint32_t t = t_io;
+  uint32_t slot = t % ns, par = (t / ns) & 1u;  // ring slot of tile t and the parity of its use
   int32_t u0, n;
   cta_units(Pd, c, G, u0, n);
   unsigned long long best = 0ull;  // LM: packed running maximum of this warp
-  long long cyc_wait = 0, cyc_comp = 0;  // timeline: SM cycles waiting for tiles / computing
+  long long cyc_wait = 0, cyc_comp = 0, cyc_epi = 0;  // timeline: SM cycles waiting / computing / epilogues
   const int rounds = n > 0 ? (n + upr - 1) / upr : 0;
+  const long long cyc_start = clock64();
   for (int r = 0; r < rounds; ++r) {
     const int m = min(upr, n - r * upr);
     const bool active = cw < m;
@@ -367,9 +401,8 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
 #pragma unroll
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = 0.0f;
     for (int ck = 0; ck < n_chunks; ++ck) {
-      const uint32_t slot = t % ns, use = t / ns;
       const long long cy0 = clock64();
-      bool ok = aborted(ctl) || mbar_wait(&ctl->full[slot], use & 1, &ctl->abort, wait_ns);
+      bool ok = aborted(ctl) || mbar_wait(&ctl->full[slot], par, &ctl->abort, wait_ns);
       const long long cy1 = clock64();
       cyc_wait += cy1 - cy0;
       if (!ok) {
@@ -385,10 +418,10 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
         const int xoff = ck * KC;
         for (int v = lane; v < nvec; v += 32) {
           float x8[8];
-          if (!XPERSLOT) load_x8(xbuf + xoff + v * 8, x8);
+          if (!XPERSLOT) load_xs8(xbuf, (xoff >> 3) + v, x8);
 #pragma unroll
           for (int s = 0; s < SLOTS; ++s) {
-            if (XPERSLOT) load_x8(xbuf + s * K + xoff + v * 8, x8);
+            if (XPERSLOT) load_xs8(xbuf + s * Kp, (xoff >> 3) + v, x8);
 #pragma unroll
             for (int j = 0; j < ROWS; ++j) {
               float w8[8];
@@ -402,6 +435,10 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->empty[slot]);
       ++t;
+      if (++slot == ns) {
+        slot = 0;
+        par ^= 1u;
+      }
     }
     if (r == rounds - 1 && cw == 0 && lane == 0) {
       stamp(p, c, Pd.index, 9);
@@ -410,6 +447,7 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
         p.timeline[((size_t)c * p.n_phases + Pd.index) * kStamps + 13] = (unsigned long long)cyc_comp;
       }
     }
+    const long long ce0 = clock64();
     if (!active || aborted(ctl)) continue;
 #pragma unroll
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = warp_fold(acc[i]);
@@ -501,6 +539,11 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
         }
       }
     }
+    cyc_epi += clock64() - ce0;
+  }
+  if (p.timeline && cw == 0 && lane == 0 && rounds > 0) {
+    p.timeline[((size_t)c * p.n_phases + Pd.index) * kStamps + 14] = (unsigned long long)(clock64() - cyc_start);
+    p.timeline[((size_t)c * p.n_phases + Pd.index) * kStamps + 15] = (unsigned long long)cyc_epi;
   }
   if (kind == PK_LM) {
     if (lane == 0) ctl->red_k[cw] = best;
@@ -698,8 +741,15 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
 #pragma unroll
         for (int i = 0; i < DPL; ++i) w[i] = ll_load(qs + lane + 32 * i);
 #pragma unroll
-        for (int i = 0; i < DPL; ++i)
-          sq[lane + 32 * i] = ll_wait(qs + lane + 32 * i, qe, w[i], p, ctl) ? ll_value(w[i]) : 0.0f;
+        for (int i = 0; i < DPL; ++i) {
+          if (ll_epoch(w[i]) != qe) {
+            if (!ll_wait(qs + lane + 32 * i, qe, w[i], p, ctl)) break;
+#pragma unroll
+            for (int j = i + 1; j < DPL; ++j)  // reload the rest together (see ll_fetch)
+              if (ll_epoch(w[j]) != qe) w[j] = ll_load(qs + lane + 32 * j);
+          }
+          sq[lane + 32 * i] = ll_value(w[i]);
+        }
       }
       bool ok = mbar_wait(&ctl->att_bar[slot], att_uses & 1, &ctl->abort, wait_ns);
       ++att_uses;
@@ -708,10 +758,21 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
         // the block holding this step's position: its K/V row comes from the tagged copies
         // (the cache row may not have landed when the bulk copy read it)
         const int jr = ctx - 1 - j0;
-        for (int i = lane; i < HD; i += 32) {
-          ll_t wk = ll_load(knew + (size_t)g * HD + i), wv = ll_load(vnew + (size_t)g * HD + i);
-          if (ll_wait(knew + (size_t)g * HD + i, qe, wk, p, ctl)) SK[(size_t)jr * KSTR + i] = (uint16_t)wk;
-          if (ll_wait(vnew + (size_t)g * HD + i, qe, wv, p, ctl)) SV[(size_t)jr * HD + i] = (uint16_t)wv;
+        const ll_t* kn = knew + (size_t)g * HD + lane;
+        const ll_t* vn = vnew + (size_t)g * HD + lane;
+        ll_t w[2 * DPL];  // K words, then V words
+#pragma unroll
+        for (int i = 0; i < 2 * DPL; ++i) w[i] = ll_load(i < DPL ? kn + 32 * i : vn + 32 * (i - DPL));
+#pragma unroll
+        for (int i = 0; i < 2 * DPL; ++i) {
+          if (ll_epoch(w[i]) != qe) {
+            if (!ll_wait(i < DPL ? kn + 32 * i : vn + 32 * (i - DPL), qe, w[i], p, ctl)) break;
+#pragma unroll
+            for (int j = i + 1; j < 2 * DPL; ++j)  // reload the rest together (see ll_fetch)
+              if (ll_epoch(w[j]) != qe) w[j] = ll_load(j < DPL ? kn + 32 * j : vn + 32 * (j - DPL));
+          }
+          if (i < DPL) SK[(size_t)jr * KSTR + lane + 32 * i] = (uint16_t)w[i];
+          else SV[(size_t)jr * HD + lane + 32 * (i - DPL)] = (uint16_t)w[i];
         }
       }
       asm volatile("bar.sync %0, %1;" ::"r"(2 + slot), "r"(gmax * 32) : "memory");
@@ -989,6 +1050,7 @@ __device__ void run_expert(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf
     gemv_phase<1, SLOTS, DT_E4M3, true>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
 }
 
+template <bool MOE>
 __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, const Step& st, uint32_t c,
                          uint32_t G, int ph0, int ph1, bool use_barrier, int cw, int lane) {
   uint32_t t = 0;
@@ -1034,47 +1096,50 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
       case PK_WO:
         if (n > 0) {
           stage_residual(p, ctl, P, c, G, 2, e_res, cw, lane);
-          ll_fetch(p, ctl, xbuf, p.attn, p.hq * p.hd, e_src, tid);
+          ll_fetch(p, ctl, xbuf, p.attn, p.hq * p.hd, p.hq * p.hd, 0, e_src, tid);
         }
         break;
       case PK_DOWN:
         if (n > 0) {
           stage_residual(p, ctl, P, c, G, 2, e_res, cw, lane);
-          ll_fetch(p, ctl, xbuf, p.h, p.ff, e_src, tid);
+          ll_fetch(p, ctl, xbuf, p.h, p.ff, p.ff, 0, e_src, tid);
         }
         break;
       case PK_EDOWN:
-        if (sel_layer != L) {
-          if (cw == 0) {
-            select_experts(p, ctl, L, e_sel, lane);
-            if (lane == 0) mbar_arrive(&ctl->sel_bar);
+        if constexpr (MOE) {
+          if (sel_layer != L) {
+            if (cw == 0) {
+              select_experts(p, ctl, L, e_sel, lane);
+              if (lane == 0) mbar_arrive(&ctl->sel_bar);
+            }
+            sel_layer = L;
           }
-          sel_layer = L;
-        }
-        if (n > 0) {
-          stage_residual(p, ctl, P, c, G, 1, e_res, cw, lane);
-          ll_fetch(p, ctl, xbuf, p.h, p.topk * p.fexp, e_src, tid);
-        } else {
-          consumer_sync();  // the choice (shared memory) is read by every warp's epilogue
+          if (n > 0) {
+            stage_residual(p, ctl, P, c, G, 1, e_res, cw, lane);
+            ll_fetch(p, ctl, xbuf, p.h, p.topk * p.fexp, p.fexp, (p.fexp + 255) & ~255, e_src, tid);
+          } else {
+            consumer_sync();  // the choice (shared memory) is read by every warp's epilogue
+          }
         }
         break;
       case PK_GU:
       case PK_ROUTER:
         if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, e_src, -1, c, cw, lane);
         break;
-      case PK_EGU: {
-        if (cw == 0) {
-          select_experts(p, ctl, L, e_sel, lane);
-          if (lane == 0) {
-            if (c == 0 && !ab) for (int i = 0; i < p.topk; ++i) p.sel_out[L * p.topk + i] = ctl->sel[i];
-            mbar_arrive(&ctl->sel_bar);  // release the choice to the producer
+      case PK_EGU:
+        if constexpr (MOE) {
+          if (cw == 0) {
+            select_experts(p, ctl, L, e_sel, lane);
+            if (lane == 0) {
+              if (c == 0 && !ab) for (int i = 0; i < p.topk; ++i) p.sel_out[L * p.topk + i] = ctl->sel[i];
+              mbar_arrive(&ctl->sel_bar);  // release the choice to the producer
+            }
           }
+          sel_layer = L;
+          if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, e_src, -1, c, cw, lane);
+          else consumer_sync();
         }
-        sel_layer = L;
-        if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, e_src, -1, c, cw, lane);
-        else consumer_sync();
         break;
-      }
       case PK_LM:
         if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.final_norm, nullptr, e_src, p.L, c, cw, lane);
         break;
@@ -1095,15 +1160,19 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
     } else if (P.kind == PK_SAMPLE) {
       if (st.temperature > 0.0f) sample_phase(p, ctl, st, c, G, cw, lane);
     } else if (P.kind == PK_EGU || P.kind == PK_EDOWN) {
-      switch (p.topk) {
-        case 1: run_expert<1>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
-        case 2: run_expert<2>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
-        case 4: run_expert<4>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
-        default: run_expert<8>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
+      if constexpr (MOE) {
+        switch (p.topk) {
+          case 1: run_expert<1>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
+          case 2: run_expert<2>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
+          case 4: run_expert<4>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
+          default: run_expert<8>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
+        }
       }
     } else if (P.kind == PK_ROUTER) {
-      if (p.rdt == DT_BF16) gemv_phase<1, 1, DT_BF16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
-      else gemv_phase<1, 1, DT_F16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+      if constexpr (MOE) {
+        if (p.rdt == DT_BF16) gemv_phase<1, 1, DT_BF16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+        else gemv_phase<1, 1, DT_F16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+      }
     } else {
       if (p.wdt == DT_BF16) run_gemv<DT_BF16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
       else run_gemv<DT_F16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
@@ -1127,6 +1196,9 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
   }
 }
 
+// MOE: the kernel of the top-k expert models; dense models run the instantiation without the
+// router and expert paths.
+template <bool MOE>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ Params p, int32_t ph0, int32_t ph1, int32_t use_barrier,
                   int32_t xbuf_floats) {
@@ -1163,7 +1235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumerWarps) {
     if (lane == 0) producer(p, ctl, ring, c, G, ph0, ph1);
   } else {
-    consumer(p, ctl, ring, xbuf, st, c, G, ph0, ph1, use_barrier != 0, warp, lane);
+    consumer<MOE>(p, ctl, ring, xbuf, st, c, G, ph0, ph1, use_barrier != 0, warp, lane);
   }
 }
 
@@ -1172,19 +1244,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace adp {
 
 // Host-side launchers of the decode kernel.
-cudaError_t decode_prepare(size_t smem_bytes, int* blocks_per_sm) {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+cudaError_t decode_prepare(size_t smem_bytes, bool moe, int* blocks_per_sm) {
+  const void* k = moe ? (const void*)decode_kernel<true> : (const void*)decode_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, decode_kernel, kThreads, smem_bytes);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kThreads, smem_bytes);
 }
 
 cudaError_t decode_launch(const Params& p, int ph0, int ph1, bool persistent, int grid, size_t smem_bytes,
                           int xbuf_floats, cudaStream_t stream) {
   int32_t a0 = ph0, a1 = ph1, ub = persistent ? 1 : 0, xf = xbuf_floats;
   void* args[] = {(void*)&p, &a0, &a1, &ub, &xf};
-  if (persistent)
-    return cudaLaunchCooperativeKernel((const void*)decode_kernel, dim3(grid), dim3(kThreads), args, smem_bytes, stream);
-  return cudaLaunchKernel((const void*)decode_kernel, dim3(grid), dim3(kThreads), args, smem_bytes, stream);
+  const void* k = p.E > 0 ? (const void*)decode_kernel<true> : (const void*)decode_kernel<false>;
+  if (persistent) return cudaLaunchCooperativeKernel(k, dim3(grid), dim3(kThreads), args, smem_bytes, stream);
+  return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, smem_bytes, stream);
 }
 
 }  // namespace adp

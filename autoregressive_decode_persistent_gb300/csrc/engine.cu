@@ -243,7 +243,12 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   // K (rows padded by 16 bytes), V, the group's queries, the weights e_j
   const size_t item = (size_t)kAttnBlock * (hd + 8) * 2 + (size_t)kAttnBlock * hd * 2 + (size_t)kMaxGroup * hd * 4 +
                       (size_t)kMaxGroup * kAttnBlock * 4;
-  const size_t vec_bytes = std::max((size_t)std::max(std::max(d, hq * hd), ffw) * 4, ((size_t)2 * 8 * nbmax_ + 8) * 4);
+  // GEMV input vectors are stored in shared memory padded to multiples of 256 floats (per expert
+  // slot for the expert down projection)
+  auto pad256 = [](int n) { return (size_t)((n + 255) / 256 * 256); };
+  const size_t vec_floats = std::max({pad256(d), pad256(hq * hd),
+                                      c.n_experts ? (size_t)c.top_k * pad256(c.d_expert) : pad256(c.d_ff)});
+  const size_t vec_bytes = std::max(vec_floats * 4, ((size_t)2 * 8 * nbmax_ + 8) * 4);
   // The deepest weight ring (kMaxSlots down to 3 slots) that leaves room for the input vector and
   // one attention item; the attention slots then take the room that is left (at most one query
   // head per consumer warp).
@@ -268,7 +273,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   m->p.att_gmax = gmax;
   m->p.att_slot_bytes = (int)item;
   int bps = 0;
-  CK(decode_prepare(m->smem, &bps));
+  CK(decode_prepare(m->smem, c.n_experts > 0, &bps));
   if (bps < 1) return ADP_ERR_NOT_CORESIDENT;
 
   // weight image
