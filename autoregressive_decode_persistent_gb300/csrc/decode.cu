@@ -44,8 +44,7 @@ struct Ctl {
   float gate[kMaxTopK];
   float stage[1024];  // router logits or sampling block sums, loaded in one batch
   uint64_t att_bar[kAttnSlots];  // TMA completion of each attention slot's K/V block
-  int32_t n_done;                // KV groups whose last attention block finished in this CTA
-  int32_t done[64];
+  uint64_t merge_bar;            // TMA completion of the attention merge's block outputs
   float rope_cs[128], rope_sn[128];  // RoPE row of this step's position (QKV epilogue)
   float xres[64];                    // residual rows this CTA updates (Wo / down epilogues)
 };
@@ -568,8 +567,6 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
 // ---------------------------------------------------------------- finalisation
 
 __device__ void finalize_token(const Params& p, const Step& st, int32_t token) {
-  // every CTA has finished this step's attention: clear its per-layer block counters
-  for (int i = 0; i < p.L * p.hkv; ++i) p.head_ctr[i] = 0u;
   *p.epoch = st.ebase + (uint32_t)p.n_phases;  // the next step's phases publish new epochs
   StepState* s = p.state;
   s->out_token = token;
@@ -655,29 +652,10 @@ __device__ __forceinline__ void prefetch_attention_kv(const Params& p, int L, in
   }
 }
 
-// Blocks [b0, nb) of one merged output: Ls += w_b l_b, O += w_b o_b in block order, the
-// partials loaded 16 blocks at a time.
-template <int HD>
-__device__ __forceinline__ void merge_tail(const float* w, const float* lsum, const float* src, int b0, int nb,
-                                           float& Ls, float& O) {
-  for (; b0 < nb; b0 += 16) {
-    float ob[16];
-#pragma unroll
-    for (int t2 = 0; t2 < 16; ++t2) ob[t2] = b0 + t2 < nb ? __ldcg(src + (size_t)(b0 + t2) * HD) : 0.0f;
-#pragma unroll
-    for (int t2 = 0; t2 < 16; ++t2) {
-      if (b0 + t2 < nb) {
-        Ls = fmaf(w[b0 + t2], lsum[b0 + t2], Ls);
-        O = fmaf(w[b0 + t2], ob[t2], O);
-      }
-    }
-  }
-}
-
 template <int HD, int KVDT>
 __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float* xbuf, const PhaseDesc& P,
                                              const Step& st, uint32_t c, uint32_t G, int cw, int lane,
-                                             uint32_t& att_uses_io, uint32_t ew) {
+                                             uint32_t& att_uses_io, uint32_t& merge_uses, uint32_t ew) {
   constexpr int NV = HD / 8;         // 8-element vectors per K row (partial sums of the contract dot)
   constexpr int KSTR = HD + 8;       // padded K row stride in shared memory (conflict-free row reads)
   constexpr int DPL = HD / 32;       // output dims per lane in the PV pass
@@ -694,10 +672,9 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
   const ll_t* knew = p.knew;
   const ll_t* vnew = p.vnew;
   const uint32_t qe = st.ebase + 1 + (uint32_t)P.src_ph;  // epoch of this layer's QKV outputs
-  float* part_m = p.part_m;
-  float* part_l = p.part_l;
-  float* part_o = p.part_o;
-  uint32_t* head_ctr = p.head_ctr;
+  ll_t* part_m = p.part_m;
+  ll_t* part_l = p.part_l;
+  ll_t* part_o = p.part_o;
   ll_t* attn = p.attn;
   uint32_t att_uses = att_uses_io;
   const int nb = (ctx + kAttnBlock - 1) / kAttnBlock;
@@ -779,6 +756,7 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
       ok = ok && !aborted(ctl);
       if (cw == 0 && lane == 0 && it == (int)c) stamp(p, c, P.index, 4);
       if (active && ok) {
+        const long long cs0 = clock64();
         // score of position j0 + lane: the contract dot over the K row, its 32-slot tree in registers
         float sj = __int_as_float(0xFF800000);  // -inf
         if (lane < nvalid) {
@@ -798,6 +776,7 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
             for (int i = 0; i < off; ++i) a[i] = __fadd_rn(a[i], a[i + off]);
           sj = __fmul_rn(a[0], scale);
         }
+        const long long cs1 = clock64();
         // block maximum and weights e_j = exp(s_j - m_b), shared with the warp through SS
         float m = sj;
 #pragma unroll
@@ -805,12 +784,29 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
         float* se = SS + hh * kAttnBlock;
         se[lane] = lane < nvalid ? exp_c(__fsub_rn(sj, m)) : 0.0f;
         __syncwarp();
+        const long long cs2 = clock64();
         // l = sequential sum of e_j; o = sequential fma chain over j
         float l = 0.0f, o[DPL];
 #pragma unroll
         for (int i = 0; i < DPL; ++i) o[i] = 0.0f;
         const uint16_t* vcol = SV + lane * DPL;
-        for (int jb = 0; jb < nvalid; jb += 8) {
+        if (nvalid == kAttnBlock) {  // a full block: no bounds in the chain
+#pragma unroll
+          for (int jb = 0; jb < kAttnBlock; jb += 8) {
+            float vv[8][DPL], ee[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              kv_dims_smem<KVDT, DPL>(vcol + (size_t)(jb + k) * HD, vv[k]);
+              ee[k] = se[jb + k];
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              l = __fadd_rn(l, ee[k]);
+#pragma unroll
+              for (int i = 0; i < DPL; ++i) o[i] = fmaf(ee[k], vv[k][i], o[i]);
+            }
+          }
+        } else for (int jb = 0; jb < nvalid; jb += 8) {
           float vv[8][DPL], ee[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
@@ -827,25 +823,26 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
             }
           }
         }
+        const long long cs3 = clock64();
         if (cw == 0 && lane == 0 && it == (int)c) stamp(p, c, P.index, 6);
-        // block partial; o is stored [head][block][dim]: coalesced stores here and loads in the merge
+        // block partial as epoch-tagged words, [head][block] and [head][block][dim]: the head's
+        // merger polls them directly (no counter, no fence on this side)
         if (lane == 0) {
-          __stcg(part_m + (size_t)h * nbmax + b, m);
-          __stcg(part_l + (size_t)h * nbmax + b, l);
+          ll_store(part_m + (size_t)h * nbmax + b, ll_pack(m, ew));
+          ll_store(part_l + (size_t)h * nbmax + b, ll_pack(l, ew));
         }
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) __stcg(part_o + ((size_t)h * nbmax + b) * HD + lane * DPL + i, o[i]);
-        __syncwarp();
-        if (lane == 0) {
-          // release: this warp's partials before the count; acquire: the merger sees every partial
-          uint32_t old;
-          asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(head_ctr + L * hkv + g) : "memory");
-          if (old == (uint32_t)((h1 - h0) * nb - 1)) {
-            const int k = atomicAdd(&ctl->n_done, 1);
-            ctl->done[k] = g;
+        for (int i = 0; i < DPL; ++i) ll_store(part_o + ((size_t)h * nbmax + b) * HD + lane * DPL + i, ll_pack(o[i], ew));
+        if (cw == 0 && lane == 0 && it == (int)c) {
+          stamp(p, c, P.index, 5);
+          if (p.timeline) {
+            unsigned long long* tl = p.timeline + ((size_t)c * p.n_phases + P.index) * kStamps;
+            tl[12] = (unsigned long long)(cs1 - cs0);
+            tl[13] = (unsigned long long)(cs2 - cs1);
+            tl[14] = (unsigned long long)(cs3 - cs2);
+            tl[15] = (unsigned long long)(clock64() - cs3);
           }
         }
-        if (cw == 0 && lane == 0 && it == (int)c) stamp(p, c, P.index, 5);
       }
       // the slot's staging area is reused by its next item only after every warp of the slot is done
       asm volatile("bar.sync %0, %1;" ::"r"(2 + slot), "r"(gmax * 32) : "memory");
@@ -853,73 +850,87 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
   }
   consumer_sync();
   if (tid == 0) stamp(p, c, P.index, 7);
-  // merge the groups completed here: all consumer warps, in ascending block order
-  const int nd = *(volatile int32_t*)&ctl->n_done;
-  for (int k = 0; k < nd; ++k) {
-    const int g = ctl->done[k];
-    int h0, h1;
-    group_heads(g, hq, hkv, h0, h1);
-    const int gh = h1 - h0;
-    float* Wm = xbuf;                         // [gh][nbmax] block maxima, then weights w_b
-    float* Wl = xbuf + kMaxGroup * nbmax;     // [gh][nbmax] block sums
+  // Merge: CTA G-1-h merges query head h (after its own items, if any).  Thread d < HD owns output
+  // dimension d; the block maxima and sums are staged in shared memory, the weights
+  // w_b = exp(m_b - M) and L = sum_b w_b l_b computed once, then o_d = (sum_b w_b o_bd) / L, both
+  // sums fused-multiply-added in block order.  Every partial is polled by its epoch, so the merge
+  // starts as soon as the last one lands.
+  const int h = (int)G - 1 - (int)c;
+  if (h >= 0 && h < hq && !aborted(ctl)) {
+    float* Wm = xbuf;           // [nb] block maxima, then weights w_b
+    float* Wl = xbuf + nbmax;   // [nb] block sums; Wl[nbmax] = L
     constexpr int T = kConsumerWarps * 32;
-    constexpr int kPre = 32;                  // blocks of a thread's first two outputs loaded up front
-    const int n_out = gh * HD;
-    // Every load of a context up to 32 blocks is issued here at once (one round trip to L2):
-    // the block partials of this thread's first two outputs, and the block maxima and sums.
-    float pre[2][kPre];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int oi = tid + r * T;
-      const float* src = part_o + (size_t)(h0 + oi / HD) * nbmax * HD + oi % HD;
-#pragma unroll
-      for (int t2 = 0; t2 < kPre; ++t2) pre[r][t2] = (oi < n_out && t2 < nb) ? __ldcg(src + (size_t)t2 * HD) : 0.0f;
-    }
-    for (int i = tid; i < gh * nb; i += T) {
-      const int hx = i / nb, bb = i % nb;
-      Wm[hx * nbmax + bb] = __ldcg(part_m + (size_t)(h0 + hx) * nbmax + bb);
-      Wl[hx * nbmax + bb] = __ldcg(part_l + (size_t)(h0 + hx) * nbmax + bb);
+    constexpr int kPre = 32;    // blocks of o loaded per batch
+    const ll_t* po = part_o + (size_t)h * nbmax * HD + tid;  // this thread's dimension, block 0
+    for (int i = tid; i < 2 * nb; i += T) {
+      const ll_t* src = i < nb ? part_m + (size_t)h * nbmax + i : part_l + (size_t)h * nbmax + (i - nb);
+      ll_t x = ll_load(src);
+      if (ll_wait(src, ew, x, p, ctl)) (i < nb ? Wm[i] : Wl[i - nb]) = ll_value(x);
     }
     consumer_sync();
-    if (tid == 0 && k == 0) stamp(p, c, P.index, 10);
-    if (cw < gh) {  // one warp per head: M = max_b m_b, then w_b = exp(m_b - M)
+    if (tid == 0) stamp(p, c, P.index, 10);
+    // Every block's maximum and sum has arrived, so its outputs almost surely have too: one bulk
+    // copy per batch brings them ([block][dim], epoch-tagged) into shared memory while warp 0
+    // forms the weights.
+    ll_t* So = reinterpret_cast<ll_t*>(xbuf + ((2 * nbmax + 2 + 3) & ~3));  // 16-byte aligned
+    const int batch = (int)(((size_t)p.xbuf_floats - (size_t)((2 * nbmax + 2 + 3) & ~3)) * 4 / ((size_t)HD * 8));
+    auto issue = [&](int b0) {
+      const int nbk = min(batch, nb - b0);
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // outputs other CTAs stored, read by TMA
+      mbar_arrive_expect_tx(&ctl->merge_bar, (uint32_t)nbk * HD * 8);
+      tma_load_1d(So, part_o + ((size_t)h * nbmax + b0) * HD, (uint32_t)nbk * HD * 8, &ctl->merge_bar,
+                  policy_evict_first());
+    };
+    if (tid == 0) issue(0);
+    if (cw == 0) {
       float M = __int_as_float(0xFF800000);
-      for (int bb = lane; bb < nb; bb += 32) M = fmaxf(M, Wm[cw * nbmax + bb]);
+      for (int bb = lane; bb < nb; bb += 32) M = fmaxf(M, Wm[bb]);
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
-      for (int bb = lane; bb < nb; bb += 32) Wm[cw * nbmax + bb] = exp_c(__fsub_rn(Wm[cw * nbmax + bb], M));
-    }
-    consumer_sync();
-    // o_h = (sum_b w_b o_b) / (sum_b w_b l_b), both sums fused-multiply-added in block order
+      for (int bb = lane; bb < nb; bb += 32) Wm[bb] = exp_c(__fsub_rn(Wm[bb], M));
+      __syncwarp();
+      if (lane == 0) {
+        float Ls = 0.0f;
+        int bb = 0;
+        for (; bb + 8 <= nb; bb += 8) {
+          float wv[8], lv[8];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int oi = tid + r * T;
-      if (oi < n_out) {
-        const int hx = oi / HD, dd = oi % HD;
-        const float* w = Wm + hx * nbmax;
-        const float* lsum = Wl + hx * nbmax;
-        float Ls = 0.0f, O = 0.0f;
-#pragma unroll
-        for (int t2 = 0; t2 < kPre; ++t2) {
-          if (t2 < nb) {
-            Ls = fmaf(w[t2], lsum[t2], Ls);
-            O = fmaf(w[t2], pre[r][t2], O);
+          for (int k = 0; k < 8; ++k) {
+            wv[k] = Wm[bb + k];
+            lv[k] = Wl[bb + k];
           }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) Ls = fmaf(wv[k], lv[k], Ls);
         }
-        merge_tail<HD>(w, lsum, part_o + (size_t)(h0 + hx) * nbmax * HD + dd, kPre, nb, Ls, O);
-        ll_store(attn + (size_t)(h0 + hx) * HD + dd, ll_pack(__fdiv_rn(O, Ls), ew));
+        for (; bb < nb; ++bb) Ls = fmaf(Wm[bb], Wl[bb], Ls);
+        Wl[nbmax] = Ls;
+        stamp(p, c, P.index, 12);
       }
     }
-    for (int oi = tid + 2 * T; oi < n_out; oi += T) {  // groups of more than 2 x 480 outputs
-      const int hx = oi / HD, dd = oi % HD;
-      float Ls = 0.0f, O = 0.0f;
-      merge_tail<HD>(Wm + hx * nbmax, Wl + hx * nbmax, part_o + (size_t)(h0 + hx) * nbmax * HD + dd, 0, nb, Ls, O);
-      ll_store(attn + (size_t)(h0 + hx) * HD + dd, ll_pack(__fdiv_rn(O, Ls), ew));
-    }
     consumer_sync();
-    if (tid == 0 && k == 0) stamp(p, c, P.index, 11);
+    float O = 0.0f;
+    bool ok = true;
+    for (int b0 = 0; b0 < nb; b0 += batch) {
+      const int nbk = min(batch, nb - b0);
+      ok = ok && mbar_wait(&ctl->merge_bar, merge_uses & 1, &ctl->abort, wait_ns);
+      ++merge_uses;
+      if (!ok && tid == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
+      if (ok && tid < HD) {
+        for (int t2 = 0; t2 < nbk && ok; ++t2) {
+          ll_t x = So[(size_t)t2 * HD + tid];
+          if (ll_epoch(x) != ew) ok = ll_wait(part_o + ((size_t)h * nbmax + b0 + t2) * HD + tid, ew, x, p, ctl);
+          O = fmaf(Wm[b0 + t2], ll_value(x), O);
+        }
+      }
+      if (b0 + nbk < nb) {  // the staging area is reused by the next batch after every thread read it
+        consumer_sync();
+        if (tid == 0) issue(b0 + nbk);
+      }
+    }
+    if (tid == 0) stamp(p, c, P.index, 13);
+    if (ok && tid < HD) ll_store(attn + (size_t)h * HD + tid, ll_pack(__fdiv_rn(O, Wl[nbmax]), ew));
+    if (tid == 0) stamp(p, c, P.index, 11);
   }
-  if (tid == 0) ctl->n_done = 0;
   att_uses_io = att_uses;
 }
 
@@ -1056,7 +1067,7 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
   uint32_t t = 0;
   int bidx = 0;
   int sel_layer = -1;
-  uint32_t att_uses = 0;
+  uint32_t att_uses = 0, merge_uses = 0;
   const int tid = cw * 32 + lane;
   for (int ph = ph0; ph < ph1; ++ph) {
     // every warp of this CTA has left the previous phase before this one reuses the shared input
@@ -1149,13 +1160,13 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
     if (cw == 0 && lane == 0) stamp(p, c, ph, 1);
     if (P.kind == PK_ATTN) {
       if (p.kvdt == DT_BF16) {
-        if (p.hd == 128) attention_phase<128, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
-        else if (p.hd == 64) attention_phase<64, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
-        else attention_phase<256, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+        if (p.hd == 128) attention_phase<128, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+        else if (p.hd == 64) attention_phase<64, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+        else attention_phase<256, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
       } else {
-        if (p.hd == 128) attention_phase<128, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
-        else if (p.hd == 64) attention_phase<64, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
-        else attention_phase<256, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+        if (p.hd == 128) attention_phase<128, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+        else if (p.hd == 64) attention_phase<64, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+        else attention_phase<256, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
       }
     } else if (P.kind == PK_SAMPLE) {
       if (st.temperature > 0.0f) sample_phase(p, ctl, st, c, G, cw, lane);
@@ -1214,8 +1225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->empty[s], kConsumerWarps);
     }
     mbar_init(&ctl->sel_bar, 1);
+    mbar_init(&ctl->merge_bar, 1);
     for (int w = 0; w < kAttnSlots; ++w) mbar_init(&ctl->att_bar[w], 1);
-    ctl->n_done = 0;
     ctl->abort = *(volatile int32_t*)p.err != 0 ? 1 : 0;
     ctl->flag = 0;
     mbar_fence_init();

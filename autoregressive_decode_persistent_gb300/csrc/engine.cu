@@ -77,7 +77,7 @@ struct adp_model {
   const void* graph_key_logits = nullptr;
   bool graph_key_sample = false;
   int sticky = ADP_OK;
-  size_t ll_bytes[7] = {0};  // sizes of the epoch-tagged exchange buffers
+  size_t ll_bytes[10] = {0};  // sizes of the epoch-tagged exchange buffers
 
   template <class T>
   int alloc(T** ptr, size_t count) {
@@ -211,8 +211,8 @@ static void plan(adp_model* m) {
 // Zero the epoch base and every epoch-tagged exchange buffer (epoch 0 is never awaited).
 static int clear_exchange(adp_model* m) {
   const Params& p = m->p;
-  void* bufs[7] = {p.x, p.q, p.attn, p.h, p.rlog, p.knew, p.vnew};
-  for (int i = 0; i < 7; ++i) CK(cudaMemsetAsync(bufs[i], 0, m->ll_bytes[i], m->stream));
+  void* bufs[10] = {p.x, p.q, p.attn, p.h, p.rlog, p.knew, p.vnew, p.part_m, p.part_l, p.part_o};
+  for (int i = 0; i < 10; ++i) CK(cudaMemsetAsync(bufs[i], 0, m->ll_bytes[i], m->stream));
   CK(cudaMemsetAsync(p.epoch, 0, 4, m->stream));
   return ADP_OK;
 }
@@ -240,6 +240,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
     gmax = std::max(gmax, h1 - h0);
   }
   if (gmax < 1 || gmax > kMaxGroup) return ADP_ERR_UNSUPPORTED_CONFIG;
+  if (hq > m->G) return ADP_ERR_UNSUPPORTED_CONFIG;  // CTA G-1-h merges query head h
   // K (rows padded by 16 bytes), V, the group's queries, the weights e_j
   const size_t item = (size_t)kAttnBlock * (hd + 8) * 2 + (size_t)kAttnBlock * hd * 2 + (size_t)kMaxGroup * hd * 4 +
                       (size_t)kMaxGroup * kAttnBlock * 4;
@@ -265,6 +266,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   if (!nslots) return ADP_ERR_UNSUPPORTED_CONFIG;
   xbytes = (xbytes + 127) & ~(size_t)127;
   m->xbuf_floats = (int)(xbytes / 4);
+  m->p.xbuf_floats = m->xbuf_floats;
   m->smem = (size_t)nslots * kSlotBytes + xbytes + ctl_bytes();
   if (m->smem > optin) return ADP_ERR_UNSUPPORTED_CONFIG;
   m->p.nslots = nslots;
@@ -364,7 +366,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
       (rc = m->alloc(&p.h, ffw)) || (rc = m->alloc(&p.rlog, std::max(c.n_experts, 1))) ||
       (rc = m->alloc(&p.knew, hkv * hd)) || (rc = m->alloc(&p.vnew, hkv * hd)) || (rc = m->alloc(&p.epoch, 1)) ||
       (rc = m->alloc(&p.part_m, (size_t)hq * nbmax)) || (rc = m->alloc(&p.part_l, (size_t)hq * nbmax)) ||
-      (rc = m->alloc(&p.part_o, (size_t)hq * nbmax * hd)) || (rc = m->alloc(&p.head_ctr, (size_t)L * hkv)) ||
+      (rc = m->alloc(&p.part_o, (size_t)hq * nbmax * hd)) ||
       (rc = m->alloc(&p.sblock, nblk)) || (rc = m->alloc(&p.sample_ctr, 1)) || (rc = m->alloc(&p.argkey, 1)) ||
       (rc = m->alloc(&p.lm_ctr, 1)) || (rc = m->alloc(&p.bar_ctr, 1)) || (rc = m->alloc(&p.err, 1)) ||
       (rc = m->alloc(&p.sel_out, (size_t)L * topk)) || (rc = m->alloc(&p.state, 1)) ||
@@ -377,8 +379,10 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   m->ll_bytes[4] = (size_t)std::max(c.n_experts, 1) * 8;
   m->ll_bytes[5] = (size_t)hkv * hd * 8;
   m->ll_bytes[6] = (size_t)hkv * hd * 8;
+  m->ll_bytes[7] = (size_t)hq * nbmax * 8;
+  m->ll_bytes[8] = (size_t)hq * nbmax * 8;
+  m->ll_bytes[9] = (size_t)hq * nbmax * hd * 8;
   if ((rc = clear_exchange(m))) return rc;
-  CK(cudaMemsetAsync(p.head_ctr, 0, (size_t)L * hkv * 4, m->stream));
   CK(cudaMemsetAsync(p.sample_ctr, 0, 4, m->stream));
   CK(cudaMemsetAsync(p.argkey, 0, 8, m->stream));
   CK(cudaMemsetAsync(p.lm_ctr, 0, 4, m->stream));
@@ -695,7 +699,6 @@ extern "C" int adp_reset(adp_model* m) {
   if (!m) return ADP_ERR_INVALID_ARG;
   cudaStreamSynchronize(m->stream);
   const Params& p = m->p;
-  CK(cudaMemsetAsync(p.head_ctr, 0, (size_t)m->cfg.n_layers * m->cfg.n_kv_heads * 4, m->stream));
   CK(cudaMemsetAsync(p.sample_ctr, 0, 4, m->stream));
   CK(cudaMemsetAsync(p.argkey, 0, 8, m->stream));
   CK(cudaMemsetAsync(p.lm_ctr, 0, 4, m->stream));
@@ -753,10 +756,9 @@ int adp::scratch_layout(const adp_model* m, ScratchLayout* out) {
   l.knew = take(hkv * hd * 8);
   l.vnew = take(hkv * hd * 8);
   l.epoch = take(4);
-  l.part_m = take(hq * nbmax * 4);
-  l.part_l = take(hq * nbmax * 4);
-  l.part_o = take(hq * nbmax * hd * 4);
-  l.head_ctr = take(L * hkv * 4);
+  l.part_m = take(hq * nbmax * 8);
+  l.part_l = take(hq * nbmax * 8);
+  l.part_o = take(hq * nbmax * hd * 8);
   l.sblock = take(nblk * 4);
   l.sample_ctr = take(4);
   l.argkey = take(8);
@@ -799,10 +801,9 @@ int adp::decode_step_in_scratch(adp_model* m, adp_kv* kv, int32_t token, const a
   p.knew = reinterpret_cast<unsigned long long*>(at(lay.knew));
   p.vnew = reinterpret_cast<unsigned long long*>(at(lay.vnew));
   p.epoch = reinterpret_cast<uint32_t*>(at(lay.epoch));
-  p.part_m = reinterpret_cast<float*>(at(lay.part_m));
-  p.part_l = reinterpret_cast<float*>(at(lay.part_l));
-  p.part_o = reinterpret_cast<float*>(at(lay.part_o));
-  p.head_ctr = reinterpret_cast<uint32_t*>(at(lay.head_ctr));
+  p.part_m = reinterpret_cast<unsigned long long*>(at(lay.part_m));
+  p.part_l = reinterpret_cast<unsigned long long*>(at(lay.part_l));
+  p.part_o = reinterpret_cast<unsigned long long*>(at(lay.part_o));
   p.sblock = reinterpret_cast<float*>(at(lay.sblock));
   p.sample_ctr = reinterpret_cast<uint32_t*>(at(lay.sample_ctr));
   p.argkey = reinterpret_cast<unsigned long long*>(at(lay.argkey));

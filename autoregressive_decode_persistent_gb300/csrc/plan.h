@@ -91,6 +91,7 @@ struct Params {
   int32_t att_slots;                  // attention items a CTA works on at once
   int32_t att_gmax;                   // warps per slot (largest number of query heads per KV head)
   int32_t att_slot_bytes;             // shared-memory staging bytes of one slot
+  int32_t xbuf_floats;                // floats of the shared input-vector / staging area
   // KV cache [L][hkv][max_ctx][hd]
   uint16_t* kc;
   uint16_t* vc;
@@ -108,10 +109,9 @@ struct Params {
   unsigned long long* h;     // [max(ff, topk*f)] FFN activations
   unsigned long long* rlog;  // [E] router logits
   uint32_t* epoch;           // epoch base of the next step (advanced by the step's last CTA)
-  float* part_m;   // [hq][nbmax]
-  float* part_l;   // [hq][nbmax]
-  float* part_o;   // [hq][nbmax][hd]
-  uint32_t* head_ctr;          // [L][hkv] attention blocks finished per KV group (cleared per step)
+  unsigned long long* part_m;  // [hq][nbmax] attention block maxima (epoch-tagged)
+  unsigned long long* part_l;  // [hq][nbmax] attention block sums (epoch-tagged)
+  unsigned long long* part_o;  // [hq][nbmax][hd] attention block outputs (epoch-tagged)
   float* sblock;               // [ceil(V/256)] sampling block sums
   uint32_t* sample_ctr;
   unsigned long long* argkey;  // packed (ordered logit, ~index) maximum

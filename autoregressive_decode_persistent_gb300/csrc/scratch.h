@@ -8,11 +8,11 @@
 namespace adp {
 
 // Byte offsets, in one scratch area, of everything a decode step writes besides the KV cache:
-// the epoch-tagged exchange vectors, the epoch base, the attention partials and counters, the
+// the epoch-tagged exchange vectors and attention partials, the epoch base, the
 // sampling and argmax words, the grid-barrier counter, the error word, the router choices, the
 // step state and the logits.  Each region starts at a multiple of 256 bytes.
 struct ScratchLayout {
-  size_t x, q, attn, h, rlog, knew, vnew, epoch, part_m, part_l, part_o, head_ctr, sblock, sample_ctr, argkey,
+  size_t x, q, attn, h, rlog, knew, vnew, epoch, part_m, part_l, part_o, sblock, sample_ctr, argkey,
       lm_ctr, bar_ctr, err, sel_out, state, logits;
   size_t total;
 };

@@ -159,7 +159,7 @@ int adp_decode_step(adp_model* m, adp_kv* kv, int32_t token, const adp_sampling*
  *  - The first call on a device sets up: with that device current it looks up the array's device
  *    address (cudaGetSymbolAddress, which may make the CUDA runtime load the array's module).
  *    Make that first call before any stream capture begins.  The model's device must be current.
- *  - A model whose step needs more than 8 MiB of scratch (dominated by 4 * n_heads *
+ *  - A model whose step needs more than 8 MiB of scratch (dominated by 8 * n_heads *
  *    ceil(max_ctx / 32) * head_dim bytes of attention partials plus 4 * vocab bytes of logits) is
  *    rejected with ADP_ERR_UNSUPPORTED_CONFIG before anything runs; adp_last_error() gives both sizes.
  *  - Every call shares the array.  All of it must be zero before a model's first step in it: it
