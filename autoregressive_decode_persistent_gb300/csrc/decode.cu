@@ -67,11 +67,21 @@ __device__ __forceinline__ void stamp(const Params& p, uint32_t c, int ph, int k
   if (p.timeline) p.timeline[((size_t)c * p.n_phases + ph) * kStamps + k] = globaltimer();
 }
 
-// Per-CTA share of a phase: units [u0, u0 + n).
+// Per-CTA share of a phase: units [u0, u0 + n).  (c + 1) * n_units stays below 2^32: the model
+// checks n_units * G < 2^32 at creation.
 __device__ __forceinline__ void cta_units(const PhaseDesc& P, uint32_t c, uint32_t G, int32_t& u0, int32_t& n) {
-  const long long a = (long long)c * P.n_units / G, b = (long long)(c + 1) * P.n_units / G;
+  const uint32_t nu = (uint32_t)P.n_units;
+  const uint32_t a = c * nu / G, b = (c + 1) * nu / G;
   u0 = (int32_t)a;
   n = (int32_t)(b - a);
+}
+
+// The step's phase table, copied into shared memory after the control block at kernel start
+// (every phase begins by reading its descriptor: from global memory that would be a round trip
+// to L2 on the critical path of every phase).
+constexpr size_t kCtlPad = (sizeof(Ctl) + 15) & ~(size_t)15;
+__device__ __forceinline__ const PhaseDesc* phase_table(const Ctl* ctl) {
+  return reinterpret_cast<const PhaseDesc*>(reinterpret_cast<const uint8_t*>(ctl) + kCtlPad);
 }
 
 // ---------------------------------------------------------------- producer (TMA) warp
@@ -88,10 +98,10 @@ struct L2Cursor {
   uint64_t pos;  // stream position of the cursor
 };
 
-__device__ __forceinline__ void l2_advance(const Params& p, L2Cursor& cur, uint64_t issue_pos, int ph1, uint32_t c,
+__device__ __forceinline__ void l2_advance(const Params& p, const Ctl* ctl, L2Cursor& cur, uint64_t issue_pos, int ph1, uint32_t c,
                                            uint32_t G) {
   while (cur.pos < issue_pos + p.l2_lookahead && cur.ph < ph1) {
-    const PhaseDesc& Q = p.phases[cur.ph];
+    const PhaseDesc& Q = phase_table(ctl)[cur.ph];
     if (!Q.has_weights) { ++cur.ph; cur.off = 0; continue; }
     if (Q.kind == PK_EGU || Q.kind == PK_EDOWN) return;  // experts not chosen yet
     int32_t u0, n;
@@ -117,7 +127,7 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
   L2Cursor cur{ph0, 0, 0};
   uint64_t issue_pos = 0;  // stream position of the next dense tile
   for (int ph = ph0; ph < ph1 && !stop; ++ph) {
-    const PhaseDesc P = p.phases[ph];
+    const PhaseDesc P = phase_table(ctl)[ph];
     if (!P.has_weights) continue;
     int32_t u0, n;
     cta_units(P, c, G, u0, n);
@@ -150,7 +160,7 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
         if (t >= ns) {
           if (!mbar_try_wait(&ctl->empty[slot], (use - 1) & 1)) {
             const uint64_t tb = p.timeline ? globaltimer() : 0;
-            l2_advance(p, cur, issue_pos, ph1, c, G);  // keep HBM busy while the consumers catch up
+            l2_advance(p, ctl, cur, issue_pos, ph1, c, G);  // keep HBM busy while the consumers catch up
             if (!mbar_wait(&ctl->empty[slot], (use - 1) & 1, &ctl->abort, p.wait_ns)) {
               if (!aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
               stop = true;
@@ -1073,7 +1083,7 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
     // every warp of this CTA has left the previous phase before this one reuses the shared input
     // vector, the staging areas and the staged residual rows
     if (ph > ph0) consumer_sync();
-    const PhaseDesc P = p.phases[ph];
+    const PhaseDesc P = phase_table(ctl)[ph];
     const int L = P.layer;
     const bool ab = aborted(ctl);
     // epochs: what this phase publishes (0 = withheld by the test hook) and what it reads
@@ -1231,6 +1241,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl->flag = 0;
     mbar_fence_init();
   }
+  {
+    static_assert(sizeof(PhaseDesc) % 8 == 0, "phase descriptors are copied as 8-byte words");
+    const uint2* src = reinterpret_cast<const uint2*>(p.phases);
+    uint2* dst = reinterpret_cast<uint2*>(const_cast<PhaseDesc*>(phase_table(ctl)));
+    const int nv = p.n_phases * (int)(sizeof(PhaseDesc) / 8);
+    for (int i = threadIdx.x; i < nv; i += kThreads) dst[i] = __ldg(src + i);
+  }
   __syncthreads();
   if (*(volatile int32_t*)&ctl->abort) return;  // sticky device error: nothing runs until reset
   Step st;
@@ -1274,5 +1291,5 @@ cudaError_t decode_launch(const Params& p, int ph0, int ph1, bool persistent, in
 }  // namespace adp
 
 namespace adp {
-size_t ctl_bytes() { return sizeof(Ctl); }
+size_t ctl_bytes(int n_phases) { return kCtlPad + (size_t)n_phases * sizeof(PhaseDesc); }
 }  // namespace adp

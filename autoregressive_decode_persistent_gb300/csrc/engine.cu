@@ -227,12 +227,14 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   if (!prop.cooperativeLaunch) return ADP_ERR_NOT_CORESIDENT;
   m->G = prop.multiProcessorCount;  // one persistent CTA per SM
   plan(m);
+  for (const PhaseDesc& P : m->phases)  // per-CTA shares are computed in 32-bit arithmetic
+    if ((uint64_t)P.n_units * (uint64_t)m->G >= (1ull << 32)) return ADP_ERR_UNSUPPORTED_CONFIG;
   const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim, L = c.n_layers;
   const int ffw = c.n_experts ? c.top_k * c.d_expert : c.d_ff;
   // xbuf holds a phase's input vector, the attention warps' K/V staging areas, or the merge's
   // per-block weights: sized for the largest use that fits beside the ring.
   const int nbmax_ = (c.max_ctx + kAttnBlock - 1) / kAttnBlock;
-  const size_t ctl_sz = (ctl_bytes() + 127) & ~(size_t)127;
+  const size_t ctl_sz = (ctl_bytes((int)m->phases.size()) + 127) & ~(size_t)127;
   const size_t optin = (size_t)prop.sharedMemPerBlockOptin;
   int gmax = 0;  // most query heads sharing one KV head (floor(h * hkv / hq) grouping)
   for (int g = 0; g < c.n_kv_heads; ++g) {
@@ -267,7 +269,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   xbytes = (xbytes + 127) & ~(size_t)127;
   m->xbuf_floats = (int)(xbytes / 4);
   m->p.xbuf_floats = m->xbuf_floats;
-  m->smem = (size_t)nslots * kSlotBytes + xbytes + ctl_bytes();
+  m->smem = (size_t)nslots * kSlotBytes + xbytes + ctl_bytes((int)m->phases.size());
   if (m->smem > optin) return ADP_ERR_UNSUPPORTED_CONFIG;
   m->p.nslots = nslots;
   m->max_nslots = nslots;

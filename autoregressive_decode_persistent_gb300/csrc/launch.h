@@ -21,6 +21,6 @@ cudaError_t decode_launch(const Params& p, int ph0, int ph1, bool persistent, in
                           int xbuf_floats, cudaStream_t stream);
 cudaError_t repack_launch(uint8_t* image, const PhaseDesc& P, const RepackSrc& S, int grid, int experts,
                           cudaStream_t stream);
-size_t ctl_bytes();
+size_t ctl_bytes(int n_phases);  // control block + phase table in shared memory
 
 }  // namespace adp
