@@ -128,14 +128,16 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(cfg, W, seconds: float = 15.0, max_steps: int | None = None):
-    """The CPU oracle as it stands (plain mode) on a bounded sample of the workload."""
+def cpu_baseline(cfg, W, seconds: float = 15.0, max_steps: int | None = None, warmup: int = 1):
+    """The CPU oracle as it stands (plain mode) on a bounded sample of the workload: `warmup`
+    untimed steps, then steps until `seconds` have passed or `max_steps` were taken."""
     import synth
     from oracle import PLAIN, OracleModel
     om = OracleModel(cfg, W)
     om.load_kv_prefix(*synth.kv_prefix(cfg, cfg["prompt_len"]))
     toks = synth.prompt(cfg, 64, seed=99)
-    om.step(int(toks[0]), PLAIN)  # first call: tables, page-in
+    for i in range(max(1, warmup)):  # first calls: tables, page-in
+        om.step(int(toks[i % len(toks)]), PLAIN)
     n, t0 = 0, time.perf_counter()
     while True:
         om.step(int(toks[(n + 1) % len(toks)]), PLAIN)
@@ -146,7 +148,8 @@ def cpu_baseline(cfg, W, seconds: float = 15.0, max_steps: int | None = None):
     cores = len(os.sched_getaffinity(0))
     return {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} plain-fp32 decode steps of the full 2.3B model at contexts "
-                      f"{cfg['prompt_len'] + 1}..{cfg['prompt_len'] + n + 1} (synthetic 512-position KV prefix), "
+                      f"{cfg['prompt_len'] + max(1, warmup) + 1}..{cfg['prompt_len'] + max(1, warmup) + n} "
+                      f"(synthetic 512-position KV prefix, {max(1, warmup)} untimed steps first), "
                       f"OpenMP over {cores} host threads, {el:.1f} s"}, n, el
 
 
@@ -424,7 +427,7 @@ def run_reference(args, rank: int, world: int):
     cfg = synth.get_config(WORKLOAD)
     W = synth.model_weights(cfg)
     budget = max(10.0, min(120.0, args.cpu_seconds * 4))
-    cpu, n, el = cpu_baseline(cfg, W, seconds=budget, max_steps=max(2, args.steps))
+    cpu, n, el = cpu_baseline(cfg, W, seconds=budget, max_steps=max(2, args.steps), warmup=args.warmup)
     value = cpu["value"]
     line = {
         "impl": "reference",
@@ -433,7 +436,7 @@ def run_reference(args, rank: int, world: int):
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": n,
-        "warmup": 1,
+        "warmup": args.warmup,
         "ms_per_step": round(el * 1e3 / n, 3),
         "higher_is_better": True,
         "scaling": "weak",
