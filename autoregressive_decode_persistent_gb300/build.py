@@ -27,8 +27,22 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build the engine")
 
 
+def _extra_flags() -> list[str]:
+    """Extra nvcc flags from ADP_NVCC_FLAGS (e.g. -DADP_CYCLE_STAMPS for the timeline's cycle
+    breakdowns); a change of them forces a rebuild."""
+    return os.environ.get("ADP_NVCC_FLAGS", "").split()
+
+
+FLAGS_STAMP = os.path.join(HERE, "_build", "flags.txt")
+
+
 def _stale() -> bool:
     if not os.path.exists(LIB):
+        return True
+    try:
+        if open(FLAGS_STAMP).read() != " ".join(_extra_flags()):
+            return True
+    except OSError:
         return True
     t = os.path.getmtime(LIB)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
@@ -45,7 +59,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(outdir, src.replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [cc, *ARCH, *FLAGS, *_extra_flags(), "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
@@ -61,6 +75,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(FLAGS_STAMP, "w") as fh:
+        fh.write(" ".join(_extra_flags()))
     return LIB
 
 

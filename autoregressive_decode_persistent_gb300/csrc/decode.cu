@@ -62,6 +62,14 @@ __device__ __forceinline__ void set_error(const Params& p, Ctl* ctl, int32_t cod
 
 __device__ __forceinline__ bool aborted(Ctl* ctl) { return *(volatile int32_t*)&ctl->abort != 0; }
 
+// SM cycle counter for the timeline's cycle breakdowns (entries 12..15), compiled in only with
+// -DADP_CYCLE_STAMPS: the reads sit in the GEMV chunk loop.
+#ifdef ADP_CYCLE_STAMPS
+__device__ __forceinline__ long long cyc_now() { return clock64(); }
+#else
+__device__ __forceinline__ long long cyc_now() { return 0; }
+#endif
+
 // Timeline stamp k of phase ph for this CTA (debug hook; one thread writes each slot).
 __device__ __forceinline__ void stamp(const Params& p, uint32_t c, int ph, int k) {
   if (p.timeline) p.timeline[((size_t)c * p.n_phases + ph) * kStamps + k] = globaltimer();
@@ -401,7 +409,7 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
   unsigned long long best = 0ull;  // LM: packed running maximum of this warp
   long long cyc_wait = 0, cyc_comp = 0, cyc_epi = 0;  // timeline: SM cycles waiting / computing / epilogues
   const int rounds = n > 0 ? (n + upr - 1) / upr : 0;
-  const long long cyc_start = clock64();
+  const long long cyc_start = cyc_now();
   for (int r = 0; r < rounds; ++r) {
     const int m = min(upr, n - r * upr);
     const bool active = cw < m;
@@ -410,9 +418,9 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
 #pragma unroll
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = 0.0f;
     for (int ck = 0; ck < n_chunks; ++ck) {
-      const long long cy0 = clock64();
+      const long long cy0 = cyc_now();
       bool ok = aborted(ctl) || mbar_wait(&ctl->full[slot], par, &ctl->abort, wait_ns);
-      const long long cy1 = clock64();
+      const long long cy1 = cyc_now();
       cyc_wait += cy1 - cy0;
       if (!ok) {
         if (lane == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
@@ -440,7 +448,7 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
           }
         }
       }
-      cyc_comp += clock64() - cy1;
+      cyc_comp += cyc_now() - cy1;
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->empty[slot]);
       ++t;
@@ -456,7 +464,7 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
         p.timeline[((size_t)c * p.n_phases + Pd.index) * kStamps + 13] = (unsigned long long)cyc_comp;
       }
     }
-    const long long ce0 = clock64();
+    const long long ce0 = cyc_now();
     if (!active || aborted(ctl)) continue;
 #pragma unroll
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = warp_fold(acc[i]);
@@ -548,10 +556,10 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
         }
       }
     }
-    cyc_epi += clock64() - ce0;
+    cyc_epi += cyc_now() - ce0;
   }
   if (p.timeline && cw == 0 && lane == 0 && rounds > 0) {
-    p.timeline[((size_t)c * p.n_phases + Pd.index) * kStamps + 14] = (unsigned long long)(clock64() - cyc_start);
+    p.timeline[((size_t)c * p.n_phases + Pd.index) * kStamps + 14] = (unsigned long long)(cyc_now() - cyc_start);
     p.timeline[((size_t)c * p.n_phases + Pd.index) * kStamps + 15] = (unsigned long long)cyc_epi;
   }
   if (kind == PK_LM) {
@@ -766,7 +774,7 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
       ok = ok && !aborted(ctl);
       if (cw == 0 && lane == 0 && it == (int)c) stamp(p, c, P.index, 4);
       if (active && ok) {
-        const long long cs0 = clock64();
+        const long long cs0 = cyc_now();
         // score of position j0 + lane: the contract dot over the K row, its 32-slot tree in registers
         float sj = __int_as_float(0xFF800000);  // -inf
         if (lane < nvalid) {
@@ -786,7 +794,7 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
             for (int i = 0; i < off; ++i) a[i] = __fadd_rn(a[i], a[i + off]);
           sj = __fmul_rn(a[0], scale);
         }
-        const long long cs1 = clock64();
+        const long long cs1 = cyc_now();
         // block maximum and weights e_j = exp(s_j - m_b), shared with the warp through SS
         float m = sj;
 #pragma unroll
@@ -794,7 +802,7 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
         float* se = SS + hh * kAttnBlock;
         se[lane] = lane < nvalid ? exp_c(__fsub_rn(sj, m)) : 0.0f;
         __syncwarp();
-        const long long cs2 = clock64();
+        const long long cs2 = cyc_now();
         // l = sequential sum of e_j; o = sequential fma chain over j
         float l = 0.0f, o[DPL];
 #pragma unroll
@@ -833,7 +841,7 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
             }
           }
         }
-        const long long cs3 = clock64();
+        const long long cs3 = cyc_now();
         if (cw == 0 && lane == 0 && it == (int)c) stamp(p, c, P.index, 6);
         // block partial as epoch-tagged words, [head][block] and [head][block][dim]: the head's
         // merger polls them directly (no counter, no fence on this side)
@@ -850,7 +858,7 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
             tl[12] = (unsigned long long)(cs1 - cs0);
             tl[13] = (unsigned long long)(cs2 - cs1);
             tl[14] = (unsigned long long)(cs3 - cs2);
-            tl[15] = (unsigned long long)(clock64() - cs3);
+            tl[15] = (unsigned long long)(cyc_now() - cs3);
           }
         }
       }

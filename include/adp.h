@@ -215,8 +215,11 @@ int adp_debug_trace_residual(adp_model* m, float* dev_buf);
  * warp 0), 4 first and 5 last weight tile issued (producer warp), 7 ns the producer spent with
  * the ring full; weighted phases: 8 first tile ready and 9 last K-chunk done (consumer warp 0);
  * attention: 4 first item's data staged, 6 its block computed, 5 its partial published, 7 all
- * items done, 10 first merge's partials loaded, 11 its outputs published.  Unused entries keep what the buffer held.  NULL = off.  Sizes from
- * adp_debug_timeline_shape. */
+ * items done, 10 a merged head's partials seen, 12 its weights formed, 13 its outputs summed,
+ * 11 published.  In builds with -DADP_CYCLE_STAMPS entries 12..15 of weighted phases hold SM
+ * cycles of consumer warp 0 (waiting for tiles, computing, whole round loop, epilogues) and of
+ * the first attention item (scores, weights, weighted sum, publication).  Unused entries keep
+ * what the buffer held.  NULL = off.  Sizes from adp_debug_timeline_shape. */
 int adp_debug_timeline(adp_model* m, uint64_t* dev_buf);
 int adp_debug_timeline_shape(const adp_model* m, int32_t* ctas, int32_t* phases);
 /* 1: also take a grid barrier after every phase (debugging the epoch-tagged exchange). */
