@@ -45,6 +45,7 @@ struct Ctl {
   float stage[1024];  // router logits or sampling block sums, loaded in one batch
   uint64_t att_bar[kAttnSlots];  // TMA completion of each attention slot's K/V block
   uint64_t merge_bar;            // TMA completion of the attention merge's block outputs
+  int32_t bcast_tok;             // the token of the next step of a multi-step launch
   float rope_cs[128], rope_sn[128];  // RoPE row of this step's position (QKV epilogue)
   float xres[64];                    // residual rows this CTA updates (Wo / down epilogues)
 };
@@ -134,66 +135,70 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
   bool stop = false;
   L2Cursor cur{ph0, 0, 0};
   uint64_t issue_pos = 0;  // stream position of the next dense tile
-  for (int ph = ph0; ph < ph1 && !stop; ++ph) {
-    const PhaseDesc P = phase_table(ctl)[ph];
-    if (!P.has_weights) continue;
-    int32_t u0, n;
-    cta_units(P, c, G, u0, n);
-    const bool expert = P.kind == PK_EGU || P.kind == PK_EDOWN;
-    if (!expert && cur.ph < ph) cur = L2Cursor{ph, 0, issue_pos};  // behind, or waited at the experts
-    if (expert && sel_layer != P.layer) {
-      // expert weights are known only after routing: wait for this layer's selection
-      if (!mbar_wait(&ctl->sel_bar, sel_uses & 1, &ctl->abort, p.wait_ns)) {
-        if (!aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
-        break;
+  for (int step = 0; step < p.n_steps && !stop; ++step) {  // the launch's decode steps
+    sel_layer = -1;
+    cur = L2Cursor{ph0, 0, issue_pos};
+    for (int ph = ph0; ph < ph1 && !stop; ++ph) {
+      const PhaseDesc P = phase_table(ctl)[ph];
+      if (!P.has_weights) continue;
+      int32_t u0, n;
+      cta_units(P, c, G, u0, n);
+      const bool expert = P.kind == PK_EGU || P.kind == PK_EDOWN;
+      if (!expert && cur.ph < ph) cur = L2Cursor{ph, 0, issue_pos};  // behind, or waited at the experts
+      if (expert && sel_layer != P.layer) {
+        // expert weights are known only after routing: wait for this layer's selection
+        if (!mbar_wait(&ctl->sel_bar, sel_uses & 1, &ctl->abort, p.wait_ns)) {
+          if (!aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
+          break;
+        }
+        ++sel_uses;
+        sel_layer = P.layer;
       }
-      ++sel_uses;
-      sel_layer = P.layer;
-    }
-    if (n <= 0) continue;
-    const uint64_t unit_bytes = (uint64_t)P.unit_rows * P.K * P.eb;
-    const uint8_t* base = p.image + P.region + (uint64_t)u0 * unit_bytes;
-    const int rounds = (n + P.upr - 1) / P.upr;
-    bool first = true;
-    uint64_t blocked = 0;  // ns spent with the ring full (timeline only)
-    for (int r = 0; r < rounds && !stop; ++r) {
-      const int m = min(P.upr, n - r * P.upr);
-      const uint64_t round_off = (uint64_t)r * P.upr * unit_bytes;
-      for (int ck = 0; ck < P.n_chunks; ++ck) {
-        if (aborted(ctl)) { stop = true; break; }
-        const int kck = min(P.KC, P.K - ck * P.KC);
-        const uint32_t bytes = (uint32_t)m * P.unit_rows * kck * P.eb;
-        const uint64_t off = round_off + (uint64_t)m * P.unit_rows * ck * P.KC * P.eb;
-        const uint32_t slot = t % ns, use = t / ns;
-        if (t >= ns) {
-          if (!mbar_try_wait(&ctl->empty[slot], (use - 1) & 1)) {
-            const uint64_t tb = p.timeline ? globaltimer() : 0;
-            l2_advance(p, ctl, cur, issue_pos, ph1, c, G);  // keep HBM busy while the consumers catch up
-            if (!mbar_wait(&ctl->empty[slot], (use - 1) & 1, &ctl->abort, p.wait_ns)) {
-              if (!aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
-              stop = true;
-              break;
+      if (n <= 0) continue;
+      const uint64_t unit_bytes = (uint64_t)P.unit_rows * P.K * P.eb;
+      const uint8_t* base = p.image + P.region + (uint64_t)u0 * unit_bytes;
+      const int rounds = (n + P.upr - 1) / P.upr;
+      bool first = true;
+      uint64_t blocked = 0;  // ns spent with the ring full (timeline only)
+      for (int r = 0; r < rounds && !stop; ++r) {
+        const int m = min(P.upr, n - r * P.upr);
+        const uint64_t round_off = (uint64_t)r * P.upr * unit_bytes;
+        for (int ck = 0; ck < P.n_chunks; ++ck) {
+          if (aborted(ctl)) { stop = true; break; }
+          const int kck = min(P.KC, P.K - ck * P.KC);
+          const uint32_t bytes = (uint32_t)m * P.unit_rows * kck * P.eb;
+          const uint64_t off = round_off + (uint64_t)m * P.unit_rows * ck * P.KC * P.eb;
+          const uint32_t slot = t % ns, use = t / ns;
+          if (t >= ns) {
+            if (!mbar_try_wait(&ctl->empty[slot], (use - 1) & 1)) {
+              const uint64_t tb = p.timeline ? globaltimer() : 0;
+              l2_advance(p, ctl, cur, issue_pos, ph1, c, G);  // keep HBM busy while the consumers catch up
+              if (!mbar_wait(&ctl->empty[slot], (use - 1) & 1, &ctl->abort, p.wait_ns)) {
+                if (!aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
+                stop = true;
+                break;
+              }
+              if (p.timeline) blocked += globaltimer() - tb;
             }
-            if (p.timeline) blocked += globaltimer() - tb;
           }
+          if (first) {
+            stamp(p, c, ph, 4);
+            first = false;
+          }
+          mbar_arrive_expect_tx(&ctl->full[slot], bytes * P.slots);
+          uint8_t* dst = ring + (size_t)slot * kSlotBytes;
+          for (int s = 0; s < P.slots; ++s) {
+            const uint8_t* src = base + off;
+            if (expert) src += (uint64_t)(*(volatile int32_t*)&ctl->sel[s]) * P.expert_stride;
+            tma_load_1d(dst + (size_t)s * bytes, src, bytes, &ctl->full[slot], pol);
+          }
+          if (!expert) issue_pos += bytes;
+          ++t;
         }
-        if (first) {
-          stamp(p, c, ph, 4);
-          first = false;
-        }
-        mbar_arrive_expect_tx(&ctl->full[slot], bytes * P.slots);
-        uint8_t* dst = ring + (size_t)slot * kSlotBytes;
-        for (int s = 0; s < P.slots; ++s) {
-          const uint8_t* src = base + off;
-          if (expert) src += (uint64_t)(*(volatile int32_t*)&ctl->sel[s]) * P.expert_stride;
-          tma_load_1d(dst + (size_t)s * bytes, src, bytes, &ctl->full[slot], pol);
-        }
-        if (!expert) issue_pos += bytes;
-        ++t;
       }
+      stamp(p, c, ph, 5);
+      if (p.timeline) p.timeline[((size_t)c * p.n_phases + ph) * kStamps + 7] = blocked;
     }
-    stamp(p, c, ph, 5);
-    if (p.timeline) p.timeline[((size_t)c * p.n_phases + ph) * kStamps + 7] = blocked;
   }
   // No bulk copy may still be writing this CTA's shared memory when it exits.
   int32_t never = 0;
@@ -584,8 +589,12 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
 
 // ---------------------------------------------------------------- finalisation
 
+// The step's token: into the step state and output sequence for the host, and as an
+// epoch-tagged word for the next step of the same launch (which every CTA waits on before it
+// gathers the embedding row).  Called after the step's shared counters are reset.
 __device__ void finalize_token(const Params& p, const Step& st, int32_t token) {
-  *p.epoch = st.ebase + (uint32_t)p.n_phases;  // the next step's phases publish new epochs
+  const uint32_t next = st.ebase + (uint32_t)p.n_phases;  // the next step's epoch base
+  *p.epoch = next;
   StepState* s = p.state;
   s->out_token = token;
   if (p.out_seq) p.out_seq[st.seq_index] = token;
@@ -593,6 +602,7 @@ __device__ void finalize_token(const Params& p, const Step& st, int32_t token) {
   s->pos = st.pos + 1;
   s->seq_index = st.seq_index + 1;
   __threadfence();
+  ll_store(p.tok_word, ll_pack_bits((uint32_t)token, next));
 }
 
 // ---------------------------------------------------------------- attention phase
@@ -1029,9 +1039,9 @@ __device__ __forceinline__ void sample_phase(const Params& p, Ctl* ctl, const St
     }
     if (token < 0) token = lastpos;
     if (lane == 0) {
-      finalize_token(p, st, token);
       *p.argkey = 0ull;
       *p.sample_ctr = 0u;
+      finalize_token(p, st, token);
     }
   }
 }
@@ -1080,148 +1090,169 @@ __device__ void run_expert(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf
 }
 
 template <bool MOE>
-__device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, const Step& st, uint32_t c,
+__device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, Step st, uint32_t c,
                          uint32_t G, int ph0, int ph1, bool use_barrier, int cw, int lane) {
   uint32_t t = 0;
   int bidx = 0;
   int sel_layer = -1;
   uint32_t att_uses = 0, merge_uses = 0;
   const int tid = cw * 32 + lane;
-  for (int ph = ph0; ph < ph1; ++ph) {
-    // every warp of this CTA has left the previous phase before this one reuses the shared input
-    // vector, the staging areas and the staged residual rows
-    if (ph > ph0) consumer_sync();
-    const PhaseDesc P = phase_table(ctl)[ph];
-    const int L = P.layer;
-    const bool ab = aborted(ctl);
-    // epochs: what this phase publishes (0 = withheld by the test hook) and what it reads
-    const uint32_t ew = ((int)c == p.skip_cta && ph == p.skip_phase) ? 0u : st.ebase + 1 + (uint32_t)ph;
-    const uint32_t e_src = st.ebase + 1 + (uint32_t)P.src_ph;
-    const uint32_t e_res = st.ebase + 1 + (uint32_t)P.res_ph;
-    const uint32_t e_sel = st.ebase + 1 + (uint32_t)P.sel_ph;
-    int32_t u0, n;
-    cta_units(P, c, G, u0, n);
-    if (cw == 0 && lane == 0) stamp(p, c, ph, 0);
-    // ---- prologue: the GEMV input vector into shared memory (skipped by CTAs without units)
-    switch (P.kind) {
-      case PK_QKV: {
-        const void* emb = L == 0 ? (const uint8_t*)p.tok_emb + (size_t)st.token * p.d * 2 : nullptr;
-        if (L == 0 && !ab) {  // the residual starts as the embedding row: publish this CTA's slice
-          const int a = (int)((long long)c * p.d / G), b = (int)((long long)(c + 1) * p.d / G);
-          for (int i = a + tid; i < b; i += kConsumerWarps * 32)
-            ll_store(p.x + i, ll_pack(load_elem(emb, (size_t)i, p.wdt), ew));
+  for (int step = 0; step < p.n_steps; ++step) {
+    if (step > 0) {
+      // the next step of this launch: its position, epochs and inputs follow from the last one,
+      // except the token, which the step's last CTA publishes
+      st.ebase += (uint32_t)p.n_phases;
+      st.pos += 1;
+      st.seq_index += 1;
+      if (p.u_seq) st.u = __ldcg(p.u_seq + st.seq_index);
+      if (p.tok_seq) {
+        st.token = __ldcg(p.tok_seq + st.seq_index);
+      } else {
+        if (tid == 0) {
+          ll_t w = ll_load(p.tok_word);
+          ctl->bcast_tok = ll_wait(p.tok_word, st.ebase, w, p, ctl) ? (int32_t)(uint32_t)w : 0;
         }
-        if (cw == kConsumerWarps - 1 && lane == 0 && !ab) prefetch_attention_kv(p, L, st.pos + 1, c, G);
-        if (n > 0) {
-          const int half = p.hd / 2;  // the RoPE row of this position, for the epilogue
-          if (tid < half) {
-            ctl->rope_cs[tid] = __ldg(p.rope_cos + (size_t)st.pos * half + tid);
-            ctl->rope_sn[tid] = __ldg(p.rope_sin + (size_t)st.pos * half + tid);
-          }
-          rmsnorm_prologue(p, ctl, xbuf, p.attn_norm[L], emb, e_src, L, c, cw, lane);
-        }
-        break;
+        consumer_sync();
+        st.token = ctl->bcast_tok;
       }
-      case PK_WO:
-        if (n > 0) {
-          stage_residual(p, ctl, P, c, G, 2, e_res, cw, lane);
-          ll_fetch(p, ctl, xbuf, p.attn, p.hq * p.hd, p.hq * p.hd, 0, e_src, tid);
+      sel_layer = -1;
+    }
+    for (int ph = ph0; ph < ph1; ++ph) {
+      // every warp of this CTA has left the previous phase before this one reuses the shared input
+      // vector, the staging areas and the staged residual rows
+      if (ph > ph0 || step > 0) consumer_sync();
+      const PhaseDesc P = phase_table(ctl)[ph];
+      const int L = P.layer;
+      const bool ab = aborted(ctl);
+      // epochs: what this phase publishes (0 = withheld by the test hook) and what it reads
+      const uint32_t ew = ((int)c == p.skip_cta && ph == p.skip_phase) ? 0u : st.ebase + 1 + (uint32_t)ph;
+      const uint32_t e_src = st.ebase + 1 + (uint32_t)P.src_ph;
+      const uint32_t e_res = st.ebase + 1 + (uint32_t)P.res_ph;
+      const uint32_t e_sel = st.ebase + 1 + (uint32_t)P.sel_ph;
+      int32_t u0, n;
+      cta_units(P, c, G, u0, n);
+      if (cw == 0 && lane == 0) stamp(p, c, ph, 0);
+      // ---- prologue: the GEMV input vector into shared memory (skipped by CTAs without units)
+      switch (P.kind) {
+        case PK_QKV: {
+          const void* emb = L == 0 ? (const uint8_t*)p.tok_emb + (size_t)st.token * p.d * 2 : nullptr;
+          if (L == 0 && !ab) {  // the residual starts as the embedding row: publish this CTA's slice
+            const int a = (int)((long long)c * p.d / G), b = (int)((long long)(c + 1) * p.d / G);
+            for (int i = a + tid; i < b; i += kConsumerWarps * 32)
+              ll_store(p.x + i, ll_pack(load_elem(emb, (size_t)i, p.wdt), ew));
+          }
+          if (cw == kConsumerWarps - 1 && lane == 0 && !ab) prefetch_attention_kv(p, L, st.pos + 1, c, G);
+          if (n > 0) {
+            const int half = p.hd / 2;  // the RoPE row of this position, for the epilogue
+            if (tid < half) {
+              ctl->rope_cs[tid] = __ldg(p.rope_cos + (size_t)st.pos * half + tid);
+              ctl->rope_sn[tid] = __ldg(p.rope_sin + (size_t)st.pos * half + tid);
+            }
+            rmsnorm_prologue(p, ctl, xbuf, p.attn_norm[L], emb, e_src, L, c, cw, lane);
+          }
+          break;
         }
-        break;
-      case PK_DOWN:
-        if (n > 0) {
-          stage_residual(p, ctl, P, c, G, 2, e_res, cw, lane);
-          ll_fetch(p, ctl, xbuf, p.h, p.ff, p.ff, 0, e_src, tid);
-        }
-        break;
-      case PK_EDOWN:
-        if constexpr (MOE) {
-          if (sel_layer != L) {
+        case PK_WO:
+          if (n > 0) {
+            stage_residual(p, ctl, P, c, G, 2, e_res, cw, lane);
+            ll_fetch(p, ctl, xbuf, p.attn, p.hq * p.hd, p.hq * p.hd, 0, e_src, tid);
+          }
+          break;
+        case PK_DOWN:
+          if (n > 0) {
+            stage_residual(p, ctl, P, c, G, 2, e_res, cw, lane);
+            ll_fetch(p, ctl, xbuf, p.h, p.ff, p.ff, 0, e_src, tid);
+          }
+          break;
+        case PK_EDOWN:
+          if constexpr (MOE) {
+            if (sel_layer != L) {
+              if (cw == 0) {
+                select_experts(p, ctl, L, e_sel, lane);
+                if (lane == 0) mbar_arrive(&ctl->sel_bar);
+              }
+              sel_layer = L;
+            }
+            if (n > 0) {
+              stage_residual(p, ctl, P, c, G, 1, e_res, cw, lane);
+              ll_fetch(p, ctl, xbuf, p.h, p.topk * p.fexp, p.fexp, (p.fexp + 255) & ~255, e_src, tid);
+            } else {
+              consumer_sync();  // the choice (shared memory) is read by every warp's epilogue
+            }
+          }
+          break;
+        case PK_GU:
+        case PK_ROUTER:
+          if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, e_src, -1, c, cw, lane);
+          break;
+        case PK_EGU:
+          if constexpr (MOE) {
             if (cw == 0) {
               select_experts(p, ctl, L, e_sel, lane);
-              if (lane == 0) mbar_arrive(&ctl->sel_bar);
+              if (lane == 0) {
+                if (c == 0 && !ab) for (int i = 0; i < p.topk; ++i) p.sel_out[L * p.topk + i] = ctl->sel[i];
+                mbar_arrive(&ctl->sel_bar);  // release the choice to the producer
+              }
             }
             sel_layer = L;
+            if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, e_src, -1, c, cw, lane);
+            else consumer_sync();
           }
-          if (n > 0) {
-            stage_residual(p, ctl, P, c, G, 1, e_res, cw, lane);
-            ll_fetch(p, ctl, xbuf, p.h, p.topk * p.fexp, p.fexp, (p.fexp + 255) & ~255, e_src, tid);
-          } else {
-            consumer_sync();  // the choice (shared memory) is read by every warp's epilogue
-          }
+          break;
+        case PK_LM:
+          if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.final_norm, nullptr, e_src, p.L, c, cw, lane);
+          break;
+        default: break;
+      }
+      // ---- body
+      if (cw == 0 && lane == 0) stamp(p, c, ph, 1);
+      if (P.kind == PK_ATTN) {
+        if (p.kvdt == DT_BF16) {
+          if (p.hd == 128) attention_phase<128, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+          else if (p.hd == 64) attention_phase<64, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+          else attention_phase<256, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+        } else {
+          if (p.hd == 128) attention_phase<128, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+          else if (p.hd == 64) attention_phase<64, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+          else attention_phase<256, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
         }
-        break;
-      case PK_GU:
-      case PK_ROUTER:
-        if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, e_src, -1, c, cw, lane);
-        break;
-      case PK_EGU:
+      } else if (P.kind == PK_SAMPLE) {
+        if (st.temperature > 0.0f) sample_phase(p, ctl, st, c, G, cw, lane);
+      } else if (P.kind == PK_EGU || P.kind == PK_EDOWN) {
         if constexpr (MOE) {
-          if (cw == 0) {
-            select_experts(p, ctl, L, e_sel, lane);
-            if (lane == 0) {
-              if (c == 0 && !ab) for (int i = 0; i < p.topk; ++i) p.sel_out[L * p.topk + i] = ctl->sel[i];
-              mbar_arrive(&ctl->sel_bar);  // release the choice to the producer
-            }
+          switch (p.topk) {
+            case 1: run_expert<1>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
+            case 2: run_expert<2>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
+            case 4: run_expert<4>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
+            default: run_expert<8>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
           }
-          sel_layer = L;
-          if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, e_src, -1, c, cw, lane);
-          else consumer_sync();
         }
-        break;
-      case PK_LM:
-        if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.final_norm, nullptr, e_src, p.L, c, cw, lane);
-        break;
-      default: break;
-    }
-    // ---- body
-    if (cw == 0 && lane == 0) stamp(p, c, ph, 1);
-    if (P.kind == PK_ATTN) {
-      if (p.kvdt == DT_BF16) {
-        if (p.hd == 128) attention_phase<128, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
-        else if (p.hd == 64) attention_phase<64, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
-        else attention_phase<256, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+      } else if (P.kind == PK_ROUTER) {
+        if constexpr (MOE) {
+          if (p.rdt == DT_BF16) gemv_phase<1, 1, DT_BF16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+          else gemv_phase<1, 1, DT_F16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+        }
       } else {
-        if (p.hd == 128) attention_phase<128, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
-        else if (p.hd == 64) attention_phase<64, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
-        else attention_phase<256, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+        if (p.wdt == DT_BF16) run_gemv<DT_BF16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+        else run_gemv<DT_F16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
       }
-    } else if (P.kind == PK_SAMPLE) {
-      if (st.temperature > 0.0f) sample_phase(p, ctl, st, c, G, cw, lane);
-    } else if (P.kind == PK_EGU || P.kind == PK_EDOWN) {
-      if constexpr (MOE) {
-        switch (p.topk) {
-          case 1: run_expert<1>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
-          case 2: run_expert<2>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
-          case 4: run_expert<4>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
-          default: run_expert<8>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew); break;
-        }
+      // ---- the LM head's last CTA picks the greedy token
+      if (P.kind == PK_LM && ctl->flag && st.temperature <= 0.0f && cw == 0 && lane == 0) {
+        __threadfence();
+        const unsigned long long key = atomicAdd(p.argkey, 0ull);
+        *p.argkey = 0ull;
+        *p.lm_ctr = 0u;
+        finalize_token(p, st, (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull)));
+      } else if (P.kind == PK_LM && ctl->flag && cw == 0 && lane == 0) {
+        *p.lm_ctr = 0u;  // sampling: the maximum stays in argkey for the sampling phase
       }
-    } else if (P.kind == PK_ROUTER) {
-      if constexpr (MOE) {
-        if (p.rdt == DT_BF16) gemv_phase<1, 1, DT_BF16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
-        else gemv_phase<1, 1, DT_F16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
-      }
-    } else {
-      if (p.wdt == DT_BF16) run_gemv<DT_BF16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
-      else run_gemv<DT_F16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+      if (cw == 0 && lane == 0) stamp(p, c, ph, 2);
+      // ---- dependent phases wait on the epochs of their inputs; only sampling, which needs the
+      // maximum over every CTA's logits, takes a grid barrier
+      if (use_barrier && ph + 1 < ph1 && ((P.kind == PK_LM && st.temperature > 0.0f) || p.debug_barriers))
+        grid_barrier(p, ctl, c, G, bidx);
+      if (cw == 0 && lane == 0) stamp(p, c, ph, 3);
     }
-    // ---- the LM head's last CTA picks the greedy token
-    if (P.kind == PK_LM && ctl->flag && st.temperature <= 0.0f && cw == 0 && lane == 0) {
-      __threadfence();
-      const unsigned long long key = atomicAdd(p.argkey, 0ull);
-      finalize_token(p, st, (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull)));
-      *p.argkey = 0ull;
-      *p.lm_ctr = 0u;
-    } else if (P.kind == PK_LM && ctl->flag && cw == 0 && lane == 0) {
-      *p.lm_ctr = 0u;  // sampling: the maximum stays in argkey for the sampling phase
-    }
-    if (cw == 0 && lane == 0) stamp(p, c, ph, 2);
-    // ---- dependent phases wait on the epochs of their inputs; only sampling, which needs the
-    // maximum over every CTA's logits, takes a grid barrier
-    if (use_barrier && ph + 1 < ph1 && ((P.kind == PK_LM && st.temperature > 0.0f) || p.debug_barriers))
-      grid_barrier(p, ctl, c, G, bidx);
-    if (cw == 0 && lane == 0) stamp(p, c, ph, 3);
   }
 }
 

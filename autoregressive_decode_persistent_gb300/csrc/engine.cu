@@ -77,7 +77,7 @@ struct adp_model {
   const void* graph_key_logits = nullptr;
   bool graph_key_sample = false;
   int sticky = ADP_OK;
-  size_t ll_bytes[10] = {0};  // sizes of the epoch-tagged exchange buffers
+  size_t ll_bytes[11] = {0};  // sizes of the epoch-tagged exchange buffers
 
   template <class T>
   int alloc(T** ptr, size_t count) {
@@ -211,8 +211,8 @@ static void plan(adp_model* m) {
 // Zero the epoch base and every epoch-tagged exchange buffer (epoch 0 is never awaited).
 static int clear_exchange(adp_model* m) {
   const Params& p = m->p;
-  void* bufs[10] = {p.x, p.q, p.attn, p.h, p.rlog, p.knew, p.vnew, p.part_m, p.part_l, p.part_o};
-  for (int i = 0; i < 10; ++i) CK(cudaMemsetAsync(bufs[i], 0, m->ll_bytes[i], m->stream));
+  void* bufs[11] = {p.x, p.q, p.attn, p.h, p.rlog, p.knew, p.vnew, p.part_m, p.part_l, p.part_o, p.tok_word};
+  for (int i = 0; i < 11; ++i) CK(cudaMemsetAsync(bufs[i], 0, m->ll_bytes[i], m->stream));
   CK(cudaMemsetAsync(p.epoch, 0, 4, m->stream));
   return ADP_OK;
 }
@@ -367,6 +367,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   if ((rc = m->alloc(&p.x, d)) || (rc = m->alloc(&p.q, hq * hd)) || (rc = m->alloc(&p.attn, hq * hd)) ||
       (rc = m->alloc(&p.h, ffw)) || (rc = m->alloc(&p.rlog, std::max(c.n_experts, 1))) ||
       (rc = m->alloc(&p.knew, hkv * hd)) || (rc = m->alloc(&p.vnew, hkv * hd)) || (rc = m->alloc(&p.epoch, 1)) ||
+      (rc = m->alloc(&p.tok_word, 1)) ||
       (rc = m->alloc(&p.part_m, (size_t)hq * nbmax)) || (rc = m->alloc(&p.part_l, (size_t)hq * nbmax)) ||
       (rc = m->alloc(&p.part_o, (size_t)hq * nbmax * hd)) ||
       (rc = m->alloc(&p.sblock, nblk)) || (rc = m->alloc(&p.sample_ctr, 1)) || (rc = m->alloc(&p.argkey, 1)) ||
@@ -384,6 +385,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   m->ll_bytes[7] = (size_t)hq * nbmax * 8;
   m->ll_bytes[8] = (size_t)hq * nbmax * 8;
   m->ll_bytes[9] = (size_t)hq * nbmax * hd * 8;
+  m->ll_bytes[10] = 8;
   if ((rc = clear_exchange(m))) return rc;
   CK(cudaMemsetAsync(p.sample_ctr, 0, 4, m->stream));
   CK(cudaMemsetAsync(p.argkey, 0, 8, m->stream));
@@ -417,6 +419,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   p.rope_sin = d_sin;
   p.wait_ns = 200000000ull;
   p.l2_lookahead = 0;
+  p.n_steps = 1;
   p.skip_cta = -1;
   p.skip_phase = -1;
   CK(cudaStreamSynchronize(m->stream));
@@ -574,6 +577,24 @@ static Params step_params(adp_model* m, adp_kv* kv, float* logits, const int32_t
   return p;
 }
 
+static int enqueue_step(adp_model* m, const Params& p, bool sampling);
+
+// Enqueue n decode steps: in the persistent mode one launch that runs them back to back (each
+// step takes the token the previous one chose, or the next of p.tok_seq); in the ablation modes
+// the launches of one step, n times.
+static int enqueue_steps(adp_model* m, const Params& p, bool sampling, int n) {
+  if (m->mode == 0) {
+    Params q = p;
+    q.n_steps = n;
+    return enqueue_step(m, q, sampling);
+  }
+  for (int i = 0; i < n; ++i) {
+    const int rc = enqueue_step(m, p, sampling);
+    if (rc) return rc;
+  }
+  return ADP_OK;
+}
+
 // Enqueue the launches of one decode step in the model's kernel mode.
 static int enqueue_step(adp_model* m, const Params& p, bool sampling) {
   const int nph = (int)m->phases.size();
@@ -659,9 +680,10 @@ extern "C" int adp_prefill(adp_model* m, adp_kv* kv, const int32_t* host_tokens,
   const float T = sampling ? sampling->temperature : 0.0f;
   int rs = put_state(m, kv->len, 0, T, sampling ? sampling->u : 0.0f);
   if (rs) return rs;
-  for (int i = 0; i < n; ++i) {
-    Params p = step_params(m, kv, i == n - 1 ? dev_logits : nullptr, m->d_tokseq, nullptr, nullptr);
-    int rc = enqueue_step(m, p, T > 0.0f);
+  {
+    // every step writes its logits to the same place: the last step's remain
+    Params p = step_params(m, kv, dev_logits, m->d_tokseq, nullptr, nullptr);
+    int rc = enqueue_steps(m, p, T > 0.0f, n);
     if (rc) return rc;
   }
   m->p.skip_cta = m->p.skip_phase = -1;
@@ -683,10 +705,8 @@ extern "C" int adp_generate_async(adp_model* m, adp_kv* kv, int32_t token, int32
   int rs = put_state(m, kv->len, token, temperature, 0.0f);
   if (rs) return rs;
   Params p = step_params(m, kv, nullptr, nullptr, temperature > 0.0f ? dev_u : nullptr, dev_tokens_out);
-  for (int i = 0; i < n; ++i) {
-    int rc = enqueue_step(m, p, temperature > 0.0f);
-    if (rc) return rc;
-  }
+  int rc = enqueue_steps(m, p, temperature > 0.0f, n);
+  if (rc) return rc;
   kv->len += n;
   return ADP_OK;
 }
@@ -758,6 +778,7 @@ int adp::scratch_layout(const adp_model* m, ScratchLayout* out) {
   l.knew = take(hkv * hd * 8);
   l.vnew = take(hkv * hd * 8);
   l.epoch = take(4);
+  l.tok_word = take(8);
   l.part_m = take(hq * nbmax * 8);
   l.part_l = take(hq * nbmax * 8);
   l.part_o = take(hq * nbmax * hd * 8);
@@ -803,6 +824,8 @@ int adp::decode_step_in_scratch(adp_model* m, adp_kv* kv, int32_t token, const a
   p.knew = reinterpret_cast<unsigned long long*>(at(lay.knew));
   p.vnew = reinterpret_cast<unsigned long long*>(at(lay.vnew));
   p.epoch = reinterpret_cast<uint32_t*>(at(lay.epoch));
+  p.tok_word = reinterpret_cast<unsigned long long*>(at(lay.tok_word));
+  p.n_steps = 1;
   p.part_m = reinterpret_cast<unsigned long long*>(at(lay.part_m));
   p.part_l = reinterpret_cast<unsigned long long*>(at(lay.part_l));
   p.part_o = reinterpret_cast<unsigned long long*>(at(lay.part_o));

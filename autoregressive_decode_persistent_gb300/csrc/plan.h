@@ -109,6 +109,7 @@ struct Params {
   unsigned long long* h;     // [max(ff, topk*f)] FFN activations
   unsigned long long* rlog;  // [E] router logits
   uint32_t* epoch;           // epoch base of the next step (advanced by the step's last CTA)
+  unsigned long long* tok_word;  // the token a step chose, tagged with the next step's epoch base
   unsigned long long* part_m;  // [hq][nbmax] attention block maxima (epoch-tagged)
   unsigned long long* part_l;  // [hq][nbmax] attention block sums (epoch-tagged)
   unsigned long long* part_o;  // [hq][nbmax][hd] attention block outputs (epoch-tagged)
@@ -130,6 +131,7 @@ struct Params {
   uint64_t wait_ns;            // limit of every in-kernel wait
   uint32_t l2_lookahead;       // bytes of weight stream prefetched into L2 beyond the TMA loads
   int32_t debug_barriers;      // 1: also take a grid barrier after every phase (debugging)
+  int32_t n_steps;             // decode steps this launch runs back to back (persistent launch)
   int32_t nslots;              // weight ring depth (slots of kSlotBytes)
   int32_t skip_cta, skip_phase;  // test hook: that CTA does not publish that phase's outputs
 };

@@ -12,7 +12,7 @@ namespace adp {
 // sampling and argmax words, the grid-barrier counter, the error word, the router choices, the
 // step state and the logits.  Each region starts at a multiple of 256 bytes.
 struct ScratchLayout {
-  size_t x, q, attn, h, rlog, knew, vnew, epoch, part_m, part_l, part_o, sblock, sample_ctr, argkey,
+  size_t x, q, attn, h, rlog, knew, vnew, epoch, tok_word, part_m, part_l, part_o, sblock, sample_ctr, argkey,
       lm_ctr, bar_ctr, err, sel_out, state, logits;
   size_t total;
 };

@@ -11,8 +11,9 @@ Printed (one JSON line, rank 0):
              and KV resident in HBM, CUDA events around the timed region on the model's stream;
   e2e        tokens/s through adp_decode_step with the token in and out of host memory every
              step (a 32-byte step state host->device, 8 bytes device->host, one sync per step);
-  roofline   algorithmic bytes per launch (every weight once + KV of the context + the new KV
-             row) / average launch duration, against the measured HBM copy bandwidth;
+  roofline   algorithmic bytes per launch (per step: every weight once + KV of the context + the
+             new KV row; up to 512 steps per launch) / average launch duration, against the
+             measured HBM copy bandwidth;
   cpu_baseline  the CPU oracle (plain fp32, all host cores) timed on a bounded sample.
 
 --impl reference times the CPU oracle as the reference arm on the same workload.
@@ -59,14 +60,15 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic(src_hash: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    """DRAM bytes per decode step from the committed ncu summary, if it was taken on this kernel
+    source (a launch of n chained steps moves n times as much)."""
     path = os.path.join(ROOT, "profiles", "decode_kernel_dense-2.3b-fp16.md")
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:
         return None
     m_hash = re.search(r"kernel source sha256\[:16\]:\s*`?([0-9a-f]{16})", text)
-    m_tr = re.search(r"traffic bytes per launch:\s*`?([0-9.e+]+)", text)
+    m_tr = re.search(r"traffic bytes per step:\s*`?([0-9.e+]+)", text)
     if not m_hash or not m_tr or m_hash.group(1) != src_hash:
         return None
     return float(m_tr.group(1))
@@ -261,8 +263,9 @@ def run_engine(args, rank: int, world: int):
         k = min(left, WINDOW)
         total_bytes += bound.mean_bytes_per_token(cfg, P + 1, k) * k
         left -= k
-    per_launch = total_bytes / args.steps
-    launch_ms = ms / args.steps
+    n_launch = -(-args.steps // WINDOW)  # one launch per window of chained steps
+    per_launch = total_bytes / n_launch
+    launch_ms = ms / n_launch
     peak, peak_kind = _peaks()
     achieved = per_launch / (launch_ms * 1e-3) / 1e9
 
@@ -286,10 +289,11 @@ def run_engine(args, rank: int, world: int):
         write_timeline(args.timeline, model, kv, tok0, P, cfg)
 
     res = {
-        "ms": ms, "steps": args.steps, "achieved_gbs": achieved, "per_launch_bytes": per_launch,
+        "ms": ms, "steps": args.steps, "n_launch": n_launch, "achieved_gbs": achieved, "per_launch_bytes": per_launch,
         "launch_ms": launch_ms, "peak": peak, "peak_kind": peak_kind, "e2e": e2e, "n_e2e": n_e2e,
         "clocks": clocks.summary(), "ctas": model.num_ctas, "image_bytes": model.image_bytes,
-        "launches": model.launches_per_step * args.steps, "ablation": ablation,
+        # one cooperative launch per window of chained steps (adp_generate_async)
+        "launches": -(-args.steps // WINDOW) * model.launches_per_step, "ablation": ablation,
     }
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu"] = cpu_baseline(cfg, W, seconds=args.cpu_seconds)[0]
@@ -392,7 +396,8 @@ def emit_engine(args, cfg, res, world):
                         "batch 1, prompt 512, greedy decode at contexts 513..1024",
             "weights": "f16", "kv_cache": "f16", "batch": 1, "prompt": cfg["prompt_len"],
             "contexts": f"{cfg['prompt_len'] + 1}..{cfg['prompt_len'] + min(res['steps'], WINDOW)}",
-            "kernel": "persistent (one cooperative launch per decode step)",
+            "kernel": "persistent: one cooperative launch per window of up to 512 chained decode steps "
+                      "(e2e: one launch per step)",
             "ctas": res["ctas"],
             "l2": "inputs larger than L2: every step streams 4.69 GB of weights (L2 129 MB)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -402,7 +407,9 @@ def emit_engine(args, cfg, res, world):
                 "path": "adp_decode_step per token (host token in, host token out, stream sync)"},
         "roofline": {"bound": "hbm", "achieved": round(res["achieved_gbs"], 1), "peak": res["peak"],
                      "unit": "GB/s", "frac": round(res["achieved_gbs"] / res["peak"], 4),
-                     "traffic": profiled_traffic(src), "kernel": "adp::decode_kernel",
+                     "traffic": (None if profiled_traffic(src) is None
+                                 else round(profiled_traffic(src) * res["steps"] / res["n_launch"])),
+                     "kernel": "adp::decode_kernel",
                      "bytes_per_launch": int(res["per_launch_bytes"]),
                      "launch_ms": round(res["launch_ms"], 5),
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({res['peak_kind']}; read+write copy)",

@@ -179,9 +179,13 @@ int adp_prefill(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t n,
                 int32_t* next_token, float* dev_logits);
 
 /* Generation without host round trips: n decode steps starting from `token`, each step feeding
- * the token the previous one chose.  dev_u: optional DEVICE array of n uniforms (used when
- * temperature > 0).  dev_tokens_out: DEVICE array [n] that receives the chosen tokens.  Returns
- * after enqueueing (does not synchronise); adp_sync reports device errors. */
+ * the token the previous one chose.  In the persistent kernel mode the n steps run inside ONE
+ * cooperative launch: the step's last CTA publishes the chosen token as an epoch-tagged word and
+ * every CTA takes it from there before the next step's embedding gather, while the weight stream
+ * runs on across the step boundary (the ablation modes launch each step separately).
+ * dev_u: optional DEVICE array of n uniforms (used when temperature > 0).  dev_tokens_out: DEVICE
+ * array [n] that receives the chosen tokens.  Returns after enqueueing (does not synchronise);
+ * adp_sync reports device errors.  adp_prefill likewise runs its n steps in one launch. */
 int adp_generate_async(adp_model* m, adp_kv* kv, int32_t token, int32_t n, float temperature, const float* dev_u,
                        int32_t* dev_tokens_out);
 int adp_sync(adp_model* m);                          /* synchronise the stream; report sticky errors */

@@ -206,3 +206,32 @@ def test_moe_forced_experts_match_oracle(torch_cuda):
         nxt = kv.step(int(t), logits=lg)
         assert nxt == ref["next"]
         assert np.array_equal(lg.cpu().numpy().view(np.uint32), ref["logits"].view(np.uint32))
+
+
+@pytest.mark.parametrize("name,temperature", [("tiny", 0.7), ("moe-32x1408-top4-e4m3", 0.0),
+                                              ("dense-8b-bf16", 0.0)])
+def test_in_kernel_multi_step_generation_matches_oracle(torch_cuda, name, temperature):
+    """adp_generate_async runs n decode steps in one persistent launch, each step taking the token
+    the previous one chose (and, at T > 0, the next uniform): the tokens and the whole KV cache
+    equal the oracle's free run in contract mode."""
+    import torch
+    from autoregressive_decode_persistent_gb300 import adp
+    cfg = synth.get_config(name) if name == "tiny" else synth.shrink(synth.get_config(name))
+    W = synth.model_weights(cfg)
+    prompt = synth.prompt(cfg, 6)
+    n = 30
+    us = synth.sampling_uniforms(len(prompt) + n) if temperature > 0 else None
+    toks, _, nexts, _, om = oracle_free_run(cfg, W, prompt, n, EXACT, temperature, us)
+    model = _model(cfg, W)
+    kv = model.new_kv()
+    t0 = kv.prefill(prompt[:-1]) if len(prompt) > 1 else None
+    assert t0 == nexts[len(prompt) - 2] or temperature > 0
+    out = torch.empty(n + 1, dtype=torch.int32, device=model.device)
+    dev_u = torch.tensor(us[len(prompt) - 1:], dtype=torch.float32, device=model.device) if us is not None else None
+    kv.generate_async(int(prompt[-1]), n + 1, out, temperature, dev_u)
+    adp.adp_sync(model.handle)
+    assert out.cpu().tolist() == nexts[len(prompt) - 1:len(prompt) + n]
+    k, v = kv.read()
+    m = len(prompt) + n
+    assert np.array_equal(k[:, :, :m], om.kc[:, :, :m]) and np.array_equal(v[:, :, :m], om.vc[:, :, :m])
+    model.close()
