@@ -48,9 +48,11 @@ def weight_bytes_per_token(cfg: dict) -> int:
     embedding row and the final norm gain."""
     c = cfg
     eb = _EB[c["weight_dtype"]]
+    q8 = c["weight_dtype"] == "e4m3"       # e4m3 layer matrices carry an fp32 scale per row
+    ee = _EB[c.get("embed_dtype") or c["weight_dtype"]]  # embedding, LM head, norm gains
     d, hq, hkv, hd, V = c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"], c["vocab"]
-    attn = (hq * hd * d * 2 + 2 * hkv * hd * d) * eb
-    norms = 2 * d * eb
+    attn = (hq * hd * d * 2 + 2 * hkv * hd * d) * eb + ((hq * hd + 2 * hkv * hd + d) * 4 if q8 else 0)
+    norms = 2 * d * ee
     if c["n_experts"]:
         f, k = c["d_expert"], c["top_k"]
         xeb = _EB[c["expert_dtype"]]
@@ -58,10 +60,10 @@ def weight_bytes_per_token(cfg: dict) -> int:
         experts = k * (3 * f * d * xeb + (2 * f + d) * 4)
         ffn = router + experts
     else:
-        ffn = 3 * c["d_ff"] * d * eb
+        ffn = 3 * c["d_ff"] * d * eb + ((2 * c["d_ff"] + d) * 4 if q8 else 0)
     per_layer = attn + norms + ffn
-    head = V * d * eb
-    return c["n_layers"] * per_layer + head + d * eb + d * eb
+    head = V * d * ee
+    return c["n_layers"] * per_layer + head + d * ee + d * ee
 
 
 def kv_read_bytes(cfg: dict, context: int) -> int:

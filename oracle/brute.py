@@ -73,21 +73,28 @@ def forward(cfg: dict, W: dict, tokens, force=None):
     (gates are then the softmax probabilities of those experts renormalised over them)."""
     c = cfg
     wdt, kvdt = c["weight_dtype"], c["kv_dtype"]
+    edt = c.get("embed_dtype") or wdt  # embedding, LM head, norm gains
+
+    def mat(Lw, name):
+        """A layer matrix as float64; e4m3 rows times their per-row scale."""
+        m = widen(Lw[name], wdt)
+        return m * Lw[name + "_scale"].astype(np.float64)[:, None] if wdt == "e4m3" else m
+
     d, hq, hkv, hd = c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"]
     tokens = np.asarray(tokens, dtype=np.int64)
     n = len(tokens)
     pos = np.arange(n)
-    emb = widen(W["tok_emb"], wdt)
+    emb = widen(W["tok_emb"], edt)
     x = emb[tokens].copy()
     eps = c["rms_eps"]
     causal = np.tril(np.ones((n, n), dtype=bool))
     group = np.array([(h * hkv) // hq for h in range(hq)])
     routes = []
     for l, Lw in enumerate(W["layers"]):
-        xn = rmsnorm(x, widen(Lw["attn_norm"], wdt), eps)
-        q = (xn @ widen(Lw["wq"], wdt).T).reshape(n, hq, hd)
-        k = (xn @ widen(Lw["wk"], wdt).T).reshape(n, hkv, hd)
-        v = (xn @ widen(Lw["wv"], wdt).T).reshape(n, hkv, hd)
+        xn = rmsnorm(x, widen(Lw["attn_norm"], edt), eps)
+        q = (xn @ mat(Lw, "wq").T).reshape(n, hq, hd)
+        k = (xn @ mat(Lw, "wk").T).reshape(n, hkv, hd)
+        v = (xn @ mat(Lw, "wv").T).reshape(n, hkv, hd)
         q = rope(q, pos, c["rope_theta"])
         k = store_round(rope(k, pos, c["rope_theta"]), kvdt)
         v = store_round(v, kvdt)
@@ -99,12 +106,12 @@ def forward(cfg: dict, W: dict, tokens, force=None):
             p = np.exp(s)
             p = p / p.sum(axis=1, keepdims=True)
             att[:, h, :] = p @ v[:, group[h], :]
-        x = x + att.reshape(n, hq * hd) @ widen(Lw["wo"], wdt).T
-        xn = rmsnorm(x, widen(Lw["ffn_norm"], wdt), eps)
+        x = x + att.reshape(n, hq * hd) @ mat(Lw, "wo").T
+        xn = rmsnorm(x, widen(Lw["ffn_norm"], edt), eps)
         if not c["n_experts"]:
-            g = xn @ widen(Lw["w_gate"], wdt).T
-            u = xn @ widen(Lw["w_up"], wdt).T
-            x = x + (silu(g) * u) @ widen(Lw["w_down"], wdt).T
+            g = xn @ mat(Lw, "w_gate").T
+            u = xn @ mat(Lw, "w_up").T
+            x = x + (silu(g) * u) @ mat(Lw, "w_down").T
         else:
             E, K = c["n_experts"], c["top_k"]
             r = xn @ widen(Lw["router"], c["router_dtype"]).T
@@ -126,7 +133,7 @@ def forward(cfg: dict, W: dict, tokens, force=None):
                     out[t] += gk * (Qd @ h_e)
             x = x + out
             routes.append(sel_l)
-    xn = rmsnorm(x, widen(W["final_norm"], wdt), eps)
+    xn = rmsnorm(x, widen(W["final_norm"], edt), eps)
     head = W["tok_emb"] if c["tied_embeddings"] else W["lm_head"]
-    logits = xn @ widen(head, wdt).T
+    logits = xn @ widen(head, edt).T
     return logits, (np.stack(routes, axis=1) if routes else None)

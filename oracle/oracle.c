@@ -68,6 +68,7 @@ typedef struct {
   int32_t weight_dtype, kv_dtype;
   int32_t n_experts, top_k, d_expert;
   int32_t router_dtype, expert_dtype;
+  int32_t embed_dtype;  /* embedding, LM head, norm gains when weight_dtype is e4m3 */
 } orc_config;
 
 typedef struct {
@@ -76,6 +77,8 @@ typedef struct {
   const void *router;
   const void *e_gate, *e_up, *e_down;
   const float *e_gate_scale, *e_up_scale, *e_down_scale;
+  /* per-output-channel scales of the layer matrices when weight_dtype is e4m3 (else NULL) */
+  const float *wq_scale, *wk_scale, *wv_scale, *wo_scale, *w_gate_scale, *w_up_scale, *w_down_scale;
 } orc_layer;
 
 typedef struct {
@@ -480,6 +483,8 @@ int orc_step(const orc_config* c, const orc_weights* W, void* kc, void* vc, int3
   if (!c || !W || !kc || !vc || !logits) return ORC_EINVAL;
   const int L = c->n_layers, d = c->d_model, hq = c->n_heads, hkv = c->n_kv_heads, hd = c->head_dim;
   const int V = c->vocab, wdt = c->weight_dtype, kvdt = c->kv_dtype;
+  /* with e4m3 layer matrices the embedding, LM head and norm gains keep a 16-bit type */
+  const int edt = wdt == ORC_E4M3 ? c->embed_dtype : wdt;
   if (pos < 0 || pos >= c->max_ctx) return ORC_ECTX;
   if (token < 0 || token >= V) return ORC_EINVAL;
   const int moe = c->n_experts > 0;
@@ -501,7 +506,7 @@ int orc_step(const orc_config* c, const orc_weights* W, void* kc, void* vc, int3
   int rc = ORC_OK;
   if (!x || !xn || !q || !k || !v || !att || !y || !g || !uu || !acc || !cs || !sn || !r) { rc = ORC_ENOMEM; goto done; }
 
-  widen_row(W->tok_emb, (size_t)token, d, wdt, x);   /* embedding: exact widening */
+  widen_row(W->tok_emb, (size_t)token, d, edt, x);   /* embedding: exact widening */
   orc_rope_row(c->rope_theta, hd, pos, cs, sn);
   const float scale = (float)(1.0 / sqrt((double)hd));
 
@@ -509,10 +514,10 @@ int orc_step(const orc_config* c, const orc_weights* W, void* kc, void* vc, int3
     const orc_layer* lw = &W->layers[l];
     if (trace) memcpy(trace + (size_t)l * d, x, sizeof(float) * (size_t)d);
     /* attention block */
-    orc_rmsnorm(x, lw->attn_norm, wdt, d, c->rms_eps, mode, xn);
-    if ((rc = gemv(lw->wq, wdt, hq * hd, d, xn, NULL, q, mode))) goto done;
-    if ((rc = gemv(lw->wk, wdt, hkv * hd, d, xn, NULL, k, mode))) goto done;
-    if ((rc = gemv(lw->wv, wdt, hkv * hd, d, xn, NULL, v, mode))) goto done;
+    orc_rmsnorm(x, lw->attn_norm, edt, d, c->rms_eps, mode, xn);
+    if ((rc = gemv(lw->wq, wdt, hq * hd, d, xn, lw->wq_scale, q, mode))) goto done;
+    if ((rc = gemv(lw->wk, wdt, hkv * hd, d, xn, lw->wk_scale, k, mode))) goto done;
+    if ((rc = gemv(lw->wv, wdt, hkv * hd, d, xn, lw->wv_scale, v, mode))) goto done;
     for (int h = 0; h < hq; ++h) rope_apply(q + (size_t)h * hd, hd, cs, sn, mode);
     for (int h = 0; h < hkv; ++h) rope_apply(k + (size_t)h * hd, hd, cs, sn, mode);
     for (int h = 0; h < hkv; ++h) {
@@ -529,15 +534,15 @@ int orc_step(const orc_config* c, const orc_weights* W, void* kc, void* vc, int3
       orc_attention_head(q + (size_t)h * hd, (const uint16_t*)kc + base, (const uint16_t*)vc + base, kvdt, pos + 1,
                          hd, scale, mode, att + (size_t)h * hd);
     }
-    if ((rc = gemv(lw->wo, wdt, d, hq * hd, att, NULL, y, mode))) goto done;
+    if ((rc = gemv(lw->wo, wdt, d, hq * hd, att, lw->wo_scale, y, mode))) goto done;
     for (int i = 0; i < d; ++i) x[i] = x[i] + y[i];
     /* feed-forward block */
-    orc_rmsnorm(x, lw->ffn_norm, wdt, d, c->rms_eps, mode, xn);
+    orc_rmsnorm(x, lw->ffn_norm, edt, d, c->rms_eps, mode, xn);
     if (!moe) {
-      if ((rc = gemv(lw->w_gate, wdt, ff, d, xn, NULL, g, mode))) goto done;
-      if ((rc = gemv(lw->w_up, wdt, ff, d, xn, NULL, uu, mode))) goto done;
+      if ((rc = gemv(lw->w_gate, wdt, ff, d, xn, lw->w_gate_scale, g, mode))) goto done;
+      if ((rc = gemv(lw->w_up, wdt, ff, d, xn, lw->w_up_scale, uu, mode))) goto done;
       for (int i = 0; i < ff; ++i) g[i] = silu_mul(g[i], uu[i], mode);
-      if ((rc = gemv(lw->w_down, wdt, d, ff, g, NULL, y, mode))) goto done;
+      if ((rc = gemv(lw->w_down, wdt, d, ff, g, lw->w_down_scale, y, mode))) goto done;
       for (int i = 0; i < d; ++i) x[i] = x[i] + y[i];
     } else {
       const int E = c->n_experts, K = c->top_k;
@@ -578,10 +583,10 @@ int orc_step(const orc_config* c, const orc_weights* W, void* kc, void* vc, int3
     }
   }
   if (trace) memcpy(trace + (size_t)L * d, x, sizeof(float) * (size_t)d);
-  orc_rmsnorm(x, W->final_norm, wdt, d, c->rms_eps, mode, xn);
+  orc_rmsnorm(x, W->final_norm, edt, d, c->rms_eps, mode, xn);
   {
     const void* head = c->tied_embeddings ? W->tok_emb : W->lm_head;
-    if ((rc = gemv(head, wdt, V, d, xn, NULL, logits, mode))) goto done;
+    if ((rc = gemv(head, edt, V, d, xn, NULL, logits, mode))) goto done;
   }
   if (next) *next = temperature > 0.0f ? orc_sample(logits, V, temperature, u, mode) : orc_argmax(logits, V);
 done:

@@ -38,13 +38,16 @@ class Config(ctypes.Structure):
                                                "d_ff", "vocab", "max_ctx")] + \
                [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)] + \
                [(n, ctypes.c_int32) for n in ("tied_embeddings", "weight_dtype", "kv_dtype", "n_experts",
-                                               "top_k", "d_expert", "router_dtype", "expert_dtype")]
+                                               "top_k", "d_expert", "router_dtype", "expert_dtype",
+                                               "embed_dtype")]
 
 
 class Layer(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate",
                                                 "w_up", "w_down", "router", "e_gate", "e_up", "e_down",
-                                                "e_gate_scale", "e_up_scale", "e_down_scale")]
+                                                "e_gate_scale", "e_up_scale", "e_down_scale",
+                                                "wq_scale", "wk_scale", "wv_scale", "wo_scale",
+                                                "w_gate_scale", "w_up_scale", "w_down_scale")]
 
 
 class Weights(ctypes.Structure):
@@ -108,13 +111,16 @@ class OracleModel:
         self.c = Config(c["n_layers"], c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"],
                         c.get("d_ff", 0), c["vocab"], c["max_ctx"], c["rms_eps"], c["rope_theta"],
                         1 if c["tied_embeddings"] else 0, _DT[c["weight_dtype"]], _DT[c["kv_dtype"]],
-                        c["n_experts"], c["top_k"], c["d_expert"], _DT[c["router_dtype"]], _DT[c["expert_dtype"]])
+                        c["n_experts"], c["top_k"], c["d_expert"], _DT[c["router_dtype"]], _DT[c["expert_dtype"]],
+                        _DT[c.get("embed_dtype") or c["weight_dtype"]])
         self._keep = []
         layers = (Layer * c["n_layers"])()
         for i, Lw in enumerate(W["layers"]):
             f = {}
             for k in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down", "router",
-                      "e_gate", "e_up", "e_down", "e_gate_scale", "e_up_scale", "e_down_scale"):
+                      "e_gate", "e_up", "e_down", "e_gate_scale", "e_up_scale", "e_down_scale",
+                      "wq_scale", "wk_scale", "wv_scale", "wo_scale", "w_gate_scale", "w_up_scale",
+                      "w_down_scale"):
                 a = _c(Lw.get(k))
                 self._keep.append(a)
                 f[k] = _p(a)

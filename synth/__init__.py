@@ -159,9 +159,10 @@ def model_weights(cfg: dict, seed: int | None = None) -> dict:
     """Host copies of every stored tensor of a model, as numpy arrays of raw bits.
 
     Layout (row-major [out, in]):
-      tok_emb [V, d]; lm_head [V, d] (None when tied); final_norm [d]
-      layers[l]: attn_norm [d], wq [hq*hd, d], wk/wv [hkv*hd, d], wo [d, hq*hd], ffn_norm [d],
-        dense: w_gate/w_up [ff, d], w_down [d, ff]
+      tok_emb [V, d]; lm_head [V, d] (None when tied); final_norm [d]   (embed dtype)
+      layers[l]: attn_norm [d], ffn_norm [d] (embed dtype), wq [hq*hd, d], wk/wv [hkv*hd, d],
+        wo [d, hq*hd]; dense: w_gate/w_up [ff, d], w_down [d, ff] (weight dtype; with e4m3
+        weights each matrix M also has M_scale [rows] f32, applied after the dot)
         MoE:   router [E, d]; e_gate/e_up [E, f, d] e4m3; e_down [E, d, f] e4m3;
                e_gate_scale/e_up_scale [E, f] f32; e_down_scale [E, d] f32
     """
@@ -169,26 +170,32 @@ def model_weights(cfg: dict, seed: int | None = None) -> dict:
     if seed is None:
         seed = SEED_WEIGHTS + c["index"]
     wdt = c["weight_dtype"]
+    edt = c.get("embed_dtype") or wdt
     d, hq, hkv, hd = c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"]
     V = c["vocab"]
-    W = {"tok_emb": normal_stored(seed, TID_EMB, (V, d), wdt)}
-    W["lm_head"] = None if c["tied_embeddings"] else normal_stored(seed, TID_LM, (V, d), wdt)
-    W["final_norm"] = ones_stored(d, wdt)
+    W = {"tok_emb": normal_stored(seed, TID_EMB, (V, d), edt)}
+    W["lm_head"] = None if c["tied_embeddings"] else normal_stored(seed, TID_LM, (V, d), edt)
+    W["final_norm"] = ones_stored(d, edt)
+
+    def mat(L, name, tid, rows, cols):
+        """A layer matrix in the weight dtype; e4m3 ones come with per-row scales `<name>_scale`."""
+        if wdt == "e4m3":
+            L[name], L[name + "_scale"] = normal_e4m3_rows(seed, tid, rows, cols)
+        else:
+            L[name] = normal_stored(seed, tid, (rows, cols), wdt)
+
     layers = []
     for l in range(c["n_layers"]):
-        L = {
-            "attn_norm": ones_stored(d, wdt),
-            "wq": normal_stored(seed, _tid_layer(l, K_WQ), (hq * hd, d), wdt),
-            "wk": normal_stored(seed, _tid_layer(l, K_WK), (hkv * hd, d), wdt),
-            "wv": normal_stored(seed, _tid_layer(l, K_WV), (hkv * hd, d), wdt),
-            "wo": normal_stored(seed, _tid_layer(l, K_WO), (d, hq * hd), wdt),
-            "ffn_norm": ones_stored(d, wdt),
-        }
+        L = {"attn_norm": ones_stored(d, edt), "ffn_norm": ones_stored(d, edt)}
+        mat(L, "wq", _tid_layer(l, K_WQ), hq * hd, d)
+        mat(L, "wk", _tid_layer(l, K_WK), hkv * hd, d)
+        mat(L, "wv", _tid_layer(l, K_WV), hkv * hd, d)
+        mat(L, "wo", _tid_layer(l, K_WO), d, hq * hd)
         if c["n_experts"] == 0:
             ff = c["d_ff"]
-            L["w_gate"] = normal_stored(seed, _tid_layer(l, K_WG), (ff, d), wdt)
-            L["w_up"] = normal_stored(seed, _tid_layer(l, K_WU), (ff, d), wdt)
-            L["w_down"] = normal_stored(seed, _tid_layer(l, K_WD), (d, ff), wdt)
+            mat(L, "w_gate", _tid_layer(l, K_WG), ff, d)
+            mat(L, "w_up", _tid_layer(l, K_WU), ff, d)
+            mat(L, "w_down", _tid_layer(l, K_WD), d, ff)
         else:
             E, f = c["n_experts"], c["d_expert"]
             L["router"] = normal_stored(seed, _tid_layer(l, K_ROUTER), (E, d), c["router_dtype"])

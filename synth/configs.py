@@ -22,6 +22,7 @@ _BASE = dict(
     rope_theta=10000.0,
     tied_embeddings=True,
     weight_dtype="f16",
+    embed_dtype=None,  # embedding, LM head and norm gains: None = weight_dtype
     kv_dtype="f16",
     n_experts=0,
     top_k=0,
@@ -59,6 +60,11 @@ CONFIGS = [
          n_kv_heads=4, head_dim=128, d_ff=0, vocab=32000, max_ctx=4096, weight_dtype="bf16",
          kv_dtype="bf16", n_experts=32, top_k=4, d_expert=1408, router_dtype="f16",
          expert_dtype="e4m3", prompt_len=256, decode_steps=512),
+    # 5: the 2.3B model with fp8 layer weights: every layer matrix e4m3 with per-output-channel
+    #    fp32 scales (applied after the dot), embedding / tied LM head and norm gains fp16
+    _cfg(index=5, name="dense-2.3b-e4m3", n_layers=25, d_model=2560, n_heads=20, n_kv_heads=4,
+         head_dim=128, d_ff=9728, vocab=32000, max_ctx=4096, weight_dtype="e4m3", embed_dtype="f16",
+         prompt_len=512, decode_steps=512),
 ]
 
 BY_NAME = {c["name"]: c for c in CONFIGS}
