@@ -41,13 +41,15 @@ class Config(ctypes.Structure):
                                                "d_ff", "vocab", "max_ctx")] + \
                [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)] + \
                [(n, ctypes.c_int32) for n in ("tied_embeddings", "weight_dtype", "kv_dtype", "n_experts",
-                                               "top_k", "d_expert", "router_dtype", "expert_dtype")]
+                                               "top_k", "d_expert", "router_dtype", "expert_dtype",
+                                               "embed_dtype")]
 
 
 class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up",
                                                 "w_down", "router", "e_gate", "e_up", "e_down", "e_gate_scale",
-                                                "e_up_scale", "e_down_scale")]
+                                                "e_up_scale", "e_down_scale", "wq_scale", "wk_scale", "wv_scale",
+                                                "wo_scale", "w_gate_scale", "w_up_scale", "w_down_scale")]
 
 
 class Weights(ctypes.Structure):

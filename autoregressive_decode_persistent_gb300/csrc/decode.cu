@@ -306,7 +306,7 @@ __device__ void rmsnorm_prologue(const Params& p, Ctl* ctl, float* xbuf, const v
     gr[k] = i < d ? __ldg(reinterpret_cast<const unsigned short*>(gain) + i) : (uint16_t)0;
   }
   if (emb_row) {
-    for (int i = tid; i < d; i += T) xbuf[xpos(i)] = load_elem(emb_row, (size_t)i, p.wdt);
+    for (int i = tid; i < d; i += T) xbuf[xpos(i)] = load_elem(emb_row, (size_t)i, p.edt);
     consumer_sync();
   } else {
     ll_fetch(p, ctl, xbuf, p.x, d, d, 0, x_epoch, tid);
@@ -331,7 +331,7 @@ __device__ void rmsnorm_prologue(const Params& p, Ctl* ctl, float* xbuf, const v
   for (int k = 0; k < kPrologueRegs; ++k) {
     const int i = tid + k * T;
     if (i < d) {
-      const float g = p.wdt == DT_BF16 ? bf16_bits_to_f32(gr[k]) : __half2float(__ushort_as_half(gr[k]));
+      const float g = p.edt == DT_BF16 ? bf16_bits_to_f32(gr[k]) : __half2float(__ushort_as_half(gr[k]));
       xbuf[xpos(i)] = __fmul_rn(__fmul_rn(xbuf[xpos(i)], r), g);
     }
   }
@@ -422,6 +422,32 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
     float acc[SLOTS * ROWS];
 #pragma unroll
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = 0.0f;
+    // e4m3 layer matrices: the per-row scales of this unit, loaded now, applied after the dot
+    constexpr bool kScaled = WDT == DT_E4M3 && SLOTS == 1;
+    float sc[ROWS];
+    if constexpr (kScaled) {
+      if (active) {
+        int mi, r0, rstep = 1;
+        if (kind == PK_QKV) {
+          const int half = p.hd / 2, nq = p.hq * half, nk = p.hkv * half;
+          const int uu = unit < nq ? unit : unit < nq + nk ? unit - nq : unit - nq - nk;
+          mi = unit < nq ? 0 : unit < nq + nk ? 1 : 2;
+          r0 = (uu / half) * p.hd + uu % half;
+          rstep = half;
+        } else if (kind == PK_GU) {
+          mi = 4;
+          r0 = unit;
+          rstep = 0;  // gate row `unit` (scale table 4), up row `unit` (table 5)
+        } else {
+          mi = kind == PK_WO ? 3 : 6;
+          r0 = unit * ROWS;
+        }
+        const float* tab = p.wscale[mi][L];
+#pragma unroll
+        for (int j = 0; j < ROWS; ++j)
+          sc[j] = (kind == PK_GU) ? __ldg(p.wscale[4 + j][L] + r0) : __ldg(tab + r0 + j * rstep);
+      }
+    }
     for (int ck = 0; ck < n_chunks; ++ck) {
       const long long cy0 = cyc_now();
       bool ok = aborted(ctl) || mbar_wait(&ctl->full[slot], par, &ctl->abort, wait_ns);
@@ -473,6 +499,10 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
     if (!active || aborted(ctl)) continue;
 #pragma unroll
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = warp_fold(acc[i]);
+    if constexpr (kScaled) {
+#pragma unroll
+      for (int j = 0; j < ROWS; ++j) acc[j] = __fmul_rn(sc[j], acc[j]);
+    }
     // ---- epilogues
     if (kind == PK_QKV) {
       if (lane == 0) {
@@ -888,8 +918,6 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
     float* Wm = xbuf;           // [nb] block maxima, then weights w_b
     float* Wl = xbuf + nbmax;   // [nb] block sums; Wl[nbmax] = L
     constexpr int T = kConsumerWarps * 32;
-    constexpr int kPre = 32;    // blocks of o loaded per batch
-    const ll_t* po = part_o + (size_t)h * nbmax * HD + tid;  // this thread's dimension, block 0
     for (int i = tid; i < 2 * nb; i += T) {
       const ll_t* src = i < nb ? part_m + (size_t)h * nbmax + i : part_l + (size_t)h * nbmax + (i - nb);
       ll_t x = ll_load(src);
@@ -1089,7 +1117,7 @@ __device__ void run_expert(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf
     gemv_phase<1, SLOTS, DT_E4M3, true>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
 }
 
-template <bool MOE>
+template <int KIND>
 __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, Step st, uint32_t c,
                          uint32_t G, int ph0, int ph1, bool use_barrier, int cw, int lane) {
   uint32_t t = 0;
@@ -1097,6 +1125,7 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
   int sel_layer = -1;
   uint32_t att_uses = 0, merge_uses = 0;
   const int tid = cw * 32 + lane;
+  constexpr bool MOE = KIND == KK_MOE;
   for (int step = 0; step < p.n_steps; ++step) {
     if (step > 0) {
       // the next step of this launch: its position, epochs and inputs follow from the last one,
@@ -1139,7 +1168,7 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
           if (L == 0 && !ab) {  // the residual starts as the embedding row: publish this CTA's slice
             const int a = (int)((long long)c * p.d / G), b = (int)((long long)(c + 1) * p.d / G);
             for (int i = a + tid; i < b; i += kConsumerWarps * 32)
-              ll_store(p.x + i, ll_pack(load_elem(emb, (size_t)i, p.wdt), ew));
+              ll_store(p.x + i, ll_pack(load_elem(emb, (size_t)i, p.edt), ew));
           }
           if (cw == kConsumerWarps - 1 && lane == 0 && !ab) prefetch_attention_kv(p, L, st.pos + 1, c, G);
           if (n > 0) {
@@ -1233,8 +1262,14 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
           else gemv_phase<1, 1, DT_F16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
         }
       } else {
-        if (p.wdt == DT_BF16) run_gemv<DT_BF16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
-        else run_gemv<DT_F16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+        if constexpr (KIND == KK_DENSE8) {
+          if (P.kind != PK_LM) run_gemv<DT_E4M3>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+          else if (p.edt == DT_BF16) run_gemv<DT_BF16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+          else run_gemv<DT_F16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+        } else {
+          if (p.wdt == DT_BF16) run_gemv<DT_BF16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+          else run_gemv<DT_F16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+        }
       }
       // ---- the LM head's last CTA picks the greedy token
       if (P.kind == PK_LM && ctl->flag && st.temperature <= 0.0f && cw == 0 && lane == 0) {
@@ -1256,9 +1291,9 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
   }
 }
 
-// MOE: the kernel of the top-k expert models; dense models run the instantiation without the
-// router and expert paths.
-template <bool MOE>
+// KIND: KK_DENSE (16-bit weights), KK_MOE (top-k expert models), KK_DENSE8 (e4m3 layer
+// matrices): each model runs the instantiation that carries only its own code paths.
+template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ Params p, int32_t ph0, int32_t ph1, int32_t use_barrier,
                   int32_t xbuf_floats) {
@@ -1302,7 +1337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumerWarps) {
     if (lane == 0) producer(p, ctl, ring, c, G, ph0, ph1);
   } else {
-    consumer<MOE>(p, ctl, ring, xbuf, st, c, G, ph0, ph1, use_barrier != 0, warp, lane);
+    consumer<KIND>(p, ctl, ring, xbuf, st, c, G, ph0, ph1, use_barrier != 0, warp, lane);
   }
 }
 
@@ -1311,8 +1346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace adp {
 
 // Host-side launchers of the decode kernel.
-cudaError_t decode_prepare(size_t smem_bytes, bool moe, int* blocks_per_sm) {
-  const void* k = moe ? (const void*)decode_kernel<true> : (const void*)decode_kernel<false>;
+static const void* kernel_of(int kind) {
+  return kind == KK_MOE ? (const void*)decode_kernel<KK_MOE>
+                        : kind == KK_DENSE8 ? (const void*)decode_kernel<KK_DENSE8> : (const void*)decode_kernel<KK_DENSE>;
+}
+
+cudaError_t decode_prepare(size_t smem_bytes, int kind, int* blocks_per_sm) {
+  const void* k = kernel_of(kind);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kThreads, smem_bytes);
@@ -1322,7 +1362,7 @@ cudaError_t decode_launch(const Params& p, int ph0, int ph1, bool persistent, in
                           int xbuf_floats, cudaStream_t stream) {
   int32_t a0 = ph0, a1 = ph1, ub = persistent ? 1 : 0, xf = xbuf_floats;
   void* args[] = {(void*)&p, &a0, &a1, &ub, &xf};
-  const void* k = p.E > 0 ? (const void*)decode_kernel<true> : (const void*)decode_kernel<false>;
+  const void* k = kernel_of(p.E > 0 ? KK_MOE : p.wdt == DT_E4M3 ? KK_DENSE8 : KK_DENSE);
   if (persistent) return cudaLaunchCooperativeKernel(k, dim3(grid), dim3(kThreads), args, smem_bytes, stream);
   return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, smem_bytes, stream);
 }

@@ -100,7 +100,11 @@ static int validate(const adp_config* c, const adp_weights* w) {
   if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (c->d_model % 8 || c->vocab % 8 || (c->n_heads * c->head_dim) % 8) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (c->d_model > 7680 || c->vocab > 1024 * 256) return ADP_ERR_UNSUPPORTED_CONFIG;
-  if (c->weight_dtype != ADP_F16 && c->weight_dtype != ADP_BF16) return ADP_ERR_UNSUPPORTED_CONFIG;
+  const bool q8 = c->weight_dtype == ADP_E4M3;  // fp8 layer matrices with per-row scales (dense only)
+  if (c->weight_dtype != ADP_F16 && c->weight_dtype != ADP_BF16 && !(q8 && c->n_experts == 0))
+    return ADP_ERR_UNSUPPORTED_CONFIG;
+  if (q8 && c->embed_dtype != ADP_F16 && c->embed_dtype != ADP_BF16) return ADP_ERR_UNSUPPORTED_CONFIG;
+  if (q8 && (c->d_model % 16 || c->d_ff % 16 || (c->n_heads * c->head_dim) % 16)) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (c->kv_dtype != ADP_F16 && c->kv_dtype != ADP_BF16) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (!c->tied_embeddings && !w->lm_head) return ADP_ERR_INVALID_ARG;
   if (c->n_experts == 0) {
@@ -116,6 +120,9 @@ static int validate(const adp_config* c, const adp_weights* w) {
     const adp_layer_weights& L = w->layers[l];
     if (!L.attn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.ffn_norm) return ADP_ERR_INVALID_ARG;
     if (c->n_experts == 0 && (!L.w_gate || !L.w_up || !L.w_down)) return ADP_ERR_INVALID_ARG;
+    if (q8 && (!L.wq_scale || !L.wk_scale || !L.wv_scale || !L.wo_scale || !L.w_gate_scale || !L.w_up_scale ||
+               !L.w_down_scale))
+      return ADP_ERR_INVALID_ARG;
     if (c->n_experts && (!L.router || !L.e_gate || !L.e_up || !L.e_down || !L.e_gate_scale || !L.e_up_scale ||
                          !L.e_down_scale))
       return ADP_ERR_INVALID_ARG;
@@ -202,7 +209,8 @@ static void plan(adp_model* m) {
       x_ph = last();
     }
   }
-  add_phase(m, PK_LM, c.n_layers, c.vocab / 4, 4, 1, d, eb, c.weight_dtype, true, 1);
+  const int edt = c.weight_dtype == ADP_E4M3 ? c.embed_dtype : c.weight_dtype;  // the LM head's type
+  add_phase(m, PK_LM, c.n_layers, c.vocab / 4, 4, 1, d, elem_bytes(edt), edt, true, 1);
   link(x_ph, -1, -1);
   add_phase(m, PK_SAMPLE, c.n_layers, 0, 0, 0, 0, 0, 0, false, 0);
   link(-1, -1, -1);
@@ -277,7 +285,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   m->p.att_gmax = gmax;
   m->p.att_slot_bytes = (int)item;
   int bps = 0;
-  CK(decode_prepare(m->smem, c.n_experts > 0, &bps));
+  CK(decode_prepare(m->smem, c.n_experts > 0 ? KK_MOE : c.weight_dtype == ADP_E4M3 ? KK_DENSE8 : KK_DENSE, &bps));
   if (bps < 1) return ADP_ERR_NOT_CORESIDENT;
 
   // weight image
@@ -324,12 +332,24 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   // per-layer pointer tables
   std::vector<const void*> an(L), fn(L);
   std::vector<const float*> sg(L), su(L), sd(L);
+  std::vector<const float*> ws[7];  // e4m3 layer-matrix scales: q, k, v, o, gate, up, down
+  for (auto& v : ws) v.resize(L);
   for (int l = 0; l < L; ++l) {
-    an[l] = w->layers[l].attn_norm;
-    fn[l] = w->layers[l].ffn_norm;
-    sg[l] = w->layers[l].e_gate_scale;
-    su[l] = w->layers[l].e_up_scale;
-    sd[l] = w->layers[l].e_down_scale;
+    const adp_layer_weights& Lw = w->layers[l];
+    an[l] = Lw.attn_norm;
+    fn[l] = Lw.ffn_norm;
+    sg[l] = Lw.e_gate_scale;
+    su[l] = Lw.e_up_scale;
+    sd[l] = Lw.e_down_scale;
+    const float* s7[7] = {Lw.wq_scale, Lw.wk_scale, Lw.wv_scale, Lw.wo_scale, Lw.w_gate_scale, Lw.w_up_scale,
+                          Lw.w_down_scale};
+    for (int i = 0; i < 7; ++i) ws[i][l] = c.weight_dtype == ADP_E4M3 ? s7[i] : nullptr;
+  }
+  for (int i = 0; i < 7; ++i) {
+    const float** t = nullptr;
+    if ((rc = m->alloc(&t, L))) return rc;
+    CK(cudaMemcpyAsync(t, ws[i].data(), L * sizeof(void*), cudaMemcpyHostToDevice, m->stream));
+    m->p.wscale[i] = t;
   }
   const void** d_an; const void** d_fn; const float** d_sg; const float** d_su; const float** d_sd;
   if ((rc = m->alloc(&d_an, L)) || (rc = m->alloc(&d_fn, L)) || (rc = m->alloc(&d_sg, L)) ||
@@ -412,6 +432,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   p.L = L; p.d = d; p.hq = hq; p.hkv = hkv; p.hd = hd; p.ff = c.d_ff; p.V = c.vocab; p.max_ctx = c.max_ctx;
   p.E = c.n_experts; p.topk = c.n_experts ? c.top_k : 0; p.fexp = c.d_expert;
   p.wdt = c.weight_dtype; p.kvdt = c.kv_dtype; p.rdt = c.router_dtype;
+  p.edt = c.weight_dtype == ADP_E4M3 ? c.embed_dtype : c.weight_dtype;
   p.eps = c.rms_eps;
   p.attn_scale = (float)(1.0 / std::sqrt((double)hd));
   p.nbmax = nbmax;

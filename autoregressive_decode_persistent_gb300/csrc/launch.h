@@ -16,7 +16,7 @@ struct RepackSrc {
   int32_t hd, hq, hkv;
 };
 
-cudaError_t decode_prepare(size_t smem_bytes, bool moe, int* blocks_per_sm);
+cudaError_t decode_prepare(size_t smem_bytes, int kind, int* blocks_per_sm);  // kind: KernelKind
 cudaError_t decode_launch(const Params& p, int ph0, int ph1, bool persistent, int grid, size_t smem_bytes,
                           int xbuf_floats, cudaStream_t stream);
 cudaError_t repack_launch(uint8_t* image, const PhaseDesc& P, const RepackSrc& S, int grid, int experts,

@@ -39,6 +39,9 @@ enum PhaseKind : int32_t {
 
 enum DType : int32_t { DT_F16 = 0, DT_BF16 = 1, DT_E4M3 = 2, DT_F32 = 3 };
 
+// Kernel instantiations: dense 16-bit weights, top-k experts, dense e4m3 layer matrices.
+enum KernelKind : int32_t { KK_DENSE = 0, KK_MOE = 1, KK_DENSE8 = 2 };
+
 struct PhaseDesc {
   int32_t kind, layer;
   int32_t n_units;        // units of the whole phase
@@ -80,11 +83,13 @@ struct Params {
   const float* const* e_gate_scale;   // [L] -> [E][f]
   const float* const* e_up_scale;     // [L] -> [E][f]
   const float* const* e_down_scale;   // [L] -> [E][d]
+  const float* const* wscale[7];      // e4m3 dense: [L] -> per-row scales of q, k, v, o, gate, up, down
   const PhaseDesc* phases;
   int32_t n_phases;
   // shapes
   int32_t L, d, hq, hkv, hd, ff, V, max_ctx, E, topk, fexp;
   int32_t wdt, kvdt, rdt;
+  int32_t edt;                        // embedding, LM head and norm gains (= wdt unless wdt is e4m3)
   float eps;
   float attn_scale;
   int32_t nbmax;                      // max attention blocks = ceil(max_ctx / 32)

@@ -28,7 +28,7 @@ def make_config(cfg: dict) -> adp.Config:
                       cfg.get("d_ff", 0), cfg["vocab"], cfg["max_ctx"], cfg["rms_eps"], cfg["rope_theta"],
                       1 if cfg["tied_embeddings"] else 0, D[cfg["weight_dtype"]], D[cfg["kv_dtype"]],
                       cfg["n_experts"], cfg["top_k"], cfg["d_expert"], D[cfg["router_dtype"]],
-                      D[cfg["expert_dtype"]])
+                      D[cfg["expert_dtype"]], D[cfg.get("embed_dtype") or cfg["weight_dtype"]])
 
 
 class DecodeModel:
@@ -55,9 +55,10 @@ class DecodeModel:
 
         layers = (adp.LayerWeights * cfg["n_layers"])()
         for i, Lw in enumerate(W["layers"]):
-            f = {k: up(Lw.get(k), k in self._MATRICES) for k in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up",
-                                             "w_down", "router", "e_gate", "e_up", "e_down", "e_gate_scale",
-                                             "e_up_scale", "e_down_scale")}
+            f = {k: up(Lw.get(k), k in self._MATRICES)
+                 for k in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down", "router",
+                           "e_gate", "e_up", "e_down", "e_gate_scale", "e_up_scale", "e_down_scale", "wq_scale",
+                           "wk_scale", "wv_scale", "wo_scale", "w_gate_scale", "w_up_scale", "w_down_scale")}
             layers[i] = adp.LayerWeights(**f)
         self._layers = layers
         self.weights = adp.Weights(up(W["tok_emb"]), up(W.get("lm_head"), True), up(W["final_norm"]), layers)
@@ -67,7 +68,7 @@ class DecodeModel:
         sh = stream.cuda_stream if stream is not None else 0
         self.handle = adp.adp_create_model(self.config, self.weights, sh)
         # The engine copied every matrix into its own tile-ordered image at creation and reads
-        # only the embedding, norm gains and expert scales in place afterwards.
+        # only the embedding, norm gains and scales in place afterwards.
         if keep_matrices:
             self._keep += matrices
         del matrices

@@ -4,7 +4,8 @@ Workload: 25 layers, d_model 2560, 20 query heads x 128, 4 KV heads, SwiGLU 9728
 vocabulary 32000, fp16 weights ~N(0, 0.02) from a seed; a 512-token uniform-random prompt is
 prefilled, then greedy decode steps run at contexts 513..1024 (a run longer than 512 steps
 rewinds the cache to 512 and decodes the window again). One step = one decode step of the
-whole model = one persistent kernel launch.
+whole model; the steps of a window run inside one persistent kernel launch.
+--workload dense-2.3b-e4m3 measures the same model with e4m3 layer matrices instead.
 
 Printed (one JSON line, rank 0):
   value      tokens/s, device-timed: the steps chained on the GPU (adp_generate_async), weights
@@ -38,6 +39,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "batch-1 decode tokens/s/request (2.3B fp16); achieved HBM GB/s vs GB300 peak"
 WORKLOAD = "dense-2.3b-fp16"
+# --workload: the 2.3B model as benchmarked (default), or with e4m3 layer matrices (a "next" row:
+# fp8 dense weights; same shape, per-row fp32 scales, fp16 embedding and tied LM head)
+WORKLOADS = {
+    "dense-2.3b-fp16": {"metric": METRIC, "weights": "f16",
+                        "data": "synthetic: seeded N(0,0.02) fp16 weights, 512 uniform-random prompt ids"},
+    "dense-2.3b-e4m3": {"metric": "batch-1 decode tokens/s/request (2.3B, e4m3 layer weights); achieved HBM GB/s "
+                                  "vs GB300 peak",
+                        "weights": "e4m3 layer matrices with per-row f32 scales; f16 embedding, LM head, norms",
+                        "data": "synthetic: seeded N(0,0.02) weights quantised to e4m3 per row, 512 uniform-random "
+                                "prompt ids"},
+}
 WINDOW = 512  # decode steps per pass over contexts 513..1024
 
 
@@ -62,7 +74,7 @@ def kernel_source_hash() -> str:
 def profiled_traffic(src_hash: str):
     """DRAM bytes per decode step from the committed ncu summary, if it was taken on this kernel
     source (a launch of n chained steps moves n times as much)."""
-    path = os.path.join(ROOT, "profiles", "decode_kernel_dense-2.3b-fp16.md")
+    path = os.path.join(ROOT, "profiles", f"decode_kernel_{WORKLOAD}.md")
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:
@@ -149,7 +161,7 @@ def cpu_baseline(cfg, W, seconds: float = 15.0, max_steps: int | None = None, wa
             break
     cores = len(os.sched_getaffinity(0))
     return {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} plain-fp32 decode steps of the full 2.3B model at contexts "
+            "sample": f"{n} plain-fp32 decode steps of the full {cfg['name']} model at contexts "
                       f"{cfg['prompt_len'] + max(1, warmup) + 1}..{cfg['prompt_len'] + max(1, warmup) + n} "
                       f"(synthetic 512-position KV prefix, {max(1, warmup)} untimed steps first), "
                       f"OpenMP over {cores} host threads, {el:.1f} s"}, n, el
@@ -289,7 +301,7 @@ def run_engine(args, rank: int, world: int):
         write_timeline(args.timeline, model, kv, tok0, P, cfg)
 
     res = {
-        "ms": ms, "steps": args.steps, "n_launch": n_launch, "achieved_gbs": achieved, "per_launch_bytes": per_launch,
+        "ms": ms, "steps": args.steps, "n_launch": n_launch, "weight_bytes": bound.weight_bytes_per_token(cfg), "achieved_gbs": achieved, "per_launch_bytes": per_launch,
         "launch_ms": launch_ms, "peak": peak, "peak_kind": peak_kind, "e2e": e2e, "n_e2e": n_e2e,
         "clocks": clocks.summary(), "ctas": model.num_ctas, "image_bytes": model.image_bytes,
         # one cooperative launch per window of chained steps (adp_generate_async)
@@ -379,7 +391,7 @@ def emit_engine(args, cfg, res, world):
     value = whole_job_rate(res["steps"], res["ms"] * 1e-3, world)
     src = kernel_source_hash()
     line = {
-        "metric": METRIC,
+        "metric": WORKLOADS[WORKLOAD]["metric"],
         "value": round(value, 2),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -390,16 +402,17 @@ def emit_engine(args, cfg, res, world):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "data": "synthetic: seeded N(0,0.02) fp16 weights, 512 uniform-random prompt ids",
+        "data": WORKLOADS[WORKLOAD]["data"],
         "config": {
             "workload": f"{WORKLOAD}: 25 layers, d 2560, 20x128 q heads, 4 kv heads, ffn 9728, tied vocab 32000; "
                         "batch 1, prompt 512, greedy decode at contexts 513..1024",
-            "weights": "f16", "kv_cache": "f16", "batch": 1, "prompt": cfg["prompt_len"],
+            "weights": WORKLOADS[WORKLOAD]["weights"], "kv_cache": "f16", "batch": 1, "prompt": cfg["prompt_len"],
             "contexts": f"{cfg['prompt_len'] + 1}..{cfg['prompt_len'] + min(res['steps'], WINDOW)}",
             "kernel": "persistent: one cooperative launch per window of up to 512 chained decode steps "
                       "(e2e: one launch per step)",
             "ctas": res["ctas"],
-            "l2": "inputs larger than L2: every step streams 4.69 GB of weights (L2 129 MB)",
+            "l2": f"inputs larger than L2: every step streams {res['weight_bytes'] / 1e9:.2f} GB of weights "
+                  "(L2 129 MB)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "e2e": {"value": round(res["e2e"], 2), "unit": "tokens/s", "h2d_bytes_per_step": 32,
@@ -438,7 +451,7 @@ def run_reference(args, rank: int, world: int):
     value = cpu["value"]
     line = {
         "impl": "reference",
-        "metric": METRIC,
+        "metric": WORKLOADS[WORKLOAD]["metric"],
         "value": round(value, 4),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -449,9 +462,10 @@ def run_reference(args, rank: int, world: int):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "data": "synthetic: seeded N(0,0.02) fp16 weights",
+        "data": WORKLOADS[WORKLOAD]["data"],
         "config": {"workload": f"{WORKLOAD}: 25 layers, d 2560, tied vocab 32000; batch 1, greedy decode at "
-                               "contexts from 513", "weights": "f16", "batch": 1, "prompt": cfg["prompt_len"]},
+                               "contexts from 513", "weights": WORKLOADS[WORKLOAD]["weights"], "batch": 1,
+                   "prompt": cfg["prompt_len"]},
         "cpu_baseline": cpu,
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "reference": "CPU oracle (oracle/oracle.c, plain mode): the pages publish no code to install",
@@ -467,12 +481,15 @@ def main():
     ap.add_argument("--impl", choices=["engine", "reference"], default="engine")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=WORKLOAD,
+                    help="the benchmarked model (default: the 2.3B fp16 decoder)")
     ap.add_argument("--ablation-steps", type=int, default=64,
                     help="steps of the one-launch-per-phase ablation (0 = skip)")
     ap.add_argument("--timeline", default=None, help="write a per-phase breakdown of one step (JSON) here")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: use this many layers of the workload's shape (the line says so)")
     args = ap.parse_args()
+    globals()["WORKLOAD"] = args.workload
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))

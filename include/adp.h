@@ -67,9 +67,12 @@ typedef struct {
   int32_t n_layers, d_model, n_heads, n_kv_heads, head_dim, d_ff, vocab, max_ctx;
   float rms_eps, rope_theta;
   int32_t tied_embeddings;          /* 1: logits use tok_emb as the LM head */
-  int32_t weight_dtype, kv_dtype;   /* adp_dtype: ADP_F16 or ADP_BF16 for both */
+  int32_t weight_dtype, kv_dtype;   /* adp_dtype: ADP_F16 or ADP_BF16 for both; weight_dtype may be
+                                       ADP_E4M3 for a dense model (see embed_dtype and the scales) */
   int32_t n_experts, top_k, d_expert;
   int32_t router_dtype, expert_dtype; /* router: ADP_F16/ADP_BF16; experts: ADP_E4M3 */
+  int32_t embed_dtype;              /* with weight_dtype ADP_E4M3: type of tok_emb, lm_head and the
+                                       norm gains (ADP_F16 or ADP_BF16); otherwise ignored */
 } adp_config;
 
 /* Per-layer weights: DEVICE pointers, contiguous row-major, borrowed (never written; the
@@ -82,6 +85,11 @@ typedef struct {
   const void *e_gate, *e_up, *e_down;                     /* MoE: [E, f, d], [E, f, d], [E, d, f] e4m3 */
   const float *e_gate_scale, *e_up_scale, *e_down_scale;  /* MoE: [E, f], [E, f], [E, d] fp32, applied
                                                              to each output channel after its dot product */
+  /* weight_dtype ADP_E4M3 (dense): one fp32 scale per output row of wq, wk, wv, wo, w_gate, w_up,
+   * w_down ([hq*hd], [hkv*hd] x2, [d], [ff] x2, [d]), applied after that row's dot product (read
+   * in place); else NULL.  The pages project fp8 weights as the next step for large models
+   * ([H] translated comment thread, author reply: "FP8" MoE). */
+  const float *wq_scale, *wk_scale, *wv_scale, *wo_scale, *w_gate_scale, *w_up_scale, *w_down_scale;
 } adp_layer_weights;
 
 typedef struct {

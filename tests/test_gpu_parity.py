@@ -74,7 +74,7 @@ def test_tiny_temperature_sampling_bit_exact(torch_cuda):
     _check_case(cfg, 16, 48, temperature=0.7)
 
 
-@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "moe-32x1408-top4-e4m3"])
+@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "moe-32x1408-top4-e4m3", "dense-2.3b-e4m3"])
 def test_shrunk_workloads_bit_exact(torch_cuda, name):
     cfg = synth.shrink(synth.get_config(name))
     _check_case(cfg, 8, 40)
@@ -209,7 +209,7 @@ def test_moe_forced_experts_match_oracle(torch_cuda):
 
 
 @pytest.mark.parametrize("name,temperature", [("tiny", 0.7), ("moe-32x1408-top4-e4m3", 0.0),
-                                              ("dense-8b-bf16", 0.0)])
+                                              ("dense-8b-bf16", 0.0), ("dense-2.3b-e4m3", 0.0)])
 def test_in_kernel_multi_step_generation_matches_oracle(torch_cuda, name, temperature):
     """adp_generate_async runs n decode steps in one persistent launch, each step taking the token
     the previous one chose (and, at T > 0, the next uniform): the tokens and the whole KV cache
