@@ -450,7 +450,8 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
     }
     for (int ck = 0; ck < n_chunks; ++ck) {
       const long long cy0 = cyc_now();
-      bool ok = aborted(ctl) || mbar_wait(&ctl->full[slot], par, &ctl->abort, wait_ns);
+      // the wait itself gives up when another warp has aborted the step
+      const bool ok = mbar_wait(&ctl->full[slot], par, &ctl->abort, wait_ns);
       const long long cy1 = cyc_now();
       cyc_wait += cy1 - cy0;
       if (!ok) {
@@ -458,7 +459,7 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
         __syncwarp();
       }
       if (r == 0 && ck == 0 && cw == 0 && lane == 0) stamp(p, c, Pd.index, 8);
-      if (active && !aborted(ctl)) {
+      if (active && ok) {
         const int kck = min(KC, K - ck * KC);
         const int nvec = kck >> 3;
         const uint32_t slot_bytes = (uint32_t)m * ROWS * kck * EB;
