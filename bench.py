@@ -286,12 +286,18 @@ def run_engine(args, rank: int, world: int):
     kv.truncate(P)
     t = tok0
     torch.cuda.synchronize(dev)
+    per_step = []
     h0 = time.perf_counter()
     for i in range(n_e2e):
         if i and i % WINDOW == 0:
             kv.truncate(P)
+        s0 = time.perf_counter()
         t = kv.step(t)
+        per_step.append(time.perf_counter() - s0)
     h1 = time.perf_counter()
+    per_step.sort()
+    step_pct = {"p50_us": round(per_step[len(per_step) // 2] * 1e6, 1),
+                "p99_us": round(per_step[min(len(per_step) - 1, int(len(per_step) * 0.99))] * 1e6, 1)}
     ms, e2e_s = max_over_ranks([ms, h1 - h0], world)
     e2e = whole_job_rate(n_e2e, e2e_s, world)
 
@@ -301,7 +307,7 @@ def run_engine(args, rank: int, world: int):
         write_timeline(args.timeline, model, kv, tok0, P, cfg)
 
     res = {
-        "ms": ms, "steps": args.steps, "n_launch": n_launch, "weight_bytes": bound.weight_bytes_per_token(cfg), "achieved_gbs": achieved, "per_launch_bytes": per_launch,
+        "ms": ms, "steps": args.steps, "n_launch": n_launch, "step_pct": step_pct, "weight_bytes": bound.weight_bytes_per_token(cfg), "achieved_gbs": achieved, "per_launch_bytes": per_launch,
         "launch_ms": launch_ms, "peak": peak, "peak_kind": peak_kind, "e2e": e2e, "n_e2e": n_e2e,
         "clocks": clocks.summary(), "ctas": model.num_ctas, "image_bytes": model.image_bytes,
         # one cooperative launch per window of chained steps (adp_generate_async)
@@ -416,7 +422,7 @@ def emit_engine(args, cfg, res, world):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "e2e": {"value": round(res["e2e"], 2), "unit": "tokens/s", "h2d_bytes_per_step": 32,
-                "d2h_bytes_per_step": 8, "steps": res["n_e2e"],
+                "d2h_bytes_per_step": 8, "steps": res["n_e2e"], "per_step": res["step_pct"],
                 "path": "adp_decode_step per token (host token in, host token out, stream sync)"},
         "roofline": {"bound": "hbm", "achieved": round(res["achieved_gbs"], 1), "peak": res["peak"],
                      "unit": "GB/s", "frac": round(res["achieved_gbs"] / res["peak"], 4),
