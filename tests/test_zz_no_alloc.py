@@ -71,15 +71,18 @@ def test_two_calls_in_a_row_match_decode_step(lib):
 
 
 def test_sampling_and_alternating_models(lib):
-    """Temperature sampling, and two models with different scratch layouts taking turns."""
+    """Temperature sampling, and models with different scratch layouts and kernel kinds (16-bit
+    dense, e4m3 dense) taking turns."""
     a = _pair(synth.get_config("tiny"), 8)
     b = _pair(synth.shrink(synth.get_config("dense-2.3b-fp16")), 8)
-    ta, tb = a[3], b[3]
+    e = _pair(synth.shrink(synth.get_config("dense-2.3b-e4m3")), 8)
+    ta, tb, te = a[3], b[3], e[3]
     for i in range(3):
         ta = _both(lib, *a[:3], ta, 0.7, 0.25 + 0.2 * i)
         tb = _both(lib, *b[:3], tb)
-    a[0].close()
-    b[0].close()
+        te = _both(lib, *e[:3], te)
+    for m in (a, b, e):
+        m[0].close()
 
 
 def test_scratch_beyond_the_static_array_is_rejected(lib):
