@@ -102,6 +102,7 @@ _SIGS = [
     ("adp_debug_set_l2_lookahead", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
     ("adp_debug_set_ring_slots", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     ("adp_debug_ring_slots", ctypes.c_int, [ctypes.c_void_p]),
+    ("adp_debug_set_epoch_base", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
     ("adp_debug_set_wait_limit", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64]),
     ("adp_debug_skip_publication", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32]),
 ]
@@ -298,6 +299,10 @@ def adp_debug_set_ring_slots(model, slots: int):
 
 def adp_debug_ring_slots(model) -> int:
     return int(load_library().adp_debug_ring_slots(model))
+
+
+def adp_debug_set_epoch_base(model, base: int):
+    _check(load_library().adp_debug_set_epoch_base(model, int(base)), "adp_debug_set_epoch_base")
 
 
 def adp_debug_set_wait_limit(model, ns: int):

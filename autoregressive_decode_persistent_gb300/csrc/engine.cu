@@ -77,6 +77,7 @@ struct adp_model {
   const void* graph_key_logits = nullptr;
   bool graph_key_sample = false;
   int sticky = ADP_OK;
+  uint64_t epochs_used = 0;  // epochs handed out since the exchange buffers were last cleared
   size_t ll_bytes[11] = {0};  // sizes of the epoch-tagged exchange buffers
 
   template <class T>
@@ -222,6 +223,20 @@ static int clear_exchange(adp_model* m) {
   void* bufs[11] = {p.x, p.q, p.attn, p.h, p.rlog, p.knew, p.vnew, p.part_m, p.part_l, p.part_o, p.tok_word};
   for (int i = 0; i < 11; ++i) CK(cudaMemsetAsync(bufs[i], 0, m->ll_bytes[i], m->stream));
   CK(cudaMemsetAsync(p.epoch, 0, 4, m->stream));
+  m->epochs_used = 0;
+  return ADP_OK;
+}
+
+// Epochs are 32-bit and every step takes n_phases of them.  Before the steps about to be
+// enqueued would run past 2^32, start over: zero the exchange buffers and the epoch base
+// (stream-ordered, between launches), so that tags never wrap around.
+static int reserve_epochs(adp_model* m, int n_steps) {
+  const uint64_t need = (uint64_t)m->phases.size() * ((uint64_t)n_steps + 1);
+  if (m->epochs_used + need >= (1ull << 32)) {
+    const int rc = clear_exchange(m);
+    if (rc) return rc;
+  }
+  m->epochs_used += (uint64_t)m->phases.size() * (uint64_t)n_steps;
   return ADP_OK;
 }
 
@@ -604,6 +619,8 @@ static int enqueue_step(adp_model* m, const Params& p, bool sampling);
 // step takes the token the previous one chose, or the next of p.tok_seq); in the ablation modes
 // the launches of one step, n times.
 static int enqueue_steps(adp_model* m, const Params& p, bool sampling, int n) {
+  const int rs = reserve_epochs(m, n);
+  if (rs) return rs;
   if (m->mode == 0) {
     Params q = p;
     q.n_steps = n;
@@ -673,7 +690,7 @@ extern "C" int adp_decode_step(adp_model* m, adp_kv* kv, int32_t token, const ad
   int rs = put_state(m, kv->len, token, T, sampling ? sampling->u : 0.0f);
   if (rs) return rs;
   Params p = step_params(m, kv, dev_logits, nullptr, nullptr, nullptr);
-  int rc = enqueue_step(m, p, T > 0.0f);
+  int rc = enqueue_steps(m, p, T > 0.0f, 1);
   m->p.skip_cta = m->p.skip_phase = -1;
   if (rc) return rc;
   rc = finish(m);
@@ -813,6 +830,7 @@ int adp::scratch_layout(const adp_model* m, ScratchLayout* out) {
   l.state = take(sizeof(StepState));
   l.logits = take((size_t)c.vocab * 4);
   l.total = off;
+  l.n_phases = m->phases.size();
   return ADP_OK;
 }
 
@@ -970,6 +988,17 @@ extern "C" int adp_debug_set_ring_slots(adp_model* m, int32_t slots) {
 }
 
 extern "C" int adp_debug_ring_slots(const adp_model* m) { return m ? m->p.nslots : 0; }
+
+extern "C" int adp_debug_set_epoch_base(adp_model* m, uint32_t base) {
+  if (!m) return ADP_ERR_INVALID_ARG;
+  CK(cudaStreamSynchronize(m->stream));
+  int rc = clear_exchange(m);
+  if (rc) return rc;
+  CK(cudaMemcpyAsync(m->p.epoch, &base, 4, cudaMemcpyHostToDevice, m->stream));
+  CK(cudaStreamSynchronize(m->stream));
+  m->epochs_used = base;
+  return ADP_OK;
+}
 
 extern "C" int adp_debug_set_wait_limit(adp_model* m, uint64_t ns) {
   if (!m || ns == 0) return ADP_ERR_INVALID_ARG;

@@ -5,8 +5,8 @@
 // Every call, from every model, shares the one array.  Its contents must start at zero: they do
 // when the module is loaded, every completed step leaves them in a state the next step accepts
 // (attention and sampling counters back at zero, the epoch base advanced past every tag written),
-// and this file clears the array again whenever a model with a different layout uses it or a step
-// ends in a device-side error.  Calls that overlap in time (two host threads, or two streams)
+// and this file clears the array again whenever a model with a different layout uses it, a step
+// ends in a device-side error, or the 32-bit epoch tags would run past 2^32.  Calls that overlap in time (two host threads, or two streams)
 // race on the array and give wrong results: serialise them.
 #include <cuda_runtime.h>
 
@@ -25,6 +25,7 @@ struct DeviceSlot {
   unsigned char* addr = nullptr;  // device address of g_step_scratch on this device
   bool have_layout = false;
   adp::ScratchLayout layout{};    // layout of the last step taken in the array
+  uint64_t epochs_used = 0;       // epochs handed out since the array was last zeroed
 };
 
 std::mutex g_mutex;
@@ -68,12 +69,16 @@ extern "C" int adp_decode_step_noalloc(adp_model* m, adp_kv* kv, int32_t token, 
     s.addr = static_cast<unsigned char*>(ptr);
   }
   // A model with another layout would read words that the last one left at other offsets.
-  const bool same = s.have_layout && std::memcmp(&s.layout, &lay, sizeof lay) == 0;
+  // ... and 32-bit epoch tags must not run past 2^32: start over before they would.
+  const bool same = s.have_layout && std::memcmp(&s.layout, &lay, sizeof lay) == 0 &&
+                    s.epochs_used + 2 * lay.n_phases < (1ull << 32);
   const size_t zero = same ? 0 : kStaticScratchBytes;
+  if (!same) s.epochs_used = 0;
   s.layout = lay;
   s.have_layout = true;
   const int rc = adp::decode_step_in_scratch(m, kv, token, sampling, next_token, dev_logits, s.addr, lay, zero,
                                              kStaticScratchBytes);
   if (rc != ADP_OK) s.have_layout = false;  // the next call starts the array over from zero
+  else s.epochs_used += lay.n_phases;
   return rc;
 }

@@ -15,6 +15,7 @@ struct ScratchLayout {
   size_t x, q, attn, h, rlog, knew, vnew, epoch, tok_word, part_m, part_l, part_o, sblock, sample_ctr, argkey,
       lm_ctr, bar_ctr, err, sel_out, state, logits;
   size_t total;
+  size_t n_phases;  // epochs one step takes
 };
 
 // Layout for model m (host only, no CUDA call).  Returns ADP_ERR_INVALID_ARG for a null model.

@@ -62,10 +62,14 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+KERNEL_SOURCES = ("decode.cu", "device.cuh", "plan.h")  # the decode kernel's device code
+
+
 def kernel_source_hash() -> str:
+    """sha256[:16] over the decode kernel's sources (host-only files do not change its traffic)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "autoregressive_decode_persistent_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

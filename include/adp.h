@@ -245,6 +245,9 @@ int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes);
  * else ADP_ERR_INVALID_ARG), for measurements.  adp_debug_ring_slots reads the current depth. */
 int adp_debug_set_ring_slots(adp_model* m, int32_t slots);
 int adp_debug_ring_slots(const adp_model* m);
+/* Test hook: clear the exchange buffers and start the model's 32-bit epoch counter at `base`
+ * (the engine clears and restarts it by itself before a step would run past 2^32). */
+int adp_debug_set_epoch_base(adp_model* m, uint32_t base);
 /* Wait limit of every in-kernel spin (grid barrier, weight pipeline), nanoseconds (default 2e8). */
 int adp_debug_set_wait_limit(adp_model* m, uint64_t ns);
 /* Test hook: in the next step, CTA `cta` withholds the outputs of phase number `phase` (-1 = off),

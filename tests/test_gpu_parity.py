@@ -235,3 +235,37 @@ def test_in_kernel_multi_step_generation_matches_oracle(torch_cuda, name, temper
     m = len(prompt) + n
     assert np.array_equal(k[:, :, :m], om.kc[:, :, :m]) and np.array_equal(v[:, :, :m], om.vc[:, :, :m])
     model.close()
+
+
+def test_epoch_counter_restarts_before_it_would_wrap(torch_cuda):
+    """Started two steps short of 2^32 epochs, the engine zeroes its exchange buffers and restarts
+    the counter before the step that would run past it: tokens and logits equal a fresh model's,
+    for single steps and for a multi-step launch."""
+    import torch
+    from autoregressive_decode_persistent_gb300 import adp
+    cfg = synth.get_config("tiny")
+    W = synth.model_weights(cfg)
+    a, b = _model(cfg, W), _model(cfg, W)
+    kva, kvb = a.new_kv(), b.new_kv()
+    nph = 2 * 5 + 2  # tiny: five phases per layer, then the LM head and sampling
+    # restart at the third single step; right away; before the multi-step launch
+    for base in (2**32 - 4 * nph, 2**32 - 7, 2**32 - 10 * nph):
+        adp.adp_debug_set_epoch_base(a.handle, base)
+        kva.reset()
+        kvb.reset()
+        lga = torch.empty(cfg["vocab"], device=a.device)
+        lgb = torch.empty(cfg["vocab"], device=b.device)
+        ta = tb = 3
+        for _ in range(4):
+            ta = kva.step(ta, logits=lga)
+            tb = kvb.step(tb, logits=lgb)
+            assert ta == tb and torch.equal(lga, lgb)
+        oa = torch.empty(12, dtype=torch.int32, device=a.device)
+        ob = torch.empty(12, dtype=torch.int32, device=b.device)
+        kva.generate_async(ta, 12, oa)
+        kvb.generate_async(tb, 12, ob)
+        adp.adp_sync(a.handle)
+        adp.adp_sync(b.handle)
+        assert oa.cpu().tolist() == ob.cpu().tolist()
+    a.close()
+    b.close()
