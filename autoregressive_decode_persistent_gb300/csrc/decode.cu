@@ -407,8 +407,8 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
   const int pos = st.pos;
   const uint64_t wait_ns = p.wait_ns;
   const uint32_t ns = (uint32_t)p.nslots;
-  uint32_t t = t_io;
-  uint32_t slot = t % ns, par = (t / ns) & 1u;  // ring slot of tile t and the parity of its use
+  // the consumer's ring cursor: slot of its next tile (low byte) and that slot's use parity
+  uint32_t slot = t_io & 0xFFu, par = t_io >> 8;
   int32_t u0, n;
   cta_units(Pd, c, G, u0, n);
   unsigned long long best = 0ull;  // LM: packed running maximum of this warp
@@ -483,7 +483,6 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
       cyc_comp += cyc_now() - cy1;
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->empty[slot]);
-      ++t;
       if (++slot == ns) {
         slot = 0;
         par ^= 1u;
@@ -615,7 +614,7 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
     }
     consumer_sync();
   }
-  t_io = t;
+  t_io = slot | (par << 8);
 }
 
 // ---------------------------------------------------------------- finalisation
