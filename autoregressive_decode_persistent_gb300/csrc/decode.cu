@@ -87,10 +87,20 @@ __device__ __forceinline__ void cta_units(const PhaseDesc& P, uint32_t c, uint32
 
 // The step's phase table, copied into shared memory after the control block at kernel start
 // (every phase begins by reading its descriptor: from global memory that would be a round trip
-// to L2 on the critical path of every phase).
+// to L2 on the critical path of every phase), followed by this CTA's unit range of each phase.
 constexpr size_t kCtlPad = (sizeof(Ctl) + 15) & ~(size_t)15;
 __device__ __forceinline__ const PhaseDesc* phase_table(const Ctl* ctl) {
   return reinterpret_cast<const PhaseDesc*>(reinterpret_cast<const uint8_t*>(ctl) + kCtlPad);
+}
+__device__ __forceinline__ int2* share_table(const Ctl* ctl, int n_phases) {
+  return const_cast<int2*>(reinterpret_cast<const int2*>(phase_table(ctl) + n_phases));
+}
+// This CTA's units [u0, u0 + n) of phase P, as computed at kernel start.
+__device__ __forceinline__ void cta_share(const Params& p, const Ctl* ctl, const PhaseDesc& P, int32_t& u0,
+                                          int32_t& n) {
+  const int2 v = share_table(ctl, p.n_phases)[P.index];
+  u0 = v.x;
+  n = v.y;
 }
 
 // ---------------------------------------------------------------- producer (TMA) warp
@@ -114,7 +124,7 @@ __device__ __forceinline__ void l2_advance(const Params& p, const Ctl* ctl, L2Cu
     if (!Q.has_weights) { ++cur.ph; cur.off = 0; continue; }
     if (Q.kind == PK_EGU || Q.kind == PK_EDOWN) return;  // experts not chosen yet
     int32_t u0, n;
-    cta_units(Q, c, G, u0, n);
+    cta_share(p, ctl, Q, u0, n);
     const uint64_t unit_bytes = (uint64_t)Q.unit_rows * Q.K * Q.eb;
     const uint64_t len = (uint64_t)n * unit_bytes;
     if (cur.off >= len) { ++cur.ph; cur.off = 0; continue; }
@@ -129,7 +139,8 @@ __device__ __forceinline__ void l2_advance(const Params& p, const Ctl* ctl, L2Cu
 __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, uint32_t G, int ph0, int ph1) {
   const uint64_t pol = policy_evict_first();
   const uint32_t ns = (uint32_t)p.nslots;
-  uint32_t t = 0;
+  uint32_t t = 0;               // tiles issued
+  uint32_t pslot = 0, puse = 0;  // ring slot of the next tile and how often it was filled before
   uint32_t sel_uses = 0;
   int sel_layer = -1;
   bool stop = false;
@@ -142,7 +153,7 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
       const PhaseDesc P = phase_table(ctl)[ph];
       if (!P.has_weights) continue;
       int32_t u0, n;
-      cta_units(P, c, G, u0, n);
+      cta_share(p, ctl, P, u0, n);
       const bool expert = P.kind == PK_EGU || P.kind == PK_EDOWN;
       if (!expert && cur.ph < ph) cur = L2Cursor{ph, 0, issue_pos};  // behind, or waited at the experts
       if (expert && sel_layer != P.layer) {
@@ -168,8 +179,8 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
           const int kck = min(P.KC, P.K - ck * P.KC);
           const uint32_t bytes = (uint32_t)m * P.unit_rows * kck * P.eb;
           const uint64_t off = round_off + (uint64_t)m * P.unit_rows * ck * P.KC * P.eb;
-          const uint32_t slot = t % ns, use = t / ns;
-          if (t >= ns) {
+          const uint32_t slot = pslot, use = puse;
+          if (use > 0) {
             if (!mbar_try_wait(&ctl->empty[slot], (use - 1) & 1)) {
               const uint64_t tb = p.timeline ? globaltimer() : 0;
               l2_advance(p, ctl, cur, issue_pos, ph1, c, G);  // keep HBM busy while the consumers catch up
@@ -194,6 +205,10 @@ __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, u
           }
           if (!expert) issue_pos += bytes;
           ++t;
+          if (++pslot == ns) {
+            pslot = 0;
+            ++puse;
+          }
         }
       }
       stamp(p, c, ph, 5);
@@ -343,7 +358,7 @@ __device__ void rmsnorm_prologue(const Params& p, Ctl* ctl, float* xbuf, const v
 __device__ void stage_residual(const Params& p, Ctl* ctl, const PhaseDesc& P, uint32_t c, uint32_t G,
                                int rows_per_unit, uint32_t x_epoch, int cw, int lane) {
   int32_t u0, n;
-  cta_units(P, c, G, u0, n);
+  cta_share(p, ctl, P, u0, n);
   const int tid = cw * 32 + lane;
   if (tid < n * rows_per_unit) {
     const ll_t* src = p.x + (size_t)u0 * rows_per_unit + tid;
@@ -410,7 +425,7 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
   // the consumer's ring cursor: slot of its next tile (low byte) and that slot's use parity
   uint32_t slot = t_io & 0xFFu, par = t_io >> 8;
   int32_t u0, n;
-  cta_units(Pd, c, G, u0, n);
+  cta_share(p, ctl, Pd, u0, n);
   unsigned long long best = 0ull;  // LM: packed running maximum of this warp
   long long cyc_wait = 0, cyc_comp = 0, cyc_epi = 0;  // timeline: SM cycles waiting / computing / epilogues
   const int rounds = n > 0 ? (n + upr - 1) / upr : 0;
@@ -1159,7 +1174,7 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
       const uint32_t e_res = st.ebase + 1 + (uint32_t)P.res_ph;
       const uint32_t e_sel = st.ebase + 1 + (uint32_t)P.sel_ph;
       int32_t u0, n;
-      cta_units(P, c, G, u0, n);
+      cta_share(p, ctl, P, u0, n);
       if (cw == 0 && lane == 0) stamp(p, c, ph, 0);
       // ---- prologue: the GEMV input vector into shared memory (skipped by CTAs without units)
       switch (P.kind) {
@@ -1321,6 +1336,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint2* dst = reinterpret_cast<uint2*>(const_cast<PhaseDesc*>(phase_table(ctl)));
     const int nv = p.n_phases * (int)(sizeof(PhaseDesc) / 8);
     for (int i = threadIdx.x; i < nv; i += kThreads) dst[i] = __ldg(src + i);
+    int2* shares = share_table(ctl, p.n_phases);
+    for (int i = threadIdx.x; i < p.n_phases; i += kThreads) {
+      int32_t u0, n;
+      cta_units(p.phases[i], blockIdx.x, gridDim.x, u0, n);
+      shares[i] = make_int2(u0, n);
+    }
   }
   __syncthreads();
   if (*(volatile int32_t*)&ctl->abort) return;  // sticky device error: nothing runs until reset
@@ -1370,5 +1391,5 @@ cudaError_t decode_launch(const Params& p, int ph0, int ph1, bool persistent, in
 }  // namespace adp
 
 namespace adp {
-size_t ctl_bytes(int n_phases) { return kCtlPad + (size_t)n_phases * sizeof(PhaseDesc); }
+size_t ctl_bytes(int n_phases) { return kCtlPad + (size_t)n_phases * (sizeof(PhaseDesc) + sizeof(int2)); }
 }  // namespace adp
