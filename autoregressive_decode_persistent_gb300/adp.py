@@ -85,6 +85,11 @@ _SIGS = [
     ("adp_generate_async", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                           ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]),
     ("adp_sync", ctypes.c_int, [ctypes.c_void_p]),
+    ("adp_decode_batch", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                        ctypes.POINTER(Sampling), ctypes.c_void_p, ctypes.c_void_p]),
+    ("adp_generate_batch_async", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    ("adp_max_batch", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     ("adp_reset", ctypes.c_int, [ctypes.c_void_p]),
     ("adp_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("adp_last_error", ctypes.c_char_p, []),
@@ -231,6 +236,44 @@ def adp_generate_async(model, kv, token: int, n: int, temperature: float, dev_u,
 
 def adp_sync(model):
     _check(load_library().adp_sync(model), "adp_sync")
+
+
+def _kv_table(kvs):
+    """HOST array of adp_kv handles (kept alive by the caller for the duration of the call)."""
+    return (ctypes.c_void_p * len(kvs))(*[k.value if isinstance(k, ctypes.c_void_p) else k for k in kvs])
+
+
+def adp_decode_batch(model, kvs, tokens, temperatures=None, us=None, dev_logits=None) -> list[int]:
+    """One batched step: kvs[r] takes tokens[r]; returns the chosen tokens (HOST list)."""
+    nb = len(kvs)
+    table = _kv_table(kvs)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    assert len(tok) == nb
+    samp = None
+    if temperatures is not None:
+        arr = (Sampling * nb)(*[Sampling(float(temperatures[r]), float(us[r] if us is not None else 0.0))
+                                for r in range(nb)])
+        samp = ctypes.cast(arr, ctypes.POINTER(Sampling))
+    out = np.zeros(nb, dtype=np.int32)
+    _check(load_library().adp_decode_batch(model, table, nb, _ptr(tok), samp, _ptr(out), _ptr(dev_logits)),
+           "adp_decode_batch")
+    return [int(t) for t in out]
+
+
+def adp_generate_batch_async(model, kvs, tokens, n: int, temperatures=None, dev_u=None, dev_tokens_out=None):
+    nb = len(kvs)
+    table = _kv_table(kvs)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    assert len(tok) == nb
+    temps = None if temperatures is None else np.ascontiguousarray(temperatures, dtype=np.float32)
+    _check(load_library().adp_generate_batch_async(model, table, nb, _ptr(tok), int(n), _ptr(temps), _ptr(dev_u),
+                                                   _ptr(dev_tokens_out)), "adp_generate_batch_async")
+
+
+def adp_max_batch(model) -> int:
+    nb = ctypes.c_int32()
+    _check(load_library().adp_max_batch(model, ctypes.byref(nb)), "adp_max_batch")
+    return nb.value
 
 
 def adp_reset(model):

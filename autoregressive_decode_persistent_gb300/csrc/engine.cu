@@ -9,6 +9,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -70,6 +71,7 @@ struct adp_model {
   int32_t* d_force = nullptr;
   bool force_on = false;
   float* d_logits_scratch = nullptr;
+  std::vector<adp_kv*> kvs;  // live caches of this model (orphaned when the model goes first)
   int mode = 0;
   // multi-kernel graph cache
   cudaGraphExec_t graph = nullptr;
@@ -79,6 +81,27 @@ struct adp_model {
   int sticky = ADP_OK;
   uint64_t epochs_used = 0;  // epochs handed out since the exchange buffers were last cleared
   size_t ll_bytes[11] = {0};  // sizes of the epoch-tagged exchange buffers
+  // Batched decode (set up at the first batched call): per-request buffers for kMaxBatch
+  // requests, the per-request step state and KV cache tables, and the shared-memory layout of
+  // each batch size.
+  struct BatchHost {
+    StepState st[kMaxBatch];
+    uint16_t* kcb[kMaxBatch];
+    uint16_t* vcb[kMaxBatch];
+  };
+  struct Batch {
+    int init_rc = 1;  // 1: not set up yet; else the set-up's status
+    int max_nb = 0;
+    size_t smem[kMaxBatch + 1] = {};
+    int nslots[kMaxBatch + 1] = {}, xbuf_floats[kMaxBatch + 1] = {}, att_slots[kMaxBatch + 1] = {};
+    Params p{};                    // the batch buffers (per-request copies back to back)
+    BatchHost* h = nullptr;        // pinned staging of the step state and cache tables
+    BatchHost* d = nullptr;
+    cudaEvent_t copied = nullptr;  // the last copy out of h has executed
+    int32_t* h_out = nullptr;      // pinned: out_token per request, then err
+    float* d_logits = nullptr;     // [kMaxBatch][V] logits when the caller passes none
+    size_t ll_bytes[11] = {0};
+  } bt;
 
   template <class T>
   int alloc(T** ptr, size_t count) {
@@ -222,6 +245,12 @@ static int clear_exchange(adp_model* m) {
   const Params& p = m->p;
   void* bufs[11] = {p.x, p.q, p.attn, p.h, p.rlog, p.knew, p.vnew, p.part_m, p.part_l, p.part_o, p.tok_word};
   for (int i = 0; i < 11; ++i) CK(cudaMemsetAsync(bufs[i], 0, m->ll_bytes[i], m->stream));
+  if (m->bt.init_rc == ADP_OK) {
+    const Params& b = m->bt.p;
+    void* bb[11] = {b.x, b.q, b.attn, b.h, nullptr, b.knew, b.vnew, b.part_m, b.part_l, b.part_o, b.tok_word};
+    for (int i = 0; i < 11; ++i)
+      if (bb[i]) CK(cudaMemsetAsync(bb[i], 0, m->bt.ll_bytes[i], m->stream));
+  }
   CK(cudaMemsetAsync(p.epoch, 0, 4, m->stream));
   m->epochs_used = 0;
   return ADP_OK;
@@ -489,6 +518,10 @@ extern "C" void adp_destroy_model(adp_model* m) {
   for (void* q : m->allocs) cudaFree(q);
   if (m->h_state) cudaFreeHost(m->h_state);
   if (m->h_out) cudaFreeHost(m->h_out);
+  if (m->bt.copied) cudaEventDestroy(m->bt.copied);
+  if (m->bt.h) cudaFreeHost(m->bt.h);
+  if (m->bt.h_out) cudaFreeHost(m->bt.h_out);
+  for (adp_kv* kv : m->kvs) kv->m = nullptr;  // still valid for adp_kv_destroy, for nothing else
   delete m;
 }
 
@@ -510,26 +543,31 @@ extern "C" int adp_kv_create(adp_model* m, adp_kv** out) {
     adp_kv_destroy(kv);
     return cuda_fail(e, "adp_kv_create");
   }
+  m->kvs.push_back(kv);
   *out = kv;
   return ADP_OK;
 }
 
 extern "C" void adp_kv_destroy(adp_kv* kv) {
   if (!kv) return;
-  if (kv->m && kv->m->stream) cudaStreamSynchronize(kv->m->stream);
+  if (kv->m) {
+    if (kv->m->stream) cudaStreamSynchronize(kv->m->stream);
+    auto& v = kv->m->kvs;
+    v.erase(std::remove(v.begin(), v.end(), kv), v.end());
+  }
   if (kv->k) cudaFree(kv->k);
   if (kv->v) cudaFree(kv->v);
   delete kv;
 }
 
 extern "C" int adp_kv_reset(adp_kv* kv) {
-  if (!kv) return ADP_ERR_INVALID_ARG;
+  if (!kv || !kv->m) return ADP_ERR_INVALID_ARG;
   kv->len = 0;
   return ADP_OK;
 }
 
 extern "C" int adp_kv_truncate(adp_kv* kv, int32_t len) {
-  if (!kv || len < 0 || len > kv->len) return ADP_ERR_INVALID_ARG;
+  if (!kv || !kv->m || len < 0 || len > kv->len) return ADP_ERR_INVALID_ARG;
   kv->len = len;
   return ADP_OK;
 }
@@ -564,7 +602,7 @@ static int kv_copy(const adp_kv* kv, void* host_k, void* host_v, int32_t len, bo
 }
 
 extern "C" int adp_kv_load(adp_kv* kv, const void* host_k, const void* host_v, int32_t len) {
-  if (!kv || len < 0 || (len > 0 && (!host_k || !host_v))) return ADP_ERR_INVALID_ARG;
+  if (!kv || !kv->m || len < 0 || (len > 0 && (!host_k || !host_v))) return ADP_ERR_INVALID_ARG;
   if (len > kv->m->cfg.max_ctx) return ADP_ERR_CONTEXT_OVERFLOW;
   int rc = kv_copy(kv, const_cast<void*>(host_k), const_cast<void*>(host_v), len, true);
   if (rc == ADP_OK) kv->len = len;
@@ -572,7 +610,7 @@ extern "C" int adp_kv_load(adp_kv* kv, const void* host_k, const void* host_v, i
 }
 
 extern "C" int adp_kv_read(const adp_kv* kv, void* host_k, void* host_v, int32_t len) {
-  if (!kv || len < 0 || (len > 0 && (!host_k || !host_v))) return ADP_ERR_INVALID_ARG;
+  if (!kv || !kv->m || len < 0 || (len > 0 && (!host_k || !host_v))) return ADP_ERR_INVALID_ARG;
   if (len > kv->m->cfg.max_ctx) return ADP_ERR_CONTEXT_OVERFLOW;
   return kv_copy(kv, host_k, host_v, len, false);
 }
@@ -749,6 +787,210 @@ extern "C" int adp_generate_async(adp_model* m, adp_kv* kv, int32_t token, int32
   return ADP_OK;
 }
 
+// ---------------------------------------------------------------- small-batch decode
+
+// Set up batched decode once per model: the shared-memory layout of every batch size that fits
+// (nb input vectors of the widest GEMV input beside a ring of at least two slots), the
+// per-request exchange buffers and the step-state staging.  Dense 16-bit models only.
+static int batch_init(adp_model* m) {
+  adp_model::Batch& B = m->bt;
+  if (B.init_rc != 1) return B.init_rc;
+  const adp_config& c = m->cfg;
+  B.init_rc = ADP_ERR_UNSUPPORTED_CONFIG;
+  if (c.n_experts != 0 || (c.weight_dtype != ADP_F16 && c.weight_dtype != ADP_BF16)) return B.init_rc;
+  const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim;
+  cudaDeviceProp prop;
+  CK(cudaGetDeviceProperties(&prop, m->device));
+  const size_t optin = (size_t)prop.sharedMemPerBlockOptin;
+  const int nph = (int)m->phases.size();
+  const size_t ctl_sz = (ctl_bytes(nph) + 16 + batch_ctl_bytes() + 127) & ~(size_t)127;
+  const int nbmax = (c.max_ctx + kAttnBlock - 1) / kAttnBlock;
+  const size_t item = (size_t)kAttnBlock * (hd + 8) * 2 + (size_t)kAttnBlock * hd * 2 + (size_t)kMaxGroup * hd * 4 +
+                      (size_t)kMaxGroup * kAttnBlock * 4;
+  auto pad256 = [](int n) { return (size_t)((n + 255) / 256 * 256); };
+  const size_t vec_floats = std::max({pad256(d), pad256(hq * hd), pad256(c.d_ff)});
+  const size_t merge_bytes = ((size_t)2 * 8 * nbmax + 8) * 4;
+  const int gmax = m->p.att_gmax;
+  size_t smem_max = 0;
+  for (int nb = 1; nb <= kMaxBatch; ++nb) {
+    if (nb * hq > m->G) break;  // CTA G-1-(r*hq+h) merges head h of request r
+    const size_t vec_bytes = std::max((size_t)nb * vec_floats * 4, merge_bytes);
+    int ns = 0, att = 0;
+    size_t xbytes = 0;
+    for (int k = kMaxSlots; k >= 2 && !ns; --k) {
+      if ((size_t)k * kSlotBytes + ctl_sz > optin) continue;
+      const size_t room = optin - (size_t)k * kSlotBytes - ctl_sz;
+      if (room < vec_bytes || room < item) continue;
+      ns = k;
+      att = (int)std::min<size_t>(std::min(kAttnSlots, kConsumerWarps / gmax), room / item);
+      xbytes = std::max(vec_bytes, (size_t)att * item);
+    }
+    if (!ns) break;
+    xbytes = (xbytes + 127) & ~(size_t)127;
+    B.nslots[nb] = ns;
+    B.att_slots[nb] = att;
+    B.xbuf_floats[nb] = (int)(xbytes / 4);
+    B.smem[nb] = (size_t)ns * kSlotBytes + xbytes + ctl_sz;
+    smem_max = std::max(smem_max, B.smem[nb]);
+    B.max_nb = nb;
+  }
+  if (B.max_nb == 0) return B.init_rc;
+  int bps = 0;
+  CK(decode_batch_prepare(smem_max, &bps));
+  if (bps < 1) return B.init_rc = ADP_ERR_NOT_CORESIDENT;
+  // per-request copies of the exchange buffers, for kMaxBatch requests
+  Params& p = B.p;
+  p = m->p;
+  const size_t R = kMaxBatch;
+  const int nblk = (c.vocab + kVocabBlock - 1) / kVocabBlock;
+  int rc;
+  if ((rc = m->alloc(&p.x, R * d)) || (rc = m->alloc(&p.q, R * hq * hd)) || (rc = m->alloc(&p.attn, R * hq * hd)) ||
+      (rc = m->alloc(&p.h, R * c.d_ff)) || (rc = m->alloc(&p.knew, R * hkv * hd)) ||
+      (rc = m->alloc(&p.vnew, R * hkv * hd)) || (rc = m->alloc(&p.tok_word, R)) ||
+      (rc = m->alloc(&p.part_m, R * hq * nbmax)) || (rc = m->alloc(&p.part_l, R * hq * nbmax)) ||
+      (rc = m->alloc(&p.part_o, R * hq * nbmax * hd)) || (rc = m->alloc(&p.sblock, R * nblk)) ||
+      (rc = m->alloc(&p.sample_ctr, R)) || (rc = m->alloc(&p.argkey, R)) || (rc = m->alloc(&B.d, 1)) ||
+      (rc = m->alloc(&B.d_logits, R * c.vocab)))
+    return B.init_rc = rc;
+  p.rlog = nullptr;
+  const size_t sizes[11] = {R * d * 8, R * hq * hd * 8, R * hq * hd * 8, R * c.d_ff * 8, 0, R * hkv * hd * 8,
+                            R * hkv * hd * 8, R * hq * nbmax * 8, R * hq * nbmax * 8, R * hq * nbmax * hd * 8, R * 8};
+  for (int i = 0; i < 11; ++i) B.ll_bytes[i] = sizes[i];
+  void* bb[11] = {p.x, p.q, p.attn, p.h, nullptr, p.knew, p.vnew, p.part_m, p.part_l, p.part_o, p.tok_word};
+  for (int i = 0; i < 11; ++i)
+    if (bb[i]) CK(cudaMemsetAsync(bb[i], 0, sizes[i], m->stream));
+  CK(cudaMemsetAsync(p.sample_ctr, 0, 4 * R, m->stream));
+  CK(cudaMemsetAsync(p.argkey, 0, 8 * R, m->stream));
+  CK(cudaMemsetAsync(B.d, 0, sizeof(adp_model::BatchHost), m->stream));
+  CK(cudaMallocHost(&B.h, sizeof(adp_model::BatchHost)));
+  std::memset(B.h, 0, sizeof(adp_model::BatchHost));
+  CK(cudaMallocHost(&B.h_out, (kMaxBatch + 1) * sizeof(int32_t)));
+  CK(cudaEventCreateWithFlags(&B.copied, cudaEventDisableTiming));
+  CK(cudaEventRecord(B.copied, m->stream));
+  uint8_t* dbase = reinterpret_cast<uint8_t*>(B.d);  // device addresses of the staged fields
+  p.state = reinterpret_cast<StepState*>(dbase + offsetof(adp_model::BatchHost, st));
+  p.kcb = reinterpret_cast<uint16_t* const*>(dbase + offsetof(adp_model::BatchHost, kcb));
+  p.vcb = reinterpret_cast<uint16_t* const*>(dbase + offsetof(adp_model::BatchHost, vcb));
+  p.force_sel = nullptr;
+  p.trace = nullptr;
+  CK(cudaStreamSynchronize(m->stream));
+  return B.init_rc = ADP_OK;
+}
+
+// Checks shared by the batched entry points; on success the batch is set up.
+static int batch_check(adp_model* m, adp_kv* const* kvs, int32_t nb, const int32_t* tokens, int32_t n_steps) {
+  if (!m || !kvs || !tokens || nb < 1 || n_steps < 0) return ADP_ERR_INVALID_ARG;
+  if (m->sticky) return m->sticky;
+  for (int r = 0; r < nb; ++r) {
+    if (!kvs[r] || kvs[r]->m != m) return ADP_ERR_INVALID_ARG;
+    for (int s = 0; s < r; ++s)
+      if (kvs[s] == kvs[r]) return ADP_ERR_INVALID_ARG;  // one cache cannot take two tokens per step
+    if (tokens[r] < 0 || tokens[r] >= m->cfg.vocab) return ADP_ERR_INVALID_ARG;
+  }
+  const int rc = batch_init(m);
+  if (rc) return rc;
+  if (nb > m->bt.max_nb) return ADP_ERR_UNSUPPORTED_CONFIG;
+  for (int r = 0; r < nb; ++r)
+    if (kvs[r]->len + std::max(n_steps, 1) > m->cfg.max_ctx) return ADP_ERR_CONTEXT_OVERFLOW;
+  return ADP_OK;
+}
+
+// Stage the step state and KV cache tables of the batch and enqueue n steps in one launch.
+static int batch_enqueue(adp_model* m, adp_kv* const* kvs, int32_t nb, const int32_t* tokens, const float* temps,
+                         const float* us, int32_t n, const float* dev_u, int32_t* dev_out, float* dev_logits) {
+  adp_model::Batch& B = m->bt;
+  CK(cudaEventSynchronize(B.copied));
+  bool sampling = false;
+  for (int r = 0; r < nb; ++r) {
+    StepState& st = B.h->st[r];
+    st.pos = kvs[r]->len;
+    st.token = tokens[r];
+    st.temperature = temps ? temps[r] : 0.0f;
+    st.u = us ? us[r] : 0.0f;
+    st.seq_index = 0;
+    st.out_token = -1;
+    B.h->kcb[r] = kvs[r]->k;
+    B.h->vcb[r] = kvs[r]->v;
+    sampling = sampling || st.temperature > 0.0f;
+  }
+  CK(cudaMemcpyAsync(B.d, B.h, sizeof(adp_model::BatchHost), cudaMemcpyHostToDevice, m->stream));
+  CK(cudaEventRecord(B.copied, m->stream));
+  const int rs = reserve_epochs(m, n);
+  if (rs) return rs;
+  Params q = B.p;
+  q.nb = nb;
+  q.n_steps = n;
+  q.nslots = B.nslots[nb];
+  q.att_slots = B.att_slots[nb];
+  q.xbuf_floats = B.xbuf_floats[nb];
+  q.logits = dev_logits ? dev_logits : B.d_logits;
+  q.tok_seq = nullptr;
+  q.u_seq = dev_u;
+  q.out_seq = dev_out;
+  q.timeline = m->p.timeline;
+  q.wait_ns = m->p.wait_ns;
+  q.debug_barriers = m->p.debug_barriers;
+  q.skip_cta = q.skip_phase = -1;
+  const int nph = (int)m->phases.size();
+  CK(decode_batch_launch(q, 0, sampling ? nph : nph - 1, m->G, B.smem[nb], B.xbuf_floats[nb], m->stream));
+  return ADP_OK;
+}
+
+extern "C" int adp_max_batch(adp_model* m, int32_t* nb) {
+  if (!m || !nb) return ADP_ERR_INVALID_ARG;
+  const int rc = batch_init(m);
+  *nb = rc == ADP_OK ? m->bt.max_nb : 0;
+  return rc == ADP_ERR_UNSUPPORTED_CONFIG ? ADP_OK : rc;
+}
+
+extern "C" int adp_decode_batch(adp_model* m, adp_kv* const* kvs, int32_t nb, const int32_t* tokens,
+                                const adp_sampling* sampling, int32_t* next_tokens, float* dev_logits) {
+  if (!next_tokens) return ADP_ERR_INVALID_ARG;
+  int rc = batch_check(m, kvs, nb, tokens, 1);
+  if (rc) return rc;
+  float temps[kMaxBatch], us[kMaxBatch];
+  for (int r = 0; r < nb; ++r) {
+    temps[r] = sampling ? sampling[r].temperature : 0.0f;
+    us[r] = sampling ? sampling[r].u : 0.0f;
+  }
+  rc = batch_enqueue(m, kvs, nb, tokens, temps, us, 1, nullptr, nullptr, dev_logits);
+  if (rc) return rc;
+  adp_model::Batch& B = m->bt;
+  for (int r = 0; r < nb; ++r)
+    CK(cudaMemcpyAsync(&B.h_out[r], &B.p.state[r].out_token, 4, cudaMemcpyDeviceToHost, m->stream));
+  CK(cudaMemcpyAsync(&B.h_out[kMaxBatch], m->p.err, 4, cudaMemcpyDeviceToHost, m->stream));
+  CK(cudaStreamSynchronize(m->stream));
+  rc = map_device_error(B.h_out[kMaxBatch]);
+  if (rc) {
+    m->sticky = rc;
+    return rc;
+  }
+  for (int r = 0; r < nb; ++r) {
+    next_tokens[r] = B.h_out[r];
+    kvs[r]->len += 1;
+  }
+  return ADP_OK;
+}
+
+extern "C" int adp_generate_batch_async(adp_model* m, adp_kv* const* kvs, int32_t nb, const int32_t* tokens,
+                                        int32_t n, const float* temperatures, const float* dev_u,
+                                        int32_t* dev_tokens_out) {
+  if (!dev_tokens_out) return ADP_ERR_INVALID_ARG;
+  int rc = batch_check(m, kvs, nb, tokens, n);
+  if (rc) return rc;
+  bool sampling = false;
+  for (int r = 0; r < nb && temperatures; ++r) sampling = sampling || temperatures[r] > 0.0f;
+  if (sampling && !dev_u) return ADP_ERR_INVALID_ARG;
+  for (int r = 0; r < nb; ++r)
+    if (kvs[r]->len + n > m->cfg.max_ctx) return ADP_ERR_CONTEXT_OVERFLOW;
+  if (n == 0) return ADP_OK;
+  rc = batch_enqueue(m, kvs, nb, tokens, temperatures, nullptr, n, sampling ? dev_u : nullptr, dev_tokens_out,
+                     nullptr);
+  if (rc) return rc;
+  for (int r = 0; r < nb; ++r) kvs[r]->len += n;
+  return ADP_OK;
+}
+
 extern "C" int adp_sync(adp_model* m) {
   if (!m) return ADP_ERR_INVALID_ARG;
   if (m->sticky) return m->sticky;
@@ -764,6 +1006,10 @@ extern "C" int adp_reset(adp_model* m) {
   CK(cudaMemsetAsync(p.lm_ctr, 0, 4, m->stream));
   CK(cudaMemsetAsync(p.bar_ctr, 0, 8, m->stream));
   CK(cudaMemsetAsync(p.err, 0, 4, m->stream));
+  if (m->bt.init_rc == ADP_OK) {
+    CK(cudaMemsetAsync(m->bt.p.sample_ctr, 0, 4 * kMaxBatch, m->stream));
+    CK(cudaMemsetAsync(m->bt.p.argkey, 0, 8 * kMaxBatch, m->stream));
+  }
   int rc = clear_exchange(m);
   if (rc) return rc;
   CK(cudaStreamSynchronize(m->stream));

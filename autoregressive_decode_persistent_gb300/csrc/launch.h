@@ -22,5 +22,11 @@ cudaError_t decode_launch(const Params& p, int ph0, int ph1, bool persistent, in
 cudaError_t repack_launch(uint8_t* image, const PhaseDesc& P, const RepackSrc& S, int grid, int experts,
                           cudaStream_t stream);
 size_t ctl_bytes(int n_phases);  // control block + phase table in shared memory
+// The batched kernel (KK_BATCH): always one persistent cooperative launch.  Its shared memory
+// adds batch_ctl_bytes() after ctl_bytes(n_phases).
+cudaError_t decode_batch_prepare(size_t smem_bytes, int* blocks_per_sm);
+cudaError_t decode_batch_launch(const Params& p, int ph0, int ph1, int grid, size_t smem_bytes, int xbuf_floats,
+                                cudaStream_t stream);
+size_t batch_ctl_bytes();
 
 }  // namespace adp

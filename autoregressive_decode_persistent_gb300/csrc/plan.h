@@ -21,8 +21,9 @@ constexpr int kVocabBlock = 256;                    // vocabulary entries per sa
 constexpr int kMaxTopK = 8;
 constexpr int kAttnSlots = 8;                       // attention items in flight per CTA (max)
 constexpr int kMaxGroup = 8;                        // query heads per KV head (max)
-constexpr int kChunkAlign = 256;
-constexpr int kStamps = 16;                         // timeline stamps per (CTA, phase)                    // K-chunks start at multiples of 32 lanes x 8 elements
+constexpr int kChunkAlign = 256;                    // K-chunks start at multiples of 32 lanes x 8 elements
+constexpr int kStamps = 16;                         // timeline stamps per (CTA, phase)
+constexpr int kMaxBatch = 4;                        // requests of one batched decode step (max)
 
 enum PhaseKind : int32_t {
   PK_QKV = 0,    // rmsnorm prologue; RoPE pairs of q/k, v; epilogue writes q and the KV rows
@@ -39,8 +40,9 @@ enum PhaseKind : int32_t {
 
 enum DType : int32_t { DT_F16 = 0, DT_BF16 = 1, DT_E4M3 = 2, DT_F32 = 3 };
 
-// Kernel instantiations: dense 16-bit weights, top-k experts, dense e4m3 layer matrices.
-enum KernelKind : int32_t { KK_DENSE = 0, KK_MOE = 1, KK_DENSE8 = 2 };
+// Kernel instantiations: dense 16-bit weights, top-k experts, dense e4m3 layer matrices, and the
+// batched kernel (dense 16-bit weights, up to kMaxBatch requests per step).
+enum KernelKind : int32_t { KK_DENSE = 0, KK_MOE = 1, KK_DENSE8 = 2, KK_BATCH = 3 };
 
 struct PhaseDesc {
   int32_t kind, layer;
@@ -139,6 +141,13 @@ struct Params {
   int32_t n_steps;             // decode steps this launch runs back to back (persistent launch)
   int32_t nslots;              // weight ring depth (slots of kSlotBytes)
   int32_t skip_cta, skip_phase;  // test hook: that CTA does not publish that phase's outputs
+  // Batched kernel only: nb requests per step.  Every per-request buffer above (x, q, knew, vnew,
+  // attn, h, part_*, logits, argkey, sblock, sample_ctr, tok_word, state) then holds nb copies of
+  // its single-request layout back to back, and the token / uniform / output sequences are
+  // [step][nb].
+  int32_t nb;
+  uint16_t* const* kcb;        // [nb] each request's K cache [L][hkv][max_ctx][hd]
+  uint16_t* const* vcb;        // [nb] each request's V cache
 };
 
 // Device error codes (the host maps them to ADP_ERR_*).

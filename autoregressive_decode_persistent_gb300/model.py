@@ -107,6 +107,18 @@ class DecodeModel:
     def launches_per_step(self) -> int:
         return adp.adp_launches_per_step(self.handle)
 
+    # -- small batches: independent requests (one KVCache each) stepped together
+    @property
+    def max_batch(self) -> int:
+        return adp.adp_max_batch(self.handle)
+
+    def step_batch(self, kvs, tokens, temperatures=None, us=None, logits: torch.Tensor | None = None) -> list[int]:
+        return adp.adp_decode_batch(self.handle, [k.handle for k in kvs], tokens, temperatures, us, logits)
+
+    def generate_batch_async(self, kvs, tokens, n: int, out: torch.Tensor, temperatures=None,
+                             uniforms: torch.Tensor | None = None):
+        adp.adp_generate_batch_async(self.handle, [k.handle for k in kvs], tokens, n, temperatures, uniforms, out)
+
 
 class KVCache:
     def __init__(self, model: DecodeModel):

@@ -126,7 +126,9 @@ void adp_destroy_model(adp_model* m);
 /* KV cache of one sequence ([H] §"GPU推論の速度制限要因：メモリ帯域幅": the KV cache is the
  * other stream each token reads; [A] §"どう出したか": kept uncompressed).  Engine-owned device
  * memory, layout [n_layers][n_kv_heads][max_ctx][head_dim] of cfg.kv_dtype for K and for V;
- * K rows hold post-RoPE keys.  A cache belongs to the model it was created from. */
+ * K rows hold post-RoPE keys.  A cache belongs to the model it was created from.  The model may
+ * be destroyed before its caches: they then accept only adp_kv_destroy (every other call on them
+ * returns ADP_ERR_INVALID_ARG). */
 int adp_kv_create(adp_model* m, adp_kv** out);
 void adp_kv_destroy(adp_kv* kv);
 int adp_kv_reset(adp_kv* kv);                        /* length := 0 */
@@ -197,6 +199,35 @@ int adp_prefill(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t n,
 int adp_generate_async(adp_model* m, adp_kv* kv, int32_t token, int32_t n, float temperature, const float* dev_u,
                        int32_t* dev_tokens_out);
 int adp_sync(adp_model* m);                          /* synchronise the stream; report sticky errors */
+
+/* Small-batch decode: nb independent requests of one model advance one token each in ONE
+ * persistent launch that streams the weights once for all of them.  The pages' authors plan
+ * small batches and warn that they trade against per-request speed ("Real-time LLM inference on
+ * standard GPUs" discussion thread, their reply on batching); the pages fix no batched
+ * algorithm.  Per request the arithmetic is adp_decode_step's contract unchanged, so request
+ * r's next token, logits and KV row are bit-identical to decoding it alone.
+ *  kvs:        HOST array [nb] of distinct caches of this model, each at its own length (the
+ *              request's position); each gains one row.
+ *  tokens:     HOST array [nb], each in [0, vocab).
+ *  sampling:   HOST array [nb] (temperature and uniform per request), or NULL for greedy.
+ *  next_tokens: HOST array [nb] that receives the chosen tokens.
+ *  dev_logits: optional DEVICE float array [nb][vocab].
+ * nb must be in [1, adp_max_batch]: the batched kernel keeps nb copies of the widest GEMV input
+ * vector (fp32) in shared memory beside a weight ring of at least two slots, and merges head h of
+ * request r on CTA G-1-(r*n_heads+h).  Dense fp16 / bf16 models only (experts differ per request;
+ * e4m3 layer matrices are not batched): others get ADP_ERR_UNSUPPORTED_CONFIG.  Synchronises;
+ * errors as adp_decode_step (a device error is sticky and no cache grows). */
+int adp_decode_batch(adp_model* m, adp_kv* const* kvs, int32_t nb, const int32_t* tokens,
+                     const adp_sampling* sampling, int32_t* next_tokens, float* dev_logits);
+/* n batched steps in one launch, each request feeding itself the token it chose.
+ * temperatures: HOST array [nb] or NULL (greedy); dev_u: DEVICE array [n][nb] of uniforms,
+ * required when some temperature is > 0; dev_tokens_out: DEVICE array [n][nb].  Returns after
+ * enqueueing; adp_sync reports device errors. */
+int adp_generate_batch_async(adp_model* m, adp_kv* const* kvs, int32_t nb, const int32_t* tokens, int32_t n,
+                             const float* temperatures, const float* dev_u, int32_t* dev_tokens_out);
+/* Largest nb this model can batch (0 when the model cannot batch at all).  The first call sets
+ * up the batch buffers (device memory for 4 requests' exchange words and logits). */
+int adp_max_batch(adp_model* m, int32_t* nb);
 
 int adp_reset(adp_model* m);                         /* clear a sticky device error and sync counters */
 const char* adp_status_string(int status);

@@ -221,6 +221,17 @@ def sampling_uniforms(n: int, first: int = 0, seed: int = SEED_SAMPLING) -> np.n
     return uniforms(seed, first, n)
 
 
+def batch_prompts(cfg: dict, lengths) -> list[np.ndarray]:
+    """Prompts of independent requests decoded as one batch: request r draws its tokens from the
+    prompt stream of seed SEED_PROMPT + config index + 100 * r (request 0 has the usual prompt)."""
+    return [prompt(cfg, int(n), seed=SEED_PROMPT + cfg["index"] + 100 * r) for r, n in enumerate(lengths)]
+
+
+def batch_uniforms(n: int, r: int) -> np.ndarray:
+    """Sampling uniforms of request r of a batch: the sampling stream of seed SEED_SAMPLING + r."""
+    return uniforms(SEED_SAMPLING + r, 0, n)
+
+
 def kv_prefix(cfg: dict, length: int, seed: int | None = None):
     """Synthetic KV-cache contents for positions [0, length): N(0, 1) in the KV storage dtype,
     shaped [L, hkv, length, hd] (raw bits). N(0,1) matches the scale of K/V rows that a

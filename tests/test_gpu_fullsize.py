@@ -83,3 +83,43 @@ def test_full_size_prefill_path(built):
         assert np.array_equal(lg.cpu().numpy().view(np.uint32), ref["logits"].view(np.uint32))
     k, v = kv.read()
     assert np.array_equal(k, om.kc[:, :, :18]) and np.array_equal(v, om.vc[:, :, :18])
+
+
+def test_full_size_batch(built):
+    """The 2.3B fp16 workload decoded as a batch of as many requests as the model can batch,
+    each with its own KV prefix (lengths 512, 700, 1000), teacher-forced for 3 steps: per request
+    bit-exact against the oracle's contract mode and within tolerance of its plain mode."""
+    import torch
+    from autoregressive_decode_persistent_gb300.model import DecodeModel
+    cfg = synth.get_config("dense-2.3b-fp16")
+    W = synth.model_weights(cfg)
+    model = DecodeModel(cfg, W)
+    nb = model.max_batch
+    assert nb >= 2
+    prefixes = [512, 700, 1000, 300][:nb]
+    steps = 3
+    firsts = synth.batch_prompts(cfg, [1] * nb)
+    runs, kvps, kvs = [], [], []
+    for r in range(nb):
+        kvp = synth.kv_prefix(cfg, prefixes[r], seed=synth.SEED_KV + 50 + r)
+        kvps.append(kvp)
+        runs.append(oracle_free_run(cfg, W, firsts[r], steps - 1, EXACT, 0.0, None, kvp))
+        kv = model.new_kv()
+        kv.load(*kvp)
+        kvs.append(kv)
+    lg = torch.empty((nb, cfg["vocab"]), device=model.device)
+    got = []
+    for i in range(steps):
+        nxt = model.step_batch(kvs, [runs[r][0][i] for r in range(nb)], logits=lg)
+        got.append(lg.cpu().numpy().copy())
+        for r in range(nb):
+            assert nxt[r] == runs[r][2][i], (r, i)
+            assert np.array_equal(got[i][r].view(np.uint32), runs[r][1][i].view(np.uint32)), (r, i)
+    for r in range(nb):
+        k, v = kvs[r].read()
+        om, P = runs[r][4], prefixes[r]
+        assert np.array_equal(k[:, :, P:P + steps], om.kc[:, :, P:P + steps])
+        assert np.array_equal(v[:, :, P:P + steps], om.vc[:, :, P:P + steps])
+        ref_p, _, _ = oracle_forced(cfg, W, runs[r][0], PLAIN, 0.0, None, kvps[r])
+        assert_logits_within_tolerance(np.stack([g[r] for g in got]), ref_p)
+    model.close()

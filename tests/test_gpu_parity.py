@@ -269,3 +269,19 @@ def test_epoch_counter_restarts_before_it_would_wrap(torch_cuda):
         assert oa.cpu().tolist() == ob.cpu().tolist()
     a.close()
     b.close()
+
+
+def test_model_destroyed_before_its_caches(torch_cuda):
+    """A model may go before its caches: they are orphaned, accept only adp_kv_destroy, and
+    reject every other call."""
+    from autoregressive_decode_persistent_gb300 import adp
+    cfg = synth.get_config("tiny")
+    model = _model(cfg, synth.model_weights(cfg))
+    kv = model.new_kv()
+    kv.step(3)
+    h = kv.handle
+    model.close()
+    with pytest.raises(adp.AdpError) as e:
+        adp.adp_kv_reset(h)
+    assert e.value.code == adp.ADP_ERR_INVALID_ARG
+    kv.close()
