@@ -88,6 +88,19 @@ def mean_bytes_per_token(cfg: dict, first_context: int, n_steps: int) -> float:
     return w + per_pos * mean_ctx
 
 
+def batch_step_bytes(cfg: dict, contexts) -> int:
+    """Algorithmic HBM bytes of one batched decode step: every weight once for the whole batch,
+    plus each request's KV cache up to its own context and its new KV row."""
+    return weight_bytes_per_token(cfg) + sum(kv_read_bytes(cfg, c) + kv_write_bytes(cfg) for c in contexts)
+
+
+def mean_batch_step_bytes(cfg: dict, nb: int, first_context: int, n_steps: int) -> float:
+    """Average batched-step bytes over steps in which all nb requests sit at contexts
+    first_context, first_context + 1, ..."""
+    mean_ctx = first_context + (n_steps - 1) / 2.0
+    return weight_bytes_per_token(cfg) + nb * (kv_write_bytes(cfg) + kv_read_bytes(cfg, 1) * mean_ctx)
+
+
 def roofline_tokens_per_s(cfg: dict, context: float, bandwidth_bytes_per_s: float) -> float:
     w = weight_bytes_per_token(cfg) + kv_write_bytes(cfg)
     return bandwidth_bytes_per_s / (w + kv_read_bytes(cfg, 1) * context)

@@ -6,6 +6,8 @@ prefilled, then greedy decode steps run at contexts 513..1024 (a run longer than
 rewinds the cache to 512 and decodes the window again). One step = one decode step of the
 whole model; the steps of a window run inside one persistent kernel launch.
 --workload dense-2.3b-e4m3 measures the same model with e4m3 layer matrices instead.
+--batch N (N >= 2) measures N independent requests decoded together by the batched kernel
+(value = tokens/s of all requests; the default, batch 1, is the benchmark's headline).
 
 Printed (one JSON line, rank 0):
   value      tokens/s, device-timed: the steps chained on the GPU (adp_generate_async), weights
@@ -62,23 +64,24 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-KERNEL_SOURCES = ("decode.cu", "device.cuh", "plan.h")  # the decode kernel's device code
+KERNEL_SOURCES = ("decode.cu", "decode_core.cuh", "device.cuh", "plan.h")  # the decode kernel's device code
+BATCH_KERNEL_SOURCES = ("decode_batch.cu", "decode_core.cuh", "device.cuh", "plan.h")  # the batched kernel's
 
 
-def kernel_source_hash() -> str:
-    """sha256[:16] over the decode kernel's sources (host-only files do not change its traffic)."""
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
+    """sha256[:16] over a kernel's sources (host-only files do not change its traffic)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "autoregressive_decode_persistent_gb300", "csrc")
-    for f in KERNEL_SOURCES:
+    for f in sources:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(src_hash: str):
+def profiled_traffic(src_hash: str, name: str | None = None):
     """DRAM bytes per decode step from the committed ncu summary, if it was taken on this kernel
     source (a launch of n chained steps moves n times as much)."""
-    path = os.path.join(ROOT, "profiles", f"decode_kernel_{WORKLOAD}.md")
+    path = os.path.join(ROOT, "profiles", name or f"decode_kernel_{WORKLOAD}.md")
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:
@@ -324,6 +327,150 @@ def run_engine(args, rank: int, world: int):
     return cfg, res
 
 
+def run_engine_batch(args, rank: int, world: int):
+    """The same workload as nb independent requests decoded together by the batched kernel: each
+    request has its own 512-token prompt (prefilled alone) and cache; the timed region runs
+    windows of chained batched steps (adp_generate_batch_async), every request at contexts
+    513..1024."""
+    import torch
+
+    import synth
+    from autoregressive_decode_persistent_gb300 import adp, bound, build
+    from autoregressive_decode_persistent_gb300.model import DecodeModel
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(dev)
+    build.build()
+    cfg = synth.get_config(WORKLOAD)
+    if args.layers:
+        cfg["n_layers"] = args.layers
+    nb = args.batch
+    W = synth.model_weights(cfg)
+    model = DecodeModel(cfg, W, device=dev)
+    if nb > model.max_batch:
+        raise SystemExit(f"--batch {nb}: this model batches at most {model.max_batch} requests")
+    stream = torch.cuda.current_stream(dev)
+    P = cfg["prompt_len"]
+    kvs = [model.new_kv() for _ in range(nb)]
+    tok0 = [kvs[r].prefill(p) for r, p in enumerate(synth.batch_prompts(cfg, [P] * nb))]
+    out = torch.empty((WINDOW, nb), dtype=torch.int32, device=dev)
+
+    def passes(n_steps):
+        left = n_steps
+        while left > 0:
+            k = min(left, WINDOW)
+            for kv in kvs:
+                kv.truncate(P)
+            model.generate_batch_async(kvs, tok0, k, out)
+            left -= k
+
+    passes(args.warmup)
+    adp.adp_sync(model.handle)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        e0.record(stream)
+        passes(args.steps)
+        e1.record(stream)
+        e1.synchronize()
+    adp.adp_sync(model.handle)
+    ms = e0.elapsed_time(e1)
+    total_bytes = 0
+    left = args.steps
+    while left > 0:
+        k = min(left, WINDOW)
+        total_bytes += bound.mean_batch_step_bytes(cfg, nb, P + 1, k) * k
+        left -= k
+    n_launch = -(-args.steps // WINDOW)
+    per_launch = total_bytes / n_launch
+    launch_ms = ms / n_launch
+    peak, peak_kind = _peaks()
+    achieved = per_launch / (launch_ms * 1e-3) / 1e9
+    # e2e: adp_decode_batch per step, the nb tokens in and out of host memory every step
+    n_e2e = min(args.steps, 2 * WINDOW)
+    for kv in kvs:
+        kv.truncate(P)
+    t = list(tok0)
+    torch.cuda.synchronize(dev)
+    per_step = []
+    h0 = time.perf_counter()
+    for i in range(n_e2e):
+        if i and i % WINDOW == 0:
+            for kv in kvs:
+                kv.truncate(P)
+        s0 = time.perf_counter()
+        t = model.step_batch(kvs, t)
+        per_step.append(time.perf_counter() - s0)
+    h1 = time.perf_counter()
+    per_step.sort()
+    step_pct = {"p50_us": round(per_step[len(per_step) // 2] * 1e6, 1),
+                "p99_us": round(per_step[min(len(per_step) - 1, int(len(per_step) * 0.99))] * 1e6, 1)}
+    ms, e2e_s = max_over_ranks([ms, h1 - h0], world)
+    res = {
+        "ms": ms, "steps": args.steps, "nb": nb, "n_launch": n_launch, "step_pct": step_pct,
+        "weight_bytes": bound.weight_bytes_per_token(cfg), "achieved_gbs": achieved, "per_launch_bytes": per_launch,
+        "launch_ms": launch_ms, "peak": peak, "peak_kind": peak_kind,
+        "e2e": whole_job_rate(n_e2e * nb, e2e_s, world), "n_e2e": n_e2e, "clocks": clocks.summary(),
+        "ctas": model.num_ctas, "launches": n_launch,
+    }
+    for kv in kvs:
+        kv.close()
+    model.close()
+    return cfg, res
+
+
+def emit_batch(args, cfg, res, world):
+    nb = res["nb"]
+    value = whole_job_rate(res["steps"] * nb, res["ms"] * 1e-3, world)
+    src = kernel_source_hash(BATCH_KERNEL_SOURCES)
+    prof = f"decode_batch_kernel_{WORKLOAD}-b{nb}.md"
+    tr = profiled_traffic(src, prof)
+    line = {
+        "metric": f"batch-{nb} decode tokens/s, all requests (2.3B fp16); achieved HBM GB/s vs GB300 peak",
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": res["steps"],
+        "warmup": args.warmup,
+        "ms_per_step": round(res["ms"] / res["steps"], 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": WORKLOADS[WORKLOAD]["data"] + f"; {nb} requests with their own prompts",
+        "config": {
+            "workload": f"{WORKLOAD} as {nb} independent requests decoded together: each prompt 512, greedy "
+                        "decode at contexts 513..1024",
+            "weights": WORKLOADS[WORKLOAD]["weights"], "kv_cache": "f16", "batch": nb, "prompt": cfg["prompt_len"],
+            "per_request_tokens_per_s": round(value / nb, 2),
+            "kernel": "batched persistent kernel: one cooperative launch per window of up to 512 chained "
+                      "batched steps (e2e: one launch per step)",
+            "ctas": res["ctas"],
+            "l2": f"inputs larger than L2: every step streams {res['weight_bytes'] / 1e9:.2f} GB of weights",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "e2e": {"value": round(res["e2e"], 2), "unit": "tokens/s", "h2d_bytes_per_step": 192,
+                "d2h_bytes_per_step": 4 * nb + 4, "steps": res["n_e2e"], "per_step": res["step_pct"],
+                "path": "adp_decode_batch per step (host tokens in and out, stream sync)"},
+        "roofline": {"bound": "hbm", "achieved": round(res["achieved_gbs"], 1), "peak": res["peak"],
+                     "unit": "GB/s", "frac": round(res["achieved_gbs"] / res["peak"], 4),
+                     "traffic": None if tr is None else round(tr * res["steps"] / res["n_launch"]),
+                     "kernel": "adp::decode_batch_kernel", "bytes_per_launch": int(res["per_launch_bytes"]),
+                     "launch_ms": round(res["launch_ms"], 5),
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({res['peak_kind']}; read+write copy)"},
+        "gpu_launches": res["launches"],
+        **({"profiling_variant": f"{cfg['n_layers']} layers (not the workload)"} if args.layers else {}),
+        "clocks": res["clocks"],
+        "kernel_source": src,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def write_timeline(path, model, kv, tok0, P, cfg):
     """Per-phase breakdown of one decode step from the kernel's %globaltimer stamps."""
     import numpy as np
@@ -496,6 +643,9 @@ def main():
     ap.add_argument("--ablation-steps", type=int, default=64,
                     help="steps of the one-launch-per-phase ablation (0 = skip)")
     ap.add_argument("--timeline", default=None, help="write a per-phase breakdown of one step (JSON) here")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="decode this many independent requests together (batched kernel; default 1: the "
+                         "single-request benchmark)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: use this many layers of the workload's shape (the line says so)")
     args = ap.parse_args()
@@ -507,8 +657,14 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")
+    if args.batch < 1:
+        ap.error("--batch must be >= 1")
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.batch > 1:
+        cfg, res = run_engine_batch(args, rank, world)
+        if rank == 0:
+            emit_batch(args, cfg, res, world)
     else:
         cfg, res = run_engine(args, rank, world)
         if rank == 0:

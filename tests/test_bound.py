@@ -82,3 +82,16 @@ def test_mean_bytes_per_token_is_average_of_steps():
     c = synth.get_config("tiny")
     steps = [bound.bytes_per_token(c, 17 + i) for i in range(64)]
     assert bound.mean_bytes_per_token(c, 17, 64) == pytest.approx(sum(steps) / len(steps))
+
+
+def test_batched_step_bytes():
+    """A batched step reads the weights once and each request's own KV prefix: with one request it
+    is the single-request step; each extra request adds exactly its KV read and write."""
+    c = synth.get_config("dense-2.3b-fp16")
+    assert bound.batch_step_bytes(c, [700]) == bound.bytes_per_token(c, 700)
+    two = bound.batch_step_bytes(c, [513, 1024])
+    assert two == bound.bytes_per_token(c, 513) + bound.bytes_per_token(c, 1024) - bound.weight_bytes_per_token(c)
+    # KV row of the 2.3B model: 25 layers x 4 KV heads x 128 dims x 2 (K, V) x 2 bytes = 51,200
+    assert bound.batch_step_bytes(c, [10, 10]) - bound.batch_step_bytes(c, [10, 9]) == 51_200
+    steps = [bound.batch_step_bytes(c, [513 + i] * 3) for i in range(512)]
+    assert bound.mean_batch_step_bytes(c, 3, 513, 512) == pytest.approx(sum(steps) / len(steps))
