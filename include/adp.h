@@ -3,7 +3,9 @@
  *
  * The engine runs one autoregressive decode step of a decoder-only transformer
  * (dense SwiGLU or top-k MoE with e4m3 experts) as ONE persistent CUDA kernel per
- * step with grid-wide barriers, instead of a kernel per operation.
+ * step, its phases ordered by epoch-tagged exchange words instead of a kernel per
+ * operation; a second persistent kernel decodes small batches of independent requests
+ * (adp_decode_batch).
  *
  * Pages this interface follows (cited by title and section):
  *  [H] "標準GPUによるリアルタイムLLM推論：リクエストあたり3,000トークン/秒" (hakusoku.com
