@@ -90,6 +90,8 @@ _SIGS = [
     ("adp_generate_batch_async", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                                 ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     ("adp_max_batch", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
+    ("adp_debug_tc_gemm", ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     ("adp_reset", ctypes.c_int, [ctypes.c_void_p]),
     ("adp_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("adp_last_error", ctypes.c_char_p, []),
@@ -268,6 +270,13 @@ def adp_generate_batch_async(model, kvs, tokens, n: int, temperatures=None, dev_
     temps = None if temperatures is None else np.ascontiguousarray(temperatures, dtype=np.float32)
     _check(load_library().adp_generate_batch_async(model, table, nb, _ptr(tok), int(n), _ptr(temps), _ptr(dev_u),
                                                    _ptr(dev_tokens_out)), "adp_generate_batch_async")
+
+
+def adp_debug_tc_gemm(bf16: bool, A, W, C):
+    """C = A W^T on the tensor cores (A [M, K], W [N, K] 16-bit, C [M, N] fp32; device tensors)."""
+    M, K = A.shape
+    N = W.shape[0]
+    _check(load_library().adp_debug_tc_gemm(int(bf16), M, N, K, _ptr(A), _ptr(W), _ptr(C)), "adp_debug_tc_gemm")
 
 
 def adp_max_batch(model) -> int:

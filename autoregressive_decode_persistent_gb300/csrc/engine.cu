@@ -936,6 +936,28 @@ static int batch_enqueue(adp_model* m, adp_kv* const* kvs, int32_t nb, const int
   return ADP_OK;
 }
 
+extern "C" int adp_debug_tc_gemm(int32_t bf16, int32_t M, int32_t N, int32_t K, const void* A, const void* W,
+                                 float* C) {
+  if (M < 1 || N < 1 || K < 1 || !A || !W || !C || (bf16 != 0 && bf16 != 1)) return ADP_ERR_INVALID_ARG;
+  uint8_t *at = nullptr, *wt = nullptr;
+  int32_t* err = nullptr;
+  int32_t herr = 0;
+  cudaError_t e = cudaMalloc(&at, tc_tiled_bytes(M, K, 128));
+  if (e == cudaSuccess) e = cudaMalloc(&wt, tc_tiled_bytes(N, K, 256));
+  if (e == cudaSuccess) e = cudaMalloc(&err, 4);
+  if (e == cudaSuccess) e = cudaMemset(err, 0, 4);
+  if (e == cudaSuccess) e = tc_tile((const uint16_t*)A, M, K, K, at, 128, 0);
+  if (e == cudaSuccess) e = tc_tile((const uint16_t*)W, N, K, K, wt, 256, 0);
+  if (e == cudaSuccess) e = tc_gemm(bf16, false, at, wt, C, N, M, N, K, err, 1000000000ull, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&herr, err, 4, cudaMemcpyDeviceToHost);
+  cudaFree(at);
+  cudaFree(wt);
+  cudaFree(err);
+  if (e != cudaSuccess) return cuda_fail(e, "adp_debug_tc_gemm");
+  return herr ? ADP_ERR_PIPELINE_TIMEOUT : ADP_OK;
+}
+
 extern "C" int adp_max_batch(adp_model* m, int32_t* nb) {
   if (!m || !nb) return ADP_ERR_INVALID_ARG;
   const int rc = batch_init(m);

@@ -29,4 +29,12 @@ cudaError_t decode_batch_launch(const Params& p, int ph0, int ph1, int grid, siz
                                 cudaStream_t stream);
 size_t batch_ctl_bytes();
 
+// Tensor-core GEMM of the prefill path (prefill.cu): C[M, N] (=, or += when add) A W^T with A and
+// W in the tiled tensor-core layout (A: 128-row tiles, W: 256-row tiles, 64 K-elements each).
+cudaError_t tc_gemm(int bf16, bool add, const uint8_t* A_tiled, const uint8_t* W_tiled, float* C, int ldc, int M,
+                    int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st);
+// Row-major 16-bit [rows, K] (row stride ld) -> tiles of tile_rows x 64, zero-padded.
+cudaError_t tc_tile(const uint16_t* src, int rows, int K, int ld, uint8_t* dst, int tile_rows, cudaStream_t st);
+size_t tc_tiled_bytes(int rows, int K, int tile_rows);
+
 }  // namespace adp

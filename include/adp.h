@@ -287,6 +287,10 @@ int adp_debug_set_wait_limit(adp_model* m, uint64_t ns);
  * so that every phase waiting for them runs out of time and the step returns
  * ADP_ERR_BARRIER_TIMEOUT (a dependency wait ran out) instead of hanging. */
 int adp_debug_skip_publication(adp_model* m, int32_t cta, int32_t phase);
+/* The prefill path's tensor-core GEMM alone (test hook): C[M, N] = A[M, K] W[N, K]^T in fp32, with
+ * A and W DEVICE row-major 16-bit matrices (f16, or bf16 when bf16 = 1) and C a DEVICE fp32 [M, N]
+ * array.  Tiles the operands into temporary device buffers, runs, synchronises the device. */
+int adp_debug_tc_gemm(int32_t bf16, int32_t M, int32_t N, int32_t K, const void* A, const void* W, float* C);
 
 #if defined(__GNUC__)
 #pragma GCC visibility pop
