@@ -82,6 +82,8 @@ _SIGS = [
                                                ctypes.c_void_p]),
     ("adp_prefill", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                    ctypes.POINTER(Sampling), ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
+    ("adp_prefill_tc", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                      ctypes.POINTER(Sampling), ctypes.POINTER(ctypes.c_int32), ctypes.c_void_p]),
     ("adp_generate_async", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                           ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p]),
     ("adp_sync", ctypes.c_int, [ctypes.c_void_p]),
@@ -228,6 +230,14 @@ def adp_prefill(model, kv, tokens, temperature: float = 0.0, u: float = 0.0, dev
     nxt = ctypes.c_int32()
     _check(load_library().adp_prefill(model, kv, _ptr(t), len(t), _sampling(temperature, u), ctypes.byref(nxt),
                                       _ptr(dev_logits)), "adp_prefill")
+    return nxt.value
+
+
+def adp_prefill_tc(model, kv, tokens, temperature: float = 0.0, u: float = 0.0, dev_logits=None) -> int:
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    nxt = ctypes.c_int32()
+    _check(load_library().adp_prefill_tc(model, kv, _ptr(t), len(t), _sampling(temperature, u), ctypes.byref(nxt),
+                                         _ptr(dev_logits)), "adp_prefill_tc")
     return nxt.value
 
 

@@ -81,6 +81,18 @@ struct adp_model {
   int sticky = ADP_OK;
   uint64_t epochs_used = 0;  // epochs handed out since the exchange buffers were last cleared
   size_t ll_bytes[11] = {0};  // sizes of the epoch-tagged exchange buffers
+  std::vector<const void*> h_attn_norm, h_ffn_norm;  // per-layer gains (device pointers)
+  // Tensor-core prefill (set up at the first adp_prefill_tc): the layer matrices again, as GEMM
+  // operand tiles, and scratch for up to tc_cap prompt tokens.
+  struct TcState {
+    int init_rc = 1;
+    std::vector<const uint8_t*> wqkv, wo, wgu, wdown;
+    int cap = 0;
+    int32_t* tokens = nullptr;
+    float* x = nullptr;
+    uint8_t* A = nullptr;
+    float* C = nullptr;
+  } tc;
   // Batched decode (set up at the first batched call): per-request buffers for kMaxBatch
   // requests, the per-request step state and KV cache tables, and the shared-memory layout of
   // each batch size.
@@ -382,6 +394,8 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
     const adp_layer_weights& Lw = w->layers[l];
     an[l] = Lw.attn_norm;
     fn[l] = Lw.ffn_norm;
+    m->h_attn_norm.push_back(Lw.attn_norm);
+    m->h_ffn_norm.push_back(Lw.ffn_norm);
     sg[l] = Lw.e_gate_scale;
     su[l] = Lw.e_up_scale;
     sd[l] = Lw.e_down_scale;
@@ -1011,6 +1025,120 @@ extern "C" int adp_generate_batch_async(adp_model* m, adp_kv* const* kvs, int32_
   if (rc) return rc;
   for (int r = 0; r < nb; ++r) kvs[r]->len += n;
   return ADP_OK;
+}
+
+// ---------------------------------------------------------------- tensor-core prefill
+
+// Set up the tensor-core prefill once per model: every layer matrix again as GEMM operand tiles
+// (rebuilt from the decode image), for dense models with 16-bit weights and head_dim 64 or 128.
+static int tc_init(adp_model* m) {
+  adp_model::TcState& T = m->tc;
+  if (T.init_rc != 1) return T.init_rc;
+  const adp_config& c = m->cfg;
+  T.init_rc = ADP_ERR_UNSUPPORTED_CONFIG;
+  if (c.n_experts != 0 || (c.weight_dtype != ADP_F16 && c.weight_dtype != ADP_BF16)) return T.init_rc;
+  if (c.head_dim != 64 && c.head_dim != 128) return T.init_rc;
+  const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim;
+  for (const PhaseDesc& P : m->phases) {
+    int rows = 0;
+    std::vector<const uint8_t*>* dst = nullptr;
+    switch (P.kind) {
+      case PK_QKV: rows = (hq + 2 * hkv) * hd; dst = &T.wqkv; break;
+      case PK_WO: rows = d; dst = &T.wo; break;
+      case PK_GU: rows = 2 * c.d_ff; dst = &T.wgu; break;
+      case PK_DOWN: rows = d; dst = &T.wdown; break;
+      default: continue;
+    }
+    uint8_t* buf = nullptr;
+    const size_t bytes = tc_tiled_bytes(rows, P.K, 256);
+    int rc = m->alloc(&buf, bytes);
+    if (rc) return T.init_rc = rc;
+    CK(cudaMemsetAsync(buf, 0, bytes, m->stream));
+    CK(tc_unpack(m->image, P, m->G, hd, hq, hkv, c.d_ff, buf, m->stream));
+    dst->push_back(buf);
+  }
+  CK(cudaStreamSynchronize(m->stream));
+  return T.init_rc = ADP_OK;
+}
+
+// Scratch of the tensor-core prefill for P tokens (grown on demand; the old buffers are freed).
+static int tc_reserve(adp_model* m, int P) {
+  adp_model::TcState& T = m->tc;
+  if (P <= T.cap) return ADP_OK;
+  CK(cudaStreamSynchronize(m->stream));
+  for (void* q : {(void*)T.tokens, (void*)T.x, (void*)T.A, (void*)T.C}) {
+    if (!q) continue;
+    m->allocs.erase(std::remove(m->allocs.begin(), m->allocs.end(), q), m->allocs.end());
+    cudaFree(q);
+  }
+  T.tokens = nullptr;
+  T.x = nullptr;
+  T.A = nullptr;
+  T.C = nullptr;
+  T.cap = 0;
+  const adp_config& c = m->cfg;
+  const int kmax = std::max({c.d_model, c.n_heads * c.head_dim, c.d_ff});
+  const size_t nmax = (size_t)std::max((c.n_heads + 2 * c.n_kv_heads) * c.head_dim, 2 * c.d_ff);
+  int rc;
+  if ((rc = m->alloc(&T.tokens, (size_t)P)) || (rc = m->alloc(&T.x, (size_t)P * c.d_model)) ||
+      (rc = m->alloc(&T.A, tc_tiled_bytes(P, kmax, 128))) || (rc = m->alloc(&T.C, (size_t)P * nmax)))
+    return rc;
+  // the A tiles' padding (rows beyond P, columns beyond a GEMM's K) must read as zero
+  CK(cudaMemsetAsync(T.A, 0, tc_tiled_bytes(P, kmax, 128), m->stream));
+  T.cap = P;
+  return ADP_OK;
+}
+
+extern "C" int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t n,
+                              const adp_sampling* sampling, int32_t* next_token, float* dev_logits) {
+  if (!m || !kv || !next_token || kv->m != m || n < 1 || !host_tokens) return ADP_ERR_INVALID_ARG;
+  if (m->sticky) return m->sticky;
+  if (kv->len + n > m->cfg.max_ctx) return ADP_ERR_CONTEXT_OVERFLOW;
+  for (int i = 0; i < n; ++i)
+    if (host_tokens[i] < 0 || host_tokens[i] >= m->cfg.vocab) return ADP_ERR_INVALID_ARG;
+  int rc = tc_init(m);
+  if (rc) return rc;
+  const int P = n - 1;  // the last prompt token goes through the decode kernel
+  if (P > 0) {
+    if ((rc = tc_reserve(m, P))) return rc;
+    const adp_config& c = m->cfg;
+    CK(cudaMemcpyAsync(m->tc.tokens, host_tokens, (size_t)P * 4, cudaMemcpyHostToDevice, m->stream));
+    TcPrefill a{};
+    a.P = P;
+    a.pos0 = kv->len;
+    a.n_layers = c.n_layers;
+    a.d = c.d_model;
+    a.hq = c.n_heads;
+    a.hkv = c.n_kv_heads;
+    a.hd = c.head_dim;
+    a.ff = c.d_ff;
+    a.max_ctx = c.max_ctx;
+    a.bf16 = c.weight_dtype == ADP_BF16 ? 1 : 0;
+    a.kvdt = c.kv_dtype;
+    a.eps = c.rms_eps;
+    a.scale = m->p.attn_scale;
+    a.tokens = m->tc.tokens;
+    a.tok_emb = m->p.tok_emb;
+    a.attn_norm = m->h_attn_norm.data();
+    a.ffn_norm = m->h_ffn_norm.data();
+    a.wqkv = m->tc.wqkv.data();
+    a.wo = m->tc.wo.data();
+    a.wgu = m->tc.wgu.data();
+    a.wdown = m->tc.wdown.data();
+    a.kc = kv->k;
+    a.vc = kv->v;
+    a.rope_cos = m->p.rope_cos;
+    a.rope_sin = m->p.rope_sin;
+    a.x = m->tc.x;
+    a.A = m->tc.A;
+    a.C = m->tc.C;
+    a.err = m->p.err;
+    a.wait_ns = std::max<uint64_t>(m->p.wait_ns, 1000000000ull);
+    CK(tc_prefill(a, m->stream));
+    kv->len += P;
+  }
+  // the last token: one decode step (synchronises and reports any device error, the GEMMs' too)
+  return adp_decode_step(m, kv, host_tokens[n - 1], sampling, next_token, dev_logits);
 }
 
 extern "C" int adp_sync(adp_model* m) {

@@ -37,4 +37,33 @@ cudaError_t tc_gemm(int bf16, bool add, const uint8_t* A_tiled, const uint8_t* W
 cudaError_t tc_tile(const uint16_t* src, int rows, int K, int ld, uint8_t* dst, int tile_rows, cudaStream_t st);
 size_t tc_tiled_bytes(int rows, int K, int tile_rows);
 
+// One tensor-core prefill of P prompt tokens at positions pos0 .. pos0 + P - 1 through every
+// layer: K/V rows into the cache; x ends as the residual after the last layer.
+struct TcPrefill {
+  int P, pos0, n_layers, d, hq, hkv, hd, ff, max_ctx, bf16, kvdt;
+  float eps, scale;
+  const int32_t* tokens;        // device [P]
+  const void* tok_emb;          // device [V, d] (16-bit)
+  const void* const* attn_norm;  // host array [L] of device gains
+  const void* const* ffn_norm;
+  const uint8_t* const* wqkv;   // host arrays [L] of device tiled weights (256-row tiles)
+  const uint8_t* const* wo;
+  const uint8_t* const* wgu;
+  const uint8_t* const* wdown;
+  uint16_t* kc;
+  uint16_t* vc;
+  const float* rope_cos;
+  const float* rope_sin;
+  float* x;        // device [P, d]
+  uint8_t* A;      // device A-operand tiles, rows padded to 128, K up to max(d, hq*hd, ff)
+  float* C;        // device [P, max((hq + 2 hkv) hd, 2 ff)]
+  int32_t* err;
+  uint64_t wait_ns;
+};
+cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st);
+// Phase P's tiles of the decode image -> one GEMM weight operand in 256-row tiles (dst cleared
+// beforehand; rows in the order of the caller's matrices).
+cudaError_t tc_unpack(const uint8_t* image, const PhaseDesc& P, int G, int hd, int hq, int hkv, int ff, uint8_t* dst,
+                      cudaStream_t st);
+
 }  // namespace adp

@@ -18,6 +18,7 @@
 
 #include <algorithm>
 
+#include "decode_core.cuh"
 #include "launch.h"
 #include "tc.cuh"
 
@@ -176,6 +177,299 @@ size_t tc_tiled_bytes(int rows, int K, int tile_rows) {
   const size_t rows_pad = (size_t)(rows + tile_rows - 1) / tile_rows * tile_rows;
   const size_t k_tiles = (size_t)(K + kTcBK - 1) / kTcBK;
   return rows_pad * k_tiles * kTcBK * 2;
+}
+
+}  // namespace adp
+
+// ---------------------------------------------------------------- the prefill pipeline
+
+namespace adp {
+
+// Logical row of the prefill GEMM's weight matrix for row j of decode unit u of phase P:
+// QKV -> [q rows; k rows; v rows] (head-major, as the caller's wq/wk/wv), gate|up -> [gate; up],
+// Wo and down -> their own rows.
+__device__ __forceinline__ int tc_logical_row(const PhaseDesc& P, int u, int j, int hd, int hq, int hkv, int ff) {
+  if (P.kind == PK_QKV) {
+    const int half = hd / 2, nq = hq * half, nk = hkv * half;
+    int base = 0, uu = u;
+    if (u >= nq + nk) {
+      base = (hq + hkv) * hd;
+      uu = u - nq - nk;
+    } else if (u >= nq) {
+      base = hq * hd;
+      uu = u - nq;
+    }
+    return base + (uu / half) * hd + uu % half + j * half;
+  }
+  if (P.kind == PK_GU) return u + j * ff;
+  return u * P.unit_rows + j;
+}
+
+// The decode image's tiles of phase P back into one tiled GEMM operand (256-row tiles): the
+// inverse of the repack, walked the same way (CTA c's units, rounds, K-chunks).
+__global__ void tc_unpack_kernel(const uint8_t* __restrict__ image, PhaseDesc P, uint8_t* dst, int k_tiles, int hd,
+                                 int hq, int hkv, int ff) {
+  const uint32_t c = blockIdx.x, G = gridDim.x;
+  const long long a0 = (long long)c * P.n_units / G, a1 = (long long)(c + 1) * P.n_units / G;
+  const int u0 = (int)a0, n = (int)(a1 - a0);
+  if (n <= 0) return;
+  const uint64_t unit_bytes = (uint64_t)P.unit_rows * P.K * 2;
+  const uint8_t* src_cta = image + P.region + (uint64_t)u0 * unit_bytes;
+  const int nv16 = P.K / 8;
+  const long long total = (long long)n * P.unit_rows * nv16;
+  for (long long idx = threadIdx.x; idx < total; idx += blockDim.x) {
+    const int lu = (int)(idx / ((long long)P.unit_rows * nv16));
+    const int rem = (int)(idx % ((long long)P.unit_rows * nv16));
+    const int j = rem / nv16, cv = rem % nv16;
+    const int col = cv * 8;
+    const int ck = col / P.KC;
+    const int kck = min(P.KC, P.K - ck * P.KC);
+    const int r = lu / P.upr, i = lu % P.upr;
+    const int m = min(P.upr, n - r * P.upr);
+    const uint64_t off = (uint64_t)r * P.upr * unit_bytes + (uint64_t)m * P.unit_rows * ck * P.KC * 2 +
+                         ((uint64_t)(i * P.unit_rows + j) * kck + (col - ck * P.KC)) * 2;
+    const int row = tc_logical_row(P, u0 + lu, j, hd, hq, hkv, ff);
+    const size_t tile = (size_t)(row / kTcBN) * k_tiles + col / kTcBK;
+    *reinterpret_cast<uint4*>(dst + tile * kTcBBytes + tc_tile_offset(row % kTcBN, col % kTcBK)) =
+        *reinterpret_cast<const uint4*>(src_cta + off);
+  }
+}
+
+cudaError_t tc_unpack(const uint8_t* image, const PhaseDesc& P, int G, int hd, int hq, int hkv, int ff, uint8_t* dst,
+                      cudaStream_t st) {
+  const int k_tiles = (P.K + kTcBK - 1) / kTcBK;
+  tc_unpack_kernel<<<G, 256, 0, st>>>(image, P, dst, k_tiles, hd, hq, hkv, ff);
+  return cudaGetLastError();
+}
+
+// 16-bit storage of an fp32 activation (RNE) for the GEMM's A operand.
+__device__ __forceinline__ uint16_t tc_store16(float v, int bf16) {
+  if (bf16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return __half_as_ushort(__float2half_rn(v));
+}
+
+__device__ __forceinline__ size_t tc_a_offset(int t, int k, int k_tiles) {
+  return ((size_t)(t / kTcBM) * k_tiles + k / kTcBK) * kTcABytes + tc_tile_offset(t % kTcBM, k % kTcBK);
+}
+
+// x[t] = embedding row of token t (exact widening).
+__global__ void tc_embed_kernel(const int32_t* __restrict__ tok, const uint16_t* __restrict__ emb, int d, int bf16,
+                                float* x) {
+  const int t = blockIdx.x;
+  const uint16_t* row = emb + (size_t)tok[t] * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x)
+    x[(size_t)t * d + i] = bf16 ? bf16_bits_to_f32(row[i]) : __half2float(__ushort_as_half(row[i]));
+}
+
+// A[t] = rmsnorm(x[t]) * gain, rounded to the weights' 16-bit type, in the A-operand tiles (one
+// warp per token; the padding columns up to the tile edge stay zero from the buffer's clear).
+__global__ void tc_rmsnorm_kernel(const float* __restrict__ x, const uint16_t* __restrict__ gain, int P, int d,
+                                  float eps, int bf16, uint8_t* A, int k_tiles) {
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= P) return;
+  const float* xr = x + (size_t)t * d;
+  float ss = 0.0f;
+  for (int i = lane; i < d; i += 32) ss = fmaf(xr[i], xr[i], ss);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+  const float r = 1.0f / sqrtf(ss / (float)d + eps);
+  for (int i = lane; i < d; i += 32) {
+    const float g = bf16 ? bf16_bits_to_f32(gain[i]) : __half2float(__ushort_as_half(gain[i]));
+    *reinterpret_cast<uint16_t*>(A + tc_a_offset(t, i, k_tiles)) = tc_store16(xr[i] * r * g, bf16);
+  }
+}
+
+// RoPE on the q and k columns of C (token t at position pos0 + t), the rotated k and the v
+// columns rounded into the KV cache rows of that position.
+__global__ void tc_rope_kv_kernel(float* C, int ldc, int P, int pos0, int L, int hq, int hkv, int hd, int max_ctx,
+                                  const float* __restrict__ rcos, const float* __restrict__ rsin, int kvdt,
+                                  uint16_t* kc, uint16_t* vc) {
+  const int t = blockIdx.x;
+  const int pos = pos0 + t;
+  const int half = hd / 2;
+  float* row = C + (size_t)t * ldc;
+  const int pairs = (hq + hkv) * half;
+  for (int p = threadIdx.x; p < pairs + hkv * half; p += blockDim.x) {
+    if (p < pairs) {
+      const int head = p / half, i = p % half;
+      float* a = row + head * hd + i;  // q heads, then k heads (columns hq*hd ..)
+      const float cs = rcos[(size_t)pos * half + i], sn = rsin[(size_t)pos * half + i];
+      const float x0 = a[0], x1 = a[half];
+      const float y0 = fmaf(x0, cs, -(x1 * sn)), y1 = fmaf(x1, cs, x0 * sn);
+      if (head < hq) {
+        a[0] = y0;
+        a[half] = y1;
+      } else {
+        const size_t o = (((size_t)L * hkv + (head - hq)) * max_ctx + pos) * hd + i;
+        kc[o] = round_kv(y0, kvdt);
+        kc[o + half] = round_kv(y1, kvdt);
+      }
+    } else {
+      const int q = p - pairs, g = q / half, i = q % half;
+      const float* v = row + (hq + hkv) * hd + g * hd;
+      const size_t o = (((size_t)L * hkv + g) * max_ctx + pos) * hd + i;
+      vc[o] = round_kv(v[i], kvdt);
+      vc[o + half] = round_kv(v[i + half], kvdt);
+    }
+  }
+}
+
+// Causal attention of the prompt's queries (CTA: query head h, 32 consecutive tokens; warp: 4
+// of them) over the cached positions 0..pos of each: 32-key blocks of K and V staged in shared
+// memory, online softmax in fp32, output rounded into the A-operand tiles of the Wo GEMM.
+template <int HD, int KVDT>
+__global__ void __launch_bounds__(256) tc_attention_kernel(const float* __restrict__ C, int ldc, int P, int pos0,
+                                                          int L, int hq, int hkv, int max_ctx, float scale,
+                                                          const uint16_t* __restrict__ kc,
+                                                          const uint16_t* __restrict__ vc, int bf16, uint8_t* A,
+                                                          int k_tiles) {
+  constexpr int KSTR = HD + 8, DPL = HD / 32, QW = 4;
+  __shared__ __align__(16) uint16_t SK[32 * KSTR];
+  __shared__ __align__(16) uint16_t SV[32 * HD];
+  __shared__ __align__(16) float SQ[8][QW][HD];
+  __shared__ float SP[8][32];
+  const int h = blockIdx.x, t0 = blockIdx.y * 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = h * hkv / hq;
+  for (int i = threadIdx.x; i < QW * 8 * HD; i += blockDim.x) {
+    const int w = i / (QW * HD), qi = (i / HD) % QW, dd = i % HD;
+    const int t = t0 + w * QW + qi;
+    SQ[w][qi][dd] = t < P ? C[(size_t)t * ldc + h * HD + dd] : 0.0f;
+  }
+  float m[QW], l[QW], o[QW][DPL];
+#pragma unroll
+  for (int qi = 0; qi < QW; ++qi) {
+    m[qi] = -INFINITY;
+    l[qi] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) o[qi][k] = 0.0f;
+  }
+  const int kmax = pos0 + min(t0 + 31, P - 1);
+  const size_t head0 = ((size_t)L * hkv + g) * max_ctx;
+  for (int kb0 = 0; kb0 <= kmax; kb0 += 32) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 32 * (HD / 8); i += blockDim.x) {
+      const int r = i / (HD / 8), v8 = i % (HD / 8);
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      if (kb0 + r <= kmax) {
+        kv = *reinterpret_cast<const uint4*>(kc + (head0 + kb0 + r) * HD + v8 * 8);
+        vv = *reinterpret_cast<const uint4*>(vc + (head0 + kb0 + r) * HD + v8 * 8);
+      }
+      *reinterpret_cast<uint4*>(SK + r * KSTR + v8 * 8) = kv;
+      *reinterpret_cast<uint4*>(SV + r * HD + v8 * 8) = vv;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int qi = 0; qi < QW; ++qi) {
+      const int t = t0 + warp * QW + qi;
+      if (t >= P) continue;
+      const int pos = pos0 + t;
+      if (kb0 > pos) continue;
+      const int kp = kb0 + lane;
+      float s = -INFINITY;
+      if (kp <= pos) {
+        float acc = 0.0f;
+        const float* q = SQ[warp][qi];
+#pragma unroll 4
+        for (int v = 0; v < HD / 8; ++v) {
+          float k8[8];
+          kv8<KVDT>(*reinterpret_cast<const uint4*>(SK + lane * KSTR + v * 8), k8);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc = fmaf(q[v * 8 + e], k8[e], acc);
+        }
+        s = acc * scale;
+      }
+      float mb = s;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, off));
+      const float mn = fmaxf(m[qi], mb);
+      const float corr = expf(m[qi] - mn);
+      const float pj = kp <= pos ? expf(s - mn) : 0.0f;
+      SP[warp][lane] = pj;
+      float ps = pj;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
+      __syncwarp();
+      l[qi] = l[qi] * corr + ps;
+#pragma unroll
+      for (int k = 0; k < DPL; ++k) o[qi][k] *= corr;
+      const int nj = min(32, pos - kb0 + 1);
+      for (int j = 0; j < nj; ++j) {
+        const float pw = SP[warp][j];
+        float vf[DPL];
+        kv_dims_smem<KVDT, DPL>(SV + j * HD + lane * DPL, vf);
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) o[qi][k] = fmaf(pw, vf[k], o[qi][k]);
+      }
+      m[qi] = mn;
+      __syncwarp();
+    }
+  }
+#pragma unroll
+  for (int qi = 0; qi < QW; ++qi) {
+    const int t = t0 + warp * QW + qi;
+    if (t >= P) continue;
+    const float inv = 1.0f / l[qi];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) {
+      const int col = h * HD + lane * DPL + k;
+      *reinterpret_cast<uint16_t*>(A + tc_a_offset(t, col, k_tiles)) = tc_store16(o[qi][k] * inv, bf16);
+    }
+  }
+}
+
+// h = silu(g) * u from the gate|up GEMM's output, rounded into the A-operand tiles of down.
+__global__ void tc_swiglu_kernel(const float* __restrict__ C, int ldc, int P, int ff, int bf16, uint8_t* A,
+                                 int k_tiles) {
+  const int t = blockIdx.x;
+  if (t >= P) return;
+  const float* row = C + (size_t)t * ldc;
+  for (int i = threadIdx.x; i < ff; i += blockDim.x) {
+    const float g = row[i], u = row[ff + i];
+    *reinterpret_cast<uint16_t*>(A + tc_a_offset(t, i, k_tiles)) = tc_store16(g / (1.0f + expf(-g)) * u, bf16);
+  }
+}
+
+cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st) {
+  const int P = a.P;
+  const int qkv_n = (a.hq + 2 * a.hkv) * a.hd;
+  const int kt_d = (a.d + kTcBK - 1) / kTcBK, kt_att = (a.hq * a.hd + kTcBK - 1) / kTcBK,
+            kt_ff = (a.ff + kTcBK - 1) / kTcBK;
+  cudaError_t e;
+  tc_embed_kernel<<<P, 256, 0, st>>>(a.tokens, (const uint16_t*)a.tok_emb, a.d, a.bf16, a.x);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  for (int L = 0; L < a.n_layers; ++L) {
+    tc_rmsnorm_kernel<<<(P + 7) / 8, 256, 0, st>>>(a.x, (const uint16_t*)a.attn_norm[L], P, a.d, a.eps, a.bf16, a.A,
+                                                   kt_d);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = tc_gemm(a.bf16, false, a.A, a.wqkv[L], a.C, qkv_n, P, qkv_n, a.d, a.err, a.wait_ns, st)) != cudaSuccess)
+      return e;
+    tc_rope_kv_kernel<<<P, 256, 0, st>>>(a.C, qkv_n, P, a.pos0, L, a.hq, a.hkv, a.hd, a.max_ctx, a.rope_cos,
+                                         a.rope_sin, a.kvdt, a.kc, a.vc);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const dim3 ag(a.hq, (P + 31) / 32);  // head_dim 64 or 128 (checked by the engine)
+    if (a.kvdt == DT_BF16) {
+      if (a.hd == 128) tc_attention_kernel<128, DT_BF16><<<ag, 256, 0, st>>>(a.C, qkv_n, P, a.pos0, L, a.hq, a.hkv, a.max_ctx, a.scale, a.kc, a.vc, a.bf16, a.A, kt_att);
+      else tc_attention_kernel<64, DT_BF16><<<ag, 256, 0, st>>>(a.C, qkv_n, P, a.pos0, L, a.hq, a.hkv, a.max_ctx, a.scale, a.kc, a.vc, a.bf16, a.A, kt_att);
+    } else {
+      if (a.hd == 128) tc_attention_kernel<128, DT_F16><<<ag, 256, 0, st>>>(a.C, qkv_n, P, a.pos0, L, a.hq, a.hkv, a.max_ctx, a.scale, a.kc, a.vc, a.bf16, a.A, kt_att);
+      else tc_attention_kernel<64, DT_F16><<<ag, 256, 0, st>>>(a.C, qkv_n, P, a.pos0, L, a.hq, a.hkv, a.max_ctx, a.scale, a.kc, a.vc, a.bf16, a.A, kt_att);
+    }
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = tc_gemm(a.bf16, true, a.A, a.wo[L], a.x, a.d, P, a.d, a.hq * a.hd, a.err, a.wait_ns, st)) != cudaSuccess)
+      return e;
+    tc_rmsnorm_kernel<<<(P + 7) / 8, 256, 0, st>>>(a.x, (const uint16_t*)a.ffn_norm[L], P, a.d, a.eps, a.bf16, a.A,
+                                                   kt_d);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = tc_gemm(a.bf16, false, a.A, a.wgu[L], a.C, 2 * a.ff, P, 2 * a.ff, a.d, a.err, a.wait_ns, st)) !=
+        cudaSuccess)
+      return e;
+    tc_swiglu_kernel<<<P, 256, 0, st>>>(a.C, 2 * a.ff, P, a.ff, a.bf16, a.A, kt_ff);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = tc_gemm(a.bf16, true, a.A, a.wdown[L], a.x, a.d, P, a.d, a.ff, a.err, a.wait_ns, st)) != cudaSuccess)
+      return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace adp

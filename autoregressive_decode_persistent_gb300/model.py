@@ -163,6 +163,9 @@ class KVCache:
     def prefill(self, tokens, temperature: float = 0.0, u: float = 0.0, logits: torch.Tensor | None = None) -> int:
         return adp.adp_prefill(self.model.handle, self.handle, tokens, temperature, u, logits)
 
+    def prefill_tc(self, tokens, temperature: float = 0.0, u: float = 0.0, logits: torch.Tensor | None = None) -> int:
+        return adp.adp_prefill_tc(self.model.handle, self.handle, tokens, temperature, u, logits)
+
     def generate_async(self, token: int, n: int, out: torch.Tensor, temperature: float = 0.0,
                        uniforms: torch.Tensor | None = None):
         adp.adp_generate_async(self.model.handle, self.handle, token, n, temperature, uniforms, out)

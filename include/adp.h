@@ -202,6 +202,22 @@ int adp_generate_async(adp_model* m, adp_kv* kv, int32_t token, int32_t n, float
                        int32_t* dev_tokens_out);
 int adp_sync(adp_model* m);                          /* synchronise the stream; report sticky errors */
 
+/* Tensor-core prefill: the prompt's first n-1 tokens go through every layer as dense GEMMs on the
+ * tcgen05 tensor cores ([P, d] x [d, n] contractions, fp32 accumulation in TMEM, activations
+ * rounded to the weights' 16-bit type before each GEMM), with RMSNorm, RoPE, causal attention
+ * (fp32, CUDA cores) and SwiGLU between them; their K/V rows go into the cache.  The last token
+ * then runs as one adp_decode_step, whose logits and next token are returned.  The pages time
+ * time-to-first-token ("標準GPUによるリアルタイムLLM推論：リクエストあたり3,000トークン/秒",
+ * §"単一リクエストLLMデコード速度の重要性") but fix no prefill algorithm; this path is not the
+ * decode step's arithmetic contract, so its KV rows and logits agree with the oracle within the
+ * tolerances, not bit for bit (adp_prefill is the bit-exact path).
+ * Arguments, errors and synchronisation as adp_prefill.  Dense models with f16/bf16 weights and
+ * head_dim 64 or 128 only (else ADP_ERR_UNSUPPORTED_CONFIG).  The first call builds a second copy
+ * of the layer matrices in the tensor cores' tile layout (device memory owned by the model, as
+ * large as the layer matrices); scratch grows with the longest prompt seen. */
+int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t n, const adp_sampling* sampling,
+                   int32_t* next_token, float* dev_logits);
+
 /* Small-batch decode: nb independent requests of one model advance one token each in ONE
  * persistent launch that streams the weights once for all of them.  The pages' authors plan
  * small batches and warn that they trade against per-request speed ("Real-time LLM inference on

@@ -31,3 +31,115 @@ def test_tc_gemm_matches_float64(lib, M, N, K, bf16):
     err = (c.cpu().double() - ref).abs()
     assert torch.isfinite(c).all()
     assert (err <= bound).all(), float((err / bound).max())
+
+
+def _kv_within_tolerance(got, ref):
+    """KV rows written by the tensor-core path against the oracle's: per layer, relative L2
+    <= 5e-3 and max-abs <= 2e-2 (the logits' tolerances, applied to the cache)."""
+    for layer in range(ref.shape[0]):
+        g = got[layer].astype(np.float64)
+        r = ref[layer].astype(np.float64)
+        d = g - r
+        assert np.max(np.abs(d)) <= 2e-2, (layer, float(np.max(np.abs(d))))
+        assert np.linalg.norm(d) / max(np.linalg.norm(r), 1e-30) <= 5e-3, layer
+
+
+def _as_float(bits, cfg):
+    import torch
+    t = torch.from_numpy(bits.astype(np.int16).view(np.int16))
+    dt = torch.bfloat16 if cfg["kv_dtype"] == "bf16" else torch.float16
+    return t.view(dt).float().numpy()
+
+
+def _prefill_case(cfg, prompt_len, prefix_len=0, n_decode=3):
+    """adp_prefill_tc of a prompt (after an optional synthetic KV prefix) against the oracle's plain
+    mode: the last prompt token's logits, every new KV row, and a few decode steps after it."""
+    import torch
+    import synth
+    from oracle import PLAIN, OracleModel
+    from gpu_common import assert_logits_within_tolerance
+    from autoregressive_decode_persistent_gb300.model import DecodeModel
+    W = synth.model_weights(cfg)
+    prompt = synth.prompt(cfg, prompt_len)
+    om = OracleModel(cfg, W)
+    kvp = synth.kv_prefix(cfg, prefix_len) if prefix_len else None
+    if kvp is not None:
+        om.load_kv_prefix(*kvp)
+    out = None
+    for t in prompt:
+        out = om.step(int(t), PLAIN)
+    model = DecodeModel(cfg, W)
+    kv = model.new_kv()
+    if kvp is not None:
+        kv.load(*kvp)
+    lg = torch.empty(cfg["vocab"], device=model.device)
+    nxt = kv.prefill_tc(prompt, logits=lg)
+    assert len(kv) == prefix_len + prompt_len
+    assert_logits_within_tolerance(lg.cpu().numpy()[None], out["logits"][None].astype(np.float64))
+    n = prefix_len + prompt_len
+    k, v = kv.read()
+    _kv_within_tolerance(_as_float(k[:, :, prefix_len:n], cfg), _as_float(om.kc[:, :, prefix_len:n], cfg))
+    _kv_within_tolerance(_as_float(v[:, :, prefix_len:n], cfg), _as_float(om.vc[:, :, prefix_len:n], cfg))
+    # decode continues from the tensor-core cache (teacher-forced on the oracle's tokens)
+    t = out["next"]
+    for _ in range(n_decode):
+        ref = om.step(int(t), PLAIN)
+        kv.step(int(t), logits=lg)
+        assert_logits_within_tolerance(lg.cpu().numpy()[None], ref["logits"][None].astype(np.float64))
+        t = ref["next"]
+    model.close()
+    return nxt
+
+
+def test_prefill_tc_tiny(lib):
+    import synth
+    _prefill_case(synth.get_config("tiny"), 40)
+
+
+def test_prefill_tc_ragged_and_after_prefix(lib):
+    """head_dim 128, widths that are not multiples of the GEMM tiles (d 384, ffn 1000), 132
+    tensor-core tokens (two 128-row tiles, the second ragged) after a 21-row cache prefix."""
+    import synth
+    cfg = synth.shrink(synth.get_config("tiny"), head_dim=128, n_heads=4, n_kv_heads=2, d_model=384, d_ff=1000)
+    _prefill_case(cfg, 133, prefix_len=21)
+
+
+def test_prefill_tc_full_size(lib):
+    """The 2.3B fp16 model at full size: a 448-row synthetic cache prefix, then a 64-token prompt
+    through the tensor-core path and three decode steps."""
+    import synth
+    _prefill_case(synth.get_config("dense-2.3b-fp16"), 64, prefix_len=448)
+
+
+@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16"])
+def test_prefill_tc_shrunk_workloads(lib, name):
+    import synth
+    _prefill_case(synth.shrink(synth.get_config(name)), 70)
+
+
+def test_prefill_tc_single_token_is_a_decode_step(lib):
+    import torch
+    import synth
+    from autoregressive_decode_persistent_gb300.model import DecodeModel
+    cfg = synth.get_config("tiny")
+    model = DecodeModel(cfg, synth.model_weights(cfg))
+    a, b = model.new_kv(), model.new_kv()
+    la = torch.empty(cfg["vocab"], device=model.device)
+    lb = torch.empty(cfg["vocab"], device=model.device)
+    assert a.prefill_tc([17], logits=la) == b.step(17, logits=lb)
+    assert torch.equal(la, lb)
+    model.close()
+
+
+def test_prefill_tc_rejects_unsupported_models(lib):
+    import synth
+    from autoregressive_decode_persistent_gb300.model import DecodeModel
+    for name in ("moe-32x1408-top4-e4m3", "dense-2.3b-e4m3"):
+        cfg = synth.shrink(synth.get_config(name))
+        model = DecodeModel(cfg, synth.model_weights(cfg))
+        kv = model.new_kv()
+        with pytest.raises(lib.AdpError) as e:
+            kv.prefill_tc([1, 2, 3])
+        assert e.value.code == lib.ADP_ERR_UNSUPPORTED_CONFIG
+        assert len(kv) == 0
+        model.close()
