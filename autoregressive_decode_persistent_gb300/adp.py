@@ -92,6 +92,8 @@ _SIGS = [
     ("adp_generate_batch_async", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                                 ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     ("adp_max_batch", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
+    ("adp_debug_tc_gemm_time", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.POINTER(ctypes.c_float)]),
     ("adp_debug_tc_gemm", ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     ("adp_reset", ctypes.c_int, [ctypes.c_void_p]),
@@ -287,6 +289,13 @@ def adp_debug_tc_gemm(bf16: bool, A, W, C):
     M, K = A.shape
     N = W.shape[0]
     _check(load_library().adp_debug_tc_gemm(int(bf16), M, N, K, _ptr(A), _ptr(W), _ptr(C)), "adp_debug_tc_gemm")
+
+
+def adp_debug_tc_gemm_time(model, which: int, M: int, reps: int) -> float:
+    ms = ctypes.c_float()
+    _check(load_library().adp_debug_tc_gemm_time(model, int(which), int(M), int(reps), ctypes.byref(ms)),
+           "adp_debug_tc_gemm_time")
+    return ms.value
 
 
 def adp_max_batch(model) -> int:

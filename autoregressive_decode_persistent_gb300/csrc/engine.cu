@@ -1089,6 +1089,41 @@ static int tc_reserve(adp_model* m, int P) {
   return ADP_OK;
 }
 
+extern "C" int adp_debug_tc_gemm_time(adp_model* m, int32_t which, int32_t M, int32_t reps, float* ms_per_launch) {
+  if (!m || !ms_per_launch || which < 0 || which > 3 || M < 1 || reps < 1) return ADP_ERR_INVALID_ARG;
+  int rc = tc_init(m);
+  if (rc) return rc;
+  if ((rc = tc_reserve(m, M))) return rc;
+  const adp_config& c = m->cfg;
+  const int qkv_n = (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  const int N[4] = {qkv_n, c.d_model, 2 * c.d_ff, c.d_model};
+  const int K[4] = {c.d_model, c.n_heads * c.head_dim, c.d_model, c.d_ff};
+  const uint8_t* Wt[4] = {m->tc.wqkv[0], m->tc.wo[0], m->tc.wgu[0], m->tc.wdown[0]};
+  const int kmax = std::max({c.d_model, c.n_heads * c.head_dim, c.d_ff});
+  // operand A: every element 0x3C3C (about 1.06 in f16, 0.0115 in bf16)
+  CK(cudaMemsetAsync(m->tc.A, 0x3C, tc_tiled_bytes(M, kmax, 128), m->stream));
+  const int bf16 = c.weight_dtype == ADP_BF16 ? 1 : 0;
+  cudaEvent_t e0, e1;
+  CK(cudaEventCreate(&e0));
+  CK(cudaEventCreate(&e1));
+  CK(tc_gemm(bf16, false, m->tc.A, Wt[which], m->tc.C, N[which], M, N[which], K[which], m->p.err, 1000000000ull,
+             m->stream));  // warm-up
+  CK(cudaEventRecord(e0, m->stream));
+  for (int i = 0; i < reps; ++i)
+    CK(tc_gemm(bf16, false, m->tc.A, Wt[which], m->tc.C, N[which], M, N[which], K[which], m->p.err, 1000000000ull,
+               m->stream));
+  CK(cudaEventRecord(e1, m->stream));
+  CK(cudaEventSynchronize(e1));
+  float ms = 0.0f;
+  CK(cudaEventElapsedTime(&ms, e0, e1));
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  CK(cudaMemsetAsync(m->tc.A, 0, tc_tiled_bytes(M, kmax, 128), m->stream));  // padding reads as zero again
+  CK(cudaStreamSynchronize(m->stream));
+  *ms_per_launch = ms / (float)reps;
+  return ADP_OK;
+}
+
 extern "C" int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t n,
                               const adp_sampling* sampling, int32_t* next_token, float* dev_logits) {
   if (!m || !kv || !next_token || kv->m != m || n < 1 || !host_tokens) return ADP_ERR_INVALID_ARG;

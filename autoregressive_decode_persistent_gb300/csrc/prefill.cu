@@ -41,7 +41,9 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   int32_t* abort_flag = reinterpret_cast<int32_t*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nb = blockIdx.x, mb = blockIdx.y;
+  // M-blocks vary fastest across the grid, so the CTAs running together share few weight tiles
+  // (each read from DRAM once, then from L2) and every A tile stays in L2
+  const int mb = blockIdx.x, nb = blockIdx.y;
   const uint8_t* Ab = A + (size_t)mb * k_tiles * kTcABytes;
   const uint8_t* Wb = W + (size_t)nb * k_tiles * kTcBBytes;
   if (threadIdx.x == 0) {
@@ -116,9 +118,21 @@ __global__ void __launch_bounds__(128, 1)
       const int col0 = nb * kTcBN + c0;
       if (row < m_valid) {
         float* dst = C + (size_t)row * ldc + col0;
+        if (col0 + 32 <= n_valid && (ldc & 3) == 0) {  // whole 16-byte groups
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (col0 + j < n_valid) dst[j] = ADD ? __fadd_rn(dst[j], v[j]) : v[j];
+          for (int j = 0; j < 32; j += 4) {
+            float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            if (ADD) {
+              const float4 a = *reinterpret_cast<const float4*>(dst + j);
+              o = make_float4(__fadd_rn(a.x, o.x), __fadd_rn(a.y, o.y), __fadd_rn(a.z, o.z), __fadd_rn(a.w, o.w));
+            }
+            *reinterpret_cast<float4*>(dst + j) = o;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (col0 + j < n_valid) dst[j] = ADD ? __fadd_rn(dst[j], v[j]) : v[j];
+        }
       }
     }
   } else if (threadIdx.x == 0) {
@@ -163,7 +177,7 @@ cudaError_t tc_tile(const uint16_t* src, int rows, int K, int ld, uint8_t* dst, 
 cudaError_t tc_gemm(int bf16, bool add, const uint8_t* A_tiled, const uint8_t* W_tiled, float* C, int ldc, int M,
                     int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st) {
   const int k_tiles = (K + kTcBK - 1) / kTcBK;
-  const dim3 grid((N + kTcBN - 1) / kTcBN, (M + kTcBM - 1) / kTcBM);
+  const dim3 grid((M + kTcBM - 1) / kTcBM, (N + kTcBN - 1) / kTcBN);
   const void* k = bf16 ? (add ? (const void*)tc_gemm_kernel<1, true> : (const void*)tc_gemm_kernel<1, false>)
                        : (add ? (const void*)tc_gemm_kernel<0, true> : (const void*)tc_gemm_kernel<0, false>);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);

@@ -8,6 +8,8 @@ whole model; the steps of a window run inside one persistent kernel launch.
 --workload dense-2.3b-e4m3 measures the same model with e4m3 layer matrices instead.
 --batch N (N >= 2) measures N independent requests decoded together by the batched kernel
 (value = tokens/s of all requests; the default, batch 1, is the benchmark's headline).
+--prefill measures time to first token of the 3,584-token prompt through the tensor-core
+prefill (adp_prefill_tc), beside the decode-kernel prefill.
 
 Printed (one JSON line, rank 0):
   value      tokens/s, device-timed: the steps chained on the GPU (adp_generate_async), weights
@@ -471,6 +473,119 @@ def emit_batch(args, cfg, res, world):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill(args, rank: int, world: int):
+    """Time to first token of the long-prompt workload (3,584-token prompt on the 2.3B fp16 model):
+    adp_prefill_tc (prompt contractions on the tensor cores, the last token through the decode
+    kernel) against adp_prefill (every prompt token a decode step, the bit-exact path)."""
+    import torch
+
+    import synth
+    from autoregressive_decode_persistent_gb300 import adp, build
+    from autoregressive_decode_persistent_gb300.model import DecodeModel
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(dev)
+    build.build()
+    cfg = synth.get_config("dense-2.3b-fp16-long-t0.7")
+    if args.layers:
+        cfg["n_layers"] = args.layers
+    W = synth.model_weights(cfg)
+    model = DecodeModel(cfg, W, device=dev)
+    prompt = synth.prompt(cfg)
+    P = len(prompt)
+    kv = model.new_kv()
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):  # the first call also builds the tensor-core weight tiles
+        kv.reset()
+        kv.prefill_tc(prompt)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    times = []
+    with ClockSampler(local) as clocks:
+        for _ in range(args.steps):
+            kv.reset()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            h0 = time.perf_counter()
+            e0.record(stream)
+            kv.prefill_tc(prompt)  # host tokens in, host token out (synchronises)
+            e1.record(stream)
+            e1.synchronize()
+            times.append((e0.elapsed_time(e1), (time.perf_counter() - h0) * 1e3))
+    dev_ms = statistics.median(t[0] for t in times)
+    host_ms = statistics.median(t[1] for t in times)
+    # the bit-exact path: P decode steps in one persistent launch
+    kv.reset()
+    torch.cuda.synchronize(dev)
+    h0 = time.perf_counter()
+    kv.prefill(prompt)
+    step_ms = (time.perf_counter() - h0) * 1e3
+    # the dominant kernel: the gate|up GEMM over the prompt's P - 1 tokens, timed alone
+    M = P - 1
+    N, K = 2 * cfg["d_ff"], cfg["d_model"]
+    g_ms = adp.adp_debug_tc_gemm_time(model.handle, 2, M, 20)
+    dev_ms, host_ms = max_over_ranks([dev_ms, host_ms], world)
+    res = {"dev_ms": dev_ms, "host_ms": host_ms, "step_ms": step_ms, "P": P, "gemm_ms": g_ms,
+           "gemm_flops": 2.0 * M * N * K, "gemm_shape": (M, N, K), "clocks": clocks.summary(),
+           "ctas": model.num_ctas, "n_layers": cfg["n_layers"]}
+    kv.close()
+    model.close()
+    return cfg, res
+
+
+def emit_prefill(args, cfg, res, world):
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, peak_kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        peak, peak_kind = 1900.0, "fallback"
+    achieved = res["gemm_flops"] / (res["gemm_ms"] * 1e-3) / 1e12
+    M, N, K = res["gemm_shape"]
+    L = res["n_layers"]
+    line = {
+        "metric": f"time to first token, {res['P']}-token prompt (2.3B fp16, tensor-core prefill)",
+        "value": round(res["dev_ms"], 3),
+        "unit": "ms",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(res["dev_ms"], 3),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 GEMM operands, f32 accumulation and activations",
+        "data": "synthetic: seeded N(0,0.02) fp16 weights, 3584 uniform-random prompt ids",
+        "config": {
+            "workload": "dense-2.3b-fp16-long-t0.7 prompt: 3584 tokens at positions 0..3583 into an empty cache, "
+                        "then the first generated token (greedy)",
+            "prefill_tokens_per_s": round(res["P"] / (res["dev_ms"] * 1e-3), 1),
+            "decode_path_ttft_ms": round(res["step_ms"], 1),
+            "speedup_over_decode_path": round(res["step_ms"] / res["dev_ms"], 2),
+            "kernel": f"per layer 4 tcgen05 GEMMs (M {M}) + norm, RoPE/KV, attention, SwiGLU kernels; the last "
+                      "prompt token through the persistent decode kernel",
+            "ctas": res["ctas"],
+            "l2": "inputs larger than L2: 4.69 GB of weight tiles and the growing KV cache per prefill",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "e2e": {"value": round(res["host_ms"], 3), "unit": "ms", "h2d_bytes_per_step": 4 * res["P"] + 32,
+                "d2h_bytes_per_step": 8, "path": "adp_prefill_tc: host token ids in, next token out (synchronises)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": f"adp::tc_gemm_kernel (gate|up: M {M}, N {N}, K {K}), {res['gemm_ms'] * 1e3:.1f} us "
+                               "per launch, 20 launches timed alone",
+                     "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({peak_kind}, burst; f16 has the same nominal "
+                                    "tensor rate as bf16)"},
+        "gpu_launches": 1 + 9 * L + 1,
+        **({"profiling_variant": f"{L} layers (not the workload)"} if args.layers else {}),
+        "clocks": res["clocks"],
+        "kernel_source": kernel_source_hash(("prefill.cu", "tc.cuh", "device.cuh", "plan.h")),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def write_timeline(path, model, kv, tok0, P, cfg):
     """Per-phase breakdown of one decode step from the kernel's %globaltimer stamps."""
     import numpy as np
@@ -646,6 +761,8 @@ def main():
     ap.add_argument("--batch", type=int, default=1,
                     help="decode this many independent requests together (batched kernel; default 1: the "
                          "single-request benchmark)")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time to first token of the 3584-token prompt through the tensor-core prefill")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: use this many layers of the workload's shape (the line says so)")
     args = ap.parse_args()
@@ -661,6 +778,10 @@ def main():
         ap.error("--batch must be >= 1")
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.prefill:
+        cfg, res = run_prefill(args, rank, world)
+        if rank == 0:
+            emit_prefill(args, cfg, res, world)
     elif args.batch > 1:
         cfg, res = run_engine_batch(args, rank, world)
         if rank == 0:

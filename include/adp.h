@@ -307,6 +307,10 @@ int adp_debug_skip_publication(adp_model* m, int32_t cta, int32_t phase);
  * A and W DEVICE row-major 16-bit matrices (f16, or bf16 when bf16 = 1) and C a DEVICE fp32 [M, N]
  * array.  Tiles the operands into temporary device buffers, runs, synchronises the device. */
 int adp_debug_tc_gemm(int32_t bf16, int32_t M, int32_t N, int32_t K, const void* A, const void* W, float* C);
+/* Benchmark hook of the tensor-core prefill: times `reps` back-to-back launches of one of the
+ * model's prefill GEMMs (which: 0 QKV, 1 Wo, 2 gate|up, 3 down; layer 0's weights) on M tokens of
+ * a constant operand, with CUDA events on the model's stream; *ms_per_launch receives the mean. */
+int adp_debug_tc_gemm_time(adp_model* m, int32_t which, int32_t M, int32_t reps, float* ms_per_launch);
 
 #if defined(__GNUC__)
 #pragma GCC visibility pop
