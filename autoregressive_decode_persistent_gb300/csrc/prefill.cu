@@ -1,6 +1,7 @@
-// Tensor-core prefill: the weight contractions of a whole prompt as dense GEMMs on the
-// fifth-generation tensor cores (tcgen05, accumulators in TMEM), with the norms, RoPE, causal
-// attention and SwiGLU between them as plain CUDA kernels.
+// Tensor-core prefill: the weight contractions of a whole prompt as dense GEMMs and its causal
+// attention as flash-style MMAs, both on the fifth-generation tensor cores (tcgen05,
+// accumulators in TMEM), with the norms, RoPE / KV write and SwiGLU between them as plain CUDA
+// kernels.
 //
 // The pages time-to-first-token as a metric of their own ("標準GPUによるリアルタイムLLM推論：
 // リクエストあたり3,000トークン/秒", "単一リクエストLLMデコード速度の重要性") and give no prefill
@@ -328,110 +329,6 @@ __global__ void tc_rope_kv_kernel(float* C, int ldc, int P, int pos0, int L, int
   }
 }
 
-// Causal attention of the prompt's queries (CTA: query head h, 32 consecutive tokens; warp: 4
-// of them) over the cached positions 0..pos of each: 32-key blocks of K and V staged in shared
-// memory, online softmax in fp32, output rounded into the A-operand tiles of the Wo GEMM.
-template <int HD, int KVDT>
-__global__ void __launch_bounds__(256) tc_attention_kernel(const float* __restrict__ C, int ldc, int P, int pos0,
-                                                          int L, int hq, int hkv, int max_ctx, float scale,
-                                                          const uint16_t* __restrict__ kc,
-                                                          const uint16_t* __restrict__ vc, int bf16, uint8_t* A,
-                                                          int k_tiles) {
-  constexpr int KSTR = HD + 8, DPL = HD / 32, QW = 4;
-  __shared__ __align__(16) uint16_t SK[32 * KSTR];
-  __shared__ __align__(16) uint16_t SV[32 * HD];
-  __shared__ __align__(16) float SQ[8][QW][HD];
-  __shared__ float SP[8][32];
-  const int h = blockIdx.x, t0 = blockIdx.y * 32;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = h * hkv / hq;
-  for (int i = threadIdx.x; i < QW * 8 * HD; i += blockDim.x) {
-    const int w = i / (QW * HD), qi = (i / HD) % QW, dd = i % HD;
-    const int t = t0 + w * QW + qi;
-    SQ[w][qi][dd] = t < P ? C[(size_t)t * ldc + h * HD + dd] : 0.0f;
-  }
-  float m[QW], l[QW], o[QW][DPL];
-#pragma unroll
-  for (int qi = 0; qi < QW; ++qi) {
-    m[qi] = -INFINITY;
-    l[qi] = 0.0f;
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) o[qi][k] = 0.0f;
-  }
-  const int kmax = pos0 + min(t0 + 31, P - 1);
-  const size_t head0 = ((size_t)L * hkv + g) * max_ctx;
-  for (int kb0 = 0; kb0 <= kmax; kb0 += 32) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < 32 * (HD / 8); i += blockDim.x) {
-      const int r = i / (HD / 8), v8 = i % (HD / 8);
-      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-      if (kb0 + r <= kmax) {
-        kv = *reinterpret_cast<const uint4*>(kc + (head0 + kb0 + r) * HD + v8 * 8);
-        vv = *reinterpret_cast<const uint4*>(vc + (head0 + kb0 + r) * HD + v8 * 8);
-      }
-      *reinterpret_cast<uint4*>(SK + r * KSTR + v8 * 8) = kv;
-      *reinterpret_cast<uint4*>(SV + r * HD + v8 * 8) = vv;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int qi = 0; qi < QW; ++qi) {
-      const int t = t0 + warp * QW + qi;
-      if (t >= P) continue;
-      const int pos = pos0 + t;
-      if (kb0 > pos) continue;
-      const int kp = kb0 + lane;
-      float s = -INFINITY;
-      if (kp <= pos) {
-        float acc = 0.0f;
-        const float* q = SQ[warp][qi];
-#pragma unroll 4
-        for (int v = 0; v < HD / 8; ++v) {
-          float k8[8];
-          kv8<KVDT>(*reinterpret_cast<const uint4*>(SK + lane * KSTR + v * 8), k8);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc = fmaf(q[v * 8 + e], k8[e], acc);
-        }
-        s = acc * scale;
-      }
-      float mb = s;
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, off));
-      const float mn = fmaxf(m[qi], mb);
-      const float corr = expf(m[qi] - mn);
-      const float pj = kp <= pos ? expf(s - mn) : 0.0f;
-      SP[warp][lane] = pj;
-      float ps = pj;
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
-      __syncwarp();
-      l[qi] = l[qi] * corr + ps;
-#pragma unroll
-      for (int k = 0; k < DPL; ++k) o[qi][k] *= corr;
-      const int nj = min(32, pos - kb0 + 1);
-      for (int j = 0; j < nj; ++j) {
-        const float pw = SP[warp][j];
-        float vf[DPL];
-        kv_dims_smem<KVDT, DPL>(SV + j * HD + lane * DPL, vf);
-#pragma unroll
-        for (int k = 0; k < DPL; ++k) o[qi][k] = fmaf(pw, vf[k], o[qi][k]);
-      }
-      m[qi] = mn;
-      __syncwarp();
-    }
-  }
-#pragma unroll
-  for (int qi = 0; qi < QW; ++qi) {
-    const int t = t0 + warp * QW + qi;
-    if (t >= P) continue;
-    const float inv = 1.0f / l[qi];
-#pragma unroll
-    for (int k = 0; k < DPL; ++k) {
-      const int col = h * HD + lane * DPL + k;
-      *reinterpret_cast<uint16_t*>(A + tc_a_offset(t, col, k_tiles)) = tc_store16(o[qi][k] * inv, bf16);
-    }
-  }
-}
-
 // h = silu(g) * u from the gate|up GEMM's output, rounded into the A-operand tiles of down.
 __global__ void tc_swiglu_kernel(const float* __restrict__ C, int ldc, int P, int ff, int bf16, uint8_t* A,
                                  int k_tiles) {
@@ -443,6 +340,8 @@ __global__ void tc_swiglu_kernel(const float* __restrict__ C, int ldc, int P, in
     *reinterpret_cast<uint16_t*>(A + tc_a_offset(t, i, k_tiles)) = tc_store16(g / (1.0f + expf(-g)) * u, bf16);
   }
 }
+
+cudaError_t tc_flash(const TcPrefill& a, int qkv_n, int L, int kt_att, cudaStream_t st);
 
 cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st) {
   const int P = a.P;
@@ -461,15 +360,7 @@ cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st) {
     tc_rope_kv_kernel<<<P, 256, 0, st>>>(a.C, qkv_n, P, a.pos0, L, a.hq, a.hkv, a.hd, a.max_ctx, a.rope_cos,
                                          a.rope_sin, a.kvdt, a.kc, a.vc);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const dim3 ag(a.hq, (P + 31) / 32);  // head_dim 64 or 128 (checked by the engine)
-    if (a.kvdt == DT_BF16) {
-      if (a.hd == 128) tc_attention_kernel<128, DT_BF16><<<ag, 256, 0, st>>>(a.C, qkv_n, P, a.pos0, L, a.hq, a.hkv, a.max_ctx, a.scale, a.kc, a.vc, a.bf16, a.A, kt_att);
-      else tc_attention_kernel<64, DT_BF16><<<ag, 256, 0, st>>>(a.C, qkv_n, P, a.pos0, L, a.hq, a.hkv, a.max_ctx, a.scale, a.kc, a.vc, a.bf16, a.A, kt_att);
-    } else {
-      if (a.hd == 128) tc_attention_kernel<128, DT_F16><<<ag, 256, 0, st>>>(a.C, qkv_n, P, a.pos0, L, a.hq, a.hkv, a.max_ctx, a.scale, a.kc, a.vc, a.bf16, a.A, kt_att);
-      else tc_attention_kernel<64, DT_F16><<<ag, 256, 0, st>>>(a.C, qkv_n, P, a.pos0, L, a.hq, a.hkv, a.max_ctx, a.scale, a.kc, a.vc, a.bf16, a.A, kt_att);
-    }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = tc_flash(a, qkv_n, L, kt_att, st)) != cudaSuccess) return e;
     if ((e = tc_gemm(a.bf16, true, a.A, a.wo[L], a.x, a.d, P, a.d, a.hq * a.hd, a.err, a.wait_ns, st)) != cudaSuccess)
       return e;
     tc_rmsnorm_kernel<<<(P + 7) / 8, 256, 0, st>>>(a.x, (const uint16_t*)a.ffn_norm[L], P, a.d, a.eps, a.bf16, a.A,
@@ -484,6 +375,218 @@ cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st) {
       return e;
   }
   return cudaSuccess;
+}
+
+}  // namespace adp
+
+namespace adp {
+
+// Causal attention of the prompt on the tensor cores, flash style.  CTA = query head h x 128
+// consecutive prompt tokens (thread t = token t0 + t = TMEM lane t), 128 threads.  Per block of
+// 128 cached keys: the K block and the V block (transposed) are staged in shared memory in the
+// K-major core-matrix layout; S = Q K^T (128 x 128, K = head_dim) accumulates in TMEM columns
+// [0, 128); each thread turns its row of S into the online softmax (scale, causal mask, running
+// max m and sum l in fp32, the block's probabilities rounded to the KV type into the P tile) and
+// rescales its row of O (TMEM columns [128, 128 + head_dim)) by exp(m_old - m_new); then
+// O += P V (K = 128 keys).  At the end O / l is rounded into the A-operand tiles of Wo.
+template <int HD, int KVDT>
+__global__ void __launch_bounds__(128) tc_flash_kernel(const float* __restrict__ C, int ldc, int P, int pos0, int L,
+                                                      int hq, int hkv, int max_ctx, float scale,
+                                                      const uint16_t* __restrict__ kc,
+                                                      const uint16_t* __restrict__ vc, int out_bf16, uint8_t* A,
+                                                      int k_tiles, int32_t* err, uint64_t wait_ns) {
+  constexpr int KT = HD / kTcBK;                        // 64-wide K tiles of Q and K
+  constexpr uint32_t QK_TILE = 128 * kTcBK * 2;         // 16 KB: 128 rows x 64
+  constexpr uint32_t VT_TILE = HD * kTcBK * 2;          // V^T tile: head_dim rows x 64 keys
+  constexpr int KV_BF16 = KVDT == DT_BF16 ? 1 : 0;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* Qs = smem;                                   // KT tiles
+  uint8_t* Ks = Qs + KT * QK_TILE;                      // KT tiles
+  uint8_t* Vt = Ks + KT * QK_TILE;                      // 2 tiles (keys 0..63, 64..127)
+  uint8_t* Ps = Vt + 2 * VT_TILE;                       // 2 tiles
+  uint64_t* bar = reinterpret_cast<uint64_t*>(Ps + 2 * QK_TILE);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  const int h = blockIdx.x, t0 = blockIdx.y * 128;
+  const int t = threadIdx.x, warp = t >> 5;
+  const int g = h * hkv / hq;
+  if (t == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  // Q row t (post-RoPE, fp32 in C) rounded to the KV type
+  {
+    const int tok = t0 + t;
+#pragma unroll 4
+    for (int k = 0; k < HD; k += 8) {
+      uint16_t e[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) e[j] = tok < P ? tc_store16(C[(size_t)tok * ldc + h * HD + k + j], KV_BF16) : 0;
+      *reinterpret_cast<uint4*>(Qs + (k / kTcBK) * QK_TILE + tc_tile_offset(t, k % kTcBK)) =
+          make_uint4(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16), e[4] | ((uint32_t)e[5] << 16),
+                     e[6] | ((uint32_t)e[7] << 16));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t tS = tmem + lane_base, tO = tmem + lane_base + 128;
+  const int pos = pos0 + min(t0 + t, P - 1);            // this row's position (padding rows: the last)
+  const int kmax = pos0 + min(t0 + 127, P - 1);
+  const size_t head0 = ((size_t)L * hkv + g) * max_ctx;
+  constexpr uint32_t idS = tc_idesc_f16(KV_BF16, 128, 128);
+  constexpr uint32_t idO = tc_idesc_f16(KV_BF16, 128, HD);
+  float m = -INFINITY, l = 0.0f;
+  uint32_t phase = 0;
+  bool ok = true;
+  int32_t never = 0;
+  for (int kb0 = 0; kb0 <= kmax && ok; kb0 += 128) {
+    // ---- stage key rows kb0 + t: K as a B operand (keys x head_dim), V transposed (head_dim x keys)
+    {
+      const int kp = kb0 + t;
+      const uint16_t* kr = kc + (head0 + kp) * HD;
+      const uint16_t* vr = vc + (head0 + kp) * HD;
+#pragma unroll 4
+      for (int k = 0; k < HD; k += 8) {
+        uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+        if (kp <= kmax) {
+          kv = *reinterpret_cast<const uint4*>(kr + k);
+          vv = *reinterpret_cast<const uint4*>(vr + k);
+        }
+        *reinterpret_cast<uint4*>(Ks + (k / kTcBK) * QK_TILE + tc_tile_offset(t, k % kTcBK)) = kv;
+        const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint16_t e = (uint16_t)(w4[j >> 1] >> ((j & 1) * 16));
+          *reinterpret_cast<uint16_t*>(Vt + (t / kTcBK) * VT_TILE + tc_tile_offset(k + j, t % kTcBK)) = e;
+        }
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // ---- S = Q K^T
+    if (t == 0) {
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = (kk / 4) * QK_TILE + (kk % 4) * 256;
+        tc_mma_f16(tmem, tc_smem_desc(smem_u32(Qs) + off, 128, 1024), tc_smem_desc(smem_u32(Ks) + off, 128, 1024),
+                   idS, kk > 0);
+      }
+      tc_commit(bar);
+    }
+    __syncwarp();
+    ok = mbar_wait(bar, phase, &never, wait_ns);
+    phase ^= 1u;
+    tc_fence_after();
+    // ---- online softmax of row t
+    float mb = -INFINITY;
+#pragma unroll
+    for (int c0 = 0; c0 < 128; c0 += 32) {
+      float v[32];
+      tmem_ld32(tS + c0, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (kb0 + c0 + j <= pos) mb = fmaxf(mb, v[j] * scale);
+    }
+    const float mn = fmaxf(m, mb);
+    const float corr = expf(m - mn);
+    float ps = 0.0f;
+#pragma unroll
+    for (int c0 = 0; c0 < 128; c0 += 32) {
+      float v[32];
+      tmem_ld32(tS + c0, v);
+      uint16_t e[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float p = kb0 + c0 + j <= pos ? expf(v[j] * scale - mn) : 0.0f;
+        ps += p;
+        e[j] = tc_store16(p, KV_BF16);
+      }
+#pragma unroll
+      for (int j = 0; j < 32; j += 8)
+        *reinterpret_cast<uint4*>(Ps + ((c0 + j) / kTcBK) * QK_TILE + tc_tile_offset(t, (c0 + j) % kTcBK)) =
+            make_uint4(e[j] | ((uint32_t)e[j + 1] << 16), e[j + 2] | ((uint32_t)e[j + 3] << 16),
+                       e[j + 4] | ((uint32_t)e[j + 5] << 16), e[j + 6] | ((uint32_t)e[j + 7] << 16));
+    }
+    l = l * corr + ps;
+    m = mn;
+    if (kb0 > 0) {  // O *= exp(m_old - m_new) before this block's products are added
+#pragma unroll
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        float v[32];
+        tmem_ld32(tO + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= corr;
+        tmem_st32(tO + c0, v);
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // ---- O += P V
+    if (t == 0) {
+#pragma unroll
+      for (int kk = 0; kk < 128 / 16; ++kk) {
+        const uint32_t pa = smem_u32(Ps) + (kk / 4) * QK_TILE + (kk % 4) * 256;
+        const uint32_t vb = smem_u32(Vt) + (kk / 4) * VT_TILE + (kk % 4) * 256;
+        tc_mma_f16(tmem + 128, tc_smem_desc(pa, 128, 1024), tc_smem_desc(vb, 128, 1024), idO, kb0 > 0 || kk > 0);
+      }
+      tc_commit(bar);
+    }
+    __syncwarp();
+    ok = mbar_wait(bar, phase, &never, wait_ns) && ok;
+    phase ^= 1u;
+    tc_fence_after();
+  }
+  // ---- O / l into the Wo GEMM's A tiles
+  const int tok = t0 + t;
+  if (ok) {
+    const float inv = 1.0f / l;
+#pragma unroll
+    for (int c0 = 0; c0 < HD; c0 += 32) {
+      float v[32];
+      tmem_ld32(tO + c0, v);
+      if (tok < P) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          *reinterpret_cast<uint16_t*>(A + tc_a_offset(tok, h * HD + c0 + j, k_tiles)) =
+              tc_store16(v[j] * inv, out_bf16);
+      }
+    }
+  } else if (t == 0) {
+    atomicCAS(err, 0, DE_PIPELINE_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+template <int HD, int KVDT>
+cudaError_t tc_flash_launch(const TcPrefill& a, int qkv_n, int L, int kt_att, cudaStream_t st) {
+  constexpr size_t smem = (size_t)2 * (HD / kTcBK) * 128 * kTcBK * 2 + 2 * (size_t)HD * kTcBK * 2 +
+                          2 * (size_t)128 * kTcBK * 2 + 64;
+  const void* k = (const void*)tc_flash_kernel<HD, KVDT>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  tc_flash_kernel<HD, KVDT><<<dim3(a.hq, (a.P + 127) / 128), 128, smem, st>>>(
+      a.C, qkv_n, a.P, a.pos0, L, a.hq, a.hkv, a.max_ctx, a.scale, a.kc, a.vc, a.bf16, a.A, kt_att, a.err, a.wait_ns);
+  return cudaGetLastError();
+}
+
+cudaError_t tc_flash(const TcPrefill& a, int qkv_n, int L, int kt_att, cudaStream_t st) {
+  if (a.kvdt == DT_BF16)
+    return a.hd == 128 ? tc_flash_launch<128, DT_BF16>(a, qkv_n, L, kt_att, st)
+                       : tc_flash_launch<64, DT_BF16>(a, qkv_n, L, kt_att, st);
+  return a.hd == 128 ? tc_flash_launch<128, DT_F16>(a, qkv_n, L, kt_att, st)
+                     : tc_flash_launch<64, DT_F16>(a, qkv_n, L, kt_att, st);
 }
 
 }  // namespace adp
