@@ -401,12 +401,13 @@ __global__ void __launch_bounds__(128) tc_flash_kernel(const float* __restrict__
   constexpr int KV_BF16 = KVDT == DT_BF16 ? 1 : 0;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* Qs = smem;                                   // KT tiles
-  uint8_t* Ks = Qs + KT * QK_TILE;                      // KT tiles
-  uint8_t* Vt = Ks + KT * QK_TILE;                      // 2 tiles (keys 0..63, 64..127)
-  uint8_t* Ps = Vt + 2 * VT_TILE;                       // 2 tiles
-  uint64_t* bar = reinterpret_cast<uint64_t*>(Ps + 2 * QK_TILE);
+  uint8_t* Ks = Qs + KT * QK_TILE;                      // max(KT, 2) tiles
+  uint8_t* Ps = Ks;                                     // P reuses the K block once S is computed
+  uint8_t* Vt = Ks + (KT > 2 ? KT : 2) * QK_TILE;       // 2 tiles (keys 0..63, 64..127)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(Vt + 2 * VT_TILE);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
-  const int h = blockIdx.x, t0 = blockIdx.y * 128;
+  // the longest causal rows (last query blocks) start first
+  const int h = blockIdx.x, t0 = (gridDim.y - 1 - blockIdx.y) * 128;
   const int t = threadIdx.x, warp = t >> 5;
   const int g = h * hkv / hq;
   if (t == 0) {
@@ -448,22 +449,38 @@ __global__ void __launch_bounds__(128) tc_flash_kernel(const float* __restrict__
   for (int kb0 = 0; kb0 <= kmax && ok; kb0 += 128) {
     // ---- stage key rows kb0 + t: K as a B operand (keys x head_dim), V transposed (head_dim x keys)
     {
+      // every load of the row first, then the shared-memory stores (16 loads in flight per thread)
       const int kp = kb0 + t;
-      const uint16_t* kr = kc + (head0 + kp) * HD;
-      const uint16_t* vr = vc + (head0 + kp) * HD;
-#pragma unroll 4
-      for (int k = 0; k < HD; k += 8) {
-        uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-        if (kp <= kmax) {
-          kv = *reinterpret_cast<const uint4*>(kr + k);
-          vv = *reinterpret_cast<const uint4*>(vr + k);
-        }
-        *reinterpret_cast<uint4*>(Ks + (k / kTcBK) * QK_TILE + tc_tile_offset(t, k % kTcBK)) = kv;
-        const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
+      const bool in = kp <= kmax;
+      const uint4* kr = reinterpret_cast<const uint4*>(kc + (head0 + (in ? kp : 0)) * HD);
+      const uint4* vr = reinterpret_cast<const uint4*>(vc + (head0 + (in ? kp : 0)) * HD);
+      constexpr int NC = HD / 8;  // 16-byte chunks per row
+      constexpr int HB = NC < 16 ? NC : 16;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint16_t e = (uint16_t)(w4[j >> 1] >> ((j & 1) * 16));
-          *reinterpret_cast<uint16_t*>(Vt + (t / kTcBK) * VT_TILE + tc_tile_offset(k + j, t % kTcBK)) = e;
+      for (int c0 = 0; c0 < NC; c0 += HB) {
+        uint4 kv[HB];
+#pragma unroll
+        for (int c = 0; c < HB; ++c) kv[c] = in ? __ldg(kr + c0 + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int c = 0; c < HB; ++c) {
+          const int k = (c0 + c) * 8;
+          *reinterpret_cast<uint4*>(Ks + (k / kTcBK) * QK_TILE + tc_tile_offset(t, k % kTcBK)) = kv[c];
+        }
+      }
+#pragma unroll
+      for (int c0 = 0; c0 < NC; c0 += HB) {
+        uint4 vv[HB];
+#pragma unroll
+        for (int c = 0; c < HB; ++c) vv[c] = in ? __ldg(vr + c0 + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int c = 0; c < HB; ++c) {
+          const int k = (c0 + c) * 8;
+          const uint32_t w4[4] = {vv[c].x, vv[c].y, vv[c].z, vv[c].w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint16_t e = (uint16_t)(w4[j >> 1] >> ((j & 1) * 16));
+            *reinterpret_cast<uint16_t*>(Vt + (t / kTcBK) * VT_TILE + tc_tile_offset(k + j, t % kTcBK)) = e;
+          }
         }
       }
     }
@@ -485,7 +502,7 @@ __global__ void __launch_bounds__(128) tc_flash_kernel(const float* __restrict__
     ok = mbar_wait(bar, phase, &never, wait_ns);
     phase ^= 1u;
     tc_fence_after();
-    // ---- online softmax of row t
+    // ---- online softmax of row t (its probabilities overwrite the K block, which S no longer needs)
     float mb = -INFINITY;
 #pragma unroll
     for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -571,8 +588,8 @@ __global__ void __launch_bounds__(128) tc_flash_kernel(const float* __restrict__
 
 template <int HD, int KVDT>
 cudaError_t tc_flash_launch(const TcPrefill& a, int qkv_n, int L, int kt_att, cudaStream_t st) {
-  constexpr size_t smem = (size_t)2 * (HD / kTcBK) * 128 * kTcBK * 2 + 2 * (size_t)HD * kTcBK * 2 +
-                          2 * (size_t)128 * kTcBK * 2 + 64;
+  constexpr int KT = HD / kTcBK;
+  constexpr size_t smem = (size_t)(KT + (KT > 2 ? KT : 2)) * 128 * kTcBK * 2 + 2 * (size_t)HD * kTcBK * 2 + 64;
   const void* k = (const void*)tc_flash_kernel<HD, KVDT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
