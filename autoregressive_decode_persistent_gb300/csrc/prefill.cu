@@ -19,7 +19,6 @@
 
 #include <algorithm>
 
-#include "decode_core.cuh"
 #include "launch.h"
 #include "tc.cuh"
 

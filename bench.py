@@ -564,8 +564,8 @@ def emit_prefill(args, cfg, res, world):
             "prefill_tokens_per_s": round(res["P"] / (res["dev_ms"] * 1e-3), 1),
             "decode_path_ttft_ms": round(res["step_ms"], 1),
             "speedup_over_decode_path": round(res["step_ms"] / res["dev_ms"], 2),
-            "kernel": f"per layer 4 tcgen05 GEMMs (M {M}) + norm, RoPE/KV, attention, SwiGLU kernels; the last "
-                      "prompt token through the persistent decode kernel",
+            "kernel": f"per layer 4 tcgen05 GEMMs (M {M}), tcgen05 flash attention, and norm, RoPE/KV, SwiGLU "
+                      "kernels; the last prompt token through the persistent decode kernel",
             "ctas": res["ctas"],
             "l2": "inputs larger than L2: 4.69 GB of weight tiles and the growing KV cache per prefill",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
