@@ -45,3 +45,44 @@ def test_reference_arm_prints_its_line():
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["warmup"] == 3
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_batch_line_has_the_contract_keys(capsys):
+    """--batch N: value counts the tokens of all requests; the roofline is the batched kernel's."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    cfg = synth.get_config("dense-2.3b-fp16")
+    res = {"ms": 1000.0, "steps": 512, "nb": 3, "n_launch": 1, "step_pct": {"p50_us": 1.0, "p99_us": 2.0},
+           "weight_bytes": 4686090240, "achieved_gbs": 2100.0, "per_launch_bytes": 2.46e12, "launch_ms": 1000.0,
+           "peak": 6757.9, "peak_kind": "measured", "e2e": 1300.0, "n_e2e": 512,
+           "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 10}, "ctas": 152,
+           "launches": 1}
+    bench.emit_batch(types.SimpleNamespace(warmup=8, layers=0), cfg, res, 1)
+    line = json.loads(capsys.readouterr().out.strip())
+    for k in REQUIRED:
+        assert k in line, k
+    assert line["value"] == pytest.approx(3 * 512.0)
+    assert line["config"]["batch"] == 3 and line["higher_is_better"] is True
+    assert line["roofline"]["kernel"] == "adp::decode_batch_kernel"
+    assert line["e2e"]["d2h_bytes_per_step"] == 16
+
+
+def test_prefill_line_has_the_contract_keys(capsys):
+    """--prefill: time to first token (lower is better), roofline of the tensor-core GEMM."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    cfg = synth.get_config("dense-2.3b-fp16-long-t0.7")
+    res = {"dev_ms": 31.0, "host_ms": 31.5, "step_ms": 4700.0, "P": 3584, "gemm_ms": 0.333,
+           "gemm_flops": 2.0 * 3583 * 19456 * 2560, "gemm_shape": (3583, 19456, 2560),
+           "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 4}, "ctas": 152,
+           "n_layers": 25}
+    bench.emit_prefill(types.SimpleNamespace(warmup=3, steps=5, layers=0), cfg, res, 1)
+    line = json.loads(capsys.readouterr().out.strip())
+    for k in REQUIRED:
+        assert k in line, k
+    assert line["higher_is_better"] is False and line["unit"] == "ms" and line["value"] == pytest.approx(31.0)
+    assert line["roofline"]["bound"] == "tensor" and line["roofline"]["unit"] == "TFLOP/s"
+    assert line["roofline"]["achieved"] == pytest.approx(2.0 * 3583 * 19456 * 2560 / 0.333e-3 / 1e12, rel=1e-3)
+    assert line["gpu_launches"] == 1 + 9 * 25 + 1
