@@ -82,6 +82,7 @@ struct adp_model {
   uint64_t epochs_used = 0;  // epochs handed out since the exchange buffers were last cleared
   size_t ll_bytes[11] = {0};  // sizes of the epoch-tagged exchange buffers
   std::vector<const void*> h_attn_norm, h_ffn_norm;  // per-layer gains (device pointers)
+  std::vector<const float*> h_wscale[7];             // e4m3 dense: per-layer row scales of q, k, v, o, gate, up, down
   // Tensor-core prefill (set up at the first adp_prefill_tc): the layer matrices again, as GEMM
   // operand tiles, and scratch for up to tc_cap prompt tokens.
   struct TcState {
@@ -401,7 +402,10 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
     sd[l] = Lw.e_down_scale;
     const float* s7[7] = {Lw.wq_scale, Lw.wk_scale, Lw.wv_scale, Lw.wo_scale, Lw.w_gate_scale, Lw.w_up_scale,
                           Lw.w_down_scale};
-    for (int i = 0; i < 7; ++i) ws[i][l] = c.weight_dtype == ADP_E4M3 ? s7[i] : nullptr;
+    for (int i = 0; i < 7; ++i) {
+      ws[i][l] = c.weight_dtype == ADP_E4M3 ? s7[i] : nullptr;
+      m->h_wscale[i].push_back(ws[i][l]);
+    }
   }
   for (int i = 0; i < 7; ++i) {
     const float** t = nullptr;
@@ -1029,24 +1033,33 @@ extern "C" int adp_generate_batch_async(adp_model* m, adp_kv* const* kvs, int32_
 
 // ---------------------------------------------------------------- tensor-core prefill
 
+// The 16-bit type of the tensor-core prefill's GEMM operands: the weights' own, or for e4m3
+// layer matrices the embedding's (the matrices are dequantised into it).
+static int tc_operand_bf16(const adp_config& c) {
+  return (c.weight_dtype == ADP_E4M3 ? c.embed_dtype : c.weight_dtype) == ADP_BF16 ? 1 : 0;
+}
+
 // Set up the tensor-core prefill once per model: every layer matrix again as GEMM operand tiles
-// (rebuilt from the decode image), for dense models with 16-bit weights and head_dim 64 or 128.
+// (rebuilt from the decode image), for dense models (16-bit or e4m3 layer matrices) with head_dim
+// 64 or 128.
 static int tc_init(adp_model* m) {
   adp_model::TcState& T = m->tc;
   if (T.init_rc != 1) return T.init_rc;
   const adp_config& c = m->cfg;
   T.init_rc = ADP_ERR_UNSUPPORTED_CONFIG;
-  if (c.n_experts != 0 || (c.weight_dtype != ADP_F16 && c.weight_dtype != ADP_BF16)) return T.init_rc;
+  if (c.n_experts != 0) return T.init_rc;
   if (c.head_dim != 64 && c.head_dim != 128) return T.init_rc;
   const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim;
   for (const PhaseDesc& P : m->phases) {
     int rows = 0;
     std::vector<const uint8_t*>* dst = nullptr;
+    const float* sc3[3] = {nullptr, nullptr, nullptr};  // row scales of e4m3 matrices
+    auto scale = [&](int i) { return m->h_wscale[i].empty() ? nullptr : m->h_wscale[i][P.layer]; };
     switch (P.kind) {
-      case PK_QKV: rows = (hq + 2 * hkv) * hd; dst = &T.wqkv; break;
-      case PK_WO: rows = d; dst = &T.wo; break;
-      case PK_GU: rows = 2 * c.d_ff; dst = &T.wgu; break;
-      case PK_DOWN: rows = d; dst = &T.wdown; break;
+      case PK_QKV: rows = (hq + 2 * hkv) * hd; dst = &T.wqkv; sc3[0] = scale(0); sc3[1] = scale(1); sc3[2] = scale(2); break;
+      case PK_WO: rows = d; dst = &T.wo; sc3[0] = scale(3); break;
+      case PK_GU: rows = 2 * c.d_ff; dst = &T.wgu; sc3[0] = scale(4); sc3[1] = scale(5); break;
+      case PK_DOWN: rows = d; dst = &T.wdown; sc3[0] = scale(6); break;
       default: continue;
     }
     uint8_t* buf = nullptr;
@@ -1054,7 +1067,8 @@ static int tc_init(adp_model* m) {
     int rc = m->alloc(&buf, bytes);
     if (rc) return T.init_rc = rc;
     CK(cudaMemsetAsync(buf, 0, bytes, m->stream));
-    CK(tc_unpack(m->image, P, m->G, hd, hq, hkv, c.d_ff, buf, m->stream));
+    CK(tc_unpack(m->image, P, m->G, hd, hq, hkv, c.d_ff, buf, sc3[0], sc3[1], sc3[2], tc_operand_bf16(c),
+                 m->stream));
     dst->push_back(buf);
   }
   CK(cudaStreamSynchronize(m->stream));
@@ -1102,7 +1116,7 @@ extern "C" int adp_debug_tc_gemm_time(adp_model* m, int32_t which, int32_t M, in
   const int kmax = std::max({c.d_model, c.n_heads * c.head_dim, c.d_ff});
   // operand A: every element 0x3C3C (about 1.06 in f16, 0.0115 in bf16)
   CK(cudaMemsetAsync(m->tc.A, 0x3C, tc_tiled_bytes(M, kmax, 128), m->stream));
-  const int bf16 = c.weight_dtype == ADP_BF16 ? 1 : 0;
+  const int bf16 = tc_operand_bf16(c);
   cudaEvent_t e0, e1;
   CK(cudaEventCreate(&e0));
   CK(cudaEventCreate(&e1));
@@ -1148,7 +1162,7 @@ extern "C" int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_toke
     a.hd = c.head_dim;
     a.ff = c.d_ff;
     a.max_ctx = c.max_ctx;
-    a.bf16 = c.weight_dtype == ADP_BF16 ? 1 : 0;
+    a.bf16 = tc_operand_bf16(c);
     a.kvdt = c.kv_dtype;
     a.eps = c.rms_eps;
     a.scale = m->p.attn_scale;

@@ -63,7 +63,9 @@ struct TcPrefill {
 cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st);
 // Phase P's tiles of the decode image -> one GEMM weight operand in 256-row tiles (dst cleared
 // beforehand; rows in the order of the caller's matrices).
+// e4m3 phases (eb 1) are dequantised with their row scales (sa, sb, sc: the q/k/v, gate/up or single
+// matrix's tables) into the operand type (out_bf16); 16-bit phases are copied.
 cudaError_t tc_unpack(const uint8_t* image, const PhaseDesc& P, int G, int hd, int hq, int hkv, int ff, uint8_t* dst,
-                      cudaStream_t st);
+                      const float* sa, const float* sb, const float* sc, int out_bf16, cudaStream_t st);
 
 }  // namespace adp

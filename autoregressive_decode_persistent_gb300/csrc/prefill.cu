@@ -125,8 +125,11 @@ __global__ void __launch_bounds__(128, 1)
             if (ADD) {
               const float4 a = *reinterpret_cast<const float4*>(dst + j);
               o = make_float4(__fadd_rn(a.x, o.x), __fadd_rn(a.y, o.y), __fadd_rn(a.z, o.z), __fadd_rn(a.w, o.w));
+              *reinterpret_cast<float4*>(dst + j) = o;
+            } else {
+              // streaming store: the output should not evict the operand tiles other CTAs still read
+              __stcs(reinterpret_cast<float4*>(dst + j), o);
             }
-            *reinterpret_cast<float4*>(dst + j) = o;
           }
         } else {
 #pragma unroll
@@ -219,47 +222,75 @@ __device__ __forceinline__ int tc_logical_row(const PhaseDesc& P, int u, int j, 
   return u * P.unit_rows + j;
 }
 
+// 16-bit storage of an fp32 value (RNE): bf16 or f16.
+__device__ __forceinline__ uint16_t tc_store16(float v, int bf16) {
+  if (bf16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return __half_as_ushort(__float2half_rn(v));
+}
+
+// Per-row scale of an e4m3 layer matrix for logical row `row` of phase P's GEMM operand (the
+// scale tables of the matrices the rows come from: q, k, v; gate, up; or the one matrix).
+__device__ __forceinline__ float tc_row_scale(const PhaseDesc& P, int row, int hd, int hq, int hkv, int ff,
+                                              const float* sa, const float* sb, const float* sc) {
+  if (P.kind == PK_QKV) {
+    if (row < hq * hd) return sa[row];
+    if (row < (hq + hkv) * hd) return sb[row - hq * hd];
+    return sc[row - (hq + hkv) * hd];
+  }
+  if (P.kind == PK_GU) return row < ff ? sa[row] : sb[row - ff];
+  return sa[row];
+}
+
 // The decode image's tiles of phase P back into one tiled GEMM operand (256-row tiles): the
-// inverse of the repack, walked the same way (CTA c's units, rounds, K-chunks).
+// inverse of the repack, walked the same way (CTA c's units, rounds, K-chunks).  16-bit weights
+// are copied as they are; e4m3 weights become scale x code (fp32, then RNE to the operand type).
 __global__ void tc_unpack_kernel(const uint8_t* __restrict__ image, PhaseDesc P, uint8_t* dst, int k_tiles, int hd,
-                                 int hq, int hkv, int ff) {
+                                 int hq, int hkv, int ff, const float* sa, const float* sb, const float* sc,
+                                 int out_bf16) {
   const uint32_t c = blockIdx.x, G = gridDim.x;
   const long long a0 = (long long)c * P.n_units / G, a1 = (long long)(c + 1) * P.n_units / G;
   const int u0 = (int)a0, n = (int)(a1 - a0);
   if (n <= 0) return;
-  const uint64_t unit_bytes = (uint64_t)P.unit_rows * P.K * 2;
+  const int eb = P.eb;
+  const uint64_t unit_bytes = (uint64_t)P.unit_rows * P.K * eb;
   const uint8_t* src_cta = image + P.region + (uint64_t)u0 * unit_bytes;
-  const int nv16 = P.K / 8;
-  const long long total = (long long)n * P.unit_rows * nv16;
+  const int nv8 = P.K / 8;
+  const long long total = (long long)n * P.unit_rows * nv8;
   for (long long idx = threadIdx.x; idx < total; idx += blockDim.x) {
-    const int lu = (int)(idx / ((long long)P.unit_rows * nv16));
-    const int rem = (int)(idx % ((long long)P.unit_rows * nv16));
-    const int j = rem / nv16, cv = rem % nv16;
+    const int lu = (int)(idx / ((long long)P.unit_rows * nv8));
+    const int rem = (int)(idx % ((long long)P.unit_rows * nv8));
+    const int j = rem / nv8, cv = rem % nv8;
     const int col = cv * 8;
     const int ck = col / P.KC;
     const int kck = min(P.KC, P.K - ck * P.KC);
     const int r = lu / P.upr, i = lu % P.upr;
     const int m = min(P.upr, n - r * P.upr);
-    const uint64_t off = (uint64_t)r * P.upr * unit_bytes + (uint64_t)m * P.unit_rows * ck * P.KC * 2 +
-                         ((uint64_t)(i * P.unit_rows + j) * kck + (col - ck * P.KC)) * 2;
+    const uint64_t off = (uint64_t)r * P.upr * unit_bytes + (uint64_t)m * P.unit_rows * ck * P.KC * eb +
+                         ((uint64_t)(i * P.unit_rows + j) * kck + (col - ck * P.KC)) * eb;
     const int row = tc_logical_row(P, u0 + lu, j, hd, hq, hkv, ff);
     const size_t tile = (size_t)(row / kTcBN) * k_tiles + col / kTcBK;
-    *reinterpret_cast<uint4*>(dst + tile * kTcBBytes + tc_tile_offset(row % kTcBN, col % kTcBK)) =
-        *reinterpret_cast<const uint4*>(src_cta + off);
+    uint4 v;
+    if (eb == 2) {
+      v = *reinterpret_cast<const uint4*>(src_cta + off);
+    } else {
+      float w[8];
+      load8<DT_E4M3>(src_cta + off, w);
+      const float s = tc_row_scale(P, row, hd, hq, hkv, ff, sa, sb, sc);
+      uint16_t e[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) e[k] = tc_store16(s * w[k], out_bf16);
+      v = make_uint4(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16), e[4] | ((uint32_t)e[5] << 16),
+                     e[6] | ((uint32_t)e[7] << 16));
+    }
+    *reinterpret_cast<uint4*>(dst + tile * kTcBBytes + tc_tile_offset(row % kTcBN, col % kTcBK)) = v;
   }
 }
 
 cudaError_t tc_unpack(const uint8_t* image, const PhaseDesc& P, int G, int hd, int hq, int hkv, int ff, uint8_t* dst,
-                      cudaStream_t st) {
+                      const float* sa, const float* sb, const float* sc, int out_bf16, cudaStream_t st) {
   const int k_tiles = (P.K + kTcBK - 1) / kTcBK;
-  tc_unpack_kernel<<<G, 256, 0, st>>>(image, P, dst, k_tiles, hd, hq, hkv, ff);
+  tc_unpack_kernel<<<G, 256, 0, st>>>(image, P, dst, k_tiles, hd, hq, hkv, ff, sa, sb, sc, out_bf16);
   return cudaGetLastError();
-}
-
-// 16-bit storage of an fp32 activation (RNE) for the GEMM's A operand.
-__device__ __forceinline__ uint16_t tc_store16(float v, int bf16) {
-  if (bf16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-  return __half_as_ushort(__float2half_rn(v));
 }
 
 __device__ __forceinline__ size_t tc_a_offset(int t, int k, int k_tiles) {

@@ -211,10 +211,11 @@ int adp_sync(adp_model* m);                          /* synchronise the stream; 
  * §"単一リクエストLLMデコード速度の重要性") but fix no prefill algorithm; this path is not the
  * decode step's arithmetic contract, so its KV rows and logits agree with the oracle within the
  * tolerances, not bit for bit (adp_prefill is the bit-exact path).
- * Arguments, errors and synchronisation as adp_prefill.  Dense models with f16/bf16 weights and
- * head_dim 64 or 128 only (else ADP_ERR_UNSUPPORTED_CONFIG).  The first call builds a second copy
- * of the layer matrices in the tensor cores' tile layout (device memory owned by the model, as
- * large as the layer matrices); scratch grows with the longest prompt seen. */
+ * Arguments, errors and synchronisation as adp_prefill.  Dense models with head_dim 64 or 128 only
+ * (else ADP_ERR_UNSUPPORTED_CONFIG); e4m3 layer matrices are dequantised with their row scales
+ * into the embedding's 16-bit type for the GEMMs.  The first call builds a second copy of the
+ * layer matrices in the tensor cores' tile layout (16-bit, device memory owned by the model);
+ * scratch grows with the longest prompt seen. */
 int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t n, const adp_sampling* sampling,
                    int32_t* next_token, float* dev_logits);
 

@@ -104,14 +104,16 @@ def test_prefill_tc_ragged_and_after_prefix(lib):
     _prefill_case(cfg, 133, prefix_len=21)
 
 
-def test_prefill_tc_full_size(lib):
-    """The 2.3B fp16 model at full size: a 448-row synthetic cache prefix, then a 64-token prompt
-    through the tensor-core path and three decode steps."""
+@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-2.3b-e4m3"])
+def test_prefill_tc_full_size(lib, name):
+    """The 2.3B model at full size (fp16, and e4m3 layer matrices dequantised for the GEMMs): a
+    448-row synthetic cache prefix, then a 64-token prompt through the tensor-core path and three
+    decode steps."""
     import synth
-    _prefill_case(synth.get_config("dense-2.3b-fp16"), 64, prefix_len=448)
+    _prefill_case(synth.get_config(name), 64, prefix_len=448)
 
 
-@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16"])
+@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "dense-2.3b-e4m3"])
 def test_prefill_tc_shrunk_workloads(lib, name):
     import synth
     _prefill_case(synth.shrink(synth.get_config(name)), 70)
@@ -134,7 +136,7 @@ def test_prefill_tc_single_token_is_a_decode_step(lib):
 def test_prefill_tc_rejects_unsupported_models(lib):
     import synth
     from autoregressive_decode_persistent_gb300.model import DecodeModel
-    for name in ("moe-32x1408-top4-e4m3", "dense-2.3b-e4m3"):
+    for name in ("moe-32x1408-top4-e4m3",):
         cfg = synth.shrink(synth.get_config(name))
         model = DecodeModel(cfg, synth.model_weights(cfg))
         kv = model.new_kv()
