@@ -150,7 +150,7 @@ template <int ROWS, int WDT>
 __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, uint8_t* ring, float* xbuf,
                                            const PhaseDesc& Pd, uint32_t c, uint32_t G, int cw, int lane,
                                            uint32_t& t_io, uint32_t ew) {
-  constexpr int EB = 2;
+  constexpr int EB = WDT == DT_E4M3 ? 1 : 2;
   constexpr int NA = kMaxBatch * ROWS;
   const int kind = Pd.kind, L = Pd.layer, K = Pd.K, KC = Pd.KC, n_chunks = Pd.n_chunks, upr = Pd.upr;
   const int Kp = vec_stride(K);
@@ -171,6 +171,31 @@ __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, 
     float acc[NA];
 #pragma unroll
     for (int i = 0; i < NA; ++i) acc[i] = 0.0f;
+    // e4m3 layer matrices: this unit's row scales, applied after the fold (as for one request)
+    float sc[ROWS];
+    if constexpr (WDT == DT_E4M3) {
+      if (active) {
+        int mi, r0, rstep = 1;
+        if (kind == PK_QKV) {
+          const int half = p.hd / 2, nq = p.hq * half, nk = p.hkv * half;
+          const int uu = unit < nq ? unit : unit < nq + nk ? unit - nq : unit - nq - nk;
+          mi = unit < nq ? 0 : unit < nq + nk ? 1 : 2;
+          r0 = (uu / half) * p.hd + uu % half;
+          rstep = half;
+        } else if (kind == PK_GU) {
+          mi = 4;
+          r0 = unit;
+          rstep = 0;
+        } else {
+          mi = kind == PK_WO ? 3 : 6;
+          r0 = unit * ROWS;
+        }
+        const float* tab = p.wscale[mi][L];
+#pragma unroll
+        for (int j = 0; j < ROWS; ++j)
+          sc[j] = (kind == PK_GU) ? __ldg(p.wscale[4 + j][L] + r0) : __ldg(tab + r0 + j * rstep);
+      }
+    }
     for (int ck = 0; ck < n_chunks; ++ck) {
       const bool ok = mbar_wait(&ctl->full[slot], par, &ctl->abort, wait_ns);
       if (!ok) {
@@ -211,7 +236,10 @@ __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, 
     for (int r = 0; r < kMaxBatch; ++r)
       if (r < nb)
 #pragma unroll
-        for (int j = 0; j < ROWS; ++j) acc[r * ROWS + j] = warp_fold(acc[r * ROWS + j]);
+        for (int j = 0; j < ROWS; ++j) {
+          acc[r * ROWS + j] = warp_fold(acc[r * ROWS + j]);
+          if constexpr (WDT == DT_E4M3) acc[r * ROWS + j] = __fmul_rn(sc[j], acc[r * ROWS + j]);
+        }
     // ---- epilogues (every lane holds every folded sum)
     if (kind == PK_QKV) {
       if (lane < nb) {
@@ -741,7 +769,9 @@ __device__ void consumer_batch(const Params& p, Ctl* ctl, BCtl* bc, uint8_t* rin
         }
       } else if (P.kind == PK_SAMPLE) {
         if (bc->any_sample) sample_batch(p, ctl, bc, ebase, c, G, cw, lane);
-      } else if (p.wdt == DT_BF16) {
+      } else if (p.wdt == DT_E4M3 && P.kind != PK_LM) {
+        gemv_batch<2, DT_E4M3>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew);
+      } else if ((P.kind == PK_LM ? p.edt : p.wdt) == DT_BF16) {
         run_gemv_batch<DT_BF16>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew);
       } else {
         run_gemv_batch<DT_F16>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew);

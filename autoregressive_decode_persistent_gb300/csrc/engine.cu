@@ -809,13 +809,13 @@ extern "C" int adp_generate_async(adp_model* m, adp_kv* kv, int32_t token, int32
 
 // Set up batched decode once per model: the shared-memory layout of every batch size that fits
 // (nb input vectors of the widest GEMV input beside a ring of at least two slots), the
-// per-request exchange buffers and the step-state staging.  Dense 16-bit models only.
+// per-request exchange buffers and the step-state staging.  Dense models only.
 static int batch_init(adp_model* m) {
   adp_model::Batch& B = m->bt;
   if (B.init_rc != 1) return B.init_rc;
   const adp_config& c = m->cfg;
   B.init_rc = ADP_ERR_UNSUPPORTED_CONFIG;
-  if (c.n_experts != 0 || (c.weight_dtype != ADP_F16 && c.weight_dtype != ADP_BF16)) return B.init_rc;
+  if (c.n_experts != 0) return B.init_rc;  // experts differ per request
   const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim;
   cudaDeviceProp prop;
   CK(cudaGetDeviceProperties(&prop, m->device));

@@ -433,7 +433,8 @@ def emit_batch(args, cfg, res, world):
     prof = f"decode_batch_kernel_{WORKLOAD}-b{nb}.md"
     tr = profiled_traffic(src, prof)
     line = {
-        "metric": f"batch-{nb} decode tokens/s, all requests (2.3B fp16); achieved HBM GB/s vs GB300 peak",
+        "metric": f"batch-{nb} decode tokens/s, all requests (2.3B, {WORKLOADS[WORKLOAD]['weights'].split(';')[0]}); "
+                  "achieved HBM GB/s vs GB300 peak",
         "value": round(value, 2),
         "unit": "tokens/s",
         "n_gpus": world,

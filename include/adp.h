@@ -233,9 +233,9 @@ int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t
  *  dev_logits: optional DEVICE float array [nb][vocab].
  * nb must be in [1, adp_max_batch]: the batched kernel keeps nb copies of the widest GEMV input
  * vector (fp32) in shared memory beside a weight ring of at least two slots, and merges head h of
- * request r on CTA G-1-(r*n_heads+h).  Dense fp16 / bf16 models only (experts differ per request;
- * e4m3 layer matrices are not batched): others get ADP_ERR_UNSUPPORTED_CONFIG.  Synchronises;
- * errors as adp_decode_step (a device error is sticky and no cache grows). */
+ * request r on CTA G-1-(r*n_heads+h).  Dense models only (16-bit or e4m3 layer matrices; experts
+ * differ per request, so MoE models get ADP_ERR_UNSUPPORTED_CONFIG).  Synchronises; errors as
+ * adp_decode_step (a device error is sticky and no cache grows). */
 int adp_decode_batch(adp_model* m, adp_kv* const* kvs, int32_t nb, const int32_t* tokens,
                      const adp_sampling* sampling, int32_t* next_tokens, float* dev_logits);
 /* n batched steps in one launch, each request feeding itself the token it chose.

@@ -93,7 +93,7 @@ def test_tiny_batch_mixes_greedy_and_sampled_requests(torch_cuda):
     _check_batch(synth.get_config("tiny"), [9, 30, 3], 16, temperatures=[0.7, 0.0, 0.7])
 
 
-@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16"])
+@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "dense-2.3b-e4m3"])
 def test_shrunk_workloads_batch_bit_exact(torch_cuda, name):
     cfg = synth.shrink(synth.get_config(name))
     _check_batch(cfg, [8, 35], 10)
