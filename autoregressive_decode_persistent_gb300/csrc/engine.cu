@@ -960,7 +960,7 @@ extern "C" int adp_debug_tc_gemm(int32_t bf16, int32_t M, int32_t N, int32_t K, 
   uint8_t *at = nullptr, *wt = nullptr;
   int32_t* err = nullptr;
   int32_t herr = 0;
-  cudaError_t e = cudaMalloc(&at, tc_tiled_bytes(M, K, 128));
+  cudaError_t e = cudaMalloc(&at, tc_tiled_bytes(M, K, 256));  // rows padded to the GEMM's 256-row blocks
   if (e == cudaSuccess) e = cudaMalloc(&wt, tc_tiled_bytes(N, K, 256));
   if (e == cudaSuccess) e = cudaMalloc(&err, 4);
   if (e == cudaSuccess) e = cudaMemset(err, 0, 4);
@@ -1095,10 +1095,11 @@ static int tc_reserve(adp_model* m, int P) {
   const size_t nmax = (size_t)std::max((c.n_heads + 2 * c.n_kv_heads) * c.head_dim, 2 * c.d_ff);
   int rc;
   if ((rc = m->alloc(&T.tokens, (size_t)P)) || (rc = m->alloc(&T.x, (size_t)P * c.d_model)) ||
-      (rc = m->alloc(&T.A, tc_tiled_bytes(P, kmax, 128))) || (rc = m->alloc(&T.C, (size_t)P * nmax)))
+      (rc = m->alloc(&T.A, tc_tiled_bytes(P, kmax, 256))) || (rc = m->alloc(&T.C, (size_t)P * nmax)))
     return rc;
-  // the A tiles' padding (rows beyond P, columns beyond a GEMM's K) must read as zero
-  CK(cudaMemsetAsync(T.A, 0, tc_tiled_bytes(P, kmax, 128), m->stream));
+  // the A tiles' padding (rows beyond P up to the GEMM's 256-row blocks, columns beyond a GEMM's
+  // K) must read as zero
+  CK(cudaMemsetAsync(T.A, 0, tc_tiled_bytes(P, kmax, 256), m->stream));
   T.cap = P;
   return ADP_OK;
 }
@@ -1115,7 +1116,7 @@ extern "C" int adp_debug_tc_gemm_time(adp_model* m, int32_t which, int32_t M, in
   const uint8_t* Wt[4] = {m->tc.wqkv[0], m->tc.wo[0], m->tc.wgu[0], m->tc.wdown[0]};
   const int kmax = std::max({c.d_model, c.n_heads * c.head_dim, c.d_ff});
   // operand A: every element 0x3C3C (about 1.06 in f16, 0.0115 in bf16)
-  CK(cudaMemsetAsync(m->tc.A, 0x3C, tc_tiled_bytes(M, kmax, 128), m->stream));
+  CK(cudaMemsetAsync(m->tc.A, 0x3C, tc_tiled_bytes(M, kmax, 256), m->stream));
   const int bf16 = tc_operand_bf16(c);
   cudaEvent_t e0, e1;
   CK(cudaEventCreate(&e0));
@@ -1132,7 +1133,7 @@ extern "C" int adp_debug_tc_gemm_time(adp_model* m, int32_t which, int32_t M, in
   CK(cudaEventElapsedTime(&ms, e0, e1));
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
-  CK(cudaMemsetAsync(m->tc.A, 0, tc_tiled_bytes(M, kmax, 128), m->stream));  // padding reads as zero again
+  CK(cudaMemsetAsync(m->tc.A, 0, tc_tiled_bytes(M, kmax, 256), m->stream));  // padding reads as zero again
   CK(cudaStreamSynchronize(m->stream));
   *ms_per_launch = ms / (float)reps;
   return ADP_OK;

@@ -11,10 +11,12 @@
 // GEMM: C[M, N] (fp32) = A[M, K] W[N, K]^T with A and W 16-bit (f16 or bf16), both K-major.
 // Operands live in global memory already in the tensor cores' shared-memory layout (tc.cuh),
 // tile by tile: A as 128-row x 64-K tiles, W as 256-row x 64-K tiles, each contiguous, so one
-// 1-D bulk copy stages a tile.  One CTA computes one 128 x 256 output tile: warp 0 streams the
-// K-tiles through a 4-stage ring, one thread of warp 1 issues 4 MMAs (K = 16 each) per stage into
-// a 128-lane x 256-column fp32 accumulator in TMEM and commits each stage back to the producer,
-// and all four warps read the accumulator out (lane = row) when the last MMA has completed.
+// 1-D bulk copy stages a tile.  One CTA computes one 256 x 256 output tile as two 128-row halves:
+// warp 0 streams the K-tiles (two A tiles and one W tile, 64 KB) through a 3-stage ring, one
+// thread of warp 1 issues 8 MMAs (2 halves x K = 16 x 4) per stage into two 128-lane x 256-column
+// fp32 accumulators in TMEM (all 512 columns) and commits each stage back to the producer, and
+// all four warps read the accumulators out (lane = row) when the last MMA has completed.  Each
+// staged W tile thus serves 256 output rows, which halves the bytes staged per flop for W.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -24,10 +26,11 @@
 
 namespace adp {
 
-constexpr int kTcBM = 128, kTcBN = 256, kTcStages = 4;
-constexpr uint32_t kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
+constexpr int kTcBM = 128, kTcBN = 256, kTcStages = 3;
+constexpr int kTcHalves = 2;                        // a CTA's output tile: 2 x 128 rows x 256 columns
+constexpr uint32_t kTcABytes = kTcBM * kTcBK * 2;  // 16 KB: one 128-row A tile
 constexpr uint32_t kTcBBytes = kTcBN * kTcBK * 2;  // 32 KB
-constexpr uint32_t kTcStageBytes = kTcABytes + kTcBBytes;
+constexpr uint32_t kTcStageBytes = kTcHalves * kTcABytes + kTcBBytes;  // 64 KB
 constexpr size_t kTcSmem = (size_t)kTcStages * kTcStageBytes + 256;
 
 template <int BF16, bool ADD>
@@ -43,8 +46,8 @@ __global__ void __launch_bounds__(128, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // M-blocks vary fastest across the grid, so the CTAs running together share few weight tiles
   // (each read from DRAM once, then from L2) and every A tile stays in L2
-  const int mb = blockIdx.x, nb = blockIdx.y;
-  const uint8_t* Ab = A + (size_t)mb * k_tiles * kTcABytes;
+  const int mb = blockIdx.x, nb = blockIdx.y;  // rows 256 mb .., columns 256 nb ..
+  const uint8_t* Ab = A + (size_t)(kTcHalves * mb) * k_tiles * kTcABytes;  // 128-row tile 2 mb (2 mb + 1 follows)
   const uint8_t* Wb = W + (size_t)nb * k_tiles * kTcBBytes;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
@@ -56,7 +59,7 @@ __global__ void __launch_bounds__(128, 1)
     mbar_fence_init();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, kTcBN);
+    tmem_alloc(tmem_slot, kTcHalves * kTcBN);  // two 128 x 256 fp32 accumulators: all 512 columns
     tmem_relinquish();
   }
   tc_fence_before();
@@ -76,8 +79,9 @@ __global__ void __launch_bounds__(128, 1)
       }
       uint8_t* dst = smem + (size_t)s * kTcStageBytes;
       mbar_arrive_expect_tx(&full[s], kTcStageBytes);
-      tma_load_1d(dst, Ab + (size_t)ks * kTcABytes, kTcABytes, &full[s], pol);
-      tma_load_1d(dst + kTcABytes, Wb + (size_t)ks * kTcBBytes, kTcBBytes, &full[s], pol);
+      for (int hh = 0; hh < kTcHalves; ++hh)
+        tma_load_1d(dst + hh * kTcABytes, Ab + ((size_t)hh * k_tiles + ks) * kTcABytes, kTcABytes, &full[s], pol);
+      tma_load_1d(dst + kTcHalves * kTcABytes, Wb + (size_t)ks * kTcBBytes, kTcBBytes, &full[s], pol);
       issued = ks + 1;
     }
     // no bulk copy may still be writing this CTA's shared memory when it exits
@@ -95,11 +99,13 @@ __global__ void __launch_bounds__(128, 1)
       }
       tc_fence_after();
       const uint32_t a0 = smem_u32(smem + (size_t)s * kTcStageBytes);
-      const uint32_t b0 = a0 + kTcABytes;
+      const uint32_t b0 = a0 + kTcHalves * kTcABytes;
 #pragma unroll
-      for (int kk = 0; kk < kTcBK / 16; ++kk)
-        tc_mma_f16(tmem, tc_smem_desc(a0 + kk * 256, 128, 1024), tc_smem_desc(b0 + kk * 256, 128, 1024), idesc,
-                   ks > 0 || kk > 0);
+      for (int hh = 0; hh < kTcHalves; ++hh)
+#pragma unroll
+        for (int kk = 0; kk < kTcBK / 16; ++kk)
+          tc_mma_f16(tmem + hh * kTcBN, tc_smem_desc(a0 + hh * kTcABytes + kk * 256, 128, 1024),
+                     tc_smem_desc(b0 + kk * 256, 128, 1024), idesc, ks > 0 || kk > 0);
       tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
     }
     tc_commit(done);
@@ -111,10 +117,11 @@ __global__ void __launch_bounds__(128, 1)
   const bool ok = mbar_wait(done, 0, &never, wait_ns) && !*ab;
   tc_fence_after();
   if (ok) {
-    const int row = mb * kTcBM + warp * 32 + lane;
+   for (int hh = 0; hh < kTcHalves; ++hh) {
+    const int row = (kTcHalves * mb + hh) * kTcBM + warp * 32 + lane;
     for (int c0 = 0; c0 < kTcBN; c0 += 32) {
       float v[32];
-      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(hh * kTcBN + c0), v);
       const int col0 = nb * kTcBN + c0;
       if (row < m_valid) {
         float* dst = C + (size_t)row * ldc + col0;
@@ -138,12 +145,13 @@ __global__ void __launch_bounds__(128, 1)
         }
       }
     }
+   }
   } else if (threadIdx.x == 0) {
     atomicCAS(err, 0, DE_PIPELINE_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) tmem_dealloc(tmem, kTcBN);
+  if (warp == 2) tmem_dealloc(tmem, kTcHalves * kTcBN);
 }
 
 // Row-major 16-bit [rows, K] (row stride ld elements) -> tiles of `tile_rows` x 64 in the
@@ -180,7 +188,7 @@ cudaError_t tc_tile(const uint16_t* src, int rows, int K, int ld, uint8_t* dst, 
 cudaError_t tc_gemm(int bf16, bool add, const uint8_t* A_tiled, const uint8_t* W_tiled, float* C, int ldc, int M,
                     int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st) {
   const int k_tiles = (K + kTcBK - 1) / kTcBK;
-  const dim3 grid((M + kTcBM - 1) / kTcBM, (N + kTcBN - 1) / kTcBN);
+  const dim3 grid((M + kTcHalves * kTcBM - 1) / (kTcHalves * kTcBM), (N + kTcBN - 1) / kTcBN);
   const void* k = bf16 ? (add ? (const void*)tc_gemm_kernel<1, true> : (const void*)tc_gemm_kernel<1, false>)
                        : (add ? (const void*)tc_gemm_kernel<0, true> : (const void*)tc_gemm_kernel<0, false>);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
@@ -190,6 +198,8 @@ cudaError_t tc_gemm(int bf16, bool add, const uint8_t* A_tiled, const uint8_t* W
   return cudaLaunchKernel(k, grid, dim3(128), args, kTcSmem, st);
 }
 
+// (A operands are allocated with their rows padded to 256 (tc_tiled_bytes(rows, K, 256)): a CTA stages
+// two 128-row tiles.)
 size_t tc_tiled_bytes(int rows, int K, int tile_rows) {
   const size_t rows_pad = (size_t)(rows + tile_rows - 1) / tile_rows * tile_rows;
   const size_t k_tiles = (size_t)(K + kTcBK - 1) / kTcBK;
