@@ -552,8 +552,9 @@ __global__ void __launch_bounds__(128) tc_flash_kernel(const float* __restrict__
       for (int j = 0; j < 32; ++j)
         if (kb0 + c0 + j <= pos) mb = fmaxf(mb, v[j] * scale);
     }
+    // exponentials by CUDA's fast intrinsic (ex2-based; this path is checked within tolerances)
     const float mn = fmaxf(m, mb);
-    const float corr = expf(m - mn);
+    const float corr = __expf(m - mn);
     float ps = 0.0f;
 #pragma unroll
     for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -562,7 +563,7 @@ __global__ void __launch_bounds__(128) tc_flash_kernel(const float* __restrict__
       uint16_t e[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float p = kb0 + c0 + j <= pos ? expf(v[j] * scale - mn) : 0.0f;
+        const float p = kb0 + c0 + j <= pos ? __expf(v[j] * scale - mn) : 0.0f;
         ps += p;
         e[j] = tc_store16(p, KV_BF16);
       }
