@@ -7,9 +7,9 @@
 // Pages followed (title, section):
 //  "標準GPUによるリアルタイムLLM推論：リクエストあたり3,000トークン/秒": the batch-1 step streams every
 //   active weight once per token ("GPU推論の速度制限要因：メモリ帯域幅"); one GPU-resident program
-//   runs the whole decode path ("Kog Inference Engineの特徴とイノベーション");
-//  "Real-time LLM inference on standard GPUs" discussion thread (the authors' reply on batching):
-//   small batches are planned, traded against per-request speed.
+//   runs the whole decode path ("Kog Inference Engineの特徴とイノベーション"); in the translated
+//   comment thread the authors answer on batching: small batches are planned, traded against
+//   per-request speed.
 //
 // Per request the arithmetic is the single-request kernel's contract, unchanged: the same
 // lane-partial dot products in the same order, RMSNorm, RoPE, attention blocks of 32 positions,

@@ -221,9 +221,8 @@ int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t
 
 /* Small-batch decode: nb independent requests of one model advance one token each in ONE
  * persistent launch that streams the weights once for all of them.  The pages' authors plan
- * small batches and warn that they trade against per-request speed ("Real-time LLM inference on
- * standard GPUs" discussion thread, their reply on batching); the pages fix no batched
- * algorithm.  Per request the arithmetic is adp_decode_step's contract unchanged, so request
+ * small batches and warn that they trade against per-request speed ([H], the translated comment
+ * thread, the author reply on batching); the pages fix no batched algorithm.  Per request the arithmetic is adp_decode_step's contract unchanged, so request
  * r's next token, logits and KV row are bit-identical to decoding it alone.
  *  kvs:        HOST array [nb] of distinct caches of this model, each at its own length (the
  *              request's position); each gains one row.
