@@ -486,44 +486,37 @@ __global__ void __launch_bounds__(128) tc_flash_kernel(const float* __restrict__
   uint32_t phase = 0;
   bool ok = true;
   int32_t never = 0;
+  // this thread's key row of the block at kb: K and V, 16-byte chunks (zero past kmax)
+  constexpr int NC = HD / 8;
+  uint4 kreg[NC], vreg[NC];
+  auto load_rows = [&](int kb) {
+    const int kp = kb + t;
+    const bool in = kp <= kmax;
+    const uint4* kr = reinterpret_cast<const uint4*>(kc + (head0 + (in ? kp : 0)) * HD);
+    const uint4* vr = reinterpret_cast<const uint4*>(vc + (head0 + (in ? kp : 0)) * HD);
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      kreg[c] = in ? __ldg(kr + c) : make_uint4(0, 0, 0, 0);
+      vreg[c] = in ? __ldg(vr + c) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  load_rows(0);
   for (int kb0 = 0; kb0 <= kmax && ok; kb0 += 128) {
-    // ---- stage key rows kb0 + t: K as a B operand (keys x head_dim), V transposed (head_dim x keys)
-    {
-      // every load of the row first, then the shared-memory stores (16 loads in flight per thread)
-      const int kp = kb0 + t;
-      const bool in = kp <= kmax;
-      const uint4* kr = reinterpret_cast<const uint4*>(kc + (head0 + (in ? kp : 0)) * HD);
-      const uint4* vr = reinterpret_cast<const uint4*>(vc + (head0 + (in ? kp : 0)) * HD);
-      constexpr int NC = HD / 8;  // 16-byte chunks per row
-      constexpr int HB = NC < 16 ? NC : 16;
+    // ---- stage key rows kb0 + t (held in registers since the previous block): K as a B operand
+    // (keys x head_dim), V transposed (head_dim x keys); then start loading the next block's rows,
+    // which arrive while this block's MMAs and softmax run
 #pragma unroll
-      for (int c0 = 0; c0 < NC; c0 += HB) {
-        uint4 kv[HB];
+    for (int c = 0; c < NC; ++c) {
+      const int k = c * 8;
+      *reinterpret_cast<uint4*>(Ks + (k / kTcBK) * QK_TILE + tc_tile_offset(t, k % kTcBK)) = kreg[c];
+      const uint32_t w4[4] = {vreg[c].x, vreg[c].y, vreg[c].z, vreg[c].w};
 #pragma unroll
-        for (int c = 0; c < HB; ++c) kv[c] = in ? __ldg(kr + c0 + c) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int c = 0; c < HB; ++c) {
-          const int k = (c0 + c) * 8;
-          *reinterpret_cast<uint4*>(Ks + (k / kTcBK) * QK_TILE + tc_tile_offset(t, k % kTcBK)) = kv[c];
-        }
-      }
-#pragma unroll
-      for (int c0 = 0; c0 < NC; c0 += HB) {
-        uint4 vv[HB];
-#pragma unroll
-        for (int c = 0; c < HB; ++c) vv[c] = in ? __ldg(vr + c0 + c) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int c = 0; c < HB; ++c) {
-          const int k = (c0 + c) * 8;
-          const uint32_t w4[4] = {vv[c].x, vv[c].y, vv[c].z, vv[c].w};
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint16_t e = (uint16_t)(w4[j >> 1] >> ((j & 1) * 16));
-            *reinterpret_cast<uint16_t*>(Vt + (t / kTcBK) * VT_TILE + tc_tile_offset(k + j, t % kTcBK)) = e;
-          }
-        }
+      for (int j = 0; j < 8; ++j) {
+        const uint16_t e = (uint16_t)(w4[j >> 1] >> ((j & 1) * 16));
+        *reinterpret_cast<uint16_t*>(Vt + (t / kTcBK) * VT_TILE + tc_tile_offset(k + j, t % kTcBK)) = e;
       }
     }
+    load_rows(kb0 + 128);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
