@@ -92,6 +92,7 @@ struct adp_model {
     int32_t* tokens = nullptr;
     float* x = nullptr;
     uint8_t* A = nullptr;
+    uint8_t* A2 = nullptr;
     float* C = nullptr;
   } tc;
   // Batched decode (set up at the first batched call): per-request buffers for kMaxBatch
@@ -966,7 +967,7 @@ extern "C" int adp_debug_tc_gemm(int32_t bf16, int32_t M, int32_t N, int32_t K, 
   if (e == cudaSuccess) e = cudaMemset(err, 0, 4);
   if (e == cudaSuccess) e = tc_tile((const uint16_t*)A, M, K, K, at, 128, 0);
   if (e == cudaSuccess) e = tc_tile((const uint16_t*)W, N, K, K, wt, 256, 0);
-  if (e == cudaSuccess) e = tc_gemm(bf16, false, at, wt, C, N, M, N, K, err, 1000000000ull, 0);
+  if (e == cudaSuccess) e = tc_gemm(bf16, TC_STORE, at, wt, C, N, M, N, K, err, 1000000000ull, 0);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = cudaMemcpy(&herr, err, 4, cudaMemcpyDeviceToHost);
   cudaFree(at);
@@ -1080,7 +1081,7 @@ static int tc_reserve(adp_model* m, int P) {
   adp_model::TcState& T = m->tc;
   if (P <= T.cap) return ADP_OK;
   CK(cudaStreamSynchronize(m->stream));
-  for (void* q : {(void*)T.tokens, (void*)T.x, (void*)T.A, (void*)T.C}) {
+  for (void* q : {(void*)T.tokens, (void*)T.x, (void*)T.A, (void*)T.A2, (void*)T.C}) {
     if (!q) continue;
     m->allocs.erase(std::remove(m->allocs.begin(), m->allocs.end(), q), m->allocs.end());
     cudaFree(q);
@@ -1088,18 +1089,21 @@ static int tc_reserve(adp_model* m, int P) {
   T.tokens = nullptr;
   T.x = nullptr;
   T.A = nullptr;
+  T.A2 = nullptr;
   T.C = nullptr;
   T.cap = 0;
   const adp_config& c = m->cfg;
-  const int kmax = std::max({c.d_model, c.n_heads * c.head_dim, c.d_ff});
-  const size_t nmax = (size_t)std::max((c.n_heads + 2 * c.n_kv_heads) * c.head_dim, 2 * c.d_ff);
+  const int kmax = std::max(c.d_model, c.n_heads * c.head_dim);
+  const size_t nmax = (size_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
   int rc;
   if ((rc = m->alloc(&T.tokens, (size_t)P)) || (rc = m->alloc(&T.x, (size_t)P * c.d_model)) ||
-      (rc = m->alloc(&T.A, tc_tiled_bytes(P, kmax, 256))) || (rc = m->alloc(&T.C, (size_t)P * nmax)))
+      (rc = m->alloc(&T.A, tc_tiled_bytes(P, kmax, 256))) || (rc = m->alloc(&T.A2, tc_tiled_bytes(P, c.d_ff, 256))) ||
+      (rc = m->alloc(&T.C, (size_t)P * nmax)))
     return rc;
   // the A tiles' padding (rows beyond P up to the GEMM's 256-row blocks, columns beyond a GEMM's
   // K) must read as zero
   CK(cudaMemsetAsync(T.A, 0, tc_tiled_bytes(P, kmax, 256), m->stream));
+  CK(cudaMemsetAsync(T.A2, 0, tc_tiled_bytes(P, c.d_ff, 256), m->stream));
   T.cap = P;
   return ADP_OK;
 }
@@ -1114,26 +1118,35 @@ extern "C" int adp_debug_tc_gemm_time(adp_model* m, int32_t which, int32_t M, in
   const int N[4] = {qkv_n, c.d_model, 2 * c.d_ff, c.d_model};
   const int K[4] = {c.d_model, c.n_heads * c.head_dim, c.d_model, c.d_ff};
   const uint8_t* Wt[4] = {m->tc.wqkv[0], m->tc.wo[0], m->tc.wgu[0], m->tc.wdown[0]};
-  const int kmax = std::max({c.d_model, c.n_heads * c.head_dim, c.d_ff});
-  // operand A: every element 0x3C3C (about 1.06 in f16, 0.0115 in bf16)
+  // each GEMM as the prefill runs it: QKV stores into C, Wo and down add into the residual x,
+  // gate|up writes SwiGLU into the down GEMM's A tiles; down reads those tiles
+  const int kmax = std::max(c.d_model, c.n_heads * c.head_dim);
+  const int mode[4] = {TC_STORE, TC_ADD, TC_SWIGLU, TC_ADD};
+  const uint8_t* Ain[4] = {m->tc.A, m->tc.A, m->tc.A, m->tc.A2};
+  float* out[4] = {m->tc.C, m->tc.x, reinterpret_cast<float*>(m->tc.A2), m->tc.x};
+  const int ldo[4] = {qkv_n, c.d_model, (c.d_ff + 63) / 64, c.d_model};
+  // operands A: every element 0x3C3C (about 1.06 in f16, 0.0115 in bf16); the residual zero
   CK(cudaMemsetAsync(m->tc.A, 0x3C, tc_tiled_bytes(M, kmax, 256), m->stream));
+  CK(cudaMemsetAsync(m->tc.A2, 0x3C, tc_tiled_bytes(M, c.d_ff, 256), m->stream));
+  CK(cudaMemsetAsync(m->tc.x, 0, (size_t)M * c.d_model * 4, m->stream));
   const int bf16 = tc_operand_bf16(c);
   cudaEvent_t e0, e1;
   CK(cudaEventCreate(&e0));
   CK(cudaEventCreate(&e1));
-  CK(tc_gemm(bf16, false, m->tc.A, Wt[which], m->tc.C, N[which], M, N[which], K[which], m->p.err, 1000000000ull,
-             m->stream));  // warm-up
+  const int w = which;
+  CK(tc_gemm(bf16, mode[w], Ain[w], Wt[w], out[w], ldo[w], M, N[w], K[w], m->p.err, 1000000000ull, m->stream));
   CK(cudaEventRecord(e0, m->stream));
   for (int i = 0; i < reps; ++i)
-    CK(tc_gemm(bf16, false, m->tc.A, Wt[which], m->tc.C, N[which], M, N[which], K[which], m->p.err, 1000000000ull,
-               m->stream));
+    CK(tc_gemm(bf16, mode[w], Ain[w], Wt[w], out[w], ldo[w], M, N[w], K[w], m->p.err, 1000000000ull, m->stream));
   CK(cudaEventRecord(e1, m->stream));
   CK(cudaEventSynchronize(e1));
   float ms = 0.0f;
   CK(cudaEventElapsedTime(&ms, e0, e1));
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
-  CK(cudaMemsetAsync(m->tc.A, 0, tc_tiled_bytes(M, kmax, 256), m->stream));  // padding reads as zero again
+  // padding reads as zero again
+  CK(cudaMemsetAsync(m->tc.A, 0, tc_tiled_bytes(M, kmax, 256), m->stream));
+  CK(cudaMemsetAsync(m->tc.A2, 0, tc_tiled_bytes(M, c.d_ff, 256), m->stream));
   CK(cudaStreamSynchronize(m->stream));
   *ms_per_launch = ms / (float)reps;
   return ADP_OK;
@@ -1181,6 +1194,7 @@ extern "C" int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_toke
     a.rope_sin = m->p.rope_sin;
     a.x = m->tc.x;
     a.A = m->tc.A;
+    a.A2 = m->tc.A2;
     a.C = m->tc.C;
     a.err = m->p.err;
     a.wait_ns = std::max<uint64_t>(m->p.wait_ns, 1000000000ull);

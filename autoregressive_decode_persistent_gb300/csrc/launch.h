@@ -29,9 +29,15 @@ cudaError_t decode_batch_launch(const Params& p, int ph0, int ph1, int grid, siz
                                 cudaStream_t stream);
 size_t batch_ctl_bytes();
 
-// Tensor-core GEMM of the prefill path (prefill.cu): C[M, N] (=, or += when add) A W^T with A and
-// W in the tiled tensor-core layout (A: 128-row tiles, W: 256-row tiles, 64 K-elements each).
-cudaError_t tc_gemm(int bf16, bool add, const uint8_t* A_tiled, const uint8_t* W_tiled, float* C, int ldc, int M,
+// Epilogues of the prefill GEMM: C = A W^T (fp32, streaming stores), C += A W^T (the fp32
+// residual), or SwiGLU of interleaved (gate, up) output column pairs rounded into the next GEMM's
+// A tiles (C is then that tile buffer and ldc its number of 64-wide K tiles).
+enum TcMode : int { TC_STORE = 0, TC_ADD = 1, TC_SWIGLU = 2 };
+
+// Tensor-core GEMM of the prefill path (prefill.cu): A W^T with A and W in the tiled tensor-core
+// layout (A: 128-row tiles, rows allocated in multiples of 256; W: 256-row tiles; 64 K-elements
+// each), epilogue `mode`.
+cudaError_t tc_gemm(int bf16, int mode, const uint8_t* A_tiled, const uint8_t* W_tiled, float* C, int ldc, int M,
                     int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st);
 // Row-major 16-bit [rows, K] (row stride ld) -> tiles of tile_rows x 64, zero-padded.
 cudaError_t tc_tile(const uint16_t* src, int rows, int K, int ld, uint8_t* dst, int tile_rows, cudaStream_t st);
@@ -55,14 +61,16 @@ struct TcPrefill {
   const float* rope_cos;
   const float* rope_sin;
   float* x;        // device [P, d]
-  uint8_t* A;      // device A-operand tiles, rows padded to 128, K up to max(d, hq*hd, ff)
-  float* C;        // device [P, max((hq + 2 hkv) hd, 2 ff)]
+  uint8_t* A;      // device A-operand tiles, rows padded to 256, K up to max(d, hq*hd)
+  uint8_t* A2;     // device A-operand tiles of the down GEMM (K = ff), written by gate|up's epilogue
+  float* C;        // device [P, (hq + 2 hkv) hd]: the QKV GEMM's output
   int32_t* err;
   uint64_t wait_ns;
 };
 cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st);
 // Phase P's tiles of the decode image -> one GEMM weight operand in 256-row tiles (dst cleared
-// beforehand; rows in the order of the caller's matrices).
+// beforehand; rows in the order of the caller's matrices, except gate|up: gate_i and up_i
+// interleaved as rows 2i and 2i + 1).
 // e4m3 phases (eb 1) are dequantised with their row scales (sa, sb, sc: the q/k/v, gate/up or single
 // matrix's tables) into the operand type (out_bf16); 16-bit phases are copied.
 cudaError_t tc_unpack(const uint8_t* image, const PhaseDesc& P, int G, int hd, int hq, int hkv, int ff, uint8_t* dst,

@@ -33,7 +33,16 @@ constexpr uint32_t kTcBBytes = kTcBN * kTcBK * 2;  // 32 KB
 constexpr uint32_t kTcStageBytes = kTcHalves * kTcABytes + kTcBBytes;  // 64 KB
 constexpr size_t kTcSmem = (size_t)kTcStages * kTcStageBytes + 256;
 
-template <int BF16, bool ADD>
+// 16-bit storage of an fp32 value (RNE): bf16 or f16.
+__device__ __forceinline__ uint16_t tc_store16(float v, int bf16) {
+  if (bf16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return __half_as_ushort(__float2half_rn(v));
+}
+
+
+// MODE TC_SWIGLU: C is the A-operand tile buffer of the next GEMM (K = n_valid / 2) and ldc its
+// number of 64-wide K tiles; output columns 2i and 2i + 1 are gate_i and up_i.
+template <int BF16, int MODE>
 __global__ void __launch_bounds__(128, 1)
     tc_gemm_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ W, float* C, int ldc, int m_valid,
                    int n_valid, int k_tiles, int32_t* err, uint64_t wait_ns) {
@@ -123,13 +132,36 @@ __global__ void __launch_bounds__(128, 1)
       float v[32];
       tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(hh * kTcBN + c0), v);
       const int col0 = nb * kTcBN + c0;
+      if (MODE == TC_SWIGLU) {
+        // 16 (gate, up) pairs -> h = silu(g) u, two 16-byte runs of the next GEMM's A tile row
+        const int i0 = col0 / 2, ffw = n_valid / 2;
+        if (row < m_valid) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            if (i0 + 8 * q >= ffw) continue;
+            uint16_t e[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float g = v[16 * q + 2 * k], u = v[16 * q + 2 * k + 1];
+              e[k] = tc_store16(g / (1.0f + __expf(-g)) * u, BF16);
+            }
+            const int i = i0 + 8 * q;
+            uint8_t* H = reinterpret_cast<uint8_t*>(C);
+            *reinterpret_cast<uint4*>(H + ((size_t)(row / kTcBM) * ldc + i / kTcBK) * kTcABytes +
+                                      tc_tile_offset(row % kTcBM, i % kTcBK)) =
+                make_uint4(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16),
+                           e[4] | ((uint32_t)e[5] << 16), e[6] | ((uint32_t)e[7] << 16));
+          }
+        }
+        continue;
+      }
       if (row < m_valid) {
         float* dst = C + (size_t)row * ldc + col0;
         if (col0 + 32 <= n_valid && (ldc & 3) == 0) {  // whole 16-byte groups
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
             float4 o = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-            if (ADD) {
+            if (MODE == TC_ADD) {
               const float4 a = *reinterpret_cast<const float4*>(dst + j);
               o = make_float4(__fadd_rn(a.x, o.x), __fadd_rn(a.y, o.y), __fadd_rn(a.z, o.z), __fadd_rn(a.w, o.w));
               *reinterpret_cast<float4*>(dst + j) = o;
@@ -141,7 +173,7 @@ __global__ void __launch_bounds__(128, 1)
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (col0 + j < n_valid) dst[j] = ADD ? __fadd_rn(dst[j], v[j]) : v[j];
+            if (col0 + j < n_valid) dst[j] = MODE == TC_ADD ? __fadd_rn(dst[j], v[j]) : v[j];
         }
       }
     }
@@ -185,12 +217,16 @@ cudaError_t tc_tile(const uint16_t* src, int rows, int K, int ld, uint8_t* dst, 
   return cudaGetLastError();
 }
 
-cudaError_t tc_gemm(int bf16, bool add, const uint8_t* A_tiled, const uint8_t* W_tiled, float* C, int ldc, int M,
+cudaError_t tc_gemm(int bf16, int mode, const uint8_t* A_tiled, const uint8_t* W_tiled, float* C, int ldc, int M,
                     int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st) {
   const int k_tiles = (K + kTcBK - 1) / kTcBK;
   const dim3 grid((M + kTcHalves * kTcBM - 1) / (kTcHalves * kTcBM), (N + kTcBN - 1) / kTcBN);
-  const void* k = bf16 ? (add ? (const void*)tc_gemm_kernel<1, true> : (const void*)tc_gemm_kernel<1, false>)
-                       : (add ? (const void*)tc_gemm_kernel<0, true> : (const void*)tc_gemm_kernel<0, false>);
+  const void* kernels[2][3] = {
+      {(const void*)tc_gemm_kernel<0, TC_STORE>, (const void*)tc_gemm_kernel<0, TC_ADD>,
+       (const void*)tc_gemm_kernel<0, TC_SWIGLU>},
+      {(const void*)tc_gemm_kernel<1, TC_STORE>, (const void*)tc_gemm_kernel<1, TC_ADD>,
+       (const void*)tc_gemm_kernel<1, TC_SWIGLU>}};
+  const void* k = kernels[bf16 ? 1 : 0][mode];
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
   if (e != cudaSuccess) return e;
   void* args[] = {(void*)&A_tiled, (void*)&W_tiled, (void*)&C, (void*)&ldc, (void*)&M, (void*)&N, (void*)&k_tiles,
@@ -228,14 +264,8 @@ __device__ __forceinline__ int tc_logical_row(const PhaseDesc& P, int u, int j, 
     }
     return base + (uu / half) * hd + uu % half + j * half;
   }
-  if (P.kind == PK_GU) return u + j * ff;
+  if (P.kind == PK_GU) return 2 * u + j;  // gate_u, up_u side by side: the GEMM's SwiGLU epilogue pairs them
   return u * P.unit_rows + j;
-}
-
-// 16-bit storage of an fp32 value (RNE): bf16 or f16.
-__device__ __forceinline__ uint16_t tc_store16(float v, int bf16) {
-  if (bf16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-  return __half_as_ushort(__float2half_rn(v));
 }
 
 // Per-row scale of an e4m3 layer matrix for logical row `row` of phase P's GEMM operand (the
@@ -247,7 +277,7 @@ __device__ __forceinline__ float tc_row_scale(const PhaseDesc& P, int row, int h
     if (row < (hq + hkv) * hd) return sb[row - hq * hd];
     return sc[row - (hq + hkv) * hd];
   }
-  if (P.kind == PK_GU) return row < ff ? sa[row] : sb[row - ff];
+  if (P.kind == PK_GU) return (row & 1) ? sb[row >> 1] : sa[row >> 1];
   return sa[row];
 }
 
@@ -369,18 +399,6 @@ __global__ void tc_rope_kv_kernel(float* C, int ldc, int P, int pos0, int L, int
   }
 }
 
-// h = silu(g) * u from the gate|up GEMM's output, rounded into the A-operand tiles of down.
-__global__ void tc_swiglu_kernel(const float* __restrict__ C, int ldc, int P, int ff, int bf16, uint8_t* A,
-                                 int k_tiles) {
-  const int t = blockIdx.x;
-  if (t >= P) return;
-  const float* row = C + (size_t)t * ldc;
-  for (int i = threadIdx.x; i < ff; i += blockDim.x) {
-    const float g = row[i], u = row[ff + i];
-    *reinterpret_cast<uint16_t*>(A + tc_a_offset(t, i, k_tiles)) = tc_store16(g / (1.0f + expf(-g)) * u, bf16);
-  }
-}
-
 cudaError_t tc_flash(const TcPrefill& a, int qkv_n, int L, int kt_att, cudaStream_t st);
 
 cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st) {
@@ -395,23 +413,22 @@ cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st) {
     tc_rmsnorm_kernel<<<(P + 7) / 8, 256, 0, st>>>(a.x, (const uint16_t*)a.attn_norm[L], P, a.d, a.eps, a.bf16, a.A,
                                                    kt_d);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = tc_gemm(a.bf16, false, a.A, a.wqkv[L], a.C, qkv_n, P, qkv_n, a.d, a.err, a.wait_ns, st)) != cudaSuccess)
+    if ((e = tc_gemm(a.bf16, TC_STORE, a.A, a.wqkv[L], a.C, qkv_n, P, qkv_n, a.d, a.err, a.wait_ns, st)) != cudaSuccess)
       return e;
     tc_rope_kv_kernel<<<P, 256, 0, st>>>(a.C, qkv_n, P, a.pos0, L, a.hq, a.hkv, a.hd, a.max_ctx, a.rope_cos,
                                          a.rope_sin, a.kvdt, a.kc, a.vc);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = tc_flash(a, qkv_n, L, kt_att, st)) != cudaSuccess) return e;
-    if ((e = tc_gemm(a.bf16, true, a.A, a.wo[L], a.x, a.d, P, a.d, a.hq * a.hd, a.err, a.wait_ns, st)) != cudaSuccess)
+    if ((e = tc_gemm(a.bf16, TC_ADD, a.A, a.wo[L], a.x, a.d, P, a.d, a.hq * a.hd, a.err, a.wait_ns, st)) != cudaSuccess)
       return e;
     tc_rmsnorm_kernel<<<(P + 7) / 8, 256, 0, st>>>(a.x, (const uint16_t*)a.ffn_norm[L], P, a.d, a.eps, a.bf16, a.A,
                                                    kt_d);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = tc_gemm(a.bf16, false, a.A, a.wgu[L], a.C, 2 * a.ff, P, 2 * a.ff, a.d, a.err, a.wait_ns, st)) !=
-        cudaSuccess)
+    // gate|up with SwiGLU in the epilogue: h goes straight into the down GEMM's A tiles (A2)
+    if ((e = tc_gemm(a.bf16, TC_SWIGLU, a.A, a.wgu[L], reinterpret_cast<float*>(a.A2), kt_ff, P, 2 * a.ff, a.d,
+                     a.err, a.wait_ns, st)) != cudaSuccess)
       return e;
-    tc_swiglu_kernel<<<P, 256, 0, st>>>(a.C, 2 * a.ff, P, a.ff, a.bf16, a.A, kt_ff);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = tc_gemm(a.bf16, true, a.A, a.wdown[L], a.x, a.d, P, a.d, a.ff, a.err, a.wait_ns, st)) != cudaSuccess)
+    if ((e = tc_gemm(a.bf16, TC_ADD, a.A2, a.wdown[L], a.x, a.d, P, a.d, a.ff, a.err, a.wait_ns, st)) != cudaSuccess)
       return e;
   }
   return cudaSuccess;
