@@ -93,7 +93,8 @@ struct adp_model {
     float* x = nullptr;
     uint8_t* A = nullptr;
     uint8_t* A2 = nullptr;
-    float* C = nullptr;
+    uint8_t* Qt = nullptr;  // query tiles of the attention kernel
+    float* C = nullptr;     // fp32 QKV output (the timing hook's plain-store QKV GEMM only)
   } tc;
   // Batched decode (set up at the first batched call): per-request buffers for kMaxBatch
   // requests, the per-request step state and KV cache tables, and the shared-memory layout of
@@ -1081,7 +1082,7 @@ static int tc_reserve(adp_model* m, int P) {
   adp_model::TcState& T = m->tc;
   if (P <= T.cap) return ADP_OK;
   CK(cudaStreamSynchronize(m->stream));
-  for (void* q : {(void*)T.tokens, (void*)T.x, (void*)T.A, (void*)T.A2, (void*)T.C}) {
+  for (void* q : {(void*)T.tokens, (void*)T.x, (void*)T.A, (void*)T.A2, (void*)T.Qt, (void*)T.C}) {
     if (!q) continue;
     m->allocs.erase(std::remove(m->allocs.begin(), m->allocs.end(), q), m->allocs.end());
     cudaFree(q);
@@ -1090,6 +1091,7 @@ static int tc_reserve(adp_model* m, int P) {
   T.x = nullptr;
   T.A = nullptr;
   T.A2 = nullptr;
+  T.Qt = nullptr;
   T.C = nullptr;
   T.cap = 0;
   const adp_config& c = m->cfg;
@@ -1098,8 +1100,10 @@ static int tc_reserve(adp_model* m, int P) {
   int rc;
   if ((rc = m->alloc(&T.tokens, (size_t)P)) || (rc = m->alloc(&T.x, (size_t)P * c.d_model)) ||
       (rc = m->alloc(&T.A, tc_tiled_bytes(P, kmax, 256))) || (rc = m->alloc(&T.A2, tc_tiled_bytes(P, c.d_ff, 256))) ||
+      (rc = m->alloc(&T.Qt, (size_t)c.n_heads * tc_tiled_bytes(P, c.head_dim, 128))) ||
       (rc = m->alloc(&T.C, (size_t)P * nmax)))
     return rc;
+  CK(cudaMemsetAsync(T.Qt, 0, (size_t)c.n_heads * tc_tiled_bytes(P, c.head_dim, 128), m->stream));
   // the A tiles' padding (rows beyond P up to the GEMM's 256-row blocks, columns beyond a GEMM's
   // K) must read as zero
   CK(cudaMemsetAsync(T.A, 0, tc_tiled_bytes(P, kmax, 256), m->stream));
@@ -1195,7 +1199,7 @@ extern "C" int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_toke
     a.x = m->tc.x;
     a.A = m->tc.A;
     a.A2 = m->tc.A2;
-    a.C = m->tc.C;
+    a.Qt = m->tc.Qt;
     a.err = m->p.err;
     a.wait_ns = std::max<uint64_t>(m->p.wait_ns, 1000000000ull);
     CK(tc_prefill(a, m->stream));

@@ -32,13 +32,24 @@ size_t batch_ctl_bytes();
 // Epilogues of the prefill GEMM: C = A W^T (fp32, streaming stores), C += A W^T (the fp32
 // residual), or SwiGLU of interleaved (gate, up) output column pairs rounded into the next GEMM's
 // A tiles (C is then that tile buffer and ldc its number of 64-wide K tiles).
-enum TcMode : int { TC_STORE = 0, TC_ADD = 1, TC_SWIGLU = 2 };
+enum TcMode : int { TC_STORE = 0, TC_ADD = 1, TC_SWIGLU = 2, TC_QKV = 3 };
+
+// The QKV GEMM's epilogue (TC_QKV): RoPE on the q and k columns of each token (position pos0 + row),
+// q rounded into the attention kernel's query tiles, k and v rounded into the KV cache rows.
+struct TcQkvEpi {
+  const float* rope_cos;  // [max_ctx][hd/2]
+  const float* rope_sin;
+  uint16_t* kc;           // [L][hkv][max_ctx][hd]
+  uint16_t* vc;
+  uint8_t* qt;            // [hq][ceil(P/128)][hd/64 tiles of 128 x 64]: queries in the core-matrix layout
+  int pos0, L, hq, hkv, hd, max_ctx, kvdt, n_tb;
+};
 
 // Tensor-core GEMM of the prefill path (prefill.cu): A W^T with A and W in the tiled tensor-core
 // layout (A: 128-row tiles, rows allocated in multiples of 256; W: 256-row tiles; 64 K-elements
 // each), epilogue `mode`.
 cudaError_t tc_gemm(int bf16, int mode, const uint8_t* A_tiled, const uint8_t* W_tiled, float* C, int ldc, int M,
-                    int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st);
+                    int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st, const TcQkvEpi* qkv = nullptr);
 // Row-major 16-bit [rows, K] (row stride ld) -> tiles of tile_rows x 64, zero-padded.
 cudaError_t tc_tile(const uint16_t* src, int rows, int K, int ld, uint8_t* dst, int tile_rows, cudaStream_t st);
 size_t tc_tiled_bytes(int rows, int K, int tile_rows);
@@ -63,7 +74,7 @@ struct TcPrefill {
   float* x;        // device [P, d]
   uint8_t* A;      // device A-operand tiles, rows padded to 256, K up to max(d, hq*hd)
   uint8_t* A2;     // device A-operand tiles of the down GEMM (K = ff), written by gate|up's epilogue
-  float* C;        // device [P, (hq + 2 hkv) hd]: the QKV GEMM's output
+  uint8_t* Qt;     // device query tiles written by the QKV GEMM's epilogue (see TcQkvEpi)
   int32_t* err;
   uint64_t wait_ns;
 };

@@ -45,7 +45,7 @@ __device__ __forceinline__ uint16_t tc_store16(float v, int bf16) {
 template <int BF16, int MODE>
 __global__ void __launch_bounds__(128, 1)
     tc_gemm_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ W, float* C, int ldc, int m_valid,
-                   int n_valid, int k_tiles, int32_t* err, uint64_t wait_ns) {
+                   int n_valid, int k_tiles, int32_t* err, uint64_t wait_ns, const __grid_constant__ TcQkvEpi qe) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kTcStages * kTcStageBytes);
   uint64_t* empty = full + kTcStages;
@@ -128,6 +128,68 @@ __global__ void __launch_bounds__(128, 1)
   if (ok) {
    for (int hh = 0; hh < kTcHalves; ++hh) {
     const int row = (kTcHalves * mb + hh) * kTcBM + warp * 32 + lane;
+    if (MODE == TC_QKV) {
+      // whole heads lie in one 256-column tile; RoPE pairs (i, i + hd/2) of q and k, then q into
+      // the query tiles and k, v into the cache rows of position pos0 + row
+      const int hd = qe.hd, half = hd / 2;
+      const int pos = qe.pos0 + row;
+      const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(hh * kTcBN);
+      for (int hb = 0; hb < kTcBN; hb += hd) {
+        const int head = (nb * kTcBN + hb) / hd;  // of the q heads, then the k heads, then the v heads
+        if (head >= qe.hq + 2 * qe.hkv) break;
+        for (int ci = 0; ci < half; ci += 32) {
+          float a[32], b[32];
+          tmem_ld32(tbase + (uint32_t)(hb + ci), a);
+          tmem_ld32(tbase + (uint32_t)(hb + half + ci), b);
+          if (row >= m_valid) continue;
+          uint16_t ea[32], eb[32];
+          if (head >= qe.hq + qe.hkv) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              ea[j] = round_kv(a[j], qe.kvdt);
+              eb[j] = round_kv(b[j], qe.kvdt);
+            }
+          } else {
+            const float* cs = qe.rope_cos + (size_t)pos * half + ci;
+            const float* sn = qe.rope_sin + (size_t)pos * half + ci;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float c = __ldg(cs + j), s = __ldg(sn + j);
+              const float y0 = fmaf(a[j], c, -(b[j] * s)), y1 = fmaf(b[j], c, a[j] * s);
+              ea[j] = round_kv(y0, qe.kvdt);
+              eb[j] = round_kv(y1, qe.kvdt);
+            }
+          }
+          if (head < qe.hq) {
+            uint8_t* qb = qe.qt + ((size_t)head * qe.n_tb + row / kTcBM) * (size_t)(hd / kTcBK) * kTcABytes;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              const int ka = ci + j, kb = ci + half + j;
+              *reinterpret_cast<uint4*>(qb + (ka / kTcBK) * kTcABytes + tc_tile_offset(row % kTcBM, ka % kTcBK)) =
+                  make_uint4(ea[j] | ((uint32_t)ea[j + 1] << 16), ea[j + 2] | ((uint32_t)ea[j + 3] << 16),
+                             ea[j + 4] | ((uint32_t)ea[j + 5] << 16), ea[j + 6] | ((uint32_t)ea[j + 7] << 16));
+              *reinterpret_cast<uint4*>(qb + (kb / kTcBK) * kTcABytes + tc_tile_offset(row % kTcBM, kb % kTcBK)) =
+                  make_uint4(eb[j] | ((uint32_t)eb[j + 1] << 16), eb[j + 2] | ((uint32_t)eb[j + 3] << 16),
+                             eb[j + 4] | ((uint32_t)eb[j + 5] << 16), eb[j + 6] | ((uint32_t)eb[j + 7] << 16));
+            }
+          } else {
+            const bool is_v = head >= qe.hq + qe.hkv;
+            const int g = is_v ? head - qe.hq - qe.hkv : head - qe.hq;
+            uint16_t* dst = (is_v ? qe.vc : qe.kc) + (((size_t)qe.L * qe.hkv + g) * qe.max_ctx + pos) * hd;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              *reinterpret_cast<uint4*>(dst + ci + j) =
+                  make_uint4(ea[j] | ((uint32_t)ea[j + 1] << 16), ea[j + 2] | ((uint32_t)ea[j + 3] << 16),
+                             ea[j + 4] | ((uint32_t)ea[j + 5] << 16), ea[j + 6] | ((uint32_t)ea[j + 7] << 16));
+              *reinterpret_cast<uint4*>(dst + ci + half + j) =
+                  make_uint4(eb[j] | ((uint32_t)eb[j + 1] << 16), eb[j + 2] | ((uint32_t)eb[j + 3] << 16),
+                             eb[j + 4] | ((uint32_t)eb[j + 5] << 16), eb[j + 6] | ((uint32_t)eb[j + 7] << 16));
+            }
+          }
+        }
+      }
+      continue;
+    }
     for (int c0 = 0; c0 < kTcBN; c0 += 32) {
       float v[32];
       tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(hh * kTcBN + c0), v);
@@ -218,19 +280,24 @@ cudaError_t tc_tile(const uint16_t* src, int rows, int K, int ld, uint8_t* dst, 
 }
 
 cudaError_t tc_gemm(int bf16, int mode, const uint8_t* A_tiled, const uint8_t* W_tiled, float* C, int ldc, int M,
-                    int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st) {
+                    int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st, const TcQkvEpi* qkv) {
   const int k_tiles = (K + kTcBK - 1) / kTcBK;
   const dim3 grid((M + kTcHalves * kTcBM - 1) / (kTcHalves * kTcBM), (N + kTcBN - 1) / kTcBN);
-  const void* kernels[2][3] = {
+  const void* kernels[2][4] = {
       {(const void*)tc_gemm_kernel<0, TC_STORE>, (const void*)tc_gemm_kernel<0, TC_ADD>,
-       (const void*)tc_gemm_kernel<0, TC_SWIGLU>},
+       (const void*)tc_gemm_kernel<0, TC_SWIGLU>, (const void*)tc_gemm_kernel<0, TC_QKV>},
       {(const void*)tc_gemm_kernel<1, TC_STORE>, (const void*)tc_gemm_kernel<1, TC_ADD>,
-       (const void*)tc_gemm_kernel<1, TC_SWIGLU>}};
+       (const void*)tc_gemm_kernel<1, TC_SWIGLU>, (const void*)tc_gemm_kernel<1, TC_QKV>}};
+  TcQkvEpi qe{};
+  if (mode == TC_QKV) {
+    if (!qkv) return cudaErrorInvalidValue;
+    qe = *qkv;
+  }
   const void* k = kernels[bf16 ? 1 : 0][mode];
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
   if (e != cudaSuccess) return e;
-  void* args[] = {(void*)&A_tiled, (void*)&W_tiled, (void*)&C, (void*)&ldc, (void*)&M, (void*)&N, (void*)&k_tiles,
-                  (void*)&err, (void*)&wait_ns};
+  void* args[] = {(void*)&A_tiled, (void*)&W_tiled, (void*)&C,   (void*)&ldc,     (void*)&M, (void*)&N,
+                  (void*)&k_tiles, (void*)&err,    (void*)&wait_ns, (void*)&qe};
   return cudaLaunchKernel(k, grid, dim3(128), args, kTcSmem, st);
 }
 
@@ -364,41 +431,6 @@ __global__ void tc_rmsnorm_kernel(const float* __restrict__ x, const uint16_t* _
   }
 }
 
-// RoPE on the q and k columns of C (token t at position pos0 + t), the rotated k and the v
-// columns rounded into the KV cache rows of that position.
-__global__ void tc_rope_kv_kernel(float* C, int ldc, int P, int pos0, int L, int hq, int hkv, int hd, int max_ctx,
-                                  const float* __restrict__ rcos, const float* __restrict__ rsin, int kvdt,
-                                  uint16_t* kc, uint16_t* vc) {
-  const int t = blockIdx.x;
-  const int pos = pos0 + t;
-  const int half = hd / 2;
-  float* row = C + (size_t)t * ldc;
-  const int pairs = (hq + hkv) * half;
-  for (int p = threadIdx.x; p < pairs + hkv * half; p += blockDim.x) {
-    if (p < pairs) {
-      const int head = p / half, i = p % half;
-      float* a = row + head * hd + i;  // q heads, then k heads (columns hq*hd ..)
-      const float cs = rcos[(size_t)pos * half + i], sn = rsin[(size_t)pos * half + i];
-      const float x0 = a[0], x1 = a[half];
-      const float y0 = fmaf(x0, cs, -(x1 * sn)), y1 = fmaf(x1, cs, x0 * sn);
-      if (head < hq) {
-        a[0] = y0;
-        a[half] = y1;
-      } else {
-        const size_t o = (((size_t)L * hkv + (head - hq)) * max_ctx + pos) * hd + i;
-        kc[o] = round_kv(y0, kvdt);
-        kc[o + half] = round_kv(y1, kvdt);
-      }
-    } else {
-      const int q = p - pairs, g = q / half, i = q % half;
-      const float* v = row + (hq + hkv) * hd + g * hd;
-      const size_t o = (((size_t)L * hkv + g) * max_ctx + pos) * hd + i;
-      vc[o] = round_kv(v[i], kvdt);
-      vc[o + half] = round_kv(v[i + half], kvdt);
-    }
-  }
-}
-
 cudaError_t tc_flash(const TcPrefill& a, int qkv_n, int L, int kt_att, cudaStream_t st);
 
 cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st) {
@@ -413,11 +445,12 @@ cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st) {
     tc_rmsnorm_kernel<<<(P + 7) / 8, 256, 0, st>>>(a.x, (const uint16_t*)a.attn_norm[L], P, a.d, a.eps, a.bf16, a.A,
                                                    kt_d);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = tc_gemm(a.bf16, TC_STORE, a.A, a.wqkv[L], a.C, qkv_n, P, qkv_n, a.d, a.err, a.wait_ns, st)) != cudaSuccess)
+    // QKV with RoPE and the cache writes in the epilogue; queries into the attention's tiles
+    const TcQkvEpi qe{a.rope_cos, a.rope_sin, a.kc, a.vc, a.Qt, a.pos0, L, a.hq, a.hkv, a.hd, a.max_ctx, a.kvdt,
+                      (P + kTcBM - 1) / kTcBM};
+    if ((e = tc_gemm(a.bf16, TC_QKV, a.A, a.wqkv[L], nullptr, 0, P, qkv_n, a.d, a.err, a.wait_ns, st, &qe)) !=
+        cudaSuccess)
       return e;
-    tc_rope_kv_kernel<<<P, 256, 0, st>>>(a.C, qkv_n, P, a.pos0, L, a.hq, a.hkv, a.hd, a.max_ctx, a.rope_cos,
-                                         a.rope_sin, a.kvdt, a.kc, a.vc);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = tc_flash(a, qkv_n, L, kt_att, st)) != cudaSuccess) return e;
     if ((e = tc_gemm(a.bf16, TC_ADD, a.A, a.wo[L], a.x, a.d, P, a.d, a.hq * a.hd, a.err, a.wait_ns, st)) != cudaSuccess)
       return e;
@@ -439,7 +472,8 @@ cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st) {
 namespace adp {
 
 // Causal attention of the prompt on the tensor cores, flash style.  CTA = query head h x 128
-// consecutive prompt tokens (thread t = token t0 + t = TMEM lane t), 128 threads.  Per block of
+// consecutive prompt tokens (thread t = token t0 + t = TMEM lane t), 128 threads; its queries come
+// ready in the core-matrix layout from the QKV GEMM's epilogue.  Per block of
 // 128 cached keys: the K block and the V block (transposed) are staged in shared memory in the
 // K-major core-matrix layout; S = Q K^T (128 x 128, K = head_dim) accumulates in TMEM columns
 // [0, 128); each thread turns its row of S into the online softmax (scale, causal mask, running
@@ -447,7 +481,7 @@ namespace adp {
 // rescales its row of O (TMEM columns [128, 128 + head_dim)) by exp(m_old - m_new); then
 // O += P V (K = 128 keys).  At the end O / l is rounded into the A-operand tiles of Wo.
 template <int HD, int KVDT>
-__global__ void __launch_bounds__(128) tc_flash_kernel(const float* __restrict__ C, int ldc, int P, int pos0, int L,
+__global__ void __launch_bounds__(128) tc_flash_kernel(const uint8_t* __restrict__ qt, int n_tb, int P, int pos0, int L,
                                                       int hq, int hkv, int max_ctx, float scale,
                                                       const uint16_t* __restrict__ kc,
                                                       const uint16_t* __restrict__ vc, int out_bf16, uint8_t* A,
@@ -475,18 +509,12 @@ __global__ void __launch_bounds__(128) tc_flash_kernel(const float* __restrict__
     tmem_alloc(tmem_slot, 256);
     tmem_relinquish();
   }
-  // Q row t (post-RoPE, fp32 in C) rounded to the KV type
+  // the query tiles of (head h, tokens t0 ..), written by the QKV GEMM's epilogue (post-RoPE, KV type)
   {
-    const int tok = t0 + t;
+    const uint4* src = reinterpret_cast<const uint4*>(qt + ((size_t)h * n_tb + t0 / 128) * KT * QK_TILE);
+    uint4* dst = reinterpret_cast<uint4*>(Qs);
 #pragma unroll 4
-    for (int k = 0; k < HD; k += 8) {
-      uint16_t e[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) e[j] = tok < P ? tc_store16(C[(size_t)tok * ldc + h * HD + k + j], KV_BF16) : 0;
-      *reinterpret_cast<uint4*>(Qs + (k / kTcBK) * QK_TILE + tc_tile_offset(t, k % kTcBK)) =
-          make_uint4(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16), e[4] | ((uint32_t)e[5] << 16),
-                     e[6] | ((uint32_t)e[7] << 16));
-    }
+    for (int i = t; i < KT * (int)QK_TILE / 16; i += 128) dst[i] = __ldg(src + i);
   }
   tc_fence_before();
   __syncthreads();
@@ -645,7 +673,8 @@ cudaError_t tc_flash_launch(const TcPrefill& a, int qkv_n, int L, int kt_att, cu
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   tc_flash_kernel<HD, KVDT><<<dim3(a.hq, (a.P + 127) / 128), 128, smem, st>>>(
-      a.C, qkv_n, a.P, a.pos0, L, a.hq, a.hkv, a.max_ctx, a.scale, a.kc, a.vc, a.bf16, a.A, kt_att, a.err, a.wait_ns);
+      a.Qt, (a.P + 127) / 128, a.P, a.pos0, L, a.hq, a.hkv, a.max_ctx, a.scale, a.kc, a.vc, a.bf16, a.A, kt_att,
+      a.err, a.wait_ns);
   return cudaGetLastError();
 }
 

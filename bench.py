@@ -565,9 +565,9 @@ def emit_prefill(args, cfg, res, world):
             "prefill_tokens_per_s": round(res["P"] / (res["dev_ms"] * 1e-3), 1),
             "decode_path_ttft_ms": round(res["step_ms"], 1),
             "speedup_over_decode_path": round(res["step_ms"] / res["dev_ms"], 2),
-            "kernel": f"per layer 4 tcgen05 GEMMs (M {M}; SwiGLU in the gate|up epilogue), tcgen05 flash "
-                      "attention, and norm and RoPE/KV kernels; the last prompt token through the persistent "
-                      "decode kernel",
+            "kernel": f"per layer 4 tcgen05 GEMMs (M {M}; RoPE and the KV write in the QKV epilogue, SwiGLU in "
+                      "the gate|up epilogue), tcgen05 flash attention and 2 norm kernels; the last prompt token "
+                      "through the persistent decode kernel",
             "ctas": res["ctas"],
             "l2": "inputs larger than L2: 4.69 GB of weight tiles and the growing KV cache per prefill",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -580,7 +580,7 @@ def emit_prefill(args, cfg, res, world):
                                f"{res['gemm_ms'] * 1e3:.1f} us per launch, 20 launches timed alone",
                      "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({peak_kind}, burst; f16 has the same nominal "
                                     "tensor rate as bf16)"},
-        "gpu_launches": 1 + 8 * L + 1,  # embedding; per layer 2 norms, 4 GEMMs, RoPE/KV, attention; the last token
+        "gpu_launches": 1 + 7 * L + 1,  # embedding; per layer 2 norms, 4 GEMMs, attention; the last token
         **({"profiling_variant": f"{L} layers (not the workload)"} if args.layers else {}),
         "clocks": res["clocks"],
         "kernel_source": kernel_source_hash(("prefill.cu", "tc.cuh", "device.cuh", "plan.h")),

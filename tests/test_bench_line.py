@@ -85,4 +85,4 @@ def test_prefill_line_has_the_contract_keys(capsys):
     assert line["higher_is_better"] is False and line["unit"] == "ms" and line["value"] == pytest.approx(31.0)
     assert line["roofline"]["bound"] == "tensor" and line["roofline"]["unit"] == "TFLOP/s"
     assert line["roofline"]["achieved"] == pytest.approx(2.0 * 3583 * 19456 * 2560 / 0.333e-3 / 1e12, rel=1e-3)
-    assert line["gpu_launches"] == 1 + 8 * 25 + 1
+    assert line["gpu_launches"] == 1 + 7 * 25 + 1
