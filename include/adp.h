@@ -204,8 +204,9 @@ int adp_sync(adp_model* m);                          /* synchronise the stream; 
 
 /* Tensor-core prefill: the prompt's first n-1 tokens go through every layer as dense GEMMs on the
  * tcgen05 tensor cores ([P, d] x [d, n] contractions, fp32 accumulation in TMEM, activations
- * rounded to the weights' 16-bit type before each GEMM), with RMSNorm, RoPE, causal attention
- * (fp32, CUDA cores) and SwiGLU between them; their K/V rows go into the cache.  The last token
+ * rounded to the weights' 16-bit type before each GEMM; RoPE with the K/V cache write and SwiGLU
+ * in the GEMMs' epilogues), causal attention as flash-style tcgen05 MMAs (online softmax in fp32)
+ * and RMSNorm kernels between them; their K/V rows go into the cache.  The last token
  * then runs as one adp_decode_step, whose logits and next token are returned.  The pages time
  * time-to-first-token ("標準GPUによるリアルタイムLLM推論：リクエストあたり3,000トークン/秒",
  * §"単一リクエストLLMデコード速度の重要性") but fix no prefill algorithm; this path is not the
@@ -308,8 +309,9 @@ int adp_debug_skip_publication(adp_model* m, int32_t cta, int32_t phase);
  * array.  Tiles the operands into temporary device buffers, runs, synchronises the device. */
 int adp_debug_tc_gemm(int32_t bf16, int32_t M, int32_t N, int32_t K, const void* A, const void* W, float* C);
 /* Benchmark hook of the tensor-core prefill: times `reps` back-to-back launches of one of the
- * model's prefill GEMMs (which: 0 QKV, 1 Wo, 2 gate|up, 3 down; layer 0's weights) on M tokens of
- * a constant operand, with CUDA events on the model's stream; *ms_per_launch receives the mean. */
+ * model's prefill GEMMs (which: 0 QKV (with a plain fp32 store epilogue here), 1 Wo, 2 gate|up
+ * (with its SwiGLU epilogue), 3 down; layer 0's weights) on M tokens of a constant operand, with
+ * CUDA events on the model's stream; *ms_per_launch receives the mean. */
 int adp_debug_tc_gemm_time(adp_model* m, int32_t which, int32_t M, int32_t reps, float* ms_per_launch);
 
 #if defined(__GNUC__)
