@@ -47,11 +47,16 @@ def weight_bytes_per_token(cfg: dict) -> int:
     attention, router, norms and top-k experts with their fp32 scales), the LM head, one
     embedding row and the final norm gain."""
     c = cfg
-    eb = _EB[c["weight_dtype"]]
-    q8 = c["weight_dtype"] == "e4m3"       # e4m3 layer matrices carry an fp32 scale per row
+    fp4 = c["weight_dtype"] == "nvfp4"    # half a byte per element + one e4m3 scale per 16 elements
+    q8 = c["weight_dtype"] in ("e4m3", "nvfp4")  # layer matrices with an fp32 scale per row
     ee = _EB[c.get("embed_dtype") or c["weight_dtype"]]  # embedding, LM head, norm gains
+
+    def mb(n_elems: int) -> int:
+        """Bytes of n_elems layer-matrix elements."""
+        return n_elems * 9 // 16 if fp4 else n_elems * _EB[c["weight_dtype"]]
+
     d, hq, hkv, hd, V = c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"], c["vocab"]
-    attn = (hq * hd * d * 2 + 2 * hkv * hd * d) * eb + ((hq * hd + 2 * hkv * hd + d) * 4 if q8 else 0)
+    attn = mb(hq * hd * d * 2 + 2 * hkv * hd * d) + ((hq * hd + 2 * hkv * hd + d) * 4 if q8 else 0)
     norms = 2 * d * ee
     if c["n_experts"]:
         f, k = c["d_expert"], c["top_k"]
@@ -60,7 +65,7 @@ def weight_bytes_per_token(cfg: dict) -> int:
         experts = k * (3 * f * d * xeb + (2 * f + d) * 4)
         ffn = router + experts
     else:
-        ffn = 3 * c["d_ff"] * d * eb + ((2 * c["d_ff"] + d) * 4 if q8 else 0)
+        ffn = mb(3 * c["d_ff"] * d) + ((2 * c["d_ff"] + d) * 4 if q8 else 0)
     per_layer = attn + norms + ffn
     head = V * d * ee
     return c["n_layers"] * per_layer + head + d * ee + d * ee

@@ -36,6 +36,29 @@ def e4m3_decode(q: np.ndarray) -> np.ndarray:
     return s * val
 
 
+def e2m1_decode(q: np.ndarray) -> np.ndarray:
+    """4-bit E2M1 codes (NVFP4 elements): sign bit 3, exponent bits 2..1 (bias 1), one fraction
+    bit; exponent 0 is subnormal."""
+    q = q.astype(np.int64)
+    s = np.where(q & 8, -1.0, 1.0)
+    e = (q >> 1) & 3
+    m = q & 1
+    val = np.where(e == 0, 0.5 * m, (1.0 + m / 2.0) * 2.0 ** (e - 1.0))
+    return s * val
+
+
+def nvfp4_dequant(codes: np.ndarray, bscale: np.ndarray, rscale: np.ndarray) -> np.ndarray:
+    """NVFP4 matrix -> float64: packed e2m1 codes [rows, K/2] (element 2i in the low nibble), e4m3
+    block scales [rows, K/16], fp32 row scales [rows]: w = rowscale * blockscale * element."""
+    rows = codes.shape[0]
+    c = codes.astype(np.int64)
+    q = np.empty((rows, codes.shape[1] * 2), dtype=np.int64)
+    q[:, 0::2] = c & 15
+    q[:, 1::2] = c >> 4
+    blk = np.repeat(e4m3_decode(bscale), 16, axis=1)
+    return rscale.astype(np.float64)[:, None] * blk * e2m1_decode(q)
+
+
 def store_round(x: np.ndarray, dtype: str) -> np.ndarray:
     """float64 -> value after rounding to the KV storage dtype, back in float64."""
     if dtype == "f16":
@@ -76,7 +99,9 @@ def forward(cfg: dict, W: dict, tokens, force=None):
     edt = c.get("embed_dtype") or wdt  # embedding, LM head, norm gains
 
     def mat(Lw, name):
-        """A layer matrix as float64; e4m3 rows times their per-row scale."""
+        """A layer matrix as float64; e4m3 rows times their per-row scale; nvfp4 dequantised."""
+        if wdt == "nvfp4":
+            return nvfp4_dequant(Lw[name], Lw[name + "_bscale"], Lw[name + "_scale"])
         m = widen(Lw[name], wdt)
         return m * Lw[name + "_scale"].astype(np.float64)[:, None] if wdt == "e4m3" else m
 

@@ -41,6 +41,11 @@
  *             ascending order with w_b = exp_c(m_b - M): L = fma(w_b, l_b, L),
  *             O = fma(w_b, o_b, O), out = O / L.
  *    silu(g)*u = (g / (1 + exp_c(-g))) * u.
+ *    nvfp4 layer matrices (4-bit e2m1 codes, one e4m3 scale per 16 consecutive elements of a row,
+ *             one fp32 scale per row): per 8-element vector v the codes' products with x are
+ *             fused-multiply-added into t_v (from 0, elements ascending), then
+ *             partial[v mod 32] = fma(blockscale(v), t_v, partial); fold as dot; times the row
+ *             scale.  (PLAIN: rowscale * sequential sum of (blockscale * code) * x.)
  *    router softmax: sequential sum over experts; top-k ties to the lower index;
  *             gates = P / (sequential sum of the chosen P in choice order);
  *             expert outputs combined by an fma chain in choice order.
@@ -57,7 +62,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_F32 = 3 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_F32 = 3, ORC_NVFP4 = 4 };
 enum { ORC_PLAIN = 0, ORC_EXACT = 1 };
 enum { ORC_OK = 0, ORC_EINVAL = -1, ORC_ECTX = -3, ORC_ENOMEM = -4 };
 
@@ -68,7 +73,7 @@ typedef struct {
   int32_t weight_dtype, kv_dtype;
   int32_t n_experts, top_k, d_expert;
   int32_t router_dtype, expert_dtype;
-  int32_t embed_dtype;  /* embedding, LM head, norm gains when weight_dtype is e4m3 */
+  int32_t embed_dtype;  /* embedding, LM head, norm gains when weight_dtype is e4m3 or nvfp4 */
 } orc_config;
 
 typedef struct {
@@ -77,8 +82,11 @@ typedef struct {
   const void *router;
   const void *e_gate, *e_up, *e_down;
   const float *e_gate_scale, *e_up_scale, *e_down_scale;
-  /* per-output-channel scales of the layer matrices when weight_dtype is e4m3 (else NULL) */
+  /* per-output-channel scales of the layer matrices when weight_dtype is e4m3 or nvfp4 (else NULL) */
   const float *wq_scale, *wk_scale, *wv_scale, *wo_scale, *w_gate_scale, *w_up_scale, *w_down_scale;
+  /* nvfp4 only: e4m3 scale codes of each 16-element block, [rows][K/16] (else NULL); the matrices
+   * then hold two e2m1 codes per byte, element 2i in the low nibble */
+  const uint8_t *wq_bscale, *wk_bscale, *wv_bscale, *wo_bscale, *w_gate_bscale, *w_up_bscale, *w_down_bscale;
 } orc_layer;
 
 typedef struct {
@@ -90,6 +98,7 @@ typedef struct {
 
 static float F16_TABLE[65536];
 static float E4M3_TABLE[256];
+static float E2M1_TABLE[16];
 static int tables_ready = 0;
 
 /* IEEE 754 binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
@@ -113,14 +122,24 @@ static float e4m3_value(uint8_t q) {
   return s ? -v : v;
 }
 
+/* 4-bit floating point E2M1 (the element type of NVFP4): sign bit 3, exponent bits 2..1 (bias 1),
+ * one fraction bit; exponent 0 is subnormal (0 or 0.5); no infinities or NaN. */
+static float e2m1_value(uint8_t q) {
+  int s = (q >> 3) & 1, e = (q >> 1) & 3, m = q & 1;
+  float v = e == 0 ? 0.5f * (float)m : ldexpf((float)(2 + m), e - 2);
+  return s ? -v : v;
+}
+
 void orc_init(void) {
   if (tables_ready) return;
   for (int i = 0; i < 65536; ++i) F16_TABLE[i] = f16_value((uint16_t)i);
   for (int i = 0; i < 256; ++i) E4M3_TABLE[i] = e4m3_value((uint8_t)i);
+  for (int i = 0; i < 16; ++i) E2M1_TABLE[i] = e2m1_value((uint8_t)i);
   tables_ready = 1;
 }
 
 const float* orc_e4m3_table(void) { orc_init(); return E4M3_TABLE; }
+const float* orc_e2m1_table(void) { orc_init(); return E2M1_TABLE; }
 
 static inline float bf16_value(uint16_t b) {
   uint32_t u = (uint32_t)b << 16;
@@ -253,9 +272,45 @@ static inline float dotm(const float* w, const float* x, int K, int VW, int mode
 
 static inline float expm(float x, int mode) { return mode == ORC_EXACT ? orc_exp_c(x) : expf(x); }
 
-/* y[r] = scale[r] * (W[r,:] . x) for r < rows (scale NULL -> 1, applied after the dot). */
-static int gemv(const void* Wt, int dt, int rows, int K, const float* x, const float* scale, float* y, int mode) {
+/* One nvfp4 row (codes: K/2 bytes, bscale: K/16 e4m3 codes) dotted with x, before the row scale. */
+static float dot_nvfp4(const uint8_t* codes, const uint8_t* bscale, const float* x, int K, int mode) {
+  if (mode == ORC_EXACT) {
+    float a[32];
+    for (int l = 0; l < 32; ++l) a[l] = 0.0f;
+    const int nv = K / 8;
+    for (int v = 0; v < nv; ++v) {
+      float t = 0.0f;
+      for (int e = 0; e < 8; ++e) {
+        const int j = v * 8 + e;
+        const uint8_t q = (codes[j >> 1] >> ((j & 1) * 4)) & 15;
+        t = fmaf(E2M1_TABLE[q], x[j], t);
+      }
+      a[v % 32] = fmaf(E4M3_TABLE[bscale[v >> 1]], t, a[v % 32]);
+    }
+    for (int off = 16; off >= 1; off >>= 1)
+      for (int i = 0; i < off; ++i) a[i] = a[i] + a[i + off];
+    return a[0];
+  }
+  float s = 0.0f;
+  for (int j = 0; j < K; ++j) {
+    const uint8_t q = (codes[j >> 1] >> ((j & 1) * 4)) & 15;
+    s = s + (E4M3_TABLE[bscale[j >> 4]] * E2M1_TABLE[q]) * x[j];
+  }
+  return s;
+}
+
+/* y[r] = scale[r] * (W[r,:] . x) for r < rows (scale NULL -> 1, applied after the dot); nvfp4
+ * matrices (dt ORC_NVFP4) also take their block scales. */
+static int gemv(const void* Wt, int dt, int rows, int K, const float* x, const float* scale, const uint8_t* bscale,
+                float* y, int mode) {
   const int VW = 8;
+  if (dt == ORC_NVFP4) {
+    if (!bscale || !scale || K % 16) return ORC_EINVAL;
+#pragma omp parallel for schedule(static)
+    for (int r = 0; r < rows; ++r)
+      y[r] = scale[r] * dot_nvfp4((const uint8_t*)Wt + (size_t)r * (K / 2), bscale + (size_t)r * (K / 16), x, K, mode);
+    return ORC_OK;
+  }
   int fail = 0;
 #pragma omp parallel reduction(| : fail)
   {
@@ -483,8 +538,8 @@ int orc_step(const orc_config* c, const orc_weights* W, void* kc, void* vc, int3
   if (!c || !W || !kc || !vc || !logits) return ORC_EINVAL;
   const int L = c->n_layers, d = c->d_model, hq = c->n_heads, hkv = c->n_kv_heads, hd = c->head_dim;
   const int V = c->vocab, wdt = c->weight_dtype, kvdt = c->kv_dtype;
-  /* with e4m3 layer matrices the embedding, LM head and norm gains keep a 16-bit type */
-  const int edt = wdt == ORC_E4M3 ? c->embed_dtype : wdt;
+  /* with e4m3 or nvfp4 layer matrices the embedding, LM head and norm gains keep a 16-bit type */
+  const int edt = (wdt == ORC_E4M3 || wdt == ORC_NVFP4) ? c->embed_dtype : wdt;
   if (pos < 0 || pos >= c->max_ctx) return ORC_ECTX;
   if (token < 0 || token >= V) return ORC_EINVAL;
   const int moe = c->n_experts > 0;
@@ -515,9 +570,9 @@ int orc_step(const orc_config* c, const orc_weights* W, void* kc, void* vc, int3
     if (trace) memcpy(trace + (size_t)l * d, x, sizeof(float) * (size_t)d);
     /* attention block */
     orc_rmsnorm(x, lw->attn_norm, edt, d, c->rms_eps, mode, xn);
-    if ((rc = gemv(lw->wq, wdt, hq * hd, d, xn, lw->wq_scale, q, mode))) goto done;
-    if ((rc = gemv(lw->wk, wdt, hkv * hd, d, xn, lw->wk_scale, k, mode))) goto done;
-    if ((rc = gemv(lw->wv, wdt, hkv * hd, d, xn, lw->wv_scale, v, mode))) goto done;
+    if ((rc = gemv(lw->wq, wdt, hq * hd, d, xn, lw->wq_scale, lw->wq_bscale, q, mode))) goto done;
+    if ((rc = gemv(lw->wk, wdt, hkv * hd, d, xn, lw->wk_scale, lw->wk_bscale, k, mode))) goto done;
+    if ((rc = gemv(lw->wv, wdt, hkv * hd, d, xn, lw->wv_scale, lw->wv_bscale, v, mode))) goto done;
     for (int h = 0; h < hq; ++h) rope_apply(q + (size_t)h * hd, hd, cs, sn, mode);
     for (int h = 0; h < hkv; ++h) rope_apply(k + (size_t)h * hd, hd, cs, sn, mode);
     for (int h = 0; h < hkv; ++h) {
@@ -534,21 +589,21 @@ int orc_step(const orc_config* c, const orc_weights* W, void* kc, void* vc, int3
       orc_attention_head(q + (size_t)h * hd, (const uint16_t*)kc + base, (const uint16_t*)vc + base, kvdt, pos + 1,
                          hd, scale, mode, att + (size_t)h * hd);
     }
-    if ((rc = gemv(lw->wo, wdt, d, hq * hd, att, lw->wo_scale, y, mode))) goto done;
+    if ((rc = gemv(lw->wo, wdt, d, hq * hd, att, lw->wo_scale, lw->wo_bscale, y, mode))) goto done;
     for (int i = 0; i < d; ++i) x[i] = x[i] + y[i];
     /* feed-forward block */
     orc_rmsnorm(x, lw->ffn_norm, edt, d, c->rms_eps, mode, xn);
     if (!moe) {
-      if ((rc = gemv(lw->w_gate, wdt, ff, d, xn, lw->w_gate_scale, g, mode))) goto done;
-      if ((rc = gemv(lw->w_up, wdt, ff, d, xn, lw->w_up_scale, uu, mode))) goto done;
+      if ((rc = gemv(lw->w_gate, wdt, ff, d, xn, lw->w_gate_scale, lw->w_gate_bscale, g, mode))) goto done;
+      if ((rc = gemv(lw->w_up, wdt, ff, d, xn, lw->w_up_scale, lw->w_up_bscale, uu, mode))) goto done;
       for (int i = 0; i < ff; ++i) g[i] = silu_mul(g[i], uu[i], mode);
-      if ((rc = gemv(lw->w_down, wdt, d, ff, g, lw->w_down_scale, y, mode))) goto done;
+      if ((rc = gemv(lw->w_down, wdt, d, ff, g, lw->w_down_scale, lw->w_down_bscale, y, mode))) goto done;
       for (int i = 0; i < d; ++i) x[i] = x[i] + y[i];
     } else {
       const int E = c->n_experts, K = c->top_k;
       int32_t sel[64];
       float gate[64];
-      if ((rc = gemv(lw->router, c->router_dtype, E, d, xn, NULL, r, mode))) goto done;
+      if ((rc = gemv(lw->router, c->router_dtype, E, d, xn, NULL, NULL, r, mode))) goto done;
       orc_route(r, E, K, mode, sel, gate, NULL);
       if (sel_out) memcpy(sel_out + (size_t)l * K, sel, sizeof(int32_t) * (size_t)K);
       if (gate_out) memcpy(gate_out + (size_t)l * K, gate, sizeof(float) * (size_t)K);
@@ -570,10 +625,10 @@ int orc_step(const orc_config* c, const orc_weights* W, void* kc, void* vc, int3
         const uint8_t* Qg = (const uint8_t*)lw->e_gate + (size_t)e * gu_sz;
         const uint8_t* Qu = (const uint8_t*)lw->e_up + (size_t)e * gu_sz;
         const uint8_t* Qd = (const uint8_t*)lw->e_down + (size_t)e * dn_sz;
-        if ((rc = gemv(Qg, c->expert_dtype, fe, d, xn, lw->e_gate_scale + (size_t)e * fe, g, mode))) goto done;
-        if ((rc = gemv(Qu, c->expert_dtype, fe, d, xn, lw->e_up_scale + (size_t)e * fe, uu, mode))) goto done;
+        if ((rc = gemv(Qg, c->expert_dtype, fe, d, xn, lw->e_gate_scale + (size_t)e * fe, NULL, g, mode))) goto done;
+        if ((rc = gemv(Qu, c->expert_dtype, fe, d, xn, lw->e_up_scale + (size_t)e * fe, NULL, uu, mode))) goto done;
         for (int i = 0; i < fe; ++i) g[i] = silu_mul(g[i], uu[i], mode);
-        if ((rc = gemv(Qd, c->expert_dtype, d, fe, g, lw->e_down_scale + (size_t)e * d, y, mode))) goto done;
+        if ((rc = gemv(Qd, c->expert_dtype, d, fe, g, lw->e_down_scale + (size_t)e * d, NULL, y, mode))) goto done;
         if (mode == ORC_EXACT)
           for (int i = 0; i < d; ++i) acc[i] = fmaf(gate[s], y[i], acc[i]);
         else
@@ -586,7 +641,7 @@ int orc_step(const orc_config* c, const orc_weights* W, void* kc, void* vc, int3
   orc_rmsnorm(x, W->final_norm, edt, d, c->rms_eps, mode, xn);
   {
     const void* head = c->tied_embeddings ? W->tok_emb : W->lm_head;
-    if ((rc = gemv(head, edt, V, d, xn, NULL, logits, mode))) goto done;
+    if ((rc = gemv(head, edt, V, d, xn, NULL, NULL, logits, mode))) goto done;
   }
   if (next) *next = temperature > 0.0f ? orc_sample(logits, V, temperature, u, mode) : orc_argmax(logits, V);
 done:

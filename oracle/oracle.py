@@ -14,7 +14,7 @@ import threading
 import numpy as np
 
 PLAIN, EXACT = 0, 1
-_DT = {"f16": 0, "bf16": 1, "e4m3": 2, "f32": 3}
+_DT = {"f16": 0, "bf16": 1, "e4m3": 2, "f32": 3, "nvfp4": 4}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
@@ -47,7 +47,9 @@ class Layer(ctypes.Structure):
                                                 "w_up", "w_down", "router", "e_gate", "e_up", "e_down",
                                                 "e_gate_scale", "e_up_scale", "e_down_scale",
                                                 "wq_scale", "wk_scale", "wv_scale", "wo_scale",
-                                                "w_gate_scale", "w_up_scale", "w_down_scale")]
+                                                "w_gate_scale", "w_up_scale", "w_down_scale",
+                                                "wq_bscale", "wk_bscale", "wv_bscale", "wo_bscale",
+                                                "w_gate_bscale", "w_up_bscale", "w_down_bscale")]
 
 
 class Weights(ctypes.Structure):
@@ -88,6 +90,8 @@ def lib():
             L.orc_round_bf16.restype = ctypes.c_uint16
             L.orc_e4m3_table.argtypes = []
             L.orc_e4m3_table.restype = ctypes.POINTER(ctypes.c_float)
+            L.orc_e2m1_table.argtypes = []
+            L.orc_e2m1_table.restype = ctypes.POINTER(ctypes.c_float)
             L.orc_init()
             _lib = L
     return _lib
@@ -120,7 +124,8 @@ class OracleModel:
             for k in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down", "router",
                       "e_gate", "e_up", "e_down", "e_gate_scale", "e_up_scale", "e_down_scale",
                       "wq_scale", "wk_scale", "wv_scale", "wo_scale", "w_gate_scale", "w_up_scale",
-                      "w_down_scale"):
+                      "w_down_scale", "wq_bscale", "wk_bscale", "wv_bscale", "wo_bscale", "w_gate_bscale",
+                      "w_up_bscale", "w_down_bscale"):
                 a = _c(Lw.get(k))
                 self._keep.append(a)
                 f[k] = _p(a)

@@ -105,6 +105,45 @@ def normal_e4m3_rows(seed: int, tensor_id: int, rows: int, cols: int, std: float
     return q, s
 
 
+# Magnitudes of the 4-bit E2M1 codes 0..7 (code = 2 * exponent field + fraction bit) and the
+# midpoints between neighbours, for round-to-nearest-even quantisation.
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float32)
+_E2M1_MID = (_E2M1_MAG[:-1] + _E2M1_MAG[1:]) / 2
+
+
+def normal_nvfp4_rows(seed: int, tensor_id: int, rows: int, cols: int, std: float = WEIGHT_STD):
+    """NVFP4 quantisation of seeded N(0, std) fp32 draws (an input recipe, not engine arithmetic):
+    per row s = max|w| / (6 * 448) (fp32); per 16-element block the scale b = e4m3_RNE(max|w_block|
+    / (6 s)); elements q = e2m1_RNE(w / (s * b)), saturating at 6, ties to the even code.
+    Returns (codes [rows, cols/2] uint8, element 2i in the low nibble; block scales [rows, cols/16]
+    uint8 e4m3; row scales [rows] float32)."""
+    assert cols % 16 == 0
+    w = normal_f32(seed, tensor_id, (rows, cols), std)
+    amax = np.abs(w).max(axis=1)
+    s = np.where(amax > 0, amax / np.float32(6.0 * 448.0), np.float32(1.0)).astype(np.float32)
+    blk = np.abs(w.reshape(rows, cols // 16, 16)).max(axis=2)
+    b_codes = f32_to_stored((blk / (np.float32(6.0) * s[:, None])).astype(np.float32), "e4m3")
+    b = _e4m3_values(b_codes)
+    denom = (s[:, None] * b).astype(np.float32)
+    denom16 = np.repeat(denom, 16, axis=1)
+    a = np.where(denom16 > 0, np.abs(w) / np.where(denom16 > 0, denom16, 1), 0).astype(np.float32)
+    k = np.searchsorted(_E2M1_MID, a, side="left")
+    tie = (k < 7) & (a == _E2M1_MID[np.minimum(k, 6)])
+    k = np.where(tie & (k % 2 == 1), k + 1, k)
+    k = np.minimum(k, 7)
+    code = (k | np.where((w < 0) & (k > 0), 8, 0)).astype(np.uint8)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
+    return packed, b_codes.astype(np.uint8), s
+
+
+def _e4m3_values(q: np.ndarray) -> np.ndarray:
+    """fp32 values of e4m3 codes (finite codes only: the quantiser never stores NaN)."""
+    q = q.astype(np.int64)
+    e, m = (q >> 3) & 15, q & 7
+    v = np.where(e == 0, m * 2.0 ** -9, (8 + m) * 2.0 ** (e - 10.0))
+    return np.where(q & 0x80, -v, v).astype(np.float32)
+
+
 def f32_to_stored(x: np.ndarray, dtype: str) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     if dtype == "e4m3":
@@ -178,9 +217,12 @@ def model_weights(cfg: dict, seed: int | None = None) -> dict:
     W["final_norm"] = ones_stored(d, edt)
 
     def mat(L, name, tid, rows, cols):
-        """A layer matrix in the weight dtype; e4m3 ones come with per-row scales `<name>_scale`."""
+        """A layer matrix in the weight dtype; e4m3 ones come with per-row scales `<name>_scale`,
+        nvfp4 ones with row scales and e4m3 block scales `<name>_bscale` (codes packed)."""
         if wdt == "e4m3":
             L[name], L[name + "_scale"] = normal_e4m3_rows(seed, tid, rows, cols)
+        elif wdt == "nvfp4":
+            L[name], L[name + "_bscale"], L[name + "_scale"] = normal_nvfp4_rows(seed, tid, rows, cols)
         else:
             L[name] = normal_stored(seed, tid, (rows, cols), wdt)
 

@@ -65,6 +65,12 @@ CONFIGS = [
     _cfg(index=5, name="dense-2.3b-e4m3", n_layers=25, d_model=2560, n_heads=20, n_kv_heads=4,
          head_dim=128, d_ff=9728, vocab=32000, max_ctx=4096, weight_dtype="e4m3", embed_dtype="f16",
          prompt_len=512, decode_steps=512),
+    # 6: the 2.3B model with nvfp4 layer weights (e2m1 elements, an e4m3 scale per 16 consecutive
+    #    elements of a row, an fp32 scale per row), embedding / tied LM head and norm gains fp16;
+    #    the oracle and its pins only so far (the decode kernels do not take this type yet)
+    _cfg(index=6, name="dense-2.3b-nvfp4", n_layers=25, d_model=2560, n_heads=20, n_kv_heads=4,
+         head_dim=128, d_ff=9728, vocab=32000, max_ctx=4096, weight_dtype="nvfp4", embed_dtype="f16",
+         prompt_len=512, decode_steps=512),
 ]
 
 BY_NAME = {c["name"]: c for c in CONFIGS}

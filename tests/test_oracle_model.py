@@ -57,7 +57,8 @@ def test_tiny_against_brute_force():
     assert diff < 0.05
 
 
-@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "moe-32x1408-top4-e4m3", "dense-2.3b-e4m3"])
+@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "moe-32x1408-top4-e4m3", "dense-2.3b-e4m3",
+                                  "dense-2.3b-nvfp4"])
 def test_shrunk_workloads_against_brute_force(name):
     cfg = synth.shrink(synth.get_config(name))
     check_against_brute(cfg, 8, 24)

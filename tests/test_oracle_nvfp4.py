@@ -1,0 +1,91 @@
+"""Pins of the oracle's NVFP4 layer matrices (e2m1 elements, an e4m3 scale per 16 elements of a
+row, an fp32 scale per row) and of the seeded quantiser that produces them.
+
+The element values are the format's definition written out (4-bit floating point E2M1: one sign
+bit, two exponent bits with bias 1, one fraction bit, a subnormal for exponent 0); the whole
+model is pinned by the float64 brute force in test_oracle_model.py, which dequantises the stored
+bytes with its own code."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import EXACT, PLAIN, OracleModel, brute
+from oracle.oracle import lib
+
+# every E2M1 code 0..15: +0, 0.5, 1, 1.5, 2, 3, 4, 6, then the same negated
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def test_e2m1_codes_decode_to_the_format_values():
+    t = lib().orc_e2m1_table()
+    got = [t[i] for i in range(16)]
+    assert got == E2M1_VALUES
+    assert [float(x) for x in brute.e2m1_decode(np.arange(16))] == E2M1_VALUES
+    assert np.signbit(got[8])  # code 8 is negative zero
+
+
+@pytest.fixture(scope="module")
+def quantised():
+    return synth.normal_nvfp4_rows(1234, 5, 48, 320)
+
+
+def test_quantiser_layout_and_ranges(quantised):
+    codes, bscale, rscale = quantised
+    assert codes.shape == (48, 160) and bscale.shape == (48, 20) and rscale.shape == (48,)
+    assert codes.dtype == np.uint8 and bscale.dtype == np.uint8 and rscale.dtype == np.float32
+    b = brute.e4m3_decode(bscale)
+    assert np.all(np.isfinite(b)) and np.all(b >= 0) and np.all(b <= 448)
+    w = synth.normal_f32(1234, 5, (48, 320), synth.WEIGHT_STD)
+    # row scale: max |w| of the row over 6 * 448
+    assert np.allclose(rscale.astype(np.float64) * 6 * 448, np.abs(w).max(axis=1), rtol=1e-6)
+
+
+def test_quantiser_picks_a_nearest_code(quantised):
+    """Each dequantised element is (row scale x block scale) times an E2M1 magnitude nearest to
+    the draw's (saturating at 6), with the draw's sign."""
+    codes, bscale, rscale = quantised
+    w = synth.normal_f32(1234, 5, (48, 320), synth.WEIGHT_STD).astype(np.float64)
+    deq = brute.nvfp4_dequant(codes, bscale, rscale)
+    unit = rscale.astype(np.float64)[:, None] * np.repeat(brute.e4m3_decode(bscale), 16, axis=1)
+    a = np.abs(w) / unit
+    q = np.abs(deq) / unit
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], dtype=np.float64)
+    assert np.all(np.min(np.abs(q[..., None] - mags), axis=-1) <= 1e-9)  # q is an E2M1 magnitude
+    nearest_err = np.min(np.abs(a[..., None] - mags), axis=-1)
+    assert np.all(np.abs(a - q) <= nearest_err + 1e-6)
+    assert np.all(np.sign(deq) * np.sign(w) >= 0)
+    # every block's largest element lands at the top of the range (block scale = its max / 6)
+    top = q.reshape(48, 20, 16).max(axis=2)
+    assert np.all((top >= 4) & (top <= 6))
+
+
+def test_ties_go_to_the_even_code():
+    """Midpoints between E2M1 magnitudes round to the code with an even fraction bit."""
+    mid = synth._E2M1_MID
+    k = np.searchsorted(mid, mid, side="left")
+    k = np.where(k % 2 == 1, k + 1, k)
+    assert list(k) == [0, 2, 2, 4, 4, 6, 6]  # 0.25->0, 0.75->1, 1.25->1, 1.75->2, 2.5->2, 3.5->4, 5->4
+
+
+def test_exact_and_plain_modes_agree_within_the_logit_tolerances():
+    cfg = synth.shrink(synth.get_config("dense-2.3b-nvfp4"))
+    W = synth.model_weights(cfg)
+    a, b = OracleModel(cfg, W), OracleModel(cfg, W)
+    for t in synth.prompt(cfg, 6):
+        x = a.step(int(t), EXACT)["logits"].astype(np.float64)
+        y = b.step(int(t), PLAIN)["logits"].astype(np.float64)
+        assert np.max(np.abs(x - y)) <= 2e-2
+        assert np.linalg.norm(x - y) / np.linalg.norm(y) <= 5e-3
+
+
+def test_nvfp4_model_differs_from_its_fp16_source():
+    """The quantisation is real: the nvfp4 model's logits are close to, but not equal to, those of
+    the same seeded model kept in fp16 (a dropped scale or nibble swap would not be close)."""
+    c4 = synth.shrink(synth.get_config("dense-2.3b-nvfp4"))
+    c16 = dict(c4, weight_dtype="f16", embed_dtype=None, index=c4["index"])
+    t = synth.prompt(c4, 4)
+    l4 = brute.forward(c4, synth.model_weights(c4), t)[0]
+    l16 = brute.forward(c16, synth.model_weights(c16), t)[0]
+    d = np.abs(l4 - l16)
+    assert d.max() > 1e-3  # not the same weights
+    assert np.linalg.norm(l4 - l16) / np.linalg.norm(l16) < 0.3  # but the same model, quantised
