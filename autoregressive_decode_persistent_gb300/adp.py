@@ -13,8 +13,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libadp.so")
 
-ADP_F16, ADP_BF16, ADP_E4M3, ADP_F32 = 0, 1, 2, 3
-DTYPES = {"f16": ADP_F16, "bf16": ADP_BF16, "e4m3": ADP_E4M3, "f32": ADP_F32}
+ADP_F16, ADP_BF16, ADP_E4M3, ADP_F32, ADP_NVFP4 = 0, 1, 2, 3, 4
+DTYPES = {"f16": ADP_F16, "bf16": ADP_BF16, "e4m3": ADP_E4M3, "f32": ADP_F32, "nvfp4": ADP_NVFP4}
 
 ADP_OK = 0
 ADP_ERR_INVALID_ARG = -1
@@ -49,7 +49,9 @@ class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up",
                                                 "w_down", "router", "e_gate", "e_up", "e_down", "e_gate_scale",
                                                 "e_up_scale", "e_down_scale", "wq_scale", "wk_scale", "wv_scale",
-                                                "wo_scale", "w_gate_scale", "w_up_scale", "w_down_scale")]
+                                                "wo_scale", "w_gate_scale", "w_up_scale", "w_down_scale",
+                                                "wq_bscale", "wk_bscale", "wv_bscale", "wo_bscale",
+                                                "w_gate_bscale", "w_up_bscale", "w_down_bscale")]
 
 
 class Weights(ctypes.Structure):

@@ -140,7 +140,7 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
                                         uint32_t ew) {
   // every field the loops use lives in registers (the descriptors are in local memory, and each
   // mbarrier asm statement would otherwise force them to be reloaded)
-  constexpr int EB = WDT == DT_E4M3 ? 1 : 2;
+  constexpr int EB = WDT == DT_E4M3 ? 1 : 2;  // element bytes (NVFP4 tiles are addressed apart)
   const int kind = Pd.kind, L = Pd.layer, K = Pd.K, KC = Pd.KC, n_chunks = Pd.n_chunks, upr = Pd.upr;
   const int Kp = (K + 255) & ~255;  // floats per input vector in the split layout
   const int pos = st.pos;
@@ -161,8 +161,9 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
     float acc[SLOTS * ROWS];
 #pragma unroll
     for (int i = 0; i < SLOTS * ROWS; ++i) acc[i] = 0.0f;
-    // e4m3 layer matrices: the per-row scales of this unit, loaded now, applied after the dot
-    constexpr bool kScaled = WDT == DT_E4M3 && SLOTS == 1;
+    // e4m3 and NVFP4 layer matrices: the per-row scales of this unit, loaded now, applied after
+    // the dot
+    constexpr bool kScaled = (WDT == DT_E4M3 || WDT == DT_NVFP4) && SLOTS == 1;
     float sc[ROWS];
     if constexpr (kScaled) {
       if (active) {
@@ -204,17 +205,36 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
         const uint32_t slot_bytes = (uint32_t)m * ROWS * kck * EB;
         const uint8_t* tile = ring + (size_t)slot * kSlotBytes;
         const int xoff = ck * KC;
-        for (int v = lane; v < nvec; v += 32) {
-          float x8[8];
-          if (!XPERSLOT) load_xs8(xbuf, (xoff >> 3) + v, x8);
-#pragma unroll
-          for (int s = 0; s < SLOTS; ++s) {
-            if (XPERSLOT) load_xs8(xbuf + s * Kp, (xoff >> 3) + v, x8);
+        if constexpr (WDT == DT_NVFP4) {
+          // [m * ROWS rows][kck / 2] code bytes, then [m * ROWS][kck / 16] block scales.  Per
+          // 8-element vector: the element products fused-multiply-added from zero, then that sum
+          // times its block scale added into the lane partial.
+          const uint8_t* codes = tile + (size_t)cw * ROWS * (kck >> 1);
+          const uint8_t* bsc = tile + (size_t)m * ROWS * (kck >> 1) + (size_t)cw * ROWS * (kck >> 4);
+          for (int v = lane; v < nvec; v += 32) {
+            float x8[8];
+            load_xs8(xbuf, (xoff >> 3) + v, x8);
 #pragma unroll
             for (int j = 0; j < ROWS; ++j) {
               float w8[8];
-              load8<WDT>(tile + (size_t)s * slot_bytes + ((size_t)(cw * ROWS + j) * kck + (size_t)v * 8) * EB, w8);
-              acc[s * ROWS + j] = fma8(w8, x8, acc[s * ROWS + j]);
+              load8_e2m1(*reinterpret_cast<const uint32_t*>(codes + (size_t)j * (kck >> 1) + (size_t)v * 4), w8);
+              const float bs = e4m3_to_f32(bsc[(size_t)j * (kck >> 4) + (v >> 1)]);
+              acc[j] = fmaf(bs, fma8(w8, x8, 0.0f), acc[j]);
+            }
+          }
+        } else {
+          for (int v = lane; v < nvec; v += 32) {
+            float x8[8];
+            if (!XPERSLOT) load_xs8(xbuf, (xoff >> 3) + v, x8);
+#pragma unroll
+            for (int s = 0; s < SLOTS; ++s) {
+              if (XPERSLOT) load_xs8(xbuf + s * Kp, (xoff >> 3) + v, x8);
+#pragma unroll
+              for (int j = 0; j < ROWS; ++j) {
+                float w8[8];
+                load8<WDT>(tile + (size_t)s * slot_bytes + ((size_t)(cw * ROWS + j) * kck + (size_t)v * 8) * EB, w8);
+                acc[s * ROWS + j] = fma8(w8, x8, acc[s * ROWS + j]);
+              }
             }
           }
         }
@@ -940,8 +960,8 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
           else gemv_phase<1, 1, DT_F16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
         }
       } else {
-        if constexpr (KIND == KK_DENSE8) {
-          if (P.kind != PK_LM) run_gemv<DT_E4M3>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+        if constexpr (KIND == KK_DENSE8 || KIND == KK_DENSE4) {
+          if (P.kind != PK_LM) run_gemv<KIND == KK_DENSE8 ? DT_E4M3 : DT_NVFP4>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
           else if (p.edt == DT_BF16) run_gemv<DT_BF16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
           else run_gemv<DT_F16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
         } else {
@@ -970,7 +990,8 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
 }
 
 // KIND: KK_DENSE (16-bit weights), KK_MOE (top-k expert models), KK_DENSE8 (e4m3 layer
-// matrices): each model runs the instantiation that carries only its own code paths.
+// matrices), KK_DENSE4 (NVFP4 layer matrices): each model runs the instantiation that carries
+// only its own code paths.
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ Params p, int32_t ph0, int32_t ph1, int32_t use_barrier,
@@ -1006,8 +1027,12 @@ namespace adp {
 
 // Host-side launchers of the decode kernel.
 static const void* kernel_of(int kind) {
-  return kind == KK_MOE ? (const void*)decode_kernel<KK_MOE>
-                        : kind == KK_DENSE8 ? (const void*)decode_kernel<KK_DENSE8> : (const void*)decode_kernel<KK_DENSE>;
+  switch (kind) {
+    case KK_MOE: return (const void*)decode_kernel<KK_MOE>;
+    case KK_DENSE8: return (const void*)decode_kernel<KK_DENSE8>;
+    case KK_DENSE4: return (const void*)decode_kernel<KK_DENSE4>;
+    default: return (const void*)decode_kernel<KK_DENSE>;
+  }
 }
 
 cudaError_t decode_prepare(size_t smem_bytes, int kind, int* blocks_per_sm) {
@@ -1021,7 +1046,7 @@ cudaError_t decode_launch(const Params& p, int ph0, int ph1, bool persistent, in
                           int xbuf_floats, cudaStream_t stream) {
   int32_t a0 = ph0, a1 = ph1, ub = persistent ? 1 : 0, xf = xbuf_floats;
   void* args[] = {(void*)&p, &a0, &a1, &ub, &xf};
-  const void* k = kernel_of(p.E > 0 ? KK_MOE : p.wdt == DT_E4M3 ? KK_DENSE8 : KK_DENSE);
+  const void* k = kernel_of(p.E > 0 ? KK_MOE : p.wdt == DT_E4M3 ? KK_DENSE8 : p.wdt == DT_NVFP4 ? KK_DENSE4 : KK_DENSE);
   if (persistent) return cudaLaunchCooperativeKernel(k, dim3(grid), dim3(kThreads), args, smem_bytes, stream);
   return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, smem_bytes, stream);
 }

@@ -108,7 +108,7 @@ __device__ __forceinline__ void l2_advance(const Params& p, const Ctl* ctl, L2Cu
     if (Q.kind == PK_EGU || Q.kind == PK_EDOWN) return;  // experts not chosen yet
     int32_t u0, n;
     cta_share(p, ctl, Q, u0, n);
-    const uint64_t unit_bytes = (uint64_t)Q.unit_rows * Q.K * Q.eb;
+    const uint64_t unit_bytes = wbytes(Q, (uint64_t)Q.unit_rows * Q.K);
     const uint64_t len = (uint64_t)n * unit_bytes;
     if (cur.off >= len) { ++cur.ph; cur.off = 0; continue; }
     const uint64_t left = len - cur.off;
@@ -149,7 +149,7 @@ static __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32
         sel_layer = P.layer;
       }
       if (n <= 0) continue;
-      const uint64_t unit_bytes = (uint64_t)P.unit_rows * P.K * P.eb;
+      const uint64_t unit_bytes = wbytes(P, (uint64_t)P.unit_rows * P.K);
       const uint8_t* base = p.image + P.region + (uint64_t)u0 * unit_bytes;
       const int rounds = (n + P.upr - 1) / P.upr;
       bool first = true;
@@ -160,8 +160,8 @@ static __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32
         for (int ck = 0; ck < P.n_chunks; ++ck) {
           if (aborted(ctl)) { stop = true; break; }
           const int kck = min(P.KC, P.K - ck * P.KC);
-          const uint32_t bytes = (uint32_t)m * P.unit_rows * kck * P.eb;
-          const uint64_t off = round_off + (uint64_t)m * P.unit_rows * ck * P.KC * P.eb;
+          const uint32_t bytes = (uint32_t)wbytes(P, (uint64_t)m * P.unit_rows * kck);
+          const uint64_t off = round_off + wbytes(P, (uint64_t)m * P.unit_rows * ck * P.KC);
           const uint32_t slot = pslot, use = puse;
           if (use > 0) {
             if (!mbar_try_wait(&ctl->empty[slot], (use - 1) & 1)) {

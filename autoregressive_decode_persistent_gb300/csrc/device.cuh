@@ -7,6 +7,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
 
@@ -172,6 +173,24 @@ __device__ __forceinline__ void load8(const uint8_t* p, float (&w)[8]) {
       w[4 * i + 3] = b.y;
     }
   }
+}
+
+// 8 NVFP4 elements from one 32-bit word of codes (element 2i in the low nibble of byte i) -> fp32
+// (exact: every E2M1 value is an fp16 value).
+__device__ __forceinline__ void load8_e2m1(uint32_t q, float (&w)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((q >> (8 * i)) & 0xFFu), __NV_E2M1);
+    const float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+    w[2 * i] = f.x;
+    w[2 * i + 1] = f.y;
+  }
+}
+
+// One e4m3 code -> fp32 (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint8_t b) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
+  return __half2float(*reinterpret_cast<__half*>(&h));
 }
 
 __device__ __forceinline__ float load_elem(const void* base, size_t i, int dt) {

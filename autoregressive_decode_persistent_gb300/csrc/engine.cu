@@ -37,7 +37,13 @@ int cuda_fail(cudaError_t e, const char* what) {
     if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
   } while (0)
 
-int elem_bytes(int dt) { return dt == ADP_E4M3 ? 1 : (dt == ADP_F32 ? 4 : 2); }
+// Bytes per element of a weight type (0 for NVFP4, whose image bytes come from wbytes()).
+int elem_bytes(int dt) { return dt == ADP_NVFP4 ? 0 : dt == ADP_E4M3 ? 1 : (dt == ADP_F32 ? 4 : 2); }
+
+// Layer matrices quantised with fp32 row scales (e4m3, NVFP4): the embedding, the LM head and
+// the norm gains then keep the 16-bit embed_dtype.
+static bool quantised(int wdt) { return wdt == ADP_E4M3 || wdt == ADP_NVFP4; }
+static int head_dtype(const adp_config& c) { return quantised(c.weight_dtype) ? c.embed_dtype : c.weight_dtype; }
 
 }  // namespace
 
@@ -139,11 +145,15 @@ static int validate(const adp_config* c, const adp_weights* w) {
   if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (c->d_model % 8 || c->vocab % 8 || (c->n_heads * c->head_dim) % 8) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (c->d_model > 7680 || c->vocab > 1024 * 256) return ADP_ERR_UNSUPPORTED_CONFIG;
-  const bool q8 = c->weight_dtype == ADP_E4M3;  // fp8 layer matrices with per-row scales (dense only)
+  // fp8 or NVFP4 layer matrices with per-row scales (dense only)
+  const bool q8 = quantised(c->weight_dtype), q4 = c->weight_dtype == ADP_NVFP4;
   if (c->weight_dtype != ADP_F16 && c->weight_dtype != ADP_BF16 && !(q8 && c->n_experts == 0))
     return ADP_ERR_UNSUPPORTED_CONFIG;
   if (q8 && c->embed_dtype != ADP_F16 && c->embed_dtype != ADP_BF16) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (q8 && (c->d_model % 16 || c->d_ff % 16 || (c->n_heads * c->head_dim) % 16)) return ADP_ERR_UNSUPPORTED_CONFIG;
+  // NVFP4 tiles stay 16-byte multiples when every reduction length is a multiple of 128
+  if (q4 && (c->d_model % 128 || c->d_ff % 128 || (c->n_heads * c->head_dim) % 128))
+    return ADP_ERR_UNSUPPORTED_CONFIG;
   if (c->kv_dtype != ADP_F16 && c->kv_dtype != ADP_BF16) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (!c->tied_embeddings && !w->lm_head) return ADP_ERR_INVALID_ARG;
   if (c->n_experts == 0) {
@@ -161,6 +171,9 @@ static int validate(const adp_config* c, const adp_weights* w) {
     if (c->n_experts == 0 && (!L.w_gate || !L.w_up || !L.w_down)) return ADP_ERR_INVALID_ARG;
     if (q8 && (!L.wq_scale || !L.wk_scale || !L.wv_scale || !L.wo_scale || !L.w_gate_scale || !L.w_up_scale ||
                !L.w_down_scale))
+      return ADP_ERR_INVALID_ARG;
+    if (q4 && (!L.wq_bscale || !L.wk_bscale || !L.wv_bscale || !L.wo_bscale || !L.w_gate_bscale ||
+               !L.w_up_bscale || !L.w_down_bscale))
       return ADP_ERR_INVALID_ARG;
     if (c->n_experts && (!L.router || !L.e_gate || !L.e_up || !L.e_down || !L.e_gate_scale || !L.e_up_scale ||
                          !L.e_down_scale))
@@ -189,14 +202,15 @@ static void add_phase(adp_model* m, int kind, int layer, int n_units, int unit_r
     const int maxu = std::max(1, (n_units + m->G - 1) / m->G);
     const int nrounds = (maxu + kConsumerWarps - 1) / kConsumerWarps;
     int upr = (maxu + nrounds - 1) / nrounds;
-    while (upr > 1 && (long long)upr * unit_rows * slots * eb * kChunkAlign > kSlotBytes) --upr;
+    while (upr > 1 && wbytes(P, (uint64_t)upr * unit_rows * slots * kChunkAlign) > (uint64_t)kSlotBytes) --upr;
     P.upr = upr;
-    int KC = (kSlotBytes / (upr * unit_rows * slots * eb)) / kChunkAlign * kChunkAlign;
+    // the widest K-chunk (a multiple of kChunkAlign) whose round of tiles fits one slot
+    int KC = (int)(kSlotBytes / wbytes(P, (uint64_t)upr * unit_rows * slots * kChunkAlign)) * kChunkAlign;
     const int Kr = (K + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
     KC = std::min(KC, Kr);
     P.KC = KC;
     P.n_chunks = (K + KC - 1) / KC;
-    const uint64_t region = (uint64_t)n_units * unit_rows * K * eb;
+    const uint64_t region = wbytes(P, (uint64_t)n_units * unit_rows * K);
     P.region = m->image_bytes;
     P.expert_stride = (region + 255) / 256 * 256;
     m->image_bytes += P.expert_stride * (uint64_t)experts;
@@ -248,7 +262,7 @@ static void plan(adp_model* m) {
       x_ph = last();
     }
   }
-  const int edt = c.weight_dtype == ADP_E4M3 ? c.embed_dtype : c.weight_dtype;  // the LM head's type
+  const int edt = head_dtype(c);  // the LM head's type
   add_phase(m, PK_LM, c.n_layers, c.vocab / 4, 4, 1, d, elem_bytes(edt), edt, true, 1);
   link(x_ph, -1, -1);
   add_phase(m, PK_SAMPLE, c.n_layers, 0, 0, 0, 0, 0, 0, false, 0);
@@ -344,7 +358,12 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   m->p.att_gmax = gmax;
   m->p.att_slot_bytes = (int)item;
   int bps = 0;
-  CK(decode_prepare(m->smem, c.n_experts > 0 ? KK_MOE : c.weight_dtype == ADP_E4M3 ? KK_DENSE8 : KK_DENSE, &bps));
+  CK(decode_prepare(m->smem,
+                    c.n_experts > 0                   ? KK_MOE
+                    : c.weight_dtype == ADP_E4M3  ? KK_DENSE8
+                    : c.weight_dtype == ADP_NVFP4 ? KK_DENSE4
+                                                      : KK_DENSE,
+                    &bps));
   if (bps < 1) return ADP_ERR_NOT_CORESIDENT;
 
   // weight image
@@ -366,10 +385,16 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
     } else {
       const adp_layer_weights& Lw = w->layers[P.layer];
       switch (P.kind) {
-        case PK_QKV: S.a = (const uint8_t*)Lw.wq; S.b = (const uint8_t*)Lw.wk; S.c = (const uint8_t*)Lw.wv; break;
-        case PK_WO: S.a = (const uint8_t*)Lw.wo; break;
-        case PK_GU: S.a = (const uint8_t*)Lw.w_gate; S.b = (const uint8_t*)Lw.w_up; break;
-        case PK_DOWN: S.a = (const uint8_t*)Lw.w_down; break;
+        case PK_QKV:
+          S.a = (const uint8_t*)Lw.wq; S.b = (const uint8_t*)Lw.wk; S.c = (const uint8_t*)Lw.wv;
+          S.sa = Lw.wq_bscale; S.sb = Lw.wk_bscale; S.sc = Lw.wv_bscale;
+          break;
+        case PK_WO: S.a = (const uint8_t*)Lw.wo; S.sa = Lw.wo_bscale; break;
+        case PK_GU:
+          S.a = (const uint8_t*)Lw.w_gate; S.b = (const uint8_t*)Lw.w_up;
+          S.sa = Lw.w_gate_bscale; S.sb = Lw.w_up_bscale;
+          break;
+        case PK_DOWN: S.a = (const uint8_t*)Lw.w_down; S.sa = Lw.w_down_bscale; break;
         case PK_ROUTER: S.a = (const uint8_t*)Lw.router; break;
         case PK_EGU:
           S.a = (const uint8_t*)Lw.e_gate; S.b = (const uint8_t*)Lw.e_up;
@@ -405,7 +430,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
     const float* s7[7] = {Lw.wq_scale, Lw.wk_scale, Lw.wv_scale, Lw.wo_scale, Lw.w_gate_scale, Lw.w_up_scale,
                           Lw.w_down_scale};
     for (int i = 0; i < 7; ++i) {
-      ws[i][l] = c.weight_dtype == ADP_E4M3 ? s7[i] : nullptr;
+      ws[i][l] = quantised(c.weight_dtype) ? s7[i] : nullptr;
       m->h_wscale[i].push_back(ws[i][l]);
     }
   }
@@ -496,7 +521,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   p.L = L; p.d = d; p.hq = hq; p.hkv = hkv; p.hd = hd; p.ff = c.d_ff; p.V = c.vocab; p.max_ctx = c.max_ctx;
   p.E = c.n_experts; p.topk = c.n_experts ? c.top_k : 0; p.fexp = c.d_expert;
   p.wdt = c.weight_dtype; p.kvdt = c.kv_dtype; p.rdt = c.router_dtype;
-  p.edt = c.weight_dtype == ADP_E4M3 ? c.embed_dtype : c.weight_dtype;
+  p.edt = head_dtype(c);
   p.eps = c.rms_eps;
   p.attn_scale = (float)(1.0 / std::sqrt((double)hd));
   p.nbmax = nbmax;
@@ -818,6 +843,7 @@ static int batch_init(adp_model* m) {
   const adp_config& c = m->cfg;
   B.init_rc = ADP_ERR_UNSUPPORTED_CONFIG;
   if (c.n_experts != 0) return B.init_rc;  // experts differ per request
+  if (c.weight_dtype == ADP_NVFP4) return B.init_rc;  // the batched kernel reads 16-bit or e4m3 weights
   const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim;
   cudaDeviceProp prop;
   CK(cudaGetDeviceProperties(&prop, m->device));
@@ -1038,11 +1064,11 @@ extern "C" int adp_generate_batch_async(adp_model* m, adp_kv* const* kvs, int32_
 // The 16-bit type of the tensor-core prefill's GEMM operands: the weights' own, or for e4m3
 // layer matrices the embedding's (the matrices are dequantised into it).
 static int tc_operand_bf16(const adp_config& c) {
-  return (c.weight_dtype == ADP_E4M3 ? c.embed_dtype : c.weight_dtype) == ADP_BF16 ? 1 : 0;
+  return head_dtype(c) == ADP_BF16 ? 1 : 0;
 }
 
 // Set up the tensor-core prefill once per model: every layer matrix again as GEMM operand tiles
-// (rebuilt from the decode image), for dense models (16-bit or e4m3 layer matrices) with head_dim
+// (rebuilt from the decode image), for dense models (16-bit, e4m3 or NVFP4 layer matrices) with head_dim
 // 64 or 128.
 static int tc_init(adp_model* m) {
   adp_model::TcState& T = m->tc;

@@ -12,6 +12,9 @@ struct RepackSrc {
   const uint8_t* a;            // wq / wo / w_gate / w_down / head / router / e_gate / e_down
   const uint8_t* b;            // wk / w_up / e_up
   const uint8_t* c;            // wv
+  const uint8_t* sa;           // NVFP4 only: the block scales [rows][K / 16] of a, b, c
+  const uint8_t* sb;
+  const uint8_t* sc;
   uint64_t expert_src_stride;  // bytes of one expert's matrix in the caller's [E, rows, K] tensor
   int32_t hd, hq, hkv;
 };

@@ -38,11 +38,14 @@ enum PhaseKind : int32_t {
   PK_SAMPLE = 9  // inverse-CDF sampling over the logits (temperature > 0 only)
 };
 
-enum DType : int32_t { DT_F16 = 0, DT_BF16 = 1, DT_E4M3 = 2, DT_F32 = 3 };
+// DT_NVFP4: 4-bit E2M1 codes (two per byte, the even element in the low nibble) with one e4m3
+// scale per 16 consecutive elements of a row.
+enum DType : int32_t { DT_F16 = 0, DT_BF16 = 1, DT_E4M3 = 2, DT_F32 = 3, DT_NVFP4 = 4 };
 
-// Kernel instantiations: dense 16-bit weights, top-k experts, dense e4m3 layer matrices, and the
-// batched kernel (dense 16-bit weights, up to kMaxBatch requests per step).
-enum KernelKind : int32_t { KK_DENSE = 0, KK_MOE = 1, KK_DENSE8 = 2, KK_BATCH = 3 };
+// Kernel instantiations: dense 16-bit weights, top-k experts, dense e4m3 layer matrices, the
+// batched kernel (dense 16-bit or e4m3 weights, up to kMaxBatch requests per step), and dense
+// NVFP4 layer matrices.
+enum KernelKind : int32_t { KK_DENSE = 0, KK_MOE = 1, KK_DENSE8 = 2, KK_BATCH = 3, KK_DENSE4 = 4 };
 
 struct PhaseDesc {
   int32_t kind, layer;
@@ -53,7 +56,7 @@ struct PhaseDesc {
   int32_t KC;             // K-chunk width, multiple of kChunkAlign
   int32_t n_chunks;       // ceil(K / KC)
   int32_t upr;            // units per round (<= kConsumerWarps)
-  int32_t eb;             // weight element bytes
+  int32_t eb;             // weight element bytes (0 for NVFP4: see wbytes)
   int32_t wdt;            // weight DType
   int32_t has_weights;
   int32_t index;          // position of this phase in the step's phase list
@@ -149,6 +152,19 @@ struct Params {
   uint16_t* const* kcb;        // [nb] each request's K cache [L][hkv][max_ctx][hd]
   uint16_t* const* vcb;        // [nb] each request's V cache
 };
+
+#ifdef __CUDACC__
+#define ADP_HD __host__ __device__
+#else
+#define ADP_HD
+#endif
+
+// Image bytes of n consecutive weight elements of one row (n * eb).  NVFP4 rows take n / 2 bytes
+// of codes plus n / 16 block-scale bytes (n a multiple of 16): within one tile of R rows x kck
+// elements the R x kck / 2 code bytes come first, row after row, then the R x kck / 16 scales.
+ADP_HD inline uint64_t wbytes(const PhaseDesc& P, uint64_t n) {
+  return P.wdt == DT_NVFP4 ? n / 16 * 9 : n * (uint64_t)P.eb;
+}
 
 // Device error codes (the host maps them to ADP_ERR_*).
 enum DevErr : int32_t { DE_NONE = 0, DE_BARRIER_TIMEOUT = 1, DE_PIPELINE_TIMEOUT = 2 };  // 1: a dependency wait

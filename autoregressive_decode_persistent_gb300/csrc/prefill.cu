@@ -350,7 +350,8 @@ __device__ __forceinline__ float tc_row_scale(const PhaseDesc& P, int row, int h
 
 // The decode image's tiles of phase P back into one tiled GEMM operand (256-row tiles): the
 // inverse of the repack, walked the same way (CTA c's units, rounds, K-chunks).  16-bit weights
-// are copied as they are; e4m3 weights become scale x code (fp32, then RNE to the operand type).
+// are copied as they are; e4m3 weights become scale x code and NVFP4 weights row scale x (block
+// scale x code) (fp32, then RNE to the operand type).
 __global__ void tc_unpack_kernel(const uint8_t* __restrict__ image, PhaseDesc P, uint8_t* dst, int k_tiles, int hd,
                                  int hq, int hkv, int ff, const float* sa, const float* sb, const float* sc,
                                  int out_bf16) {
@@ -359,7 +360,7 @@ __global__ void tc_unpack_kernel(const uint8_t* __restrict__ image, PhaseDesc P,
   const int u0 = (int)a0, n = (int)(a1 - a0);
   if (n <= 0) return;
   const int eb = P.eb;
-  const uint64_t unit_bytes = (uint64_t)P.unit_rows * P.K * eb;
+  const uint64_t unit_bytes = wbytes(P, (uint64_t)P.unit_rows * P.K);
   const uint8_t* src_cta = image + P.region + (uint64_t)u0 * unit_bytes;
   const int nv8 = P.K / 8;
   const long long total = (long long)n * P.unit_rows * nv8;
@@ -372,16 +373,25 @@ __global__ void tc_unpack_kernel(const uint8_t* __restrict__ image, PhaseDesc P,
     const int kck = min(P.KC, P.K - ck * P.KC);
     const int r = lu / P.upr, i = lu % P.upr;
     const int m = min(P.upr, n - r * P.upr);
-    const uint64_t off = (uint64_t)r * P.upr * unit_bytes + (uint64_t)m * P.unit_rows * ck * P.KC * eb +
-                         ((uint64_t)(i * P.unit_rows + j) * kck + (col - ck * P.KC)) * eb;
+    const uint64_t tile_off = (uint64_t)r * P.upr * unit_bytes + wbytes(P, (uint64_t)m * P.unit_rows * ck * P.KC);
+    const uint64_t prow = (uint64_t)i * P.unit_rows + j, kc0 = (uint64_t)(col - ck * P.KC);
+    const uint64_t off = tile_off + (prow * kck + kc0) * eb;
     const int row = tc_logical_row(P, u0 + lu, j, hd, hq, hkv, ff);
     const size_t tile = (size_t)(row / kTcBN) * k_tiles + col / kTcBK;
     uint4 v;
-    if (eb == 2) {
+    if (P.wdt != DT_NVFP4 && eb == 2) {
       v = *reinterpret_cast<const uint4*>(src_cta + off);
     } else {
       float w[8];
-      load8<DT_E4M3>(src_cta + off, w);
+      if (P.wdt == DT_NVFP4) {
+        load8_e2m1(*reinterpret_cast<const uint32_t*>(src_cta + tile_off + prow * (kck / 2) + kc0 / 2), w);
+        const float bs = e4m3_to_f32(src_cta[tile_off + (uint64_t)m * P.unit_rows * (kck / 2) + prow * (kck / 16) +
+                                             kc0 / 16]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = bs * w[k];  // exact: 2 + 4 significant bits
+      } else {
+        load8<DT_E4M3>(src_cta + off, w);
+      }
       const float s = tc_row_scale(P, row, hd, hq, hkv, ff, sa, sb, sc);
       uint16_t e[8];
 #pragma unroll

@@ -34,7 +34,9 @@ def make_config(cfg: dict) -> adp.Config:
 class DecodeModel:
     """A model on one GPU plus its KV caches (see include/adp.h for the semantics)."""
 
-    _MATRICES = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "router", "e_gate", "e_up", "e_down")
+    _MATRICES = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "router", "e_gate", "e_up", "e_down",
+                 "wq_bscale", "wk_bscale", "wv_bscale", "wo_bscale", "w_gate_bscale", "w_up_bscale",
+                 "w_down_bscale")
 
     def __init__(self, cfg: dict, host_weights: dict, device: str = "cuda:0", stream: torch.cuda.Stream | None = None,
                  keep_matrices: bool = False):
@@ -58,7 +60,9 @@ class DecodeModel:
             f = {k: up(Lw.get(k), k in self._MATRICES)
                  for k in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down", "router",
                            "e_gate", "e_up", "e_down", "e_gate_scale", "e_up_scale", "e_down_scale", "wq_scale",
-                           "wk_scale", "wv_scale", "wo_scale", "w_gate_scale", "w_up_scale", "w_down_scale")}
+                           "wk_scale", "wv_scale", "wo_scale", "w_gate_scale", "w_up_scale", "w_down_scale",
+                           "wq_bscale", "wk_bscale", "wv_bscale", "wo_bscale", "w_gate_bscale", "w_up_bscale",
+                           "w_down_bscale")}
             layers[i] = adp.LayerWeights(**f)
         self._layers = layers
         self.weights = adp.Weights(up(W["tok_emb"]), up(W.get("lm_head"), True), up(W["final_norm"]), layers)

@@ -5,7 +5,8 @@ vocabulary 32000, fp16 weights ~N(0, 0.02) from a seed; a 512-token uniform-rand
 prefilled, then greedy decode steps run at contexts 513..1024 (a run longer than 512 steps
 rewinds the cache to 512 and decodes the window again). One step = one decode step of the
 whole model; the steps of a window run inside one persistent kernel launch.
---workload dense-2.3b-e4m3 measures the same model with e4m3 layer matrices instead.
+--workload dense-2.3b-e4m3 (dense-2.3b-nvfp4) measures the same model with e4m3 (NVFP4) layer
+matrices instead.
 --batch N (N >= 2) measures N independent requests decoded together by the batched kernel
 (value = tokens/s of all requests; the default, batch 1, is the benchmark's headline).
 --prefill measures time to first token of the 3,584-token prompt through the tensor-core
@@ -43,8 +44,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "batch-1 decode tokens/s/request (2.3B fp16); achieved HBM GB/s vs GB300 peak"
 WORKLOAD = "dense-2.3b-fp16"
-# --workload: the 2.3B model as benchmarked (default), or with e4m3 layer matrices (a "next" row:
-# fp8 dense weights; same shape, per-row fp32 scales, fp16 embedding and tied LM head)
+# --workload: the 2.3B model as benchmarked (default), or with e4m3 or NVFP4 layer matrices (the
+# "next" row of low-precision dense weights; same shape, per-row fp32 scales (NVFP4: and an e4m3
+# scale per 16 elements), fp16 embedding and tied LM head)
 WORKLOADS = {
     "dense-2.3b-fp16": {"metric": METRIC, "weights": "f16",
                         "data": "synthetic: seeded N(0,0.02) fp16 weights, 512 uniform-random prompt ids"},
@@ -53,6 +55,12 @@ WORKLOADS = {
                         "weights": "e4m3 layer matrices with per-row f32 scales; f16 embedding, LM head, norms",
                         "data": "synthetic: seeded N(0,0.02) weights quantised to e4m3 per row, 512 uniform-random "
                                 "prompt ids"},
+    "dense-2.3b-nvfp4": {"metric": "batch-1 decode tokens/s/request (2.3B, NVFP4 layer weights); achieved HBM GB/s "
+                                   "vs GB300 peak",
+                         "weights": "nvfp4 layer matrices (e2m1, e4m3 scale per 16 elements, f32 row scales); f16 "
+                                    "embedding, LM head, norms",
+                         "data": "synthetic: seeded N(0,0.02) weights quantised to NVFP4 per row and 16-element "
+                                 "block, 512 uniform-random prompt ids"},
 }
 WINDOW = 512  # decode steps per pass over contexts 513..1024
 

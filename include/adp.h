@@ -42,8 +42,9 @@ extern "C" {
 #pragma GCC visibility push(default)
 #endif
 
-/* Storage types of weights and of the KV cache. */
-typedef enum { ADP_F16 = 0, ADP_BF16 = 1, ADP_E4M3 = 2, ADP_F32 = 3 } adp_dtype;
+/* Storage types of weights and of the KV cache.  ADP_NVFP4: 4-bit E2M1 codes, two per byte (the
+ * even element in the low nibble), with one e4m3 scale per 16 consecutive elements of a row. */
+typedef enum { ADP_F16 = 0, ADP_BF16 = 1, ADP_E4M3 = 2, ADP_F32 = 3, ADP_NVFP4 = 4 } adp_dtype;
 
 enum {
   ADP_OK = 0,
@@ -70,10 +71,12 @@ typedef struct {
   float rms_eps, rope_theta;
   int32_t tied_embeddings;          /* 1: logits use tok_emb as the LM head */
   int32_t weight_dtype, kv_dtype;   /* adp_dtype: ADP_F16 or ADP_BF16 for both; weight_dtype may be
-                                       ADP_E4M3 for a dense model (see embed_dtype and the scales) */
+                                       ADP_E4M3 or ADP_NVFP4 for a dense model (see embed_dtype and
+                                       the scales; NVFP4 needs d_model, d_ff and n_heads*head_dim
+                                       to be multiples of 128) */
   int32_t n_experts, top_k, d_expert;
   int32_t router_dtype, expert_dtype; /* router: ADP_F16/ADP_BF16; experts: ADP_E4M3 */
-  int32_t embed_dtype;              /* with weight_dtype ADP_E4M3: type of tok_emb, lm_head and the
+  int32_t embed_dtype;              /* with weight_dtype ADP_E4M3/NVFP4: type of tok_emb, lm_head and the
                                        norm gains (ADP_F16 or ADP_BF16); otherwise ignored */
 } adp_config;
 
@@ -92,6 +95,14 @@ typedef struct {
    * in place); else NULL.  The pages project fp8 weights as the next step for large models
    * ([H] translated comment thread, author reply: "FP8" MoE). */
   const float *wq_scale, *wk_scale, *wv_scale, *wo_scale, *w_gate_scale, *w_up_scale, *w_down_scale;
+  /* weight_dtype ADP_NVFP4 (dense): the seven matrices above hold [rows, K/2] bytes of E2M1 codes
+   * and these their e4m3 block scales, [rows, K/16] bytes (one per 16 consecutive elements of a
+   * row); an element is row scale x block scale x code, the row scale (above) applied after the
+   * dot product.  Per 8-element vector of a row the element products are summed by fused
+   * multiply-adds from zero, and that sum times its block scale is fused-multiply-added into the
+   * vector's lane partial.  Copied into the image at creation; else NULL.  The pages project
+   * 4-bit weights for larger models ([H] translated comment thread, author reply: mixed FP4/FP8). */
+  const uint8_t *wq_bscale, *wk_bscale, *wv_bscale, *wo_bscale, *w_gate_bscale, *w_up_bscale, *w_down_bscale;
 } adp_layer_weights;
 
 typedef struct {
@@ -213,8 +224,8 @@ int adp_sync(adp_model* m);                          /* synchronise the stream; 
  * decode step's arithmetic contract, so its KV rows and logits agree with the oracle within the
  * tolerances, not bit for bit (adp_prefill is the bit-exact path).
  * Arguments, errors and synchronisation as adp_prefill.  Dense models with head_dim 64 or 128 only
- * (else ADP_ERR_UNSUPPORTED_CONFIG); e4m3 layer matrices are dequantised with their row scales
- * into the embedding's 16-bit type for the GEMMs.  The first call builds a second copy of the
+ * (else ADP_ERR_UNSUPPORTED_CONFIG); e4m3 and NVFP4 layer matrices are dequantised with their
+ * row (and block) scales into the embedding's 16-bit type for the GEMMs.  The first call builds a second copy of the
  * layer matrices in the tensor cores' tile layout (16-bit, device memory owned by the model);
  * scratch grows with the longest prompt seen. */
 int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t n, const adp_sampling* sampling,
@@ -233,9 +244,9 @@ int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t
  *  dev_logits: optional DEVICE float array [nb][vocab].
  * nb must be in [1, adp_max_batch]: the batched kernel keeps nb copies of the widest GEMV input
  * vector (fp32) in shared memory beside a weight ring of at least two slots, and merges head h of
- * request r on CTA G-1-(r*n_heads+h).  Dense models only (16-bit or e4m3 layer matrices; experts
- * differ per request, so MoE models get ADP_ERR_UNSUPPORTED_CONFIG).  Synchronises; errors as
- * adp_decode_step (a device error is sticky and no cache grows). */
+ * request r on CTA G-1-(r*n_heads+h).  Dense models with 16-bit or e4m3 layer matrices only
+ * (experts differ per request: MoE models, like NVFP4 ones, get ADP_ERR_UNSUPPORTED_CONFIG).
+ * Synchronises; errors as adp_decode_step (a device error is sticky and no cache grows). */
 int adp_decode_batch(adp_model* m, adp_kv* const* kvs, int32_t nb, const int32_t* tokens,
                      const adp_sampling* sampling, int32_t* next_tokens, float* dev_logits);
 /* n batched steps in one launch, each request feeding itself the token it chose.

@@ -66,8 +66,7 @@ CONFIGS = [
          head_dim=128, d_ff=9728, vocab=32000, max_ctx=4096, weight_dtype="e4m3", embed_dtype="f16",
          prompt_len=512, decode_steps=512),
     # 6: the 2.3B model with nvfp4 layer weights (e2m1 elements, an e4m3 scale per 16 consecutive
-    #    elements of a row, an fp32 scale per row), embedding / tied LM head and norm gains fp16;
-    #    the oracle and its pins only so far (the decode kernels do not take this type yet)
+    #    elements of a row, an fp32 scale per row), embedding / tied LM head and norm gains fp16
     _cfg(index=6, name="dense-2.3b-nvfp4", n_layers=25, d_model=2560, n_heads=20, n_kv_heads=4,
          head_dim=128, d_ff=9728, vocab=32000, max_ctx=4096, weight_dtype="nvfp4", embed_dtype="f16",
          prompt_len=512, decode_steps=512),
@@ -93,7 +92,8 @@ def shrink(cfg: dict, **overrides) -> dict:
     if cfg["n_experts"]:
         c.update(n_experts=8, top_k=cfg["top_k"], d_expert=192)
     else:
-        c.update(d_ff=688)
+        # nvfp4 matrices keep every reduction length a multiple of 128
+        c.update(d_ff=640 if cfg["weight_dtype"] == "nvfp4" else 688)
     c.update(overrides)
     return c
 

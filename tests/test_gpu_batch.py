@@ -205,5 +205,8 @@ def test_batch_rejections(torch_cuda):
     with pytest.raises(adp.AdpError) as e:
         m3.step_batch([m3.new_kv()], [1])
     assert e.value.code == adp.ADP_ERR_UNSUPPORTED_CONFIG
-    for m in (model, m2, m3):
+    q4 = synth.shrink(synth.get_config("dense-2.3b-nvfp4"))
+    m4 = _model(q4, synth.model_weights(q4))
+    assert m4.max_batch == 0
+    for m in (model, m2, m3, m4):
         m.close()

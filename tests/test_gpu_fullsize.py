@@ -31,6 +31,7 @@ def built():
     ("dense-8b-bf16", 1024, 3, 0.0),
     ("moe-32x1408-top4-e4m3", 256, 5, 0.0),
     ("dense-2.3b-e4m3", 512, 5, 0.0),
+    ("dense-2.3b-nvfp4", 512, 5, 0.0),
 ])
 def test_full_size_workload(built, name, prefix, steps, temperature):
     from autoregressive_decode_persistent_gb300.model import DecodeModel

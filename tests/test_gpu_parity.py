@@ -74,10 +74,33 @@ def test_tiny_temperature_sampling_bit_exact(torch_cuda):
     _check_case(cfg, 16, 48, temperature=0.7)
 
 
-@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "moe-32x1408-top4-e4m3", "dense-2.3b-e4m3"])
+@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "moe-32x1408-top4-e4m3", "dense-2.3b-e4m3",
+                                  "dense-2.3b-nvfp4"])
 def test_shrunk_workloads_bit_exact(torch_cuda, name):
     cfg = synth.shrink(synth.get_config(name))
     _check_case(cfg, 8, 40)
+
+
+def test_nvfp4_rows_split_into_several_chunks(torch_cuda):
+    """NVFP4 at the 2.3B model's widths (one layer, small vocabulary): the FFN down projection's
+    9728-long rows stream as several K-chunks with a ragged last one, each tile carrying its rows'
+    codes and then their block scales."""
+    cfg = synth.shrink(synth.get_config("dense-2.3b-nvfp4"), n_layers=1, d_model=2560, d_ff=9728)
+    _check_case(cfg, 6, 10)
+
+
+def test_nvfp4_widths_must_be_multiples_of_128(torch_cuda):
+    from autoregressive_decode_persistent_gb300 import adp
+    cfg = synth.shrink(synth.get_config("dense-2.3b-nvfp4"))
+    W = synth.model_weights(cfg)
+    bad = dict(cfg, d_ff=704)
+    with pytest.raises(adp.AdpError) as e:
+        _model(bad, synth.model_weights(bad))
+    assert e.value.code == adp.ADP_ERR_UNSUPPORTED_CONFIG
+    W["layers"][0]["wq_bscale"] = None
+    with pytest.raises(adp.AdpError) as e:
+        _model(cfg, W)
+    assert e.value.code == adp.ADP_ERR_INVALID_ARG
 
 
 def test_mha_and_single_kv_head_variants(torch_cuda):
@@ -209,7 +232,8 @@ def test_moe_forced_experts_match_oracle(torch_cuda):
 
 
 @pytest.mark.parametrize("name,temperature", [("tiny", 0.7), ("moe-32x1408-top4-e4m3", 0.0),
-                                              ("dense-8b-bf16", 0.0), ("dense-2.3b-e4m3", 0.0)])
+                                              ("dense-8b-bf16", 0.0), ("dense-2.3b-e4m3", 0.0),
+                                              ("dense-2.3b-nvfp4", 0.7)])
 def test_in_kernel_multi_step_generation_matches_oracle(torch_cuda, name, temperature):
     """adp_generate_async runs n decode steps in one persistent launch, each step taking the token
     the previous one chose (and, at T > 0, the next uniform): the tokens and the whole KV cache

@@ -104,16 +104,16 @@ def test_prefill_tc_ragged_and_after_prefix(lib):
     _prefill_case(cfg, 133, prefix_len=21)
 
 
-@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-2.3b-e4m3"])
+@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-2.3b-e4m3", "dense-2.3b-nvfp4"])
 def test_prefill_tc_full_size(lib, name):
-    """The 2.3B model at full size (fp16, and e4m3 layer matrices dequantised for the GEMMs): a
+    """The 2.3B model at full size (fp16, and e4m3 or NVFP4 layer matrices dequantised for the GEMMs): a
     448-row synthetic cache prefix, then a 64-token prompt through the tensor-core path and three
     decode steps."""
     import synth
     _prefill_case(synth.get_config(name), 64, prefix_len=448)
 
 
-@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "dense-2.3b-e4m3"])
+@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "dense-2.3b-e4m3", "dense-2.3b-nvfp4"])
 def test_prefill_tc_shrunk_workloads(lib, name):
     import synth
     _prefill_case(synth.shrink(synth.get_config(name)), 70)
