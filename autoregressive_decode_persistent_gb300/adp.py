@@ -63,6 +63,12 @@ class Sampling(ctypes.Structure):
     _fields_ = [("temperature", ctypes.c_float), ("u", ctypes.c_float)]
 
 
+class PhasePlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("kind", "layer", "n_units", "unit_rows", "slots", "K", "KC",
+                                               "n_chunks", "upr", "dtype")] + \
+               [("region", ctypes.c_uint64), ("expert_stride", ctypes.c_uint64)]
+
+
 _lib = None
 
 # (name, restype, argtypes)
@@ -103,6 +109,8 @@ _SIGS = [
     ("adp_last_error", ctypes.c_char_p, []),
     ("adp_num_ctas", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     ("adp_image_bytes", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint64)]),
+    ("adp_plan", ctypes.c_int, [ctypes.POINTER(Config), ctypes.c_int32, ctypes.POINTER(PhasePlan), ctypes.c_int32,
+                                ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_uint64)]),
     ("adp_launches_per_step", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     ("adp_debug_kernel_mode", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     ("adp_debug_force_experts", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
@@ -320,6 +328,16 @@ def adp_image_bytes(model) -> int:
     n = ctypes.c_uint64()
     _check(load_library().adp_image_bytes(model, ctypes.byref(n)), "adp_image_bytes")
     return n.value
+
+
+def adp_plan(config: Config, n_sms: int) -> tuple[list[dict], int]:
+    """The phase plan and weight-image size of a config on a GPU with n_sms SMs (host only)."""
+    L = load_library()
+    n, img = ctypes.c_int32(), ctypes.c_uint64()
+    _check(L.adp_plan(ctypes.byref(config), n_sms, None, 0, ctypes.byref(n), ctypes.byref(img)), "adp_plan")
+    out = (PhasePlan * n.value)()
+    _check(L.adp_plan(ctypes.byref(config), n_sms, out, n.value, ctypes.byref(n), ctypes.byref(img)), "adp_plan")
+    return [{f: getattr(p, f) for f, _ in PhasePlan._fields_} for p in out], img.value
 
 
 def adp_launches_per_step(model) -> int:

@@ -137,8 +137,9 @@ struct adp_model {
 
 // ---------------------------------------------------------------- validation and planning
 
-static int validate(const adp_config* c, const adp_weights* w) {
-  if (!c || !w || !w->layers || !w->tok_emb || !w->final_norm) return ADP_ERR_INVALID_ARG;
+// The shape and type checks of a config (no weights).
+static int validate_config(const adp_config* c) {
+  if (!c) return ADP_ERR_INVALID_ARG;
   if (c->n_layers < 1 || c->d_model < 8 || c->n_heads < 1 || c->n_kv_heads < 1 || c->vocab < 8 || c->max_ctx < 1)
     return ADP_ERR_INVALID_ARG;
   if (c->n_kv_heads > c->n_heads) return ADP_ERR_UNSUPPORTED_CONFIG;
@@ -155,7 +156,6 @@ static int validate(const adp_config* c, const adp_weights* w) {
   if (q4 && (c->d_model % 128 || c->d_ff % 128 || (c->n_heads * c->head_dim) % 128))
     return ADP_ERR_UNSUPPORTED_CONFIG;
   if (c->kv_dtype != ADP_F16 && c->kv_dtype != ADP_BF16) return ADP_ERR_UNSUPPORTED_CONFIG;
-  if (!c->tied_embeddings && !w->lm_head) return ADP_ERR_INVALID_ARG;
   if (c->n_experts == 0) {
     if (c->d_ff < 8 || c->d_ff % 8) return ADP_ERR_UNSUPPORTED_CONFIG;
   } else {
@@ -165,6 +165,15 @@ static int validate(const adp_config* c, const adp_weights* w) {
     if (c->top_k != 1 && c->top_k != 2 && c->top_k != 4 && c->top_k != 8) return ADP_ERR_UNSUPPORTED_CONFIG;
     if (c->d_expert < 16 || c->d_expert % 16 || c->d_model % 16) return ADP_ERR_UNSUPPORTED_CONFIG;
   }
+  return ADP_OK;
+}
+
+static int validate(const adp_config* c, const adp_weights* w) {
+  if (!c || !w || !w->layers || !w->tok_emb || !w->final_norm) return ADP_ERR_INVALID_ARG;
+  const int rc = validate_config(c);
+  if (rc) return rc;
+  const bool q8 = quantised(c->weight_dtype), q4 = c->weight_dtype == ADP_NVFP4;
+  if (!c->tied_embeddings && !w->lm_head) return ADP_ERR_INVALID_ARG;
   for (int l = 0; l < c->n_layers; ++l) {
     const adp_layer_weights& L = w->layers[l];
     if (!L.attn_norm || !L.wq || !L.wk || !L.wv || !L.wo || !L.ffn_norm) return ADP_ERR_INVALID_ARG;
@@ -1393,6 +1402,40 @@ extern "C" int adp_num_ctas(const adp_model* m, int32_t* ctas) {
 extern "C" int adp_image_bytes(const adp_model* m, uint64_t* bytes) {
   if (!m || !bytes) return ADP_ERR_INVALID_ARG;
   *bytes = m->image_bytes;
+  return ADP_OK;
+}
+
+// The phase plan of a config on a GPU with n_sms SMs, computed on the host alone (no CUDA call):
+// the same plan() a model built on such a GPU streams.
+extern "C" int adp_plan(const adp_config* cfg, int32_t n_sms, adp_phase_plan* out, int32_t cap, int32_t* n_phases,
+                        uint64_t* image_bytes) {
+  if (!cfg || n_sms < 1 || cap < 0 || (cap > 0 && !out) || !n_phases || !image_bytes) return ADP_ERR_INVALID_ARG;
+  const int rc = validate_config(cfg);
+  if (rc) return rc;
+  adp_model m;
+  m.cfg = *cfg;
+  m.G = n_sms;
+  plan(&m);
+  for (const PhaseDesc& P : m.phases)
+    if ((uint64_t)P.n_units * (uint64_t)m.G >= (1ull << 32)) return ADP_ERR_UNSUPPORTED_CONFIG;
+  *n_phases = (int32_t)m.phases.size();
+  *image_bytes = m.image_bytes;
+  for (int i = 0; i < cap && i < (int)m.phases.size(); ++i) {
+    const PhaseDesc& P = m.phases[i];
+    adp_phase_plan& o = out[i];
+    o.kind = P.kind;
+    o.layer = P.layer;
+    o.n_units = P.n_units;
+    o.unit_rows = P.unit_rows;
+    o.slots = P.slots;
+    o.K = P.K;
+    o.KC = P.KC;
+    o.n_chunks = P.n_chunks;
+    o.upr = P.upr;
+    o.dtype = P.has_weights ? P.wdt : -1;
+    o.region = P.region;
+    o.expert_stride = P.expert_stride;
+  }
   return ADP_OK;
 }
 

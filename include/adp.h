@@ -264,6 +264,33 @@ const char* adp_status_string(int status);
 const char* adp_last_error(void);                    /* text of the last ADP_ERR_CUDA in this thread */
 
 /* Introspection used by tests and the benchmark. */
+/* One phase of a decode step's plan (host-side description, see adp_plan). */
+typedef struct {
+  int32_t kind;       /* 0 QKV, 1 attention, 2 Wo, 3 FFN gate|up, 4 FFN down, 5 router, 6 expert gate|up,
+                         7 expert down, 8 LM head, 9 sampling */
+  int32_t layer;      /* n_layers for the LM head and sampling */
+  int32_t n_units;    /* units of the phase, split evenly over the persistent CTAs (0: no weights) */
+  int32_t unit_rows;  /* weight rows per unit (per expert slot) */
+  int32_t slots;      /* expert slots per tile (1 for dense phases) */
+  int32_t K;          /* reduction length */
+  int32_t KC;         /* K-chunk width (a multiple of 256; the last chunk may be shorter) */
+  int32_t n_chunks;   /* ceil(K / KC) */
+  int32_t upr;        /* units per round of a CTA (a tile is min(upr, units left) x one K-chunk) */
+  int32_t dtype;      /* adp_dtype of the phase's weights, -1 without weights */
+  uint64_t region;        /* byte offset of the phase's region in the weight image */
+  uint64_t expert_stride; /* bytes of the region (per expert), a multiple of 256 */
+} adp_phase_plan;
+
+/* The plan of a decode step for cfg on a GPU with n_sms SMs (one persistent CTA each), computed on
+ * the host without any CUDA call: the phases in step order and the size of the tile-ordered
+ * weight image, exactly as adp_create_model lays them out on such a GPU.  CTA c of G owns units
+ * [floor(c n / G), floor((c + 1) n / G)) of a phase of n units, stored from byte region +
+ * floor(c n / G) x unit bytes as its rounds x K-chunks of tiles.  Writes min(cap, *n_phases) entries
+ * of out (caller-owned HOST memory); *n_phases gets the full count and *image_bytes the image size.
+ * Errors: ADP_ERR_INVALID_ARG (null pointers, n_sms < 1) and the config errors of adp_create_model. */
+int adp_plan(const adp_config* cfg, int32_t n_sms, adp_phase_plan* out, int32_t cap, int32_t* n_phases,
+             uint64_t* image_bytes);
+
 int adp_num_ctas(const adp_model* m, int32_t* ctas);            /* persistent grid size (SMs) */
 int adp_image_bytes(const adp_model* m, uint64_t* bytes);       /* bytes of the tile-ordered weight image */
 int adp_launches_per_step(const adp_model* m, int32_t* n);      /* kernel launches of one decode step */
