@@ -207,3 +207,26 @@ def test_plan_rejects_what_the_kernels_cannot_run(adp):
     with pytest.raises(adp.AdpError) as e:
         adp.adp_plan(make_config(cfg), 0)
     assert e.value.code == adp.ADP_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("cfg", CASES, ids=IDS)
+def test_streamed_bytes_are_the_roofline_bytes(adp, cfg):
+    """The weight bytes the roofline counts per step (bound.py, from the model's definition) are
+    the bytes the plan streams (layer matrices and LM head; for MoE the top-k experts' tiles)
+    plus what the kernel reads in place: norm gains, one embedding row, and the fp32 scales."""
+    from autoregressive_decode_persistent_gb300 import bound
+    ph, _ = _plan(adp, cfg)
+    d, hq, hkv, hd, L = cfg["d_model"], cfg["n_heads"], cfg["n_kv_heads"], cfg["head_dim"], cfg["n_layers"]
+    ee = 2  # 16-bit embedding, LM head and gains in every workload
+    streamed = 0
+    for p in ph:
+        if p["dtype"] < 0:
+            continue
+        b = wbytes(p["dtype"], p["n_units"] * p["unit_rows"] * p["K"])
+        streamed += b * (cfg["top_k"] if p["kind"] in (KINDS["egu"], KINDS["edown"]) else 1)
+    in_place = L * 2 * d * ee + 2 * d * ee  # norm gains, final norm, embedding row
+    if cfg["weight_dtype"] in ("e4m3", "nvfp4"):
+        in_place += L * (hq * hd + 2 * hkv * hd + d + 2 * cfg["d_ff"] + d) * 4  # row scales
+    if cfg["n_experts"]:
+        in_place += L * cfg["top_k"] * (2 * cfg["d_expert"] + d) * 4  # expert output-channel scales
+    assert streamed + in_place == bound.weight_bytes_per_token(cfg)
