@@ -299,6 +299,12 @@ static float dot_nvfp4(const uint8_t* codes, const uint8_t* bscale, const float*
   return s;
 }
 
+/* Exported for the pins: dot_nvfp4 of one row. */
+float orc_dot_nvfp4(const uint8_t* codes, const uint8_t* bscale, const float* x, int K, int mode) {
+  orc_init();
+  return dot_nvfp4(codes, bscale, x, K, mode);
+}
+
 /* y[r] = scale[r] * (W[r,:] . x) for r < rows (scale NULL -> 1, applied after the dot); nvfp4
  * matrices (dt ORC_NVFP4) also take their block scales. */
 static int gemv(const void* Wt, int dt, int rows, int K, const float* x, const float* scale, const uint8_t* bscale,

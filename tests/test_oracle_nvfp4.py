@@ -24,6 +24,75 @@ def test_e2m1_codes_decode_to_the_format_values():
     assert np.signbit(got[8])  # code 8 is negative zero
 
 
+# e4m3 codes of the block scales used below (sign 0, exponent bias 7, three fraction bits)
+E4M3_ONE, E4M3_ONE_AND_HALF = 0x38, 0x3C
+
+
+def _pack(codes):
+    """Element 2i in the low nibble of byte i."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.ascontiguousarray(c[0::2] | (c[1::2] << 4))
+
+
+def dot4(codes, bscale, x, mode):
+    q = _pack(codes)
+    b = np.ascontiguousarray(bscale, dtype=np.uint8)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return lib().orc_dot_nvfp4(q.ctypes.data, b.ctypes.data, x.ctypes.data, len(x), mode)
+
+
+@pytest.mark.parametrize("mode", [EXACT, PLAIN])
+def test_nvfp4_dot_is_exact_when_every_partial_is_representable(mode):
+    """Block scales that are powers of two and inputs that are small multiples of 1/4: every
+    product and partial sum is exact in fp32, so both modes must return the rational dot of the
+    format's values (a swapped nibble, a misplaced block, a mis-decoded scale or a dropped sign
+    fails here)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(77)
+    K = 512
+    codes = rng.integers(0, 16, K)
+    k = rng.integers(-3, 4, K // 16)
+    bscale = ((k + 7) << 3).astype(np.uint8)  # e4m3 code of 2^k
+    x = (rng.integers(-3, 4, K) / 4.0).astype(np.float32)
+    want = sum(Fraction(E2M1_VALUES[codes[j]]) * Fraction(2) ** int(k[j // 16]) * Fraction(float(x[j]))
+               for j in range(K))
+    assert Fraction(float(dot4(codes, bscale, x, mode))) == want
+
+
+def test_nvfp4_dot_exact_assigns_vectors_to_lanes_and_folds_as_a_tree():
+    """K = 512, all scales 1: vector 0 sums to 2^24 (code 4 times 2^22), vectors 1 and 33 to 1
+    each. The contract puts vectors 1 and 33 in lane 1 (2, exact) and folds it into lane 0 last:
+    2^24 + 2. The plain order adds each 1 to 2^24 and loses both (ties to even)."""
+    K = 512
+    codes = np.zeros(K, np.int64)
+    x = np.zeros(K, np.float32)
+    codes[0], x[0] = 6, 2.0 ** 22  # E2M1 code 6 is 4
+    codes[8], x[8] = 2, 1.0        # code 2 is 1
+    codes[264], x[264] = 2, 1.0
+    bscale = np.full(K // 16, E4M3_ONE, np.uint8)
+    assert dot4(codes, bscale, x, EXACT) == 2.0 ** 24 + 2
+    assert dot4(codes, bscale, x, PLAIN) == 2.0 ** 24
+
+
+def test_nvfp4_dot_exact_applies_the_block_scale_with_one_rounding():
+    """Lane 0 holds a = 1 - 2^-24 from vector 0 (scale 1); vector 32 has t = 1 + 2^-23 and block
+    scale 1.5. One fused step gives RN(1.5 t + a) = RN(2.5 + 2^-23): the midpoint between 2.5 and
+    2.5 + 2^-22, so 2.5 (even). Rounding 1.5 t first (1.5 + 3 2^-24, a midpoint, rounds to
+    1.5 + 2^-22) and then adding a gives 2.5 + 3 2^-24, which rounds to 2.5 + 2^-22; so does the
+    plain order."""
+    K = 512
+    codes = np.zeros(K, np.int64)
+    x = np.zeros(K, np.float32)
+    a = np.float32(1.0) - np.float32(2.0 ** -24)
+    t = np.float32(1.0) + np.float32(2.0 ** -23)
+    codes[0], x[0] = 2, a
+    codes[256], x[256] = 2, t
+    bscale = np.full(K // 16, E4M3_ONE, np.uint8)
+    bscale[16] = E4M3_ONE_AND_HALF
+    assert dot4(codes, bscale, x, EXACT) == 2.5
+    assert dot4(codes, bscale, x, PLAIN) == np.float32(2.5) + np.float32(2.0 ** -22)
+
+
 @pytest.fixture(scope="module")
 def quantised():
     return synth.normal_nvfp4_rows(1234, 5, 48, 320)
