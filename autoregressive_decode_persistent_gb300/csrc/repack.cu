@@ -1,7 +1,8 @@
 // Copy the caller's row-major weight matrices into the model-owned image, in the order each
 // persistent CTA consumes them: for CTA c, its units [u0, u0 + n) in rounds of `upr` units,
-// each round as K-chunks, each chunk as [unit][row][KC elements].  One TMA bulk copy then
-// moves one tile.  Runs once, at model creation.
+// each round as K-chunks, each chunk as [unit][row][KC elements] (NVFP4: the chunk's codes as
+// [unit][row][KC / 2 bytes], then its block scales as [unit][row][KC / 16 bytes]).  One TMA bulk
+// copy then moves one tile.  Runs once, at model creation.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
