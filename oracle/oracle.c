@@ -333,6 +333,13 @@ static int gemv(const void* Wt, int dt, int rows, int K, const float* x, const f
   return fail ? ORC_ENOMEM : ORC_OK;
 }
 
+/* Exported for the pins: gemv of one matrix. */
+int orc_gemv(const void* Wt, int dt, int rows, int K, const float* x, const float* scale, const uint8_t* bscale,
+             float* y, int mode) {
+  orc_init();
+  return gemv(Wt, dt, rows, K, x, scale, bscale, y, mode);
+}
+
 /* RMSNorm: xn_i = x_i * (mean(x^2) + eps)^(-1/2) * g_i. */
 void orc_rmsnorm(const float* x, const void* g, int gdt, int d, float eps, int mode, float* out) {
   float ss = mode == ORC_EXACT ? orc_dot_exact(x, x, d, 8) : orc_dot_plain(x, x, d);

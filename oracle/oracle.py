@@ -90,6 +90,8 @@ def lib():
             L.orc_round_bf16.restype = ctypes.c_uint16
             L.orc_e4m3_table.argtypes = []
             L.orc_e4m3_table.restype = ctypes.POINTER(ctypes.c_float)
+            L.orc_gemv.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_int]
+            L.orc_gemv.restype = ctypes.c_int
             L.orc_dot_nvfp4.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int]
             L.orc_dot_nvfp4.restype = f32
             L.orc_e2m1_table.argtypes = []

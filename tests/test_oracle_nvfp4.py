@@ -158,3 +158,58 @@ def test_nvfp4_model_differs_from_its_fp16_source():
     d = np.abs(l4 - l16)
     assert d.max() > 1e-3  # not the same weights
     assert np.linalg.norm(l4 - l16) / np.linalg.norm(l16) < 0.3  # but the same model, quantised
+
+
+def gemv(W, dt, rows, K, x, scale, bscale, mode):
+    """The oracle's matrix-vector product (dt: 2 e4m3, 4 NVFP4), one output per row."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    s = np.ascontiguousarray(scale, dtype=np.float32)
+    b = None if bscale is None else np.ascontiguousarray(bscale, dtype=np.uint8)
+    y = np.zeros(rows, np.float32)
+    rc = lib().orc_gemv(W.ctypes.data, dt, rows, K, x.ctypes.data, s.ctypes.data,
+                        None if b is None else b.ctypes.data, y.ctypes.data, mode)
+    assert rc == 0
+    return y
+
+
+@pytest.mark.parametrize("mode", [EXACT, PLAIN])
+@pytest.mark.parametrize("fmt", ["e4m3", "nvfp4"])
+def test_row_scale_multiplies_the_finished_dot(mode, fmt):
+    """Row (+1, -1, 0, ...) against x = (1 + 2^-23, 1, 0, ...) with row scale s = 1 + 2^-23: the
+    dot is 2^-23 exactly, and s times it, 2^-23 + 2^-46, is exact too. Scaling the elements first
+    would round s (1 + 2^-23) to 1 + 2^-22 and return 2^-23."""
+    K = 16
+    x = np.zeros(K, np.float32)
+    x[0], x[1] = np.float32(1.0) + np.float32(2.0 ** -23), 1.0
+    s = np.array([np.float32(1.0) + np.float32(2.0 ** -23)], np.float32)
+    if fmt == "e4m3":
+        W = np.zeros(K, np.uint8)
+        W[0], W[1] = 0x38, 0xB8  # e4m3 +1, -1
+        y = gemv(W, 2, 1, K, x, s, None, mode)
+    else:
+        codes = np.zeros(K, np.int64)
+        codes[0], codes[1] = 2, 10  # E2M1 +1, -1
+        y = gemv(_pack(codes), 4, 1, K, x, s, np.array([E4M3_ONE], np.uint8), mode)
+    assert float(y[0]) == 2.0 ** -23 + 2.0 ** -46
+
+
+@pytest.mark.parametrize("mode", [EXACT, PLAIN])
+def test_nvfp4_rows_are_exact_with_representable_operands(mode):
+    """Several rows, power-of-two row and block scales, inputs in multiples of 1/4: each output is
+    the exact rational row dot times its row scale (a row or block misplaced between rows fails)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(5)
+    rows, K = 6, 256
+    codes = rng.integers(0, 16, (rows, K))
+    kb = rng.integers(-2, 3, (rows, K // 16))
+    kr = rng.integers(-4, 5, rows)
+    x = (rng.integers(-3, 4, K) / 4.0).astype(np.float32)
+    packed = np.stack([_pack(c) for c in codes])
+    bscale = ((kb + 7) << 3).astype(np.uint8)
+    scale = (2.0 ** kr).astype(np.float32)
+    y = gemv(packed, 4, rows, K, x, scale, bscale, mode)
+    for r in range(rows):
+        want = sum(Fraction(E2M1_VALUES[codes[r, j]]) * Fraction(2) ** int(kb[r, j // 16]) * Fraction(float(x[j]))
+                   for j in range(K)) * Fraction(2) ** int(kr[r])
+        assert Fraction(float(y[r])) == want, r
