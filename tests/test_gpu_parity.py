@@ -309,3 +309,17 @@ def test_model_destroyed_before_its_caches(torch_cuda):
         adp.adp_kv_reset(h)
     assert e.value.code == adp.ADP_ERR_INVALID_ARG
     kv.close()
+
+
+@pytest.mark.parametrize("name", ["tiny", "dense-2.3b-nvfp4", "moe-32x1408-top4-e4m3"])
+def test_host_plan_is_the_models_plan(torch_cuda, name):
+    """adp_plan on the host, for this GPU's SM count, gives the weight image and phase list the
+    created model streams."""
+    from autoregressive_decode_persistent_gb300 import adp
+    from autoregressive_decode_persistent_gb300.model import make_config
+    cfg = synth.get_config(name) if name == "tiny" else synth.shrink(synth.get_config(name))
+    model = _model(cfg, synth.model_weights(cfg), mode=1)
+    ph, img = adp.adp_plan(make_config(cfg), model.num_ctas)
+    assert img == model.image_bytes
+    assert len(ph) - 1 == model.launches_per_step  # one launch per phase but the last (sampling)
+    model.close()
