@@ -1433,6 +1433,10 @@ extern "C" int adp_plan(const adp_config* cfg, int32_t n_sms, adp_phase_plan* ou
     o.n_chunks = P.n_chunks;
     o.upr = P.upr;
     o.dtype = P.has_weights ? P.wdt : -1;
+    o.src_phase = P.src_ph;
+    o.res_phase = P.res_ph;
+    o.sel_phase = P.sel_ph;
+    o.pad = 0;
     o.region = P.region;
     o.expert_stride = P.expert_stride;
   }

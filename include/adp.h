@@ -277,6 +277,10 @@ typedef struct {
   int32_t n_chunks;   /* ceil(K / KC) */
   int32_t upr;        /* units per round of a CTA (a tile is min(upr, units left) x one K-chunk) */
   int32_t dtype;      /* adp_dtype of the phase's weights, -1 without weights */
+  int32_t src_phase;  /* phase whose output vector this phase reads (-1: the embedding row) */
+  int32_t res_phase;  /* phase that wrote the residual rows this phase adds to (-1: none) */
+  int32_t sel_phase;  /* router phase whose logits choose this phase's experts (-1: none) */
+  int32_t pad;
   uint64_t region;        /* byte offset of the phase's region in the weight image */
   uint64_t expert_stride; /* bytes of the region (per expert), a multiple of 256 */
 } adp_phase_plan;

@@ -230,3 +230,36 @@ def test_streamed_bytes_are_the_roofline_bytes(adp, cfg):
     if cfg["n_experts"]:
         in_place += L * cfg["top_k"] * (2 * cfg["d_expert"] + d) * 4  # expert output-channel scales
     assert streamed + in_place == bound.weight_bytes_per_token(cfg)
+
+
+@pytest.mark.parametrize("cfg", CASES, ids=IDS)
+def test_each_phase_waits_on_the_phases_that_produce_its_inputs(adp, cfg):
+    """The step's dataflow, from the model's definition: QKV reads the residual x (layer 0: the
+    embedding row, which layer 0's QKV phase publishes as x), attention reads QKV, Wo reads the
+    attention output and adds to x, gate|up (or the router and the experts' gate|up) reads x,
+    down reads the FFN activations and adds to x, the experts take the router's choice, and the
+    LM head reads the last x. Every awaited phase comes earlier in the step."""
+    ph, _ = _plan(adp, cfg)
+    x_writer = -1  # latest writer of the residual
+    router = -1
+    for i, p in enumerate(ph):
+        k = p["kind"]
+        want = {KINDS["qkv"]: (x_writer, -1, -1), KINDS["lm"]: (x_writer, -1, -1), KINDS["sample"]: (-1, -1, -1)}
+        if k == KINDS["attn"]:
+            want[k] = (i - 1, -1, -1)
+        elif k == KINDS["wo"]:
+            want[k] = (i - 1, x_writer, -1)
+        elif k in (KINDS["gu"], KINDS["router"]):
+            want[k] = (x_writer, -1, -1)
+        elif k == KINDS["egu"]:
+            want[k] = (x_writer, -1, router)
+        elif k in (KINDS["down"], KINDS["edown"]):
+            want[k] = (i - 1, x_writer, router if k == KINDS["edown"] else -1)
+        assert (p["src_phase"], p["res_phase"], p["sel_phase"]) == want[k], (i, p)
+        assert all(j < i for j in (p["src_phase"], p["res_phase"], p["sel_phase"]))
+        if k == KINDS["qkv"] and p["layer"] == 0:
+            x_writer = i  # x = the embedding row, published by layer 0's QKV phase
+        elif k in (KINDS["wo"], KINDS["down"], KINDS["edown"]):
+            x_writer = i
+        elif k == KINDS["router"]:
+            router = i
