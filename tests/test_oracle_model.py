@@ -64,6 +64,15 @@ def test_shrunk_workloads_against_brute_force(name):
     check_against_brute(cfg, 8, 24)
 
 
+@pytest.mark.parametrize("overrides", [{"embed_dtype": "bf16"}, {"tied_embeddings": False},
+                                       {"head_dim": 128, "n_heads": 4, "n_kv_heads": 4, "d_model": 512}])
+def test_nvfp4_variants_against_brute_force(overrides):
+    """NVFP4 layer matrices with a bf16 embedding / LM head / gains, with an untied LM head, and
+    with 128-wide heads (MHA): the paths around the 4-bit matrices the 2.3B case does not take."""
+    cfg = synth.shrink(synth.get_config("dense-2.3b-nvfp4"), **overrides)
+    check_against_brute(cfg, 8, 12)
+
+
 def test_multi_head_attention_variant_against_brute_force():
     cfg = synth.shrink(synth.get_config("tiny"), n_kv_heads=4, n_heads=4)
     check_against_brute(cfg, 8, 16)
