@@ -44,9 +44,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "batch-1 decode tokens/s/request (2.3B fp16); achieved HBM GB/s vs GB300 peak"
 WORKLOAD = "dense-2.3b-fp16"
-# --workload: the 2.3B model as benchmarked (default), or with e4m3 or NVFP4 layer matrices (the
-# "next" row of low-precision dense weights; same shape, per-row fp32 scales (NVFP4: and an e4m3
-# scale per 16 elements), fp16 embedding and tied LM head)
+# --workload: the 2.3B model as benchmarked (default), or with e4m3 or NVFP4 layer matrices
+# (low-precision dense weights; same shape, per-row fp32 scales (NVFP4: and an e4m3 scale per 16
+# elements), fp16 embedding and tied LM head)
 WORKLOADS = {
     "dense-2.3b-fp16": {"metric": METRIC, "weights": "f16",
                         "data": "synthetic: seeded N(0,0.02) fp16 weights, 512 uniform-random prompt ids"},
