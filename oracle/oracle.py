@@ -22,15 +22,20 @@ _lock = threading.Lock()
 _lib = None
 
 
+def compile_c(src: str, out: str) -> str:
+    """Compile an oracle source file into a shared library with the oracle's flags."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11", "-ffp-contract=off",
+                           "-Wall", "-o", tmp, src, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
 def build_lib(force: bool = False) -> str:
     src = os.path.join(_HERE, "oracle.c")
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(src):
         return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11", "-ffp-contract=off",
-                           "-Wall", "-o", tmp, src, "-lm"])
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    return compile_c(src, _LIB_PATH)
 
 
 class Config(ctypes.Structure):
@@ -57,47 +62,52 @@ class Weights(ctypes.Structure):
                 ("layers", ctypes.POINTER(Layer))]
 
 
+def load(path: str):
+    """oracle.c's functions from a compiled copy at `path`, with their signatures set."""
+    L = ctypes.CDLL(path)
+    vp, f32, i32 = ctypes.c_void_p, ctypes.c_float, ctypes.c_int32
+    L.orc_init.argtypes = []
+    L.orc_step.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp, vp, i32, i32, i32, f32, f32,
+                           vp, vp, vp, vp, vp, vp]
+    L.orc_step.restype = ctypes.c_int
+    L.orc_exp_c.argtypes = [f32]
+    L.orc_exp_c.restype = f32
+    L.orc_dot_exact.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int]
+    L.orc_dot_exact.restype = f32
+    L.orc_dot_plain.argtypes = [vp, vp, ctypes.c_int]
+    L.orc_dot_plain.restype = f32
+    L.orc_rmsnorm.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, f32, ctypes.c_int, vp]
+    L.orc_rope_row.argtypes = [f32, ctypes.c_int, ctypes.c_int, vp, vp]
+    L.orc_rope.argtypes = [vp, ctypes.c_int, ctypes.c_int, f32, ctypes.c_int]
+    L.orc_attention_head.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, f32,
+                                     ctypes.c_int, vp]
+    L.orc_route.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp]
+    L.orc_argmax.argtypes = [vp, ctypes.c_int]
+    L.orc_argmax.restype = i32
+    L.orc_sample.argtypes = [vp, ctypes.c_int, f32, f32, ctypes.c_int]
+    L.orc_sample.restype = i32
+    L.orc_round_f16.argtypes = [f32]
+    L.orc_round_f16.restype = ctypes.c_uint16
+    L.orc_round_bf16.argtypes = [f32]
+    L.orc_round_bf16.restype = ctypes.c_uint16
+    L.orc_e4m3_table.argtypes = []
+    L.orc_e4m3_table.restype = ctypes.POINTER(ctypes.c_float)
+    L.orc_gemv.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_int]
+    L.orc_gemv.restype = ctypes.c_int
+    L.orc_dot_nvfp4.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int]
+    L.orc_dot_nvfp4.restype = f32
+    L.orc_e2m1_table.argtypes = []
+    L.orc_e2m1_table.restype = ctypes.POINTER(ctypes.c_float)
+    L.orc_init()
+    return L
+
+
 def lib():
     global _lib
     with _lock:
         if _lib is None:
             build_lib()
-            L = ctypes.CDLL(_LIB_PATH)
-            vp, f32, i32 = ctypes.c_void_p, ctypes.c_float, ctypes.c_int32
-            L.orc_init.argtypes = []
-            L.orc_step.argtypes = [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp, vp, i32, i32, i32, f32, f32,
-                                   vp, vp, vp, vp, vp, vp]
-            L.orc_step.restype = ctypes.c_int
-            L.orc_exp_c.argtypes = [f32]
-            L.orc_exp_c.restype = f32
-            L.orc_dot_exact.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int]
-            L.orc_dot_exact.restype = f32
-            L.orc_dot_plain.argtypes = [vp, vp, ctypes.c_int]
-            L.orc_dot_plain.restype = f32
-            L.orc_rmsnorm.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, f32, ctypes.c_int, vp]
-            L.orc_rope_row.argtypes = [f32, ctypes.c_int, ctypes.c_int, vp, vp]
-            L.orc_rope.argtypes = [vp, ctypes.c_int, ctypes.c_int, f32, ctypes.c_int]
-            L.orc_attention_head.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, f32,
-                                             ctypes.c_int, vp]
-            L.orc_route.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp]
-            L.orc_argmax.argtypes = [vp, ctypes.c_int]
-            L.orc_argmax.restype = i32
-            L.orc_sample.argtypes = [vp, ctypes.c_int, f32, f32, ctypes.c_int]
-            L.orc_sample.restype = i32
-            L.orc_round_f16.argtypes = [f32]
-            L.orc_round_f16.restype = ctypes.c_uint16
-            L.orc_round_bf16.argtypes = [f32]
-            L.orc_round_bf16.restype = ctypes.c_uint16
-            L.orc_e4m3_table.argtypes = []
-            L.orc_e4m3_table.restype = ctypes.POINTER(ctypes.c_float)
-            L.orc_gemv.argtypes = [vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp, ctypes.c_int]
-            L.orc_gemv.restype = ctypes.c_int
-            L.orc_dot_nvfp4.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int]
-            L.orc_dot_nvfp4.restype = f32
-            L.orc_e2m1_table.argtypes = []
-            L.orc_e2m1_table.restype = ctypes.POINTER(ctypes.c_float)
-            L.orc_init()
-            _lib = L
+            _lib = load(_LIB_PATH)
     return _lib
 
 
@@ -112,8 +122,10 @@ def _c(a):
 class OracleModel:
     """Host model + host KV cache; `step` runs one decode step in the chosen mode."""
 
-    def __init__(self, cfg: dict, W: dict):
+    def __init__(self, cfg: dict, W: dict, library=None):
+        """library: the compiled oracle to call (default: oracle.c as built by build_lib)."""
         self.cfg = cfg
+        self._lib = library
         self.W = W
         c = cfg
         self.c = Config(c["n_layers"], c["d_model"], c["n_heads"], c["n_kv_heads"], c["head_dim"],
@@ -165,7 +177,7 @@ class OracleModel:
         gate = np.zeros((c["n_layers"], k), dtype=np.float32)
         tr = np.zeros((c["n_layers"] + 1, c["d_model"]), dtype=np.float32) if trace else None
         fz = None if force is None else np.ascontiguousarray(force, dtype=np.int32)
-        rc = lib().orc_step(ctypes.byref(self.c), ctypes.byref(self.w), _p(self.kc), _p(self.vc), pos, int(token),
+        rc = (self._lib or lib()).orc_step(ctypes.byref(self.c), ctypes.byref(self.w), _p(self.kc), _p(self.vc), pos, int(token),
                             mode, float(temperature), float(u), _p(fz), _p(logits), _p(nxt), _p(sel), _p(gate),
                             _p(tr))
         if rc != 0:
