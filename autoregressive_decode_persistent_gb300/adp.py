@@ -12,6 +12,14 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libadp.so")
+# The test build (libadp_test.so) also exports the test-only hooks; it is loaded instead of the
+# release library when the environment sets ADP_TEST_HOOKS=1 (the test suite does).
+TEST_LIB_PATH = os.path.join(_HERE, "libadp_test.so")
+TEST_HOOKS = ("adp_debug_set_epoch_base", "adp_debug_set_wait_limit", "adp_debug_skip_publication")
+
+
+def default_library_path() -> str:
+    return TEST_LIB_PATH if os.environ.get("ADP_TEST_HOOKS") == "1" else LIB_PATH
 
 ADP_F16, ADP_BF16, ADP_E4M3, ADP_F32, ADP_NVFP4 = 0, 1, 2, 3, 4
 DTYPES = {"f16": ADP_F16, "bf16": ADP_BF16, "e4m3": ADP_E4M3, "f32": ADP_F32, "nvfp4": ADP_NVFP4}
@@ -122,6 +130,7 @@ _SIGS = [
                                                 ctypes.POINTER(ctypes.c_int32)]),
     ("adp_debug_barriers", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     ("adp_debug_set_l2_lookahead", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
+    ("adp_debug_set_prefetch_flags", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
     ("adp_debug_set_ring_slots", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     ("adp_debug_ring_slots", ctypes.c_int, [ctypes.c_void_p]),
     ("adp_debug_set_epoch_base", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
@@ -135,17 +144,26 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     global _lib
     if _lib is not None and path is None:
         return _lib
-    p = path or LIB_PATH
+    p = path or default_library_path()
     if not os.path.exists(p):
         raise RuntimeError(f"{p} is missing: the CUDA engine must be built (no CPU fallback exists)")
     L = ctypes.CDLL(p)
     for name, res, args in _SIGS:
+        if name in TEST_HOOKS and not hasattr(L, name):
+            continue  # the release build: calling the hook raises below
         f = getattr(L, name)
         f.restype = res
         f.argtypes = args
     if path is None:
         _lib = L
     return L
+
+
+def _hook(name: str):
+    L = load_library()
+    if not hasattr(L, name):
+        raise RuntimeError(f"{name} is a test-only hook: load the test build (ADP_TEST_HOOKS=1, libadp_test.so)")
+    return getattr(L, name)
 
 
 def _check(rc: int, where: str):
@@ -385,6 +403,10 @@ def adp_debug_set_l2_lookahead(model, nbytes: int):
     _check(load_library().adp_debug_set_l2_lookahead(model, int(nbytes)), "adp_debug_set_l2_lookahead")
 
 
+def adp_debug_set_prefetch_flags(model, flags: int):
+    _check(load_library().adp_debug_set_prefetch_flags(model, int(flags)), "adp_debug_set_prefetch_flags")
+
+
 def adp_debug_set_ring_slots(model, slots: int):
     _check(load_library().adp_debug_set_ring_slots(model, int(slots)), "adp_debug_set_ring_slots")
 
@@ -394,12 +416,12 @@ def adp_debug_ring_slots(model) -> int:
 
 
 def adp_debug_set_epoch_base(model, base: int):
-    _check(load_library().adp_debug_set_epoch_base(model, int(base)), "adp_debug_set_epoch_base")
+    _check(_hook("adp_debug_set_epoch_base")(model, int(base)), "adp_debug_set_epoch_base")
 
 
 def adp_debug_set_wait_limit(model, ns: int):
-    _check(load_library().adp_debug_set_wait_limit(model, int(ns)), "adp_debug_set_wait_limit")
+    _check(_hook("adp_debug_set_wait_limit")(model, int(ns)), "adp_debug_set_wait_limit")
 
 
 def adp_debug_skip_publication(model, cta: int, phase: int):
-    _check(load_library().adp_debug_skip_publication(model, int(cta), int(phase)), "adp_debug_skip_publication")
+    _check(_hook("adp_debug_skip_publication")(model, int(cta), int(phase)), "adp_debug_skip_publication")

@@ -3,6 +3,11 @@
 Six translation units compiled in parallel, then linked as a shared library with the
 static CUDA runtime. -fmad=false keeps every multiply-add that the arithmetic contract does
 not fuse explicitly as a separate multiply and add; no fast-math flags.
+
+A second library, libadp_test.so, links the same objects with the host engine compiled once more
+under -DADP_TEST_HOOKS: it also exports the test-only hooks (withholding a phase's outputs,
+shortening the in-kernel waits, moving the epoch counter).  The tests load it; the release
+library, which the benchmark and applications load, does not carry those hooks.
 """
 from __future__ import annotations
 
@@ -14,6 +19,7 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libadp.so")
+TEST_LIB = os.path.join(HERE, "libadp_test.so")
 SOURCES = ["decode.cu", "decode_batch.cu", "prefill.cu", "repack.cu", "engine.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
@@ -37,14 +43,14 @@ FLAGS_STAMP = os.path.join(HERE, "_build", "flags.txt")
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(TEST_LIB):
         return True
     try:
         if open(FLAGS_STAMP).read() != " ".join(_extra_flags()):
             return True
     except OSError:
         return True
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(TEST_LIB))
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     deps.append(os.path.join(os.path.dirname(HERE), "include", "adp.h"))
     return any(os.path.getmtime(d) > t for d in deps)
@@ -57,9 +63,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     outdir = os.path.join(HERE, "_build")
     os.makedirs(outdir, exist_ok=True)
 
-    def compile_one(src):
-        obj = os.path.join(outdir, src.replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *FLAGS, *_extra_flags(), "-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(job):
+        src, extra, obj_name = job
+        obj = os.path.join(outdir, obj_name)
+        cmd = [cc, *ARCH, *FLAGS, *_extra_flags(), *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stderr}")
@@ -67,14 +74,19 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
+    jobs = [(src, [], src.replace(".cu", ".o")) for src in SOURCES]
+    jobs.append(("engine.cu", ["-DADP_TEST_HOOKS"], "engine_hooks.o"))
+    with cf.ThreadPoolExecutor(len(jobs)) as ex:
+        objs = list(ex.map(compile_one, jobs))
+    release = objs[:len(SOURCES)]
+    test = [o if not o.endswith(os.sep + "engine.o") else objs[-1] for o in release]
+    for lib, members in ((LIB, release), (TEST_LIB, test)):
+        tmp = lib + f".tmp{os.getpid()}"
+        cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *members]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stderr}")
+        os.replace(tmp, lib)
     with open(FLAGS_STAMP, "w") as fh:
         fh.write(" ".join(_extra_flags()))
     return LIB

@@ -316,6 +316,10 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   CK(cudaGetDeviceProperties(&prop, m->device));
   if (!prop.cooperativeLaunch) return ADP_ERR_NOT_CORESIDENT;
   m->G = prop.multiProcessorCount;  // one persistent CTA per SM
+  {
+    const int rc = noalloc_prepare_device(m->device);  // the static scratch of adp_decode_step_noalloc
+    if (rc) return rc;
+  }
   plan(m);
   for (const PhaseDesc& P : m->phases)  // per-CTA shares are computed in 32-bit arithmetic
     if ((uint64_t)P.n_units * (uint64_t)m->G >= (1ull << 32)) return ADP_ERR_UNSUPPORTED_CONFIG;
@@ -357,6 +361,8 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   }
   if (!nslots) return ADP_ERR_UNSUPPORTED_CONFIG;
   xbytes = (xbytes + 127) & ~(size_t)127;
+  // the attention merge stages at least one block's outputs after the block maxima and sums
+  if ((long long)(xbytes / 4) - ((2 * nbmax_ + 2 + 3) & ~3) < hd) return ADP_ERR_UNSUPPORTED_CONFIG;
   m->xbuf_floats = (int)(xbytes / 4);
   m->p.xbuf_floats = m->xbuf_floats;
   m->smem = (size_t)nslots * kSlotBytes + xbytes + ctl_bytes((int)m->phases.size());
@@ -538,6 +544,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   p.rope_sin = d_sin;
   p.wait_ns = 200000000ull;
   p.l2_lookahead = 0;
+  p.pf_flags = 0;
   p.n_steps = 1;
   p.skip_cta = -1;
   p.skip_phase = -1;
@@ -1292,6 +1299,8 @@ extern "C" const char* adp_last_error(void) { return g_last_error.c_str(); }
 
 void adp::set_last_error(const char* msg) { g_last_error = msg; }
 
+int adp::model_device(const adp_model* m) { return m ? m->device : -1; }
+
 int adp::scratch_layout(const adp_model* m, ScratchLayout* out) {
   if (!m || !out) return ADP_ERR_INVALID_ARG;
   const adp_config& c = m->cfg;
@@ -1378,6 +1387,7 @@ int adp::decode_step_in_scratch(adp_model* m, adp_kv* kv, int32_t token, const a
   if (!dev_logits) p.logits = reinterpret_cast<float*>(at(lay.logits));
   const int nph = (int)m->phases.size();
   CK(decode_launch(p, 0, T > 0.0f ? nph : nph - 1, true, m->G, m->smem, m->xbuf_floats, m->stream));
+  m->p.skip_cta = m->p.skip_phase = -1;  // the publication test hook covers one step, as in adp_decode_step
   CK(cudaMemcpyAsync(&m->h_out[0], &d_state->out_token, 4, cudaMemcpyDeviceToHost, m->stream));
   CK(cudaMemcpyAsync(&m->h_out[1], p.err, 4, cudaMemcpyDeviceToHost, m->stream));
   CK(cudaStreamSynchronize(m->stream));
@@ -1517,6 +1527,13 @@ extern "C" int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes) {
   return ADP_OK;
 }
 
+extern "C" int adp_debug_set_prefetch_flags(adp_model* m, uint32_t flags) {
+  if (!m || (flags & ~(uint32_t)(PF_KV_AHEAD | PF_KV_LAST | PF_W_LAST))) return ADP_ERR_INVALID_ARG;
+  m->p.pf_flags = flags;
+  if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
+  return ADP_OK;
+}
+
 extern "C" int adp_debug_set_ring_slots(adp_model* m, int32_t slots) {
   if (!m || slots < 3 || slots > m->max_nslots) return ADP_ERR_INVALID_ARG;
   m->p.nslots = slots;  // the shared-memory size stays the one chosen at creation
@@ -1526,6 +1543,9 @@ extern "C" int adp_debug_set_ring_slots(adp_model* m, int32_t slots) {
 
 extern "C" int adp_debug_ring_slots(const adp_model* m) { return m ? m->p.nslots : 0; }
 
+// Test-only hooks: compiled into the test build of the library (-DADP_TEST_HOOKS) only, so that a
+// release caller cannot make a model withhold outputs, shorten its waits or move its epoch counter.
+#ifdef ADP_TEST_HOOKS
 extern "C" int adp_debug_set_epoch_base(adp_model* m, uint32_t base) {
   if (!m) return ADP_ERR_INVALID_ARG;
   CK(cudaStreamSynchronize(m->stream));
@@ -1550,3 +1570,4 @@ extern "C" int adp_debug_skip_publication(adp_model* m, int32_t cta, int32_t pha
   m->p.skip_phase = phase;
   return ADP_OK;
 }
+#endif  // ADP_TEST_HOOKS

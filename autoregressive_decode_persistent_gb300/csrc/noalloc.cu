@@ -2,6 +2,10 @@
 // file instead of in buffers that the model allocated, so that the call itself allocates no
 // device memory (no cudaMalloc/cudaFree, no allocating library routine).
 //
+// The array's device address is looked up per device by adp_create_model (with the model's device
+// current), because that lookup may load this file's module, and loading the module is what puts
+// the array in device memory: creation allocates anyway, the no-alloc call must not.
+//
 // Every call, from every model, shares the one array.  Its contents must start at zero: they do
 // when the module is loaded, every completed step leaves them in a state the next step accepts
 // (attention and sampling counters back at zero, the epoch base advanced past every tag written),
@@ -35,6 +39,28 @@ DeviceSlot g_slots[kMaxDevices];
 
 static __device__ __align__(256) unsigned char g_step_scratch[kStaticScratchBytes];
 
+int adp::noalloc_prepare_device(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) {
+    adp::set_last_error("adp_create_model: CUDA device index beyond the no-alloc step's device table");
+    return ADP_ERR_UNSUPPORTED_CONFIG;
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceSlot& s = g_slots[dev];
+  if (s.addr) return ADP_OK;
+  // set-up, once per device, with that device current (the caller's contract)
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_step_scratch);
+  if (e != cudaSuccess || !ptr) {
+    char msg[200];
+    std::snprintf(msg, sizeof msg, "adp_create_model: cudaGetSymbolAddress of the no-alloc scratch: %s",
+                  cudaGetErrorString(e));
+    adp::set_last_error(msg);
+    return ADP_ERR_CUDA;
+  }
+  s.addr = static_cast<unsigned char*>(ptr);
+  return ADP_OK;
+}
+
 extern "C" int adp_decode_step_noalloc(adp_model* m, adp_kv* kv, int32_t token, const adp_sampling* sampling,
                                        int32_t* next_token, float* dev_logits) {
   adp::ScratchLayout lay;
@@ -49,24 +75,25 @@ extern "C" int adp_decode_step_noalloc(adp_model* m, adp_kv* kv, int32_t token, 
     return ADP_ERR_UNSUPPORTED_CONFIG;
   }
   int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
+  const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     adp::set_last_error("adp_decode_step_noalloc: no usable current CUDA device");
     return ADP_ERR_CUDA;
   }
+  if (dev != adp::model_device(m)) {
+    // the array of one device and a stream of another would not meet: refuse before any work
+    char msg[200];
+    std::snprintf(msg, sizeof msg,
+                  "adp_decode_step_noalloc: the current CUDA device (%d) is not the model's device (%d)", dev,
+                  adp::model_device(m));
+    adp::set_last_error(msg);
+    return ADP_ERR_INVALID_ARG;
+  }
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceSlot& s = g_slots[dev];
-  if (!s.addr) {
-    // set-up, once per device, with that device current
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_step_scratch);
-    if (e != cudaSuccess || !ptr) {
-      char msg[200];
-      std::snprintf(msg, sizeof msg, "adp_decode_step_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-      adp::set_last_error(msg);
-      return ADP_ERR_CUDA;
-    }
-    s.addr = static_cast<unsigned char*>(ptr);
+  if (!s.addr) {  // adp_create_model sets every model's device up; nothing is looked up (or loaded) here
+    adp::set_last_error("adp_decode_step_noalloc: the device's static scratch was not set up");
+    return ADP_ERR_CUDA;
   }
   // A model with another layout would read words that the last one left at other offsets.
   // ... and 32-bit epoch tags must not run past 2^32: start over before they would.

@@ -140,6 +140,7 @@ struct Params {
   unsigned long long* timeline; // [G][n_phases][kStamps] %globaltimer stamps or null
   uint64_t wait_ns;            // limit of every in-kernel wait
   uint32_t l2_lookahead;       // bytes of weight stream prefetched into L2 beyond the TMA loads
+  uint32_t pf_flags;           // PF_* bits: how the KV cache and the weight lookahead are prefetched
   int32_t debug_barriers;      // 1: also take a grid barrier after every phase (debugging)
   int32_t n_steps;             // decode steps this launch runs back to back (persistent launch)
   int32_t nslots;              // weight ring depth (slots of kSlotBytes)
@@ -165,6 +166,12 @@ struct Params {
 ADP_HD inline uint64_t wbytes(const PhaseDesc& P, uint64_t n) {
   return P.wdt == DT_NVFP4 ? n / 16 * 9 : n * (uint64_t)P.eb;
 }
+
+// Prefetch options (Params::pf_flags).  PF_KV_AHEAD: a layer's attention K/V blocks are brought
+// into L2 one layer early (during the previous layer's QKV phase) instead of during its own QKV
+// phase; PF_KV_LAST / PF_W_LAST: those K/V prefetches / the weight-stream lookahead carry the L2
+// evict-last priority.
+enum PrefetchFlags : uint32_t { PF_KV_AHEAD = 1u, PF_KV_LAST = 2u, PF_W_LAST = 4u };
 
 // Device error codes (the host maps them to ADP_ERR_*).
 enum DevErr : int32_t { DE_NONE = 0, DE_BARRIER_TIMEOUT = 1, DE_PIPELINE_TIMEOUT = 2 };  // 1: a dependency wait

@@ -32,4 +32,13 @@ int decode_step_in_scratch(adp_model* m, adp_kv* kv, int32_t token, const adp_sa
 // Record a message for adp_last_error().
 void set_last_error(const char* msg);
 
+// The CUDA device a model was created on (-1 for a null model).
+int model_device(const adp_model* m);
+
+// Set-up of adp_decode_step_noalloc for the current device (noalloc.cu): looks up the device
+// address of the static scratch array once per device.  Called by adp_create_model with the
+// model's device current, where allocation is expected: loading the array's module is what places
+// the array in device memory, so no later no-alloc call on that device can be the one that does.
+int noalloc_prepare_device(int device);
+
 }  // namespace adp

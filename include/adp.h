@@ -179,9 +179,12 @@ int adp_decode_step(adp_model* m, adp_kv* kv, int32_t token, const adp_sampling*
  * that cannot take the device-wide synchronisation that cudaMalloc and cudaFree may cause.
  * Arguments, results and the kernel are those of adp_decode_step (always the single persistent
  * launch), with the same output; the model's own scratch is left untouched.
- *  - The first call on a device sets up: with that device current it looks up the array's device
- *    address (cudaGetSymbolAddress, which may make the CUDA runtime load the array's module).
- *    Make that first call before any stream capture begins.  The model's device must be current.
+ *  - Set-up happens in adp_create_model, not here: with the model's device current it looks up the
+ *    array's device address once per device (cudaGetSymbolAddress, which may make the CUDA runtime
+ *    load the library module holding the array, and so place the 8 MiB array in device memory).
+ *    So the first no-alloc call on a device allocates nothing either.
+ *  - The model's device must be the current device; otherwise ADP_ERR_INVALID_ARG (with a message in
+ *    adp_last_error()) is returned before anything runs.
  *  - A model whose step needs more than 8 MiB of scratch (dominated by 8 * n_heads *
  *    ceil(max_ctx / 32) * head_dim bytes of attention partials plus 4 * vocab bytes of logits) is
  *    rejected with ADP_ERR_UNSUPPORTED_CONFIG before anything runs; adp_last_error() gives both sizes.
@@ -332,12 +335,21 @@ int adp_debug_barriers(adp_model* m, int on);
  * loads (default 0 = off).  A tuning knob: it lets HBM keep streaming while the compute
  * warps wait at barriers. */
 int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes);
+/* How the step prefetches into L2 (bits; default 0): 1 = each layer's attention K/V blocks one
+ * layer early (during the previous layer's QKV phase), 2 = those K/V prefetches with the L2
+ * evict-last priority, 4 = the weight lookahead with the evict-last priority.  Other bits:
+ * ADP_ERR_INVALID_ARG.  A tuning knob; results do not depend on it. */
+int adp_debug_set_prefetch_flags(adp_model* m, uint32_t flags);
 /* Depth of the per-CTA weight ring in 32 KB slots: the model takes the deepest ring (at most 6)
  * that fits beside its other shared-memory buffers; this lowers it (3 <= slots <= that depth,
  * else ADP_ERR_INVALID_ARG), for measurements.  adp_debug_ring_slots reads the current depth. */
 int adp_debug_set_ring_slots(adp_model* m, int32_t slots);
 int adp_debug_ring_slots(const adp_model* m);
-/* Test hook: clear the exchange buffers and start the model's 32-bit epoch counter at `base`
+#ifdef ADP_TEST_HOOKS
+/* The three hooks below exist only in the test build of the library (libadp_test.so, compiled with
+ * -DADP_TEST_HOOKS); the release build (libadp.so) does not export them.
+ *
+ * Test hook: clear the exchange buffers and start the model's 32-bit epoch counter at `base`
  * (the engine clears and restarts it by itself before a step would run past 2^32). */
 int adp_debug_set_epoch_base(adp_model* m, uint32_t base);
 /* Wait limit of every in-kernel spin (grid barrier, weight pipeline), nanoseconds (default 2e8). */
@@ -346,6 +358,7 @@ int adp_debug_set_wait_limit(adp_model* m, uint64_t ns);
  * so that every phase waiting for them runs out of time and the step returns
  * ADP_ERR_BARRIER_TIMEOUT (a dependency wait ran out) instead of hanging. */
 int adp_debug_skip_publication(adp_model* m, int32_t cta, int32_t phase);
+#endif /* ADP_TEST_HOOKS */
 /* The prefill path's tensor-core GEMM alone (test hook): C[M, N] = A[M, K] W[N, K]^T in fp32, with
  * A and W DEVICE row-major 16-bit matrices (f16, or bf16 when bf16 = 1) and C a DEVICE fp32 [M, N]
  * array.  Tiles the operands into temporary device buffers, runs, synchronises the device. */
