@@ -63,8 +63,8 @@ def test_tiny_full_run_bit_exact(torch_cuda):
 @pytest.mark.parametrize("mode", [1, 2])
 def test_tiny_multikernel_modes_bit_identical_to_persistent(torch_cuda, mode):
     cfg = synth.get_config("tiny")
-    a = _check_case(cfg, 8, 24, mode=0, plain=False)
-    b = _check_case(cfg, 8, 24, mode=mode, plain=False)
+    a = _check_case(cfg, 8, 24, mode=0)
+    b = _check_case(cfg, 8, 24, mode=mode)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
 
@@ -220,15 +220,19 @@ def test_moe_forced_experts_match_oracle(torch_cuda):
     force = np.stack([rng.permutation(cfg["n_experts"])[: cfg["top_k"]] for _ in range(cfg["n_layers"])]).astype(
         np.int32)
     om = OracleModel(cfg, W)
+    om_p = OracleModel(cfg, W)
     model = _model(cfg, W)
     adp.adp_debug_force_experts(model.handle, force)
     kv = model.new_kv()
     lg = torch.empty(cfg["vocab"], device=model.device)
     for t in synth.prompt(cfg, 6):
         ref = om.step(int(t), EXACT, force=force)
+        ref_p = om_p.step(int(t), PLAIN, force=force)
         nxt = kv.step(int(t), logits=lg)
         assert nxt == ref["next"]
-        assert np.array_equal(lg.cpu().numpy().view(np.uint32), ref["logits"].view(np.uint32))
+        got = lg.cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), ref["logits"].view(np.uint32))
+        assert_logits_within_tolerance(got[None], ref_p["logits"][None].astype(np.float64))
 
 
 @pytest.mark.parametrize("name,temperature", [("tiny", 0.7), ("moe-32x1408-top4-e4m3", 0.0),
@@ -237,7 +241,9 @@ def test_moe_forced_experts_match_oracle(torch_cuda):
 def test_in_kernel_multi_step_generation_matches_oracle(torch_cuda, name, temperature):
     """adp_generate_async runs n decode steps in one persistent launch, each step taking the token
     the previous one chose (and, at T > 0, the next uniform): the tokens and the whole KV cache
-    equal the oracle's free run in contract mode."""
+    equal the oracle's free run in contract mode.  One more step on that cache (through
+    adp_decode_step) gives logits within the stated tolerances of the plain oracle run on the same
+    tokens."""
     import torch
     from autoregressive_decode_persistent_gb300 import adp
     cfg = synth.get_config(name) if name == "tiny" else synth.shrink(synth.get_config(name))
@@ -258,6 +264,10 @@ def test_in_kernel_multi_step_generation_matches_oracle(torch_cuda, name, temper
     k, v = kv.read()
     m = len(prompt) + n
     assert np.array_equal(k[:, :, :m], om.kc[:, :, :m]) and np.array_equal(v[:, :, :m], om.vc[:, :, :m])
+    lg = torch.empty(cfg["vocab"], device=model.device)
+    kv.step(nexts[-1], logits=lg)
+    ref_p, _, _ = oracle_forced(cfg, W, toks + [nexts[-1]], PLAIN)
+    assert_logits_within_tolerance(lg.cpu().numpy()[None], ref_p[-1:])
     model.close()
 
 
