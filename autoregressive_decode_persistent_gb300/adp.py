@@ -131,6 +131,8 @@ _SIGS = [
     ("adp_debug_barriers", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     ("adp_debug_set_l2_lookahead", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
     ("adp_debug_set_prefetch_flags", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
+    ("adp_measure_read_bandwidth", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int32, ctypes.c_void_p,
+                                                  ctypes.POINTER(ctypes.c_double)]),
     ("adp_debug_set_ring_slots", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
     ("adp_debug_ring_slots", ctypes.c_int, [ctypes.c_void_p]),
     ("adp_debug_set_epoch_base", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
@@ -401,6 +403,14 @@ def adp_debug_barriers(model, on: bool):
 
 def adp_debug_set_l2_lookahead(model, nbytes: int):
     _check(load_library().adp_debug_set_l2_lookahead(model, int(nbytes)), "adp_debug_set_l2_lookahead")
+
+
+def adp_measure_read_bandwidth(dev_buf, nbytes: int, reps: int, stream: int = 0) -> float:
+    """GB/s of 16-byte reads over a device buffer (see include/adp.h)."""
+    g = ctypes.c_double()
+    _check(load_library().adp_measure_read_bandwidth(_ptr(dev_buf), int(nbytes), int(reps), stream or None,
+                                                      ctypes.byref(g)), "adp_measure_read_bandwidth")
+    return g.value
 
 
 def adp_debug_set_prefetch_flags(model, flags: int):

@@ -1,6 +1,6 @@
 """Build libadp.so (the engine's C ABI) in-tree with nvcc for sm_103a.
 
-Six translation units compiled in parallel, then linked as a shared library with the
+Seven translation units compiled in parallel, then linked as a shared library with the
 static CUDA runtime. -fmad=false keeps every multiply-add that the arithmetic contract does
 not fuse explicitly as a separate multiply and add; no fast-math flags.
 
@@ -20,7 +20,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libadp.so")
 TEST_LIB = os.path.join(HERE, "libadp_test.so")
-SOURCES = ["decode.cu", "decode_batch.cu", "prefill.cu", "repack.cu", "engine.cu", "noalloc.cu"]
+SOURCES = ["decode.cu", "decode_batch.cu", "prefill.cu", "repack.cu", "engine.cu", "noalloc.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
          "-Xcompiler", "-fvisibility=hidden"]

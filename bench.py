@@ -5,8 +5,11 @@ vocabulary 32000, fp16 weights ~N(0, 0.02) from a seed; a 512-token uniform-rand
 prefilled, then greedy decode steps run at contexts 513..1024 (a run longer than 512 steps
 rewinds the cache to 512 and decodes the window again). One step = one decode step of the
 whole model; the steps of a window run inside one persistent kernel launch.
---workload dense-2.3b-e4m3 (dense-2.3b-nvfp4) measures the same model with e4m3 (NVFP4) layer
-matrices instead.
+--workload names another run: dense-2.3b-fp16-long-t0.7 (the same model after a 3,584-token
+prompt, contexts 3585..4096, temperature 0.7 sampling with the seeded uniform stream),
+dense-8b-bf16 (the 8B model, prompt 1024, contexts 1025..1280), moe-32x1408-top4-e4m3 (the MoE
+model, prompt 256, contexts 257..768), dense-2.3b-e4m3 / dense-2.3b-nvfp4 (the 2.3B shape with e4m3
+or NVFP4 layer matrices).
 --batch N (N >= 2) measures N independent requests decoded together by the batched kernel
 (value = tokens/s of all requests; the default, batch 1, is the benchmark's headline).
 --prefill measures time to first token of the 3,584-token prompt through the tensor-core
@@ -15,11 +18,13 @@ prefill (adp_prefill_tc), beside the decode-kernel prefill.
 Printed (one JSON line, rank 0):
   value      tokens/s, device-timed: the steps chained on the GPU (adp_generate_async), weights
              and KV resident in HBM, CUDA events around the timed region on the model's stream;
+             three timed regions of exactly --steps steps, the median one reported;
   e2e        tokens/s through adp_decode_step with the token in and out of host memory every
              step (a 32-byte step state host->device, 8 bytes device->host, one sync per step);
   roofline   algorithmic bytes per launch (per step: every weight once + KV of the context + the
-             new KV row; up to 512 steps per launch) / average launch duration, against the
-             measured HBM copy bandwidth;
+             new KV row; up to one window of steps per launch) / average launch duration, against
+             the measured HBM copy bandwidth, the nominal 8 TB/s and a read-bandwidth probe run in
+             the same process;
   cpu_baseline  the CPU oracle (plain fp32, all host cores) timed on a bounded sample.
 
 --impl reference times the CPU oracle as the reference arm on the same workload.
@@ -44,25 +49,57 @@ sys.path.insert(0, ROOT)
 
 METRIC = "batch-1 decode tokens/s/request (2.3B fp16); achieved HBM GB/s vs GB300 peak"
 WORKLOAD = "dense-2.3b-fp16"
-# --workload: the 2.3B model as benchmarked (default), or with e4m3 or NVFP4 layer matrices
-# (low-precision dense weights; same shape, per-row fp32 scales (NVFP4: and an e4m3 scale per 16
-# elements), fp16 embedding and tied LM head)
+# --workload: the benchmarked model and run.  The default is the 2.3B fp16 model at contexts
+# 513..1024; the others are the long-context 2.3B run with temperature sampling, the 8B bf16 model,
+# the top-4-of-32 MoE model with e4m3 experts, and the 2.3B shape with e4m3 or NVFP4 layer matrices
+# (per-row fp32 scales; NVFP4 also an e4m3 scale per 16 elements; fp16 embedding and tied LM head).
+# window: decode steps of one pass (contexts prompt + 1 .. prompt + window); temperature: 0 greedy,
+# else sampling with the seeded uniform stream; cpu_steps: cap on the CPU oracle's timed steps.
 WORKLOADS = {
-    "dense-2.3b-fp16": {"metric": METRIC, "weights": "f16",
+    "dense-2.3b-fp16": {"metric": METRIC, "weights": "f16", "window": 512, "temperature": 0.0,
                         "data": "synthetic: seeded N(0,0.02) fp16 weights, 512 uniform-random prompt ids"},
     "dense-2.3b-e4m3": {"metric": "batch-1 decode tokens/s/request (2.3B, e4m3 layer weights); achieved HBM GB/s "
                                   "vs GB300 peak",
                         "weights": "e4m3 layer matrices with per-row f32 scales; f16 embedding, LM head, norms",
+                        "window": 512, "temperature": 0.0,
                         "data": "synthetic: seeded N(0,0.02) weights quantised to e4m3 per row, 512 uniform-random "
                                 "prompt ids"},
     "dense-2.3b-nvfp4": {"metric": "batch-1 decode tokens/s/request (2.3B, NVFP4 layer weights); achieved HBM GB/s "
                                    "vs GB300 peak",
                          "weights": "nvfp4 layer matrices (e2m1, e4m3 scale per 16 elements, f32 row scales); f16 "
                                     "embedding, LM head, norms",
+                         "window": 512, "temperature": 0.0,
                          "data": "synthetic: seeded N(0,0.02) weights quantised to NVFP4 per row and 16-element "
                                  "block, 512 uniform-random prompt ids"},
+    "dense-2.3b-fp16-long-t0.7": {
+        "metric": "batch-1 decode tokens/s/request (2.3B fp16, contexts 3585..4096, T=0.7 sampling); achieved HBM "
+                  "GB/s vs GB300 peak",
+        "weights": "f16", "window": 512, "temperature": 0.7,
+        "data": "synthetic: seeded N(0,0.02) fp16 weights, 3584 uniform-random prompt ids, seeded sampling uniforms"},
+    "dense-8b-bf16": {"metric": "batch-1 decode tokens/s/request (8B bf16); achieved HBM GB/s vs GB300 peak",
+                      "weights": "bf16 (untied LM head)", "window": 256, "temperature": 0.0, "cpu_steps": 16,
+                      "data": "synthetic: seeded N(0,0.02) bf16 weights, 1024 uniform-random prompt ids"},
+    "dense-8b-e4m3": {"metric": "batch-1 decode tokens/s/request (8B, e4m3 layer weights); achieved HBM GB/s vs "
+                                "GB300 peak",
+                      "weights": "e4m3 layer matrices with per-row f32 scales; bf16 embedding, untied LM head, norms",
+                      "window": 256, "temperature": 0.0, "cpu_steps": 16,
+                      "data": "synthetic: seeded N(0,0.02) weights quantised to e4m3 per row, 1024 uniform-random "
+                              "prompt ids"},
+    "dense-8b-nvfp4": {"metric": "batch-1 decode tokens/s/request (8B, NVFP4 layer weights); achieved HBM GB/s vs "
+                                 "GB300 peak",
+                       "weights": "nvfp4 layer matrices (e2m1, e4m3 scale per 16 elements, f32 row scales); bf16 "
+                                  "embedding, untied LM head, norms",
+                       "window": 256, "temperature": 0.0, "cpu_steps": 16,
+                       "data": "synthetic: seeded N(0,0.02) weights quantised to NVFP4 per row and 16-element block, "
+                               "1024 uniform-random prompt ids"},
+    "moe-32x1408-top4-e4m3": {
+        "metric": "batch-1 decode tokens/s/request (MoE, top-4 of 32 e4m3 experts); achieved HBM GB/s vs GB300 peak",
+        "weights": "bf16 attention, embedding and tied LM head; f16 router; e4m3 experts with per-row f32 scales",
+        "window": 512, "temperature": 0.0,
+        "data": "synthetic: seeded N(0,0.02) weights (experts quantised to e4m3 per row), 256 uniform-random prompt "
+                "ids"},
 }
-WINDOW = 512  # decode steps per pass over contexts 513..1024
+WINDOW = 512  # decode steps per pass (set from the workload in main)
 
 
 def _peaks():
@@ -180,7 +217,7 @@ def cpu_baseline(cfg, W, seconds: float = 15.0, max_steps: int | None = None, wa
     return {"value": n / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} plain-fp32 decode steps of the full {cfg['name']} model at contexts "
                       f"{cfg['prompt_len'] + max(1, warmup) + 1}..{cfg['prompt_len'] + max(1, warmup) + n} "
-                      f"(synthetic 512-position KV prefix, {max(1, warmup)} untimed steps first), "
+                      f"(synthetic {cfg['prompt_len']}-position KV prefix, {max(1, warmup)} untimed steps first), "
                       f"OpenMP over {cores} host threads, {el:.1f} s"}, n, el
 
 
@@ -231,6 +268,42 @@ def launch_ablation(model, kv, tok0, P, dev, n):
     return res
 
 
+def workload_text(cfg) -> str:
+    """The workload named by what it is: the model's shape, the prompt and the decode run."""
+    c = cfg
+    w = WORKLOADS[WORKLOAD]
+    ffn = (f"{c['n_experts']} experts x ffn {c['d_expert']} top-{c['top_k']}" if c["n_experts"]
+           else f"ffn {c['d_ff']}")
+    P = c["prompt_len"]
+    how = "greedy" if w["temperature"] <= 0 else f"T = {w['temperature']} sampling"
+    return (f"{WORKLOAD}: {c['n_layers']} layers, d {c['d_model']}, {c['n_heads']}x{c['head_dim']} q heads, "
+            f"{c['n_kv_heads']} kv heads, {ffn}, {'tied' if c['tied_embeddings'] else 'untied'} vocab {c['vocab']}; "
+            f"batch 1, prompt {P}, {how} decode at contexts {P + 1}..{P + w['window']}")
+
+
+def dtype_text(cfg) -> str:
+    """The arithmetic of the path: stored weight and KV types, fp32 accumulation and activations."""
+    c = cfg
+    wt = {"f16": "f16", "bf16": "bf16", "e4m3": "e4m3 (per-row f32 scales)",
+          "nvfp4": "nvfp4 (e4m3 block and f32 row scales)"}[c["weight_dtype"]]
+    if c["n_experts"]:
+        wt += f" attention, {c['expert_dtype']} experts"
+    return f"{wt} weights, {c['kv_dtype']} KV cache, f32 accumulation and activations"
+
+
+def read_probe(dev, nbytes=4 << 30, reps=5):
+    """GB/s of the library's 16-byte read probe over a buffer larger than L2, in this process."""
+    import torch
+    from autoregressive_decode_persistent_gb300 import adp
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    buf.fill_(1)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    gbs = adp.adp_measure_read_bandwidth(buf, nbytes, reps, stream)
+    del buf
+    torch.cuda.empty_cache()
+    return gbs
+
+
 def run_engine(args, rank: int, world: int):
     import torch
 
@@ -245,6 +318,8 @@ def run_engine(args, rank: int, world: int):
     cfg = synth.get_config(WORKLOAD)
     if args.layers:
         cfg["n_layers"] = args.layers  # profiling only: a shorter model with the same layer shapes
+    T = WORKLOADS[WORKLOAD]["temperature"]
+    read_gbs = read_probe(dev)  # before the model: the probe's 4 GB buffer and the weights never coexist
     W = synth.model_weights(cfg)
     prompt = synth.prompt(cfg)
     model = DecodeModel(cfg, W, device=dev)
@@ -253,6 +328,9 @@ def run_engine(args, rank: int, world: int):
     P = cfg["prompt_len"]
     tok0 = kv.prefill(prompt)
     out = torch.empty(WINDOW, dtype=torch.int32, device=dev)
+    # sampling: the seeded uniform of each position of the window, resident on the device
+    us = synth.sampling_uniforms(WINDOW, first=P) if T > 0 else None
+    dev_u = torch.tensor(us, dtype=torch.float32, device=dev) if T > 0 else None
 
     def passes(n_steps):
         """Decode n_steps chained steps in windows of contexts P+1..P+WINDOW."""
@@ -261,7 +339,7 @@ def run_engine(args, rank: int, world: int):
         while left > 0:
             k = min(left, WINDOW)
             kv.truncate(P)
-            kv.generate_async(t, k, out)
+            kv.generate_async(t, k, out, T, dev_u)
             left -= k
 
     # warm-up (untimed)
@@ -270,20 +348,24 @@ def run_engine(args, rank: int, world: int):
     adp.adp_sync(model.handle)
     torch.cuda.synchronize(dev)
 
-    # timed region: device events on the model's stream
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    # three timed regions of exactly args.steps steps each (device events on the model's stream);
+    # the reported one is the median
+    runs = []
     with ClockSampler(local) as clocks:
-        e0.record(stream)
-        passes(args.steps)
-        e1.record(stream)
-        e1.synchronize()
-    adp.adp_sync(model.handle)
-    ms = e0.elapsed_time(e1)
+        for _ in range(3):
+            if world > 1:
+                import torch.distributed as dist
+                dist.barrier()
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            passes(args.steps)
+            e1.record(stream)
+            e1.synchronize()
+            adp.adp_sync(model.handle)
+            runs.append(e0.elapsed_time(e1))
+    ms = statistics.median(runs)
 
     # algorithmic bytes: contexts P+1 .. P+k in each window
     total_bytes = 0
@@ -309,7 +391,7 @@ def run_engine(args, rank: int, world: int):
         if i and i % WINDOW == 0:
             kv.truncate(P)
         s0 = time.perf_counter()
-        t = kv.step(t)
+        t = kv.step(t, T, float(us[i % WINDOW]) if T > 0 else 0.0)
         per_step.append(time.perf_counter() - s0)
     h1 = time.perf_counter()
     per_step.sort()
@@ -324,14 +406,16 @@ def run_engine(args, rank: int, world: int):
         write_timeline(args.timeline, model, kv, tok0, P, cfg)
 
     res = {
-        "ms": ms, "steps": args.steps, "n_launch": n_launch, "step_pct": step_pct, "weight_bytes": bound.weight_bytes_per_token(cfg), "achieved_gbs": achieved, "per_launch_bytes": per_launch,
-        "launch_ms": launch_ms, "peak": peak, "peak_kind": peak_kind, "e2e": e2e, "n_e2e": n_e2e,
-        "clocks": clocks.summary(), "ctas": model.num_ctas, "image_bytes": model.image_bytes,
+        "ms": ms, "runs_ms": runs, "steps": args.steps, "n_launch": n_launch, "step_pct": step_pct,
+        "weight_bytes": bound.weight_bytes_per_token(cfg), "achieved_gbs": achieved, "per_launch_bytes": per_launch,
+        "launch_ms": launch_ms, "peak": peak, "peak_kind": peak_kind, "read_gbs": read_gbs, "e2e": e2e,
+        "n_e2e": n_e2e, "clocks": clocks.summary(), "ctas": model.num_ctas, "image_bytes": model.image_bytes,
         # one cooperative launch per window of chained steps (adp_generate_async)
         "launches": -(-args.steps // WINDOW) * model.launches_per_step, "ablation": ablation,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        res["cpu"] = cpu_baseline(cfg, W, seconds=args.cpu_seconds)[0]
+        res["cpu"] = cpu_baseline(cfg, W, seconds=args.cpu_seconds,
+                                  max_steps=WORKLOADS[WORKLOAD].get("cpu_steps"))[0]
     kv.close()
     model.close()
     return cfg, res
@@ -452,7 +536,7 @@ def emit_batch(args, cfg, res, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": dtype_text(cfg),
         "data": WORKLOADS[WORKLOAD]["data"] + f"; {nb} requests with their own prompts",
         "config": {
             "workload": f"{WORKLOAD} as {nb} independent requests decoded together: each prompt 512, greedy "
@@ -683,18 +767,21 @@ def emit_engine(args, cfg, res, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": dtype_text(cfg),
         "data": WORKLOADS[WORKLOAD]["data"],
         "config": {
-            "workload": f"{WORKLOAD}: 25 layers, d 2560, 20x128 q heads, 4 kv heads, ffn 9728, tied vocab 32000; "
-                        "batch 1, prompt 512, greedy decode at contexts 513..1024",
-            "weights": WORKLOADS[WORKLOAD]["weights"], "kv_cache": "f16", "batch": 1, "prompt": cfg["prompt_len"],
+            "workload": workload_text(cfg),
+            "weights": WORKLOADS[WORKLOAD]["weights"], "kv_cache": cfg["kv_dtype"], "batch": 1,
+            "prompt": cfg["prompt_len"],
             "contexts": f"{cfg['prompt_len'] + 1}..{cfg['prompt_len'] + min(res['steps'], WINDOW)}",
-            "kernel": "persistent: one cooperative launch per window of up to 512 chained decode steps "
+            "temperature": WORKLOADS[WORKLOAD]["temperature"],
+            "kernel": f"persistent: one cooperative launch per window of up to {WINDOW} chained decode steps "
                       "(e2e: one launch per step)",
             "ctas": res["ctas"],
             "l2": f"inputs larger than L2: every step streams {res['weight_bytes'] / 1e9:.2f} GB of weights "
                   "(L2 129 MB)",
+            "timed_regions": "3 regions of exactly `steps` steps; value from the median region",
+            "runs_tokens_per_s": [round(whole_job_rate(res["steps"], r * 1e-3, world), 2) for r in res["runs_ms"]],
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "e2e": {"value": round(res["e2e"], 2), "unit": "tokens/s", "h2d_bytes_per_step": 32,
@@ -708,7 +795,11 @@ def emit_engine(args, cfg, res, world):
                      "bytes_per_launch": int(res["per_launch_bytes"]),
                      "launch_ms": round(res["launch_ms"], 5),
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({res['peak_kind']}; read+write copy)",
-                     "frac_of_8000": round(res["achieved_gbs"] / 8000.0, 4)},
+                     "frac_of_8000": round(res["achieved_gbs"] / 8000.0, 4),
+                     "read_probe_gbs": round(res["read_gbs"], 1),
+                     "frac_of_read_probe": round(res["achieved_gbs"] / res["read_gbs"], 4),
+                     "read_probe": "same run: adp_measure_read_bandwidth, 16-byte loads over a 4 GiB buffer, "
+                                   "5 launches timed with CUDA events"},
         "gpu_launches": res["launches"],
         **({"profiling_variant": f"{cfg['n_layers']} layers (not the workload)"} if args.layers else {}),
         "clocks": res["clocks"],
@@ -743,10 +834,9 @@ def run_reference(args, rank: int, world: int):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": dtype_text(cfg),
         "data": WORKLOADS[WORKLOAD]["data"],
-        "config": {"workload": f"{WORKLOAD}: 25 layers, d 2560, tied vocab 32000; batch 1, greedy decode at "
-                               "contexts from 513", "weights": WORKLOADS[WORKLOAD]["weights"], "batch": 1,
+        "config": {"workload": workload_text(cfg), "weights": WORKLOADS[WORKLOAD]["weights"], "batch": 1,
                    "prompt": cfg["prompt_len"]},
         "cpu_baseline": cpu,
         "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -777,6 +867,10 @@ def main():
                     help="profiling only: use this many layers of the workload's shape (the line says so)")
     args = ap.parse_args()
     globals()["WORKLOAD"] = args.workload
+    globals()["WINDOW"] = WORKLOADS[args.workload]["window"]
+    if (args.batch > 1 or args.prefill) and args.workload not in ("dense-2.3b-fp16", "dense-2.3b-e4m3",
+                                                                  "dense-2.3b-nvfp4"):
+        ap.error("--batch and --prefill measure the 2.3B model (--workload dense-2.3b-*)")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))

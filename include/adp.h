@@ -302,6 +302,17 @@ int adp_num_ctas(const adp_model* m, int32_t* ctas);            /* persistent gr
 int adp_image_bytes(const adp_model* m, uint64_t* bytes);       /* bytes of the tile-ordered weight image */
 int adp_launches_per_step(const adp_model* m, int32_t* n);      /* kernel launches of one decode step */
 
+/* Measurement helper (not part of the decode step): the read bandwidth this GPU delivers on a
+ * caller-given DEVICE buffer of `bytes` bytes (16-byte aligned; use one larger than L2 so that the
+ * reads come from HBM): `reps` launches of a grid-stride kernel of 16-byte loads on the stream
+ * (NULL = the default stream), after one untimed launch, timed with CUDA events; *gb_per_s gets
+ * bytes * reps / time.  The buffer is only read (its first word would be written only if the xor of
+ * all its words equalled one fixed constant).  Allocates nothing; synchronises the stream.
+ * Errors: ADP_ERR_INVALID_ARG, ADP_ERR_CUDA.  Bandwidth is the bound of batch-1 decode
+ * ([H] §"GPU推論の速度制限要因：メモリ帯域幅"). */
+int adp_measure_read_bandwidth(const void* dev_buf, uint64_t bytes, int32_t reps, void* cuda_stream,
+                               double* gb_per_s);
+
 /* Debug and ablation hooks ([H] §"標準推論スタックのボトルネックとKogの工夫": the launch
  * overhead the persistent kernel removes is measured by running the same device code as one
  * launch per phase).

@@ -70,6 +70,16 @@ CONFIGS = [
     _cfg(index=6, name="dense-2.3b-nvfp4", n_layers=25, d_model=2560, n_heads=20, n_kv_heads=4,
          head_dim=128, d_ff=9728, vocab=32000, max_ctx=4096, weight_dtype="nvfp4", embed_dtype="f16",
          prompt_len=512, decode_steps=512),
+    # 7, 8: the 8B model with e4m3 / nvfp4 layer matrices (scales as in 5 and 6); embedding, the
+    #    untied LM head and norm gains stay bf16, the KV cache bf16
+    _cfg(index=7, name="dense-8b-e4m3", n_layers=32, d_model=4096, n_heads=32, n_kv_heads=8,
+         head_dim=128, d_ff=14336, vocab=128256, max_ctx=8192, rope_theta=500000.0,
+         tied_embeddings=False, weight_dtype="e4m3", embed_dtype="bf16", kv_dtype="bf16", prompt_len=1024,
+         decode_steps=256),
+    _cfg(index=8, name="dense-8b-nvfp4", n_layers=32, d_model=4096, n_heads=32, n_kv_heads=8,
+         head_dim=128, d_ff=14336, vocab=128256, max_ctx=8192, rope_theta=500000.0,
+         tied_embeddings=False, weight_dtype="nvfp4", embed_dtype="bf16", kv_dtype="bf16", prompt_len=1024,
+         decode_steps=256),
 ]
 
 BY_NAME = {c["name"]: c for c in CONFIGS}

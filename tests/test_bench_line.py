@@ -14,14 +14,54 @@ REQUIRED = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step
             "vs_baseline", "dtype", "data", "config", "e2e", "roofline", "gpu_launches", "clocks")
 
 
+def _engine_res(**kw):
+    res = {"ms": 1000.0, "runs_ms": [1010.0, 1000.0, 990.0], "steps": 1024, "n_launch": 2,
+           "step_pct": {"p50_us": 1.0, "p99_us": 2.0},
+           "weight_bytes": 4686090240, "achieved_gbs": 3800.0, "per_launch_bytes": 2.4e12, "launch_ms": 500.0,
+           "peak": 6757.9, "peak_kind": "measured", "read_gbs": 7000.0, "e2e": 800.0, "n_e2e": 1024,
+           "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 10}, "ctas": 152,
+           "image_bytes": 1, "launches": 2, "ablation": None,
+           "cpu": {"value": 4.2, "unit": "tokens/s", "cores": 16, "kind": "oracle", "sample": "x"}}
+    res.update(kw)
+    return res
+
+
+@pytest.mark.parametrize("workload,window,prompt", [("dense-2.3b-fp16-long-t0.7", 512, 3584),
+                                                    ("dense-8b-bf16", 256, 1024),
+                                                    ("moe-32x1408-top4-e4m3", 512, 256)])
+def test_other_workload_lines_name_their_run(capsys, monkeypatch, workload, window, prompt):
+    """--workload lines describe the run they time: shape, prompt, contexts, sampling, stored types."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    monkeypatch.setattr(bench, "WORKLOAD", workload)
+    monkeypatch.setattr(bench, "WINDOW", bench.WORKLOADS[workload]["window"])
+    cfg = synth.get_config(workload)
+    bench.emit_engine(types.SimpleNamespace(warmup=16, layers=0), cfg, _engine_res(steps=window, n_launch=1), 1)
+    line = json.loads(capsys.readouterr().out.strip())
+    for k in REQUIRED:
+        assert k in line, k
+    assert line["metric"] == bench.WORKLOADS[workload]["metric"]
+    assert line["config"]["prompt"] == prompt
+    assert line["config"]["contexts"] == f"{prompt + 1}..{prompt + window}"
+    assert line["config"]["workload"].startswith(workload) and f"prompt {prompt}" in line["config"]["workload"]
+    assert cfg["kv_dtype"] in line["dtype"] and "f32 accumulation" in line["dtype"]
+    if workload.endswith("t0.7"):
+        assert line["config"]["temperature"] == 0.7 and "sampling" in line["config"]["workload"]
+    if workload.startswith("moe"):
+        assert "e4m3 experts" in line["dtype"] and "top-4" in line["config"]["workload"]
+    assert line["roofline"]["frac_of_read_probe"] == pytest.approx(3800.0 / 7000.0, rel=1e-3)
+
+
 def test_engine_line_has_the_contract_keys(capsys):
     sys.path.insert(0, ROOT)
     import bench
     import synth
     cfg = synth.get_config("dense-2.3b-fp16")
-    res = {"ms": 1000.0, "steps": 1024, "n_launch": 2, "step_pct": {"p50_us": 1.0, "p99_us": 2.0},
+    res = {"ms": 1000.0, "runs_ms": [1000.0, 1001.0, 999.0], "steps": 1024, "n_launch": 2,
+           "step_pct": {"p50_us": 1.0, "p99_us": 2.0},
            "weight_bytes": 4686090240, "achieved_gbs": 3800.0, "per_launch_bytes": 2.4e12, "launch_ms": 500.0,
-           "peak": 6757.9, "peak_kind": "measured", "e2e": 800.0, "n_e2e": 1024,
+           "peak": 6757.9, "peak_kind": "measured", "read_gbs": 7000.0, "e2e": 800.0, "n_e2e": 1024,
            "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 10}, "ctas": 152,
            "image_bytes": 1, "launches": 2, "ablation": None,
            "cpu": {"value": 4.2, "unit": "tokens/s", "cores": 16, "kind": "oracle", "sample": "x"}}
@@ -35,6 +75,8 @@ def test_engine_line_has_the_contract_keys(capsys):
     assert set(line["roofline"]) >= {"bound", "achieved", "peak", "unit", "frac", "traffic"}
     assert line["roofline"]["frac"] == pytest.approx(3800.0 / 6757.9, rel=1e-3)
     assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["dtype"] == "f16 weights, f16 KV cache, f32 accumulation and activations"
+    assert len(line["config"]["runs_tokens_per_s"]) == 3
 
 
 @pytest.mark.slow

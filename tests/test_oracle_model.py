@@ -58,9 +58,14 @@ def test_tiny_against_brute_force():
 
 
 @pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "moe-32x1408-top4-e4m3", "dense-2.3b-e4m3",
-                                  "dense-2.3b-nvfp4"])
+                                  "dense-2.3b-nvfp4", "dense-8b-e4m3", "dense-8b-nvfp4"])
 def test_shrunk_workloads_against_brute_force(name):
-    cfg = synth.shrink(synth.get_config(name))
+    over = {}
+    if name in ("dense-8b-e4m3", "dense-8b-nvfp4"):
+        # fp16 KV storage: a bf16 cache element that fp32 and float64 arithmetic round one ulp apart
+        # moves these logits by ~1e-4 by itself; the bf16 cache path is pinned by dense-8b-bf16
+        over["kv_dtype"] = "f16"
+    cfg = synth.shrink(synth.get_config(name), **over)
     check_against_brute(cfg, 8, 24)
 
 
