@@ -131,6 +131,7 @@ _SIGS = [
     ("adp_debug_barriers", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     ("adp_debug_set_l2_lookahead", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
     ("adp_debug_set_prefetch_flags", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32]),
+    ("adp_debug_set_l2_pacing", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint32]),
     ("adp_measure_read_bandwidth", ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int32, ctypes.c_void_p,
                                                   ctypes.POINTER(ctypes.c_double)]),
     ("adp_debug_set_ring_slots", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32]),
@@ -411,6 +412,11 @@ def adp_measure_read_bandwidth(dev_buf, nbytes: int, reps: int, stream: int = 0)
     _check(load_library().adp_measure_read_bandwidth(_ptr(dev_buf), int(nbytes), int(reps), stream or None,
                                                       ctypes.byref(g)), "adp_measure_read_bandwidth")
     return g.value
+
+
+def adp_debug_set_l2_pacing(model, bytes_per_us: int, burst_bytes: int):
+    _check(load_library().adp_debug_set_l2_pacing(model, int(bytes_per_us), int(burst_bytes)),
+           "adp_debug_set_l2_pacing")
 
 
 def adp_debug_set_prefetch_flags(model, flags: int):

@@ -77,58 +77,74 @@ __device__ void rmsnorm_prologue(const Params& p, Ctl* ctl, float* xbuf, const v
   consumer_sync();
 }
 
-// The residual rows this CTA's units update (rows_per_unit rows each), staged in shared memory
-// so that the epilogue does not wait for a load (visible after the next consumer_sync).
-__device__ void stage_residual(const Params& p, Ctl* ctl, const PhaseDesc& P, uint32_t c, uint32_t G,
-                               int rows_per_unit, uint32_t x_epoch, int cw, int lane) {
+// The residual row this thread stages for the CTA's units (rows_per_unit rows each): fetched
+// alongside the phase's input vector, into shared memory, so that the epilogue does not wait for
+// a load.
+__device__ __forceinline__ SideWord residual_word(const Params& p, Ctl* ctl, const PhaseDesc& P, int rows_per_unit,
+                                                  uint32_t x_epoch, int tid) {
   int32_t u0, n;
   cta_share(p, ctl, P, u0, n);
-  const int tid = cw * 32 + lane;
-  if (tid < n * rows_per_unit) {
-    const ll_t* src = p.x + (size_t)u0 * rows_per_unit + tid;
-    ll_t w = ll_load(src);
-    if (ll_wait(src, x_epoch, w, p, ctl)) ctl->xres[tid] = ll_value(w);
-  }
+  if (tid >= n * rows_per_unit) return SideWord{nullptr, nullptr, 0};
+  return SideWord{p.x + (size_t)u0 * rows_per_unit + tid, &ctl->xres[tid], x_epoch};
 }
 
 // Router softmax + top-k (ties to the lower index), gates renormalised over the choice; forced
-// experts (test hook) keep the router's probabilities of those experts.  Called by a whole warp:
-// the logits are staged in shared memory in one batch, lane 0 does the sequential part.
+// experts (test hook) keep the router's probabilities of those experts.  Called by a whole warp,
+// lane-parallel: the logits are staged in shared memory in one batch; lane l computes
+// e_i = exp(r_i - M) and then P_i = e_i / Z for experts i = l, l + 32, ...; lane 0 forms
+// Z = sum_i e_i sequentially in expert order; each of the top_k choices is a warp argmax over
+// (P_i, lowest index) of the experts not yet chosen; lane 0 sums the chosen P in slot order and
+// divides.  Every value is the same operation on the same operands as a sequential evaluation.
 __device__ void select_experts(const Params& p, Ctl* ctl, int layer, uint32_t r_epoch, int lane) {
   const int E = p.E, K = p.topk;
+  float* st = ctl->stage;
   for (int e = lane; e < E; e += 32) {
     ll_t w = ll_load(p.rlog + e);
-    ctl->stage[e] = ll_wait(p.rlog + e, r_epoch, w, p, ctl) ? ll_value(w) : 0.0f;
+    st[e] = ll_wait(p.rlog + e, r_epoch, w, p, ctl) ? ll_value(w) : 0.0f;
   }
   __syncwarp();
-  if (lane == 0) {
-    const float* r = ctl->stage;
-    float M = r[0];
-    for (int e = 1; e < E; ++e) M = r[e] > M ? r[e] : M;
-    float Z = 0.0f;
-    for (int e = 0; e < E; ++e) Z = __fadd_rn(Z, exp_c(__fsub_rn(r[e], M)));
-    uint32_t used[32] = {0};  // bit set over up to 1024 experts
-    float Zs = 0.0f;
-    for (int i = 0; i < K; ++i) {
-      int best = -1;
-      float bp = 0.0f;
-      if (p.force_sel) {
-        best = p.force_sel[layer * K + i];
-        bp = __fdiv_rn(exp_c(__fsub_rn(r[best], M)), Z);
-      } else {
-        for (int e = 0; e < E; ++e) {
-          if (used[e >> 5] & (1u << (e & 31))) continue;
-          const float pe = __fdiv_rn(exp_c(__fsub_rn(r[e], M)), Z);
-          if (best < 0 || pe > bp) { best = e; bp = pe; }
-        }
-        used[best >> 5] |= 1u << (best & 31);
+  float M = __int_as_float(0xFF800000);
+  for (int e = lane; e < E; e += 32) M = fmaxf(M, st[e]);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+  for (int e = lane; e < E; e += 32) st[e] = exp_c(__fsub_rn(st[e], M));
+  __syncwarp();
+  float Z = 0.0f;
+  if (lane == 0)
+    for (int e = 0; e < E; ++e) Z = __fadd_rn(Z, st[e]);
+  Z = __shfl_sync(0xFFFFFFFFu, Z, 0);
+  for (int e = lane; e < E; e += 32) st[e] = __fdiv_rn(st[e], Z);  // P_e
+  __syncwarp();
+  float Zs = 0.0f;
+  for (int i = 0; i < K; ++i) {
+    int best;
+    if (p.force_sel) {
+      best = p.force_sel[layer * K + i];
+    } else {
+      unsigned long long key = 0ull;  // chosen experts hold -1 and never win
+      for (int e = lane; e < E; e += 32) {
+        const unsigned long long k = argmax_key(st[e], (uint32_t)e);
+        key = k > key ? k : key;
       }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, key, off);
+        key = o > key ? o : key;
+      }
+      best = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+    }
+    const float bp = st[best];
+    __syncwarp();
+    if (lane == 0) {
       ctl->sel[i] = best;
       ctl->gate[i] = bp;  // probability for now
       Zs = __fadd_rn(Zs, bp);
+      if (!p.force_sel) st[best] = -1.0f;
     }
-    for (int i = 0; i < K; ++i) ctl->gate[i] = __fdiv_rn(ctl->gate[i], Zs);
+    __syncwarp();
   }
+  if (lane == 0)
+    for (int i = 0; i < K; ++i) ctl->gate[i] = __fdiv_rn(ctl->gate[i], Zs);
   __syncwarp();
 }
 
@@ -211,16 +227,36 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
           // times its block scale added into the lane partial.
           const uint8_t* codes = tile + (size_t)cw * ROWS * (kck >> 1);
           const uint8_t* bsc = tile + (size_t)m * ROWS * (kck >> 1) + (size_t)cw * ROWS * (kck >> 4);
+          auto vec4 = [&](int v, const float (&x8)[8]) {
+            if constexpr (ROWS % 2 == 0) {
+              // rows j and j + 1 share each instruction: packed fp32 FMAs (two independent IEEE fmas)
+#pragma unroll
+              for (int j = 0; j < ROWS; j += 2) {
+                float wa[8], wb[8];
+                load8_e2m1(*reinterpret_cast<const uint32_t*>(codes + (size_t)j * (kck >> 1) + (size_t)v * 4), wa);
+                load8_e2m1(*reinterpret_cast<const uint32_t*>(codes + (size_t)(j + 1) * (kck >> 1) + (size_t)v * 4),
+                           wb);
+                const float2 bs = make_float2(e4m3_to_f32(bsc[(size_t)j * (kck >> 4) + (v >> 1)]),
+                                              e4m3_to_f32(bsc[(size_t)(j + 1) * (kck >> 4) + (v >> 1)]));
+                const float2 t = fma8x2(wa, wb, x8, make_float2(0.0f, 0.0f));
+                const float2 a = __ffma2_rn(bs, t, make_float2(acc[j], acc[j + 1]));
+                acc[j] = a.x;
+                acc[j + 1] = a.y;
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < ROWS; ++j) {
+                float w8[8];
+                load8_e2m1(*reinterpret_cast<const uint32_t*>(codes + (size_t)j * (kck >> 1) + (size_t)v * 4), w8);
+                const float bs = e4m3_to_f32(bsc[(size_t)j * (kck >> 4) + (v >> 1)]);
+                acc[j] = fmaf(bs, fma8(w8, x8, 0.0f), acc[j]);
+              }
+            }
+          };
           for (int v = lane; v < nvec; v += 32) {
             float x8[8];
             load_xs8(xbuf, (xoff >> 3) + v, x8);
-#pragma unroll
-            for (int j = 0; j < ROWS; ++j) {
-              float w8[8];
-              load8_e2m1(*reinterpret_cast<const uint32_t*>(codes + (size_t)j * (kck >> 1) + (size_t)v * 4), w8);
-              const float bs = e4m3_to_f32(bsc[(size_t)j * (kck >> 4) + (v >> 1)]);
-              acc[j] = fmaf(bs, fma8(w8, x8, 0.0f), acc[j]);
-            }
+            vec4(v, x8);
           }
         } else {
           for (int v = lane; v < nvec; v += 32) {
@@ -229,11 +265,25 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
 #pragma unroll
             for (int s = 0; s < SLOTS; ++s) {
               if (XPERSLOT) load_xs8(xbuf + s * Kp, (xoff >> 3) + v, x8);
+              if constexpr (ROWS % 2 == 0) {
+                // rows j and j + 1 share each instruction: packed fp32 FMAs (two independent IEEE fmas)
 #pragma unroll
-              for (int j = 0; j < ROWS; ++j) {
-                float w8[8];
-                load8<WDT>(tile + (size_t)s * slot_bytes + ((size_t)(cw * ROWS + j) * kck + (size_t)v * 8) * EB, w8);
-                acc[s * ROWS + j] = fma8(w8, x8, acc[s * ROWS + j]);
+                for (int j = 0; j < ROWS; j += 2) {
+                  float wa[8], wb[8];
+                  load8<WDT>(tile + (size_t)s * slot_bytes + ((size_t)(cw * ROWS + j) * kck + (size_t)v * 8) * EB, wa);
+                  load8<WDT>(tile + (size_t)s * slot_bytes + ((size_t)(cw * ROWS + j + 1) * kck + (size_t)v * 8) * EB,
+                             wb);
+                  const float2 a = fma8x2(wa, wb, x8, make_float2(acc[s * ROWS + j], acc[s * ROWS + j + 1]));
+                  acc[s * ROWS + j] = a.x;
+                  acc[s * ROWS + j + 1] = a.y;
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < ROWS; ++j) {
+                  float w8[8];
+                  load8<WDT>(tile + (size_t)s * slot_bytes + ((size_t)(cw * ROWS + j) * kck + (size_t)v * 8) * EB, w8);
+                  acc[s * ROWS + j] = fma8(w8, x8, acc[s * ROWS + j]);
+                }
               }
             }
           }
@@ -401,6 +451,8 @@ __device__ void finalize_token(const Params& p, const Step& st, int32_t token) {
 // it), prefetched into L2 while the layer's QKV phase runs: they do not depend on this step
 // except for the newest row, which the attention phase takes from the exchange words anyway.
 __device__ __forceinline__ void prefetch_attention_kv(const Params& p, int L, int ctx, uint32_t c, uint32_t G) {
+  const uint64_t pol = policy_evict_last();
+  const bool last = (p.pf_flags & PF_KV_LAST) != 0;
   const int nb = (ctx + kAttnBlock - 1) / kAttnBlock;
   const int items = p.hkv * nb;
   for (int it = (int)c; it < items; it += (int)G) {
@@ -408,8 +460,13 @@ __device__ __forceinline__ void prefetch_attention_kv(const Params& p, int L, in
     const int j0 = b * kAttnBlock;
     const uint32_t bytes = (uint32_t)min(kAttnBlock, ctx - j0) * p.hd * 2;  // a multiple of 128
     const size_t cache0 = (((size_t)L * p.hkv + g) * p.max_ctx + j0) * p.hd;
-    prefetch_l2(p.kc + cache0, bytes);
-    prefetch_l2(p.vc + cache0, bytes);
+    if (last) {
+      prefetch_l2_hint(p.kc + cache0, bytes, pol);
+      prefetch_l2_hint(p.vc + cache0, bytes, pol);
+    } else {
+      prefetch_l2(p.kc + cache0, bytes);
+      prefetch_l2(p.vc + cache0, bytes);
+    }
   }
 }
 
@@ -477,6 +534,23 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
           tma_load_1d(SK + (size_t)lane * KSTR, kc + cache0 + (size_t)lane * HD, HD * 2, &ctl->att_bar[slot],
                       policy_evict_first());
       }
+      // the block holding this step's position takes its K/V row from the tagged copies (the cache
+      // row may not have landed when the bulk copy read it): those words are loaded now, with the
+      // query's, so that both round trips overlap
+      // Every thread of the slot takes words t, t + 32 * gmax, ... of that row (K then V, 2 * HD
+      // words); the first PWE of them are loaded here.
+      constexpr int PWE = 2;
+      const bool patch = j0 + nvalid == ctx;
+      const int tslot = hh * 32 + lane, nthr = gmax * 32;
+      const ll_t* kn = knew + (size_t)g * HD;
+      const ll_t* vn = vnew + (size_t)g * HD;
+      auto pword = [&](int wi) { return wi < HD ? kn + wi : vn + (wi - HD); };
+      ll_t pe[PWE];
+#pragma unroll
+      for (int k = 0; k < PWE; ++k) {
+        const int wi = tslot + k * nthr;
+        pe[k] = patch && wi < 2 * HD ? ll_load(pword(wi)) : 0ull;
+      }
       // this head's query, staged in shared memory (read by every lane in the score pass)
       float* sq = SQ + hh * HD;
       if (active) {
@@ -498,25 +572,20 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
       bool ok = mbar_wait(&ctl->att_bar[slot], att_uses & 1, &ctl->abort, wait_ns);
       ++att_uses;
       if (!ok && lane == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
-      if (hh == 0 && j0 + nvalid == ctx) {
-        // the block holding this step's position: its K/V row comes from the tagged copies
-        // (the cache row may not have landed when the bulk copy read it)
+      if (patch) {
         const int jr = ctx - 1 - j0;
-        const ll_t* kn = knew + (size_t)g * HD + lane;
-        const ll_t* vn = vnew + (size_t)g * HD + lane;
-        ll_t w[2 * DPL];  // K words, then V words
+        auto put = [&](int wi, ll_t w) {
+          if (wi < HD) SK[(size_t)jr * KSTR + wi] = (uint16_t)w;
+          else SV[(size_t)jr * HD + (wi - HD)] = (uint16_t)w;
+        };
 #pragma unroll
-        for (int i = 0; i < 2 * DPL; ++i) w[i] = ll_load(i < DPL ? kn + 32 * i : vn + 32 * (i - DPL));
-#pragma unroll
-        for (int i = 0; i < 2 * DPL; ++i) {
-          if (ll_epoch(w[i]) != qe) {
-            if (!ll_wait(i < DPL ? kn + 32 * i : vn + 32 * (i - DPL), qe, w[i], p, ctl)) break;
-#pragma unroll
-            for (int j = i + 1; j < 2 * DPL; ++j)  // reload the rest together (see ll_fetch)
-              if (ll_epoch(w[j]) != qe) w[j] = ll_load(j < DPL ? kn + 32 * j : vn + 32 * (j - DPL));
-          }
-          if (i < DPL) SK[(size_t)jr * KSTR + lane + 32 * i] = (uint16_t)w[i];
-          else SV[(size_t)jr * HD + lane + 32 * (i - DPL)] = (uint16_t)w[i];
+        for (int k = 0; k < PWE; ++k) {
+          const int wi = tslot + k * nthr;
+          if (wi < 2 * HD && ll_wait(pword(wi), qe, pe[k], p, ctl)) put(wi, pe[k]);
+        }
+        for (int wi = tslot + PWE * nthr; wi < 2 * HD; wi += nthr) {  // groups of fewer than 4 heads
+          ll_t w = ll_load(pword(wi));
+          if (ll_wait(pword(wi), qe, w, p, ctl)) put(wi, w);
         }
       }
       asm volatile("bar.sync %0, %1;" ::"r"(2 + slot), "r"(gmax * 32) : "memory");
@@ -594,12 +663,15 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
         if (cw == 0 && lane == 0 && it == (int)c) stamp(p, c, P.index, 6);
         // block partial as epoch-tagged words, [head][block] and [head][block][dim]: the head's
         // merger polls them directly (no counter, no fence on this side)
+        // the outputs go first and the maximum and sum after them, so that a merger that has seen
+        // the block's maximum and sum usually finds its outputs in place too
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) ll_store(part_o + ((size_t)h * nbmax + b) * HD + lane * DPL + i, ll_pack(o[i], ew));
+        __syncwarp();
         if (lane == 0) {
           ll_store(part_m + (size_t)h * nbmax + b, ll_pack(m, ew));
           ll_store(part_l + (size_t)h * nbmax + b, ll_pack(l, ew));
         }
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) ll_store(part_o + ((size_t)h * nbmax + b) * HD + lane * DPL + i, ll_pack(o[i], ew));
         if (cw == 0 && lane == 0 && it == (int)c) {
           stamp(p, c, P.index, 5);
           if (p.timeline) {
@@ -792,8 +864,6 @@ __device__ void run_gemv(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
   switch (P.kind) {
     case PK_QKV:
     case PK_GU:
-      gemv_phase<2, 1, WDT, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
-      break;
     case PK_WO:
     case PK_DOWN:
       gemv_phase<2, 1, WDT, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
@@ -815,9 +885,21 @@ __device__ void run_expert(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf
     gemv_phase<1, SLOTS, DT_E4M3, true>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
 }
 
-template <int KIND>
+// A model's specialisation: its head width, KV-cache type and the 16-bit type of its dense weights
+// (16-bit models) or of its embedding and LM head (the others), fixed at compile time so that a
+// kernel instantiation holds only the attention and GEMV code that model runs (SPEC 0: chosen at
+// run time from the parameters, for every other combination).
+constexpr int spec_code(int hd, int kvdt, int t16) { return (1 << 30) | hd | (kvdt << 16) | (t16 << 20); }
+template <int SPEC>
+struct Spec {
+  static constexpr bool on = SPEC != 0;
+  static constexpr int hd = SPEC & 0xFFFF, kvdt = (SPEC >> 16) & 0xF, t16 = (SPEC >> 20) & 0xF;
+};
+
+template <int KIND, int SPEC>
 __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, Step st, uint32_t c,
                          uint32_t G, int ph0, int ph1, bool use_barrier, int cw, int lane) {
+  using S = Spec<SPEC>;
   uint32_t t = 0;
   int bidx = 0;
   int sel_layer = -1;
@@ -868,7 +950,15 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
             for (int i = a + tid; i < b; i += kConsumerWarps * 32)
               ll_store(p.x + i, ll_pack(load_elem(emb, (size_t)i, p.edt), ew));
           }
-          if (cw == kConsumerWarps - 1 && lane == 0 && !ab) prefetch_attention_kv(p, L, st.pos + 1, c, G);
+          if (cw == kConsumerWarps - 1 && lane == 0 && !ab) {
+            if (!(p.pf_flags & PF_KV_AHEAD)) {
+              prefetch_attention_kv(p, L, st.pos + 1, c, G);
+            } else {  // one layer early: this layer's blocks were requested during the previous layer
+              if (L == 0 && step == 0) prefetch_attention_kv(p, 0, st.pos + 1, c, G);
+              if (L + 1 < p.L) prefetch_attention_kv(p, L + 1, st.pos + 1, c, G);
+              else if (step + 1 < p.n_steps && st.pos + 2 <= p.max_ctx) prefetch_attention_kv(p, 0, st.pos + 2, c, G);
+            }
+          }
           if (n > 0) {
             const int half = p.hd / 2;  // the RoPE row of this position, for the epilogue
             if (tid < half) {
@@ -881,14 +971,13 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
         }
         case PK_WO:
           if (n > 0) {
-            stage_residual(p, ctl, P, c, G, 2, e_res, cw, lane);
-            ll_fetch(p, ctl, xbuf, p.attn, p.hq * p.hd, p.hq * p.hd, 0, e_src, tid);
+            ll_fetch(p, ctl, xbuf, p.attn, p.hq * p.hd, p.hq * p.hd, 0, e_src, tid,
+                     residual_word(p, ctl, P, 2, e_res, tid));
           }
           break;
         case PK_DOWN:
           if (n > 0) {
-            stage_residual(p, ctl, P, c, G, 2, e_res, cw, lane);
-            ll_fetch(p, ctl, xbuf, p.h, p.ff, p.ff, 0, e_src, tid);
+            ll_fetch(p, ctl, xbuf, p.h, p.ff, p.ff, 0, e_src, tid, residual_word(p, ctl, P, 2, e_res, tid));
           }
           break;
         case PK_EDOWN:
@@ -901,8 +990,8 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
               sel_layer = L;
             }
             if (n > 0) {
-              stage_residual(p, ctl, P, c, G, 1, e_res, cw, lane);
-              ll_fetch(p, ctl, xbuf, p.h, p.topk * p.fexp, p.fexp, (p.fexp + 255) & ~255, e_src, tid);
+              ll_fetch(p, ctl, xbuf, p.h, p.topk * p.fexp, p.fexp, (p.fexp + 255) & ~255, e_src, tid,
+                       residual_word(p, ctl, P, 1, e_res, tid));
             } else {
               consumer_sync();  // the choice (shared memory) is read by every warp's epilogue
             }
@@ -934,7 +1023,9 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
       // ---- body
       if (cw == 0 && lane == 0) stamp(p, c, ph, 1);
       if (P.kind == PK_ATTN) {
-        if (p.kvdt == DT_BF16) {
+        if constexpr (S::on) {
+          attention_phase<S::hd, S::kvdt>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+        } else if (p.kvdt == DT_BF16) {
           if (p.hd == 128) attention_phase<128, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
           else if (p.hd == 64) attention_phase<64, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
           else attention_phase<256, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
@@ -961,11 +1052,14 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
         }
       } else {
         if constexpr (KIND == KK_DENSE8 || KIND == KK_DENSE4) {
-          if (P.kind != PK_LM) run_gemv<KIND == KK_DENSE8 ? DT_E4M3 : DT_NVFP4>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+          if (P.kind != PK_LM)
+            run_gemv<KIND == KK_DENSE8 ? DT_E4M3 : DT_NVFP4>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+          else if constexpr (S::on) run_gemv<S::t16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
           else if (p.edt == DT_BF16) run_gemv<DT_BF16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
           else run_gemv<DT_F16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
         } else {
-          if (p.wdt == DT_BF16) run_gemv<DT_BF16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+          if constexpr (S::on) run_gemv<S::t16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+          else if (p.wdt == DT_BF16) run_gemv<DT_BF16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
           else run_gemv<DT_F16>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
         }
       }
@@ -992,7 +1086,7 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
 // KIND: KK_DENSE (16-bit weights), KK_MOE (top-k expert models), KK_DENSE8 (e4m3 layer
 // matrices), KK_DENSE4 (NVFP4 layer matrices): each model runs the instantiation that carries
 // only its own code paths.
-template <int KIND>
+template <int KIND, int SPEC>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ Params p, int32_t ph0, int32_t ph1, int32_t use_barrier,
                   int32_t xbuf_floats) {
@@ -1017,7 +1111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumerWarps) {
     if (lane == 0) producer(p, ctl, ring, c, G, ph0, ph1);
   } else {
-    consumer<KIND>(p, ctl, ring, xbuf, st, c, G, ph0, ph1, use_barrier != 0, warp, lane);
+    consumer<KIND, SPEC>(p, ctl, ring, xbuf, st, c, G, ph0, ph1, use_barrier != 0, warp, lane);
   }
 }
 
@@ -1025,18 +1119,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace adp {
 
-// Host-side launchers of the decode kernel.
-static const void* kernel_of(int kind) {
+// Host-side launchers of the decode kernel: the instantiation of a model's kind and, for the
+// full-size workloads' combinations (head width 128; f16 or bf16 KV and 16-bit weights), its
+// specialisation; every other model runs the kind's run-time-dispatching instantiation.
+template <int KIND>
+static const void* kernel_spec(int hd, int kvdt, int t16) {
+  if (hd == 128 && kvdt == DT_F16 && t16 == DT_F16)
+    return (const void*)decode_kernel<KIND, spec_code(128, DT_F16, DT_F16)>;
+  if (hd == 128 && kvdt == DT_BF16 && t16 == DT_BF16)
+    return (const void*)decode_kernel<KIND, spec_code(128, DT_BF16, DT_BF16)>;
+  return (const void*)decode_kernel<KIND, 0>;
+}
+
+static const void* kernel_of(int kind, int hd, int kvdt, int t16) {
   switch (kind) {
-    case KK_MOE: return (const void*)decode_kernel<KK_MOE>;
-    case KK_DENSE8: return (const void*)decode_kernel<KK_DENSE8>;
-    case KK_DENSE4: return (const void*)decode_kernel<KK_DENSE4>;
-    default: return (const void*)decode_kernel<KK_DENSE>;
+    case KK_MOE: return kernel_spec<KK_MOE>(hd, kvdt, t16);
+    case KK_DENSE8: return kernel_spec<KK_DENSE8>(hd, kvdt, t16);
+    case KK_DENSE4: return kernel_spec<KK_DENSE4>(hd, kvdt, t16);
+    default: return kernel_spec<KK_DENSE>(hd, kvdt, t16);
   }
 }
 
-cudaError_t decode_prepare(size_t smem_bytes, int kind, int* blocks_per_sm) {
-  const void* k = kernel_of(kind);
+cudaError_t decode_prepare(size_t smem_bytes, int kind, int hd, int kvdt, int t16, int* blocks_per_sm) {
+  const void* k = kernel_of(kind, hd, kvdt, t16);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kThreads, smem_bytes);
@@ -1046,7 +1151,8 @@ cudaError_t decode_launch(const Params& p, int ph0, int ph1, bool persistent, in
                           int xbuf_floats, cudaStream_t stream) {
   int32_t a0 = ph0, a1 = ph1, ub = persistent ? 1 : 0, xf = xbuf_floats;
   void* args[] = {(void*)&p, &a0, &a1, &ub, &xf};
-  const void* k = kernel_of(p.E > 0 ? KK_MOE : p.wdt == DT_E4M3 ? KK_DENSE8 : p.wdt == DT_NVFP4 ? KK_DENSE4 : KK_DENSE);
+  const int kind = p.E > 0 ? KK_MOE : p.wdt == DT_E4M3 ? KK_DENSE8 : p.wdt == DT_NVFP4 ? KK_DENSE4 : KK_DENSE;
+  const void* k = kernel_of(kind, p.hd, p.kvdt, kind == KK_DENSE ? p.wdt : p.edt);
   if (persistent) return cudaLaunchCooperativeKernel(k, dim3(grid), dim3(kThreads), args, smem_bytes, stream);
   return cudaLaunchKernel(k, dim3(grid), dim3(kThreads), args, smem_bytes, stream);
 }

@@ -94,14 +94,28 @@ constexpr uint32_t kL2Chunk = 32 * 1024;
 // phases' shares (each contiguous in the image) in consumption order.  The cursor runs up to
 // p.l2_lookahead bytes beyond the TMA issue position and stops at an expert phase until routing
 // has chosen the experts.
+// With p.l2_rate set, the prefetches are paced by a token bucket (p.l2_rate bytes per microsecond,
+// at most p.l2_burst at once), so that the lookahead keeps HBM streaming without queueing a burst
+// of requests ahead of the step's latency-bound accesses.
 struct L2Cursor {
   int ph;
   uint64_t off;  // within the current phase's share
   uint64_t pos;  // stream position of the cursor
 };
 
+struct L2Pace {
+  uint64_t t;       // %globaltimer of the last refill
+  uint64_t tokens;  // bytes that may be prefetched now
+};
+
 __device__ __forceinline__ void l2_advance(const Params& p, const Ctl* ctl, L2Cursor& cur, uint64_t issue_pos, int ph1, uint32_t c,
-                                           uint32_t G) {
+                                           uint32_t G, uint64_t wpol, L2Pace& pace) {
+  if (p.l2_rate) {
+    const uint64_t now = globaltimer();
+    const uint64_t add = (now - pace.t) * p.l2_rate / 1000u;
+    pace.tokens = min((uint64_t)p.l2_burst, pace.tokens + add);
+    pace.t = now;
+  }
   while (cur.pos < issue_pos + p.l2_lookahead && cur.ph < ph1) {
     const PhaseDesc& Q = phase_table(ctl)[cur.ph];
     if (!Q.has_weights) { ++cur.ph; cur.off = 0; continue; }
@@ -113,7 +127,15 @@ __device__ __forceinline__ void l2_advance(const Params& p, const Ctl* ctl, L2Cu
     if (cur.off >= len) { ++cur.ph; cur.off = 0; continue; }
     const uint64_t left = len - cur.off;
     const uint32_t chunk = left < kL2Chunk ? (uint32_t)left : kL2Chunk;
-    if (cur.pos >= issue_pos) prefetch_l2(p.image + Q.region + (uint64_t)u0 * unit_bytes + cur.off, chunk);
+    if (p.l2_rate && cur.pos >= issue_pos) {
+      if (pace.tokens < chunk) return;
+      pace.tokens -= chunk;
+    }
+    if (cur.pos >= issue_pos) {
+      const uint8_t* src = p.image + Q.region + (uint64_t)u0 * unit_bytes + cur.off;
+      if (p.pf_flags & PF_W_LAST) prefetch_l2_hint(src, chunk, wpol);
+      else prefetch_l2(src, chunk);
+    }
     cur.off += chunk;
     cur.pos += chunk;
   }
@@ -121,6 +143,7 @@ __device__ __forceinline__ void l2_advance(const Params& p, const Ctl* ctl, L2Cu
 
 static __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32_t c, uint32_t G, int ph0, int ph1) {
   const uint64_t pol = policy_evict_first();
+  const uint64_t wpol = policy_evict_last();
   const uint32_t ns = (uint32_t)p.nslots;
   uint32_t t = 0;               // tiles issued
   uint32_t pslot = 0, puse = 0;  // ring slot of the next tile and how often it was filled before
@@ -128,6 +151,7 @@ static __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32
   int sel_layer = -1;
   bool stop = false;
   L2Cursor cur{ph0, 0, 0};
+  L2Pace pace{globaltimer(), 0};
   uint64_t issue_pos = 0;  // stream position of the next dense tile
   for (int step = 0; step < p.n_steps && !stop; ++step) {  // the launch's decode steps
     sel_layer = -1;
@@ -166,8 +190,20 @@ static __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32
           if (use > 0) {
             if (!mbar_try_wait(&ctl->empty[slot], (use - 1) & 1)) {
               const uint64_t tb = p.timeline ? globaltimer() : 0;
-              l2_advance(p, ctl, cur, issue_pos, ph1, c, G);  // keep HBM busy while the consumers catch up
-              if (!mbar_wait(&ctl->empty[slot], (use - 1) & 1, &ctl->abort, p.wait_ns)) {
+              l2_advance(p, ctl, cur, issue_pos, ph1, c, G, wpol, pace);  // keep HBM busy while the consumers catch up
+              bool ok;
+              if (p.l2_rate && p.l2_lookahead) {
+                // paced: refill and prefetch while waiting for the slot (bounded like every wait)
+                const uint64_t t0 = globaltimer();
+                for (;;) {
+                  if ((ok = mbar_try_wait(&ctl->empty[slot], (use - 1) & 1))) break;
+                  if (aborted(ctl) || globaltimer() - t0 > p.wait_ns) break;
+                  l2_advance(p, ctl, cur, issue_pos, ph1, c, G, wpol, pace);
+                }
+              } else {
+                ok = mbar_wait(&ctl->empty[slot], (use - 1) & 1, &ctl->abort, p.wait_ns);
+              }
+              if (!ok) {
                 if (!aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
                 stop = true;
                 break;
@@ -186,7 +222,10 @@ static __device__ void producer(const Params& p, Ctl* ctl, uint8_t* ring, uint32
             if (expert) src += (uint64_t)(*(volatile int32_t*)&ctl->sel[s]) * P.expert_stride;
             tma_load_1d(dst + (size_t)s * bytes, src, bytes, &ctl->full[slot], pol);
           }
-          if (!expert) issue_pos += bytes;
+          if (!expert) {
+            issue_pos += bytes;
+            if (p.l2_lookahead) l2_advance(p, ctl, cur, issue_pos, ph1, c, G, wpol, pace);
+          }
           ++t;
           if (++pslot == ns) {
             pslot = 0;
@@ -256,12 +295,22 @@ __device__ __forceinline__ bool ll_wait(const ll_t* src, uint32_t epoch, ll_t& w
   }
 }
 
+// One more epoch-tagged word a thread fetches alongside an ll_fetch batch (src null: none): it is
+// loaded before the batch and stored to *dst once it carries `epoch`, before the batch's closing
+// consumer_sync, so that its round trip overlaps the batch's instead of preceding it.
+struct SideWord {
+  const ll_t* src;
+  float* dst;
+  uint32_t epoch;
+};
+
 // The values of src[0..n) once each carries `epoch`, into dst in the split layout: n/seg vectors
 // of seg elements, each taking segp floats (all consumer threads, eight loads in flight per
 // thread; ends with consumer_sync).
 static __device__ void ll_fetch(const Params& p, Ctl* ctl, float* dst, const ll_t* src, int n, int seg, int segp,
-                         uint32_t epoch, int tid) {
+                         uint32_t epoch, int tid, SideWord side = SideWord{nullptr, nullptr, 0}) {
   constexpr int B = 8, T = kConsumerWarps * 32;
+  ll_t sw = side.src ? ll_load(side.src) : 0ull;
   for (int base = tid; base < n; base += B * T) {
     ll_t w[B];
 #pragma unroll
@@ -287,6 +336,7 @@ static __device__ void ll_fetch(const Params& p, Ctl* ctl, float* dst, const ll_
       }
     }
   }
+  if (side.src && ll_wait(side.src, side.epoch, sw, p, ctl)) *side.dst = ll_value(sw);
   consumer_sync();
 }
 

@@ -266,6 +266,15 @@ __device__ __forceinline__ float fma8(const float (&w)[8], const float (&x)[8], 
   return acc;
 }
 
+// The same for two rows against one input vector, as packed fp32 FMAs: lane .x is row a's chain,
+// lane .y row b's, each an IEEE fused multiply-add in element order (bit-identical to fma8 per row).
+__device__ __forceinline__ float2 fma8x2(const float (&wa)[8], const float (&wb)[8], const float (&x)[8],
+                                         float2 acc) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc = __ffma2_rn(make_float2(wa[e], wb[e]), make_float2(x[e], x[e]), acc);
+  return acc;
+}
+
 // Fold the 32 lane partials of a contract dot product: pairs (i, i+16), (i, i+8), ... (i, i+1).
 // Every lane ends with the same bits (addition is commutative in IEEE arithmetic).
 __device__ __forceinline__ float warp_fold(float a) {

@@ -361,8 +361,8 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   }
   if (!nslots) return ADP_ERR_UNSUPPORTED_CONFIG;
   xbytes = (xbytes + 127) & ~(size_t)127;
-  // the attention merge stages at least one block's outputs after the block maxima and sums
-  if ((long long)(xbytes / 4) - ((2 * nbmax_ + 2 + 3) & ~3) < hd) return ADP_ERR_UNSUPPORTED_CONFIG;
+  // the attention merge stages at least one block's outputs (8-byte words) after the block maxima and sums
+  if ((long long)(xbytes / 4) - ((2 * nbmax_ + 2 + 3) & ~3) < 2 * hd) return ADP_ERR_UNSUPPORTED_CONFIG;
   m->xbuf_floats = (int)(xbytes / 4);
   m->p.xbuf_floats = m->xbuf_floats;
   m->smem = (size_t)nslots * kSlotBytes + xbytes + ctl_bytes((int)m->phases.size());
@@ -373,12 +373,14 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   m->p.att_gmax = gmax;
   m->p.att_slot_bytes = (int)item;
   int bps = 0;
-  CK(decode_prepare(m->smem,
-                    c.n_experts > 0                   ? KK_MOE
-                    : c.weight_dtype == ADP_E4M3  ? KK_DENSE8
-                    : c.weight_dtype == ADP_NVFP4 ? KK_DENSE4
-                                                      : KK_DENSE,
-                    &bps));
+  {
+    const int kind = c.n_experts > 0                 ? KK_MOE
+                     : c.weight_dtype == ADP_E4M3  ? KK_DENSE8
+                     : c.weight_dtype == ADP_NVFP4 ? KK_DENSE4
+                                                   : KK_DENSE;
+    CK(decode_prepare(m->smem, kind, c.head_dim, c.kv_dtype, kind == KK_DENSE ? c.weight_dtype : head_dtype(c),
+                      &bps));
+  }
   if (bps < 1) return ADP_ERR_NOT_CORESIDENT;
 
   // weight image
@@ -545,6 +547,8 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   p.wait_ns = 200000000ull;
   p.l2_lookahead = 0;
   p.pf_flags = 0;
+  p.l2_rate = 0;
+  p.l2_burst = 0;
   p.n_steps = 1;
   p.skip_cta = -1;
   p.skip_phase = -1;
@@ -1523,6 +1527,14 @@ extern "C" int adp_debug_barriers(adp_model* m, int on) {
 extern "C" int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes) {
   if (!m) return ADP_ERR_INVALID_ARG;
   m->p.l2_lookahead = bytes;
+  if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
+  return ADP_OK;
+}
+
+extern "C" int adp_debug_set_l2_pacing(adp_model* m, uint32_t bytes_per_us, uint32_t burst_bytes) {
+  if (!m || (bytes_per_us && burst_bytes < 32768)) return ADP_ERR_INVALID_ARG;
+  m->p.l2_rate = bytes_per_us;
+  m->p.l2_burst = burst_bytes;
   if (m->graph) { cudaGraphExecDestroy(m->graph); m->graph = nullptr; }
   return ADP_OK;
 }

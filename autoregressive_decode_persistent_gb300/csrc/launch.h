@@ -19,7 +19,9 @@ struct RepackSrc {
   int32_t hd, hq, hkv;
 };
 
-cudaError_t decode_prepare(size_t smem_bytes, int kind, int* blocks_per_sm);  // kind: KernelKind
+// kind: KernelKind; hd, kvdt and t16 (the 16-bit weight type of a 16-bit model, else the embedding's)
+// select the kernel instantiation, as decode_launch does from the parameters
+cudaError_t decode_prepare(size_t smem_bytes, int kind, int hd, int kvdt, int t16, int* blocks_per_sm);
 cudaError_t decode_launch(const Params& p, int ph0, int ph1, bool persistent, int grid, size_t smem_bytes,
                           int xbuf_floats, cudaStream_t stream);
 cudaError_t repack_launch(uint8_t* image, const PhaseDesc& P, const RepackSrc& S, int grid, int experts,

@@ -141,6 +141,8 @@ struct Params {
   uint64_t wait_ns;            // limit of every in-kernel wait
   uint32_t l2_lookahead;       // bytes of weight stream prefetched into L2 beyond the TMA loads
   uint32_t pf_flags;           // PF_* bits: how the KV cache and the weight lookahead are prefetched
+  uint32_t l2_rate;            // lookahead pacing: bytes per microsecond per CTA (0 = unpaced)
+  uint32_t l2_burst;           // lookahead pacing: most bytes issued at once (token-bucket depth)
   int32_t debug_barriers;      // 1: also take a grid barrier after every phase (debugging)
   int32_t n_steps;             // decode steps this launch runs back to back (persistent launch)
   int32_t nslots;              // weight ring depth (slots of kSlotBytes)

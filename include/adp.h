@@ -351,6 +351,11 @@ int adp_debug_set_l2_lookahead(adp_model* m, uint32_t bytes);
  * evict-last priority, 4 = the weight lookahead with the evict-last priority.  Other bits:
  * ADP_ERR_INVALID_ARG.  A tuning knob; results do not depend on it. */
 int adp_debug_set_prefetch_flags(adp_model* m, uint32_t flags);
+/* Pace the weight lookahead (adp_debug_set_l2_lookahead) with a token bucket per CTA: at most
+ * bytes_per_us bytes of prefetch per microsecond, at most burst_bytes (>= 32768) at once;
+ * bytes_per_us = 0 (the default) issues the lookahead unpaced.  A tuning knob; results do not
+ * depend on it. */
+int adp_debug_set_l2_pacing(adp_model* m, uint32_t bytes_per_us, uint32_t burst_bytes);
 /* Depth of the per-CTA weight ring in 32 KB slots: the model takes the deepest ring (at most 6)
  * that fits beside its other shared-memory buffers; this lowers it (3 <= slots <= that depth,
  * else ADP_ERR_INVALID_ARG), for measurements.  adp_debug_ring_slots reads the current depth. */

@@ -32,6 +32,8 @@ def built():
     ("moe-32x1408-top4-e4m3", 256, 5, 0.0),
     ("dense-2.3b-e4m3", 512, 5, 0.0),
     ("dense-2.3b-nvfp4", 512, 5, 0.0),
+    ("dense-8b-e4m3", 1024, 3, 0.0),
+    ("dense-8b-nvfp4", 1024, 2, 0.0),
 ])
 def test_full_size_workload(built, name, prefix, steps, temperature):
     from autoregressive_decode_persistent_gb300.model import DecodeModel

@@ -75,7 +75,7 @@ def test_tiny_temperature_sampling_bit_exact(torch_cuda):
 
 
 @pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "moe-32x1408-top4-e4m3", "dense-2.3b-e4m3",
-                                  "dense-2.3b-nvfp4"])
+                                  "dense-2.3b-nvfp4", "dense-8b-e4m3", "dense-8b-nvfp4"])
 def test_shrunk_workloads_bit_exact(torch_cuda, name):
     cfg = synth.shrink(synth.get_config(name))
     _check_case(cfg, 8, 40)
