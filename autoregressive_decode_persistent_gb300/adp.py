@@ -74,7 +74,7 @@ class Sampling(ctypes.Structure):
 class PhasePlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("kind", "layer", "n_units", "unit_rows", "slots", "K", "KC",
                                                "n_chunks", "upr", "dtype", "src_phase", "res_phase",
-                                               "sel_phase", "pad")] + \
+                                               "sel_phase", "replicated")] + \
                [("region", ctypes.c_uint64), ("expert_stride", ctypes.c_uint64)]
 
 

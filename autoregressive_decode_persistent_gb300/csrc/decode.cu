@@ -95,12 +95,16 @@ __device__ __forceinline__ SideWord residual_word(const Params& p, Ctl* ctl, con
 // Z = sum_i e_i sequentially in expert order; each of the top_k choices is a warp argmax over
 // (P_i, lowest index) of the experts not yet chosen; lane 0 sums the chosen P in slot order and
 // divides.  Every value is the same operation on the same operands as a sequential evaluation.
-__device__ void select_experts(const Params& p, Ctl* ctl, int layer, uint32_t r_epoch, int lane) {
+// local: the CTA computed the router logits itself and left them in ctl->stage (the router phase
+// ran in this launch); else they are fetched from the published words.
+__device__ void select_experts(const Params& p, Ctl* ctl, int layer, uint32_t r_epoch, int lane, bool local) {
   const int E = p.E, K = p.topk;
   float* st = ctl->stage;
-  for (int e = lane; e < E; e += 32) {
-    ll_t w = ll_load(p.rlog + e);
-    st[e] = ll_wait(p.rlog + e, r_epoch, w, p, ctl) ? ll_value(w) : 0.0f;
+  if (!local) {
+    for (int e = lane; e < E; e += 32) {
+      ll_t w = ll_load(p.rlog + e);
+      st[e] = ll_wait(p.rlog + e, r_epoch, w, p, ctl) ? ll_value(w) : 0.0f;
+    }
   }
   __syncwarp();
   float M = __int_as_float(0xFF800000);
@@ -110,8 +114,17 @@ __device__ void select_experts(const Params& p, Ctl* ctl, int layer, uint32_t r_
   for (int e = lane; e < E; e += 32) st[e] = exp_c(__fsub_rn(st[e], M));
   __syncwarp();
   float Z = 0.0f;
-  if (lane == 0)
-    for (int e = 0; e < E; ++e) Z = __fadd_rn(Z, st[e]);
+  if (lane == 0) {
+    int e = 0;
+    for (; e + 8 <= E; e += 8) {  // eight loads in flight, then the sums in expert order
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = st[e + k];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) Z = __fadd_rn(Z, v[k]);
+    }
+    for (; e < E; ++e) Z = __fadd_rn(Z, st[e]);
+  }
   Z = __shfl_sync(0xFFFFFFFFu, Z, 0);
   for (int e = lane; e < E; e += 32) st[e] = __fdiv_rn(st[e], Z);  // P_e
   __syncwarp();
@@ -359,11 +372,14 @@ __device__ __forceinline__ void gemv_phase(const Params& p, Ctl* ctl, uint8_t* r
     } else if (kind == PK_GU) {
       if (lane == 0) ll_store(p.h + unit, ll_pack(silu_mul(acc[0], acc[1]), ew));
     } else if (kind == PK_ROUTER) {
+      // every CTA computes every logit (a replicated phase): into shared memory for its own
+      // choice of experts; CTA 0 also publishes them, for a launch that starts at the expert phase
       if (lane < ROWS) {
         float y = acc[0];
 #pragma unroll
         for (int j = 1; j < ROWS; ++j) if (lane == j) y = acc[j];
-        ll_store(p.rlog + unit * ROWS + lane, ll_pack(y, ew));
+        ctl->stage[unit * ROWS + lane] = y;
+        if (c == 0) ll_store(p.rlog + unit * ROWS + lane, ll_pack(y, ew));
       }
     } else if (kind == PK_EGU) {
       if (lane < p.topk) {
@@ -479,7 +495,7 @@ __device__ __forceinline__ void prefetch_attention_kv(const Params& p, int L, in
 template <int HD, int KVDT>
 __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float* xbuf, const PhaseDesc& P,
                                              const Step& st, uint32_t c, uint32_t G, int cw, int lane,
-                                             uint32_t& att_uses_io, uint32_t& merge_uses, uint32_t ew) {
+                                             uint32_t& att_uses_io, uint32_t ew) {
   constexpr int NV = HD / 8;         // 8-element vectors per K row (partial sums of the contract dot)
   constexpr int KSTR = HD + 8;       // padded K row stride in shared memory (conflict-free row reads)
   constexpr int DPL = HD / 32;       // output dims per lane in the PV pass
@@ -706,20 +722,14 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
     }
     consumer_sync();
     if (tid == 0) stamp(p, c, P.index, 10);
-    // Every block's maximum and sum has arrived, so its outputs almost surely have too: one bulk
-    // copy per batch brings them ([block][dim], epoch-tagged) into shared memory while warp 0
-    // forms the weights.
-    ll_t* So = reinterpret_cast<ll_t*>(xbuf + ((2 * nbmax + 2 + 3) & ~3));  // 16-byte aligned
-    const int batch = (int)(((size_t)p.xbuf_floats - (size_t)((2 * nbmax + 2 + 3) & ~3)) * 4 / ((size_t)HD * 8));
-    auto issue = [&](int b0) {
-      const int nbk = min(batch, nb - b0);
-      asm volatile("fence.proxy.async.global;" ::: "memory");  // outputs other CTAs stored, read by TMA
-      mbar_arrive_expect_tx(&ctl->merge_bar, (uint32_t)nbk * HD * 8);
-      tma_load_1d(So, part_o + ((size_t)h * nbmax + b0) * HD, (uint32_t)nbk * HD * 8, &ctl->merge_bar,
-                  policy_evict_first());
-    };
-    if (tid == 0) issue(0);
-    if (cw == 0) {
+    // Every block's maximum and sum has arrived, and each block publishes its outputs before
+    // them, so the outputs almost surely have too: all consumer threads load them (eight words in
+    // flight each, [block][dim]) into shared memory as fp32, while warp 0, whose own loads are in
+    // flight, forms the weights.  Blocks beyond what the staging area holds come in further batches.
+    float* So = xbuf + ((2 * nbmax + 2 + 3) & ~3);
+    const int batch = (int)(((size_t)p.xbuf_floats - (size_t)((2 * nbmax + 2 + 3) & ~3)) / (size_t)HD);
+    bool ok = true;
+    auto weights = [&]() {
       float M = __int_as_float(0xFF800000);
       for (int bb = lane; bb < nb; bb += 32) M = fmaxf(M, Wm[bb]);
 #pragma unroll
@@ -743,27 +753,58 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
         Wl[nbmax] = Ls;
         stamp(p, c, P.index, 12);
       }
-    }
-    consumer_sync();
+    };
     float O = 0.0f;
-    bool ok = true;
     for (int b0 = 0; b0 < nb; b0 += batch) {
       const int nbk = min(batch, nb - b0);
-      ok = ok && mbar_wait(&ctl->merge_bar, merge_uses & 1, &ctl->abort, wait_ns);
-      ++merge_uses;
-      if (!ok && tid == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
-      if (ok && tid < HD) {
-        for (int t2 = 0; t2 < nbk && ok; ++t2) {
-          ll_t x = So[(size_t)t2 * HD + tid];
-          if (ll_epoch(x) != ew) ok = ll_wait(part_o + ((size_t)h * nbmax + b0 + t2) * HD + tid, ew, x, p, ctl);
-          O = fmaf(Wm[b0 + t2], ll_value(x), O);
+      const ll_t* src = part_o + ((size_t)h * nbmax + b0) * HD;
+      const int nw = nbk * HD;
+      constexpr int B = 8, T = kConsumerWarps * 32;
+      bool first = b0 == 0;
+      for (int base = tid; base < nw; base += B * T) {
+        ll_t w[B];
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+          const int i = base + k * T;
+          w[k] = i < nw ? ll_load(src + i) : 0ull;
+        }
+        if (first && cw == 0) weights();  // warp 0's loads are in flight meanwhile
+        first = false;
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+          const int i = base + k * T;
+          if (i < nw) {
+            if (ll_epoch(w[k]) != ew) {
+              if (!ll_wait(src + i, ew, w[k], p, ctl)) { ok = false; break; }
+#pragma unroll
+              for (int j = k + 1; j < B; ++j) {  // reload the rest together (see ll_fetch)
+                const int ij = base + j * T;
+                if (ij < nw && ll_epoch(w[j]) != ew) w[j] = ll_load(src + ij);
+              }
+            }
+            So[i] = ll_value(w[k]);
+          }
         }
       }
-      if (b0 + nbk < nb) {  // the staging area is reused by the next batch after every thread read it
-        consumer_sync();
-        if (tid == 0) issue(b0 + nbk);
+      if (first && cw == 0) weights();  // a batch with fewer words than threads
+      consumer_sync();
+      if (tid < HD) {
+        int t2 = 0;
+        for (; t2 + 8 <= nbk; t2 += 8) {
+          float ov[8], wv[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            ov[k] = So[(size_t)(t2 + k) * HD + tid];
+            wv[k] = Wm[b0 + t2 + k];
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) O = fmaf(wv[k], ov[k], O);
+        }
+        for (; t2 < nbk; ++t2) O = fmaf(Wm[b0 + t2], So[(size_t)t2 * HD + tid], O);
       }
+      if (b0 + nbk < nb) consumer_sync();  // the staging area is reused by the next batch
     }
+    ok = ok && !aborted(ctl);
     if (tid == 0) stamp(p, c, P.index, 13);
     if (ok && tid < HD) ll_store(attn + (size_t)h * HD + tid, ll_pack(__fdiv_rn(O, Wl[nbmax]), ew));
     if (tid == 0) stamp(p, c, P.index, 11);
@@ -903,7 +944,7 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
   uint32_t t = 0;
   int bidx = 0;
   int sel_layer = -1;
-  uint32_t att_uses = 0, merge_uses = 0;
+  uint32_t att_uses = 0;
   const int tid = cw * 32 + lane;
   constexpr bool MOE = KIND == KK_MOE;
   for (int step = 0; step < p.n_steps; ++step) {
@@ -984,7 +1025,7 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
           if constexpr (MOE) {
             if (sel_layer != L) {
               if (cw == 0) {
-                select_experts(p, ctl, L, e_sel, lane);
+                select_experts(p, ctl, L, e_sel, lane, false);
                 if (lane == 0) mbar_arrive(&ctl->sel_bar);
               }
               sel_layer = L;
@@ -1003,15 +1044,18 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
           break;
         case PK_EGU:
           if constexpr (MOE) {
+            // the router phase ran in this launch: its logits are in shared memory, and the input
+            // vector still holds rmsnorm(x, ffn_norm), the router's input and this phase's
+            const bool local = P.sel_ph >= ph0;
             if (cw == 0) {
-              select_experts(p, ctl, L, e_sel, lane);
+              select_experts(p, ctl, L, e_sel, lane, local);
               if (lane == 0) {
                 if (c == 0 && !ab) for (int i = 0; i < p.topk; ++i) p.sel_out[L * p.topk + i] = ctl->sel[i];
                 mbar_arrive(&ctl->sel_bar);  // release the choice to the producer
               }
             }
             sel_layer = L;
-            if (n > 0) rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, e_src, -1, c, cw, lane);
+            if (!local && n > 0) rmsnorm_prologue(p, ctl, xbuf, p.ffn_norm[L], nullptr, e_src, -1, c, cw, lane);
             else consumer_sync();
           }
           break;
@@ -1024,15 +1068,15 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
       if (cw == 0 && lane == 0) stamp(p, c, ph, 1);
       if (P.kind == PK_ATTN) {
         if constexpr (S::on) {
-          attention_phase<S::hd, S::kvdt>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+          attention_phase<S::hd, S::kvdt>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
         } else if (p.kvdt == DT_BF16) {
-          if (p.hd == 128) attention_phase<128, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
-          else if (p.hd == 64) attention_phase<64, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
-          else attention_phase<256, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+          if (p.hd == 128) attention_phase<128, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+          else if (p.hd == 64) attention_phase<64, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+          else attention_phase<256, DT_BF16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
         } else {
-          if (p.hd == 128) attention_phase<128, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
-          else if (p.hd == 64) attention_phase<64, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
-          else attention_phase<256, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, merge_uses, ew);
+          if (p.hd == 128) attention_phase<128, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+          else if (p.hd == 64) attention_phase<64, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
+          else attention_phase<256, DT_F16>(p, ctl, xbuf, P, st, c, G, cw, lane, att_uses, ew);
         }
       } else if (P.kind == PK_SAMPLE) {
         if (st.temperature > 0.0f) sample_phase(p, ctl, st, c, G, cw, lane);
@@ -1047,8 +1091,13 @@ __device__ void consumer(const Params& p, Ctl* ctl, uint8_t* ring, float* xbuf, 
         }
       } else if (P.kind == PK_ROUTER) {
         if constexpr (MOE) {
-          if (p.rdt == DT_BF16) gemv_phase<1, 1, DT_BF16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
-          else gemv_phase<1, 1, DT_F16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+          if (P.unit_rows == 4) {
+            if (p.rdt == DT_BF16) gemv_phase<4, 1, DT_BF16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+            else gemv_phase<4, 1, DT_F16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+          } else {
+            if (p.rdt == DT_BF16) gemv_phase<1, 1, DT_BF16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+            else gemv_phase<1, 1, DT_F16, false>(p, ctl, ring, xbuf, P, st, c, G, cw, lane, t, ew);
+          }
         }
       } else {
         if constexpr (KIND == KK_DENSE8 || KIND == KK_DENSE4) {

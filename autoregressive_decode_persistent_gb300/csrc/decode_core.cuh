@@ -59,9 +59,14 @@ __device__ __forceinline__ void stamp(const Params& p, uint32_t c, int ph, int k
   if (p.timeline) p.timeline[((size_t)c * p.n_phases + ph) * kStamps + k] = globaltimer();
 }
 
-// Per-CTA share of a phase: units [u0, u0 + n).  (c + 1) * n_units stays below 2^32: the model
+// Per-CTA share of a phase: units [u0, u0 + n); a replicated phase gives every CTA all units.  (c + 1) * n_units stays below 2^32: the model
 // checks n_units * G < 2^32 at creation.
 __device__ __forceinline__ void cta_units(const PhaseDesc& P, uint32_t c, uint32_t G, int32_t& u0, int32_t& n) {
+  if (P.replicated) {  // every CTA streams the phase's one region and computes every unit
+    u0 = 0;
+    n = P.n_units;
+    return;
+  }
   const uint32_t nu = (uint32_t)P.n_units;
   const uint32_t a = c * nu / G, b = (c + 1) * nu / G;
   u0 = (int32_t)a;

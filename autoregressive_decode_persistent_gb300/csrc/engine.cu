@@ -194,12 +194,13 @@ static int validate(const adp_config* c, const adp_weights* w) {
 // Append a phase; weighted phases get a region of the image and a K-chunk width such that one
 // round of units fits one ring slot.
 static void add_phase(adp_model* m, int kind, int layer, int n_units, int unit_rows, int slots, int K, int eb,
-                      int wdt, bool weights, int experts) {
+                      int wdt, bool weights, int experts, bool replicated = false) {
   PhaseDesc P{};
   P.kind = kind;
   P.layer = layer;
   P.index = (int32_t)m->phases.size();
   P.has_weights = weights ? 1 : 0;
+  P.replicated = replicated ? 1 : 0;
   if (weights) {
     P.n_units = n_units;
     P.unit_rows = unit_rows;
@@ -208,7 +209,7 @@ static void add_phase(adp_model* m, int kind, int layer, int n_units, int unit_r
     P.eb = eb;
     P.wdt = wdt;
     // balanced rounds of at most kConsumerWarps units over the largest per-CTA share
-    const int maxu = std::max(1, (n_units + m->G - 1) / m->G);
+    const int maxu = replicated ? std::max(1, n_units) : std::max(1, (n_units + m->G - 1) / m->G);
     const int nrounds = (maxu + kConsumerWarps - 1) / kConsumerWarps;
     int upr = (maxu + nrounds - 1) / nrounds;
     while (upr > 1 && wbytes(P, (uint64_t)upr * unit_rows * slots * kChunkAlign) > (uint64_t)kSlotBytes) --upr;
@@ -260,7 +261,11 @@ static void plan(adp_model* m) {
       link(gu, x_ph, -1);
       x_ph = last();
     } else {
-      add_phase(m, PK_ROUTER, l, c.n_experts, 1, 1, d, elem_bytes(c.router_dtype), c.router_dtype, true, 1);
+      // every CTA computes all router logits itself (its experts are then chosen without a hop), in
+      // units of 4 rows when the expert count allows (one round of at most 8 units for 32 experts)
+      const int rrows = c.n_experts % 4 == 0 ? 4 : 1;
+      add_phase(m, PK_ROUTER, l, c.n_experts / rrows, rrows, 1, d, elem_bytes(c.router_dtype), c.router_dtype, true, 1,
+                true);
       link(x_ph, -1, -1);
       const int router = last();
       add_phase(m, PK_EGU, l, c.d_expert, 2, c.top_k, d, 1, ADP_E4M3, true, c.n_experts);
@@ -426,7 +431,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
         default: break;
       }
     }
-    CK(repack_launch(m->image, P, S, m->G, experts, m->stream));
+    CK(repack_launch(m->image, P, S, P.replicated ? 1 : m->G, experts, m->stream));
   }
   (void)eb;
 
@@ -1450,7 +1455,7 @@ extern "C" int adp_plan(const adp_config* cfg, int32_t n_sms, adp_phase_plan* ou
     o.src_phase = P.src_ph;
     o.res_phase = P.res_ph;
     o.sel_phase = P.sel_ph;
-    o.pad = 0;
+    o.replicated = P.replicated;
     o.region = P.region;
     o.expert_stride = P.expert_stride;
   }

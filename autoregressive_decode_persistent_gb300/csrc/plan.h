@@ -63,7 +63,7 @@ struct PhaseDesc {
   int32_t src_ph;         // phase whose output vector is this phase's input (-1: the embedding row)
   int32_t res_ph;         // phase that wrote the residual rows this phase updates (-1: none)
   int32_t sel_ph;         // router phase whose logits choose this phase's experts (-1: none)
-  int32_t pad_;
+  int32_t replicated;     // 1: every CTA takes all units (one shared region of the image), 0: an even split
   uint64_t region;        // byte offset of the phase's region in the image (expert 0 for expert phases)
   uint64_t expert_stride; // bytes of one expert's region
 };

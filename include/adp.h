@@ -283,7 +283,9 @@ typedef struct {
   int32_t src_phase;  /* phase whose output vector this phase reads (-1: the embedding row) */
   int32_t res_phase;  /* phase that wrote the residual rows this phase adds to (-1: none) */
   int32_t sel_phase;  /* router phase whose logits choose this phase's experts (-1: none) */
-  int32_t pad;
+  int32_t replicated; /* 1: every CTA streams the phase's one region and computes all its units
+                       * (the router: each CTA chooses its experts without a hop); 0: units split
+                       * evenly over the CTAs */
   uint64_t region;        /* byte offset of the phase's region in the weight image */
   uint64_t expert_stride; /* bytes of the region (per expert), a multiple of 256 */
 } adp_phase_plan;

@@ -53,8 +53,11 @@ CASES = _cases()
 IDS = [f'{c["name"]}-{i}' for i, c in enumerate(CASES)]
 
 
-def _shares(n_units, G):
-    """(u0, n) of every CTA: units [floor(c n / G), floor((c + 1) n / G))."""
+def _shares(n_units, G, replicated=0):
+    """(u0, n) of every CTA: units [floor(c n / G), floor((c + 1) n / G)); a replicated phase gives
+    every CTA all units (one shared region of the image)."""
+    if replicated:
+        return [(0, n_units)] * G
     return [(c * n_units // G, (c + 1) * n_units // G - c * n_units // G) for c in range(G)]
 
 
@@ -84,7 +87,7 @@ def test_tiles_fit_one_slot_and_are_bulk_copies(adp, cfg, n_sms):
         if KC < math.ceil(K / ALIGN) * ALIGN:
             assert wbytes(dt, upr * ur * s * (KC + ALIGN)) > SLOT
         unit_bytes = wbytes(dt, ur * K)
-        for u0, n in set(_shares(p["n_units"], n_sms)):
+        for u0, n in set(_shares(p["n_units"], n_sms, p["replicated"])):
             assert (p["region"] + u0 * unit_bytes) % 16 == 0
             if n == 0:
                 continue
@@ -99,6 +102,15 @@ def test_tiles_fit_one_slot_and_are_bulk_copies(adp, cfg, n_sms):
                     assert b % 16 == 0 and off % 16 == 0 and 0 < b * s <= SLOT
                     pos += b
             assert pos == n * unit_bytes
+
+
+@pytest.mark.parametrize("cfg", CASES, ids=IDS)
+def test_only_the_router_is_replicated(adp, cfg):
+    """Every CTA computes all router logits (its experts are chosen without a hop); every other
+    phase splits its units over the CTAs."""
+    ph, _ = _plan(adp, cfg)
+    for p in ph:
+        assert p["replicated"] == (1 if p["kind"] == KINDS["router"] else 0), p
 
 
 @pytest.mark.parametrize("cfg", CASES, ids=IDS)
