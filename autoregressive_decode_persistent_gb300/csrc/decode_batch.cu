@@ -171,9 +171,11 @@ __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, 
     float acc[NA];
 #pragma unroll
     for (int i = 0; i < NA; ++i) acc[i] = 0.0f;
-    // e4m3 layer matrices: this unit's row scales, applied after the fold (as for one request)
+    // e4m3 and NVFP4 layer matrices: this unit's row scales, applied after the fold (as for one
+    // request)
+    constexpr bool kScaled = WDT == DT_E4M3 || WDT == DT_NVFP4;
     float sc[ROWS];
-    if constexpr (WDT == DT_E4M3) {
+    if constexpr (kScaled) {
       if (active) {
         int mi, r0, rstep = 1;
         if (kind == PK_QKV) {
@@ -206,8 +208,33 @@ __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, 
       if (active && ok) {
         const int kck = min(KC, K - ck * KC);
         const int nvec = kck >> 3;
-        const uint8_t* tile = ring + (size_t)slot * kSlotBytes + (size_t)cw * ROWS * kck * EB;
         const int xv = (ck * KC) >> 3;
+        if constexpr (WDT == DT_NVFP4) {
+          // [m * ROWS rows][kck / 2] code bytes, then [m * ROWS][kck / 16] block scales; per 8-element
+          // vector the products summed from zero, times the block scale, into the lane partial (the
+          // single-request contract, per request)
+          const uint8_t* base = ring + (size_t)slot * kSlotBytes;
+          const uint8_t* codes = base + (size_t)cw * ROWS * (kck >> 1);
+          const uint8_t* bsc = base + (size_t)m * ROWS * (kck >> 1) + (size_t)cw * ROWS * (kck >> 4);
+          for (int v = lane; v < nvec; v += 32) {
+            // one row's codes at a time (fewer live registers than the 16-bit path's row pairs)
+#pragma unroll
+            for (int j = 0; j < ROWS; ++j) {
+              float w8[8];
+              load8_e2m1(*reinterpret_cast<const uint32_t*>(codes + (size_t)j * (kck >> 1) + (size_t)v * 4), w8);
+              const float bs = e4m3_to_f32(bsc[(size_t)j * (kck >> 4) + (v >> 1)]);
+#pragma unroll
+              for (int r = 0; r < kMaxBatch; ++r) {
+                if (r < nb) {
+                  float x8[8];
+                  load_xs8(xbuf + r * Kp, xv + v, x8);
+                  acc[r * ROWS + j] = fmaf(bs, fma8(w8, x8, 0.0f), acc[r * ROWS + j]);
+                }
+              }
+            }
+          }
+        } else {
+        const uint8_t* tile = ring + (size_t)slot * kSlotBytes + (size_t)cw * ROWS * kck * EB;
         for (int v = lane; v < nvec; v += 32) {
           float w[ROWS][8];
 #pragma unroll
@@ -221,6 +248,7 @@ __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, 
               for (int j = 0; j < ROWS; ++j) acc[r * ROWS + j] = fma8(w[j], x8, acc[r * ROWS + j]);
             }
           }
+        }
         }
       }
       __syncwarp();
@@ -238,7 +266,7 @@ __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, 
 #pragma unroll
         for (int j = 0; j < ROWS; ++j) {
           acc[r * ROWS + j] = warp_fold(acc[r * ROWS + j]);
-          if constexpr (WDT == DT_E4M3) acc[r * ROWS + j] = __fmul_rn(sc[j], acc[r * ROWS + j]);
+          if constexpr (kScaled) acc[r * ROWS + j] = __fmul_rn(sc[j], acc[r * ROWS + j]);
         }
     // ---- epilogues (every lane holds every folded sum)
     if (kind == PK_QKV) {
@@ -292,7 +320,7 @@ __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, 
       }
     } else if (kind == PK_GU) {
       if (lane < nb) ll_store(p.h + (size_t)lane * p.ff + unit, ll_pack(silu_mul(pick(acc, 2 * lane), pick(acc, 2 * lane + 1)), ew));
-    } else if (kind == PK_LM) {
+    } else if (kind == PK_LM && !kScaled) {  // (the LM head is always a 16-bit matrix)
       if (lane == 0) {
 #pragma unroll
         for (int r = 0; r < kMaxBatch; ++r) {
@@ -771,6 +799,8 @@ __device__ void consumer_batch(const Params& p, Ctl* ctl, BCtl* bc, uint8_t* rin
         if (bc->any_sample) sample_batch(p, ctl, bc, ebase, c, G, cw, lane);
       } else if (p.wdt == DT_E4M3 && P.kind != PK_LM) {
         gemv_batch<2, DT_E4M3>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew);
+      } else if (p.wdt == DT_NVFP4 && P.kind != PK_LM) {
+        gemv_batch<2, DT_NVFP4>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew);
       } else if ((P.kind == PK_LM ? p.edt : p.wdt) == DT_BF16) {
         run_gemv_batch<DT_BF16>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew);
       } else {

@@ -94,12 +94,15 @@ struct adp_model {
   struct TcState {
     int init_rc = 1;
     std::vector<const uint8_t*> wqkv, wo, wgu, wdown;
+    std::vector<const float*> sqkv, swo, sgu, sdown;  // column scales of quantised layer matrices
     int cap = 0;
     int32_t* tokens = nullptr;
     float* x = nullptr;
     uint8_t* A = nullptr;
     uint8_t* A2 = nullptr;
     uint8_t* Qt = nullptr;  // query tiles of the attention kernel
+    uint8_t* Kt = nullptr;  // key / transposed value tiles of every cache position (the attention's)
+    uint8_t* Vt = nullptr;
     float* C = nullptr;     // fp32 QKV output (the timing hook's plain-store QKV GEMM only)
   } tc;
   // Batched decode (set up at the first batched call): per-request buffers for kMaxBatch
@@ -868,7 +871,6 @@ static int batch_init(adp_model* m) {
   const adp_config& c = m->cfg;
   B.init_rc = ADP_ERR_UNSUPPORTED_CONFIG;
   if (c.n_experts != 0) return B.init_rc;  // experts differ per request
-  if (c.weight_dtype == ADP_NVFP4) return B.init_rc;  // the batched kernel reads 16-bit or e4m3 weights
   const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim;
   cudaDeviceProp prop;
   CK(cudaGetDeviceProperties(&prop, m->device));
@@ -1106,13 +1108,21 @@ static int tc_init(adp_model* m) {
   for (const PhaseDesc& P : m->phases) {
     int rows = 0;
     std::vector<const uint8_t*>* dst = nullptr;
-    const float* sc3[3] = {nullptr, nullptr, nullptr};  // row scales of e4m3 matrices
+    std::vector<const float*>* sdst = nullptr;
+    const float* sc3[3] = {nullptr, nullptr, nullptr};  // row scales of e4m3 / NVFP4 matrices
     auto scale = [&](int i) { return m->h_wscale[i].empty() ? nullptr : m->h_wscale[i][P.layer]; };
     switch (P.kind) {
-      case PK_QKV: rows = (hq + 2 * hkv) * hd; dst = &T.wqkv; sc3[0] = scale(0); sc3[1] = scale(1); sc3[2] = scale(2); break;
-      case PK_WO: rows = d; dst = &T.wo; sc3[0] = scale(3); break;
-      case PK_GU: rows = 2 * c.d_ff; dst = &T.wgu; sc3[0] = scale(4); sc3[1] = scale(5); break;
-      case PK_DOWN: rows = d; dst = &T.wdown; sc3[0] = scale(6); break;
+      case PK_QKV:
+        rows = (hq + 2 * hkv) * hd;
+        dst = &T.wqkv;
+        sdst = &T.sqkv;
+        sc3[0] = scale(0);
+        sc3[1] = scale(1);
+        sc3[2] = scale(2);
+        break;
+      case PK_WO: rows = d; dst = &T.wo; sdst = &T.swo; sc3[0] = scale(3); break;
+      case PK_GU: rows = 2 * c.d_ff; dst = &T.wgu; sdst = &T.sgu; sc3[0] = scale(4); sc3[1] = scale(5); break;
+      case PK_DOWN: rows = d; dst = &T.wdown; sdst = &T.sdown; sc3[0] = scale(6); break;
       default: continue;
     }
     uint8_t* buf = nullptr;
@@ -1120,10 +1130,25 @@ static int tc_init(adp_model* m) {
     int rc = m->alloc(&buf, bytes);
     if (rc) return T.init_rc = rc;
     CK(cudaMemsetAsync(buf, 0, bytes, m->stream));
-    CK(tc_unpack(m->image, P, m->G, hd, hq, hkv, c.d_ff, buf, sc3[0], sc3[1], sc3[2], tc_operand_bf16(c),
-                 m->stream));
+    CK(tc_unpack(m->image, P, m->G, hd, hq, hkv, c.d_ff, buf, tc_operand_bf16(c), m->stream));
     dst->push_back(buf);
+    if (sc3[0]) {  // quantised: the row scales become the GEMM's column scales
+      float* cs = nullptr;
+      if ((rc = m->alloc(&cs, (size_t)rows))) return T.init_rc = rc;
+      CK(tc_colscale(P, rows, hd, hq, hkv, c.d_ff, sc3[0], sc3[1], sc3[2], cs, m->stream));
+      sdst->push_back(cs);
+    }
   }
+  // 128 positions x head_dim 16-bit values per block, for every KV head: K tiles and V^T tiles
+  const size_t kv_bytes = (size_t)hkv * ((c.max_ctx + 127) / 128) * 128 * hd * 2;
+  if (!T.sqkv.empty() && (T.sqkv.size() != T.wqkv.size() || T.swo.size() != T.wo.size() ||
+                          T.sgu.size() != T.wgu.size() || T.sdown.size() != T.wdown.size()))
+    return T.init_rc = ADP_ERR_INVALID_ARG;  // every layer matrix quantised, or none
+  int rc = m->alloc(&T.Kt, kv_bytes);
+  if (!rc) rc = m->alloc(&T.Vt, kv_bytes);
+  if (rc) return T.init_rc = rc;
+  CK(cudaMemsetAsync(T.Kt, 0, kv_bytes, m->stream));
+  CK(cudaMemsetAsync(T.Vt, 0, kv_bytes, m->stream));
   CK(cudaStreamSynchronize(m->stream));
   return T.init_rc = ADP_OK;
 }
@@ -1173,6 +1198,9 @@ extern "C" int adp_debug_tc_gemm_time(adp_model* m, int32_t which, int32_t M, in
   const int N[4] = {qkv_n, c.d_model, 2 * c.d_ff, c.d_model};
   const int K[4] = {c.d_model, c.n_heads * c.head_dim, c.d_model, c.d_ff};
   const uint8_t* Wt[4] = {m->tc.wqkv[0], m->tc.wo[0], m->tc.wgu[0], m->tc.wdown[0]};
+  const bool q = !m->tc.sqkv.empty();
+  const float* Cs[4] = {q ? m->tc.sqkv[0] : nullptr, q ? m->tc.swo[0] : nullptr, q ? m->tc.sgu[0] : nullptr,
+                        q ? m->tc.sdown[0] : nullptr};
   // each GEMM as the prefill runs it: QKV stores into C, Wo and down add into the residual x,
   // gate|up writes SwiGLU into the down GEMM's A tiles; down reads those tiles
   const int kmax = std::max(c.d_model, c.n_heads * c.head_dim);
@@ -1189,10 +1217,12 @@ extern "C" int adp_debug_tc_gemm_time(adp_model* m, int32_t which, int32_t M, in
   CK(cudaEventCreate(&e0));
   CK(cudaEventCreate(&e1));
   const int w = which;
-  CK(tc_gemm(bf16, mode[w], Ain[w], Wt[w], out[w], ldo[w], M, N[w], K[w], m->p.err, 1000000000ull, m->stream));
+  CK(tc_gemm(bf16, mode[w], Ain[w], Wt[w], out[w], ldo[w], M, N[w], K[w], m->p.err, 1000000000ull, m->stream,
+             nullptr, Cs[w]));
   CK(cudaEventRecord(e0, m->stream));
   for (int i = 0; i < reps; ++i)
-    CK(tc_gemm(bf16, mode[w], Ain[w], Wt[w], out[w], ldo[w], M, N[w], K[w], m->p.err, 1000000000ull, m->stream));
+    CK(tc_gemm(bf16, mode[w], Ain[w], Wt[w], out[w], ldo[w], M, N[w], K[w], m->p.err, 1000000000ull, m->stream,
+               nullptr, Cs[w]));
   CK(cudaEventRecord(e1, m->stream));
   CK(cudaEventSynchronize(e1));
   float ms = 0.0f;
@@ -1243,6 +1273,10 @@ extern "C" int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_toke
     a.wo = m->tc.wo.data();
     a.wgu = m->tc.wgu.data();
     a.wdown = m->tc.wdown.data();
+    a.sqkv = m->tc.sqkv.empty() ? nullptr : m->tc.sqkv.data();
+    a.swo = m->tc.swo.empty() ? nullptr : m->tc.swo.data();
+    a.sgu = m->tc.sgu.empty() ? nullptr : m->tc.sgu.data();
+    a.sdown = m->tc.sdown.empty() ? nullptr : m->tc.sdown.data();
     a.kc = kv->k;
     a.vc = kv->v;
     a.rope_cos = m->p.rope_cos;
@@ -1251,6 +1285,9 @@ extern "C" int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_toke
     a.A = m->tc.A;
     a.A2 = m->tc.A2;
     a.Qt = m->tc.Qt;
+    a.Kt = m->tc.Kt;
+    a.Vt = m->tc.Vt;
+    a.n_kb = (c.max_ctx + 127) / 128;
     a.err = m->p.err;
     a.wait_ns = std::max<uint64_t>(m->p.wait_ns, 1000000000ull);
     CK(tc_prefill(a, m->stream));

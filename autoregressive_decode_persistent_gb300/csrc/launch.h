@@ -47,14 +47,19 @@ struct TcQkvEpi {
   uint16_t* kc;           // [L][hkv][max_ctx][hd]
   uint16_t* vc;
   uint8_t* qt;            // [hq][ceil(P/128)][hd/64 tiles of 128 x 64]: queries in the core-matrix layout
-  int pos0, L, hq, hkv, hd, max_ctx, kvdt, n_tb;
+  uint8_t* kt;            // [hkv][n_kb][hd/64 tiles of 128 keys x 64]: keys by position, the same layout
+  uint8_t* vt;            // [hkv][n_kb][2 tiles of hd x 64 keys]: values by position, transposed
+  int pos0, L, hq, hkv, hd, max_ctx, kvdt, n_tb, n_kb;
 };
 
 // Tensor-core GEMM of the prefill path (prefill.cu): A W^T with A and W in the tiled tensor-core
 // layout (A: 128-row tiles, rows allocated in multiples of 256; W: 256-row tiles; 64 K-elements
 // each), epilogue `mode`.
+// colscale (optional, device [N]): every output column is multiplied by its entry first (the row
+// scales of quantised weights, whose operand tiles hold the exact codes).
 cudaError_t tc_gemm(int bf16, int mode, const uint8_t* A_tiled, const uint8_t* W_tiled, float* C, int ldc, int M,
-                    int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st, const TcQkvEpi* qkv = nullptr);
+                    int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st, const TcQkvEpi* qkv = nullptr,
+                    const float* colscale = nullptr);
 // Row-major 16-bit [rows, K] (row stride ld) -> tiles of tile_rows x 64, zero-padded.
 cudaError_t tc_tile(const uint16_t* src, int rows, int K, int ld, uint8_t* dst, int tile_rows, cudaStream_t st);
 size_t tc_tiled_bytes(int rows, int K, int tile_rows);
@@ -72,6 +77,10 @@ struct TcPrefill {
   const uint8_t* const* wo;
   const uint8_t* const* wgu;
   const uint8_t* const* wdown;
+  const float* const* sqkv;     // host arrays [L] of device column scales (quantised weights), or null
+  const float* const* swo;
+  const float* const* sgu;
+  const float* const* sdown;
   uint16_t* kc;
   uint16_t* vc;
   const float* rope_cos;
@@ -80,6 +89,9 @@ struct TcPrefill {
   uint8_t* A;      // device A-operand tiles, rows padded to 256, K up to max(d, hq*hd)
   uint8_t* A2;     // device A-operand tiles of the down GEMM (K = ff), written by gate|up's epilogue
   uint8_t* Qt;     // device query tiles written by the QKV GEMM's epilogue (see TcQkvEpi)
+  uint8_t* Kt;     // device key and transposed value tiles of every position (see TcQkvEpi), zeroed
+  uint8_t* Vt;     // at allocation so that positions never written read as finite values
+  int n_kb;        // 128-key blocks in Kt and Vt: ceil(max_ctx / 128)
   int32_t* err;
   uint64_t wait_ns;
 };
@@ -87,9 +99,13 @@ cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st);
 // Phase P's tiles of the decode image -> one GEMM weight operand in 256-row tiles (dst cleared
 // beforehand; rows in the order of the caller's matrices, except gate|up: gate_i and up_i
 // interleaved as rows 2i and 2i + 1).
-// e4m3 phases (eb 1) are dequantised with their row scales (sa, sb, sc: the q/k/v, gate/up or single
-// matrix's tables) into the operand type (out_bf16); 16-bit phases are copied.
+// 16-bit phases are copied; e4m3 codes and NVFP4 block scale x code are written exactly in the
+// operand type (out_bf16), their row scales left to the GEMM's column scales (tc_colscale).
 cudaError_t tc_unpack(const uint8_t* image, const PhaseDesc& P, int G, int hd, int hq, int hkv, int ff, uint8_t* dst,
-                      const float* sa, const float* sb, const float* sc, int out_bf16, cudaStream_t st);
+                      int out_bf16, cudaStream_t st);
+// The column scales of phase P's GEMM (rows of its operand): out[row] = the row scale of that row
+// (sa, sb, sc: the q/k/v, gate/up or single matrix's tables).
+cudaError_t tc_colscale(const PhaseDesc& P, int rows, int hd, int hq, int hkv, int ff, const float* sa,
+                        const float* sb, const float* sc, float* out, cudaStream_t st);
 
 }  // namespace adp

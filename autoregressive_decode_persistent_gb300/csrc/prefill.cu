@@ -45,7 +45,8 @@ __device__ __forceinline__ uint16_t tc_store16(float v, int bf16) {
 template <int BF16, int MODE>
 __global__ void __launch_bounds__(128, 1)
     tc_gemm_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ W, float* C, int ldc, int m_valid,
-                   int n_valid, int k_tiles, int32_t* err, uint64_t wait_ns, const __grid_constant__ TcQkvEpi qe) {
+                   int n_valid, int k_tiles, int32_t* err, uint64_t wait_ns, const __grid_constant__ TcQkvEpi qe,
+                   const float* __restrict__ cs) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kTcStages * kTcStageBytes);
   uint64_t* empty = full + kTcStages;
@@ -142,6 +143,14 @@ __global__ void __launch_bounds__(128, 1)
           tmem_ld32(tbase + (uint32_t)(hb + ci), a);
           tmem_ld32(tbase + (uint32_t)(hb + half + ci), b);
           if (row >= m_valid) continue;
+          if (cs) {  // quantised weights: the row scale of each output column
+            const float* ca = cs + nb * kTcBN + hb + ci;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              a[j] *= __ldg(ca + j);
+              b[j] *= __ldg(ca + half + j);
+            }
+          }
           uint16_t ea[32], eb[32];
           if (head >= qe.hq + qe.hkv) {
 #pragma unroll
@@ -176,14 +185,31 @@ __global__ void __launch_bounds__(128, 1)
             const bool is_v = head >= qe.hq + qe.hkv;
             const int g = is_v ? head - qe.hq - qe.hkv : head - qe.hq;
             uint16_t* dst = (is_v ? qe.vc : qe.kc) + (((size_t)qe.L * qe.hkv + g) * qe.max_ctx + pos) * hd;
+            // and the attention's tiles, by position: K rows like the query tiles, V transposed
+            const int kb = pos / kTcBM, r = pos % kTcBM;
+            uint8_t* kbase = qe.kt + ((size_t)g * qe.n_kb + kb) * (size_t)(hd / kTcBK) * kTcABytes;
+            uint8_t* vbase = qe.vt + ((size_t)g * qe.n_kb + kb) * 2 * (size_t)hd * kTcBK * 2 +
+                             (r / kTcBK) * (size_t)hd * kTcBK * 2;
 #pragma unroll
             for (int j = 0; j < 32; j += 8) {
-              *reinterpret_cast<uint4*>(dst + ci + j) =
-                  make_uint4(ea[j] | ((uint32_t)ea[j + 1] << 16), ea[j + 2] | ((uint32_t)ea[j + 3] << 16),
-                             ea[j + 4] | ((uint32_t)ea[j + 5] << 16), ea[j + 6] | ((uint32_t)ea[j + 7] << 16));
-              *reinterpret_cast<uint4*>(dst + ci + half + j) =
-                  make_uint4(eb[j] | ((uint32_t)eb[j + 1] << 16), eb[j + 2] | ((uint32_t)eb[j + 3] << 16),
-                             eb[j + 4] | ((uint32_t)eb[j + 5] << 16), eb[j + 6] | ((uint32_t)eb[j + 7] << 16));
+              const uint4 wa = make_uint4(ea[j] | ((uint32_t)ea[j + 1] << 16), ea[j + 2] | ((uint32_t)ea[j + 3] << 16),
+                                          ea[j + 4] | ((uint32_t)ea[j + 5] << 16), ea[j + 6] | ((uint32_t)ea[j + 7] << 16));
+              const uint4 wb = make_uint4(eb[j] | ((uint32_t)eb[j + 1] << 16), eb[j + 2] | ((uint32_t)eb[j + 3] << 16),
+                                          eb[j + 4] | ((uint32_t)eb[j + 5] << 16), eb[j + 6] | ((uint32_t)eb[j + 7] << 16));
+              *reinterpret_cast<uint4*>(dst + ci + j) = wa;
+              *reinterpret_cast<uint4*>(dst + ci + half + j) = wb;
+              if (!is_v) {
+                const int ka = ci + j, kb2 = ci + half + j;
+                *reinterpret_cast<uint4*>(kbase + (ka / kTcBK) * kTcABytes + tc_tile_offset(r, ka % kTcBK)) = wa;
+                *reinterpret_cast<uint4*>(kbase + (kb2 / kTcBK) * kTcABytes + tc_tile_offset(r, kb2 % kTcBK)) = wb;
+              }
+            }
+            if (is_v) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                *reinterpret_cast<uint16_t*>(vbase + tc_tile_offset(ci + j, r % kTcBK)) = ea[j];
+                *reinterpret_cast<uint16_t*>(vbase + tc_tile_offset(ci + half + j, r % kTcBK)) = eb[j];
+              }
             }
           }
         }
@@ -194,6 +220,10 @@ __global__ void __launch_bounds__(128, 1)
       float v[32];
       tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(hh * kTcBN + c0), v);
       const int col0 = nb * kTcBN + c0;
+      if (cs) {  // quantised weights: the row scale of each output column (columns past N read 0)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= col0 + j < n_valid ? __ldg(cs + col0 + j) : 0.0f;
+      }
       if (MODE == TC_SWIGLU) {
         // 16 (gate, up) pairs -> h = silu(g) u, two 16-byte runs of the next GEMM's A tile row
         const int i0 = col0 / 2, ffw = n_valid / 2;
@@ -280,7 +310,8 @@ cudaError_t tc_tile(const uint16_t* src, int rows, int K, int ld, uint8_t* dst, 
 }
 
 cudaError_t tc_gemm(int bf16, int mode, const uint8_t* A_tiled, const uint8_t* W_tiled, float* C, int ldc, int M,
-                    int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st, const TcQkvEpi* qkv) {
+                    int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st, const TcQkvEpi* qkv,
+                    const float* colscale) {
   const int k_tiles = (K + kTcBK - 1) / kTcBK;
   const dim3 grid((M + kTcHalves * kTcBM - 1) / (kTcHalves * kTcBM), (N + kTcBN - 1) / kTcBN);
   const void* kernels[2][4] = {
@@ -297,7 +328,7 @@ cudaError_t tc_gemm(int bf16, int mode, const uint8_t* A_tiled, const uint8_t* W
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
   if (e != cudaSuccess) return e;
   void* args[] = {(void*)&A_tiled, (void*)&W_tiled, (void*)&C,   (void*)&ldc,     (void*)&M, (void*)&N,
-                  (void*)&k_tiles, (void*)&err,    (void*)&wait_ns, (void*)&qe};
+                  (void*)&k_tiles, (void*)&err,    (void*)&wait_ns, (void*)&qe, (void*)&colscale};
   return cudaLaunchKernel(k, grid, dim3(128), args, kTcSmem, st);
 }
 
@@ -350,11 +381,11 @@ __device__ __forceinline__ float tc_row_scale(const PhaseDesc& P, int row, int h
 
 // The decode image's tiles of phase P back into one tiled GEMM operand (256-row tiles): the
 // inverse of the repack, walked the same way (CTA c's units, rounds, K-chunks).  16-bit weights
-// are copied as they are; e4m3 weights become scale x code and NVFP4 weights row scale x (block
-// scale x code) (fp32, then RNE to the operand type).
+// are copied as they are; e4m3 weights become their codes and NVFP4 weights block scale x code,
+// both exact in either 16-bit type (4 and 2 + 4 significant bits); the row scales are applied to
+// the GEMM's output columns instead (tc_colscale_kernel), so the operand carries no rounding.
 __global__ void tc_unpack_kernel(const uint8_t* __restrict__ image, PhaseDesc P, uint8_t* dst, int k_tiles, int hd,
-                                 int hq, int hkv, int ff, const float* sa, const float* sb, const float* sc,
-                                 int out_bf16) {
+                                 int hq, int hkv, int ff, int out_bf16) {
   const uint32_t c = blockIdx.x, G = gridDim.x;
   const long long a0 = (long long)c * P.n_units / G, a1 = (long long)(c + 1) * P.n_units / G;
   const int u0 = (int)a0, n = (int)(a1 - a0);
@@ -392,10 +423,9 @@ __global__ void tc_unpack_kernel(const uint8_t* __restrict__ image, PhaseDesc P,
       } else {
         load8<DT_E4M3>(src_cta + off, w);
       }
-      const float s = tc_row_scale(P, row, hd, hq, hkv, ff, sa, sb, sc);
       uint16_t e[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) e[k] = tc_store16(s * w[k], out_bf16);
+      for (int k = 0; k < 8; ++k) e[k] = tc_store16(w[k], out_bf16);  // exact
       v = make_uint4(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16), e[4] | ((uint32_t)e[5] << 16),
                      e[6] | ((uint32_t)e[7] << 16));
     }
@@ -404,9 +434,23 @@ __global__ void tc_unpack_kernel(const uint8_t* __restrict__ image, PhaseDesc P,
 }
 
 cudaError_t tc_unpack(const uint8_t* image, const PhaseDesc& P, int G, int hd, int hq, int hkv, int ff, uint8_t* dst,
-                      const float* sa, const float* sb, const float* sc, int out_bf16, cudaStream_t st) {
+                      int out_bf16, cudaStream_t st) {
   const int k_tiles = (P.K + kTcBK - 1) / kTcBK;
-  tc_unpack_kernel<<<G, 256, 0, st>>>(image, P, dst, k_tiles, hd, hq, hkv, ff, sa, sb, sc, out_bf16);
+  tc_unpack_kernel<<<G, 256, 0, st>>>(image, P, dst, k_tiles, hd, hq, hkv, ff, out_bf16);
+  return cudaGetLastError();
+}
+
+// out[row] = the row scale of logical row `row` of phase P's GEMM operand (e4m3 and NVFP4 layer
+// matrices: the q, k, v; gate, up; or single matrix's table), for rows [0, rows).
+__global__ void tc_colscale_kernel(PhaseDesc P, int rows, int hd, int hq, int hkv, int ff, const float* sa,
+                                   const float* sb, const float* sc, float* out) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row < rows) out[row] = tc_row_scale(P, row, hd, hq, hkv, ff, sa, sb, sc);
+}
+
+cudaError_t tc_colscale(const PhaseDesc& P, int rows, int hd, int hq, int hkv, int ff, const float* sa,
+                        const float* sb, const float* sc, float* out, cudaStream_t st) {
+  tc_colscale_kernel<<<(rows + 255) / 256, 256, 0, st>>>(P, rows, hd, hq, hkv, ff, sa, sb, sc, out);
   return cudaGetLastError();
 }
 
@@ -456,22 +500,24 @@ cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st) {
                                                    kt_d);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // QKV with RoPE and the cache writes in the epilogue; queries into the attention's tiles
-    const TcQkvEpi qe{a.rope_cos, a.rope_sin, a.kc, a.vc, a.Qt, a.pos0, L, a.hq, a.hkv, a.hd, a.max_ctx, a.kvdt,
-                      (P + kTcBM - 1) / kTcBM};
-    if ((e = tc_gemm(a.bf16, TC_QKV, a.A, a.wqkv[L], nullptr, 0, P, qkv_n, a.d, a.err, a.wait_ns, st, &qe)) !=
-        cudaSuccess)
+    const TcQkvEpi qe{a.rope_cos, a.rope_sin, a.kc,   a.vc,     a.Qt,      a.Kt,  a.Vt,   a.pos0,
+                      L,          a.hq,       a.hkv, a.hd, a.max_ctx, a.kvdt, (P + kTcBM - 1) / kTcBM, a.n_kb};
+    if ((e = tc_gemm(a.bf16, TC_QKV, a.A, a.wqkv[L], nullptr, 0, P, qkv_n, a.d, a.err, a.wait_ns, st, &qe,
+                     a.sqkv ? a.sqkv[L] : nullptr)) != cudaSuccess)
       return e;
     if ((e = tc_flash(a, qkv_n, L, kt_att, st)) != cudaSuccess) return e;
-    if ((e = tc_gemm(a.bf16, TC_ADD, a.A, a.wo[L], a.x, a.d, P, a.d, a.hq * a.hd, a.err, a.wait_ns, st)) != cudaSuccess)
+    if ((e = tc_gemm(a.bf16, TC_ADD, a.A, a.wo[L], a.x, a.d, P, a.d, a.hq * a.hd, a.err, a.wait_ns, st, nullptr,
+                     a.swo ? a.swo[L] : nullptr)) != cudaSuccess)
       return e;
     tc_rmsnorm_kernel<<<(P + 7) / 8, 256, 0, st>>>(a.x, (const uint16_t*)a.ffn_norm[L], P, a.d, a.eps, a.bf16, a.A,
                                                    kt_d);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // gate|up with SwiGLU in the epilogue: h goes straight into the down GEMM's A tiles (A2)
     if ((e = tc_gemm(a.bf16, TC_SWIGLU, a.A, a.wgu[L], reinterpret_cast<float*>(a.A2), kt_ff, P, 2 * a.ff, a.d,
-                     a.err, a.wait_ns, st)) != cudaSuccess)
+                     a.err, a.wait_ns, st, nullptr, a.sgu ? a.sgu[L] : nullptr)) != cudaSuccess)
       return e;
-    if ((e = tc_gemm(a.bf16, TC_ADD, a.A2, a.wdown[L], a.x, a.d, P, a.d, a.ff, a.err, a.wait_ns, st)) != cudaSuccess)
+    if ((e = tc_gemm(a.bf16, TC_ADD, a.A2, a.wdown[L], a.x, a.d, P, a.d, a.ff, a.err, a.wait_ns, st, nullptr,
+                     a.sdown ? a.sdown[L] : nullptr)) != cudaSuccess)
       return e;
   }
   return cudaSuccess;
@@ -481,219 +527,352 @@ cudaError_t tc_prefill(const TcPrefill& a, cudaStream_t st) {
 
 namespace adp {
 
-// Causal attention of the prompt on the tensor cores, flash style.  CTA = query head h x 128
-// consecutive prompt tokens (thread t = token t0 + t = TMEM lane t), 128 threads; its queries come
-// ready in the core-matrix layout from the QKV GEMM's epilogue.  Per block of
-// 128 cached keys: the K block and the V block (transposed) are staged in shared memory in the
-// K-major core-matrix layout; S = Q K^T (128 x 128, K = head_dim) accumulates in TMEM columns
-// [0, 128); each thread turns its row of S into the online softmax (scale, causal mask, running
-// max m and sum l in fp32, the block's probabilities rounded to the KV type into the P tile) and
-// rescales its row of O (TMEM columns [128, 128 + head_dim)) by exp(m_old - m_new); then
-// O += P V (K = 128 keys).  At the end O / l is rounded into the A-operand tiles of Wo.
+// Key and value rows of positions [0, npos) of layer L from the cache into the attention's tiles
+// (the rows a prefill after a cached prefix attends to but does not compute): K as 128-key blocks of
+// hd/64 tiles of 128 x 64 (the query tiles' layout), V transposed, as blocks of two hd x 64-key
+// tiles.  One thread per (KV head, position, 8-element chunk).
+__global__ void tc_kv_tile_kernel(const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc, int L, int hkv,
+                                  int max_ctx, int hd, int npos, int n_kb, uint8_t* kt, uint8_t* vt) {
+  const int nch = hd / 8;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)hkv * npos * nch) return;
+  const int ch = (int)(i % nch), pos = (int)((i / nch) % npos), g = (int)(i / ((long long)nch * npos));
+  const size_t row = (((size_t)L * hkv + g) * max_ctx + pos) * hd + ch * 8;
+  const uint4 k8 = __ldg(reinterpret_cast<const uint4*>(kc + row));
+  const uint4 v8 = __ldg(reinterpret_cast<const uint4*>(vc + row));
+  const int kb = pos / kTcBM, r = pos % kTcBM, k = ch * 8;
+  uint8_t* kbase = kt + ((size_t)g * n_kb + kb) * (size_t)(hd / kTcBK) * kTcABytes;
+  *reinterpret_cast<uint4*>(kbase + (k / kTcBK) * kTcABytes + tc_tile_offset(r, k % kTcBK)) = k8;
+  uint8_t* vbase = vt + ((size_t)g * n_kb + kb) * 2 * (size_t)hd * kTcBK * 2 + (r / kTcBK) * (size_t)hd * kTcBK * 2;
+  const uint32_t w4[4] = {v8.x, v8.y, v8.z, v8.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<uint16_t*>(vbase + tc_tile_offset(k + j, r % kTcBK)) = (uint16_t)(w4[j >> 1] >> ((j & 1) * 16));
+}
+
+// Causal attention of the prompt on the tensor cores, flash style, as a warp-specialised pipeline.
+// CTA = query head h x 128 consecutive prompt tokens, 192 threads, two CTAs per SM:
+//  - warps 0-3: the softmax, thread t = query row t = TMEM lane t;
+//  - warp 4 (one thread): bulk copies of the query tiles and of each 64-key block (its halves of
+//    the K tiles and its transposed V tile, laid out by the QKV GEMM's epilogue) into a two-stage
+//    ring;
+//  - warp 5 (one thread): the MMAs.  S_j = Q K_j^T (128 x 64) goes into one of two TMEM buffers
+//    (columns [0, 64) and [64, 128)), so S_{j+1} is computed while the softmax works on S_j;
+//    O += P_j V_j accumulates in columns [128, 128 + head_dim).
+// The softmax keeps a running maximum m (base-2 exponent units) and sum l per row in fp32 and
+// writes the block's probabilities exp2(s log2(e) scale - m), rounded to the KV type, into the P
+// tile in shared memory.  A larger block maximum replaces m only when it exceeds m by more than 8
+// (decided per warp): until then the probabilities stay below 2^8, the same m scales l and O, so
+// the result O / l is unchanged, and O in TMEM is rescaled only on those blocks.  At the end O / l
+// is rounded into the A-operand tiles of Wo.
+constexpr int kFlashBK = 64;  // keys per block
+
+// 2^x by the hardware's approximate base-2 exponential (results below 2^-126 flush to zero, which
+// a probability may).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two probabilities rounded (RNE) to the KV type, packed low | high << 16.
+template <int BF16>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
+  if constexpr (BF16) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
 template <int HD, int KVDT>
-__global__ void __launch_bounds__(128) tc_flash_kernel(const uint8_t* __restrict__ qt, int n_tb, int P, int pos0, int L,
-                                                      int hq, int hkv, int max_ctx, float scale,
-                                                      const uint16_t* __restrict__ kc,
-                                                      const uint16_t* __restrict__ vc, int out_bf16, uint8_t* A,
-                                                      int k_tiles, int32_t* err, uint64_t wait_ns) {
-  constexpr int KT = HD / kTcBK;                        // 64-wide K tiles of Q and K
-  constexpr uint32_t QK_TILE = 128 * kTcBK * 2;         // 16 KB: 128 rows x 64
-  constexpr uint32_t VT_TILE = HD * kTcBK * 2;          // V^T tile: head_dim rows x 64 keys
+__global__ void __launch_bounds__(192, 2)
+    tc_flash_kernel(const uint8_t* __restrict__ qt, int n_tb, const uint8_t* __restrict__ kt,
+                    const uint8_t* __restrict__ vt, int n_kb, int P, int pos0, int hq, int hkv, float scale_log2,
+                    int out_bf16, uint8_t* A, int k_tiles, int32_t* err, uint64_t wait_ns) {
+  constexpr int KT = HD / kTcBK;                    // 64-wide K tiles of Q and K
+  constexpr int BK = kFlashBK;
+  constexpr uint32_t QK_TILE = 128 * kTcBK * 2;     // 16 KB: 128 rows x 64 (a query tile; a global K tile)
+  constexpr uint32_t QBLK = KT * QK_TILE;
+  constexpr uint32_t KH_TILE = BK * kTcBK * 2;      // 8 KB: 64 keys x 64 (half of a global K tile)
+  constexpr uint32_t KBLK = KT * KH_TILE;           // a K block: 64 keys x head_dim
+  constexpr uint32_t VT_TILE = HD * kTcBK * 2;      // a V^T block: head_dim rows x 64 keys
+  constexpr uint32_t STAGE = KBLK + VT_TILE;
+  constexpr uint32_t P_TILE = 128 * BK * 2;         // 16 KB: 128 queries x 64 keys
   constexpr int KV_BF16 = KVDT == DT_BF16 ? 1 : 0;
+  constexpr float kRescale = 8.0f;                  // base-2 growth of the maximum that forces a rescale
+  constexpr uint32_t kCols = 256;                   // TMEM: S0, S1 (64 columns each), O (head_dim <= 128)
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* Qs = smem;                                   // KT tiles
-  uint8_t* Ks = Qs + KT * QK_TILE;                      // max(KT, 2) tiles
-  uint8_t* Ps = Ks;                                     // P reuses the K block once S is computed
-  uint8_t* Vt = Ks + (KT > 2 ? KT : 2) * QK_TILE;       // 2 tiles (keys 0..63, 64..127)
-  uint64_t* bar = reinterpret_cast<uint64_t*>(Vt + 2 * VT_TILE);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  uint8_t* Qs = smem;
+  uint8_t* ring = Qs + QBLK;                        // 2 stages: K block, then V^T block
+  uint8_t* Ps = ring + 2 * STAGE;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(Ps + P_TILE);
+  uint64_t* qfull = bar;
+  uint64_t* kvfull = bar + 1;                       // [2]
+  uint64_t* kvempty = bar + 3;                      // [2]
+  uint64_t* sfull = bar + 5;                        // [2]
+  uint64_t* pready = bar + 7;
+  uint64_t* odone = bar + 8;
+  uint64_t* done = bar + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 10);
+  int32_t* abort_flag = reinterpret_cast<int32_t*>(tmem_slot + 1);
   // the longest causal rows (last query blocks) start first
-  const int h = blockIdx.x, t0 = (gridDim.y - 1 - blockIdx.y) * 128;
-  const int t = threadIdx.x, warp = t >> 5;
+  const int h = blockIdx.x, qb = gridDim.y - 1 - blockIdx.y, t0 = qb * 128;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int g = h * hkv / hq;
+  const int kmax = pos0 + min(t0 + 127, P - 1);    // the tile's last key position
+  const int nkb = kmax / BK + 1;                    // key blocks 0 .. kmax / 64
   if (t == 0) {
-    mbar_init(bar, 1);
+    mbar_init(qfull, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&kvfull[s], 1);
+      mbar_init(&kvempty[s], 1);
+      mbar_init(&sfull[s], 1);
+    }
+    mbar_init(pready, 128);
+    mbar_init(odone, 1);
+    mbar_init(done, 1);
+    *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 0) {
-    tmem_alloc(tmem_slot, 256);
+  if (warp == 4) {
+    tmem_alloc(tmem_slot, kCols);
     tmem_relinquish();
-  }
-  // the query tiles of (head h, tokens t0 ..), written by the QKV GEMM's epilogue (post-RoPE, KV type)
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(qt + ((size_t)h * n_tb + t0 / 128) * KT * QK_TILE);
-    uint4* dst = reinterpret_cast<uint4*>(Qs);
-#pragma unroll 4
-    for (int i = t; i < KT * (int)QK_TILE / 16; i += 128) dst[i] = __ldg(src + i);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t tS = tmem + lane_base, tO = tmem + lane_base + 128;
-  const int pos = pos0 + min(t0 + t, P - 1);            // this row's position (padding rows: the last)
-  const int kmax = pos0 + min(t0 + 127, P - 1);
-  const size_t head0 = ((size_t)L * hkv + g) * max_ctx;
-  constexpr uint32_t idS = tc_idesc_f16(KV_BF16, 128, 128);
-  constexpr uint32_t idO = tc_idesc_f16(KV_BF16, 128, HD);
-  float m = -INFINITY, l = 0.0f;
-  uint32_t phase = 0;
-  bool ok = true;
+  volatile int32_t* ab = abort_flag;
   int32_t never = 0;
-  // this thread's key row of the block at kb: K and V, 16-byte chunks (zero past kmax)
-  constexpr int NC = HD / 8;
-  uint4 kreg[NC], vreg[NC];
-  auto load_rows = [&](int kb) {
-    const int kp = kb + t;
-    const bool in = kp <= kmax;
-    const uint4* kr = reinterpret_cast<const uint4*>(kc + (head0 + (in ? kp : 0)) * HD);
-    const uint4* vr = reinterpret_cast<const uint4*>(vc + (head0 + (in ? kp : 0)) * HD);
+  if (warp == 4) {
+    if (lane == 0) {
+      // producer: the query tiles once, then key block j into stage j % 2 when the MMAs of block
+      // j - 2 have released it.  Block j is half j % 2 of 128-key block j / 2 in global memory: the
+      // first or last 8 KB of each of its K tiles (8-row groups are 1 KB apart) and one V^T tile.
+      const uint64_t pol_q = policy_evict_first();
+      const uint64_t pol_kv = policy_evict_last();  // every query tile of the KV group reads them
+      mbar_arrive_expect_tx(qfull, QBLK);
+      tma_load_1d(Qs, qt + ((size_t)h * n_tb + qb) * QBLK, QBLK, qfull, pol_q);
+      int issued = 0;
+      for (int j = 0; j < nkb; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(&kvempty[s], ((j >> 1) - 1) & 1, ab, wait_ns)) {
+          *ab = 1;
+          break;
+        }
+        uint8_t* dst = ring + s * STAGE;
+        const size_t blk = (size_t)g * n_kb + (j >> 1);
+        mbar_arrive_expect_tx(&kvfull[s], STAGE);
 #pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      kreg[c] = in ? __ldg(kr + c) : make_uint4(0, 0, 0, 0);
-      vreg[c] = in ? __ldg(vr + c) : make_uint4(0, 0, 0, 0);
-    }
-  };
-  load_rows(0);
-  for (int kb0 = 0; kb0 <= kmax && ok; kb0 += 128) {
-    // ---- stage key rows kb0 + t (held in registers since the previous block): K as a B operand
-    // (keys x head_dim), V transposed (head_dim x keys); then start loading the next block's rows,
-    // which arrive while this block's MMAs and softmax run
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      const int k = c * 8;
-      *reinterpret_cast<uint4*>(Ks + (k / kTcBK) * QK_TILE + tc_tile_offset(t, k % kTcBK)) = kreg[c];
-      const uint32_t w4[4] = {vreg[c].x, vreg[c].y, vreg[c].z, vreg[c].w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint16_t e = (uint16_t)(w4[j >> 1] >> ((j & 1) * 16));
-        *reinterpret_cast<uint16_t*>(Vt + (t / kTcBK) * VT_TILE + tc_tile_offset(k + j, t % kTcBK)) = e;
+        for (int q = 0; q < KT; ++q)
+          tma_load_1d(dst + q * KH_TILE, kt + (blk * KT + q) * QK_TILE + (j & 1) * KH_TILE, KH_TILE, &kvfull[s],
+                      pol_kv);
+        tma_load_1d(dst + KBLK, vt + blk * 2 * VT_TILE + (j & 1) * VT_TILE, VT_TILE, &kvfull[s], pol_kv);
+        issued = j + 1;
       }
-    }
-    load_rows(kb0 + 128);
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // ---- S = Q K^T
-    if (t == 0) {
-#pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        const uint32_t off = (kk / 4) * QK_TILE + (kk % 4) * 256;
-        tc_mma_f16(tmem, tc_smem_desc(smem_u32(Qs) + off, 128, 1024), tc_smem_desc(smem_u32(Ks) + off, 128, 1024),
-                   idS, kk > 0);
-      }
-      tc_commit(bar);
+      // no bulk copy may still be writing this CTA's shared memory when it exits
+      mbar_wait(qfull, 0, &never, wait_ns);
+      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j) mbar_wait(&kvfull[j & 1], (j >> 1) & 1, &never, wait_ns);
     }
     __syncwarp();
-    ok = mbar_wait(bar, phase, &never, wait_ns);
-    phase ^= 1u;
-    tc_fence_after();
-    // ---- online softmax of row t (its probabilities overwrite the K block, which S no longer needs)
-    float mb = -INFINITY;
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t idS = tc_idesc_f16(KV_BF16, 128, BK);
+      constexpr uint32_t idO = tc_idesc_f16(KV_BF16, 128, HD);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j & 1;
+        if (!mbar_wait(&kvfull[s], (j >> 1) & 1, ab, wait_ns)) return false;
+        tc_fence_after();
+        const uint32_t q0 = smem_u32(Qs), k0 = smem_u32(ring + s * STAGE);
 #pragma unroll
-    for (int c0 = 0; c0 < 128; c0 += 32) {
-      float v[32];
-      tmem_ld32(tS + c0, v);
+        for (int kk = 0; kk < HD / 16; ++kk)
+          tc_mma_f16(tmem + (uint32_t)(s * BK), tc_smem_desc(q0 + (kk / 4) * QK_TILE + (kk % 4) * 256, 128, 1024),
+                     tc_smem_desc(k0 + (kk / 4) * KH_TILE + (kk % 4) * 256, 128, 1024), idS, kk > 0);
+        tc_commit(&sfull[s]);
+        return true;
+      };
+      bool ok = mbar_wait(qfull, 0, ab, wait_ns) && issue_s(0);
+      for (int j = 0; ok && j < nkb; ++j) {
+        // S_{j+1} into the other buffer (the softmax of block j - 1 has released it), then O += P_j V_j
+        if (j + 1 < nkb && !issue_s(j + 1)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(pready, j & 1, ab, wait_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t p0 = smem_u32(Ps), v0 = smem_u32(ring + (j & 1) * STAGE + KBLK);
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (kb0 + c0 + j <= pos) mb = fmaxf(mb, v[j] * scale);
+        for (int kk = 0; kk < BK / 16; ++kk)
+          tc_mma_f16(tmem + 2 * BK, tc_smem_desc(p0 + kk * 256, 128, 1024), tc_smem_desc(v0 + kk * 256, 128, 1024), idO,
+                     j > 0 || kk > 0);
+        tc_commit(odone);
+        tc_commit(&kvempty[j & 1]);
+      }
+      if (!ok) *ab = 1;
+      tc_commit(done);  // on every path: arrives once no MMA of this CTA is in flight
     }
-    // exponentials by CUDA's fast intrinsic (ex2-based; this path is checked within tolerances)
-    const float mn = fmaxf(m, mb);
-    const float corr = __expf(m - mn);
-    float ps = 0.0f;
+    __syncwarp();
+  } else {
+    // ---- softmax warps
+    const int qpos = pos0 + min(t0 + t, P - 1);     // this row's position (padding rows: the last)
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t tO = tmem + lane_base + 2 * BK;
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    // every wait's outcome is made warp-uniform: the TMEM loads and stores are warp-collective
+    auto wait_all = [&](uint64_t* b, uint32_t parity) {
+      return __all_sync(0xFFFFFFFFu, mbar_wait(b, parity, ab, wait_ns));
+    };
+    for (int j = 0; j < nkb; ++j) {
+      const int s = j & 1;
+      if (!wait_all(&sfull[s], (j >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float v[BK];
+      tmem_ld64(tmem + lane_base + (uint32_t)(s * BK), v);
+      const int lim = qpos - j * BK;                // keys c <= lim of this block are visible to the row
+      const bool full = lim >= BK - 1;
+      // (eight independent partial maxima and sums: no long dependent chains)
+      float mq[8];
 #pragma unroll
-    for (int c0 = 0; c0 < 128; c0 += 32) {
-      float v[32];
-      tmem_ld32(tS + c0, v);
-      uint16_t e[32];
+      for (int q = 0; q < 8; ++q) mq[q] = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float p = kb0 + c0 + j <= pos ? __expf(v[j] * scale - mn) : 0.0f;
-        ps += p;
-        e[j] = tc_store16(p, KV_BF16);
+        for (int c = 0; c < BK; ++c) mq[c & 7] = fmaxf(mq[c & 7], v[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < BK; ++c) mq[c & 7] = c <= lim ? fmaxf(mq[c & 7], v[c]) : mq[c & 7];
+      }
+      const float mb = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])), fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
+      const float mbs = mb * scale_log2;
+      const bool grow = mbs > m + kRescale || (m == -INFINITY && mbs > -INFINITY);
+      const bool rescale = __any_sync(0xFFFFFFFFu, grow);
+      float corr = 1.0f;
+      if (rescale) {
+        const float mn = fmaxf(m, mbs);
+        corr = m == -INFINITY ? 0.0f : ex2_approx(m - mn);
+        m = mn;
+      }
+      // probabilities of the block, rounded to the KV type, two per 32-bit word
+      uint32_t pw[BK / 2];
+      float sq[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sq[q] = 0.0f;
+#pragma unroll
+      for (int c = 0; c < BK; c += 2) {
+        float p0 = ex2_approx(fmaf(v[c], scale_log2, -m)), p1 = ex2_approx(fmaf(v[c + 1], scale_log2, -m));
+        if (!full) {
+          p0 = c <= lim ? p0 : 0.0f;
+          p1 = c + 1 <= lim ? p1 : 0.0f;
+        }
+        sq[(c >> 1) & 7] += p0 + p1;
+        pw[c / 2] = pack16x2<KV_BF16>(p0, p1);
+      }
+      const float ps = ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));
+      l = l * corr + ps;
+      // P_{j-1} V_{j-1} must have completed before P is overwritten and O rescaled
+      if (j > 0) {
+        if (!wait_all(odone, (j - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (rescale) {
+#pragma unroll
+          for (int c0 = 0; c0 < HD; c0 += 32) {
+            float o[32];
+            tmem_ld32(tO + c0, o);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] *= corr;
+            tmem_st32(tO + c0, o);
+          }
+        }
       }
 #pragma unroll
-      for (int j = 0; j < 32; j += 8)
-        *reinterpret_cast<uint4*>(Ps + ((c0 + j) / kTcBK) * QK_TILE + tc_tile_offset(t, (c0 + j) % kTcBK)) =
-            make_uint4(e[j] | ((uint32_t)e[j + 1] << 16), e[j + 2] | ((uint32_t)e[j + 3] << 16),
-                       e[j + 4] | ((uint32_t)e[j + 5] << 16), e[j + 6] | ((uint32_t)e[j + 7] << 16));
+      for (int c = 0; c < BK; c += 8)
+        *reinterpret_cast<uint4*>(Ps + tc_tile_offset(t, c)) = make_uint4(pw[c / 2], pw[c / 2 + 1], pw[c / 2 + 2], pw[c / 2 + 3]);
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(pready);
     }
-    l = l * corr + ps;
-    m = mn;
-    if (kb0 > 0) {  // O *= exp(m_old - m_new) before this block's products are added
+    // ---- O / l into the Wo GEMM's A tiles
+    if (ok) ok = wait_all(odone, (nkb - 1) & 1);
+    tc_fence_after();
+    const int tok = t0 + t;
+    if (ok) {
+      const float inv = 1.0f / l;
 #pragma unroll
       for (int c0 = 0; c0 < HD; c0 += 32) {
-        float v[32];
-        tmem_ld32(tO + c0, v);
+        float o[32];
+        tmem_ld32(tO + c0, o);
+        if (tok < P) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] *= corr;
-        tmem_st32(tO + c0, v);
-      }
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // ---- O += P V
-    if (t == 0) {
+          for (int q = 0; q < 32; q += 8) {
+            uint32_t w[4];
 #pragma unroll
-      for (int kk = 0; kk < 128 / 16; ++kk) {
-        const uint32_t pa = smem_u32(Ps) + (kk / 4) * QK_TILE + (kk % 4) * 256;
-        const uint32_t vb = smem_u32(Vt) + (kk / 4) * VT_TILE + (kk % 4) * 256;
-        tc_mma_f16(tmem + 128, tc_smem_desc(pa, 128, 1024), tc_smem_desc(vb, 128, 1024), idO, kb0 > 0 || kk > 0);
+            for (int e = 0; e < 4; ++e)
+              w[e] = (uint32_t)tc_store16(o[q + 2 * e] * inv, out_bf16) |
+                     ((uint32_t)tc_store16(o[q + 2 * e + 1] * inv, out_bf16) << 16);
+            *reinterpret_cast<uint4*>(A + tc_a_offset(tok, h * HD + c0 + q, k_tiles)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
       }
-      tc_commit(bar);
+    } else {
+      *ab = 1;
+      if (t == 0) atomicCAS(err, 0, DE_PIPELINE_TIMEOUT);
     }
-    __syncwarp();
-    ok = mbar_wait(bar, phase, &never, wait_ns) && ok;
-    phase ^= 1u;
-    tc_fence_after();
   }
-  // ---- O / l into the Wo GEMM's A tiles
-  const int tok = t0 + t;
-  if (ok) {
-    const float inv = 1.0f / l;
-#pragma unroll
-    for (int c0 = 0; c0 < HD; c0 += 32) {
-      float v[32];
-      tmem_ld32(tO + c0, v);
-      if (tok < P) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          *reinterpret_cast<uint16_t*>(A + tc_a_offset(tok, h * HD + c0 + j, k_tiles)) =
-              tc_store16(v[j] * inv, out_bf16);
-      }
-    }
-  } else if (t == 0) {
-    atomicCAS(err, 0, DE_PIPELINE_TIMEOUT);
-  }
+  // no MMA may be in flight (nor TMEM in use) when the accumulators are freed
+  mbar_wait(done, 0, &never, wait_ns);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  tc_fence_after();
+  if (warp == 4) tmem_dealloc(tmem, kCols);
+}
+
+template <int HD>
+constexpr size_t tc_flash_smem() {
+  // query tiles + two ring stages (K block, V^T block) + the P tile + barriers; at least 80 KB, so
+  // that at most two CTAs (256 TMEM columns each) run per SM
+  constexpr size_t q = (size_t)(HD / kTcBK) * 128 * kTcBK * 2;
+  constexpr size_t stage = (size_t)(HD / kTcBK) * kFlashBK * kTcBK * 2 + (size_t)HD * kTcBK * 2;
+  constexpr size_t need = q + 2 * stage + 128 * kFlashBK * 2 + 128;
+  return need > 80 * 1024 ? need : 80 * 1024;
 }
 
 template <int HD, int KVDT>
-cudaError_t tc_flash_launch(const TcPrefill& a, int qkv_n, int L, int kt_att, cudaStream_t st) {
-  constexpr int KT = HD / kTcBK;
-  constexpr size_t smem = (size_t)(KT + (KT > 2 ? KT : 2)) * 128 * kTcBK * 2 + 2 * (size_t)HD * kTcBK * 2 + 64;
+cudaError_t tc_flash_launch(const TcPrefill& a, int kt_att, cudaStream_t st) {
+  constexpr size_t smem = tc_flash_smem<HD>();
   const void* k = (const void*)tc_flash_kernel<HD, KVDT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  tc_flash_kernel<HD, KVDT><<<dim3(a.hq, (a.P + 127) / 128), 128, smem, st>>>(
-      a.Qt, (a.P + 127) / 128, a.P, a.pos0, L, a.hq, a.hkv, a.max_ctx, a.scale, a.kc, a.vc, a.bf16, a.A, kt_att,
-      a.err, a.wait_ns);
+  tc_flash_kernel<HD, KVDT><<<dim3(a.hq, (a.P + 127) / 128), 192, smem, st>>>(
+      a.Qt, (a.P + 127) / 128, a.Kt, a.Vt, a.n_kb, a.P, a.pos0, a.hq, a.hkv, a.scale * 1.4426950408889634f, a.bf16,
+      a.A, kt_att, a.err, a.wait_ns);
   return cudaGetLastError();
 }
 
 cudaError_t tc_flash(const TcPrefill& a, int qkv_n, int L, int kt_att, cudaStream_t st) {
+  (void)qkv_n;
+  if (a.pos0 > 0) {
+    // the cached prefix's rows into the attention's tiles (the QKV epilogue writes the prompt's)
+    const long long n = (long long)a.hkv * a.pos0 * (a.hd / 8);
+    tc_kv_tile_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a.kc, a.vc, L, a.hkv, a.max_ctx, a.hd, a.pos0,
+                                                                    a.n_kb, a.Kt, a.Vt);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   if (a.kvdt == DT_BF16)
-    return a.hd == 128 ? tc_flash_launch<128, DT_BF16>(a, qkv_n, L, kt_att, st)
-                       : tc_flash_launch<64, DT_BF16>(a, qkv_n, L, kt_att, st);
-  return a.hd == 128 ? tc_flash_launch<128, DT_F16>(a, qkv_n, L, kt_att, st)
-                     : tc_flash_launch<64, DT_F16>(a, qkv_n, L, kt_att, st);
+    return a.hd == 128 ? tc_flash_launch<128, DT_BF16>(a, kt_att, st) : tc_flash_launch<64, DT_BF16>(a, kt_att, st);
+  return a.hd == 128 ? tc_flash_launch<128, DT_F16>(a, kt_att, st) : tc_flash_launch<64, DT_F16>(a, kt_att, st);
 }
 
 }  // namespace adp

@@ -97,6 +97,51 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 128 consecutive fp32 columns of this thread's TMEM lane: four loads in flight, one wait (which
+// names every loaded register, so no use of them is scheduled before it).
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+#define ADP_R8(b) "+r"(r[b]), "+r"(r[b + 1]), "+r"(r[b + 2]), "+r"(r[b + 3]), "+r"(r[b + 4]), "+r"(r[b + 5]), \
+                  "+r"(r[b + 6]), "+r"(r[b + 7])
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+  uint32_t r[128];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) tmem_ld32_issue(taddr + 32 * q, r + 32 * q);
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : ADP_R8(0), ADP_R8(8), ADP_R8(16), ADP_R8(24), ADP_R8(32), ADP_R8(40), ADP_R8(48), ADP_R8(56),
+                 ADP_R8(64), ADP_R8(72), ADP_R8(80), ADP_R8(88), ADP_R8(96), ADP_R8(104), ADP_R8(112), ADP_R8(120)
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+#undef ADP_R8
+
+// 64 consecutive fp32 columns of this thread's TMEM lane: two loads in flight, one wait.
+#define ADP_R8(b) "+r"(r[b]), "+r"(r[b + 1]), "+r"(r[b + 2]), "+r"(r[b + 3]), "+r"(r[b + 4]), "+r"(r[b + 5]), \
+                  "+r"(r[b + 6]), "+r"(r[b + 7])
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  tmem_ld32_issue(taddr, r);
+  tmem_ld32_issue(taddr + 32, r + 32);
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : ADP_R8(0), ADP_R8(8), ADP_R8(16), ADP_R8(24), ADP_R8(32), ADP_R8(40), ADP_R8(48), ADP_R8(56)
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+#undef ADP_R8
+
 // Store 32 consecutive fp32 columns of this thread's TMEM lane (waits until the store is done).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   uint32_t r[32];

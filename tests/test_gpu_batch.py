@@ -93,7 +93,8 @@ def test_tiny_batch_mixes_greedy_and_sampled_requests(torch_cuda):
     _check_batch(synth.get_config("tiny"), [9, 30, 3], 16, temperatures=[0.7, 0.0, 0.7])
 
 
-@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "dense-2.3b-e4m3"])
+@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-8b-bf16", "dense-2.3b-e4m3", "dense-2.3b-nvfp4",
+                                  "dense-8b-nvfp4"])
 def test_shrunk_workloads_batch_bit_exact(torch_cuda, name):
     cfg = synth.shrink(synth.get_config(name))
     _check_batch(cfg, [8, 35], 10)
@@ -205,8 +206,5 @@ def test_batch_rejections(torch_cuda):
     with pytest.raises(adp.AdpError) as e:
         m3.step_batch([m3.new_kv()], [1])
     assert e.value.code == adp.ADP_ERR_UNSUPPORTED_CONFIG
-    q4 = synth.shrink(synth.get_config("dense-2.3b-nvfp4"))
-    m4 = _model(q4, synth.model_weights(q4))
-    assert m4.max_batch == 0
-    for m in (model, m2, m3, m4):
+    for m in (model, m2, m3):
         m.close()

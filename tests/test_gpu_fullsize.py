@@ -95,14 +95,16 @@ def test_full_size_prefill_path(built):
     assert_logits_within_tolerance(np.stack([got[0]] + got[1:]), ref_p[15:])
 
 
-def test_full_size_batch(built):
-    """The 2.3B fp16 workload decoded as a batch of as many requests as the model can batch,
-    each with its own KV prefix (lengths 512, 700, 1000), teacher-forced for 3 steps: per request
-    bit-exact against the oracle's contract mode and within tolerance of its plain mode."""
+@pytest.mark.parametrize("name", ["dense-2.3b-fp16", "dense-2.3b-nvfp4"])
+def test_full_size_batch(built, name):
+    """A 2.3B workload (fp16, and NVFP4 layer matrices) decoded as a batch of as many requests as
+    the model can batch, each with its own KV prefix (lengths 512, 700, 1000), teacher-forced for 3
+    steps: per request bit-exact against the oracle's contract mode and within tolerance of its
+    plain mode."""
     import torch
     from autoregressive_decode_persistent_gb300.model import DecodeModel
-    cfg = synth.get_config("dense-2.3b-fp16")
-    W = synth.model_weights(cfg)
+    cfg = synth.get_config(name)
+    W = _weights(cfg)
     model = DecodeModel(cfg, W)
     nb = model.max_batch
     assert nb >= 2

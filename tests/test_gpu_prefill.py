@@ -33,15 +33,23 @@ def test_tc_gemm_matches_float64(lib, M, N, K, bf16):
     assert (err <= bound).all(), float((err / bound).max())
 
 
-def _kv_within_tolerance(got, ref):
-    """KV rows written by the tensor-core path against the oracle's: per layer, relative L2
-    <= 5e-3 and max-abs <= 2e-2 (the logits' tolerances, applied to the cache)."""
+def _kv_within_tolerance(got, ref, vocab):
+    """KV rows written by the tensor-core path (an approximation: 16-bit GEMM operands) against a
+    reference: the logits' tolerances applied to the cache.  Per layer, and per 128 positions,
+    relative L2 <= 5e-3.  Max-abs: 2e-2 is stated for one step's `vocab` logits; over a layer's n
+    elements the bound keeps the same per-element tail probability (the extreme of n samples grows
+    like sqrt(2 ln n)): 2e-2 * sqrt(ln n / ln vocab), and never below 2e-2."""
+    n = ref[0].size
+    bound = 2e-2 * max(1.0, float(np.sqrt(np.log(n) / np.log(vocab))))
     for layer in range(ref.shape[0]):
         g = got[layer].astype(np.float64)
         r = ref[layer].astype(np.float64)
         d = g - r
-        assert np.max(np.abs(d)) <= 2e-2, (layer, float(np.max(np.abs(d))))
+        assert np.max(np.abs(d)) <= bound, (layer, float(np.max(np.abs(d))), bound)
         assert np.linalg.norm(d) / max(np.linalg.norm(r), 1e-30) <= 5e-3, layer
+        for p0 in range(0, r.shape[1], 128):  # [kv head][position][head_dim]
+            dd, rr = d[:, p0:p0 + 128], r[:, p0:p0 + 128]
+            assert np.linalg.norm(dd) / max(np.linalg.norm(rr), 1e-30) <= 5e-3, (layer, p0)
 
 
 def _as_float(bits, cfg):
@@ -78,8 +86,8 @@ def _prefill_case(cfg, prompt_len, prefix_len=0, n_decode=3):
     assert_logits_within_tolerance(lg.cpu().numpy()[None], out["logits"][None].astype(np.float64))
     n = prefix_len + prompt_len
     k, v = kv.read()
-    _kv_within_tolerance(_as_float(k[:, :, prefix_len:n], cfg), _as_float(om.kc[:, :, prefix_len:n], cfg))
-    _kv_within_tolerance(_as_float(v[:, :, prefix_len:n], cfg), _as_float(om.vc[:, :, prefix_len:n], cfg))
+    _kv_within_tolerance(_as_float(k[:, :, prefix_len:n], cfg), _as_float(om.kc[:, :, prefix_len:n], cfg), cfg["vocab"])
+    _kv_within_tolerance(_as_float(v[:, :, prefix_len:n], cfg), _as_float(om.vc[:, :, prefix_len:n], cfg), cfg["vocab"])
     # decode continues from the tensor-core cache (teacher-forced on the oracle's tokens)
     t = out["next"]
     for _ in range(n_decode):
@@ -145,3 +153,39 @@ def test_prefill_tc_rejects_unsupported_models(lib):
         assert e.value.code == lib.ADP_ERR_UNSUPPORTED_CONFIG
         assert len(kv) == 0
         model.close()
+
+
+def test_prefill_tc_full_prompt_matches_the_decode_path(lib):
+    """The long-context workload's whole 3,584-token prompt at full size (28 query tiles per head, up
+    to 28 key blocks on the longest rows, the masked diagonal blocks, the last tile ragged): the
+    tensor-core prefill's KV rows and first-token logits against the decode-kernel prefill of the
+    same prompt (the bit-exact path, itself checked against the oracle), within the logits'
+    tolerances; then the decode steps after either prefix agree."""
+    import torch
+    import synth
+    from gpu_common import assert_logits_within_tolerance
+    from autoregressive_decode_persistent_gb300.model import DecodeModel
+    cfg = synth.get_config("dense-2.3b-fp16-long-t0.7")
+    prompt = synth.prompt(cfg)
+    P = len(prompt)
+    model = DecodeModel(cfg, synth.model_weights(cfg))
+    a, b = model.new_kv(), model.new_kv()
+    la = torch.empty(cfg["vocab"], device=model.device)
+    lb = torch.empty(cfg["vocab"], device=model.device)
+    ta = a.prefill_tc(prompt, logits=la)
+    tb = b.prefill(prompt, logits=lb)
+    ref = lb.cpu().numpy().astype(np.float64)
+    assert_logits_within_tolerance(la.cpu().numpy()[None], ref[None])
+    top2 = np.sort(ref)[-2:]
+    if top2[1] - top2[0] > 1e-2:
+        assert ta == tb
+    ka, va = a.read()
+    kb, vb = b.read()
+    _kv_within_tolerance(_as_float(ka[:, :, :P], cfg), _as_float(kb[:, :, :P], cfg), cfg["vocab"])
+    _kv_within_tolerance(_as_float(va[:, :, :P], cfg), _as_float(vb[:, :, :P], cfg), cfg["vocab"])
+    t = tb
+    for _ in range(2):
+        a.step(int(t), logits=la)
+        t = b.step(int(t), logits=lb)
+        assert_logits_within_tolerance(la.cpu().numpy()[None], lb.cpu().numpy()[None].astype(np.float64))
+    model.close()
