@@ -705,12 +705,18 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
   }
   consumer_sync();
   if (tid == 0) stamp(p, c, P.index, 7);
-  // Merge: CTA G-1-h merges query head h (after its own items, if any).  Thread d < HD owns output
-  // dimension d; the block maxima and sums are staged in shared memory, the weights
-  // w_b = exp(m_b - M) and L = sum_b w_b l_b computed once, then o_d = (sum_b w_b o_bd) / L, both
-  // sums fused-multiply-added in block order.  Every partial is polled by its epoch, so the merge
-  // starts as soon as the last one lands.
-  const int h = (int)G - 1 - (int)c;
+  // Merge: S CTAs merge each query head, one slice of HD / S output dimensions each: CTA
+  // G-1-(h S + s) takes dimensions [s HD/S, (s+1) HD/S) of head h (after its own items, if any).
+  // S = merge_split on long contexts (at least merge_split_blocks blocks), else 1: every slice
+  // polls all block maxima and sums, which costs more than the split saves on few blocks.  Thread d < HD / S owns one output dimension; the block maxima and sums are staged in
+  // shared memory, the weights w_b = exp(m_b - M) and L = sum_b w_b l_b computed once (every slice
+  // computes the same ones), then o_d = (sum_b w_b o_bd) / L, both sums fused-multiply-added in
+  // block order.  Every partial is polled by its epoch, so the merge starts as soon as the last one
+  // lands.
+  const int S = nb >= p.merge_split_blocks ? p.merge_split : 1;
+  const int HS = HD / S, hs_log = __ffs(HS) - 1;  // HS: a power of two
+  const int mi = (int)G - 1 - (int)c;
+  const int h = mi >= 0 ? mi / S : -1, hs = mi >= 0 ? (mi % S) * HS : 0;
   if (h >= 0 && h < hq && !aborted(ctl)) {
     float* Wm = xbuf;           // [nb] block maxima, then weights w_b
     float* Wl = xbuf + nbmax;   // [nb] block sums; Wl[nbmax] = L
@@ -727,7 +733,7 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
     // flight each, [block][dim]) into shared memory as fp32, while warp 0, whose own loads are in
     // flight, forms the weights.  Blocks beyond what the staging area holds come in further batches.
     float* So = xbuf + ((2 * nbmax + 2 + 3) & ~3);
-    const int batch = (int)(((size_t)p.xbuf_floats - (size_t)((2 * nbmax + 2 + 3) & ~3)) / (size_t)HD);
+    const int batch = (int)(((size_t)p.xbuf_floats - (size_t)((2 * nbmax + 2 + 3) & ~3)) / (size_t)HS);
     bool ok = true;
     auto weights = [&]() {
       float M = __int_as_float(0xFF800000);
@@ -757,8 +763,9 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
     float O = 0.0f;
     for (int b0 = 0; b0 < nb; b0 += batch) {
       const int nbk = min(batch, nb - b0);
-      const ll_t* src = part_o + ((size_t)h * nbmax + b0) * HD;
-      const int nw = nbk * HD;
+      const ll_t* src = part_o + ((size_t)h * nbmax + b0) * HD + hs;  // word i: block i / HS, dim hs + i % HS
+      auto word = [&](int i) { return src + (size_t)(i >> hs_log) * HD + (i & (HS - 1)); };
+      const int nw = nbk * HS;
       constexpr int B = 8, T = kConsumerWarps * 32;
       bool first = b0 == 0;
       for (int base = tid; base < nw; base += B * T) {
@@ -766,7 +773,7 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
 #pragma unroll
         for (int k = 0; k < B; ++k) {
           const int i = base + k * T;
-          w[k] = i < nw ? ll_load(src + i) : 0ull;
+          w[k] = i < nw ? ll_load(word(i)) : 0ull;
         }
         if (first && cw == 0) weights();  // warp 0's loads are in flight meanwhile
         first = false;
@@ -775,11 +782,11 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
           const int i = base + k * T;
           if (i < nw) {
             if (ll_epoch(w[k]) != ew) {
-              if (!ll_wait(src + i, ew, w[k], p, ctl)) { ok = false; break; }
+              if (!ll_wait(word(i), ew, w[k], p, ctl)) { ok = false; break; }
 #pragma unroll
               for (int j = k + 1; j < B; ++j) {  // reload the rest together (see ll_fetch)
                 const int ij = base + j * T;
-                if (ij < nw && ll_epoch(w[j]) != ew) w[j] = ll_load(src + ij);
+                if (ij < nw && ll_epoch(w[j]) != ew) w[j] = ll_load(word(ij));
               }
             }
             So[i] = ll_value(w[k]);
@@ -788,25 +795,25 @@ __device__ __forceinline__ void attention_phase(const Params& p, Ctl* ctl, float
       }
       if (first && cw == 0) weights();  // a batch with fewer words than threads
       consumer_sync();
-      if (tid < HD) {
+      if (tid < HS) {
         int t2 = 0;
         for (; t2 + 8 <= nbk; t2 += 8) {
           float ov[8], wv[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            ov[k] = So[(size_t)(t2 + k) * HD + tid];
+            ov[k] = So[(size_t)(t2 + k) * HS + tid];
             wv[k] = Wm[b0 + t2 + k];
           }
 #pragma unroll
           for (int k = 0; k < 8; ++k) O = fmaf(wv[k], ov[k], O);
         }
-        for (; t2 < nbk; ++t2) O = fmaf(Wm[b0 + t2], So[(size_t)t2 * HD + tid], O);
+        for (; t2 < nbk; ++t2) O = fmaf(Wm[b0 + t2], So[(size_t)t2 * HS + tid], O);
       }
       if (b0 + nbk < nb) consumer_sync();  // the staging area is reused by the next batch
     }
     ok = ok && !aborted(ctl);
     if (tid == 0) stamp(p, c, P.index, 13);
-    if (ok && tid < HD) ll_store(attn + (size_t)h * HD + tid, ll_pack(__fdiv_rn(O, Wl[nbmax]), ew));
+    if (ok && tid < HS) ll_store(attn + (size_t)h * HD + hs + tid, ll_pack(__fdiv_rn(O, Wl[nbmax]), ew));
     if (tid == 0) stamp(p, c, P.index, 11);
   }
   att_uses_io = att_uses;

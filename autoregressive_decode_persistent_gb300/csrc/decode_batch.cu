@@ -217,19 +217,20 @@ __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, 
           const uint8_t* codes = base + (size_t)cw * ROWS * (kck >> 1);
           const uint8_t* bsc = base + (size_t)m * ROWS * (kck >> 1) + (size_t)cw * ROWS * (kck >> 4);
           for (int v = lane; v < nvec; v += 32) {
-            // one row's codes at a time (fewer live registers than the 16-bit path's row pairs)
+            float w[ROWS][8], bs[ROWS];
 #pragma unroll
             for (int j = 0; j < ROWS; ++j) {
-              float w8[8];
-              load8_e2m1(*reinterpret_cast<const uint32_t*>(codes + (size_t)j * (kck >> 1) + (size_t)v * 4), w8);
-              const float bs = e4m3_to_f32(bsc[(size_t)j * (kck >> 4) + (v >> 1)]);
+              load8_e2m1(*reinterpret_cast<const uint32_t*>(codes + (size_t)j * (kck >> 1) + (size_t)v * 4), w[j]);
+              bs[j] = e4m3_to_f32(bsc[(size_t)j * (kck >> 4) + (v >> 1)]);
+            }
+            // each request's input vector read once for all rows of the unit
 #pragma unroll
-              for (int r = 0; r < kMaxBatch; ++r) {
-                if (r < nb) {
-                  float x8[8];
-                  load_xs8(xbuf + r * Kp, xv + v, x8);
-                  acc[r * ROWS + j] = fmaf(bs, fma8(w8, x8, 0.0f), acc[r * ROWS + j]);
-                }
+            for (int r = 0; r < kMaxBatch; ++r) {
+              if (r < nb) {
+                float x8[8];
+                load_xs8(xbuf + r * Kp, xv + v, x8);
+#pragma unroll
+                for (int j = 0; j < ROWS; ++j) acc[r * ROWS + j] = fmaf(bs[j], fma8(w[j], x8, 0.0f), acc[r * ROWS + j]);
               }
             }
           }

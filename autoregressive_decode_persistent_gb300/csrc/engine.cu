@@ -550,6 +550,11 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   p.eps = c.rms_eps;
   p.attn_scale = (float)(1.0 / std::sqrt((double)hd));
   p.nbmax = nbmax;
+  // on long contexts each query head is merged by up to four CTAs (head_dim slices), as many as
+  // the grid has CTAs for; the merge time grows with the block count, the split's fixed cost does
+  // not (measured break-even near 50 blocks on the 2.3B model)
+  p.merge_split = hq * 4 <= m->G && hd % 4 == 0 ? 4 : hq * 2 <= m->G && hd % 2 == 0 ? 2 : 1;
+  p.merge_split_blocks = 64;
   p.rope_cos = d_cos;
   p.rope_sin = d_sin;
   p.wait_ns = 200000000ull;

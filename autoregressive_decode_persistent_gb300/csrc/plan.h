@@ -102,6 +102,8 @@ struct Params {
   int32_t att_gmax;                   // warps per slot (largest number of query heads per KV head)
   int32_t att_slot_bytes;             // shared-memory staging bytes of one slot
   int32_t xbuf_floats;                // floats of the shared input-vector / staging area
+  int32_t merge_split;                // CTAs merging each query head, one slice of head_dim each (1, 2, 4),
+  int32_t merge_split_blocks;         // from this many attention blocks on (fewer: one CTA per head)
   // KV cache [L][hkv][max_ctx][hd]
   uint16_t* kc;
   uint16_t* vc;
