@@ -27,11 +27,14 @@
 namespace adp {
 
 constexpr int kTcBM = 128, kTcBN = 256, kTcStages = 3;
-constexpr int kTcHalves = 2;                        // a CTA's output tile: 2 x 128 rows x 256 columns
 constexpr uint32_t kTcABytes = kTcBM * kTcBK * 2;  // 16 KB: one 128-row A tile
 constexpr uint32_t kTcBBytes = kTcBN * kTcBK * 2;  // 32 KB
-constexpr uint32_t kTcStageBytes = kTcHalves * kTcABytes + kTcBBytes;  // 64 KB
-constexpr size_t kTcSmem = (size_t)kTcStages * kTcStageBytes + 256;
+// a CTA's output tile: HALVES x 128 rows x 256 columns (HALVES 2: each staged weight tile serves
+// 256 rows; HALVES 1: twice the CTAs, for grids that would otherwise end in a nearly empty wave)
+template <int HALVES>
+__host__ __device__ constexpr uint32_t tc_stage_bytes() { return HALVES * kTcABytes + kTcBBytes; }
+template <int HALVES>
+constexpr size_t tc_gemm_smem() { return (size_t)kTcStages * tc_stage_bytes<HALVES>() + 256; }
 
 // 16-bit storage of an fp32 value (RNE): bf16 or f16.
 __device__ __forceinline__ uint16_t tc_store16(float v, int bf16) {
@@ -42,11 +45,12 @@ __device__ __forceinline__ uint16_t tc_store16(float v, int bf16) {
 
 // MODE TC_SWIGLU: C is the A-operand tile buffer of the next GEMM (K = n_valid / 2) and ldc its
 // number of 64-wide K tiles; output columns 2i and 2i + 1 are gate_i and up_i.
-template <int BF16, int MODE>
+template <int BF16, int MODE, int HALVES>
 __global__ void __launch_bounds__(128, 1)
     tc_gemm_kernel(const uint8_t* __restrict__ A, const uint8_t* __restrict__ W, float* C, int ldc, int m_valid,
                    int n_valid, int k_tiles, int32_t* err, uint64_t wait_ns, const __grid_constant__ TcQkvEpi qe,
                    const float* __restrict__ cs) {
+  constexpr uint32_t kTcStageBytes = tc_stage_bytes<HALVES>();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kTcStages * kTcStageBytes);
   uint64_t* empty = full + kTcStages;
@@ -56,8 +60,8 @@ __global__ void __launch_bounds__(128, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // M-blocks vary fastest across the grid, so the CTAs running together share few weight tiles
   // (each read from DRAM once, then from L2) and every A tile stays in L2
-  const int mb = blockIdx.x, nb = blockIdx.y;  // rows 256 mb .., columns 256 nb ..
-  const uint8_t* Ab = A + (size_t)(kTcHalves * mb) * k_tiles * kTcABytes;  // 128-row tile 2 mb (2 mb + 1 follows)
+  const int mb = blockIdx.x, nb = blockIdx.y;  // rows 128 HALVES mb .., columns 256 nb ..
+  const uint8_t* Ab = A + (size_t)(HALVES * mb) * k_tiles * kTcABytes;  // 128-row tile HALVES mb (and the next)
   const uint8_t* Wb = W + (size_t)nb * k_tiles * kTcBBytes;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
@@ -69,7 +73,7 @@ __global__ void __launch_bounds__(128, 1)
     mbar_fence_init();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, kTcHalves * kTcBN);  // two 128 x 256 fp32 accumulators: all 512 columns
+    tmem_alloc(tmem_slot, HALVES * kTcBN);  // HALVES 128 x 256 fp32 accumulators
     tmem_relinquish();
   }
   tc_fence_before();
@@ -89,9 +93,9 @@ __global__ void __launch_bounds__(128, 1)
       }
       uint8_t* dst = smem + (size_t)s * kTcStageBytes;
       mbar_arrive_expect_tx(&full[s], kTcStageBytes);
-      for (int hh = 0; hh < kTcHalves; ++hh)
+      for (int hh = 0; hh < HALVES; ++hh)
         tma_load_1d(dst + hh * kTcABytes, Ab + ((size_t)hh * k_tiles + ks) * kTcABytes, kTcABytes, &full[s], pol);
-      tma_load_1d(dst + kTcHalves * kTcABytes, Wb + (size_t)ks * kTcBBytes, kTcBBytes, &full[s], pol);
+      tma_load_1d(dst + HALVES * kTcABytes, Wb + (size_t)ks * kTcBBytes, kTcBBytes, &full[s], pol);
       issued = ks + 1;
     }
     // no bulk copy may still be writing this CTA's shared memory when it exits
@@ -109,9 +113,9 @@ __global__ void __launch_bounds__(128, 1)
       }
       tc_fence_after();
       const uint32_t a0 = smem_u32(smem + (size_t)s * kTcStageBytes);
-      const uint32_t b0 = a0 + kTcHalves * kTcABytes;
+      const uint32_t b0 = a0 + HALVES * kTcABytes;
 #pragma unroll
-      for (int hh = 0; hh < kTcHalves; ++hh)
+      for (int hh = 0; hh < HALVES; ++hh)
 #pragma unroll
         for (int kk = 0; kk < kTcBK / 16; ++kk)
           tc_mma_f16(tmem + hh * kTcBN, tc_smem_desc(a0 + hh * kTcABytes + kk * 256, 128, 1024),
@@ -127,8 +131,8 @@ __global__ void __launch_bounds__(128, 1)
   const bool ok = mbar_wait(done, 0, &never, wait_ns) && !*ab;
   tc_fence_after();
   if (ok) {
-   for (int hh = 0; hh < kTcHalves; ++hh) {
-    const int row = (kTcHalves * mb + hh) * kTcBM + warp * 32 + lane;
+   for (int hh = 0; hh < HALVES; ++hh) {
+    const int row = (HALVES * mb + hh) * kTcBM + warp * 32 + lane;
     if (MODE == TC_QKV) {
       // whole heads lie in one 256-column tile; RoPE pairs (i, i + hd/2) of q and k, then q into
       // the query tiles and k, v into the cache rows of position pos0 + row
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) tmem_dealloc(tmem, kTcHalves * kTcBN);
+  if (warp == 2) tmem_dealloc(tmem, HALVES * kTcBN);
 }
 
 // Row-major 16-bit [rows, K] (row stride ld elements) -> tiles of `tile_rows` x 64 in the
@@ -309,27 +313,49 @@ cudaError_t tc_tile(const uint16_t* src, int rows, int K, int ld, uint8_t* dst, 
   return cudaGetLastError();
 }
 
+// Whole waves of CTAs each kernel would take on this GPU, in units of a 256-row tile's work: 128-row
+// tiles (HALVES 1) when they finish sooner, e.g. 2 waves of 256-row tiles whose second is nearly
+// empty against 3 waves of half the work.
+static int tc_halves_for(int M, int N) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+      sms = 1;
+  }
+  const long long nt = (N + kTcBN - 1) / kTcBN;
+  const long long c2 = (long long)((M + 2 * kTcBM - 1) / (2 * kTcBM)) * nt, c1 = (long long)((M + kTcBM - 1) / kTcBM) * nt;
+  const long long w2 = 2 * ((c2 + sms - 1) / sms), w1 = (c1 + sms - 1) / sms;  // in half-tile units
+  return w1 < w2 ? 1 : 2;
+}
+
 cudaError_t tc_gemm(int bf16, int mode, const uint8_t* A_tiled, const uint8_t* W_tiled, float* C, int ldc, int M,
                     int N, int K, int32_t* err, uint64_t wait_ns, cudaStream_t st, const TcQkvEpi* qkv,
                     const float* colscale) {
   const int k_tiles = (K + kTcBK - 1) / kTcBK;
-  const dim3 grid((M + kTcHalves * kTcBM - 1) / (kTcHalves * kTcBM), (N + kTcBN - 1) / kTcBN);
-  const void* kernels[2][4] = {
-      {(const void*)tc_gemm_kernel<0, TC_STORE>, (const void*)tc_gemm_kernel<0, TC_ADD>,
-       (const void*)tc_gemm_kernel<0, TC_SWIGLU>, (const void*)tc_gemm_kernel<0, TC_QKV>},
-      {(const void*)tc_gemm_kernel<1, TC_STORE>, (const void*)tc_gemm_kernel<1, TC_ADD>,
-       (const void*)tc_gemm_kernel<1, TC_SWIGLU>, (const void*)tc_gemm_kernel<1, TC_QKV>}};
+  const int halves = tc_halves_for(M, N);
+  const dim3 grid((M + halves * kTcBM - 1) / (halves * kTcBM), (N + kTcBN - 1) / kTcBN);
+  const void* kernels[2][2][4] = {
+      {{(const void*)tc_gemm_kernel<0, TC_STORE, 1>, (const void*)tc_gemm_kernel<0, TC_ADD, 1>,
+        (const void*)tc_gemm_kernel<0, TC_SWIGLU, 1>, (const void*)tc_gemm_kernel<0, TC_QKV, 1>},
+       {(const void*)tc_gemm_kernel<1, TC_STORE, 1>, (const void*)tc_gemm_kernel<1, TC_ADD, 1>,
+        (const void*)tc_gemm_kernel<1, TC_SWIGLU, 1>, (const void*)tc_gemm_kernel<1, TC_QKV, 1>}},
+      {{(const void*)tc_gemm_kernel<0, TC_STORE, 2>, (const void*)tc_gemm_kernel<0, TC_ADD, 2>,
+        (const void*)tc_gemm_kernel<0, TC_SWIGLU, 2>, (const void*)tc_gemm_kernel<0, TC_QKV, 2>},
+       {(const void*)tc_gemm_kernel<1, TC_STORE, 2>, (const void*)tc_gemm_kernel<1, TC_ADD, 2>,
+        (const void*)tc_gemm_kernel<1, TC_SWIGLU, 2>, (const void*)tc_gemm_kernel<1, TC_QKV, 2>}}};
   TcQkvEpi qe{};
   if (mode == TC_QKV) {
     if (!qkv) return cudaErrorInvalidValue;
     qe = *qkv;
   }
-  const void* k = kernels[bf16 ? 1 : 0][mode];
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+  const void* k = kernels[halves - 1][bf16 ? 1 : 0][mode];
+  const size_t smem = halves == 1 ? tc_gemm_smem<1>() : tc_gemm_smem<2>();
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   void* args[] = {(void*)&A_tiled, (void*)&W_tiled, (void*)&C,   (void*)&ldc,     (void*)&M, (void*)&N,
                   (void*)&k_tiles, (void*)&err,    (void*)&wait_ns, (void*)&qe, (void*)&colscale};
-  return cudaLaunchKernel(k, grid, dim3(128), args, kTcSmem, st);
+  return cudaLaunchKernel(k, grid, dim3(128), args, smem, st);
 }
 
 // (A operands are allocated with their rows padded to 256 (tc_tiled_bytes(rows, K, 256)): a CTA stages

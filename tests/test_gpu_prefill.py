@@ -14,11 +14,14 @@ def lib():
     return adp
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 100), (5, 17, 8), (384, 1024, 2560), (130, 512, 704)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 300, 100), (5, 17, 8), (384, 1024, 2560), (130, 512, 704),
+                                   (2000, 4864, 100)])
 @pytest.mark.parametrize("bf16", [False, True])
 def test_tc_gemm_matches_float64(lib, M, N, K, bf16):
     """fp32 accumulation of exact 16-bit products: every entry within 2^-20 of the row's sum of
-    |a_k w_k| (fp32 rounding of K partial sums) of the float64 product."""
+    |a_k w_k| (fp32 rounding of K partial sums) of the float64 product.  The GEMM takes 128-row
+    tiles where 256-row ones would leave a nearly empty last wave: on a 152-SM GB300 the small
+    shapes run with 128-row tiles and 2000 x 4864 (one full wave of 256-row tiles) with 256."""
     import torch
     dt = torch.bfloat16 if bf16 else torch.float16
     g = torch.Generator().manual_seed(M * 7 + N * 3 + K)
