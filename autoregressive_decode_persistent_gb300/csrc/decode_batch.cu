@@ -41,7 +41,7 @@ struct BCtl {
   float rnorm[kMaxBatch];                                  // 1 / rms of each request's input
   unsigned long long red_k[kConsumerWarps][kMaxBatch];     // per-warp argmax keys (LM head)
   int32_t any_sample;                                      // some request samples (temperature > 0)
-  int32_t pad;
+  int32_t down_seg;  // elements of each request's down-projection input staged at once (< ff: segments)
 };
 
 __device__ __forceinline__ BCtl* bctl_of(const Ctl* ctl, int n_phases) {
@@ -146,14 +146,57 @@ __device__ void stage_residual_batch(const Params& p, Ctl* ctl, BCtl* bc, const 
 // One GEMV phase for nb requests: each weight vector of the tile, loaded once, meets every
 // request's input vector.  Per (request, row) the dot product is the contract's: lane l takes
 // vectors l, l + 32, ... in order with fused multiply-adds, then the fixed butterfly.
-template <int ROWS, int WDT>
+// The down projection's input may be staged in segments of down_seg elements per request (when
+// nb whole vectors would leave the ring too few slots): at the chunk where the next segment starts,
+// every consumer warp has finished the previous one, and the segment's words (epoch e_src) replace
+// it; the chunks, and so the operations of every dot product, keep their order.
+// A segment of seg words of the down projection's input for each of the n / seg requests (request
+// r's words at src + r ff) once each carries `epoch`, into xbuf in the split layout (request r at
+// r segp), as ll_fetch does for whole vectors (eight loads in flight per thread; ends with
+// consumer_sync).  Out of line: inlined into the GEMV loop, where every accumulator is live, its
+// loads in flight pushed an accumulator array to local memory.
+__device__ __noinline__ void fetch_down_segment(const Params& p, Ctl* ctl, float* xbuf, const ll_t* src, int n, int seg,
+                                                int segp, uint32_t epoch, int tid) {
+  constexpr int B = 8, T = kConsumerWarps * 32;
+  auto at = [=](int i) { return src + (size_t)(i / seg) * p.ff + i % seg; };
+  for (int base = tid; base < n; base += B * T) {
+    ll_t w[B];
+#pragma unroll
+    for (int k = 0; k < B; ++k) {
+      const int i = base + k * T;
+      w[k] = i < n ? ll_load(at(i)) : 0ull;
+    }
+#pragma unroll
+    for (int k = 0; k < B; ++k) {
+      const int i = base + k * T;
+      if (i < n) {
+        if (ll_epoch(w[k]) != epoch) {
+          if (!ll_wait(at(i), epoch, w[k], p, ctl)) break;
+#pragma unroll
+          for (int j = k + 1; j < B; ++j) {  // the later words of the batch: reload those still behind
+            const int ij = base + j * T;
+            if (ij < n && ll_epoch(w[j]) != epoch) w[j] = ll_load(at(ij));
+          }
+        }
+        xbuf[(i / seg) * segp + xpos(i % seg)] = ll_value(w[k]);
+      }
+    }
+  }
+  consumer_sync();
+}
+
+template <int ROWS, int WDT, bool SEG>
 __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, uint8_t* ring, float* xbuf,
                                            const PhaseDesc& Pd, uint32_t c, uint32_t G, int cw, int lane,
-                                           uint32_t& t_io, uint32_t ew) {
+                                           uint32_t& t_io, uint32_t ew, uint32_t e_src) {
   constexpr int EB = WDT == DT_E4M3 ? 1 : 2;
   constexpr int NA = kMaxBatch * ROWS;
+  constexpr bool kScaled = WDT == DT_E4M3 || WDT == DT_NVFP4;  // per-row scales after the fold
   const int kind = Pd.kind, L = Pd.layer, K = Pd.K, KC = Pd.KC, n_chunks = Pd.n_chunks, upr = Pd.upr;
-  const int Kp = vec_stride(K);
+  const int dseg = SEG ? bc->down_seg : K;
+  const bool segd = SEG && ROWS == 2 && kind == PK_DOWN && dseg < K;
+  const int Kp = vec_stride(segd ? dseg : K);
+  int seg_cur = 0, seg_k0 = 0;  // the staged segment of the down input (segment 0 from the prologue)
   const int nb = p.nb;
   const uint64_t wait_ns = p.wait_ns;
   const uint32_t ns = (uint32_t)p.nslots;
@@ -173,7 +216,6 @@ __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, 
     for (int i = 0; i < NA; ++i) acc[i] = 0.0f;
     // e4m3 and NVFP4 layer matrices: this unit's row scales, applied after the fold (as for one
     // request)
-    constexpr bool kScaled = WDT == DT_E4M3 || WDT == DT_NVFP4;
     float sc[ROWS];
     if constexpr (kScaled) {
       if (active) {
@@ -199,6 +241,13 @@ __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, 
       }
     }
     for (int ck = 0; ck < n_chunks; ++ck) {
+      if (SEG && ROWS == 2 && segd && (ck * KC) / dseg != seg_cur) {
+        consumer_sync();  // no warp reads the previous segment any more
+        seg_cur = (ck * KC) / dseg;
+        seg_k0 = seg_cur * dseg;
+        const int len = min(dseg, K - seg_k0);
+        fetch_down_segment(p, ctl, xbuf, p.h + seg_k0, nb * len, len, Kp, e_src, cw * 32 + lane);
+      }
       const bool ok = mbar_wait(&ctl->full[slot], par, &ctl->abort, wait_ns);
       if (!ok) {
         if (lane == 0 && !aborted(ctl)) set_error(p, ctl, DE_PIPELINE_TIMEOUT);
@@ -208,7 +257,7 @@ __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, 
       if (active && ok) {
         const int kck = min(KC, K - ck * KC);
         const int nvec = kck >> 3;
-        const int xv = (ck * KC) >> 3;
+        const int xv = (ck * KC - seg_k0) >> 3;
         if constexpr (WDT == DT_NVFP4) {
           // [m * ROWS rows][kck / 2] code bytes, then [m * ROWS][kck / 16] block scales; per 8-element
           // vector the products summed from zero, times the block scale, into the lane partial (the
@@ -321,43 +370,48 @@ __device__ __forceinline__ void gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, 
       }
     } else if (kind == PK_GU) {
       if (lane < nb) ll_store(p.h + (size_t)lane * p.ff + unit, ll_pack(silu_mul(pick(acc, 2 * lane), pick(acc, 2 * lane + 1)), ew));
-    } else if (kind == PK_LM && !kScaled) {  // (the LM head is always a 16-bit matrix)
-      if (lane == 0) {
+    } else if (kind == PK_LM) {
+      // (compiled only where the LM head runs: 4-row units of a 16-bit matrix)
+      if constexpr (ROWS == 4 && !kScaled) {
+        if (lane == 0) {
 #pragma unroll
-        for (int r = 0; r < kMaxBatch; ++r) {
-          if (r < nb) {
+          for (int r = 0; r < kMaxBatch; ++r) {
+            if (r < nb) {
 #pragma unroll
-            for (int j = 0; j < ROWS; ++j) {
-              const int row = unit * ROWS + j;
-              __stcg(p.logits + (size_t)r * p.V + row, acc[r * ROWS + j]);
-              const unsigned long long k = argmax_key(acc[r * ROWS + j], (uint32_t)row);
-              best[r] = k > best[r] ? k : best[r];
+              for (int j = 0; j < ROWS; ++j) {
+                const int row = unit * ROWS + j;
+                __stcg(p.logits + (size_t)r * p.V + row, acc[r * ROWS + j]);
+                const unsigned long long k = argmax_key(acc[r * ROWS + j], (uint32_t)row);
+                best[r] = k > best[r] ? k : best[r];
+              }
             }
           }
         }
       }
     }
   }
-  if (kind == PK_LM) {
-    if (lane == 0)
+  if constexpr (ROWS == 4 && !kScaled) {
+    if (kind == PK_LM) {
+      if (lane == 0)
 #pragma unroll
-      for (int r = 0; r < kMaxBatch; ++r) bc->red_k[cw][r] = best[r];
-    consumer_sync();
-    if (cw == 0 && lane == 0) {
-      if (!aborted(ctl)) {
-        for (int r = 0; r < nb; ++r) {
-          unsigned long long k = 0ull;
-          for (int w = 0; w < kConsumerWarps; ++w) k = bc->red_k[w][r] > k ? bc->red_k[w][r] : k;
-          if (k) atomicMax(p.argkey + r, k);
+        for (int r = 0; r < kMaxBatch; ++r) bc->red_k[cw][r] = best[r];
+      consumer_sync();
+      if (cw == 0 && lane == 0) {
+        if (!aborted(ctl)) {
+          for (int r = 0; r < nb; ++r) {
+            unsigned long long k = 0ull;
+            for (int w = 0; w < kConsumerWarps; ++w) k = bc->red_k[w][r] > k ? bc->red_k[w][r] : k;
+            if (k) atomicMax(p.argkey + r, k);
+          }
+          __threadfence();
+          const uint32_t old = atomicAdd(p.lm_ctr, 1u);
+          ctl->flag = (old == G - 1) ? 1 : 0;
+        } else {
+          ctl->flag = 0;
         }
-        __threadfence();
-        const uint32_t old = atomicAdd(p.lm_ctr, 1u);
-        ctl->flag = (old == G - 1) ? 1 : 0;
-      } else {
-        ctl->flag = 0;
       }
+      consumer_sync();
     }
-    consumer_sync();
   }
   t_io = slot | (par << 8);
 }
@@ -696,13 +750,14 @@ __device__ __forceinline__ void sample_batch(const Params& p, Ctl* ctl, BCtl* bc
   }
 }
 
-template <int WDT>
+template <int WDT, bool SEG>
 __device__ void run_gemv_batch(const Params& p, Ctl* ctl, BCtl* bc, uint8_t* ring, float* xbuf, const PhaseDesc& P,
-                               uint32_t c, uint32_t G, int cw, int lane, uint32_t& t, uint32_t ew) {
-  if (P.kind == PK_LM) gemv_batch<4, WDT>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew);
-  else gemv_batch<2, WDT>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew);
+                               uint32_t c, uint32_t G, int cw, int lane, uint32_t& t, uint32_t ew, uint32_t e_src) {
+  if (P.kind == PK_LM) gemv_batch<4, WDT, false>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew, e_src);
+  else gemv_batch<2, WDT, SEG>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew, e_src);
 }
 
+template <bool SEG>
 __device__ void consumer_batch(const Params& p, Ctl* ctl, BCtl* bc, uint8_t* ring, float* xbuf, uint32_t ebase,
                                uint32_t c, uint32_t G, int ph0, int ph1, bool use_barrier, int cw, int lane) {
   uint32_t t = 0;
@@ -773,7 +828,12 @@ __device__ void consumer_batch(const Params& p, Ctl* ctl, BCtl* bc, uint8_t* rin
         case PK_DOWN:
           if (n > 0) {
             stage_residual_batch(p, ctl, bc, P, 2, e_res, tid);
-            ll_fetch(p, ctl, xbuf, p.h, nb * p.ff, p.ff, vec_stride(p.ff), e_src, tid);
+            // the whole input, or its first segment (the GEMV fetches the others)
+            if (SEG && bc->down_seg < p.ff)
+              fetch_down_segment(p, ctl, xbuf, p.h, nb * bc->down_seg, bc->down_seg, vec_stride(bc->down_seg), e_src,
+                                 tid);
+            else
+              ll_fetch(p, ctl, xbuf, p.h, nb * p.ff, p.ff, vec_stride(p.ff), e_src, tid);
           }
           break;
         case PK_GU:
@@ -799,13 +859,13 @@ __device__ void consumer_batch(const Params& p, Ctl* ctl, BCtl* bc, uint8_t* rin
       } else if (P.kind == PK_SAMPLE) {
         if (bc->any_sample) sample_batch(p, ctl, bc, ebase, c, G, cw, lane);
       } else if (p.wdt == DT_E4M3 && P.kind != PK_LM) {
-        gemv_batch<2, DT_E4M3>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew);
+        gemv_batch<2, DT_E4M3, SEG>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew, e_src);
       } else if (p.wdt == DT_NVFP4 && P.kind != PK_LM) {
-        gemv_batch<2, DT_NVFP4>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew);
+        gemv_batch<2, DT_NVFP4, SEG>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew, e_src);
       } else if ((P.kind == PK_LM ? p.edt : p.wdt) == DT_BF16) {
-        run_gemv_batch<DT_BF16>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew);
+        run_gemv_batch<DT_BF16, SEG>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew, e_src);
       } else {
-        run_gemv_batch<DT_F16>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew);
+        run_gemv_batch<DT_F16, SEG>(p, ctl, bc, ring, xbuf, P, c, G, cw, lane, t, ew, e_src);
       }
       // ---- the LM head's last CTA picks the greedy requests' tokens
       if (P.kind == PK_LM && ctl->flag && cw == 0 && lane == 0) {
@@ -829,9 +889,12 @@ __device__ void consumer_batch(const Params& p, Ctl* ctl, BCtl* bc, uint8_t* rin
   }
 }
 
+// SEG: the down projection's input staged in segments (down_seg < ff; an instantiation of its own,
+// so that batches whose inputs fit whole run none of that code).
+template <bool SEG>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_batch_kernel(const __grid_constant__ Params p, int32_t ph0, int32_t ph1, int32_t use_barrier,
-                        int32_t xbuf_floats) {
+                        int32_t xbuf_floats, int32_t down_seg) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   float* xbuf = reinterpret_cast<float*>(smem + (size_t)p.nslots * kSlotBytes);
@@ -840,6 +903,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   BCtl* bc = bctl_of(ctl, p.n_phases);
   cta_setup(p, ctl);
+  if (threadIdx.x == 0) bc->down_seg = down_seg;
   if (threadIdx.x < (unsigned)p.nb) {
     const int r = threadIdx.x;
     const StepState* s = p.state + r;
@@ -863,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumerWarps) {
     if (lane == 0) producer(p, ctl, ring, c, G, ph0, ph1);
   } else {
-    consumer_batch(p, ctl, bc, ring, xbuf, ebase, c, G, ph0, ph1, use_barrier != 0, warp, lane);
+    consumer_batch<SEG>(p, ctl, bc, ring, xbuf, ebase, c, G, ph0, ph1, use_barrier != 0, warp, lane);
   }
 }
 
@@ -872,18 +936,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace adp {
 
 cudaError_t decode_batch_prepare(size_t smem_bytes, int* blocks_per_sm) {
-  const void* k = (const void*)decode_batch_kernel;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
-  if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, kThreads, smem_bytes);
+  int bmin = 1 << 30;
+  for (const void* k : {(const void*)decode_batch_kernel<false>, (const void*)decode_batch_kernel<true>}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+    if (e != cudaSuccess) return e;
+    int b = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k, kThreads, smem_bytes)) != cudaSuccess) return e;
+    bmin = b < bmin ? b : bmin;
+  }
+  *blocks_per_sm = bmin;
+  return cudaSuccess;
 }
 
 cudaError_t decode_batch_launch(const Params& p, int ph0, int ph1, int grid, size_t smem_bytes, int xbuf_floats,
-                                cudaStream_t stream) {
-  int32_t a0 = ph0, a1 = ph1, ub = 1, xf = xbuf_floats;
-  void* args[] = {(void*)&p, &a0, &a1, &ub, &xf};
-  return cudaLaunchCooperativeKernel((const void*)decode_batch_kernel, dim3(grid), dim3(kThreads), args, smem_bytes,
-                                     stream);
+                                int down_seg, cudaStream_t stream) {
+  int32_t a0 = ph0, a1 = ph1, ub = 1, xf = xbuf_floats, ds = down_seg;
+  void* args[] = {(void*)&p, &a0, &a1, &ub, &xf, &ds};
+  const void* k = down_seg < p.ff ? (const void*)decode_batch_kernel<true> : (const void*)decode_batch_kernel<false>;
+  return cudaLaunchCooperativeKernel(k, dim3(grid), dim3(kThreads), args, smem_bytes, stream);
 }
 
 size_t batch_ctl_bytes() { return sizeof(BCtl); }

@@ -118,6 +118,7 @@ struct adp_model {
     int max_nb = 0;
     size_t smem[kMaxBatch + 1] = {};
     int nslots[kMaxBatch + 1] = {}, xbuf_floats[kMaxBatch + 1] = {}, att_slots[kMaxBatch + 1] = {};
+    int down_seg[kMaxBatch + 1] = {};  // elements of the down input staged at once per request
     Params p{};                    // the batch buffers (per-request copies back to back)
     BatchHost* h = nullptr;        // pinned staging of the step state and cache tables
     BatchHost* d = nullptr;
@@ -886,28 +887,53 @@ static int batch_init(adp_model* m) {
   const size_t item = (size_t)kAttnBlock * (hd + 8) * 2 + (size_t)kAttnBlock * hd * 2 + (size_t)kMaxGroup * hd * 4 +
                       (size_t)kMaxGroup * kAttnBlock * 4;
   auto pad256 = [](int n) { return (size_t)((n + 255) / 256 * 256); };
-  const size_t vec_floats = std::max({pad256(d), pad256(hq * hd), pad256(c.d_ff)});
   const size_t merge_bytes = ((size_t)2 * 8 * nbmax + 8) * 4;
   const int gmax = m->p.att_gmax;
+  // the down projection's K-chunk: a staged segment of its input is a whole number of chunks
+  int down_kc = c.d_ff;
+  for (const PhaseDesc& P : m->phases)
+    if (P.kind == PK_DOWN) {
+      down_kc = P.KC;
+      break;
+    }
+  const int down_chunks = (c.d_ff + down_kc - 1) / down_kc;
   size_t smem_max = 0;
   for (int nb = 1; nb <= kMaxBatch; ++nb) {
     if (nb * hq > m->G) break;  // CTA G-1-(r*hq+h) merges head h of request r
-    const size_t vec_bytes = std::max((size_t)nb * vec_floats * 4, merge_bytes);
-    int ns = 0, att = 0;
+    // the fewest segments of the down input that leave a ring of at least 2 slots: a refetch in the
+    // middle of the down GEMV cost more than a deeper ring saved (2.3B, 2 requests: 1,106 tok/s whole
+    // against 915 in two segments with 4 slots), so segments only make a batch possible at all
+    int ns = 0, att = 0, seg = 0;
     size_t xbytes = 0;
-    for (int k = kMaxSlots; k >= 2 && !ns; --k) {
-      if ((size_t)k * kSlotBytes + ctl_sz > optin) continue;
-      const size_t room = optin - (size_t)k * kSlotBytes - ctl_sz;
-      if (room < vec_bytes || room < item) continue;
-      ns = k;
-      att = (int)std::min<size_t>(std::min(kAttnSlots, kConsumerWarps / gmax), room / item);
-      xbytes = std::max(vec_bytes, (size_t)att * item);
+    for (int S = 1; S <= down_chunks; ++S) {
+      const int sg = S == 1 ? c.d_ff : ((down_chunks + S - 1) / S) * down_kc;
+      if (S > 1 && sg >= c.d_ff) continue;
+      const size_t vec_floats = std::max({pad256(d), pad256(hq * hd), pad256(std::min(sg, c.d_ff))});
+      const size_t vec_bytes = std::max((size_t)nb * vec_floats * 4, merge_bytes);
+      int ks = 0, ka = 0;
+      size_t kx = 0;
+      for (int k = kMaxSlots; k >= 2 && !ks; --k) {
+        if ((size_t)k * kSlotBytes + ctl_sz > optin) continue;
+        const size_t room = optin - (size_t)k * kSlotBytes - ctl_sz;
+        if (room < vec_bytes || room < item) continue;
+        ks = k;
+        ka = (int)std::min<size_t>(std::min(kAttnSlots, kConsumerWarps / gmax), room / item);
+        kx = std::max(vec_bytes, (size_t)ka * item);
+      }
+      if (ks) {
+        ns = ks;
+        att = ka;
+        xbytes = kx;
+        seg = std::min(sg, c.d_ff);
+        break;
+      }
     }
     if (!ns) break;
     xbytes = (xbytes + 127) & ~(size_t)127;
     B.nslots[nb] = ns;
     B.att_slots[nb] = att;
     B.xbuf_floats[nb] = (int)(xbytes / 4);
+    B.down_seg[nb] = seg;
     B.smem[nb] = (size_t)ns * kSlotBytes + xbytes + ctl_sz;
     smem_max = std::max(smem_max, B.smem[nb]);
     B.max_nb = nb;
@@ -1010,7 +1036,8 @@ static int batch_enqueue(adp_model* m, adp_kv* const* kvs, int32_t nb, const int
   q.debug_barriers = m->p.debug_barriers;
   q.skip_cta = q.skip_phase = -1;
   const int nph = (int)m->phases.size();
-  CK(decode_batch_launch(q, 0, sampling ? nph : nph - 1, m->G, B.smem[nb], B.xbuf_floats[nb], m->stream));
+  CK(decode_batch_launch(q, 0, sampling ? nph : nph - 1, m->G, B.smem[nb], B.xbuf_floats[nb], B.down_seg[nb],
+                         m->stream));
   return ADP_OK;
 }
 

@@ -30,8 +30,10 @@ size_t ctl_bytes(int n_phases);  // control block + phase table in shared memory
 // The batched kernel (KK_BATCH): always one persistent cooperative launch.  Its shared memory
 // adds batch_ctl_bytes() after ctl_bytes(n_phases).
 cudaError_t decode_batch_prepare(size_t smem_bytes, int* blocks_per_sm);
+// down_seg: elements of each request's down-projection input staged in shared memory at once
+// (the FFN width: whole; less: segments, refetched as the GEMV reaches them).
 cudaError_t decode_batch_launch(const Params& p, int ph0, int ph1, int grid, size_t smem_bytes, int xbuf_floats,
-                                cudaStream_t stream);
+                                int down_seg, cudaStream_t stream);
 size_t batch_ctl_bytes();
 
 // Epilogues of the prefill GEMM: C = A W^T (fp32, streaming stores), C += A W^T (the fp32
