@@ -78,6 +78,11 @@ class PhasePlan(ctypes.Structure):
                [("region", ctypes.c_uint64), ("expert_stride", ctypes.c_uint64)]
 
 
+class BatchLayout(ctypes.Structure):
+    _fields_ = [("ring_slots", ctypes.c_int32), ("attention_slots", ctypes.c_int32), ("xbuf_floats", ctypes.c_int32),
+                ("down_segment", ctypes.c_int32), ("control_bytes", ctypes.c_uint64), ("smem_bytes", ctypes.c_uint64)]
+
+
 _lib = None
 
 # (name, restype, argtypes)
@@ -120,6 +125,8 @@ _SIGS = [
     ("adp_image_bytes", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint64)]),
     ("adp_plan", ctypes.c_int, [ctypes.POINTER(Config), ctypes.c_int32, ctypes.POINTER(PhasePlan), ctypes.c_int32,
                                 ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_uint64)]),
+    ("adp_batch_plan", ctypes.c_int, [ctypes.POINTER(Config), ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.POINTER(BatchLayout), ctypes.POINTER(ctypes.c_int32)]),
     ("adp_launches_per_step", ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]),
     ("adp_debug_kernel_mode", ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     ("adp_debug_force_experts", ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
@@ -360,6 +367,15 @@ def adp_plan(config: Config, n_sms: int) -> tuple[list[dict], int]:
     out = (PhasePlan * n.value)()
     _check(L.adp_plan(ctypes.byref(config), n_sms, out, n.value, ctypes.byref(n), ctypes.byref(img)), "adp_plan")
     return [{f: getattr(p, f) for f, _ in PhasePlan._fields_} for p in out], img.value
+
+
+def adp_batch_plan(config: Config, n_sms: int, smem_optin: int) -> tuple[list[dict], int]:
+    """The batched kernel's layout for 1..4 requests and the largest batch that fits (host only)."""
+    out = (BatchLayout * 4)()
+    mb = ctypes.c_int32()
+    _check(load_library().adp_batch_plan(ctypes.byref(config), n_sms, smem_optin, out, ctypes.byref(mb)),
+           "adp_batch_plan")
+    return [{f: getattr(o, f) for f, _ in BatchLayout._fields_} for o in out], mb.value
 
 
 def adp_launches_per_step(model) -> int:

@@ -318,6 +318,17 @@ static int reserve_epochs(adp_model* m, int n_steps) {
 
 // ---------------------------------------------------------------- model creation
 
+// Most query heads sharing one KV head (query head h reads KV head floor(h hkv / hq)).
+static int kv_group_max(const adp_config& c) {
+  int gmax = 0;
+  for (int g = 0; g < c.n_kv_heads; ++g) {
+    const int h0 = (g * c.n_heads + c.n_kv_heads - 1) / c.n_kv_heads;
+    const int h1 = ((g + 1) * c.n_heads + c.n_kv_heads - 1) / c.n_kv_heads;
+    gmax = std::max(gmax, h1 - h0);
+  }
+  return gmax;
+}
+
 static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   const adp_config& c = *cfg;
   CK(cudaGetDevice(&m->device));
@@ -339,11 +350,7 @@ static int create(adp_model* m, const adp_config* cfg, const adp_weights* w) {
   const int nbmax_ = (c.max_ctx + kAttnBlock - 1) / kAttnBlock;
   const size_t ctl_sz = (ctl_bytes((int)m->phases.size()) + 127) & ~(size_t)127;
   const size_t optin = (size_t)prop.sharedMemPerBlockOptin;
-  int gmax = 0;  // most query heads sharing one KV head (floor(h * hkv / hq) grouping)
-  for (int g = 0; g < c.n_kv_heads; ++g) {
-    const int h0 = (g * hq + c.n_kv_heads - 1) / c.n_kv_heads, h1 = ((g + 1) * hq + c.n_kv_heads - 1) / c.n_kv_heads;
-    gmax = std::max(gmax, h1 - h0);
-  }
+  const int gmax = kv_group_max(c);  // most query heads sharing one KV head
   if (gmax < 1 || gmax > kMaxGroup) return ADP_ERR_UNSUPPORTED_CONFIG;
   if (hq > m->G) return ADP_ERR_UNSUPPORTED_CONFIG;  // CTA G-1-h merges query head h
   // K (rows padded by 16 bytes), V, the group's queries, the weights e_j
@@ -868,38 +875,41 @@ extern "C" int adp_generate_async(adp_model* m, adp_kv* kv, int32_t token, int32
 
 // ---------------------------------------------------------------- small-batch decode
 
-// Set up batched decode once per model: the shared-memory layout of every batch size that fits
-// (nb input vectors of the widest GEMV input beside a ring of at least two slots), the
-// per-request exchange buffers and the step-state staging.  Dense models only.
-static int batch_init(adp_model* m) {
-  adp_model::Batch& B = m->bt;
-  if (B.init_rc != 1) return B.init_rc;
-  const adp_config& c = m->cfg;
-  B.init_rc = ADP_ERR_UNSUPPORTED_CONFIG;
-  if (c.n_experts != 0) return B.init_rc;  // experts differ per request
-  const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim;
-  cudaDeviceProp prop;
-  CK(cudaGetDeviceProperties(&prop, m->device));
-  const size_t optin = (size_t)prop.sharedMemPerBlockOptin;
-  const int nph = (int)m->phases.size();
+// The batched kernel's shared-memory layout of one batch size (nslots 0: the size does not fit).
+struct BatchLayout {
+  size_t smem = 0, ctl = 0;
+  int nslots = 0, att_slots = 0, xbuf_floats = 0, down_seg = 0;
+};
+
+// The layout of every batch size 1..kMaxBatch on a GPU of G SMs with `optin` bytes of shared memory
+// per block (host only): nb input vectors of the widest GEMV input beside a ring of at least two
+// slots; when nb whole down-projection inputs do not fit, they are staged in segments of whole
+// K-chunks (the fewest that fit).  Returns the largest batch that fits (0: none; MoE models, whose
+// experts differ per request, are not batched).
+static int plan_batches(const adp_config& c, const std::vector<PhaseDesc>& phases, int G, size_t optin,
+                        BatchLayout (&out)[kMaxBatch + 1]) {
+  for (auto& o : out) o = BatchLayout{};
+  if (c.n_experts != 0) return 0;
+  const int d = c.d_model, hq = c.n_heads, hd = c.head_dim;
+  const int nph = (int)phases.size();
   const size_t ctl_sz = (ctl_bytes(nph) + 16 + batch_ctl_bytes() + 127) & ~(size_t)127;
   const int nbmax = (c.max_ctx + kAttnBlock - 1) / kAttnBlock;
   const size_t item = (size_t)kAttnBlock * (hd + 8) * 2 + (size_t)kAttnBlock * hd * 2 + (size_t)kMaxGroup * hd * 4 +
                       (size_t)kMaxGroup * kAttnBlock * 4;
   auto pad256 = [](int n) { return (size_t)((n + 255) / 256 * 256); };
   const size_t merge_bytes = ((size_t)2 * 8 * nbmax + 8) * 4;
-  const int gmax = m->p.att_gmax;
+  const int gmax = kv_group_max(c);
   // the down projection's K-chunk: a staged segment of its input is a whole number of chunks
   int down_kc = c.d_ff;
-  for (const PhaseDesc& P : m->phases)
+  for (const PhaseDesc& P : phases)
     if (P.kind == PK_DOWN) {
       down_kc = P.KC;
       break;
     }
   const int down_chunks = (c.d_ff + down_kc - 1) / down_kc;
-  size_t smem_max = 0;
+  int max_nb = 0;
   for (int nb = 1; nb <= kMaxBatch; ++nb) {
-    if (nb * hq > m->G) break;  // CTA G-1-(r*hq+h) merges head h of request r
+    if (nb * hq > G) break;  // CTA G-1-(r*hq+h) merges head h of request r
     // the fewest segments of the down input that leave a ring of at least 2 slots: a refetch in the
     // middle of the down GEMV cost more than a deeper ring saved (2.3B, 2 requests: 1,106 tok/s whole
     // against 915 in two segments with 4 slots), so segments only make a batch possible at all
@@ -930,13 +940,40 @@ static int batch_init(adp_model* m) {
     }
     if (!ns) break;
     xbytes = (xbytes + 127) & ~(size_t)127;
-    B.nslots[nb] = ns;
-    B.att_slots[nb] = att;
-    B.xbuf_floats[nb] = (int)(xbytes / 4);
-    B.down_seg[nb] = seg;
-    B.smem[nb] = (size_t)ns * kSlotBytes + xbytes + ctl_sz;
+    BatchLayout& o = out[nb];
+    o.nslots = ns;
+    o.att_slots = att;
+    o.xbuf_floats = (int)(xbytes / 4);
+    o.down_seg = seg;
+    o.ctl = ctl_sz;
+    o.smem = (size_t)ns * kSlotBytes + xbytes + ctl_sz;
+    max_nb = nb;
+  }
+  return max_nb;
+}
+
+// Set up batched decode once per model: the shared-memory layout of every batch size that fits
+// (plan_batches), the per-request exchange buffers and the step-state staging.  Dense models only.
+static int batch_init(adp_model* m) {
+  adp_model::Batch& B = m->bt;
+  if (B.init_rc != 1) return B.init_rc;
+  const adp_config& c = m->cfg;
+  B.init_rc = ADP_ERR_UNSUPPORTED_CONFIG;
+  if (c.n_experts != 0) return B.init_rc;  // experts differ per request
+  const int d = c.d_model, hq = c.n_heads, hkv = c.n_kv_heads, hd = c.head_dim;
+  cudaDeviceProp prop;
+  CK(cudaGetDeviceProperties(&prop, m->device));
+  const int nbmax = (c.max_ctx + kAttnBlock - 1) / kAttnBlock;
+  BatchLayout lay[kMaxBatch + 1];
+  B.max_nb = plan_batches(c, m->phases, m->G, (size_t)prop.sharedMemPerBlockOptin, lay);
+  size_t smem_max = 0;
+  for (int nb = 1; nb <= B.max_nb; ++nb) {
+    B.nslots[nb] = lay[nb].nslots;
+    B.att_slots[nb] = lay[nb].att_slots;
+    B.xbuf_floats[nb] = lay[nb].xbuf_floats;
+    B.down_seg[nb] = lay[nb].down_seg;
+    B.smem[nb] = lay[nb].smem;
     smem_max = std::max(smem_max, B.smem[nb]);
-    B.max_nb = nb;
   }
   if (B.max_nb == 0) return B.init_rc;
   int bps = 0;
@@ -1527,6 +1564,29 @@ extern "C" int adp_plan(const adp_config* cfg, int32_t n_sms, adp_phase_plan* ou
     o.replicated = P.replicated;
     o.region = P.region;
     o.expert_stride = P.expert_stride;
+  }
+  return ADP_OK;
+}
+
+extern "C" int adp_batch_plan(const adp_config* cfg, int32_t n_sms, int32_t smem_optin, adp_batch_layout* out,
+                              int32_t* max_batch) {
+  if (!cfg || n_sms < 1 || smem_optin < 1 || !out || !max_batch) return ADP_ERR_INVALID_ARG;
+  const int rc = validate_config(cfg);
+  if (rc) return rc;
+  adp_model m;
+  m.cfg = *cfg;
+  m.G = n_sms;
+  plan(&m);
+  BatchLayout lay[kMaxBatch + 1];
+  *max_batch = plan_batches(m.cfg, m.phases, n_sms, (size_t)smem_optin, lay);
+  for (int nb = 1; nb <= kMaxBatch; ++nb) {
+    adp_batch_layout& o = out[nb - 1];
+    o.ring_slots = lay[nb].nslots;
+    o.attention_slots = lay[nb].att_slots;
+    o.xbuf_floats = lay[nb].xbuf_floats;
+    o.down_segment = lay[nb].down_seg;
+    o.control_bytes = lay[nb].ctl;
+    o.smem_bytes = lay[nb].smem;
   }
   return ADP_OK;
 }

@@ -300,6 +300,27 @@ typedef struct {
 int adp_plan(const adp_config* cfg, int32_t n_sms, adp_phase_plan* out, int32_t cap, int32_t* n_phases,
              uint64_t* image_bytes);
 
+/* The batched kernel's shared-memory layout for one batch size (see adp_batch_plan). */
+typedef struct {
+  int32_t ring_slots;      /* 32 KB weight slots of the ring (0: this batch size does not fit) */
+  int32_t attention_slots; /* attention items a CTA stages at once */
+  int32_t xbuf_floats;     /* floats of the input-vector / staging area (nb input vectors at least) */
+  int32_t down_segment;    /* elements of each request's down-projection input staged at once: d_ff
+                              (whole), or a whole number of that phase's K-chunks (segments, when nb
+                              whole inputs do not fit beside a ring of two slots) */
+  uint64_t control_bytes;  /* the control block (phase table, per-request state) */
+  uint64_t smem_bytes;     /* dynamic shared memory of a launch: ring + staging area + control block */
+} adp_batch_layout;
+
+/* The batched kernel's layout for 1..4 requests of cfg on a GPU with n_sms SMs and smem_optin bytes
+ * of opt-in shared memory per block, computed on the host without any CUDA call, exactly as the
+ * first batched call lays it out (adp_decode_batch; GB300: 232,448 bytes).  out: caller-owned HOST
+ * array of 4 entries, entry nb - 1 for nb requests; *max_batch gets the largest batch that fits
+ * (0: none; MoE models are not batched).  Errors: ADP_ERR_INVALID_ARG (null pointers, n_sms < 1,
+ * smem_optin < 1) and the config errors of adp_create_model. */
+int adp_batch_plan(const adp_config* cfg, int32_t n_sms, int32_t smem_optin, adp_batch_layout* out,
+                   int32_t* max_batch);
+
 int adp_num_ctas(const adp_model* m, int32_t* ctas);            /* persistent grid size (SMs) */
 int adp_image_bytes(const adp_model* m, uint64_t* bytes);       /* bytes of the tile-ordered weight image */
 int adp_launches_per_step(const adp_model* m, int32_t* n);      /* kernel launches of one decode step */

@@ -275,3 +275,49 @@ def test_each_phase_waits_on_the_phases_that_produce_its_inputs(adp, cfg):
             x_writer = i
         elif k == KINDS["router"]:
             router = i
+
+
+GB300_SMEM_OPTIN = 232448  # opt-in shared memory per block on sm_103 (227 KB)
+
+
+@pytest.mark.parametrize("name", ["tiny", "dense-2.3b-fp16", "dense-2.3b-nvfp4", "dense-8b-bf16", "dense-8b-nvfp4",
+                                  "moe-32x1408-top4-e4m3"])
+def test_batch_layouts_fit_and_segment_only_when_needed(adp, name):
+    """The batched kernel's shared-memory layout per batch size (adp_batch_plan, the same function
+    the first batched call runs): every batch that fits has a ring of at least two 32 KB slots and
+    a staging area holding every request's input vector (the down projection's whole, or a segment
+    of whole K-chunks), all within the opt-in limit; the down input is segmented only when whole
+    vectors beside a two-slot ring would not fit; with whole vectors the ring is as deep as the
+    limit allows.  MoE models are not batched."""
+    import synth
+    from autoregressive_decode_persistent_gb300.model import make_config
+    cfg = synth.get_config(name)
+    lay, max_nb = adp.adp_batch_plan(make_config(cfg), 152, GB300_SMEM_OPTIN)
+    if cfg["n_experts"]:
+        assert max_nb == 0 and all(o["ring_slots"] == 0 for o in lay)
+        return
+    assert max_nb >= 1
+    phases, _ = _plan(adp, cfg)
+    down_kc = next(P["KC"] for P in phases if P["kind"] == 4)
+    pad = lambda n: (n + 255) // 256 * 256
+    d, hq, hd, ff = cfg["d_model"], cfg["n_heads"], cfg["head_dim"], cfg["d_ff"]
+    for nb in range(1, 5):
+        o = lay[nb - 1]
+        if nb > max_nb:
+            assert o["ring_slots"] == 0
+            continue
+        assert 2 <= o["ring_slots"] <= 6 and o["attention_slots"] >= 1
+        assert o["smem_bytes"] == o["ring_slots"] * 32768 + o["xbuf_floats"] * 4 + o["control_bytes"]
+        assert o["smem_bytes"] <= GB300_SMEM_OPTIN
+        seg = o["down_segment"]
+        assert seg == ff or (seg % down_kc == 0 and seg < ff)
+        assert o["xbuf_floats"] >= nb * max(pad(d), pad(hq * hd), pad(seg))
+        whole = nb * max(pad(d), pad(hq * hd), pad(ff)) * 4 + 2 * 32768 + o["control_bytes"]
+        if seg < ff:
+            assert whole > GB300_SMEM_OPTIN  # whole vectors would not have fit
+        else:
+            assert o["ring_slots"] == 6 or o["smem_bytes"] + 32768 > GB300_SMEM_OPTIN
+    if name == "dense-2.3b-fp16":
+        # three whole inputs (3 x 38.9 KB); four only in two segments of 7 K-chunks of 768
+        assert max_nb == 4
+        assert [o["down_segment"] for o in lay] == [ff, ff, ff, 7 * 768]
