@@ -245,10 +245,11 @@ int adp_prefill_tc(adp_model* m, adp_kv* kv, const int32_t* host_tokens, int32_t
  *  sampling:   HOST array [nb] (temperature and uniform per request), or NULL for greedy.
  *  next_tokens: HOST array [nb] that receives the chosen tokens.
  *  dev_logits: optional DEVICE float array [nb][vocab].
- * nb must be in [1, adp_max_batch]: the batched kernel keeps nb copies of the widest GEMV input
- * vector (fp32) in shared memory beside a weight ring of at least two slots, and merges head h of
- * request r on CTA G-1-(r*n_heads+h).  Dense models with 16-bit or e4m3 layer matrices only
- * (experts differ per request: MoE models, like NVFP4 ones, get ADP_ERR_UNSUPPORTED_CONFIG).
+ * nb must be in [1, adp_max_batch]: the batched kernel keeps every request's GEMV input vector
+ * (fp32) in shared memory beside a weight ring of at least two slots (the down projection's
+ * input in segments of whole K-chunks when nb whole vectors do not fit; see adp_batch_plan), and
+ * merges head h of request r on CTA G-1-(r*n_heads+h).  Dense models with 16-bit, e4m3 or NVFP4
+ * layer matrices (experts differ per request: MoE models get ADP_ERR_UNSUPPORTED_CONFIG).
  * Synchronises; errors as adp_decode_step (a device error is sticky and no cache grows). */
 int adp_decode_batch(adp_model* m, adp_kv* const* kvs, int32_t nb, const int32_t* tokens,
                      const adp_sampling* sampling, int32_t* next_tokens, float* dev_logits);
